@@ -1,0 +1,198 @@
+/*
+ * still.h -- C ABI of libstill.so: one STILL intra-layer hybrid attention layer
+ * (chunk-parallel prefill forward and bounded-memory decode step) on a GB300
+ * (sm_103a).
+ *
+ * The method: "STILL: Content-Aware Intra-Layer Hybrid Attention for Efficient
+ * LLM Linearization" (besthub.dev summary), with its companion write-ups
+ * "STILL: Selecting Tokens for Intra-Layer Hybrid Attention to Linearize LLMs"
+ * (roboind.com news page) and "NeurIPS 2026 | 层内混合注意力 ... STILL"
+ * (shishifenxi.com).  Section names below are the headings of those pages.
+ *
+ * Conventions shared by every call
+ *   - Tensors are dense, row-major, on the device unless stated otherwise.
+ *     q, out: [B, Hq, N, d]; k, v: [B, Hkv, N, d]; query head h reads kv head
+ *     h / G with G = Hq / Hkv (grouped-query attention).
+ *   - still_bf16 is the raw 16-bit pattern of an IEEE bfloat16 value.
+ *   - Wf: fp32 [d, d_f], one learned NP-Map matrix per layer, shared by q, k
+ *     and all heads.
+ *   - Routing parameters: W window slots, chunk length C, softmax budget m,
+ *     T_max chunks that keep tokens; lambda = floor((m - W) / T_max) tokens kept
+ *     per completed chunk (section "Content-Aware Routing with Fixed Budget").
+ *   - Every call is asynchronous on `stream` (NULL = legacy default stream).
+ *     Argument errors are detected on the host and returned before anything
+ *     is launched; launch failures return STILL_ERR_CUDA.  Errors found by a
+ *     kernel (an index out of range) are written to a device status word
+ *     (see still_read_status) and never trap.
+ *   - Device pointers must be 16-byte aligned.  The caller owns all memory;
+ *     the library keeps no device allocation between calls.
+ *   - Supported: d in {64, 128}, d_f in {64, 128}, 1 <= C <= 16384, W >= 0,
+ *     m >= W, T_max >= 1, W >= 1 whenever lambda > 0.  N == 0 is a no-op.
+ */
+#ifndef STILL_H
+#define STILL_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t still_bf16;
+typedef struct CUstream_st *still_stream_t; /* the same handle as cudaStream_t */
+
+typedef struct {
+    int B, Hq, Hkv, N, d, d_f;
+} still_shape;
+
+typedef enum {
+    STILL_OK = 0,
+    STILL_ERR_INVALID_ARG = 1, /* null/misaligned pointer, inconsistent sizes   */
+    STILL_ERR_UNSUPPORTED = 2, /* valid request outside the compiled shapes     */
+    STILL_ERR_CUDA = 3,        /* a CUDA runtime call or launch failed          */
+    STILL_ERR_TIMEOUT = 4,     /* a bounded device-side wait gave up            */
+    STILL_ERR_BOUNDS = 5,      /* a kernel met an index outside its buffers     */
+    STILL_ERR_WORKSPACE = 6    /* workspace smaller than still_prefill_workspace_size */
+} still_status;
+
+/*
+ * Decode state of B sequences (all device memory, owned by the caller).  It is
+ * the softmax KV cache of m slots per (sequence, kv head) plus the linear
+ * recurrent state (section "Content-Aware Routing with Fixed Budget": W slots
+ * for the sliding window, m - W for kept tokens, unkept tokens accumulated into
+ * the linear-attention state, nothing re-scored or evicted).
+ *   K, V        bf16  [B, Hkv, m, d]  slots 0..W-1: window ring, token j in
+ *                                     slot j % W; slot W + c*lambda + r: the
+ *                                     r-th kept token of chunk c.  While chunk
+ *                                     c is unfinished its slots hold tokens of
+ *                                     c that left the window and may still be
+ *                                     among its top-lambda ("candidates").
+ *   slot_pos    int32 [B, Hkv, m]     token position in the slot, -1 = empty
+ *   slot_cnt    int32 [B, Hkv, m]     candidates: tokens of the chunk so far
+ *                                     that outrank the candidate
+ *   slot_score  fp32  [B, Hkv, m]     Self-Saliency score of the slot's token
+ *   S           fp32  [B, Hkv, d_f, d] sum of phi(k) v^T over folded tokens
+ *   z           fp32  [B, Hkv, d_f]   sum of phi(k) over folded tokens
+ *   score_ring  fp32  [B, Hkv, C]     scores of the unfinished chunk (j % C)
+ *   t           int64 [B, Hkv]        tokens absorbed so far
+ *   status      int32 [1]             device status word (0 = fine)
+ */
+typedef struct {
+    still_bf16 *K;
+    still_bf16 *V;
+    int32_t *slot_pos;
+    int32_t *slot_cnt;
+    float *slot_score;
+    float *S;
+    float *z;
+    float *score_ring;
+    int64_t *t;
+    int32_t *status;
+} still_decode_state;
+
+/* Human-readable name of a status code (static string). */
+const char *still_status_string(still_status s);
+
+/* lambda = floor((m - W) / T_max), or -1 when the budget is invalid. */
+int still_lambda(int W, int m, int T_max);
+
+/*
+ * Self-Saliency scores (section "Self-Saliency Score: Predicting Future
+ * Utility from Local Context"; roboind "Highlight 2: Self-Absolute Score").
+ * For each query head h and token t the window is keys [max(0, t-W+1), t];
+ * a^diag is the softmax of q_t.k_j / sqrt(d) over the window, a^nodiag the
+ * same without j = t, and Score = KL(a^nodiag || a^diag) in the closed form
+ * -log(1 - p_t + 1e-6), p_t = a^diag_t.  The kv-head score is the mean over
+ * the G query heads of the group.
+ *   q [B,Hq,N,d] bf16, k [B,Hkv,N,d] bf16 -> scores fp32 [B,Hkv,N].
+ * Requires W >= 1.
+ */
+still_status still_score(const still_shape *shape, const still_bf16 *q, const still_bf16 *k, int W,
+                         float *scores, still_stream_t stream);
+
+/*
+ * Delayed chunk-level selection (section "Delayed Chunk-Level Selection for
+ * Unified Training-Inference Parallelism"): each completed chunk c < T_max
+ * (tokens [cC, cC + C), all < N) keeps its top-lambda tokens by score, an
+ * exact tie going to the lower position; positions are written in ascending
+ * order.  Rows of chunks that keep nothing (incomplete, or past the data) and
+ * unused columns when lambda > C are -1.
+ *   scores fp32 [B,Hkv,N] -> sel_idx int32 [B,Hkv,T_max,lambda].
+ */
+still_status still_select(const still_shape *shape, const float *scores, int W, int C, int m, int T_max,
+                          int32_t *sel_idx, still_stream_t stream);
+
+/*
+ * NP-Map feature map (section "NP-Map: Norm-Preserving Feature Map"): the
+ * learned map only chooses a direction and the input norm is put back,
+ * phi(x) = ||x|| u / ||u||, u = softmax(x Wf) over the d_f features.
+ *   x bf16 [rows, d], Wf fp32 [d, d_f] -> phi fp32 [rows, d_f].
+ */
+still_status still_npmap(const still_bf16 *x, long long rows, int d, const float *Wf, int d_f, float *phi,
+                         still_stream_t stream);
+
+/* Bytes of device workspace still_prefill needs for these sizes. */
+size_t still_prefill_workspace_size(const still_shape *shape, int W, int C, int m, int T_max);
+
+/*
+ * Chunk-parallel prefill forward of one layer (sections "Content-Aware
+ * Routing with Fixed Budget", "Delayed Chunk-Level Selection ...", "NP-Map"
+ * and the shared normalisation of the two branches):
+ *   SA(t) = {t-W < j <= t} U {j kept by chunk(j) < chunk(t), j <= t-W}
+ *   LA(t) = {j <= t-W} minus SA(t)
+ *   y_t = (sum_SA e^{s-c} v + phi(q)^T S_LA) / (sum_SA e^{s-c} + phi(q)^T z_LA)
+ * with s = q.k / sqrt(d) and c = max over SA(t).
+ *   out bf16 [B,Hq,N,d]; sel_idx int32 [B,Hkv,T_max,lambda] (nullable).
+ *   workspace: device memory of still_prefill_workspace_size() bytes, or NULL
+ *   to let the call take and release it stream-ordered (cudaMallocAsync).
+ *   export_state (nullable): filled with the decode state after N tokens,
+ *   identical to what N decode steps from an empty state would hold.
+ */
+still_status still_prefill(const still_shape *shape, const still_bf16 *q, const still_bf16 *k,
+                           const still_bf16 *v, const float *Wf, int W, int C, int m, int T_max,
+                           still_bf16 *out, int32_t *sel_idx, void *workspace, size_t workspace_bytes,
+                           const still_decode_state *export_state, still_stream_t stream);
+
+/* Reset a decode state to "no token absorbed" (shape->N is ignored). */
+still_status still_decode_state_init(const still_shape *shape, const still_decode_state *state, int W, int C,
+                                     int m, int T_max, still_stream_t stream);
+
+/*
+ * One decode step for every sequence (the same routing and memory update as
+ * the prefill, one token at a time): score the new token in its window; push
+ * current-chunk candidates that fell out of the running top-lambda into (S,z);
+ * move token t-W out of the window (into a slot or into (S,z)); attend over the
+ * window and the kept slots with softmax plus phi(q)^T S; when the chunk
+ * completes, keep its top-lambda.  shape->N is ignored.
+ *   q_t bf16 [B,Hq,d], k_t, v_t bf16 [B,Hkv,d] -> out_t bf16 [B,Hq,d].
+ */
+still_status still_decode_step(const still_shape *shape, const still_decode_state *state,
+                               const still_bf16 *q_t, const still_bf16 *k_t, const still_bf16 *v_t,
+                               const float *Wf, int W, int C, int m, int T_max, still_bf16 *out_t,
+                               still_stream_t stream);
+
+/* Synchronise `stream` and read a device status word (the one in a decode
+ * state, or the first int32 of a prefill workspace). */
+still_status still_read_status(const int32_t *status_word, still_stream_t stream, int32_t *host_value);
+
+/*
+ * Kernel timing for measurement: while enabled, every kernel the library
+ * launches is bracketed by CUDA events on its stream.  still_timing_read
+ * synchronises, returns per-kernel totals (name, launches, milliseconds) for
+ * up to `max` kernels, clears the record and returns the number of kernels.
+ */
+typedef struct {
+    char name[48];
+    int launches;
+    double ms;
+} still_kernel_time;
+
+void still_timing_enable(int on);
+int still_timing_read(still_kernel_time *out, int max);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* STILL_H */

@@ -1,0 +1,351 @@
+// C ABI of libstill: argument checks, workspace plan, launch order, timing.
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "common.cuh"
+
+namespace still {
+
+// ---------------------------------------------------------------------------
+// kernel timing (host-side record of CUDA event pairs)
+// ---------------------------------------------------------------------------
+namespace {
+struct TimedLaunch {
+    std::string name;
+    cudaEvent_t a, b;
+};
+std::mutex g_tm_mu;
+bool g_tm_on = false;
+std::vector<TimedLaunch> g_tm_open;   // one per stream nesting level
+std::vector<TimedLaunch> g_tm_done;
+std::vector<cudaEvent_t> g_tm_pool;
+
+cudaEvent_t pool_event()
+{
+    if (!g_tm_pool.empty()) {
+        cudaEvent_t e = g_tm_pool.back();
+        g_tm_pool.pop_back();
+        return e;
+    }
+    cudaEvent_t e = nullptr;
+    cudaEventCreate(&e);
+    return e;
+}
+}  // namespace
+
+void timing_begin(const char *name, cudaStream_t s)
+{
+    std::lock_guard<std::mutex> lk(g_tm_mu);
+    if (!g_tm_on) return;
+    TimedLaunch t{name, pool_event(), pool_event()};
+    cudaEventRecord(t.a, s);
+    g_tm_open.push_back(t);
+}
+
+void timing_end(cudaStream_t s)
+{
+    std::lock_guard<std::mutex> lk(g_tm_mu);
+    if (!g_tm_on || g_tm_open.empty()) return;
+    TimedLaunch t = g_tm_open.back();
+    g_tm_open.pop_back();
+    cudaEventRecord(t.b, s);
+    g_tm_done.push_back(t);
+}
+
+size_t decode_smem_bytes(const Dims &dm);
+
+}  // namespace still
+
+using namespace still;
+
+namespace {
+
+bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+
+still_status check_shape(const still_shape *sh, bool need_n)
+{
+    if (!sh) return STILL_ERR_INVALID_ARG;
+    if (sh->B < 1 || sh->Hq < 1 || sh->Hkv < 1 || (need_n && sh->N < 0)) return STILL_ERR_INVALID_ARG;
+    if (sh->Hq % sh->Hkv) return STILL_ERR_INVALID_ARG;
+    if (!((sh->d == 64 || sh->d == 128) && (sh->d_f == 64 || sh->d_f == 128))) return STILL_ERR_UNSUPPORTED;
+    return STILL_OK;
+}
+
+still_status make_dims(const still_shape *sh, int W, int C, int m, int T_max, Dims *dm)
+{
+    still_status st = check_shape(sh, true);
+    if (st != STILL_OK) return st;
+    if (W < 0 || C < 1 || T_max < 1 || m < W) return STILL_ERR_INVALID_ARG;
+    const int lam = (m - W) / T_max;
+    if (W < 1 && lam > 0) return STILL_ERR_INVALID_ARG;
+    if (C > 16384) return STILL_ERR_UNSUPPORTED;
+    dm->B = sh->B; dm->Hq = sh->Hq; dm->Hkv = sh->Hkv; dm->N = sh->N; dm->d = sh->d; dm->df = sh->d_f;
+    dm->G = sh->Hq / sh->Hkv;
+    dm->W = W; dm->C = C; dm->m = m; dm->T_max = T_max; dm->lam = lam;
+    dm->n_full = sh->N / C;
+    const int nch = (sh->N + C - 1) / C;
+    dm->n_sel = nch < T_max ? nch : T_max;
+    dm->tail = (sh->N % C != 0 && sh->N / C < T_max && lam > 0) ? sh->N / C : -1;
+    return STILL_OK;
+}
+
+SegPlan plan_segments(const Dims &dm)
+{
+    SegPlan sp;
+    sp.T = 16;
+    const int ntile = (dm.N + sp.T - 1) / sp.T;
+    const int units = dm.B * dm.Hkv;
+    int target = (2 * 152 + units - 1) / units;
+    if (target < 1) target = 1;
+    if (target > ntile) target = ntile;
+    if (ntile == 0) {
+        sp.L = sp.T;
+        sp.nseg = 1;
+        return sp;
+    }
+    const int tiles_per = (ntile + target - 1) / target;
+    sp.L = tiles_per * sp.T;
+    sp.nseg = (dm.N + sp.L - 1) / sp.L;
+    return sp;
+}
+
+struct WsLayout {
+    size_t status, scores, fsel, flag, phik, dS, dz, total;
+};
+
+size_t al(size_t x) { return (x + 255) & ~size_t(255); }
+
+WsLayout ws_layout(const Dims &dm, const SegPlan &sp)
+{
+    WsLayout L;
+    size_t o = 0;
+    const size_t units = (size_t)dm.B * dm.Hkv;
+    L.status = o; o += al(256);
+    L.scores = o; o += al(units * dm.N * 4);
+    L.fsel = o; o += al(units * dm.T_max * (size_t)(dm.lam > 0 ? dm.lam : 1) * 4);
+    L.flag = o; o += al(units * dm.N);
+    L.phik = o; o += al(units * dm.N * (size_t)dm.df * 4);
+    L.dS = o; o += al(units * (size_t)(sp.nseg + 1) * dm.df * dm.d * 4);
+    L.dz = o; o += al(units * (size_t)(sp.nseg + 1) * dm.df * 4);
+    L.total = o;
+    return L;
+}
+
+still_status cuda_status(cudaError_t e)
+{
+    if (e == cudaSuccess) return STILL_OK;
+    fprintf(stderr, "libstill: CUDA error %s\n", cudaGetErrorString(e));
+    return STILL_ERR_CUDA;
+}
+
+bool state_ok(const still_decode_state *s)
+{
+    return s && s->K && s->V && s->slot_pos && s->slot_cnt && s->slot_score && s->S && s->z && s->score_ring &&
+           s->t && s->status && aligned16(s->K) && aligned16(s->V) && aligned16(s->S);
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *still_status_string(still_status s)
+{
+    switch (s) {
+    case STILL_OK: return "ok";
+    case STILL_ERR_INVALID_ARG: return "invalid argument";
+    case STILL_ERR_UNSUPPORTED: return "unsupported shape";
+    case STILL_ERR_CUDA: return "CUDA error";
+    case STILL_ERR_TIMEOUT: return "device wait timed out";
+    case STILL_ERR_BOUNDS: return "index out of bounds";
+    case STILL_ERR_WORKSPACE: return "workspace too small";
+    }
+    return "unknown status";
+}
+
+int still_lambda(int W, int m, int T_max)
+{
+    if (T_max < 1 || W < 0 || m < W) return -1;
+    return (m - W) / T_max;
+}
+
+still_status still_score(const still_shape *shape, const still_bf16 *q, const still_bf16 *k, int W, float *scores,
+                         still_stream_t stream)
+{
+    still_status st = check_shape(shape, true);
+    if (st != STILL_OK) return st;
+    if (W < 1) return STILL_ERR_INVALID_ARG;
+    if (!q || !k || !scores || !aligned16(q) || !aligned16(k) || !aligned16(scores)) return STILL_ERR_INVALID_ARG;
+    if (shape->N == 0) return STILL_OK;
+    Dims dm;
+    st = make_dims(shape, W, 1, W, 1, &dm);
+    if (st != STILL_OK) return st;
+    return cuda_status(launch_score(dm, q, k, scores, (cudaStream_t)stream));
+}
+
+still_status still_select(const still_shape *shape, const float *scores, int W, int C, int m, int T_max,
+                          int32_t *sel_idx, still_stream_t stream)
+{
+    Dims dm;
+    still_status st = make_dims(shape, W, C, m, T_max, &dm);
+    if (st != STILL_OK) return st;
+    if (!scores || !sel_idx || !aligned16(scores) || !aligned16(sel_idx)) return STILL_ERR_INVALID_ARG;
+    if (dm.lam == 0) return STILL_OK;
+    if (dm.N == 0)
+        return cuda_status(cudaMemsetAsync(sel_idx, 0xff, (size_t)dm.B * dm.Hkv * dm.T_max * dm.lam * 4,
+                                           (cudaStream_t)stream));
+    return cuda_status(launch_select(dm, scores, sel_idx, nullptr, nullptr, (cudaStream_t)stream));
+}
+
+still_status still_npmap(const still_bf16 *x, long long rows, int d, const float *Wf, int d_f, float *phi,
+                         still_stream_t stream)
+{
+    if (rows < 0 || !x || !Wf || !phi || !aligned16(x) || !aligned16(Wf) || !aligned16(phi))
+        return STILL_ERR_INVALID_ARG;
+    if (!((d == 64 || d == 128) && (d_f == 64 || d_f == 128))) return STILL_ERR_UNSUPPORTED;
+    if (rows == 0) return STILL_OK;
+    return cuda_status(launch_npmap(x, rows, d, Wf, d_f, phi, (cudaStream_t)stream));
+}
+
+size_t still_prefill_workspace_size(const still_shape *shape, int W, int C, int m, int T_max)
+{
+    Dims dm;
+    if (make_dims(shape, W, C, m, T_max, &dm) != STILL_OK) return 0;
+    return ws_layout(dm, plan_segments(dm)).total;
+}
+
+still_status still_prefill(const still_shape *shape, const still_bf16 *q, const still_bf16 *k, const still_bf16 *v,
+                           const float *Wf, int W, int C, int m, int T_max, still_bf16 *out, int32_t *sel_idx,
+                           void *workspace, size_t workspace_bytes, const still_decode_state *export_state,
+                           still_stream_t stream)
+{
+    Dims dm;
+    still_status st = make_dims(shape, W, C, m, T_max, &dm);
+    if (st != STILL_OK) return st;
+    if (!q || !k || !v || !Wf || !out) return STILL_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(Wf) || !aligned16(out) ||
+        (sel_idx && !aligned16(sel_idx)) || (workspace && !aligned16(workspace)))
+        return STILL_ERR_INVALID_ARG;
+    if (export_state && !state_ok(export_state)) return STILL_ERR_INVALID_ARG;
+    cudaStream_t s = (cudaStream_t)stream;
+    const SegPlan sp = plan_segments(dm);
+    const WsLayout L = ws_layout(dm, sp);
+    if (workspace && workspace_bytes < L.total) return STILL_ERR_WORKSPACE;
+    if (dm.N == 0) {
+        if (sel_idx && dm.lam > 0)
+            return cuda_status(cudaMemsetAsync(sel_idx, 0xff, (size_t)dm.B * dm.Hkv * dm.T_max * dm.lam * 4, s));
+        return STILL_OK;
+    }
+    void *ws = workspace;
+    if (!ws) {
+        cudaError_t e = cudaMallocAsync(&ws, L.total, s);
+        if (e != cudaSuccess) return cuda_status(e);
+    }
+    char *base = (char *)ws;
+    int32_t *status = (int32_t *)(base + L.status);
+    float *scores = (float *)(base + L.scores);
+    int32_t *fsel = (int32_t *)(base + L.fsel);
+    uint8_t *flag = (uint8_t *)(base + L.flag);
+    float *phik = (float *)(base + L.phik);
+    float *dS = (float *)(base + L.dS);
+    float *dz = (float *)(base + L.dz);
+    cudaError_t e = cudaMemsetAsync(base, 0, L.status + 256, s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(flag, 0, (size_t)dm.B * dm.Hkv * dm.N, s);
+    if (e == cudaSuccess && dm.lam > 0 && dm.W >= 1) e = launch_score(dm, q, k, scores, s);
+    if (e == cudaSuccess && dm.lam > 0) e = launch_select(dm, scores, sel_idx, fsel, flag, s);
+    if (e == cudaSuccess) e = launch_linstate(dm, sp, k, v, Wf, flag, phik, dS, dz, s);
+    if (e == cudaSuccess) e = launch_hybrid(dm, sp, q, k, v, Wf, phik, fsel, flag, dS, dz, out, status, s);
+    if (e == cudaSuccess && export_state) e = launch_export(dm, sp, k, v, scores, fsel, dS, dz, *export_state, s);
+    if (!workspace) {
+        cudaError_t e2 = cudaFreeAsync(ws, s);
+        if (e == cudaSuccess) e = e2;
+    }
+    return cuda_status(e);
+}
+
+still_status still_decode_state_init(const still_shape *shape, const still_decode_state *state, int W, int C, int m,
+                                     int T_max, still_stream_t stream)
+{
+    still_shape sh = *shape;
+    sh.N = 0;
+    Dims dm;
+    still_status st = make_dims(&sh, W, C, m, T_max, &dm);
+    if (st != STILL_OK) return st;
+    if (!state_ok(state)) return STILL_ERR_INVALID_ARG;
+    cudaStream_t s = (cudaStream_t)stream;
+    const size_t units = (size_t)dm.B * dm.Hkv;
+    cudaError_t e = cudaMemsetAsync(state->K, 0, units * m * dm.d * 2, s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(state->V, 0, units * m * dm.d * 2, s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(state->slot_pos, 0xff, units * m * 4, s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(state->slot_cnt, 0, units * m * 4, s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(state->slot_score, 0, units * m * 4, s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(state->S, 0, units * dm.df * dm.d * 4, s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(state->z, 0, units * dm.df * 4, s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(state->score_ring, 0, units * C * 4, s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(state->t, 0, units * 8, s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(state->status, 0, 4, s);
+    return cuda_status(e);
+}
+
+still_status still_decode_step(const still_shape *shape, const still_decode_state *state, const still_bf16 *q_t,
+                               const still_bf16 *k_t, const still_bf16 *v_t, const float *Wf, int W, int C, int m,
+                               int T_max, still_bf16 *out_t, still_stream_t stream)
+{
+    still_shape sh = *shape;
+    sh.N = 0;
+    Dims dm;
+    still_status st = make_dims(&sh, W, C, m, T_max, &dm);
+    if (st != STILL_OK) return st;
+    if (!state_ok(state) || !q_t || !k_t || !v_t || !Wf || !out_t) return STILL_ERR_INVALID_ARG;
+    if (!aligned16(q_t) || !aligned16(k_t) || !aligned16(v_t) || !aligned16(Wf) || !aligned16(out_t))
+        return STILL_ERR_INVALID_ARG;
+    if (dm.G > 8) return STILL_ERR_UNSUPPORTED;
+    if (decode_smem_bytes(dm) > 200 * 1024) return STILL_ERR_UNSUPPORTED;
+    return cuda_status(launch_decode(dm, *state, q_t, k_t, v_t, Wf, out_t, (cudaStream_t)stream));
+}
+
+still_status still_read_status(const int32_t *status_word, still_stream_t stream, int32_t *host_value)
+{
+    if (!status_word || !host_value) return STILL_ERR_INVALID_ARG;
+    cudaError_t e = cudaMemcpyAsync(host_value, status_word, 4, cudaMemcpyDeviceToHost, (cudaStream_t)stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize((cudaStream_t)stream);
+    return cuda_status(e);
+}
+
+void still_timing_enable(int on)
+{
+    std::lock_guard<std::mutex> lk(g_tm_mu);
+    g_tm_on = on != 0;
+}
+
+int still_timing_read(still_kernel_time *out, int max)
+{
+    std::lock_guard<std::mutex> lk(g_tm_mu);
+    std::vector<still_kernel_time> agg;
+    for (auto &t : g_tm_done) {
+        cudaEventSynchronize(t.b);
+        float ms = 0.f;
+        cudaEventElapsedTime(&ms, t.a, t.b);
+        still_kernel_time *hit = nullptr;
+        for (auto &a : agg)
+            if (t.name == a.name) hit = &a;
+        if (!hit) {
+            still_kernel_time k{};
+            strncpy(k.name, t.name.c_str(), sizeof(k.name) - 1);
+            agg.push_back(k);
+            hit = &agg.back();
+        }
+        hit->launches += 1;
+        hit->ms += ms;
+        g_tm_pool.push_back(t.a);
+        g_tm_pool.push_back(t.b);
+    }
+    g_tm_done.clear();
+    int n = (int)agg.size();
+    for (int i = 0; i < n && i < max; ++i) out[i] = agg[i];
+    return n;
+}
+
+}  // extern "C"

@@ -1,0 +1,158 @@
+// Shared device helpers and the internal launch interface of libstill.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "still.h"
+
+namespace still {
+
+// Sizes and routing parameters of one call, resolved on the host.
+struct Dims {
+    int B, Hq, Hkv, N, d, df, G;
+    int W, C, m, T_max, lam;
+    int n_full;   // completed chunks: N / C
+    int n_sel;    // chunks that run a selection: min(T_max, ceil(N / C))
+    int tail;     // the unfinished last chunk when it is < T_max, else -1
+};
+
+// Segment plan of the chunk-parallel prefill: CTA s of a (sequence, kv head)
+// walks query tiles [s*L, (s+1)*L) in order, starting from the linear state of
+// the keys that left the window before its first tile.
+struct SegPlan {
+    int T;      // query tokens per tile
+    int L;      // tokens per segment (multiple of T)
+    int nseg;   // segments per (sequence, kv head)
+};
+
+// ---- bf16 ------------------------------------------------------------------
+__device__ __forceinline__ float bf2f(uint16_t x) { return __uint_as_float(((uint32_t)x) << 16); }
+
+__device__ __forceinline__ uint16_t f2bf(float f) { return __bfloat16_as_ushort(__float2bfloat16_rn(f)); }
+
+// ---- warp reductions ---------------------------------------------------------
+__device__ __forceinline__ float warp_sum(float x)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    return x;
+}
+
+__device__ __forceinline__ float warp_max(float x)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+    return x;
+}
+
+// Ranking of the top-lambda selection: higher score first, exact ties to the
+// lower position.
+__device__ __forceinline__ bool outranks(long long i, float si, long long j, float sj)
+{
+    return si > sj || (si == sj && i < j);
+}
+
+__device__ __forceinline__ void set_status(int32_t *status, int code)
+{
+    if (status) atomicCAS(status, 0, code);
+}
+
+// Self-Saliency score from the window's softmax statistics: oth = sum of
+// e^{s-M} over the window without the token itself, self = e^{s_tt - M}.
+// -log(1 - p + eps) is taken through log1p while p is small, so that small
+// scores keep full relative precision, and through the off-diagonal mass
+// otherwise, so that 1 - p never comes from a cancelling difference.
+__device__ __forceinline__ float saliency_from_stats(float oth, float self)
+{
+    const float tot = oth + self;
+    const float p = self / tot;
+    if (p < 0.5f) return -log1pf(1e-6f - p);
+    return -logf(oth / tot + 1e-6f);
+}
+
+// ---- NP-Map of one row, by one warp -------------------------------------------
+// x: the row in shared memory (fp32, D values); Wf: global fp32 [D, DF].
+// Writes phi (DF values) to `phi` (shared or global).
+template <int D, int DF>
+__device__ __forceinline__ void warp_npmap(const float *x, const float *__restrict__ Wf, float *phi, int lane)
+{
+    constexpr int PJ = DF / 32;
+    float l[PJ];
+#pragma unroll
+    for (int r = 0; r < PJ; ++r) l[r] = 0.f;
+    for (int i = 0; i < D; ++i) {
+        float xi = x[i];
+#pragma unroll
+        for (int r = 0; r < PJ; ++r) l[r] = fmaf(xi, __ldg(Wf + i * DF + lane + 32 * r), l[r]);
+    }
+    float nx = 0.f;
+    for (int e = lane; e < D; e += 32) nx = fmaf(x[e], x[e], nx);
+    nx = sqrtf(warp_sum(nx));
+    float mx = l[0];
+#pragma unroll
+    for (int r = 1; r < PJ; ++r) mx = fmaxf(mx, l[r]);
+    mx = warp_max(mx);
+    float su = 0.f;
+#pragma unroll
+    for (int r = 0; r < PJ; ++r) { l[r] = expf(l[r] - mx); su += l[r]; }
+    su = warp_sum(su);
+    float nu = 0.f;
+#pragma unroll
+    for (int r = 0; r < PJ; ++r) { l[r] /= su; nu = fmaf(l[r], l[r], nu); }
+    nu = sqrtf(warp_sum(nu));
+    float sc = nx / nu;
+#pragma unroll
+    for (int r = 0; r < PJ; ++r) phi[lane + 32 * r] = sc * l[r];
+}
+
+// Dot product of a bf16 global row with an fp32 shared row, by one thread.
+template <int D>
+__device__ __forceinline__ float dot_bf16_row(const uint16_t *__restrict__ row, const float *x)
+{
+    float s = 0.f;
+#pragma unroll 4
+    for (int e = 0; e < D; e += 8) {
+        uint4 pk = __ldg(reinterpret_cast<const uint4 *>(row + e));
+        uint32_t w[4] = {pk.x, pk.y, pk.z, pk.w};
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+            s = fmaf(__uint_as_float(w[h] << 16), x[e + 2 * h], s);
+            s = fmaf(__uint_as_float(w[h] & 0xffff0000u), x[e + 2 * h + 1], s);
+        }
+    }
+    return s;
+}
+
+// ---- timing hooks (implemented in api.cu) -----------------------------------
+void timing_begin(const char *name, cudaStream_t s);
+void timing_end(cudaStream_t s);
+
+struct KTimer {
+    cudaStream_t s;
+    KTimer(const char *name, cudaStream_t st) : s(st) { timing_begin(name, st); }
+    ~KTimer() { timing_end(s); }
+};
+
+// ---- launchers (one per kernel family) ----------------------------------------
+cudaError_t launch_score(const Dims &dm, const uint16_t *q, const uint16_t *k, float *scores, cudaStream_t s);
+cudaError_t launch_select(const Dims &dm, const float *scores, int32_t *sel_idx, int32_t *fsel, uint8_t *flag,
+                          cudaStream_t s);
+cudaError_t launch_npmap(const uint16_t *x, long long rows, int d, const float *Wf, int df, float *phi,
+                         cudaStream_t s);
+cudaError_t launch_linstate(const Dims &dm, const SegPlan &sp, const uint16_t *k, const uint16_t *v,
+                            const float *Wf, const uint8_t *flag, float *phik, float *dS, float *dz,
+                            cudaStream_t s);
+cudaError_t launch_hybrid(const Dims &dm, const SegPlan &sp, const uint16_t *q, const uint16_t *k,
+                          const uint16_t *v, const float *Wf, const float *phik, const int32_t *fsel,
+                          const uint8_t *flag, const float *dS, const float *dz, uint16_t *out,
+                          int32_t *status, cudaStream_t s);
+cudaError_t launch_export(const Dims &dm, const SegPlan &sp, const uint16_t *k, const uint16_t *v,
+                          const float *scores, const int32_t *fsel, const float *dS, const float *dz,
+                          const still_decode_state &st, cudaStream_t s);
+cudaError_t launch_decode(const Dims &dm, const still_decode_state &st, const uint16_t *q_t,
+                          const uint16_t *k_t, const uint16_t *v_t, const float *Wf, uint16_t *out_t,
+                          cudaStream_t s);
+
+}  // namespace still

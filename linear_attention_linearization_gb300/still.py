@@ -1,0 +1,240 @@
+"""Python binding of libstill.so (the C ABI declared in include/still.h).
+
+Argument marshalling only: tensors are checked for dtype, shape, device and
+contiguity, and their device pointers are handed to the library; every step of
+the layer runs in the library's CUDA kernels.  There is no fallback: if the
+library is missing or a call fails, an exception is raised.
+"""
+from __future__ import annotations
+
+import ctypes as ct
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libstill.so")
+
+STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported shape", 3: "CUDA error",
+          4: "device wait timed out", 5: "index out of bounds", 6: "workspace too small"}
+
+
+class StillError(RuntimeError):
+    def __init__(self, code, what):
+        super().__init__(f"{what}: {STATUS.get(code, code)} ({code})")
+        self.code = code
+
+
+class Shape(ct.Structure):
+    _fields_ = [("B", ct.c_int), ("Hq", ct.c_int), ("Hkv", ct.c_int), ("N", ct.c_int),
+                ("d", ct.c_int), ("d_f", ct.c_int)]
+
+
+class DecodeStateC(ct.Structure):
+    _fields_ = [(n, ct.c_void_p) for n in
+                ("K", "V", "slot_pos", "slot_cnt", "slot_score", "S", "z", "score_ring", "t", "status")]
+
+
+class KernelTime(ct.Structure):
+    _fields_ = [("name", ct.c_char * 48), ("launches", ct.c_int), ("ms", ct.c_double)]
+
+
+_lib = None
+
+# The exported functions and their C signatures (include/still.h).
+SIGNATURES = {
+    "still_status_string": (ct.c_char_p, [ct.c_int]),
+    "still_lambda": (ct.c_int, [ct.c_int, ct.c_int, ct.c_int]),
+    "still_score": (ct.c_int, [ct.POINTER(Shape), ct.c_void_p, ct.c_void_p, ct.c_int, ct.c_void_p,
+                               ct.c_void_p]),
+    "still_select": (ct.c_int, [ct.POINTER(Shape), ct.c_void_p, ct.c_int, ct.c_int, ct.c_int, ct.c_int,
+                                ct.c_void_p, ct.c_void_p]),
+    "still_npmap": (ct.c_int, [ct.c_void_p, ct.c_longlong, ct.c_int, ct.c_void_p, ct.c_int, ct.c_void_p,
+                               ct.c_void_p]),
+    "still_prefill_workspace_size": (ct.c_size_t, [ct.POINTER(Shape), ct.c_int, ct.c_int, ct.c_int,
+                                                   ct.c_int]),
+    "still_prefill": (ct.c_int, [ct.POINTER(Shape), ct.c_void_p, ct.c_void_p, ct.c_void_p, ct.c_void_p,
+                                 ct.c_int, ct.c_int, ct.c_int, ct.c_int, ct.c_void_p, ct.c_void_p,
+                                 ct.c_void_p, ct.c_size_t, ct.POINTER(DecodeStateC), ct.c_void_p]),
+    "still_decode_state_init": (ct.c_int, [ct.POINTER(Shape), ct.POINTER(DecodeStateC), ct.c_int, ct.c_int,
+                                           ct.c_int, ct.c_int, ct.c_void_p]),
+    "still_decode_step": (ct.c_int, [ct.POINTER(Shape), ct.POINTER(DecodeStateC), ct.c_void_p, ct.c_void_p,
+                                     ct.c_void_p, ct.c_void_p, ct.c_int, ct.c_int, ct.c_int, ct.c_int,
+                                     ct.c_void_p, ct.c_void_p]),
+    "still_read_status": (ct.c_int, [ct.c_void_p, ct.c_void_p, ct.POINTER(ct.c_int32)]),
+    "still_timing_enable": (None, [ct.c_int]),
+    "still_timing_read": (ct.c_int, [ct.POINTER(KernelTime), ct.c_int]),
+}
+
+
+def lib():
+    """Load libstill.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(f"libstill.so not built ({LIB_PATH}); run "
+                              "python -m linear_attention_linearization_gb300.build")
+        L = ct.CDLL(LIB_PATH)
+        for name, (res, args) in SIGNATURES.items():
+            f = getattr(L, name)
+            f.restype = res
+            f.argtypes = args
+        _lib = L
+    return _lib
+
+
+def _check(code, what):
+    if code != 0:
+        raise StillError(code, what)
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ct.c_void_p(stream.cuda_stream)
+
+
+def _ptr(t, dtype, what):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError(f"{what} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{what} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{what} must be contiguous")
+    return ct.c_void_p(t.data_ptr())
+
+
+def lam_of(W, m, T_max):
+    return lib().still_lambda(W, m, T_max)
+
+
+def shape_of(q, k, Wf):
+    B, Hq, N, d = q.shape
+    return Shape(B, Hq, k.shape[1], N, d, Wf.shape[1])
+
+
+def score(q, k, W, scores=None, stream=None):
+    """Self-Saliency scores [B, Hkv, N] (fp32) of bf16 q [B,Hq,N,d], k [B,Hkv,N,d]."""
+    B, Hq, N, d = q.shape
+    sh = Shape(B, Hq, k.shape[1], N, d, d)
+    if scores is None:
+        scores = torch.empty((B, k.shape[1], N), dtype=torch.float32, device=q.device)
+    _check(lib().still_score(ct.byref(sh), _ptr(q, torch.bfloat16, "q"), _ptr(k, torch.bfloat16, "k"), W,
+                             _ptr(scores, torch.float32, "scores"), _stream(stream)), "still_score")
+    return scores
+
+
+def select(scores, Hq, d, W, C, m, T_max, sel_idx=None, stream=None):
+    """Top-lambda of each completed chunk: int32 [B, Hkv, T_max, lambda]."""
+    B, Hkv, N = scores.shape
+    lam = lam_of(W, m, T_max)
+    sh = Shape(B, Hq, Hkv, N, d, d)
+    if sel_idx is None:
+        sel_idx = torch.empty((B, Hkv, T_max, max(lam, 0)), dtype=torch.int32, device=scores.device)
+    _check(lib().still_select(ct.byref(sh), _ptr(scores, torch.float32, "scores"), W, C, m, T_max,
+                              _ptr(sel_idx, torch.int32, "sel_idx"), _stream(stream)), "still_select")
+    return sel_idx
+
+
+def npmap(x, Wf, stream=None):
+    """NP-Map of the rows of bf16 x [..., d] with fp32 Wf [d, d_f] -> fp32 [..., d_f]."""
+    d, df = Wf.shape
+    rows = x.numel() // d
+    phi = torch.empty(x.shape[:-1] + (df,), dtype=torch.float32, device=x.device)
+    _check(lib().still_npmap(_ptr(x, torch.bfloat16, "x"), rows, d, _ptr(Wf, torch.float32, "Wf"), df,
+                             _ptr(phi, torch.float32, "phi"), _stream(stream)), "still_npmap")
+    return phi
+
+
+def workspace_size(q, k, Wf, W, C, m, T_max):
+    sh = shape_of(q, k, Wf)
+    return lib().still_prefill_workspace_size(ct.byref(sh), W, C, m, T_max)
+
+
+class DecodeState:
+    """Caller-owned decode state of B sequences (device tensors), see still.h."""
+
+    def __init__(self, B, Hkv, d, df, C, m, device="cuda"):
+        dev = torch.device(device)
+        self.B, self.Hkv, self.d, self.df, self.C, self.m = B, Hkv, d, df, C, m
+        self.K = torch.zeros((B, Hkv, m, d), dtype=torch.bfloat16, device=dev)
+        self.V = torch.zeros((B, Hkv, m, d), dtype=torch.bfloat16, device=dev)
+        self.slot_pos = torch.full((B, Hkv, m), -1, dtype=torch.int32, device=dev)
+        self.slot_cnt = torch.zeros((B, Hkv, m), dtype=torch.int32, device=dev)
+        self.slot_score = torch.zeros((B, Hkv, m), dtype=torch.float32, device=dev)
+        self.S = torch.zeros((B, Hkv, df, d), dtype=torch.float32, device=dev)
+        self.z = torch.zeros((B, Hkv, df), dtype=torch.float32, device=dev)
+        self.score_ring = torch.zeros((B, Hkv, C), dtype=torch.float32, device=dev)
+        self.t = torch.zeros((B, Hkv), dtype=torch.int64, device=dev)
+        self.status = torch.zeros((4,), dtype=torch.int32, device=dev)
+
+    def c_struct(self):
+        return DecodeStateC(*(t.data_ptr() for t in (self.K, self.V, self.slot_pos, self.slot_cnt,
+                                                       self.slot_score, self.S, self.z, self.score_ring,
+                                                       self.t, self.status)))
+
+    def nbytes(self):
+        return sum(t.numel() * t.element_size() for t in (self.K, self.V, self.slot_pos, self.slot_cnt,
+                                                          self.slot_score, self.S, self.z, self.score_ring,
+                                                          self.t))
+
+    def read_status(self, stream=None):
+        v = ct.c_int32(0)
+        _check(lib().still_read_status(ct.c_void_p(self.status.data_ptr()), _stream(stream), ct.byref(v)),
+               "still_read_status")
+        return v.value
+
+
+def prefill(q, k, v, Wf, W, C, m, T_max, out=None, sel_idx=None, workspace=None, export_state=None,
+            stream=None):
+    """Chunk-parallel prefill of one layer.  Returns (out [B,Hq,N,d] bf16, sel_idx)."""
+    B, Hq, N, d = q.shape
+    Hkv = k.shape[1]
+    lam = lam_of(W, m, T_max)
+    sh = shape_of(q, k, Wf)
+    if out is None:
+        out = torch.empty_like(q)
+    if sel_idx is None:
+        sel_idx = torch.empty((B, Hkv, T_max, max(lam, 0)), dtype=torch.int32, device=q.device)
+    ws_ptr, ws_bytes = None, 0
+    if workspace is not None:
+        ws_ptr, ws_bytes = _ptr(workspace, torch.uint8, "workspace"), workspace.numel()
+    st = ct.byref(export_state.c_struct()) if export_state is not None else None
+    _check(lib().still_prefill(ct.byref(sh), _ptr(q, torch.bfloat16, "q"), _ptr(k, torch.bfloat16, "k"),
+                               _ptr(v, torch.bfloat16, "v"), _ptr(Wf, torch.float32, "Wf"), W, C, m, T_max,
+                               _ptr(out, torch.bfloat16, "out"),
+                               _ptr(sel_idx, torch.int32, "sel_idx") if sel_idx.numel() else None,
+                               ws_ptr, ws_bytes, st, _stream(stream)), "still_prefill")
+    return out, sel_idx
+
+
+def decode_state_init(state: DecodeState, Hq, W, C, m, T_max, stream=None):
+    sh = Shape(state.B, Hq, state.Hkv, 0, state.d, state.df)
+    _check(lib().still_decode_state_init(ct.byref(sh), ct.byref(state.c_struct()), W, C, m, T_max,
+                                         _stream(stream)), "still_decode_state_init")
+
+
+def decode_step(state: DecodeState, q_t, k_t, v_t, Wf, W, C, m, T_max, out_t=None, stream=None):
+    """One token per sequence: q_t [B,Hq,d], k_t, v_t [B,Hkv,d] (bf16) -> out_t [B,Hq,d]."""
+    B, Hq, d = q_t.shape
+    sh = Shape(B, Hq, k_t.shape[1], 0, d, Wf.shape[1])
+    if out_t is None:
+        out_t = torch.empty_like(q_t)
+    _check(lib().still_decode_step(ct.byref(sh), ct.byref(state.c_struct()), _ptr(q_t, torch.bfloat16, "q_t"),
+                                   _ptr(k_t, torch.bfloat16, "k_t"), _ptr(v_t, torch.bfloat16, "v_t"),
+                                   _ptr(Wf, torch.float32, "Wf"), W, C, m, T_max,
+                                   _ptr(out_t, torch.bfloat16, "out_t"), _stream(stream)), "still_decode_step")
+    return out_t
+
+
+def timing_enable(on=True):
+    lib().still_timing_enable(1 if on else 0)
+
+
+def timing_read():
+    """{kernel name: (launches, total ms)} since the last read."""
+    buf = (KernelTime * 64)()
+    n = lib().still_timing_read(buf, 64)
+    return {buf[i].name.decode(): (buf[i].launches, buf[i].ms) for i in range(min(n, 64))}
