@@ -1,0 +1,457 @@
+"""Benchmark of the STILL layer on GB300: one JSON line.
+
+A step is one chunk-parallel prefill forward of the Llama-3-8B-shaped layer at
+16K context (B=1, 32 query / 8 kv heads, d = d_f = 128, W=64, C=256, m=288,
+T_max=64, lambda=3): score -> select -> linear state -> hybrid attention, all
+in libstill's kernels, on seeded synthetic inputs resident in HBM.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun (N > 1) every rank runs its own layer (its own seed): weak
+scaling, no collective on the data path; value = all ranks' tokens / the max
+over ranks of the timed region.  --impl reference times the CPU oracle (the
+fp64 streaming recurrence) on the host cores instead; with N > 1 only rank 0
+runs it.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOAD = "llama3_8b_layer_prefill_16k"
+DECODE_WORKLOAD = "llama31_8b_decode_b128_ctx16k"
+METRIC = "prefill tokens/s on 1 GB300 (16K, Llama-3-8B layer); % of BF16/HBM roofline"
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=50)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--no-decode", action="store_true", help="skip the decode-step measurement")
+    p.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--cpu-tokens", type=int, default=16384, help="tokens of the CPU-baseline sample")
+    p.add_argument("--seed", type=int, default=0)
+    return p.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ---------------------------------------------------------------------------
+# algorithmic work (what the method must do; no padded or masked work)
+# ---------------------------------------------------------------------------
+
+def algorithmic(w, sel_idx):
+    """FLOPs and bytes of one prefill, the selection counted exactly."""
+    import numpy as np
+    N, d, df, Hq, Hkv, B = w.N, w.d, w.df, w.Hq, w.Hkv, w.B
+    t = np.arange(N)
+    win = np.minimum(t + 1, w.W).astype(np.float64)
+    # kept tokens visible to query t: chunk(j) < chunk(t) and j <= t - W
+    sel = sel_idx.reshape(B, Hkv, -1)
+    n_sa_sel = 0.0
+    la_keys = 0.0
+    for b in range(B):
+        for g in range(Hkv):
+            s = np.sort(sel[b, g][sel[b, g] >= 0])
+            ct = t // w.C
+            # per query: count kept j with j // C < ct and j <= t - W
+            lim_chunk = np.searchsorted(s // w.C, ct, side="left")       # kept in earlier chunks
+            lim_pos = np.searchsorted(s, t - w.W, side="right")          # kept with j <= t - W
+            vis = np.minimum(lim_chunk, lim_pos)
+            n_sa_sel += vis.sum()
+            la_keys += N - w.W - len(s) if N > w.W else 0
+    sa_keys = Hq * B * win.sum() + (Hq // Hkv) * n_sa_sel
+    F_score = 2.0 * d * Hq * B * win.sum()
+    F_feat = 2.0 * d * df * (Hq + Hkv) * B * N
+    F_fold = 2.0 * df * d * la_keys
+    F_read = 2.0 * df * (d + 1) * Hq * B * N
+    F_sa = 4.0 * d * sa_keys
+    bytes_io = 2.0 * B * N * d * (2 * Hq + 2 * Hkv) + 4.0 * d * df
+    return dict(F_score=F_score, F_feat=F_feat, F_fold=F_fold, F_readout=F_read, F_sa=F_sa,
+                flops=F_score + F_feat + F_fold + F_read + F_sa, bytes=bytes_io,
+                attn_flops=F_sa + F_read + 2.0 * d * df * Hq * B * N,
+                mean_sa_keys=sa_keys / (Hq * B * N))
+
+
+def kernel_bytes(w):
+    """Algorithmic HBM bytes per launch of each kernel."""
+    B, N, d, df, Hq, Hkv = w.B, w.N, w.d, w.df, w.Hq, w.Hkv
+    q = 2.0 * B * Hq * N * d
+    kv = 2.0 * B * Hkv * N * d
+    return {"hybrid_attn": 2 * q + 2 * kv, "score": q + kv + 4.0 * B * Hkv * N,
+            "linstate": 2 * kv, "select": 4.0 * B * Hkv * N, "scan": 0.0}
+
+
+def profile_traffic(kernel):
+    """dram bytes per launch from the committed ncu summary, if it was taken
+    from the current source of that kernel's file."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    src_of = {"hybrid_attn": "hybrid.cu", "score": "score_select.cu", "linstate": "linstate.cu"}
+    f = src_of.get(kernel)
+    if not f:
+        return None
+    sha = hashlib.sha256(open(os.path.join(ROOT, "linear_attention_linearization_gb300", "csrc", f),
+                              "rb").read()).hexdigest()[:16]
+    for line in open(path):
+        m = re.match(r"\s*(\w+)\s+sha=(\w+)\s+bytes_per_launch=([0-9.eE+]+)", line)
+        if m and m.group(1) == kernel and m.group(2) == sha:
+            return float(m.group(3))
+    return None
+
+
+# ---------------------------------------------------------------------------
+# clocks
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        self.lines = []
+        if self.proc:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in getattr(self, "lines", []):
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle
+# ---------------------------------------------------------------------------
+
+def oracle_sample(q, k, v, Wf, w, tokens, threads):
+    """Run the fp64 streaming oracle over `tokens` tokens of every kv head."""
+    from linear_attention_linearization_gb300.inputs import to_f64
+    from oracle import ref
+    qa = to_f64(q[:, :, :tokens])
+    ka = to_f64(k[:, :, :tokens])
+    va = to_f64(v[:, :, :tokens])
+    Wa = to_f64(Wf)
+    t0 = time.perf_counter()
+    ref.prefill(qa, ka, va, Wa, w.W, w.C, w.m, w.T_max, threads=threads)
+    return time.perf_counter() - t0
+
+
+def cpu_threads(units):
+    try:
+        n = len(os.sched_getaffinity(0))
+    except AttributeError:
+        n = os.cpu_count() or 1
+    return max(1, min(n, units))
+
+
+# ---------------------------------------------------------------------------
+# arms
+# ---------------------------------------------------------------------------
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        import torch
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+        pg = dist
+    return world, rank, local, pg
+
+
+def reduce_max(pg, x, device):
+    if pg is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+def run_reference(args):
+    world, rank, local, pg = dist_setup()
+    if rank != 0:
+        return
+    import torch
+    from linear_attention_linearization_gb300 import inputs
+    w = inputs.WORKLOADS[WORKLOAD]
+    tokens = 1024
+    q, k, v, Wf = inputs.make_inputs(w, seed=args.seed, N=tokens)
+    thr = cpu_threads(w.B * w.Hkv)
+    for _ in range(args.warmup):
+        oracle_sample(q, k, v, Wf, w, tokens, thr)
+    total = 0.0
+    for _ in range(args.steps):
+        total += oracle_sample(q, k, v, Wf, w, tokens, thr)
+    tps = tokens * args.steps / total
+    sample = (f"fp64 streaming oracle, all {w.Hkv} kv heads x {w.Hq} query heads, tokens 0..{tokens - 1} of the "
+              f"16K layer per step (early tokens see fewer kept keys than the layer average)")
+    line = {"impl": "reference", "metric": METRIC, "value": tps, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": WORKLOAD, **w.asdict()},
+            "cpu_baseline": {"value": tps, "unit": "tokens/s", "cores": thr, "kind": "oracle", "sample": sample},
+            "e2e": {"value": tps, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    del torch
+
+
+def run_ours(args):
+    import torch
+    from linear_attention_linearization_gb300 import build, inputs
+    build.build()
+    from linear_attention_linearization_gb300 import still
+
+    world, rank, local, pg = dist_setup()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    w = inputs.WORKLOADS[WORKLOAD]
+    seed = args.seed + 1000 * rank
+    q, k, v, Wf = inputs.make_inputs(w, seed=seed, device=dev)
+    out = torch.empty_like(q)
+    lam = w.lam
+    sel = torch.empty((w.B, w.Hkv, w.T_max, lam), dtype=torch.int32, device=dev)
+    ws = torch.empty(still.workspace_size(q, k, Wf, w.W, w.C, w.m, w.T_max), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        still.prefill(q, k, v, Wf, w.W, w.C, w.m, w.T_max, out=out, sel_idx=sel, workspace=ws, stream=stream)
+
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+    with ClockSampler(local) as clk:
+        for _ in range(max(3, args.warmup)):
+            step()
+        torch.cuda.synchronize(dev)
+        if pg is not None:
+            pg.barrier()
+        torch.cuda.synchronize(dev)
+        still.timing_read()
+        still.timing_enable(True)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
+        wall0 = time.perf_counter()
+        for i in range(args.steps):
+            flush.fill_(float(i))              # evict the previous step's data from L2
+            ev[i][0].record(stream)
+            step()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize(dev)
+        wall = time.perf_counter() - wall0
+        still.timing_enable(False)
+        if pg is not None:
+            pg.barrier()
+    ktimes = still.timing_read()
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    t_total = sum(step_ms) / 1e3
+    t_max = reduce_max(pg, t_total, dev)
+    tokens_all = world * w.B * w.N * args.steps
+    value = tokens_all / t_max
+    ms_per_step = 1e3 * t_max / args.steps
+
+    # -------- roofline of the dominant kernel --------
+    pk, pk_kind = peaks()
+    alg = algorithmic(w, sel.cpu().numpy())
+    kb = kernel_bytes(w)
+    dom = max(ktimes.items(), key=lambda kv: kv[1][1])[0] if ktimes else None
+    launches = sum(n for n, _ in ktimes.values())
+    roof = None
+    if dom:
+        n, ms = ktimes[dom]
+        per = ms / n / 1e3
+        if dom == "hybrid_attn":
+            t_hbm = kb[dom] / (pk["hbm_gbs"] * 1e9)
+            t_flop = alg["attn_flops"] / (pk["bf16_tflops"] * 1e12)
+            bound = "hbm" if t_hbm >= t_flop else "tensor"
+        else:
+            bound = "hbm"
+        if bound == "hbm":
+            ach = kb.get(dom, 0.0) / per / 1e9
+            peak_v, unit = pk["hbm_gbs"], "GB/s"
+        else:
+            ach = alg["attn_flops"] / per / 1e12
+            peak_v, unit = pk["bf16_tflops"], "TFLOP/s"
+        roof = {"kernel": dom, "bound": bound, "achieved": ach, "peak": peak_v, "unit": unit,
+                "frac": ach / peak_v, "peak_source": pk_kind, "traffic": profile_traffic(dom),
+                "algorithmic_bytes_per_launch": kb.get(dom), "algorithmic_flops_per_launch": alg["attn_flops"],
+                "launch_ms": per * 1e3}
+    step_roof_s = max(alg["flops"] / (pk["bf16_tflops"] * 1e12), alg["bytes"] / (pk["hbm_gbs"] * 1e9))
+
+    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": max(3, args.warmup), "ms_per_step": ms_per_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": WORKLOAD, **w.asdict(), "l2": "L2 flushed (258 MB write) before every timed "
+                       "step; working set 336 MB > 129 MB L2", "parallelism": f"replicas x{world}"},
+            "roofline": roof,
+            "step_roofline": {"algorithmic_flops": alg["flops"], "algorithmic_bytes": alg["bytes"],
+                              "roofline_ms": step_roof_s * 1e3, "frac_of_roofline": step_roof_s * 1e3 / ms_per_step,
+                              "mean_softmax_keys_per_query": alg["mean_sa_keys"], "peak_source": pk_kind},
+            "kernels": {k2: {"launches": n, "ms_per_launch": ms / n} for k2, (n, ms) in ktimes.items()},
+            "gpu_launches": launches, "wall_s_timed_region": wall,
+            "clocks": clk.summary()}
+
+    # -------- end to end through host buffers --------
+    if not args.no_e2e:
+        hq = q.cpu().pin_memory()
+        hk = k.cpu().pin_memory()
+        hv = v.cpu().pin_memory()
+        hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        hsel = torch.empty(sel.shape, dtype=sel.dtype).pin_memory()
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+
+        def e2e_step():
+            dq.copy_(hq, non_blocking=True)
+            dk.copy_(hk, non_blocking=True)
+            dv.copy_(hv, non_blocking=True)
+            still.prefill(dq, dk, dv, Wf, w.W, w.C, w.m, w.T_max, out=out, sel_idx=sel, workspace=ws,
+                          stream=stream)
+            hout.copy_(out, non_blocking=True)
+            hsel.copy_(sel, non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        n_e2e = max(3, min(args.steps, 20))
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(n_e2e):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        t_e2e = reduce_max(pg, a.elapsed_time(b) / 1e3, dev)
+        line["e2e"] = {"value": world * w.B * w.N * n_e2e / t_e2e, "unit": "tokens/s",
+                       "h2d_bytes_per_step": int(hq.numel() * 2 + hk.numel() * 2 + hv.numel() * 2),
+                       "d2h_bytes_per_step": int(hout.numel() * 2 + hsel.numel() * 4), "steps": n_e2e}
+
+    # -------- decode step (128 sequences at 16K) --------
+    if not args.no_decode and rank == 0:
+        line["decode_step"] = bench_decode(still, inputs, dev, stream, pk, pk_kind, args)
+
+    # -------- CPU oracle baseline --------
+    if not args.no_cpu and rank == 0 and world == 1:
+        thr = cpu_threads(w.B * w.Hkv)
+        toks = min(args.cpu_tokens, w.N)
+        secs = oracle_sample(q.cpu(), k.cpu(), v.cpu(), Wf.cpu(), w, toks, thr)
+        line["cpu_baseline"] = {"value": w.B * toks / secs, "unit": "tokens/s", "cores": thr, "kind": "oracle",
+                                "sample": f"fp64 streaming oracle over tokens 0..{toks - 1} of all {w.Hkv} kv heads "
+                                          f"({w.Hq} query heads) of the same inputs, one thread per kv head",
+                                "seconds": secs}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if pg is not None:
+        pg.destroy_process_group()
+
+
+def bench_decode(still, inputs, dev, stream, pk, pk_kind, args):
+    import torch
+    w = inputs.WORKLOADS[DECODE_WORKLOAD]
+    q, k, v, Wf = inputs.make_inputs(w, seed=args.seed + 7, device=dev)
+    st = still.DecodeState(w.B, w.Hkv, w.d, w.df, w.C, w.m, device=dev)
+    still.prefill(q, k, v, Wf, w.W, w.C, w.m, w.T_max, export_state=st, stream=stream)
+    del q, k, v
+    torch.cuda.synchronize(dev)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(args.seed + 8)
+    steps = 20
+    qt = torch.randn((steps, w.B, w.Hq, w.d), generator=gen, device=dev).to(torch.bfloat16)
+    kt = torch.randn((steps, w.B, w.Hkv, w.d), generator=gen, device=dev).to(torch.bfloat16)
+    vt = torch.randn((steps, w.B, w.Hkv, w.d), generator=gen, device=dev).to(torch.bfloat16)
+    yt = torch.empty((w.B, w.Hq, w.d), dtype=torch.bfloat16, device=dev)
+    valid = int((st.slot_pos[0, 0] >= 0).sum().item())
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+    times = []
+    for i in range(steps):
+        flush.fill_(float(i))
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        still.decode_step(st, qt[i], kt[i], vt[i], Wf, w.W, w.C, w.m, w.T_max, out_t=yt, stream=stream)
+        b.record(stream)
+        times.append((a, b))
+    torch.cuda.synchronize(dev)
+    ms = [a.elapsed_time(b) for a, b in times][3:]
+    per = statistics.median(ms) / 1e3
+    # bytes a step must move: valid K,V slots, S read + write, z, q, k, v, out
+    units = w.B * w.Hkv
+    by_valid = units * (2.0 * valid * w.d * 2 + 2.0 * w.df * w.d * 4 + 2.0 * w.df * 4) + \
+        w.B * (2.0 * w.Hq * w.d * 2 + 2.0 * w.Hkv * w.d * 2)
+    ach = by_valid / per / 1e9
+    return {"workload": DECODE_WORKLOAD, "sequences": w.B, "context": w.N, "ms_per_step": per * 1e3,
+            "tokens_per_s": w.B / per, "valid_slots": valid, "algorithmic_bytes_per_step": by_valid,
+            "roofline": {"kernel": "decode_step", "bound": "hbm", "achieved": ach, "peak": pk["hbm_gbs"],
+                         "unit": "GB/s", "frac": ach / pk["hbm_gbs"], "peak_source": pk_kind,
+                         "traffic": profile_traffic("decode_step")},
+            "state_bytes": st.nbytes()}
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

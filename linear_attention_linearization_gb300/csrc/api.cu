@@ -141,10 +141,12 @@ still_status cuda_status(cudaError_t e)
     return STILL_ERR_CUDA;
 }
 
-bool state_ok(const still_decode_state *s)
+// With m == 0 (no softmax budget at all) the slot arrays are empty and may be null.
+bool state_ok(const still_decode_state *s, int m)
 {
-    return s && s->K && s->V && s->slot_pos && s->slot_cnt && s->slot_score && s->S && s->z && s->score_ring &&
-           s->t && s->status && aligned16(s->K) && aligned16(s->V) && aligned16(s->S);
+    if (!s || !s->S || !s->z || !s->score_ring || !s->t || !s->status || !aligned16(s->S)) return false;
+    if (m == 0) return true;
+    return s->K && s->V && s->slot_pos && s->slot_cnt && s->slot_score && aligned16(s->K) && aligned16(s->V);
 }
 
 }  // namespace
@@ -224,20 +226,22 @@ still_status still_prefill(const still_shape *shape, const still_bf16 *q, const 
     Dims dm;
     still_status st = make_dims(shape, W, C, m, T_max, &dm);
     if (st != STILL_OK) return st;
-    if (!q || !k || !v || !Wf || !out) return STILL_ERR_INVALID_ARG;
-    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(Wf) || !aligned16(out) ||
-        (sel_idx && !aligned16(sel_idx)) || (workspace && !aligned16(workspace)))
-        return STILL_ERR_INVALID_ARG;
-    if (export_state && !state_ok(export_state)) return STILL_ERR_INVALID_ARG;
     cudaStream_t s = (cudaStream_t)stream;
-    const SegPlan sp = plan_segments(dm);
-    const WsLayout L = ws_layout(dm, sp);
-    if (workspace && workspace_bytes < L.total) return STILL_ERR_WORKSPACE;
+    if (sel_idx && !aligned16(sel_idx)) return STILL_ERR_INVALID_ARG;
     if (dm.N == 0) {
+        // nothing to attend; the selection table is all "no token"
         if (sel_idx && dm.lam > 0)
             return cuda_status(cudaMemsetAsync(sel_idx, 0xff, (size_t)dm.B * dm.Hkv * dm.T_max * dm.lam * 4, s));
         return STILL_OK;
     }
+    if (!q || !k || !v || !Wf || !out) return STILL_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(Wf) || !aligned16(out) ||
+        (workspace && !aligned16(workspace)))
+        return STILL_ERR_INVALID_ARG;
+    if (export_state && !state_ok(export_state, dm.m)) return STILL_ERR_INVALID_ARG;
+    const SegPlan sp = plan_segments(dm);
+    const WsLayout L = ws_layout(dm, sp);
+    if (workspace && workspace_bytes < L.total) return STILL_ERR_WORKSPACE;
     void *ws = workspace;
     if (!ws) {
         cudaError_t e = cudaMallocAsync(&ws, L.total, s);
@@ -273,7 +277,7 @@ still_status still_decode_state_init(const still_shape *shape, const still_decod
     Dims dm;
     still_status st = make_dims(&sh, W, C, m, T_max, &dm);
     if (st != STILL_OK) return st;
-    if (!state_ok(state)) return STILL_ERR_INVALID_ARG;
+    if (!state_ok(state, dm.m)) return STILL_ERR_INVALID_ARG;
     cudaStream_t s = (cudaStream_t)stream;
     const size_t units = (size_t)dm.B * dm.Hkv;
     cudaError_t e = cudaMemsetAsync(state->K, 0, units * m * dm.d * 2, s);
@@ -298,7 +302,7 @@ still_status still_decode_step(const still_shape *shape, const still_decode_stat
     Dims dm;
     still_status st = make_dims(&sh, W, C, m, T_max, &dm);
     if (st != STILL_OK) return st;
-    if (!state_ok(state) || !q_t || !k_t || !v_t || !Wf || !out_t) return STILL_ERR_INVALID_ARG;
+    if (!state_ok(state, dm.m) || !q_t || !k_t || !v_t || !Wf || !out_t) return STILL_ERR_INVALID_ARG;
     if (!aligned16(q_t) || !aligned16(k_t) || !aligned16(v_t) || !aligned16(Wf) || !aligned16(out_t))
         return STILL_ERR_INVALID_ARG;
     if (dm.G > 8) return STILL_ERR_UNSUPPORTED;
