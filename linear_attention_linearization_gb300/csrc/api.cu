@@ -92,13 +92,15 @@ still_status make_dims(const still_shape *sh, int W, int C, int m, int T_max, Di
     return STILL_OK;
 }
 
+// One CTA per segment of 32-token tiles; segments are sized so that all
+// (sequence, kv head, segment) CTAs fit one wave of one CTA per SM.
 SegPlan plan_segments(const Dims &dm)
 {
     SegPlan sp;
-    sp.T = 16;
+    sp.T = 32;
     const int ntile = (dm.N + sp.T - 1) / sp.T;
     const int units = dm.B * dm.Hkv;
-    int target = (2 * 152 + units - 1) / units;
+    int target = 152 / units;
     if (target < 1) target = 1;
     if (target > ntile) target = ntile;
     if (ntile == 0) {
@@ -113,7 +115,8 @@ SegPlan plan_segments(const Dims &dm)
 }
 
 struct WsLayout {
-    size_t status, scores, fsel, flag, phik, dS, dz, total;
+    size_t status, scores, fsel, flag, phik, kk, vk, phk, wft, dS, dz, total;
+    size_t kept_bytes;
 };
 
 size_t al(size_t x) { return (x + 255) & ~size_t(255); }
@@ -123,11 +126,17 @@ WsLayout ws_layout(const Dims &dm, const SegPlan &sp)
     WsLayout L;
     size_t o = 0;
     const size_t units = (size_t)dm.B * dm.Hkv;
+    const size_t KP = (size_t)dm.T_max * dm.lam > 0 ? (size_t)dm.T_max * dm.lam : 1;
     L.status = o; o += al(256);
     L.scores = o; o += al(units * dm.N * 4);
-    L.fsel = o; o += al(units * dm.T_max * (size_t)(dm.lam > 0 ? dm.lam : 1) * 4);
+    L.fsel = o; o += al(units * KP * 4);
     L.flag = o; o += al(units * dm.N);
-    L.phik = o; o += al(units * dm.N * (size_t)dm.df * 4);
+    L.phik = o; o += al(units * dm.N * (size_t)dm.df * 2);
+    L.kk = o; o += al(units * KP * dm.d * 2);
+    L.vk = o; o += al(units * KP * dm.d * 2);
+    L.phk = o; o += al(units * KP * dm.df * 2);
+    L.kept_bytes = o - L.kk;
+    L.wft = o; o += al((size_t)dm.df * dm.d * 2);
     L.dS = o; o += al(units * (size_t)(sp.nseg + 1) * dm.df * dm.d * 4);
     L.dz = o; o += al(units * (size_t)(sp.nseg + 1) * dm.df * 4);
     L.total = o;
@@ -252,15 +261,29 @@ still_status still_prefill(const still_shape *shape, const still_bf16 *q, const 
     float *scores = (float *)(base + L.scores);
     int32_t *fsel = (int32_t *)(base + L.fsel);
     uint8_t *flag = (uint8_t *)(base + L.flag);
-    float *phik = (float *)(base + L.phik);
+    uint16_t *phik = (uint16_t *)(base + L.phik);
+    uint16_t *kk = (uint16_t *)(base + L.kk);
+    uint16_t *vk = (uint16_t *)(base + L.vk);
+    uint16_t *phk = (uint16_t *)(base + L.phk);
+    uint16_t *wft = (uint16_t *)(base + L.wft);
     float *dS = (float *)(base + L.dS);
     float *dz = (float *)(base + L.dz);
+    const bool tc = hybrid_tc_supported(dm);
     cudaError_t e = cudaMemsetAsync(base, 0, L.status + 256, s);
     if (e == cudaSuccess) e = cudaMemsetAsync(flag, 0, (size_t)dm.B * dm.Hkv * dm.N, s);
-    if (e == cudaSuccess && dm.lam > 0 && dm.W >= 1) e = launch_score(dm, q, k, scores, s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(kk, 0, L.kept_bytes, s);
+    if (e == cudaSuccess && dm.lam > 0) e = launch_score(dm, q, k, scores, s);
     if (e == cudaSuccess && dm.lam > 0) e = launch_select(dm, scores, sel_idx, fsel, flag, s);
-    if (e == cudaSuccess) e = launch_linstate(dm, sp, k, v, Wf, flag, phik, dS, dz, s);
-    if (e == cudaSuccess) e = launch_hybrid(dm, sp, q, k, v, Wf, phik, fsel, flag, dS, dz, out, status, s);
+    if (e == cudaSuccess) e = launch_features(dm, k, v, Wf, flag, fsel, phik, kk, vk, phk, tc ? wft : nullptr, s);
+    if (e == cudaSuccess) e = launch_linstate(dm, sp, phik, v, dS, dz, s);
+    if (e == cudaSuccess) {
+        if (tc) {
+            TCBuffers bf{q, k, v, kk, vk, phik, phk, wft, out};
+            e = launch_hybrid_tc(dm, sp, bf, fsel, dS, dz, status, s);
+        } else {
+            e = launch_hybrid_general(dm, sp, q, k, v, Wf, phik, phk, fsel, dS, dz, out, status, s);
+        }
+    }
     if (e == cudaSuccess && export_state) e = launch_export(dm, sp, k, v, scores, fsel, dS, dz, *export_state, s);
     if (!workspace) {
         cudaError_t e2 = cudaFreeAsync(ws, s);

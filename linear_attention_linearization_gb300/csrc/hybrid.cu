@@ -9,13 +9,16 @@
 //   y_t   = (sum_SA e^{s-c} v + sum_LA (phi(q).phi(k)) v) /
 //           (sum_SA e^{s-c} + sum_LA phi(q).phi(k)),   c = max_SA s.
 //
-// One CTA walks the query tiles of one segment of one (sequence, kv head) in
-// order.  Its running state S_run, z_run holds every key j < t0 - W that sits
-// in no budget slot (t0 = first token of the tile).  For a query t of the
-// tile the linear keys are then
-//   S_run  +  keys e0 <= j <= t-W  that are unslotted or of t's own chunk
-//          +  slotted keys of t's own chunk below e0,          e0 = t0 - W,
+// General-shape kernel on CUDA cores: it serves the shapes outside the
+// tensor-core kernel's envelope (see hybrid_tc.cu).  One CTA walks the query
+// tiles of one segment of one (sequence, kv head) in order.  Its running state
+// S_run, z_run holds every key j < t0 - W that sits in no budget slot (t0 =
+// first token of the tile).  For a query t of the tile the linear keys are
+//   S_run  +  unslotted keys e0 <= j <= t-W                     (e0 = t0 - W)
+//          +  slotted keys of t's own chunk with j <= t-W,
 // because a kept token is a softmax key only for queries of later chunks.
+// The feature table has zero rows for slotted keys, so the second term needs
+// no test; the third reads the unmasked features of the kept table.
 #include "common.cuh"
 
 namespace still {
@@ -23,8 +26,8 @@ namespace still {
 template <int D, int DF>
 __global__ void __launch_bounds__(256) hybrid_kernel(const uint16_t *__restrict__ q, const uint16_t *__restrict__ k,
                                                      const uint16_t *__restrict__ v, const float *__restrict__ Wf,
-                                                     const float *__restrict__ phik, const int32_t *__restrict__ fsel,
-                                                     const uint8_t *__restrict__ flag, const float *__restrict__ dS,
+                                                     const uint16_t *__restrict__ phik, const uint16_t *__restrict__ phkept,
+                                                     const int32_t *__restrict__ fsel, const float *__restrict__ dS,
                                                      const float *__restrict__ dz, Dims dm, SegPlan sp,
                                                      uint16_t *__restrict__ out, int32_t *status)
 {
@@ -44,8 +47,8 @@ __global__ void __launch_bounds__(256) hybrid_kernel(const uint16_t *__restrict_
     const size_t ug = (size_t)b * dm.Hkv + g;
     const uint16_t *kg = k + ug * dm.N * D;
     const uint16_t *vg = v + ug * dm.N * D;
-    const float *phg = phik + ug * dm.N * DF;
-    const uint8_t *flg = flag + ug * dm.N;
+    const uint16_t *phg = phik + ug * dm.N * DF;
+    const uint16_t *phkg = phkept + ug * dm.T_max * dm.lam * DF;
     const int32_t *fs = fsel + ug * dm.T_max * dm.lam;
     const float inv = rsqrtf((float)D);
     const int col = tid % D, row0 = tid / D;
@@ -113,7 +116,7 @@ __global__ void __launch_bounds__(256) hybrid_kernel(const uint16_t *__restrict_
             }
 
             // linear keys: running state, then the lagged keys of this tile
-            // and the slotted keys of t's own chunk below e0
+            // and the slotted keys of t's own chunk
             float la[PD];
 #pragma unroll
             for (int r = 0; r < PD; ++r) la[r] = 0.f;
@@ -127,22 +130,22 @@ __global__ void __launch_bounds__(256) hybrid_kernel(const uint16_t *__restrict_
             dl = warp_sum(dl);
             const int ilo = max(0, e0);
             const int ni = max(0, t - dm.W - ilo + 1);
-            const int nx = (ct < dm.T_max && e0 > 0) ? dm.lam : 0;
+            const int nx = ct < dm.T_max ? dm.lam : 0;
             for (int p0 = 0; p0 < ni + nx; p0 += 32) {
                 const int p = p0 + lane;
                 int j = -1;
+                const uint16_t *pr = nullptr;
                 if (p < ni) {
                     j = ilo + p;
-                    if (flg[j] && j / dm.C != ct) j = -1;
+                    pr = phg + (size_t)j * DF;
                 } else if (p < ni + nx) {
                     j = fs[ct * dm.lam + (p - ni)];
-                    if (j >= e0) j = -1;
+                    if (j > t - dm.W) j = -1;
+                    pr = phkg + (size_t)(ct * dm.lam + (p - ni)) * DF;
                 }
                 float a = 0.f;
-                if (j >= 0) {
-                    const float *pr = phg + (size_t)j * DF;
-                    for (int i = 0; i < DF; ++i) a = fmaf(fq[i], pr[i], a);
-                }
+                if (j >= 0)
+                    for (int i = 0; i < DF; ++i) a = fmaf(fq[i], bf2f(pr[i]), a);
                 dl += warp_sum(a);
                 for (int jj = 0; jj < 32; ++jj) {
                     const float aj = __shfl_sync(0xffffffffu, a, jj);
@@ -164,10 +167,7 @@ __global__ void __launch_bounds__(256) hybrid_kernel(const uint16_t *__restrict_
         const int flo = max(0, e0), fhi = t0 + nt - dm.W;
         if (fhi > flo) {
             const int nf = fhi - flo;
-            for (int e = tid; e < nf * DF; e += 256) {
-                const int kk = e / DF, i = e % DF;
-                fph[e] = flg[flo + kk] ? 0.f : phg[(size_t)(flo + kk) * DF + i];
-            }
+            for (int e = tid; e < nf * DF; e += 256) fph[e] = bf2f(phg[(size_t)flo * DF + e]);
             for (int e = tid; e < nf * D; e += 256) fv[e] = bf2f(vg[(size_t)flo * D + e]);
             __syncthreads();
 #pragma unroll 4
@@ -189,28 +189,29 @@ __global__ void __launch_bounds__(256) hybrid_kernel(const uint16_t *__restrict_
 
 template <int D, int DF>
 static cudaError_t launch_hybrid_t(const Dims &dm, const SegPlan &sp, const uint16_t *q, const uint16_t *k,
-                                   const uint16_t *v, const float *Wf, const float *phik, const int32_t *fsel,
-                                   const uint8_t *flag, const float *dS, const float *dz, uint16_t *out,
-                                   int32_t *status, cudaStream_t s)
+                                   const uint16_t *v, const float *Wf, const uint16_t *phik,
+                                   const uint16_t *phkept, const int32_t *fsel, const float *dS, const float *dz,
+                                   uint16_t *out, int32_t *status, cudaStream_t s)
 {
     const size_t smem = sizeof(float) * ((size_t)DF * D + DF + 8 * D + 8 * DF + (size_t)sp.T * (DF + D));
     cudaError_t e = cudaFuncSetAttribute(hybrid_kernel<D, DF>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     dim3 grid(sp.nseg, dm.Hkv, dm.B);
-    hybrid_kernel<D, DF><<<grid, 256, smem, s>>>(q, k, v, Wf, phik, fsel, flag, dS, dz, dm, sp, out, status);
+    hybrid_kernel<D, DF><<<grid, 256, smem, s>>>(q, k, v, Wf, phik, phkept, fsel, dS, dz, dm, sp, out, status);
     return cudaGetLastError();
 }
 
-cudaError_t launch_hybrid(const Dims &dm, const SegPlan &sp, const uint16_t *q, const uint16_t *k,
-                          const uint16_t *v, const float *Wf, const float *phik, const int32_t *fsel,
-                          const uint8_t *flag, const float *dS, const float *dz, uint16_t *out,
-                          int32_t *status, cudaStream_t s)
+cudaError_t launch_hybrid_general(const Dims &dm, const SegPlan &sp, const uint16_t *q, const uint16_t *k,
+                                  const uint16_t *v, const float *Wf, const uint16_t *phik, const uint16_t *phkept,
+                                  const int32_t *fsel, const float *dS, const float *dz, uint16_t *out,
+                                  int32_t *status, cudaStream_t s)
 {
-    KTimer tm("hybrid_attn", s);
-    if (dm.d == 64 && dm.df == 64) return launch_hybrid_t<64, 64>(dm, sp, q, k, v, Wf, phik, fsel, flag, dS, dz, out, status, s);
-    if (dm.d == 64) return launch_hybrid_t<64, 128>(dm, sp, q, k, v, Wf, phik, fsel, flag, dS, dz, out, status, s);
-    if (dm.df == 64) return launch_hybrid_t<128, 64>(dm, sp, q, k, v, Wf, phik, fsel, flag, dS, dz, out, status, s);
-    return launch_hybrid_t<128, 128>(dm, sp, q, k, v, Wf, phik, fsel, flag, dS, dz, out, status, s);
+    KTimer tm("hybrid_attn_general", s);
+    if (dm.d == 64 && dm.df == 64)
+        return launch_hybrid_t<64, 64>(dm, sp, q, k, v, Wf, phik, phkept, fsel, dS, dz, out, status, s);
+    if (dm.d == 64) return launch_hybrid_t<64, 128>(dm, sp, q, k, v, Wf, phik, phkept, fsel, dS, dz, out, status, s);
+    if (dm.df == 64) return launch_hybrid_t<128, 64>(dm, sp, q, k, v, Wf, phik, phkept, fsel, dS, dz, out, status, s);
+    return launch_hybrid_t<128, 128>(dm, sp, q, k, v, Wf, phik, phkept, fsel, dS, dz, out, status, s);
 }
 
 }  // namespace still

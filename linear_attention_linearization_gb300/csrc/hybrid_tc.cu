@@ -1,0 +1,681 @@
+// Tensor-core hybrid attention of the prefill (tcgen05 + TMEM, fed by TMA).
+//
+// "STILL: Content-Aware Intra-Layer Hybrid Attention for Efficient LLM
+// Linearization", sections "Content-Aware Routing with Fixed Budget", "Delayed
+// Chunk-Level Selection for Unified Training-Inference Parallelism" and
+// "NP-Map: Norm-Preserving Feature Map":
+//   SA(t) = {t-W < j <= t} U {j kept by chunk(j) < chunk(t), j <= t-W}
+//   LA(t) = {j <= t-W} minus SA(t)
+//   y_t   = (sum_SA e^{s-c} v + phi(q)^T S_LA) / (sum_SA e^{s-c} + phi(q)^T z_LA)
+//
+// One CTA (one per SM) walks the 32-token tiles of one segment of one
+// (sequence, kv head).  A tile is M = 128 rows: the G <= 4 query heads of the
+// group x 32 tokens (rows of absent heads are padding).  Per tile:
+//   U   = Q Wf              -> phi(Q) = ||q|| u / ||u||, u = softmax(U)    (TMEM -> smem)
+//   S   = Q [K_band | K_kept]^T, one MMA per block of 32 keys             (TMEM)
+//         band = the 32-key blocks covering [t0-W+1, t0+31]; kept = the
+//         kept tokens of earlier chunks, a contiguous prefix of the kept table
+//   A   = phi(Q) [phi(K_lag) | phi(K_extra)]^T                             (TMEM)
+//         lag = the 32 keys [t0-W, t0-W+32) that leave the window during the
+//         tile (rows of slotted keys are zero in the feature table); extra =
+//         the kept tokens of the tile's own chunk, which are still linear keys
+//   O   = A V_lagx + sum_p P_p V_p + phi(Q) S_run                          (TMEM)
+//         P = exp(S - c) masked, c = exact row maximum over the softmax keys
+//   dS  = phi(K_lag)^T V_lag -> S_run += dS (fp32 in registers, bf16 copy in smem)
+//   y   = O / (sum P + sum A + phi(Q).z_run)                              (TMA store)
+// Masks (window, causal lag, chunk of the kept tokens) are applied to the
+// logits in TMEM by the row threads; one thread issues every TMA and MMA.
+#include "sm100.cuh"
+#include "tma_host.cuh"
+
+namespace still {
+
+using namespace sm100;
+
+struct TCParams {
+    Dims dm;
+    SegPlan sp;
+    int Wr;        // the band starts at t0 - Wr
+    int nb;        // band blocks of 32 keys
+    int KP;        // rows of the kept tables per (sequence, kv head)
+    const int32_t *fsel;
+    const float *dS;
+    const float *dz;
+    int32_t *status;
+};
+
+struct TCMaps {
+    CUtensorMap q, k, v, kk, vk, vk16, phik, phk16, wft, out;
+};
+
+constexpr int TM_S = 0, TM_O = 320, TM_A = 448, TM_COLS = 512;
+constexpr int MAX_KEY_BLOCKS = 10;   // 320 logit columns
+constexpr int NX = 16;               // extra (kept, own chunk) rows per tile
+
+template <int D, int DF>
+struct TCLayout {
+    static constexpr int CBD = D / 64, CBF = DF / 64;
+    static constexpr uint32_t Q = 0;
+    static constexpr uint32_t WF = Q + CBD * 16384;
+    static constexpr uint32_t PHIQ = WF + CBD * DF * 128;
+    static constexpr uint32_t SRUN = PHIQ + (CBD > CBF ? CBD : CBF) * 16384;
+    static constexpr uint32_t RING = SRUN + CBD * DF * 128;
+    static constexpr uint32_t P = RING + 4 * CBD * 4096;
+    static constexpr uint32_t PHIK = P + 2 * 16384;
+    static constexpr uint32_t VLAG = PHIK + CBF * 6144;
+    static constexpr uint32_t KPOS = VLAG + CBD * 6144;          // int32[MAX_KEY_BLOCKS * 32]
+    static constexpr uint32_t XPOS = KPOS + MAX_KEY_BLOCKS * 32 * 4;
+    static constexpr uint32_t ZRUN = XPOS + NX * 4;
+    static constexpr uint32_t TOTAL = ZRUN + DF * 4;
+};
+
+template <int D, int DF>
+__global__ void __launch_bounds__(128, 1) hybrid_tc_kernel(const __grid_constant__ TCMaps maps, TCParams P)
+{
+    using Lay = TCLayout<D, DF>;
+    constexpr int CBD = Lay::CBD, CBF = Lay::CBF;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    const uint32_t sb = smem_u32(sm);
+    int32_t *kpos = (int32_t *)(sm + Lay::KPOS);
+    int32_t *xpos = (int32_t *)(sm + Lay::XPOS);
+    float *zrun = (float *)(sm + Lay::ZRUN);
+
+    __shared__ uint64_t bar_q, bar_wf, bar_lag, bar_mma, bar_kfull[4], bar_kfree[4], bar_vfull[2], bar_vfree[2],
+        bar_pfree[2];
+    __shared__ uint32_t tmem_base;
+    __shared__ int s_abort;
+
+    const Dims &dm = P.dm;
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const int s = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+    const int unit = b * dm.Hkv + g;
+    const int W = dm.W, C = dm.C, lam = dm.lam;
+    const int tbeg = s * P.sp.L, tend = min((s + 1) * P.sp.L, dm.N);
+    const int ntiles = (tend - tbeg + 31) / 32;
+    const int32_t *fs = P.fsel + (size_t)unit * P.KP;
+
+    if (warp == 0) {
+        tmem_alloc(&tmem_base, TM_COLS);
+        tmem_relinquish();
+    }
+    if (tid == 0) {
+        mbar_init(&bar_q, 1);
+        mbar_init(&bar_wf, 1);
+        mbar_init(&bar_lag, 1);
+        mbar_init(&bar_mma, 1);
+        for (int i = 0; i < 4; ++i) { mbar_init(&bar_kfull[i], 1); mbar_init(&bar_kfree[i], 1); }
+        for (int i = 0; i < 2; ++i) { mbar_init(&bar_vfull[i], 1); mbar_init(&bar_vfree[i], 1); mbar_init(&bar_pfree[i], 1); }
+        fence_barrier_init();
+        s_abort = 0;
+    }
+    // padding rows of absent heads stay zero for the whole kernel
+    for (int i = tid; i < CBD * 16384 / 16; i += 128) {
+        const int row = (i * 16 % 16384) / 128;
+        if (row >= dm.G * 32) reinterpret_cast<uint4 *>(sm + Lay::Q)[i] = make_uint4(0, 0, 0, 0);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_base;
+    const uint32_t tlane = tmem + ((uint32_t)(warp * 32) << 16);   // this warp's TMEM lanes
+
+    // ---- running linear state: thread f holds row f of S_run in fp32 ------------
+    float srun[D];
+    {
+        const float *S0 = P.dS + ((size_t)unit * (P.sp.nseg + 1) + s) * (size_t)(DF * D);
+        const int f = tid;
+#pragma unroll
+        for (int c = 0; c < D; ++c) srun[c] = f < DF ? S0[(size_t)f * D + c] : 0.f;
+        if (f < DF) zrun[f] = P.dz[((size_t)unit * (P.sp.nseg + 1) + s) * DF + f];
+        if (f < DF) {
+#pragma unroll
+            for (int c8 = 0; c8 < D / 8; ++c8) {
+                uint4 pk;
+                pk.x = pack_bf16(srun[c8 * 8 + 0], srun[c8 * 8 + 1]);
+                pk.y = pack_bf16(srun[c8 * 8 + 2], srun[c8 * 8 + 3]);
+                pk.z = pack_bf16(srun[c8 * 8 + 4], srun[c8 * 8 + 5]);
+                pk.w = pack_bf16(srun[c8 * 8 + 6], srun[c8 * 8 + 7]);
+                *reinterpret_cast<uint4 *>(sm + Lay::SRUN + (c8 / 8) * (DF * 128) + sw128(f, c8 % 8)) = pk;
+            }
+        }
+    }
+
+    // ---- loads of the first tile ------------------------------------------------
+    auto load_q = [&](int t0) {
+        mbar_expect_tx(&bar_q, dm.G * CBD * 4096);
+        for (int hh = 0; hh < dm.G; ++hh)
+            for (int cb = 0; cb < CBD; ++cb)
+                tma_load_3d(sm + Lay::Q + cb * 16384 + hh * 4096, &maps.q, &bar_q, cb * 64, t0,
+                            b * dm.Hq + g * dm.G + hh);
+    };
+    auto load_lag = [&](int t0) {
+        const int ct = t0 / C;
+        const int xrow = ct < dm.T_max ? ct * lam : P.KP;   // past the table: zero fill
+        mbar_expect_tx(&bar_lag, CBF * (4096 + 2048) + CBD * (4096 + 2048));
+        for (int cb = 0; cb < CBF; ++cb) {
+            tma_load_3d(sm + Lay::PHIK + cb * 6144, &maps.phik, &bar_lag, cb * 64, t0 - W, unit);
+            tma_load_3d(sm + Lay::PHIK + cb * 6144 + 4096, &maps.phk16, &bar_lag, cb * 64, xrow, unit);
+        }
+        for (int cb = 0; cb < CBD; ++cb) {
+            tma_load_3d(sm + Lay::VLAG + cb * 6144, &maps.v, &bar_lag, cb * 64, t0 - W, unit);
+            tma_load_3d(sm + Lay::VLAG + cb * 6144 + 4096, &maps.vk16, &bar_lag, cb * 64, xrow, unit);
+        }
+    };
+    if (tid == 0) {
+        tma_prefetch_desc(&maps.q);
+        mbar_expect_tx(&bar_wf, CBD * DF * 128);
+        for (int cb = 0; cb < CBD; ++cb) tma_load_2d(sm + Lay::WF + cb * DF * 128, &maps.wft, &bar_wf, cb * 64, 0);
+        if (ntiles > 0) {
+            load_q(tbeg);
+            load_lag(tbeg);
+        }
+    }
+    fence_async_smem();
+    __syncthreads();
+
+    // barrier phase bookkeeping (thread 0 owns the producer-side ones)
+    uint32_t ph_q = 0, ph_lag = 0, ph_mma = 0;
+    uint32_t ph_kfull[4] = {0, 0, 0, 0}, ph_kfree[4] = {0, 0, 0, 0};
+    uint32_t ph_vfull[2] = {0, 0}, ph_vfree[2] = {0, 0}, ph_pfree[2] = {0, 0};
+    bool wf_ready = false;
+
+    const uint32_t id_u = idesc_bf16(128, DF, 0, 0);
+    const uint32_t id_s = idesc_bf16(128, 32, 0, 0);
+    const uint32_t id_a = idesc_bf16(128, 32 + NX, 0, 0);
+    const uint32_t id_o = idesc_bf16(128, D, 0, 1);
+    const uint32_t id_ds = idesc_bf16(128, D, 1, 1);
+    const float inv_sqrt_d = rsqrtf((float)D);
+
+    auto kdesc = [&](uint32_t base, int k, uint32_t blockbytes) {   // K-major operand, K step k
+        return sdesc(base + (k / 64) * blockbytes + (k % 64) * 2, 16, 1024);
+    };
+    auto wait_all = [&](uint64_t *bar, uint32_t &ph) {
+        if (!mbar_wait(bar, ph, P.status)) s_abort = 1;
+        ph ^= 1;
+    };
+
+    for (int it = 0; it < ntiles; ++it) {
+        const int t0 = tbeg + it * 32;
+        const int ct = t0 / C;
+        const int nkg = min(ct, dm.T_max) * lam;
+        const int ngb = (nkg + 31) / 32;
+        const int nkb = P.nb + ngb;
+        const int npb = (nkb + 1) / 2;
+        const int band_lo = t0 - P.Wr;
+        const bool has_next = it + 1 < ntiles;
+
+        // row identity
+        const int r = tid, hh = r / 32, t = t0 + (r % 32);
+        const bool row_ok = hh < dm.G && t < dm.N;
+
+        // kept positions of this tile (softmax gather list and own-chunk extras)
+        for (int e = tid; e < ngb * 32; e += 128) kpos[e] = e < nkg ? fs[e] : -1;
+        if (tid < NX) xpos[tid] = (ct < dm.T_max && tid < lam) ? fs[ct * lam + tid] : -1;
+
+        // ---------------- S phase: U = Q Wf, S = Q K^T ----------------------------
+        if (tid == 0 && !s_abort) {
+            if (!wf_ready) {
+                uint32_t ph0 = 0;
+                if (!mbar_wait(&bar_wf, ph0, P.status)) s_abort = 1;
+                wf_ready = true;
+            }
+            if (!mbar_wait(&bar_q, ph_q, P.status)) s_abort = 1;
+            ph_q ^= 1;
+            tc_fence_after();
+            for (int k = 0; k < D; k += 16)
+                mma_ss(tmem + TM_O, kdesc(sb + Lay::Q, k, 16384), kdesc(sb + Lay::WF, k, DF * 128), id_u, k > 0);
+            auto issue_k = [&](int kb) {
+                const int slot = kb & 3;
+                uint8_t *dst = sm + Lay::RING + slot * CBD * 4096;
+                mbar_expect_tx(&bar_kfull[slot], CBD * 4096);
+                for (int cb = 0; cb < CBD; ++cb) {
+                    if (kb < P.nb)
+                        tma_load_3d(dst + cb * 4096, &maps.k, &bar_kfull[slot], cb * 64, band_lo + 32 * kb, unit);
+                    else
+                        tma_load_3d(dst + cb * 4096, &maps.kk, &bar_kfull[slot], cb * 64, 32 * (kb - P.nb), unit);
+                }
+            };
+            for (int kb = 0; kb < nkb && kb < 4; ++kb) issue_k(kb);
+            for (int kb = 0; kb < nkb && !s_abort; ++kb) {
+                const int slot = kb & 3;
+                if (!mbar_wait(&bar_kfull[slot], ph_kfull[slot], P.status)) { s_abort = 1; break; }
+                ph_kfull[slot] ^= 1;
+                tc_fence_after();
+                const uint32_t kbase = sb + Lay::RING + slot * CBD * 4096;
+                for (int k = 0; k < D; k += 16)
+                    mma_ss(tmem + TM_S + 32 * kb, kdesc(sb + Lay::Q, k, 16384), kdesc(kbase, k, 4096), id_s, k > 0);
+                if (kb + 4 < nkb) mma_commit(&bar_kfree[slot]);
+                if (kb >= 1 && kb + 3 < nkb) {
+                    const int ps = (kb - 1) & 3;
+                    if (!mbar_wait(&bar_kfree[ps], ph_kfree[ps], P.status)) { s_abort = 1; break; }
+                    ph_kfree[ps] ^= 1;
+                    issue_k(kb + 3);
+                }
+            }
+            mma_commit(&bar_mma);
+        }
+        __syncthreads();
+        if (s_abort) break;
+
+        // ||q|| of this row before the next tile's Q overwrites the buffer
+        float qn = 0.f;
+#pragma unroll
+        for (int cb = 0; cb < CBD; ++cb)
+#pragma unroll
+            for (int c8 = 0; c8 < 8; ++c8) {
+                const uint4 pk = *reinterpret_cast<const uint4 *>(sm + Lay::Q + cb * 16384 + sw128(r, c8));
+                const uint32_t w4[4] = {pk.x, pk.y, pk.z, pk.w};
+#pragma unroll
+                for (int h2 = 0; h2 < 4; ++h2) {
+                    const float a0 = __uint_as_float(w4[h2] << 16), a1 = __uint_as_float(w4[h2] & 0xffff0000u);
+                    qn = fmaf(a0, a0, fmaf(a1, a1, qn));
+                }
+            }
+        qn = sqrtf(qn);
+        wait_all(&bar_mma, ph_mma);                 // U and S are in TMEM; Q and the ring are free
+        tc_fence_after();
+        __syncthreads();
+        if (s_abort) break;
+        if (tid == 0) {
+            if (has_next) load_q(t0 + 32);
+            // the first two V blocks (64 keys each) into the ring
+            for (int p = 0; p < npb && p < 2; ++p) {
+                uint8_t *dst = sm + Lay::RING + p * CBD * 8192;
+                mbar_expect_tx(&bar_vfull[p], CBD * 8192);
+                for (int h = 0; h < 2; ++h) {
+                    const int kb = 2 * p + h;
+                    for (int cb = 0; cb < CBD; ++cb) {
+                        if (kb < P.nb)
+                            tma_load_3d(dst + cb * 8192 + h * 4096, &maps.v, &bar_vfull[p], cb * 64,
+                                        band_lo + 32 * kb, unit);
+                        else
+                            tma_load_3d(dst + cb * 8192 + h * 4096, &maps.vk, &bar_vfull[p], cb * 64,
+                                        32 * (kb - P.nb), unit);
+                    }
+                }
+            }
+            tma_store_wait_read();                  // the previous tile's output left the staging buffer
+        }
+        __syncthreads();
+
+        // ---------------- phi(Q) from U (TMEM cols TM_O) -----------------------------
+        float den = 0.f;
+        {
+            float mx = -INFINITY;
+#pragma unroll
+            for (int c0 = 0; c0 < DF; c0 += 32) {
+                float u[32];
+                tmem_ld32(tlane + TM_O + c0, u);
+                tmem_ld_wait();
+#pragma unroll
+                for (int i = 0; i < 32; ++i) mx = fmaxf(mx, u[i]);
+            }
+            float s2 = 0.f;
+#pragma unroll
+            for (int c0 = 0; c0 < DF; c0 += 32) {
+                float u[32];
+                tmem_ld32(tlane + TM_O + c0, u);
+                tmem_ld_wait();
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const float e = expf(u[i] - mx);
+                    s2 = fmaf(e, e, s2);
+                }
+            }
+            const float sc = qn * rsqrtf(s2);
+#pragma unroll
+            for (int c0 = 0; c0 < DF; c0 += 32) {
+                float u[32];
+                tmem_ld32(tlane + TM_O + c0, u);
+                tmem_ld_wait();
+#pragma unroll
+                for (int c8 = 0; c8 < 4; ++c8) {
+                    uint32_t w4[4];
+#pragma unroll
+                    for (int h2 = 0; h2 < 4; ++h2) {
+                        const int i = c8 * 8 + h2 * 2;
+                        const float p0 = sc * expf(u[i] - mx), p1 = sc * expf(u[i + 1] - mx);
+                        w4[h2] = pack_bf16(p0, p1);
+                        const int f = c0 + i;
+                        den = fmaf(__uint_as_float(w4[h2] << 16), zrun[f], den);
+                        den = fmaf(__uint_as_float(w4[h2] & 0xffff0000u), zrun[f + 1], den);
+                    }
+                    const int f0 = c0 + c8 * 8;
+                    *reinterpret_cast<uint4 *>(sm + Lay::PHIQ + (f0 / 64) * 16384 + sw128(r, (f0 % 64) / 8)) =
+                        make_uint4(w4[0], w4[1], w4[2], w4[3]);
+                }
+            }
+        }
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+
+        // ---------------- A = phi(Q) [phi(K_lag) | phi(K_x)]^T ----------------------
+        if (tid == 0) {
+            if (!mbar_wait(&bar_lag, ph_lag, P.status)) s_abort = 1;
+            ph_lag ^= 1;
+            tc_fence_after();
+            for (int k = 0; k < DF; k += 16)
+                mma_ss(tmem + TM_A, kdesc(sb + Lay::PHIQ, k, 16384), kdesc(sb + Lay::PHIK, k, 6144), id_a, k > 0);
+            mma_commit(&bar_mma);
+        }
+
+        // ---------------- softmax pass 1: exact row maximum --------------------------
+        float cmax = -INFINITY;
+        for (int kb = 0; kb < nkb; ++kb) {
+            float sv[32];
+            tmem_ld32(tlane + TM_S + 32 * kb, sv);
+            tmem_ld_wait();
+            if (row_ok) {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    bool ok;
+                    if (kb < P.nb) {
+                        const int j = band_lo + 32 * kb + i;
+                        ok = j >= 0 && j <= t && j > t - W;
+                    } else {
+                        const int j = kpos[32 * (kb - P.nb) + i];
+                        ok = j >= 0 && j <= t - W;
+                    }
+                    if (ok) cmax = fmaxf(cmax, sv[i] * inv_sqrt_d);
+                }
+            }
+        }
+        const float cm = cmax == -INFINITY ? 0.f : cmax;   // no softmax key: every P is 0
+
+        // ---------------- A: mask, row sum, bf16 into P slot 0 -------------------------
+        wait_all(&bar_mma, ph_mma);
+        tc_fence_after();
+        {
+            float a32[32], a16[16];
+            tmem_ld32(tlane + TM_A, a32);
+            tmem_ld16(tlane + TM_A + 32, a16);
+            tmem_ld_wait();
+            uint32_t w[32];
+#pragma unroll
+            for (int i = 0; i < 64; i += 2) {
+                float x0 = 0.f, x1 = 0.f;
+                if (row_ok) {
+#pragma unroll
+                    for (int h2 = 0; h2 < 2; ++h2) {
+                        const int c = i + h2;
+                        float a = 0.f;
+                        if (c < 32) {
+                            const int j = t0 - W + c;
+                            if (j >= 0 && j <= t - W) a = a32[c];
+                        } else if (c < 32 + NX) {
+                            const int j = xpos[c - 32];
+                            if (j >= 0 && j <= t - W) a = a16[c - 32];
+                        }
+                        if (h2 == 0) x0 = a; else x1 = a;
+                    }
+                }
+                w[i / 2] = pack_bf16(x0, x1);
+                den += __uint_as_float(w[i / 2] << 16) + __uint_as_float(w[i / 2] & 0xffff0000u);
+            }
+#pragma unroll
+            for (int c8 = 0; c8 < 8; ++c8)
+                *reinterpret_cast<uint4 *>(sm + Lay::P + sw128(r, c8)) =
+                    make_uint4(w[c8 * 4], w[c8 * 4 + 1], w[c8 * 4 + 2], w[c8 * 4 + 3]);
+        }
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        if (tid == 0) {
+            tc_fence_after();
+            // O = A V_lagx (initialises O)
+            for (int kk = 0; kk < 32 + NX; kk += 16)
+                mma_ss(tmem + TM_O, kdesc(sb + Lay::P, kk, 16384), sdesc(sb + Lay::VLAG + kk * 128, 6144, 1024), id_o,
+                       kk > 0);
+            if (npb >= 2) mma_commit(&bar_pfree[0]);
+        }
+
+        // ---------------- softmax pass 2 + P V --------------------------------------
+        float lsum = 0.f;
+        for (int p = 0; p < npb; ++p) {
+            const int ps = (p + 1) & 1;
+            if (p >= 1) {                             // slot ps was read by the MMA two blocks back (or by A V)
+                wait_all(&bar_pfree[ps], ph_pfree[ps]);
+            }
+            uint8_t *pdst = sm + Lay::P + ps * 16384;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int kb = 2 * p + h;
+                uint32_t w[16];
+                if (kb < nkb) {
+                    float sv[32];
+                    tmem_ld32(tlane + TM_S + 32 * kb, sv);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 32; i += 2) {
+                        float pr[2];
+#pragma unroll
+                        for (int h2 = 0; h2 < 2; ++h2) {
+                            bool ok = row_ok;
+                            if (kb < P.nb) {
+                                const int j = band_lo + 32 * kb + i + h2;
+                                ok = ok && j >= 0 && j <= t && j > t - W;
+                            } else {
+                                const int j = kpos[32 * (kb - P.nb) + i + h2];
+                                ok = ok && j >= 0 && j <= t - W;
+                            }
+                            pr[h2] = ok ? expf(fmaf(sv[i + h2], inv_sqrt_d, -cm)) : 0.f;
+                        }
+                        w[i / 2] = pack_bf16(pr[0], pr[1]);
+                        lsum += __uint_as_float(w[i / 2] << 16) + __uint_as_float(w[i / 2] & 0xffff0000u);
+                    }
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) w[i] = 0u;
+                }
+#pragma unroll
+                for (int c8 = 0; c8 < 4; ++c8)
+                    *reinterpret_cast<uint4 *>(pdst + sw128(r, h * 4 + c8)) =
+                        make_uint4(w[c8 * 4], w[c8 * 4 + 1], w[c8 * 4 + 2], w[c8 * 4 + 3]);
+            }
+            fence_async_smem();
+            tc_fence_before();
+            __syncthreads();
+            if (s_abort) break;
+            if (tid == 0) {
+                const int vs = p & 1;
+                if (!mbar_wait(&bar_vfull[vs], ph_vfull[vs], P.status)) s_abort = 1;
+                ph_vfull[vs] ^= 1;
+                tc_fence_after();
+                const uint32_t vbase = sb + Lay::RING + vs * CBD * 8192;
+                for (int kk = 0; kk < 64; kk += 16)
+                    mma_ss(tmem + TM_O, kdesc(sb + Lay::P + ps * 16384, kk, 16384), sdesc(vbase + kk * 128, 8192, 1024),
+                           id_o, 1);
+                if (p + 2 < npb) {
+                    mma_commit(&bar_pfree[ps]);
+                    mma_commit(&bar_vfree[vs]);
+                }
+                // refill the V slot of block p-1 with block p+1 once its MMA is done
+                if (p >= 1 && p + 1 < npb && p + 1 >= 2) {
+                    const int os = (p - 1) & 1;
+                    if (!mbar_wait(&bar_vfree[os], ph_vfree[os], P.status)) s_abort = 1;
+                    ph_vfree[os] ^= 1;
+                    const int q2 = p + 1;
+                    uint8_t *dst = sm + Lay::RING + os * CBD * 8192;
+                    mbar_expect_tx(&bar_vfull[os], CBD * 8192);
+                    for (int h = 0; h < 2; ++h) {
+                        const int kb = 2 * q2 + h;
+                        for (int cb = 0; cb < CBD; ++cb) {
+                            if (kb < P.nb)
+                                tma_load_3d(dst + cb * 8192 + h * 4096, &maps.v, &bar_vfull[os], cb * 64,
+                                            band_lo + 32 * kb, unit);
+                            else
+                                tma_load_3d(dst + cb * 8192 + h * 4096, &maps.vk, &bar_vfull[os], cb * 64,
+                                            32 * (kb - P.nb), unit);
+                        }
+                    }
+                }
+            }
+        }
+        if (s_abort) break;
+
+        // ---------------- readout and state update MMAs ------------------------------
+        if (tid == 0) {
+            tc_fence_after();
+            for (int k = 0; k < DF; k += 16)
+                mma_ss(tmem + TM_O, kdesc(sb + Lay::PHIQ, k, 16384), sdesc(sb + Lay::SRUN + k * 128, DF * 128, 1024),
+                       id_o, 1);
+            // dS = phi(K_lag)^T V_lag into the (now free) logit columns
+            for (int kk = 0; kk < 32; kk += 16)
+                mma_ss(tmem + TM_S, sdesc(sb + Lay::PHIK + kk * 128, 6144, 1024),
+                       sdesc(sb + Lay::VLAG + kk * 128, 6144, 1024), id_ds, kk > 0);
+            mma_commit(&bar_mma);
+        }
+        wait_all(&bar_mma, ph_mma);
+        tc_fence_after();
+        if (s_abort) break;
+
+        // ---------------- epilogue: y = O / den ---------------------------------------
+        {
+            den += lsum;
+            const float inv = den != 0.f ? 1.f / den : 0.f;
+#pragma unroll
+            for (int c0 = 0; c0 < D; c0 += 32) {
+                float o[32];
+                tmem_ld32(tlane + TM_O + c0, o);
+                tmem_ld_wait();
+#pragma unroll
+                for (int c8 = 0; c8 < 4; ++c8) {
+                    uint4 pk;
+                    pk.x = pack_bf16(o[c8 * 8 + 0] * inv, o[c8 * 8 + 1] * inv);
+                    pk.y = pack_bf16(o[c8 * 8 + 2] * inv, o[c8 * 8 + 3] * inv);
+                    pk.z = pack_bf16(o[c8 * 8 + 4] * inv, o[c8 * 8 + 5] * inv);
+                    pk.w = pack_bf16(o[c8 * 8 + 6] * inv, o[c8 * 8 + 7] * inv);
+                    const int d0 = c0 + c8 * 8;
+                    *reinterpret_cast<uint4 *>(sm + Lay::PHIQ + (d0 / 64) * 16384 + sw128(r, (d0 % 64) / 8)) = pk;
+                }
+            }
+        }
+        // ---------------- state update: S_run += dS, z_run += sum phi(K_lag) ------------
+        {
+            const int f = tid;
+#pragma unroll
+            for (int c0 = 0; c0 < D; c0 += 32) {
+                float ds[32];
+                tmem_ld32(tlane + TM_S + c0, ds);
+                tmem_ld_wait();
+#pragma unroll
+                for (int i = 0; i < 32; ++i) srun[c0 + i] += ds[i];
+            }
+            if (f < DF) {
+#pragma unroll
+                for (int c8 = 0; c8 < D / 8; ++c8) {
+                    uint4 pk;
+                    pk.x = pack_bf16(srun[c8 * 8 + 0], srun[c8 * 8 + 1]);
+                    pk.y = pack_bf16(srun[c8 * 8 + 2], srun[c8 * 8 + 3]);
+                    pk.z = pack_bf16(srun[c8 * 8 + 4], srun[c8 * 8 + 5]);
+                    pk.w = pack_bf16(srun[c8 * 8 + 6], srun[c8 * 8 + 7]);
+                    *reinterpret_cast<uint4 *>(sm + Lay::SRUN + (c8 / 8) * (DF * 128) + sw128(f, c8 % 8)) = pk;
+                }
+                float za = 0.f;
+                const int cb = f / 64, c8 = (f % 64) / 8, e = f % 8;
+                for (int tok = 0; tok < 32; ++tok) {
+                    const uint16_t x =
+                        *reinterpret_cast<const uint16_t *>(sm + Lay::PHIK + cb * 6144 + sw128(tok, c8) + e * 2);
+                    za += bf2f(x);
+                }
+                zrun[f] += za;
+            }
+        }
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        if (tid == 0) {
+            for (int h2 = 0; h2 < dm.G; ++h2)
+                for (int cb = 0; cb < CBD; ++cb)
+                    tma_store_3d(&maps.out, sm + Lay::PHIQ + cb * 16384 + h2 * 4096, cb * 64, t0,
+                                 b * dm.Hq + g * dm.G + h2);
+            tma_store_commit();
+            if (has_next) load_lag(t0 + 32);
+        }
+    }
+
+    if (tid == 0) tma_store_wait_all();
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, TM_COLS);
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+bool hybrid_tc_supported(const Dims &dm)
+{
+    if (dm.d != dm.df) return false;
+    if (dm.G != 1 && dm.G != 2 && dm.G != 4) return false;
+    if (dm.C % 32 != 0 || dm.lam > NX) return false;
+    const int Wr = dm.W >= 1 ? (dm.W - 1 + 31) / 32 * 32 : 0;
+    const int nb = (Wr + 32) / 32;
+    const int nchunks = (dm.N + dm.C - 1) / dm.C;
+    const int maxg = dm.lam * min(dm.T_max, max(nchunks - 1, 0));
+    return nb + (maxg + 31) / 32 <= MAX_KEY_BLOCKS;
+}
+
+size_t hybrid_tc_smem(const Dims &dm)
+{
+    return (dm.d == 64 ? TCLayout<64, 64>::TOTAL : TCLayout<128, 128>::TOTAL) + 1024;
+}
+
+cudaError_t launch_hybrid_tc(const Dims &dm, const SegPlan &sp, const TCBuffers &bf, const int32_t *fsel,
+                             const float *dS, const float *dz, int32_t *status, cudaStream_t s)
+{
+    KTimer tm("hybrid_attn", s);
+    const int D = dm.d, DF = dm.df;
+    const uint64_t units = (uint64_t)dm.B * dm.Hkv, heads = (uint64_t)dm.B * dm.Hq;
+    const int KP = dm.T_max * dm.lam > 0 ? dm.T_max * dm.lam : 1;
+    TCMaps m;
+    bool ok = true;
+    {
+        uint64_t dq[3] = {(uint64_t)D, (uint64_t)dm.N, heads}, sq[2] = {(uint64_t)D * 2, (uint64_t)D * 2 * dm.N};
+        uint32_t box[3] = {64, 32, 1};
+        ok &= make_tma_map(&m.q, bf.q, 3, dq, sq, box, true);
+        ok &= make_tma_map(&m.out, bf.out, 3, dq, sq, box, true);
+        uint64_t dk[3] = {(uint64_t)D, (uint64_t)dm.N, units};
+        ok &= make_tma_map(&m.k, bf.k, 3, dk, sq, box, true);
+        ok &= make_tma_map(&m.v, bf.v, 3, dk, sq, box, true);
+        uint64_t df3[3] = {(uint64_t)DF, (uint64_t)dm.N, units}, sf[2] = {(uint64_t)DF * 2, (uint64_t)DF * 2 * dm.N};
+        ok &= make_tma_map(&m.phik, bf.phik, 3, df3, sf, box, true);
+        uint64_t dkp[3] = {(uint64_t)D, (uint64_t)KP, units}, skp[2] = {(uint64_t)D * 2, (uint64_t)D * 2 * KP};
+        ok &= make_tma_map(&m.kk, bf.kk, 3, dkp, skp, box, true);
+        ok &= make_tma_map(&m.vk, bf.vk, 3, dkp, skp, box, true);
+        uint32_t box16[3] = {64, 16, 1};
+        ok &= make_tma_map(&m.vk16, bf.vk, 3, dkp, skp, box16, true);
+        uint64_t dpk[3] = {(uint64_t)DF, (uint64_t)KP, units}, spk[2] = {(uint64_t)DF * 2, (uint64_t)DF * 2 * KP};
+        ok &= make_tma_map(&m.phk16, bf.phk, 3, dpk, spk, box16, true);
+        uint64_t dw[2] = {(uint64_t)D, (uint64_t)DF}, sw[1] = {(uint64_t)D * 2};
+        uint32_t boxw[2] = {64, (uint32_t)DF};
+        ok &= make_tma_map(&m.wft, bf.wft, 2, dw, sw, boxw, true);
+    }
+    if (!ok) return cudaErrorInvalidValue;
+    TCParams p;
+    p.dm = dm;
+    p.sp = sp;
+    p.Wr = dm.W >= 1 ? (dm.W - 1 + 31) / 32 * 32 : 0;
+    p.nb = (p.Wr + 32) / 32;
+    p.KP = KP;
+    p.fsel = fsel;
+    p.dS = dS;
+    p.dz = dz;
+    p.status = status;
+    dim3 grid(sp.nseg, dm.Hkv, dm.B);
+    const size_t smem = hybrid_tc_smem(dm);
+    cudaError_t e;
+    if (D == 64) {
+        e = cudaFuncSetAttribute(hybrid_tc_kernel<64, 64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        hybrid_tc_kernel<64, 64><<<grid, 128, smem, s>>>(m, p);
+    } else {
+        e = cudaFuncSetAttribute(hybrid_tc_kernel<128, 128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        hybrid_tc_kernel<128, 128><<<grid, 128, smem, s>>>(m, p);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace still

@@ -2,36 +2,29 @@
 //
 // "STILL: Content-Aware Intra-Layer Hybrid Attention for Efficient LLM
 // Linearization", section "Content-Aware Routing with Fixed Budget": tokens
-// that are not kept are accumulated into the linear-attention recurrent state;
-// section "NP-Map: Norm-Preserving Feature Map" gives the feature map phi.
+// that are not kept are accumulated into the linear-attention recurrent state.
 //
 // Segment s of a (sequence, kv head) owns the keys that leave the window
 // while its query tiles run: [s*L - W, (s+1)*L - W) clipped to [0, N - W).
 // This kernel forms, per segment, dS_s = sum phi(k_j) v_j^T and dz_s =
-// sum phi(k_j) over those keys, leaving out every key that sits in a budget
-// slot (kept by a finished chunk, or in the running top-lambda of the
-// unfinished tail chunk).  It also stores phi(k_j) for the attention kernel.
-// An exclusive scan over segments then gives the state each segment starts
-// from, and slot nseg the state after all N tokens.
+// sum phi(k_j) over those keys from the feature table (whose rows of slotted
+// keys are zero).  An exclusive scan over segments then gives the state each
+// segment starts from, and slot nseg the state after all N tokens.
 #include "common.cuh"
 
 namespace still {
 
 template <int D, int DF>
-__global__ void __launch_bounds__(256) linstate_kernel(const uint16_t *__restrict__ k,
-                                                       const uint16_t *__restrict__ v,
-                                                       const float *__restrict__ Wf,
-                                                       const uint8_t *__restrict__ flag, Dims dm, SegPlan sp,
-                                                       float *__restrict__ phik, float *__restrict__ dS,
-                                                       float *__restrict__ dz)
+__global__ void __launch_bounds__(256) linstate_kernel(const uint16_t *__restrict__ phik,
+                                                       const uint16_t *__restrict__ v, Dims dm, SegPlan sp,
+                                                       float *__restrict__ dS, float *__restrict__ dz)
 {
     constexpr int PER = DF * D / 256;   // state elements per thread
     constexpr int RSTEP = 256 / D;      // state rows between a thread's elements
-    __shared__ float xs[8][D];
     __shared__ float ph[32][DF];
     __shared__ float vs[32][D];
     const int s = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int tid = threadIdx.x;
     const size_t ug = (size_t)b * dm.Hkv + g;
     const int lo = max(0, s * sp.L - dm.W);
     const int hi = min((s + 1) * sp.L, dm.N) - dm.W;
@@ -42,23 +35,8 @@ __global__ void __launch_bounds__(256) linstate_kernel(const uint16_t *__restric
     float zacc = 0.f;
     for (int kb = lo; kb < hi; kb += 32) {
         const int nk = min(32, hi - kb);
-        for (int kk = warp; kk < nk; kk += 8) {
-            const int j = kb + kk;
-            const uint16_t *kr = k + (ug * dm.N + j) * D;
-            const uint16_t *vr = v + (ug * dm.N + j) * D;
-            __syncwarp();
-            for (int e = lane; e < D; e += 32) {
-                xs[warp][e] = bf2f(kr[e]);
-                vs[kk][e] = bf2f(vr[e]);
-            }
-            __syncwarp();
-            warp_npmap<D, DF>(xs[warp], Wf, ph[kk], lane);
-            __syncwarp();
-            for (int e = lane; e < DF; e += 32) {
-                phik[(ug * dm.N + j) * DF + e] = ph[kk][e];
-                if (flag[ug * dm.N + j]) ph[kk][e] = 0.f;
-            }
-        }
+        for (int e = tid; e < nk * DF; e += 256) ph[e / DF][e % DF] = bf2f(phik[(ug * dm.N + kb) * DF + e]);
+        for (int e = tid; e < nk * D; e += 256) vs[e / D][e % D] = bf2f(v[(ug * dm.N + kb) * D + e]);
         __syncthreads();
         for (int kk = 0; kk < nk; ++kk) {
             const float vv = vs[kk][col];
@@ -100,17 +78,16 @@ __global__ void scan_kernel(float *__restrict__ dS, float *__restrict__ dz, int 
     p[nseg * stride] = run;
 }
 
-cudaError_t launch_linstate(const Dims &dm, const SegPlan &sp, const uint16_t *k, const uint16_t *v,
-                            const float *Wf, const uint8_t *flag, float *phik, float *dS, float *dz,
-                            cudaStream_t s)
+cudaError_t launch_linstate(const Dims &dm, const SegPlan &sp, const uint16_t *phik, const uint16_t *v, float *dS,
+                            float *dz, cudaStream_t s)
 {
     {
         KTimer tm("linstate", s);
         dim3 grid(sp.nseg, dm.Hkv, dm.B);
-        if (dm.d == 64 && dm.df == 64) linstate_kernel<64, 64><<<grid, 256, 0, s>>>(k, v, Wf, flag, dm, sp, phik, dS, dz);
-        else if (dm.d == 64) linstate_kernel<64, 128><<<grid, 256, 0, s>>>(k, v, Wf, flag, dm, sp, phik, dS, dz);
-        else if (dm.df == 64) linstate_kernel<128, 64><<<grid, 256, 0, s>>>(k, v, Wf, flag, dm, sp, phik, dS, dz);
-        else linstate_kernel<128, 128><<<grid, 256, 0, s>>>(k, v, Wf, flag, dm, sp, phik, dS, dz);
+        if (dm.d == 64 && dm.df == 64) linstate_kernel<64, 64><<<grid, 256, 0, s>>>(phik, v, dm, sp, dS, dz);
+        else if (dm.d == 64) linstate_kernel<64, 128><<<grid, 256, 0, s>>>(phik, v, dm, sp, dS, dz);
+        else if (dm.df == 64) linstate_kernel<128, 64><<<grid, 256, 0, s>>>(phik, v, dm, sp, dS, dz);
+        else linstate_kernel<128, 128><<<grid, 256, 0, s>>>(phik, v, dm, sp, dS, dz);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }

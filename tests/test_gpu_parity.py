@@ -16,6 +16,7 @@ from oracle import brute, ref
 pytestmark = pytest.mark.gpu
 
 OUT_TOL = 1e-2
+STATE_TOL = 1e-2   # exported (S, z): bf16 features, see compare_state
 DEV = "cuda"
 
 
@@ -221,9 +222,12 @@ def compare_state(st, st_ref, w):
                     continue
                 rs = int(np.flatnonzero(st_ref.pos[b, g] == p)[0])
                 np.testing.assert_array_equal(K[b, g, sl], st_ref.K[b, g, rs])
+            # The prefill sums the linear state from bf16 NP-Map features (the
+            # tensor-core operand precision, relative rounding 2^-9 per feature,
+            # fp32 accumulation); the decode step uses fp32 features.
             sc = max(np.abs(st_ref.S[b, g]).max(), 1e-30)
-            assert np.abs(S[b, g] - st_ref.S[b, g]).max() <= 1e-4 * sc
-            assert np.abs(z[b, g] - st_ref.z[b, g]).max() <= 1e-4 * max(np.abs(st_ref.z[b, g]).max(), 1e-30)
+            assert np.abs(S[b, g] - st_ref.S[b, g]).max() <= STATE_TOL * sc
+            assert np.abs(z[b, g] - st_ref.z[b, g]).max() <= STATE_TOL * max(np.abs(st_ref.z[b, g]).max(), 1e-30)
     assert (st.t.cpu().numpy() == st_ref.t[:, None]).all()
 
 
