@@ -25,7 +25,8 @@
  *     kernel (an index out of range) are written to a device status word
  *     (see still_read_status) and never trap.
  *   - Device pointers must be 16-byte aligned.  The caller owns all memory;
- *     the library keeps no device allocation between calls.
+ *     the library keeps no device allocation between calls, apart from the
+ *     fixed scratch array of still_prefill_noalloc.
  *   - Supported: d in {64, 128}, d_f in {64, 128}, 1 <= C <= 16384, W >= 0,
  *     m >= W, T_max >= 1, W >= 1 whenever lambda > 0.  N == 0 is a no-op.
  */
@@ -153,6 +154,31 @@ still_status still_prefill(const still_shape *shape, const still_bf16 *q, const 
                            const still_bf16 *v, const float *Wf, int W, int C, int m, int T_max,
                            still_bf16 *out, int32_t *sel_idx, void *workspace, size_t workspace_bytes,
                            const still_decode_state *export_state, still_stream_t stream);
+
+/*
+ * The prefill above with its scratch memory taken from a fixed array inside
+ * the library instead of a workspace argument.  The pages have no counterpart:
+ * this entry point exists for callers that may not allocate device memory
+ * while they run (an engine plug-in whose execution step must not allocate,
+ * latency-critical code that cannot risk an allocation's synchronisation or
+ * out-of-memory failure).  Inputs, outputs and the optional export state are
+ * the caller's, exactly as for still_prefill.
+ *   - The array holds still_prefill_noalloc_max_bytes() = 16 MiB; sizes whose
+ *     still_prefill_workspace_size() exceeds it return STILL_ERR_WORKSPACE
+ *     (and print why) without launching anything.
+ *   - The call allocates and frees nothing.  The first call on a device looks
+ *     up the array's device address (cudaGetSymbolAddress); make that first
+ *     call before capturing a stream into a CUDA graph.
+ *   - Every GPU that loads the library keeps the array until the process
+ *     exits.  All calls on one GPU share it: calls that may overlap on the GPU
+ *     (different streams without ordering between them) race on it and must
+ *     not be issued.  Each call clears what has to start at zero itself.
+ */
+size_t still_prefill_noalloc_max_bytes(void);
+still_status still_prefill_noalloc(const still_shape *shape, const still_bf16 *q, const still_bf16 *k,
+                                   const still_bf16 *v, const float *Wf, int W, int C, int m, int T_max,
+                                   still_bf16 *out, int32_t *sel_idx, const still_decode_state *export_state,
+                                   still_stream_t stream);
 
 /* Reset a decode state to "no token absorbed" (shape->N is ignored). */
 still_status still_decode_state_init(const still_shape *shape, const still_decode_state *state, int W, int C,

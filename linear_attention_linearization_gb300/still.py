@@ -56,6 +56,10 @@ SIGNATURES = {
     "still_prefill": (ct.c_int, [ct.POINTER(Shape), ct.c_void_p, ct.c_void_p, ct.c_void_p, ct.c_void_p,
                                  ct.c_int, ct.c_int, ct.c_int, ct.c_int, ct.c_void_p, ct.c_void_p,
                                  ct.c_void_p, ct.c_size_t, ct.POINTER(DecodeStateC), ct.c_void_p]),
+    "still_prefill_noalloc_max_bytes": (ct.c_size_t, []),
+    "still_prefill_noalloc": (ct.c_int, [ct.POINTER(Shape), ct.c_void_p, ct.c_void_p, ct.c_void_p, ct.c_void_p,
+                                         ct.c_int, ct.c_int, ct.c_int, ct.c_int, ct.c_void_p, ct.c_void_p,
+                                         ct.POINTER(DecodeStateC), ct.c_void_p]),
     "still_decode_state_init": (ct.c_int, [ct.POINTER(Shape), ct.POINTER(DecodeStateC), ct.c_int, ct.c_int,
                                            ct.c_int, ct.c_int, ct.c_void_p]),
     "still_decode_step": (ct.c_int, [ct.POINTER(Shape), ct.POINTER(DecodeStateC), ct.c_void_p, ct.c_void_p,
@@ -207,6 +211,26 @@ def prefill(q, k, v, Wf, W, C, m, T_max, out=None, sel_idx=None, workspace=None,
                                _ptr(out, torch.bfloat16, "out"),
                                _ptr(sel_idx, torch.int32, "sel_idx") if sel_idx.numel() else None,
                                ws_ptr, ws_bytes, st, _stream(stream)), "still_prefill")
+    return out, sel_idx
+
+
+def prefill_noalloc(q, k, v, Wf, W, C, m, T_max, out=None, sel_idx=None, export_state=None, stream=None):
+    """still_prefill with the library's fixed scratch array instead of a workspace
+    (for callers that may not allocate device memory); raises StillError when the
+    size needs more scratch than the array holds."""
+    B, Hq, N, d = q.shape
+    lam = lam_of(W, m, T_max)
+    sh = shape_of(q, k, Wf)
+    if out is None:
+        out = torch.empty_like(q)
+    if sel_idx is None:
+        sel_idx = torch.empty((B, k.shape[1], T_max, max(lam, 0)), dtype=torch.int32, device=q.device)
+    st = ct.byref(export_state.c_struct()) if export_state is not None else None
+    _check(lib().still_prefill_noalloc(ct.byref(sh), _ptr(q, torch.bfloat16, "q"), _ptr(k, torch.bfloat16, "k"),
+                                       _ptr(v, torch.bfloat16, "v"), _ptr(Wf, torch.float32, "Wf"), W, C, m, T_max,
+                                       _ptr(out, torch.bfloat16, "out"),
+                                       _ptr(sel_idx, torch.int32, "sel_idx") if sel_idx.numel() else None,
+                                       st, _stream(stream)), "still_prefill_noalloc")
     return out, sel_idx
 
 
