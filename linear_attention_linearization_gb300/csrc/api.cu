@@ -193,6 +193,7 @@ still_status still_score(const still_shape *shape, const still_bf16 *q, const st
     Dims dm;
     st = make_dims(shape, W, 1, W, 1, &dm);
     if (st != STILL_OK) return st;
+    if (score_tc_supported(dm)) return cuda_status(launch_score_tc(dm, q, k, scores, (cudaStream_t)stream));
     return cuda_status(launch_score(dm, q, k, scores, (cudaStream_t)stream));
 }
 
@@ -272,7 +273,8 @@ still_status still_prefill(const still_shape *shape, const still_bf16 *q, const 
     cudaError_t e = cudaMemsetAsync(base, 0, L.status + 256, s);
     if (e == cudaSuccess) e = cudaMemsetAsync(flag, 0, (size_t)dm.B * dm.Hkv * dm.N, s);
     if (e == cudaSuccess) e = cudaMemsetAsync(kk, 0, L.kept_bytes, s);
-    if (e == cudaSuccess && dm.lam > 0) e = launch_score(dm, q, k, scores, s);
+    if (e == cudaSuccess && dm.lam > 0)
+        e = score_tc_supported(dm) ? launch_score_tc(dm, q, k, scores, s) : launch_score(dm, q, k, scores, s);
     if (e == cudaSuccess && dm.lam > 0) e = launch_select(dm, scores, sel_idx, fsel, flag, s);
     if (e == cudaSuccess) e = launch_features(dm, k, v, Wf, flag, fsel, phik, kk, vk, phk, tc ? wft : nullptr, s);
     if (e == cudaSuccess) e = launch_linstate(dm, sp, phik, v, dS, dz, s);

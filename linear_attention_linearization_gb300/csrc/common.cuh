@@ -137,6 +137,8 @@ struct KTimer {
 
 // ---- launchers (one per kernel family) ----------------------------------------
 cudaError_t launch_score(const Dims &dm, const uint16_t *q, const uint16_t *k, float *scores, cudaStream_t s);
+bool score_tc_supported(const Dims &dm);
+cudaError_t launch_score_tc(const Dims &dm, const uint16_t *q, const uint16_t *k, float *scores, cudaStream_t s);
 cudaError_t launch_select(const Dims &dm, const float *scores, int32_t *sel_idx, int32_t *fsel, uint8_t *flag,
                           cudaStream_t s);
 cudaError_t launch_npmap(const uint16_t *x, long long rows, int d, const float *Wf, int df, float *phi,

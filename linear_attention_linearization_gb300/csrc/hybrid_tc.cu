@@ -24,7 +24,10 @@
 //   dS  = phi(K_lag)^T V_lag -> S_run += dS (fp32 in registers, bf16 copy in smem)
 //   y   = O / (sum P + sum A + phi(Q).z_run)                              (TMA store)
 // Masks (window, causal lag, chunk of the kept tokens) are applied to the
-// logits in TMEM by the row threads; one thread issues every TMA and MMA.
+// logits in TMEM by the row threads -- two warps per TMEM lane quarter, each
+// owning half of a row's columns -- and one thread issues every TMA and MMA.
+#include <climits>
+
 #include "sm100.cuh"
 #include "tma_host.cuh"
 
@@ -70,10 +73,12 @@ struct TCLayout {
 };
 
 template <int D, int DF>
-__global__ void __launch_bounds__(128, 1) hybrid_tc_kernel(const __grid_constant__ TCMaps maps, TCParams P)
+__global__ void __launch_bounds__(256, 1) hybrid_tc_kernel(const __grid_constant__ TCMaps maps, TCParams P)
 {
     using Lay = TCLayout<D, DF>;
     constexpr int CBD = Lay::CBD, CBF = Lay::CBF;
+    constexpr int DH = D / 2, DFH = DF / 2;   // columns per half-row thread
+    constexpr float LOG2E = 1.4426950408889634f;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     const uint32_t sb = smem_u32(sm);
@@ -85,15 +90,19 @@ __global__ void __launch_bounds__(128, 1) hybrid_tc_kernel(const __grid_constant
         bar_pfree[2];
     __shared__ uint32_t tmem_base;
     __shared__ int s_abort;
+    __shared__ float xch[2][128][4];
 
     const Dims &dm = P.dm;
-    const int tid = threadIdx.x, warp = tid >> 5;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int quarter = warp & 3, half = warp >> 2;
+    const int r = quarter * 32 + lane;            // the tile row (and state row) this thread serves
     const int s = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
     const int unit = b * dm.Hkv + g;
     const int W = dm.W, C = dm.C, lam = dm.lam;
     const int tbeg = s * P.sp.L, tend = min((s + 1) * P.sp.L, dm.N);
     const int ntiles = (tend - tbeg + 31) / 32;
     const int32_t *fs = P.fsel + (size_t)unit * P.KP;
+    const float l2s = LOG2E * rsqrtf((float)D);
 
     if (warp == 0) {
         tmem_alloc(&tmem_base, TM_COLS);
@@ -110,7 +119,7 @@ __global__ void __launch_bounds__(128, 1) hybrid_tc_kernel(const __grid_constant
         s_abort = 0;
     }
     // padding rows of absent heads stay zero for the whole kernel
-    for (int i = tid; i < CBD * 16384 / 16; i += 128) {
+    for (int i = tid; i < CBD * 16384 / 16; i += 256) {
         const int row = (i * 16 % 16384) / 128;
         if (row >= dm.G * 32) reinterpret_cast<uint4 *>(sm + Lay::Q)[i] = make_uint4(0, 0, 0, 0);
     }
@@ -118,30 +127,31 @@ __global__ void __launch_bounds__(128, 1) hybrid_tc_kernel(const __grid_constant
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = tmem_base;
-    const uint32_t tlane = tmem + ((uint32_t)(warp * 32) << 16);   // this warp's TMEM lanes
+    const uint32_t tlane = tmem + ((uint32_t)(quarter * 32) << 16);   // this warp's TMEM lanes
 
-    // ---- running linear state: thread f holds row f of S_run in fp32 ------------
-    float srun[D];
+    // ---- running linear state: row f = r, columns [half*DH, half*DH + DH) in fp32
+    float srun[DH];
     {
         const float *S0 = P.dS + ((size_t)unit * (P.sp.nseg + 1) + s) * (size_t)(DF * D);
-        const int f = tid;
+        const int f = r;
 #pragma unroll
-        for (int c = 0; c < D; ++c) srun[c] = f < DF ? S0[(size_t)f * D + c] : 0.f;
-        if (f < DF) zrun[f] = P.dz[((size_t)unit * (P.sp.nseg + 1) + s) * DF + f];
+        for (int c = 0; c < DH; ++c) srun[c] = f < DF ? S0[(size_t)f * D + half * DH + c] : 0.f;
+        if (f < DF && half == 0) zrun[f] = P.dz[((size_t)unit * (P.sp.nseg + 1) + s) * DF + f];
         if (f < DF) {
 #pragma unroll
-            for (int c8 = 0; c8 < D / 8; ++c8) {
+            for (int c8 = 0; c8 < DH / 8; ++c8) {
+                const int c = half * DH + c8 * 8;
                 uint4 pk;
                 pk.x = pack_bf16(srun[c8 * 8 + 0], srun[c8 * 8 + 1]);
                 pk.y = pack_bf16(srun[c8 * 8 + 2], srun[c8 * 8 + 3]);
                 pk.z = pack_bf16(srun[c8 * 8 + 4], srun[c8 * 8 + 5]);
                 pk.w = pack_bf16(srun[c8 * 8 + 6], srun[c8 * 8 + 7]);
-                *reinterpret_cast<uint4 *>(sm + Lay::SRUN + (c8 / 8) * (DF * 128) + sw128(f, c8 % 8)) = pk;
+                *reinterpret_cast<uint4 *>(sm + Lay::SRUN + (c / 64) * (DF * 128) + sw128(f, (c % 64) / 8)) = pk;
             }
         }
     }
 
-    // ---- loads of the first tile ------------------------------------------------
+    // ---- loads --------------------------------------------------------------------
     auto load_q = [&](int t0) {
         mbar_expect_tx(&bar_q, dm.G * CBD * 4096);
         for (int hh = 0; hh < dm.G; ++hh)
@@ -162,6 +172,21 @@ __global__ void __launch_bounds__(128, 1) hybrid_tc_kernel(const __grid_constant
             tma_load_3d(sm + Lay::VLAG + cb * 6144 + 4096, &maps.vk16, &bar_lag, cb * 64, xrow, unit);
         }
     };
+    auto load_v = [&](int p, int nkb, int band_lo) {   // V block p (64 keys) into V slot p & 1
+        const int vs = p & 1;
+        uint8_t *dst = sm + Lay::RING + vs * CBD * 8192;
+        mbar_expect_tx(&bar_vfull[vs], CBD * 8192);
+        for (int h = 0; h < 2; ++h) {
+            const int kb = 2 * p + h;
+            for (int cb = 0; cb < CBD; ++cb) {
+                if (kb < P.nb)
+                    tma_load_3d(dst + cb * 8192 + h * 4096, &maps.v, &bar_vfull[vs], cb * 64, band_lo + 32 * kb, unit);
+                else
+                    tma_load_3d(dst + cb * 8192 + h * 4096, &maps.vk, &bar_vfull[vs], cb * 64, 32 * (kb - P.nb), unit);
+            }
+        }
+        (void)nkb;
+    };
     if (tid == 0) {
         tma_prefetch_desc(&maps.q);
         mbar_expect_tx(&bar_wf, CBD * DF * 128);
@@ -174,7 +199,6 @@ __global__ void __launch_bounds__(128, 1) hybrid_tc_kernel(const __grid_constant
     fence_async_smem();
     __syncthreads();
 
-    // barrier phase bookkeeping (thread 0 owns the producer-side ones)
     uint32_t ph_q = 0, ph_lag = 0, ph_mma = 0;
     uint32_t ph_kfull[4] = {0, 0, 0, 0}, ph_kfree[4] = {0, 0, 0, 0};
     uint32_t ph_vfull[2] = {0, 0}, ph_vfree[2] = {0, 0}, ph_pfree[2] = {0, 0};
@@ -185,7 +209,6 @@ __global__ void __launch_bounds__(128, 1) hybrid_tc_kernel(const __grid_constant
     const uint32_t id_a = idesc_bf16(128, 32 + NX, 0, 0);
     const uint32_t id_o = idesc_bf16(128, D, 0, 1);
     const uint32_t id_ds = idesc_bf16(128, D, 1, 1);
-    const float inv_sqrt_d = rsqrtf((float)D);
 
     auto kdesc = [&](uint32_t base, int k, uint32_t blockbytes) {   // K-major operand, K step k
         return sdesc(base + (k / 64) * blockbytes + (k % 64) * 2, 16, 1024);
@@ -205,13 +228,15 @@ __global__ void __launch_bounds__(128, 1) hybrid_tc_kernel(const __grid_constant
         const int band_lo = t0 - P.Wr;
         const bool has_next = it + 1 < ntiles;
 
-        // row identity
-        const int r = tid, hh = r / 32, t = t0 + (r % 32);
+        // row identity and its column ranges
+        const int hh = r / 32, t = t0 + (r % 32);
         const bool row_ok = hh < dm.G && t < dm.N;
+        // softmax band columns [blo, bhi]; lag columns [llo, lhi] of A
+        const int blo = row_ok ? max(t - W + 1, 0) - band_lo : 1, bhi = row_ok ? t - band_lo : 0;
+        const int llo = max(0, W - t0), lhi = row_ok ? t - t0 : -1;
 
-        // kept positions of this tile (softmax gather list and own-chunk extras)
-        for (int e = tid; e < ngb * 32; e += 128) kpos[e] = e < nkg ? fs[e] : -1;
-        if (tid < NX) xpos[tid] = (ct < dm.T_max && tid < lam) ? fs[ct * lam + tid] : -1;
+        for (int e = tid; e < ngb * 32; e += 256) kpos[e] = e < nkg ? fs[e] : INT_MAX;
+        if (tid < NX) xpos[tid] = (ct < dm.T_max && tid < lam) ? fs[ct * lam + tid] : INT_MAX;
 
         // ---------------- S phase: U = Q Wf, S = Q K^T ----------------------------
         if (tid == 0 && !s_abort) {
@@ -237,7 +262,7 @@ __global__ void __launch_bounds__(128, 1) hybrid_tc_kernel(const __grid_constant
                 }
             };
             for (int kb = 0; kb < nkb && kb < 4; ++kb) issue_k(kb);
-            for (int kb = 0; kb < nkb && !s_abort; ++kb) {
+            for (int kb = 0; kb < nkb; ++kb) {
                 const int slot = kb & 3;
                 if (!mbar_wait(&bar_kfull[slot], ph_kfull[slot], P.status)) { s_abort = 1; break; }
                 ph_kfull[slot] ^= 1;
@@ -257,91 +282,96 @@ __global__ void __launch_bounds__(128, 1) hybrid_tc_kernel(const __grid_constant
         }
         __syncthreads();
         if (s_abort) break;
-
-        // ||q|| of this row before the next tile's Q overwrites the buffer
-        float qn = 0.f;
-#pragma unroll
-        for (int cb = 0; cb < CBD; ++cb)
-#pragma unroll
-            for (int c8 = 0; c8 < 8; ++c8) {
-                const uint4 pk = *reinterpret_cast<const uint4 *>(sm + Lay::Q + cb * 16384 + sw128(r, c8));
-                const uint32_t w4[4] = {pk.x, pk.y, pk.z, pk.w};
-#pragma unroll
-                for (int h2 = 0; h2 < 4; ++h2) {
-                    const float a0 = __uint_as_float(w4[h2] << 16), a1 = __uint_as_float(w4[h2] & 0xffff0000u);
-                    qn = fmaf(a0, a0, fmaf(a1, a1, qn));
-                }
+        // number of kept keys (ascending table) at or before t - W, own-chunk extras likewise
+        int nvk = 0, nvx = 0;
+        {
+            int lo = 0, hi = nkg;
+            while (lo < hi) {
+                const int mid = (lo + hi) >> 1;
+                if (kpos[mid] <= t - W) lo = mid + 1; else hi = mid;
             }
-        qn = sqrtf(qn);
+            nvk = row_ok ? lo : 0;
+            while (nvx < NX && xpos[nvx] <= t - W) ++nvx;
+            if (!row_ok) nvx = 0;
+        }
+
+        // ||q||^2 over this thread's half of the row (before the next Q overwrites it)
+        float qn2 = 0.f;
+#pragma unroll
+        for (int c8 = 0; c8 < DH / 8; ++c8) {
+            const int c = half * DH + c8 * 8;
+            const uint4 pk = *reinterpret_cast<const uint4 *>(sm + Lay::Q + (c / 64) * 16384 + sw128(r, (c % 64) / 8));
+            const uint32_t w4[4] = {pk.x, pk.y, pk.z, pk.w};
+#pragma unroll
+            for (int h2 = 0; h2 < 4; ++h2) {
+                const float a0 = __uint_as_float(w4[h2] << 16), a1 = __uint_as_float(w4[h2] & 0xffff0000u);
+                qn2 = fmaf(a0, a0, fmaf(a1, a1, qn2));
+            }
+        }
         wait_all(&bar_mma, ph_mma);                 // U and S are in TMEM; Q and the ring are free
         tc_fence_after();
+
+        // ---------------- phi(Q), pass 1: max and sum of u^2 over my features -------
+        {
+            float mu = -INFINITY, s2 = 0.f;
+#pragma unroll
+            for (int c0 = 0; c0 < DFH; c0 += 16) {
+                float u[16];
+                tmem_ld16(tlane + TM_O + half * DFH + c0, u);
+                tmem_ld_wait();
+                float bm = -INFINITY;
+#pragma unroll
+                for (int i = 0; i < 16; ++i) bm = fmaxf(bm, u[i] * LOG2E);
+                if (bm > mu) {
+                    s2 *= exp2f(2.f * (mu - bm));
+                    mu = bm;
+                }
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const float e = exp2f(fmaf(u[i], LOG2E, -mu));
+                    s2 = fmaf(e, e, s2);
+                }
+            }
+            xch[half][r][0] = mu;
+            xch[half][r][1] = s2;
+            xch[half][r][2] = qn2;
+        }
         __syncthreads();
         if (s_abort) break;
         if (tid == 0) {
             if (has_next) load_q(t0 + 32);
-            // the first two V blocks (64 keys each) into the ring
-            for (int p = 0; p < npb && p < 2; ++p) {
-                uint8_t *dst = sm + Lay::RING + p * CBD * 8192;
-                mbar_expect_tx(&bar_vfull[p], CBD * 8192);
-                for (int h = 0; h < 2; ++h) {
-                    const int kb = 2 * p + h;
-                    for (int cb = 0; cb < CBD; ++cb) {
-                        if (kb < P.nb)
-                            tma_load_3d(dst + cb * 8192 + h * 4096, &maps.v, &bar_vfull[p], cb * 64,
-                                        band_lo + 32 * kb, unit);
-                        else
-                            tma_load_3d(dst + cb * 8192 + h * 4096, &maps.vk, &bar_vfull[p], cb * 64,
-                                        32 * (kb - P.nb), unit);
-                    }
-                }
-            }
+            for (int p = 0; p < npb && p < 2; ++p) load_v(p, nkb, band_lo);
             tma_store_wait_read();                  // the previous tile's output left the staging buffer
         }
         __syncthreads();
 
-        // ---------------- phi(Q) from U (TMEM cols TM_O) -----------------------------
+        // ---------------- phi(Q), pass 2: write my half of phi, phi . z ---------------
         float den = 0.f;
         {
-            float mx = -INFINITY;
-#pragma unroll
-            for (int c0 = 0; c0 < DF; c0 += 32) {
-                float u[32];
-                tmem_ld32(tlane + TM_O + c0, u);
-                tmem_ld_wait();
-#pragma unroll
-                for (int i = 0; i < 32; ++i) mx = fmaxf(mx, u[i]);
-            }
-            float s2 = 0.f;
-#pragma unroll
-            for (int c0 = 0; c0 < DF; c0 += 32) {
-                float u[32];
-                tmem_ld32(tlane + TM_O + c0, u);
-                tmem_ld_wait();
-#pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const float e = expf(u[i] - mx);
-                    s2 = fmaf(e, e, s2);
-                }
-            }
+            const float m0 = xch[0][r][0], m1 = xch[1][r][0];
+            const float M = fmaxf(m0, m1);
+            const float s2 = xch[0][r][1] * exp2f(2.f * (m0 - M)) + xch[1][r][1] * exp2f(2.f * (m1 - M));
+            const float qn = sqrtf(xch[0][r][2] + xch[1][r][2]);
             const float sc = qn * rsqrtf(s2);
 #pragma unroll
-            for (int c0 = 0; c0 < DF; c0 += 32) {
-                float u[32];
-                tmem_ld32(tlane + TM_O + c0, u);
+            for (int c0 = 0; c0 < DFH; c0 += 16) {
+                float u[16];
+                tmem_ld16(tlane + TM_O + half * DFH + c0, u);
                 tmem_ld_wait();
 #pragma unroll
-                for (int c8 = 0; c8 < 4; ++c8) {
+                for (int c8 = 0; c8 < 2; ++c8) {
                     uint32_t w4[4];
 #pragma unroll
                     for (int h2 = 0; h2 < 4; ++h2) {
                         const int i = c8 * 8 + h2 * 2;
-                        const float p0 = sc * expf(u[i] - mx), p1 = sc * expf(u[i + 1] - mx);
+                        const float p0 = sc * exp2f(fmaf(u[i], LOG2E, -M));
+                        const float p1 = sc * exp2f(fmaf(u[i + 1], LOG2E, -M));
                         w4[h2] = pack_bf16(p0, p1);
-                        const int f = c0 + i;
+                        const int f = half * DFH + c0 + i;
                         den = fmaf(__uint_as_float(w4[h2] << 16), zrun[f], den);
                         den = fmaf(__uint_as_float(w4[h2] & 0xffff0000u), zrun[f + 1], den);
                     }
-                    const int f0 = c0 + c8 * 8;
+                    const int f0 = half * DFH + c0 + c8 * 8;
                     *reinterpret_cast<uint4 *>(sm + Lay::PHIQ + (f0 / 64) * 16384 + sw128(r, (f0 % 64) / 8)) =
                         make_uint4(w4[0], w4[1], w4[2], w4[3]);
                 }
@@ -361,62 +391,52 @@ __global__ void __launch_bounds__(128, 1) hybrid_tc_kernel(const __grid_constant
             mma_commit(&bar_mma);
         }
 
-        // ---------------- softmax pass 1: exact row maximum --------------------------
-        float cmax = -INFINITY;
-        for (int kb = 0; kb < nkb; ++kb) {
-            float sv[32];
-            tmem_ld32(tlane + TM_S + 32 * kb, sv);
-            tmem_ld_wait();
-            if (row_ok) {
+        // ---------------- softmax pass 1: exact row maximum (blocks kb = half mod 2) ---
+        {
+            float cmax = -INFINITY;
+            for (int kb = half; kb < nkb; kb += 2) {
+                float sv[32];
+                tmem_ld32(tlane + TM_S + 32 * kb, sv);
+                tmem_ld_wait();
+                const int clo = kb < P.nb ? blo - 32 * kb : 0;
+                const int chi = kb < P.nb ? bhi - 32 * kb : nvk - 1 - 32 * (kb - P.nb);
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    bool ok;
-                    if (kb < P.nb) {
-                        const int j = band_lo + 32 * kb + i;
-                        ok = j >= 0 && j <= t && j > t - W;
-                    } else {
-                        const int j = kpos[32 * (kb - P.nb) + i];
-                        ok = j >= 0 && j <= t - W;
-                    }
-                    if (ok) cmax = fmaxf(cmax, sv[i] * inv_sqrt_d);
-                }
+                for (int i = 0; i < 32; ++i)
+                    if (i >= clo && i <= chi) cmax = fmaxf(cmax, sv[i]);
             }
+            xch[half][r][3] = cmax;
         }
-        const float cm = cmax == -INFINITY ? 0.f : cmax;   // no softmax key: every P is 0
+        __syncthreads();
+        if (s_abort) break;
+        const float cmr = fmaxf(xch[0][r][3], xch[1][r][3]);
+        const float cm = cmr == -INFINITY ? 0.f : cmr * l2s;   // no softmax key: every P is 0
 
         // ---------------- A: mask, row sum, bf16 into P slot 0 -------------------------
         wait_all(&bar_mma, ph_mma);
         tc_fence_after();
         {
-            float a32[32], a16[16];
-            tmem_ld32(tlane + TM_A, a32);
-            tmem_ld16(tlane + TM_A + 32, a16);
+            float a[32];
+            if (half == 0) {
+                tmem_ld32(tlane + TM_A, a);
+            } else {
+                float a16[16];
+                tmem_ld16(tlane + TM_A + 32, a16);
+#pragma unroll
+                for (int i = 0; i < 16; ++i) { a[i] = a16[i]; a[16 + i] = 0.f; }
+            }
             tmem_ld_wait();
-            uint32_t w[32];
+            const int alo = half == 0 ? llo : 0, ahi = half == 0 ? lhi : nvx - 1;
+            uint32_t w[16];
 #pragma unroll
-            for (int i = 0; i < 64; i += 2) {
-                float x0 = 0.f, x1 = 0.f;
-                if (row_ok) {
-#pragma unroll
-                    for (int h2 = 0; h2 < 2; ++h2) {
-                        const int c = i + h2;
-                        float a = 0.f;
-                        if (c < 32) {
-                            const int j = t0 - W + c;
-                            if (j >= 0 && j <= t - W) a = a32[c];
-                        } else if (c < 32 + NX) {
-                            const int j = xpos[c - 32];
-                            if (j >= 0 && j <= t - W) a = a16[c - 32];
-                        }
-                        if (h2 == 0) x0 = a; else x1 = a;
-                    }
-                }
+            for (int i = 0; i < 32; i += 2) {
+                const float x0 = (i >= alo && i <= ahi) ? a[i] : 0.f;
+                const float x1 = (i + 1 >= alo && i + 1 <= ahi) ? a[i + 1] : 0.f;
                 w[i / 2] = pack_bf16(x0, x1);
                 den += __uint_as_float(w[i / 2] << 16) + __uint_as_float(w[i / 2] & 0xffff0000u);
             }
 #pragma unroll
-            for (int c8 = 0; c8 < 8; ++c8)
-                *reinterpret_cast<uint4 *>(sm + Lay::P + sw128(r, c8)) =
+            for (int c8 = 0; c8 < 4; ++c8)
+                *reinterpret_cast<uint4 *>(sm + Lay::P + sw128(r, half * 4 + c8)) =
                     make_uint4(w[c8 * 4], w[c8 * 4 + 1], w[c8 * 4 + 2], w[c8 * 4 + 3]);
         }
         fence_async_smem();
@@ -432,48 +452,33 @@ __global__ void __launch_bounds__(128, 1) hybrid_tc_kernel(const __grid_constant
         }
 
         // ---------------- softmax pass 2 + P V --------------------------------------
-        float lsum = 0.f;
         for (int p = 0; p < npb; ++p) {
             const int ps = (p + 1) & 1;
-            if (p >= 1) {                             // slot ps was read by the MMA two blocks back (or by A V)
-                wait_all(&bar_pfree[ps], ph_pfree[ps]);
-            }
+            if (p >= 1) wait_all(&bar_pfree[ps], ph_pfree[ps]);   // slot read by the MMA two blocks back
             uint8_t *pdst = sm + Lay::P + ps * 16384;
+            const int kb = 2 * p + half;
+            uint32_t w[16];
+            if (kb < nkb) {
+                float sv[32];
+                tmem_ld32(tlane + TM_S + 32 * kb, sv);
+                tmem_ld_wait();
+                const int clo = kb < P.nb ? blo - 32 * kb : 0;
+                const int chi = kb < P.nb ? bhi - 32 * kb : nvk - 1 - 32 * (kb - P.nb);
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const int kb = 2 * p + h;
-                uint32_t w[16];
-                if (kb < nkb) {
-                    float sv[32];
-                    tmem_ld32(tlane + TM_S + 32 * kb, sv);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int i = 0; i < 32; i += 2) {
-                        float pr[2];
-#pragma unroll
-                        for (int h2 = 0; h2 < 2; ++h2) {
-                            bool ok = row_ok;
-                            if (kb < P.nb) {
-                                const int j = band_lo + 32 * kb + i + h2;
-                                ok = ok && j >= 0 && j <= t && j > t - W;
-                            } else {
-                                const int j = kpos[32 * (kb - P.nb) + i + h2];
-                                ok = ok && j >= 0 && j <= t - W;
-                            }
-                            pr[h2] = ok ? expf(fmaf(sv[i + h2], inv_sqrt_d, -cm)) : 0.f;
-                        }
-                        w[i / 2] = pack_bf16(pr[0], pr[1]);
-                        lsum += __uint_as_float(w[i / 2] << 16) + __uint_as_float(w[i / 2] & 0xffff0000u);
-                    }
-                } else {
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) w[i] = 0u;
+                for (int i = 0; i < 32; i += 2) {
+                    const float p0 = (i >= clo && i <= chi) ? exp2f(fmaf(sv[i], l2s, -cm)) : 0.f;
+                    const float p1 = (i + 1 >= clo && i + 1 <= chi) ? exp2f(fmaf(sv[i + 1], l2s, -cm)) : 0.f;
+                    w[i / 2] = pack_bf16(p0, p1);
+                    den += __uint_as_float(w[i / 2] << 16) + __uint_as_float(w[i / 2] & 0xffff0000u);
                 }
+            } else {
 #pragma unroll
-                for (int c8 = 0; c8 < 4; ++c8)
-                    *reinterpret_cast<uint4 *>(pdst + sw128(r, h * 4 + c8)) =
-                        make_uint4(w[c8 * 4], w[c8 * 4 + 1], w[c8 * 4 + 2], w[c8 * 4 + 3]);
+                for (int i = 0; i < 16; ++i) w[i] = 0u;
             }
+#pragma unroll
+            for (int c8 = 0; c8 < 4; ++c8)
+                *reinterpret_cast<uint4 *>(pdst + sw128(r, half * 4 + c8)) =
+                    make_uint4(w[c8 * 4], w[c8 * 4 + 1], w[c8 * 4 + 2], w[c8 * 4 + 3]);
             fence_async_smem();
             tc_fence_before();
             __syncthreads();
@@ -492,31 +497,17 @@ __global__ void __launch_bounds__(128, 1) hybrid_tc_kernel(const __grid_constant
                     mma_commit(&bar_vfree[vs]);
                 }
                 // refill the V slot of block p-1 with block p+1 once its MMA is done
-                if (p >= 1 && p + 1 < npb && p + 1 >= 2) {
+                if (p >= 1 && p + 1 < npb) {
                     const int os = (p - 1) & 1;
                     if (!mbar_wait(&bar_vfree[os], ph_vfree[os], P.status)) s_abort = 1;
                     ph_vfree[os] ^= 1;
-                    const int q2 = p + 1;
-                    uint8_t *dst = sm + Lay::RING + os * CBD * 8192;
-                    mbar_expect_tx(&bar_vfull[os], CBD * 8192);
-                    for (int h = 0; h < 2; ++h) {
-                        const int kb = 2 * q2 + h;
-                        for (int cb = 0; cb < CBD; ++cb) {
-                            if (kb < P.nb)
-                                tma_load_3d(dst + cb * 8192 + h * 4096, &maps.v, &bar_vfull[os], cb * 64,
-                                            band_lo + 32 * kb, unit);
-                            else
-                                tma_load_3d(dst + cb * 8192 + h * 4096, &maps.vk, &bar_vfull[os], cb * 64,
-                                            32 * (kb - P.nb), unit);
-                        }
-                    }
+                    load_v(p + 1, nkb, band_lo);
                 }
             }
         }
-        if (s_abort) break;
 
         // ---------------- readout and state update MMAs ------------------------------
-        if (tid == 0) {
+        if (tid == 0 && !s_abort) {
             tc_fence_after();
             for (int k = 0; k < DF; k += 16)
                 mma_ss(tmem + TM_O, kdesc(sb + Lay::PHIQ, k, 16384), sdesc(sb + Lay::SRUN + k * 128, DF * 128, 1024),
@@ -527,60 +518,62 @@ __global__ void __launch_bounds__(128, 1) hybrid_tc_kernel(const __grid_constant
                        sdesc(sb + Lay::VLAG + kk * 128, 6144, 1024), id_ds, kk > 0);
             mma_commit(&bar_mma);
         }
+        xch[half][r][0] = den;
+        __syncthreads();
+        if (s_abort) break;
         wait_all(&bar_mma, ph_mma);
         tc_fence_after();
-        if (s_abort) break;
+        const float dtot = xch[0][r][0] + xch[1][r][0];
 
-        // ---------------- epilogue: y = O / den ---------------------------------------
+        // ---------------- epilogue: y = O / den (my half of the columns) ---------------
         {
-            den += lsum;
-            const float inv = den != 0.f ? 1.f / den : 0.f;
+            const float inv = dtot != 0.f ? 1.f / dtot : 0.f;
 #pragma unroll
-            for (int c0 = 0; c0 < D; c0 += 32) {
-                float o[32];
-                tmem_ld32(tlane + TM_O + c0, o);
+            for (int c0 = 0; c0 < DH; c0 += 16) {
+                float o[16];
+                tmem_ld16(tlane + TM_O + half * DH + c0, o);
                 tmem_ld_wait();
 #pragma unroll
-                for (int c8 = 0; c8 < 4; ++c8) {
+                for (int c8 = 0; c8 < 2; ++c8) {
                     uint4 pk;
                     pk.x = pack_bf16(o[c8 * 8 + 0] * inv, o[c8 * 8 + 1] * inv);
                     pk.y = pack_bf16(o[c8 * 8 + 2] * inv, o[c8 * 8 + 3] * inv);
                     pk.z = pack_bf16(o[c8 * 8 + 4] * inv, o[c8 * 8 + 5] * inv);
                     pk.w = pack_bf16(o[c8 * 8 + 6] * inv, o[c8 * 8 + 7] * inv);
-                    const int d0 = c0 + c8 * 8;
+                    const int d0 = half * DH + c0 + c8 * 8;
                     *reinterpret_cast<uint4 *>(sm + Lay::PHIQ + (d0 / 64) * 16384 + sw128(r, (d0 % 64) / 8)) = pk;
                 }
             }
         }
         // ---------------- state update: S_run += dS, z_run += sum phi(K_lag) ------------
         {
-            const int f = tid;
+            const int f = r;
 #pragma unroll
-            for (int c0 = 0; c0 < D; c0 += 32) {
-                float ds[32];
-                tmem_ld32(tlane + TM_S + c0, ds);
+            for (int c0 = 0; c0 < DH; c0 += 16) {
+                float ds[16];
+                tmem_ld16(tlane + TM_S + half * DH + c0, ds);
                 tmem_ld_wait();
 #pragma unroll
-                for (int i = 0; i < 32; ++i) srun[c0 + i] += ds[i];
+                for (int i = 0; i < 16; ++i) srun[c0 + i] += ds[i];
             }
             if (f < DF) {
 #pragma unroll
-                for (int c8 = 0; c8 < D / 8; ++c8) {
+                for (int c8 = 0; c8 < DH / 8; ++c8) {
+                    const int c = half * DH + c8 * 8;
                     uint4 pk;
                     pk.x = pack_bf16(srun[c8 * 8 + 0], srun[c8 * 8 + 1]);
                     pk.y = pack_bf16(srun[c8 * 8 + 2], srun[c8 * 8 + 3]);
                     pk.z = pack_bf16(srun[c8 * 8 + 4], srun[c8 * 8 + 5]);
                     pk.w = pack_bf16(srun[c8 * 8 + 6], srun[c8 * 8 + 7]);
-                    *reinterpret_cast<uint4 *>(sm + Lay::SRUN + (c8 / 8) * (DF * 128) + sw128(f, c8 % 8)) = pk;
+                    *reinterpret_cast<uint4 *>(sm + Lay::SRUN + (c / 64) * (DF * 128) + sw128(f, (c % 64) / 8)) = pk;
                 }
-                float za = 0.f;
-                const int cb = f / 64, c8 = (f % 64) / 8, e = f % 8;
-                for (int tok = 0; tok < 32; ++tok) {
-                    const uint16_t x =
-                        *reinterpret_cast<const uint16_t *>(sm + Lay::PHIK + cb * 6144 + sw128(tok, c8) + e * 2);
-                    za += bf2f(x);
+                if (half == 0) {
+                    float za = 0.f;
+                    const int cb = f / 64, c8 = (f % 64) / 8, e = f % 8;
+                    for (int tok = 0; tok < 32; ++tok)
+                        za += bf2f(*reinterpret_cast<const uint16_t *>(sm + Lay::PHIK + cb * 6144 + sw128(tok, c8) + e * 2));
+                    zrun[f] += za;
                 }
-                zrun[f] += za;
             }
         }
         fence_async_smem();
@@ -669,11 +662,11 @@ cudaError_t launch_hybrid_tc(const Dims &dm, const SegPlan &sp, const TCBuffers 
     if (D == 64) {
         e = cudaFuncSetAttribute(hybrid_tc_kernel<64, 64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        hybrid_tc_kernel<64, 64><<<grid, 128, smem, s>>>(m, p);
+        hybrid_tc_kernel<64, 64><<<grid, 256, smem, s>>>(m, p);
     } else {
         e = cudaFuncSetAttribute(hybrid_tc_kernel<128, 128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        hybrid_tc_kernel<128, 128><<<grid, 128, smem, s>>>(m, p);
+        hybrid_tc_kernel<128, 128><<<grid, 256, smem, s>>>(m, p);
     }
     return cudaGetLastError();
 }
