@@ -276,8 +276,9 @@ still_status still_prefill(const still_shape *shape, const still_bf16 *q, const 
     if (e == cudaSuccess && dm.lam > 0)
         e = score_tc_supported(dm) ? launch_score_tc(dm, q, k, scores, s) : launch_score(dm, q, k, scores, s);
     if (e == cudaSuccess && dm.lam > 0) e = launch_select(dm, scores, sel_idx, fsel, flag, s);
-    if (e == cudaSuccess) e = launch_features(dm, k, v, Wf, flag, fsel, phik, kk, vk, phk, tc ? wft : nullptr, s);
-    if (e == cudaSuccess) e = launch_linstate(dm, sp, phik, v, dS, dz, s);
+    if (e == cudaSuccess) e = launch_kept(dm, k, v, Wf, fsel, kk, vk, phk, wft, s);
+    if (e == cudaSuccess) e = launch_linstate_tc(dm, sp, k, v, wft, flag, phik, dS, dz, status, s);
+    if (e == cudaSuccess) e = launch_scan(dm, sp, dS, dz, s);
     if (e == cudaSuccess) {
         if (tc) {
             TCBuffers bf{q, k, v, kk, vk, phik, phk, wft, out};

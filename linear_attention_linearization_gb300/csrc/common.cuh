@@ -143,11 +143,12 @@ cudaError_t launch_select(const Dims &dm, const float *scores, int32_t *sel_idx,
                           cudaStream_t s);
 cudaError_t launch_npmap(const uint16_t *x, long long rows, int d, const float *Wf, int df, float *phi,
                          cudaStream_t s);
-cudaError_t launch_features(const Dims &dm, const uint16_t *k, const uint16_t *v, const float *Wf,
-                            const uint8_t *flag, const int32_t *fsel, uint16_t *phik, uint16_t *kk, uint16_t *vk,
-                            uint16_t *phk, uint16_t *wft, cudaStream_t s);
-cudaError_t launch_linstate(const Dims &dm, const SegPlan &sp, const uint16_t *phik, const uint16_t *v, float *dS,
-                            float *dz, cudaStream_t s);
+cudaError_t launch_kept(const Dims &dm, const uint16_t *k, const uint16_t *v, const float *Wf, const int32_t *fsel,
+                        uint16_t *kk, uint16_t *vk, uint16_t *phk, uint16_t *wft, cudaStream_t s);
+cudaError_t launch_linstate_tc(const Dims &dm, const SegPlan &sp, const uint16_t *k, const uint16_t *v,
+                               const uint16_t *wft, const uint8_t *flag, uint16_t *phik, float *dS, float *dz,
+                               int32_t *status, cudaStream_t s);
+cudaError_t launch_scan(const Dims &dm, const SegPlan &sp, float *dS, float *dz, cudaStream_t s);
 cudaError_t launch_hybrid_general(const Dims &dm, const SegPlan &sp, const uint16_t *q, const uint16_t *k,
                                   const uint16_t *v, const float *Wf, const uint16_t *phik, const uint16_t *phkept,
                                   const int32_t *fsel, const float *dS, const float *dz, uint16_t *out,

@@ -1,14 +1,10 @@
-// Key features and kept-token tables of the prefill.
+// Kept-token tables of the prefill and the bf16 copy of Wf^T.
 //
 // "STILL: Content-Aware Intra-Layer Hybrid Attention for Efficient LLM
-// Linearization", section "NP-Map: Norm-Preserving Feature Map" (phi) and
-// section "Content-Aware Routing with Fixed Budget" (kept tokens stay out of
-// the linear state).
+// Linearization", section "Content-Aware Routing with Fixed Budget" (kept
+// tokens stay out of the linear state) and section "NP-Map: Norm-Preserving
+// Feature Map" (phi).
 //
-//   phik[j]  = bf16(phi(k_j)) for every key, or 0 when j sits in a budget slot
-//              (kept by a finished chunk, or in the running top-lambda of the
-//              unfinished tail chunk).  Every linear-state sum over keys then
-//              leaves slotted keys out without a test.
 //   kept tables, row c*lambda + r for the r-th kept token of chunk c (the
 //   order of the selection table): K, V and the unmasked phi of that token,
 //   zero rows where the selection has no token.  The kept tokens of all
@@ -17,28 +13,6 @@
 #include "common.cuh"
 
 namespace still {
-
-template <int D, int DF>
-__global__ void __launch_bounds__(256) features_kernel(const uint16_t *__restrict__ k, const float *__restrict__ Wf,
-                                                       const uint8_t *__restrict__ flag, Dims dm,
-                                                       uint16_t *__restrict__ phik)
-{
-    __shared__ float xs[8][D];
-    __shared__ float ph[8][DF];
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const size_t ug = blockIdx.y;
-    for (int j = blockIdx.x * 8 + warp; j < dm.N; j += gridDim.x * 8) {
-        const uint16_t *kr = k + (ug * dm.N + j) * D;
-        __syncwarp();
-        for (int e = lane; e < D; e += 32) xs[warp][e] = bf2f(kr[e]);
-        __syncwarp();
-        warp_npmap<D, DF>(xs[warp], Wf, ph[warp], lane);
-        __syncwarp();
-        const bool slotted = flag[ug * dm.N + j] != 0;
-        uint16_t *dst = phik + (ug * dm.N + j) * DF;
-        for (int e = lane; e < DF; e += 32) dst[e] = slotted ? (uint16_t)0 : f2bf(ph[warp][e]);
-    }
-}
 
 template <int D, int DF>
 __global__ void __launch_bounds__(256) kept_kernel(const uint16_t *__restrict__ k, const uint16_t *__restrict__ v,
@@ -84,24 +58,10 @@ __global__ void wft_kernel(const float *__restrict__ Wf, int d, int df, uint16_t
     }
 }
 
-cudaError_t launch_features(const Dims &dm, const uint16_t *k, const uint16_t *v, const float *Wf,
-                            const uint8_t *flag, const int32_t *fsel, uint16_t *phik, uint16_t *kk, uint16_t *vk,
-                            uint16_t *phk, uint16_t *wft, cudaStream_t s)
+cudaError_t launch_kept(const Dims &dm, const uint16_t *k, const uint16_t *v, const float *Wf, const int32_t *fsel,
+                        uint16_t *kk, uint16_t *vk, uint16_t *phk, uint16_t *wft, cudaStream_t s)
 {
     const int units = dm.B * dm.Hkv;
-    {
-        KTimer tm("features", s);
-        const int bx = (int)((dm.N + 7) / 8 < 256 ? (dm.N + 7) / 8 : 256);
-        dim3 grid(bx, units);
-#define STILL_FEAT(DD, FF) features_kernel<DD, FF><<<grid, 256, 0, s>>>(k, Wf, flag, dm, phik)
-        if (dm.d == 64 && dm.df == 64) STILL_FEAT(64, 64);
-        else if (dm.d == 64) STILL_FEAT(64, 128);
-        else if (dm.df == 64) STILL_FEAT(128, 64);
-        else STILL_FEAT(128, 128);
-#undef STILL_FEAT
-        cudaError_t e = cudaGetLastError();
-        if (e != cudaSuccess) return e;
-    }
     if (dm.lam > 0) {
         KTimer tm("kept_tables", s);
         const int KP = dm.T_max * dm.lam;
@@ -115,12 +75,9 @@ cudaError_t launch_features(const Dims &dm, const uint16_t *k, const uint16_t *v
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
-    if (wft) {
-        KTimer tm("wf_transpose", s);
-        wft_kernel<<<16, 256, 0, s>>>(Wf, dm.d, dm.df, wft);
-        return cudaGetLastError();
-    }
-    return cudaSuccess;
+    KTimer tm("wf_transpose", s);
+    wft_kernel<<<16, 256, 0, s>>>(Wf, dm.d, dm.df, wft);
+    return cudaGetLastError();
 }
 
 }  // namespace still

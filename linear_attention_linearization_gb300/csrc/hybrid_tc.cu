@@ -19,8 +19,10 @@
 //         lag = the 32 keys [t0-W, t0-W+32) that leave the window during the
 //         tile (rows of slotted keys are zero in the feature table); extra =
 //         the kept tokens of the tile's own chunk, which are still linear keys
-//   O   = A V_lagx + sum_p P_p V_p + phi(Q) S_run                          (TMEM)
-//         P = exp(S - c) masked, c = exact row maximum over the softmax keys
+//   O   = A V_lagx + sum_kb P_kb V_kb + phi(Q) S_run                       (TMEM)
+//         P = exp(S - c) masked, c = exact row maximum over the softmax keys;
+//         masked A and P are written back to TMEM as bf16 pairs over the
+//         columns they came from and feed the MMAs from there
 //   dS  = phi(K_lag)^T V_lag -> S_run += dS (fp32 in registers, bf16 copy in smem)
 //   y   = O / (sum P + sum A + phi(Q).z_run)                              (TMA store)
 // Masks (window, causal lag, chunk of the kept tokens) are applied to the
@@ -55,6 +57,8 @@ constexpr int TM_S = 0, TM_O = 320, TM_A = 448, TM_COLS = 512;
 constexpr int MAX_KEY_BLOCKS = 10;   // 320 logit columns
 constexpr int NX = 16;               // extra (kept, own chunk) rows per tile
 
+constexpr int RING_SLOTS = 8;        // K (then V) blocks of 32 keys in flight
+
 template <int D, int DF>
 struct TCLayout {
     static constexpr int CBD = D / 64, CBF = DF / 64;
@@ -62,9 +66,9 @@ struct TCLayout {
     static constexpr uint32_t WF = Q + CBD * 16384;
     static constexpr uint32_t PHIQ = WF + CBD * DF * 128;
     static constexpr uint32_t SRUN = PHIQ + (CBD > CBF ? CBD : CBF) * 16384;
-    static constexpr uint32_t RING = SRUN + CBD * DF * 128;
-    static constexpr uint32_t P = RING + 4 * CBD * 4096;
-    static constexpr uint32_t PHIK = P + 2 * 16384;
+    static constexpr uint32_t RING = SRUN + CBD * DF * 128;   // CBD regions of RING_SLOTS x 32 rows x 128 B
+    static constexpr uint32_t RSTRIDE = RING_SLOTS * 4096;     // bytes between the column-block regions
+    static constexpr uint32_t PHIK = RING + CBD * RSTRIDE;
     static constexpr uint32_t VLAG = PHIK + CBF * 6144;
     static constexpr uint32_t KPOS = VLAG + CBD * 6144;          // int32[MAX_KEY_BLOCKS * 32]
     static constexpr uint32_t XPOS = KPOS + MAX_KEY_BLOCKS * 32 * 4;
@@ -79,6 +83,8 @@ __global__ void __launch_bounds__(256, 1) hybrid_tc_kernel(const __grid_constant
     constexpr int CBD = Lay::CBD, CBF = Lay::CBF;
     constexpr int DH = D / 2, DFH = DF / 2;   // columns per half-row thread
     constexpr float LOG2E = 1.4426950408889634f;
+    constexpr uint32_t SLOT = CBD * 4096;     // bytes of one ring slot (32 keys x D)
+    constexpr uint32_t RSTRIDE = Lay::RSTRIDE;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     const uint32_t sb = smem_u32(sm);
@@ -86,8 +92,7 @@ __global__ void __launch_bounds__(256, 1) hybrid_tc_kernel(const __grid_constant
     int32_t *xpos = (int32_t *)(sm + Lay::XPOS);
     float *zrun = (float *)(sm + Lay::ZRUN);
 
-    __shared__ uint64_t bar_q, bar_wf, bar_lag, bar_mma, bar_kfull[4], bar_kfree[4], bar_vfull[2], bar_vfree[2],
-        bar_pfree[2];
+    __shared__ uint64_t bar_q, bar_wf, bar_lag, bar_mma, bar_ds, bar_full[RING_SLOTS], bar_free[RING_SLOTS];
     __shared__ uint32_t tmem_base;
     __shared__ int s_abort;
     __shared__ float xch[2][128][4];
@@ -113,8 +118,8 @@ __global__ void __launch_bounds__(256, 1) hybrid_tc_kernel(const __grid_constant
         mbar_init(&bar_wf, 1);
         mbar_init(&bar_lag, 1);
         mbar_init(&bar_mma, 1);
-        for (int i = 0; i < 4; ++i) { mbar_init(&bar_kfull[i], 1); mbar_init(&bar_kfree[i], 1); }
-        for (int i = 0; i < 2; ++i) { mbar_init(&bar_vfull[i], 1); mbar_init(&bar_vfree[i], 1); mbar_init(&bar_pfree[i], 1); }
+        mbar_init(&bar_ds, 1);
+        for (int i = 0; i < RING_SLOTS; ++i) { mbar_init(&bar_full[i], 1); mbar_init(&bar_free[i], 1); }
         fence_barrier_init();
         s_abort = 0;
     }
@@ -151,7 +156,7 @@ __global__ void __launch_bounds__(256, 1) hybrid_tc_kernel(const __grid_constant
         }
     }
 
-    // ---- loads --------------------------------------------------------------------
+    // ---- loads (issued by thread 0 only) -------------------------------------------
     auto load_q = [&](int t0) {
         mbar_expect_tx(&bar_q, dm.G * CBD * 4096);
         for (int hh = 0; hh < dm.G; ++hh)
@@ -172,20 +177,23 @@ __global__ void __launch_bounds__(256, 1) hybrid_tc_kernel(const __grid_constant
             tma_load_3d(sm + Lay::VLAG + cb * 6144 + 4096, &maps.vk16, &bar_lag, cb * 64, xrow, unit);
         }
     };
-    auto load_v = [&](int p, int nkb, int band_lo) {   // V block p (64 keys) into V slot p & 1
-        const int vs = p & 1;
-        uint8_t *dst = sm + Lay::RING + vs * CBD * 8192;
-        mbar_expect_tx(&bar_vfull[vs], CBD * 8192);
-        for (int h = 0; h < 2; ++h) {
-            const int kb = 2 * p + h;
-            for (int cb = 0; cb < CBD; ++cb) {
-                if (kb < P.nb)
-                    tma_load_3d(dst + cb * 8192 + h * 4096, &maps.v, &bar_vfull[vs], cb * 64, band_lo + 32 * kb, unit);
-                else
-                    tma_load_3d(dst + cb * 8192 + h * 4096, &maps.vk, &bar_vfull[vs], cb * 64, 32 * (kb - P.nb), unit);
-            }
+    // block kb (32 keys) of the key list of the tile at t0, K (kv = 0) or V (kv = 1), into ring slot kb % RING_SLOTS
+    auto load_blk = [&](int kb, int t0, int kv) {
+        const int slot = kb % RING_SLOTS;
+        uint8_t *dst = sm + Lay::RING + slot * 4096;
+        mbar_expect_tx(&bar_full[slot], SLOT);
+        const CUtensorMap *band = kv ? &maps.v : &maps.k;
+        const CUtensorMap *kept = kv ? &maps.vk : &maps.kk;
+        for (int cb = 0; cb < CBD; ++cb) {
+            if (kb < P.nb)
+                tma_load_3d(dst + cb * RSTRIDE, band, &bar_full[slot], cb * 64, t0 - P.Wr + 32 * kb, unit);
+            else
+                tma_load_3d(dst + cb * RSTRIDE, kept, &bar_full[slot], cb * 64, 32 * (kb - P.nb), unit);
         }
-        (void)nkb;
+    };
+    auto nkb_of = [&](int t0) {
+        const int nkg = min(t0 / C, dm.T_max) * lam;
+        return P.nb + (nkg + 31) / 32;
     };
     if (tid == 0) {
         tma_prefetch_desc(&maps.q);
@@ -194,14 +202,14 @@ __global__ void __launch_bounds__(256, 1) hybrid_tc_kernel(const __grid_constant
         if (ntiles > 0) {
             load_q(tbeg);
             load_lag(tbeg);
+            for (int kb = 0; kb < nkb_of(tbeg) && kb < RING_SLOTS; ++kb) load_blk(kb, tbeg, 0);
         }
     }
     fence_async_smem();
     __syncthreads();
 
-    uint32_t ph_q = 0, ph_lag = 0, ph_mma = 0;
-    uint32_t ph_kfull[4] = {0, 0, 0, 0}, ph_kfree[4] = {0, 0, 0, 0};
-    uint32_t ph_vfull[2] = {0, 0}, ph_vfree[2] = {0, 0}, ph_pfree[2] = {0, 0};
+    uint32_t ph_q = 0, ph_lag = 0, ph_mma = 0, ph_ds = 0;
+    uint32_t ph_full = 0, ph_free = 0;   // one parity bit per ring slot (thread 0)
     bool wf_ready = false;
 
     const uint32_t id_u = idesc_bf16(128, DF, 0, 0);
@@ -213,9 +221,18 @@ __global__ void __launch_bounds__(256, 1) hybrid_tc_kernel(const __grid_constant
     auto kdesc = [&](uint32_t base, int k, uint32_t blockbytes) {   // K-major operand, K step k
         return sdesc(base + (k / 64) * blockbytes + (k % 64) * 2, 16, 1024);
     };
+    // descriptors advance by adding (byte offset >> 4) to the start-address field
+    const uint64_t dQ = sdesc(sb + Lay::Q, 16, 1024), dWF = sdesc(sb + Lay::WF, 16, 1024);
+    const uint64_t dKR = sdesc(sb + Lay::RING, 16, 1024);               // K-major ring (keys as N)
+    const uint64_t dVR = sdesc(sb + Lay::RING, RSTRIDE, 1024);          // MN-major ring (keys as K)
+    auto koff = [](int k, uint32_t blockbytes) { return (uint64_t)(((k / 64) * blockbytes + (k % 64) * 2) >> 4); };
     auto wait_all = [&](uint64_t *bar, uint32_t &ph) {
         if (!mbar_wait(bar, ph, P.status)) s_abort = 1;
         ph ^= 1;
+    };
+    auto wait_slot = [&](uint64_t *bars, uint32_t &phs, int slot) {   // thread 0 only
+        if (!mbar_wait(&bars[slot], (phs >> slot) & 1u, P.status)) s_abort = 1;
+        phs ^= 1u << slot;
     };
 
     for (int it = 0; it < ntiles; ++it) {
@@ -224,7 +241,6 @@ __global__ void __launch_bounds__(256, 1) hybrid_tc_kernel(const __grid_constant
         const int nkg = min(ct, dm.T_max) * lam;
         const int ngb = (nkg + 31) / 32;
         const int nkb = P.nb + ngb;
-        const int npb = (nkb + 1) / 2;
         const int band_lo = t0 - P.Wr;
         const bool has_next = it + 1 < ntiles;
 
@@ -248,35 +264,28 @@ __global__ void __launch_bounds__(256, 1) hybrid_tc_kernel(const __grid_constant
             if (!mbar_wait(&bar_q, ph_q, P.status)) s_abort = 1;
             ph_q ^= 1;
             tc_fence_after();
+#pragma unroll
             for (int k = 0; k < D; k += 16)
-                mma_ss(tmem + TM_O, kdesc(sb + Lay::Q, k, 16384), kdesc(sb + Lay::WF, k, DF * 128), id_u, k > 0);
-            auto issue_k = [&](int kb) {
-                const int slot = kb & 3;
-                uint8_t *dst = sm + Lay::RING + slot * CBD * 4096;
-                mbar_expect_tx(&bar_kfull[slot], CBD * 4096);
-                for (int cb = 0; cb < CBD; ++cb) {
-                    if (kb < P.nb)
-                        tma_load_3d(dst + cb * 4096, &maps.k, &bar_kfull[slot], cb * 64, band_lo + 32 * kb, unit);
-                    else
-                        tma_load_3d(dst + cb * 4096, &maps.kk, &bar_kfull[slot], cb * 64, 32 * (kb - P.nb), unit);
-                }
-            };
-            for (int kb = 0; kb < nkb && kb < 4; ++kb) issue_k(kb);
-            for (int kb = 0; kb < nkb; ++kb) {
-                const int slot = kb & 3;
-                if (!mbar_wait(&bar_kfull[slot], ph_kfull[slot], P.status)) { s_abort = 1; break; }
-                ph_kfull[slot] ^= 1;
+                mma_ss(tmem + TM_O, dQ + koff(k, 16384), dWF + koff(k, DF * 128), id_u, k > 0);
+            // blocks 0 .. n1-1 sit in consecutive slots: one MMA of N = 32 n1 per K step
+            const int n1 = nkb < RING_SLOTS ? nkb : RING_SLOTS;
+            for (int kb = 0; kb < n1; ++kb) wait_slot(bar_full, ph_full, kb);
+            tc_fence_after();
+            const uint32_t id_s1 = idesc_bf16(128, 32 * n1, 0, 0);
+#pragma unroll
+            for (int k = 0; k < D; k += 16)
+                mma_ss(tmem + TM_S, dQ + koff(k, 16384), dKR + koff(k, RSTRIDE), id_s1, k > 0);
+            if (nkb > RING_SLOTS) {
+                // the rest reuse the first slots once the wide MMA has read them
+                mma_commit(&bar_free[0]);
+                wait_slot(bar_free, ph_free, 0);
+                for (int kb = RING_SLOTS; kb < nkb; ++kb) load_blk(kb, t0, 0);
+                for (int kb = RING_SLOTS; kb < nkb; ++kb) wait_slot(bar_full, ph_full, kb - RING_SLOTS);
                 tc_fence_after();
-                const uint32_t kbase = sb + Lay::RING + slot * CBD * 4096;
+                const uint32_t id_s2 = idesc_bf16(128, 32 * (nkb - RING_SLOTS), 0, 0);
+#pragma unroll
                 for (int k = 0; k < D; k += 16)
-                    mma_ss(tmem + TM_S + 32 * kb, kdesc(sb + Lay::Q, k, 16384), kdesc(kbase, k, 4096), id_s, k > 0);
-                if (kb + 4 < nkb) mma_commit(&bar_kfree[slot]);
-                if (kb >= 1 && kb + 3 < nkb) {
-                    const int ps = (kb - 1) & 3;
-                    if (!mbar_wait(&bar_kfree[ps], ph_kfree[ps], P.status)) { s_abort = 1; break; }
-                    ph_kfree[ps] ^= 1;
-                    issue_k(kb + 3);
-                }
+                    mma_ss(tmem + TM_S + 32 * RING_SLOTS, dQ + koff(k, 16384), dKR + koff(k, RSTRIDE), id_s2, k > 0);
             }
             mma_commit(&bar_mma);
         }
@@ -311,26 +320,20 @@ __global__ void __launch_bounds__(256, 1) hybrid_tc_kernel(const __grid_constant
         wait_all(&bar_mma, ph_mma);                 // U and S are in TMEM; Q and the ring are free
         tc_fence_after();
 
-        // ---------------- phi(Q), pass 1: max and sum of u^2 over my features -------
+        // ---------------- phi(Q), pass 1: exponentials of my features (kept) ----------
+        float eu[DFH];
+        float mu = -INFINITY;
         {
-            float mu = -INFINITY, s2 = 0.f;
+            float s2 = 0.f;
 #pragma unroll
-            for (int c0 = 0; c0 < DFH; c0 += 16) {
-                float u[16];
-                tmem_ld16(tlane + TM_O + half * DFH + c0, u);
-                tmem_ld_wait();
-                float bm = -INFINITY;
+            for (int c0 = 0; c0 < DFH; c0 += 16) tmem_ld16(tlane + TM_O + half * DFH + c0, *reinterpret_cast<float(*)[16]>(eu + c0));
+            tmem_ld_wait();
 #pragma unroll
-                for (int i = 0; i < 16; ++i) bm = fmaxf(bm, u[i] * LOG2E);
-                if (bm > mu) {
-                    s2 *= exp2f(2.f * (mu - bm));
-                    mu = bm;
-                }
+            for (int i = 0; i < DFH; ++i) mu = fmaxf(mu, eu[i] * LOG2E);
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const float e = exp2f(fmaf(u[i], LOG2E, -mu));
-                    s2 = fmaf(e, e, s2);
-                }
+            for (int i = 0; i < DFH; ++i) {
+                eu[i] = exp2f(fmaf(eu[i], LOG2E, -mu));
+                s2 = fmaf(eu[i], eu[i], s2);
             }
             xch[half][r][0] = mu;
             xch[half][r][1] = s2;
@@ -340,7 +343,7 @@ __global__ void __launch_bounds__(256, 1) hybrid_tc_kernel(const __grid_constant
         if (s_abort) break;
         if (tid == 0) {
             if (has_next) load_q(t0 + 32);
-            for (int p = 0; p < npb && p < 2; ++p) load_v(p, nkb, band_lo);
+            for (int kb = 0; kb < nkb && kb < RING_SLOTS; ++kb) load_blk(kb, t0, 1);   // the ring is free: V blocks
             tma_store_wait_read();                  // the previous tile's output left the staging buffer
         }
         __syncthreads();
@@ -352,20 +355,17 @@ __global__ void __launch_bounds__(256, 1) hybrid_tc_kernel(const __grid_constant
             const float M = fmaxf(m0, m1);
             const float s2 = xch[0][r][1] * exp2f(2.f * (m0 - M)) + xch[1][r][1] * exp2f(2.f * (m1 - M));
             const float qn = sqrtf(xch[0][r][2] + xch[1][r][2]);
-            const float sc = qn * rsqrtf(s2);
+            const float sc = qn * rsqrtf(s2) * exp2f(mu - M);   // my half's exponentials were taken against mu
 #pragma unroll
             for (int c0 = 0; c0 < DFH; c0 += 16) {
-                float u[16];
-                tmem_ld16(tlane + TM_O + half * DFH + c0, u);
-                tmem_ld_wait();
 #pragma unroll
                 for (int c8 = 0; c8 < 2; ++c8) {
                     uint32_t w4[4];
 #pragma unroll
                     for (int h2 = 0; h2 < 4; ++h2) {
                         const int i = c8 * 8 + h2 * 2;
-                        const float p0 = sc * exp2f(fmaf(u[i], LOG2E, -M));
-                        const float p1 = sc * exp2f(fmaf(u[i + 1], LOG2E, -M));
+                        const float p0 = sc * eu[c0 + i];
+                        const float p1 = sc * eu[c0 + i + 1];
                         w4[h2] = pack_bf16(p0, p1);
                         const int f = half * DFH + c0 + i;
                         den = fmaf(__uint_as_float(w4[h2] << 16), zrun[f], den);
@@ -394,15 +394,22 @@ __global__ void __launch_bounds__(256, 1) hybrid_tc_kernel(const __grid_constant
         // ---------------- softmax pass 1: exact row maximum (blocks kb = half mod 2) ---
         {
             float cmax = -INFINITY;
-            for (int kb = half; kb < nkb; kb += 2) {
-                float sv[32];
-                tmem_ld32(tlane + TM_S + 32 * kb, sv);
+            for (int kb = half; kb < nkb; kb += 4) {
+                float sv[2][32];
+                const bool two = kb + 2 < nkb;
+                tmem_ld32(tlane + TM_S + 32 * kb, sv[0]);
+                if (two) tmem_ld32(tlane + TM_S + 32 * (kb + 2), sv[1]);
                 tmem_ld_wait();
-                const int clo = kb < P.nb ? blo - 32 * kb : 0;
-                const int chi = kb < P.nb ? bhi - 32 * kb : nvk - 1 - 32 * (kb - P.nb);
 #pragma unroll
-                for (int i = 0; i < 32; ++i)
-                    if (i >= clo && i <= chi) cmax = fmaxf(cmax, sv[i]);
+                for (int x = 0; x < 2; ++x) {
+                    if (x == 1 && !two) break;
+                    const int bk = kb + 2 * x;
+                    const int clo = bk < P.nb ? blo - 32 * bk : 0;
+                    const int chi = bk < P.nb ? bhi - 32 * bk : nvk - 1 - 32 * (bk - P.nb);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        if (i >= clo && i <= chi) cmax = fmaxf(cmax, sv[x][i]);
+                }
             }
             xch[half][r][3] = cmax;
         }
@@ -411,128 +418,116 @@ __global__ void __launch_bounds__(256, 1) hybrid_tc_kernel(const __grid_constant
         const float cmr = fmaxf(xch[0][r][3], xch[1][r][3]);
         const float cm = cmr == -INFINITY ? 0.f : cmr * l2s;   // no softmax key: every P is 0
 
-        // ---------------- A: mask, row sum, bf16 into P slot 0 -------------------------
+        // ---------------- A: mask, row sum, bf16 pairs back into TMEM ------------------
         wait_all(&bar_mma, ph_mma);
         tc_fence_after();
-        {
+        if (half == 0) {
             float a[32];
-            if (half == 0) {
-                tmem_ld32(tlane + TM_A, a);
-            } else {
-                float a16[16];
-                tmem_ld16(tlane + TM_A + 32, a16);
-#pragma unroll
-                for (int i = 0; i < 16; ++i) { a[i] = a16[i]; a[16 + i] = 0.f; }
-            }
+            tmem_ld32(tlane + TM_A, a);
             tmem_ld_wait();
-            const int alo = half == 0 ? llo : 0, ahi = half == 0 ? lhi : nvx - 1;
             uint32_t w[16];
 #pragma unroll
             for (int i = 0; i < 32; i += 2) {
-                const float x0 = (i >= alo && i <= ahi) ? a[i] : 0.f;
-                const float x1 = (i + 1 >= alo && i + 1 <= ahi) ? a[i + 1] : 0.f;
+                const float x0 = (i >= llo && i <= lhi) ? a[i] : 0.f;
+                const float x1 = (i + 1 >= llo && i + 1 <= lhi) ? a[i + 1] : 0.f;
+                den += x0 + x1;
                 w[i / 2] = pack_bf16(x0, x1);
-                den += __uint_as_float(w[i / 2] << 16) + __uint_as_float(w[i / 2] & 0xffff0000u);
             }
+            tmem_st16(tlane + TM_A, w);
+        } else {
+            float a[16];
+            tmem_ld16(tlane + TM_A + 32, a);
+            tmem_ld_wait();
+            uint32_t w[8];
 #pragma unroll
-            for (int c8 = 0; c8 < 4; ++c8)
-                *reinterpret_cast<uint4 *>(sm + Lay::P + sw128(r, half * 4 + c8)) =
-                    make_uint4(w[c8 * 4], w[c8 * 4 + 1], w[c8 * 4 + 2], w[c8 * 4 + 3]);
+            for (int i = 0; i < 16; i += 2) {
+                const float x0 = i < nvx ? a[i] : 0.f;
+                const float x1 = i + 1 < nvx ? a[i + 1] : 0.f;
+                den += x0 + x1;
+                w[i / 2] = pack_bf16(x0, x1);
+            }
+            tmem_st8(tlane + TM_A + 16, w);
         }
-        fence_async_smem();
+
+        // ---------------- softmax pass 2: P (bf16 pairs) over the logits, in place ------
+        for (int kb = half; kb < nkb; kb += 2) {
+            float sv[32];
+            tmem_ld32(tlane + TM_S + 32 * kb, sv);
+            tmem_ld_wait();
+            const int clo = kb < P.nb ? blo - 32 * kb : 0;
+            const int chi = kb < P.nb ? bhi - 32 * kb : nvk - 1 - 32 * (kb - P.nb);
+            uint32_t w[16];
+#pragma unroll
+            for (int i = 0; i < 32; i += 2) {
+                const float p0 = (i >= clo && i <= chi) ? exp2f(fmaf(sv[i], l2s, -cm)) : 0.f;
+                const float p1 = (i + 1 >= clo && i + 1 <= chi) ? exp2f(fmaf(sv[i + 1], l2s, -cm)) : 0.f;
+                den += p0 + p1;
+                w[i / 2] = pack_bf16(p0, p1);
+            }
+            tmem_st16(tlane + TM_S + 32 * kb, w);
+        }
+        tmem_st_wait();
+        xch[half][r][0] = den;
         tc_fence_before();
         __syncthreads();
+        if (s_abort) break;
+
+        // ---------------- O = A V_lagx + sum_kb P_kb V_kb + phi(Q) S_run ---------------
         if (tid == 0) {
             tc_fence_after();
-            // O = A V_lagx (initialises O)
+            const uint64_t dVL = sdesc(sb + Lay::VLAG, 6144, 1024);
+#pragma unroll
             for (int kk = 0; kk < 32 + NX; kk += 16)
-                mma_ss(tmem + TM_O, kdesc(sb + Lay::P, kk, 16384), sdesc(sb + Lay::VLAG + kk * 128, 6144, 1024), id_o,
-                       kk > 0);
-            if (npb >= 2) mma_commit(&bar_pfree[0]);
-        }
-
-        // ---------------- softmax pass 2 + P V --------------------------------------
-        for (int p = 0; p < npb; ++p) {
-            const int ps = (p + 1) & 1;
-            if (p >= 1) wait_all(&bar_pfree[ps], ph_pfree[ps]);   // slot read by the MMA two blocks back
-            uint8_t *pdst = sm + Lay::P + ps * 16384;
-            const int kb = 2 * p + half;
-            uint32_t w[16];
-            if (kb < nkb) {
-                float sv[32];
-                tmem_ld32(tlane + TM_S + 32 * kb, sv);
-                tmem_ld_wait();
-                const int clo = kb < P.nb ? blo - 32 * kb : 0;
-                const int chi = kb < P.nb ? bhi - 32 * kb : nvk - 1 - 32 * (kb - P.nb);
-#pragma unroll
-                for (int i = 0; i < 32; i += 2) {
-                    const float p0 = (i >= clo && i <= chi) ? exp2f(fmaf(sv[i], l2s, -cm)) : 0.f;
-                    const float p1 = (i + 1 >= clo && i + 1 <= chi) ? exp2f(fmaf(sv[i + 1], l2s, -cm)) : 0.f;
-                    w[i / 2] = pack_bf16(p0, p1);
-                    den += __uint_as_float(w[i / 2] << 16) + __uint_as_float(w[i / 2] & 0xffff0000u);
-                }
-            } else {
-#pragma unroll
-                for (int i = 0; i < 16; ++i) w[i] = 0u;
-            }
-#pragma unroll
-            for (int c8 = 0; c8 < 4; ++c8)
-                *reinterpret_cast<uint4 *>(pdst + sw128(r, half * 4 + c8)) =
-                    make_uint4(w[c8 * 4], w[c8 * 4 + 1], w[c8 * 4 + 2], w[c8 * 4 + 3]);
-            fence_async_smem();
-            tc_fence_before();
-            __syncthreads();
-            if (s_abort) break;
-            if (tid == 0) {
-                const int vs = p & 1;
-                if (!mbar_wait(&bar_vfull[vs], ph_vfull[vs], P.status)) s_abort = 1;
-                ph_vfull[vs] ^= 1;
+                mma_ts(tmem + TM_O, tmem + TM_A + kk / 2, dVL + (uint64_t)(kk * 128 >> 4), id_o, kk > 0);
+            const int n1 = nkb < RING_SLOTS ? nkb : RING_SLOTS;
+            for (int kb = 0; kb < n1; ++kb) {
+                wait_slot(bar_full, ph_full, kb);
                 tc_fence_after();
-                const uint32_t vbase = sb + Lay::RING + vs * CBD * 8192;
-                for (int kk = 0; kk < 64; kk += 16)
-                    mma_ss(tmem + TM_O, kdesc(sb + Lay::P + ps * 16384, kk, 16384), sdesc(vbase + kk * 128, 8192, 1024),
-                           id_o, 1);
-                if (p + 2 < npb) {
-                    mma_commit(&bar_pfree[ps]);
-                    mma_commit(&bar_vfree[vs]);
-                }
-                // refill the V slot of block p-1 with block p+1 once its MMA is done
-                if (p >= 1 && p + 1 < npb) {
-                    const int os = (p - 1) & 1;
-                    if (!mbar_wait(&bar_vfree[os], ph_vfree[os], P.status)) s_abort = 1;
-                    ph_vfree[os] ^= 1;
-                    load_v(p + 1, nkb, band_lo);
+                mma_ts(tmem + TM_O, tmem + TM_S + 32 * kb, dVR + (uint64_t)(kb * 4096 >> 4), id_o, 1);
+                mma_ts(tmem + TM_O, tmem + TM_S + 32 * kb + 8, dVR + (uint64_t)((kb * 4096 + 2048) >> 4), id_o, 1);
+            }
+            if (nkb > RING_SLOTS) {
+                mma_commit(&bar_free[0]);
+                wait_slot(bar_free, ph_free, 0);
+                for (int kb = RING_SLOTS; kb < nkb; ++kb) load_blk(kb, t0, 1);
+                for (int kb = RING_SLOTS; kb < nkb; ++kb) {
+                    const int slot = kb - RING_SLOTS;
+                    wait_slot(bar_full, ph_full, slot);
+                    tc_fence_after();
+                    mma_ts(tmem + TM_O, tmem + TM_S + 32 * kb, dVR + (uint64_t)(slot * 4096 >> 4), id_o, 1);
+                    mma_ts(tmem + TM_O, tmem + TM_S + 32 * kb + 8, dVR + (uint64_t)((slot * 4096 + 2048) >> 4), id_o, 1);
                 }
             }
-        }
-
-        // ---------------- readout and state update MMAs ------------------------------
-        if (tid == 0 && !s_abort) {
-            tc_fence_after();
+            const uint64_t dPQ = sdesc(sb + Lay::PHIQ, 16, 1024), dSR = sdesc(sb + Lay::SRUN, DF * 128, 1024);
+#pragma unroll
             for (int k = 0; k < DF; k += 16)
-                mma_ss(tmem + TM_O, kdesc(sb + Lay::PHIQ, k, 16384), sdesc(sb + Lay::SRUN + k * 128, DF * 128, 1024),
-                       id_o, 1);
-            // dS = phi(K_lag)^T V_lag into the (now free) logit columns
+                mma_ss(tmem + TM_O, dPQ + koff(k, 16384), dSR + (uint64_t)(k * 128 >> 4), id_o, 1);
+            mma_commit(&bar_mma);
+        }
+        wait_all(&bar_mma, ph_mma);
+        tc_fence_after();
+        if (tid == 0) {
+            // dS = phi(K_lag)^T V_lag into the logit columns (every read of P is done)
             for (int kk = 0; kk < 32; kk += 16)
                 mma_ss(tmem + TM_S, sdesc(sb + Lay::PHIK + kk * 128, 6144, 1024),
                        sdesc(sb + Lay::VLAG + kk * 128, 6144, 1024), id_ds, kk > 0);
-            mma_commit(&bar_mma);
+            mma_commit(&bar_ds);
+            // the ring is free: the next tile's first K blocks
+            if (has_next)
+                for (int kb = 0; kb < nkb_of(t0 + 32) && kb < RING_SLOTS; ++kb) load_blk(kb, t0 + 32, 0);
         }
-        xch[half][r][0] = den;
-        __syncthreads();
-        if (s_abort) break;
-        wait_all(&bar_mma, ph_mma);
-        tc_fence_after();
         const float dtot = xch[0][r][0] + xch[1][r][0];
 
         // ---------------- epilogue: y = O / den (my half of the columns) ---------------
         {
             const float inv = dtot != 0.f ? 1.f / dtot : 0.f;
+            float ov[DH];
+#pragma unroll
+            for (int c0 = 0; c0 < DH; c0 += 16) tmem_ld16(tlane + TM_O + half * DH + c0, *reinterpret_cast<float(*)[16]>(ov + c0));
+            tmem_ld_wait();
 #pragma unroll
             for (int c0 = 0; c0 < DH; c0 += 16) {
-                float o[16];
-                tmem_ld16(tlane + TM_O + half * DH + c0, o);
-                tmem_ld_wait();
+                const float *o = ov + c0;
 #pragma unroll
                 for (int c8 = 0; c8 < 2; ++c8) {
                     uint4 pk;
@@ -546,15 +541,17 @@ __global__ void __launch_bounds__(256, 1) hybrid_tc_kernel(const __grid_constant
             }
         }
         // ---------------- state update: S_run += dS, z_run += sum phi(K_lag) ------------
+        wait_all(&bar_ds, ph_ds);
+        tc_fence_after();
         {
             const int f = r;
+            {
+                float ds[DH];
 #pragma unroll
-            for (int c0 = 0; c0 < DH; c0 += 16) {
-                float ds[16];
-                tmem_ld16(tlane + TM_S + half * DH + c0, ds);
+                for (int c0 = 0; c0 < DH; c0 += 16) tmem_ld16(tlane + TM_S + half * DH + c0, *reinterpret_cast<float(*)[16]>(ds + c0));
                 tmem_ld_wait();
 #pragma unroll
-                for (int i = 0; i < 16; ++i) srun[c0 + i] += ds[i];
+                for (int i = 0; i < DH; ++i) srun[i] += ds[i];
             }
             if (f < DF) {
 #pragma unroll

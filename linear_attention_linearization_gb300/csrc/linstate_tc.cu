@@ -1,0 +1,279 @@
+// Key features and per-segment linear-state sums on the tensor cores.
+//
+// "STILL: Content-Aware Intra-Layer Hybrid Attention for Efficient LLM
+// Linearization", section "NP-Map: Norm-Preserving Feature Map" (phi) and
+// section "Content-Aware Routing with Fixed Budget" (tokens that are not kept
+// are accumulated into the linear-attention recurrent state).
+//
+// CTA s of a (sequence, kv head) walks 128-key blocks of its key range:
+//   U    = K_blk Wf                          (tcgen05, TMEM)
+//   phi  = ||k|| u / ||u||, u = softmax(U)   (one thread per key row)
+//          -> the bf16 feature table (zero rows for slotted keys)
+//   dS  += phi_blk^T V_blk                   (tcgen05, accumulated in TMEM)
+//   dz  += column sums of phi_blk            (CUDA cores)
+// The range is [s*L - W, (s+1)*L - W) clipped to [0, N): the keys that leave
+// the window while segment s runs (the last segment also writes the features
+// of the final W keys).  Only keys below N - W enter dS: the others never
+// leave the window.  An exclusive scan over segments then gives each
+// segment's starting state.
+#include "sm100.cuh"
+#include "tma_host.cuh"
+
+namespace still {
+
+using namespace sm100;
+
+struct LinTCParams {
+    Dims dm;
+    SegPlan sp;
+    const uint8_t *flag;
+    uint16_t *phik;
+    float *dS;
+    float *dz;
+    int32_t *status;
+};
+
+struct LinTCMaps {
+    CUtensorMap k, v, wft;
+};
+
+template <int D, int DF>
+struct LinLayout {
+    static constexpr int CBD = D / 64, CBF = DF / 64;
+    static constexpr uint32_t WF = 0;                          // [DF rows x D]
+    static constexpr uint32_t STAGE = WF + CBD * DF * 128;     // 2 x (K [128 x D] + V [128 x D])
+    static constexpr uint32_t STAGE_BYTES = 2 * CBD * 16384;
+    static constexpr uint32_t PHI = STAGE + 2 * STAGE_BYTES;   // [128 rows x DF], always 2 blocks
+    static constexpr uint32_t TOTAL = PHI + 2 * 16384;
+};
+
+template <int D, int DF>
+__global__ void __launch_bounds__(128, 1) linstate_tc_kernel(const __grid_constant__ LinTCMaps maps, LinTCParams P)
+{
+    using Lay = LinLayout<D, DF>;
+    constexpr int CBD = Lay::CBD, CBF = Lay::CBF;
+    constexpr float LOG2E = 1.4426950408889634f;
+    constexpr int TM_U = 0, TM_DS = 128;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    const uint32_t sb = smem_u32(sm);
+    __shared__ uint64_t bar_wf, bar_full[2], bar_u, bar_ds;
+    __shared__ uint32_t tmem_base;
+    __shared__ int s_abort;
+
+    const Dims &dm = P.dm;
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const int s = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+    const size_t unit = (size_t)b * dm.Hkv + g;
+    const int klo = max(0, s * P.sp.L - dm.W);
+    const int fhi = min((s + 1) * P.sp.L, dm.N) - dm.W;                   // keys folded: [klo, fhi)
+    const int khi = s == P.sp.nseg - 1 ? dm.N : max(fhi, klo);            // features written: [klo, khi)
+    const int nblk = khi > klo ? (khi - klo + 127) / 128 : 0;
+
+    if (warp == 0) {
+        tmem_alloc(&tmem_base, 256);
+        tmem_relinquish();
+    }
+    if (tid == 0) {
+        mbar_init(&bar_wf, 1);
+        mbar_init(&bar_full[0], 1);
+        mbar_init(&bar_full[1], 1);
+        mbar_init(&bar_u, 1);
+        mbar_init(&bar_ds, 1);
+        fence_barrier_init();
+        s_abort = 0;
+    }
+    // the second feature block stays zero when d_f = 64 (it is read as padding rows of dS)
+    if (CBF == 1)
+        for (int i = tid; i < 16384 / 16; i += 128) reinterpret_cast<uint4 *>(sm + Lay::PHI + 16384)[i] = make_uint4(0, 0, 0, 0);
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_base;
+    const uint32_t tlane = tmem + ((uint32_t)(warp * 32) << 16);
+
+    auto load_blk = [&](int blk) {
+        const int st = blk & 1;
+        uint8_t *kd = sm + Lay::STAGE + st * Lay::STAGE_BYTES;
+        uint8_t *vd = kd + CBD * 16384;
+        const int j0 = klo + 128 * blk;
+        mbar_expect_tx(&bar_full[st], 2 * CBD * 16384);
+        for (int cb = 0; cb < CBD; ++cb) {
+            tma_load_3d(kd + cb * 16384, &maps.k, &bar_full[st], cb * 64, j0, (int)unit);
+            tma_load_3d(vd + cb * 16384, &maps.v, &bar_full[st], cb * 64, j0, (int)unit);
+        }
+    };
+    if (tid == 0) {
+        mbar_expect_tx(&bar_wf, CBD * DF * 128);
+        for (int cb = 0; cb < CBD; ++cb) tma_load_2d(sm + Lay::WF + cb * DF * 128, &maps.wft, &bar_wf, cb * 64, 0);
+        if (nblk > 0) load_blk(0);
+        if (nblk > 1) load_blk(1);
+    }
+    uint32_t ph_full[2] = {0, 0}, ph_u = 0, ph_ds = 0;
+    const uint32_t id_u = idesc_bf16(128, DF, 0, 0);
+    const uint32_t id_ds = idesc_bf16(128, D, 1, 1);
+    float zacc = 0.f;
+    const int r = tid;
+
+    for (int blk = 0; blk < nblk; ++blk) {
+        const int st = blk & 1;
+        const int j = klo + 128 * blk + r;
+        uint8_t *kd = sm + Lay::STAGE + st * Lay::STAGE_BYTES;
+        if (tid == 0) {
+            if (blk == 0) {
+                uint32_t ph0 = 0;
+                if (!mbar_wait(&bar_wf, ph0, P.status)) s_abort = 1;
+            }
+            if (!mbar_wait(&bar_full[st], ph_full[st], P.status)) s_abort = 1;
+            ph_full[st] ^= 1;
+            tc_fence_after();
+            const uint32_t ka = sb + Lay::STAGE + st * Lay::STAGE_BYTES;
+            for (int k = 0; k < D; k += 16)
+                mma_ss(tmem + TM_U, sdesc(ka + (k / 64) * 16384 + (k % 64) * 2, 16, 1024),
+                       sdesc(sb + Lay::WF + (k / 64) * (DF * 128) + (k % 64) * 2, 16, 1024), id_u, k > 0);
+            mma_commit(&bar_u);
+        }
+        __syncthreads();
+        if (s_abort) break;
+        // ||k|| of this row
+        float kn2 = 0.f;
+#pragma unroll
+        for (int cb = 0; cb < CBD; ++cb)
+#pragma unroll
+            for (int c8 = 0; c8 < 8; ++c8) {
+                const uint4 pk = *reinterpret_cast<const uint4 *>(kd + cb * 16384 + sw128(r, c8));
+                const uint32_t w4[4] = {pk.x, pk.y, pk.z, pk.w};
+#pragma unroll
+                for (int h2 = 0; h2 < 4; ++h2) {
+                    const float a0 = __uint_as_float(w4[h2] << 16), a1 = __uint_as_float(w4[h2] & 0xffff0000u);
+                    kn2 = fmaf(a0, a0, fmaf(a1, a1, kn2));
+                }
+            }
+        if (!mbar_wait(&bar_u, ph_u, P.status)) s_abort = 1;
+        ph_u ^= 1;
+        tc_fence_after();
+        // the previous block's dS MMA still reads the feature buffer
+        if (blk > 0) {
+            if (!mbar_wait(&bar_ds, ph_ds, P.status)) s_abort = 1;
+            ph_ds ^= 1;
+            if (tid == 0 && blk + 1 < nblk) load_blk(blk + 1);   // stage of block blk-1 is free again
+        }
+        float mu = -INFINITY, s2 = 0.f;
+#pragma unroll
+        for (int c0 = 0; c0 < DF; c0 += 32) {
+            float u[32];
+            tmem_ld32(tlane + TM_U + c0, u);
+            tmem_ld_wait();
+            float bm = -INFINITY;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) bm = fmaxf(bm, u[i] * LOG2E);
+            if (bm > mu) {
+                s2 *= exp2f(2.f * (mu - bm));
+                mu = bm;
+            }
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                const float e = exp2f(fmaf(u[i], LOG2E, -mu));
+                s2 = fmaf(e, e, s2);
+            }
+        }
+        const float sc = sqrtf(kn2) * rsqrtf(s2);
+        const bool in_range = j < khi;
+        const bool slotted = in_range && P.flag[unit * dm.N + j] != 0;
+        const bool folded = j < fhi && !slotted;
+        uint16_t *grow = P.phik + (unit * dm.N + (in_range ? j : 0)) * DF;
+#pragma unroll
+        for (int c0 = 0; c0 < DF; c0 += 32) {
+            float u[32];
+            tmem_ld32(tlane + TM_U + c0, u);
+            tmem_ld_wait();
+#pragma unroll
+            for (int c8 = 0; c8 < 4; ++c8) {
+                uint32_t w4[4];
+#pragma unroll
+                for (int h2 = 0; h2 < 4; ++h2) {
+                    const int i = c8 * 8 + h2 * 2;
+                    w4[h2] = pack_bf16(sc * exp2f(fmaf(u[i], LOG2E, -mu)), sc * exp2f(fmaf(u[i + 1], LOG2E, -mu)));
+                }
+                const int f0 = c0 + c8 * 8;
+                const uint4 val = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+                const uint4 zero = make_uint4(0, 0, 0, 0);
+                if (in_range) *reinterpret_cast<uint4 *>(grow + f0) = slotted ? zero : val;
+                *reinterpret_cast<uint4 *>(sm + Lay::PHI + (f0 / 64) * 16384 + sw128(r, (f0 % 64) / 8)) =
+                    folded ? val : zero;
+            }
+        }
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        // dz: column f of the (masked) feature block
+        if (r < DF) {
+            const int cb = r / 64, c8 = (r % 64) / 8, e = r % 8;
+            for (int row = 0; row < 128; ++row)
+                zacc += bf2f(*reinterpret_cast<const uint16_t *>(sm + Lay::PHI + cb * 16384 + sw128(row, c8) + e * 2));
+        }
+        if (tid == 0) {
+            tc_fence_after();
+            const uint32_t va = sb + Lay::STAGE + st * Lay::STAGE_BYTES + CBD * 16384;
+            for (int kk = 0; kk < 128; kk += 16)
+                mma_ss(tmem + TM_DS, sdesc(sb + Lay::PHI + kk * 128, 16384, 1024), sdesc(va + kk * 128, 16384, 1024),
+                       id_ds, (blk > 0 || kk > 0) ? 1u : 0u);
+            mma_commit(&bar_ds);
+        }
+        __syncthreads();   // zacc reads of the feature block end before it is rewritten
+    }
+    // write dS / dz of this segment
+    if (nblk > 0 && !s_abort) {
+        if (!mbar_wait(&bar_ds, ph_ds, P.status)) s_abort = 1;
+        tc_fence_after();
+    }
+    float *out = P.dS + (unit * (P.sp.nseg + 1) + s) * (size_t)(DF * D);
+    for (int c0 = 0; c0 < D; c0 += 32) {
+        float v[32];
+        tmem_ld32(tlane + TM_DS + c0, v);
+        tmem_ld_wait();
+        if (r < DF)
+            for (int i = 0; i < 32; ++i) out[(size_t)r * D + c0 + i] = nblk > 0 ? v[i] : 0.f;
+    }
+    if (r < DF) P.dz[(unit * (P.sp.nseg + 1) + s) * DF + r] = zacc;
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, 256);
+}
+
+cudaError_t launch_linstate_tc(const Dims &dm, const SegPlan &sp, const uint16_t *k, const uint16_t *v,
+                               const uint16_t *wft, const uint8_t *flag, uint16_t *phik, float *dS, float *dz,
+                               int32_t *status, cudaStream_t s)
+{
+    KTimer tm("features_linstate", s);
+    LinTCMaps m;
+    const int D = dm.d, DF = dm.df;
+    const uint64_t units = (uint64_t)dm.B * dm.Hkv;
+    uint64_t dk[3] = {(uint64_t)D, (uint64_t)dm.N, units}, sk[2] = {(uint64_t)D * 2, (uint64_t)D * 2 * dm.N};
+    uint32_t box[3] = {64, 128, 1};
+    bool ok = make_tma_map(&m.k, k, 3, dk, sk, box, true) && make_tma_map(&m.v, v, 3, dk, sk, box, true);
+    uint64_t dw[2] = {(uint64_t)D, (uint64_t)DF}, sw[1] = {(uint64_t)D * 2};
+    uint32_t boxw[2] = {64, (uint32_t)DF};
+    ok = ok && make_tma_map(&m.wft, wft, 2, dw, sw, boxw, true);
+    if (!ok) return cudaErrorInvalidValue;
+    LinTCParams p{dm, sp, flag, phik, dS, dz, status};
+    dim3 grid(sp.nseg, dm.Hkv, dm.B);
+    cudaError_t e;
+#define STILL_LIN(DD, FF)                                                                                     \
+    {                                                                                                         \
+        const size_t smem = LinLayout<DD, FF>::TOTAL + 1024;                                                  \
+        e = cudaFuncSetAttribute(linstate_tc_kernel<DD, FF>, cudaFuncAttributeMaxDynamicSharedMemorySize,     \
+                                 (int)smem);                                                                  \
+        if (e != cudaSuccess) return e;                                                                       \
+        linstate_tc_kernel<DD, FF><<<grid, 128, smem, s>>>(m, p);                                            \
+    }
+    if (D == 64 && DF == 64) STILL_LIN(64, 64)
+    else if (D == 64) STILL_LIN(64, 128)
+    else if (DF == 64) STILL_LIN(128, 64)
+    else STILL_LIN(128, 128)
+#undef STILL_LIN
+    return cudaGetLastError();
+}
+
+}  // namespace still
