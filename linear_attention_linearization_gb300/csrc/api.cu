@@ -115,7 +115,7 @@ SegPlan plan_segments(const Dims &dm)
 }
 
 struct WsLayout {
-    size_t status, scores, fsel, flag, phik, kk, vk, phk, wft, dS, dz, total;
+    size_t status, scores, fsel, kslot, phik, kk, vk, phk, wft, dS, dz, total;
     size_t kept_bytes;
 };
 
@@ -130,7 +130,7 @@ WsLayout ws_layout(const Dims &dm, const SegPlan &sp)
     L.status = o; o += al(256);
     L.scores = o; o += al(units * dm.N * 4);
     L.fsel = o; o += al(units * KP * 4);
-    L.flag = o; o += al(units * dm.N);
+    L.kslot = o; o += al(units * dm.N * 4);
     L.phik = o; o += al(units * dm.N * (size_t)dm.df * 2);
     L.kk = o; o += al(units * KP * dm.d * 2);
     L.vk = o; o += al(units * KP * dm.d * 2);
@@ -261,7 +261,7 @@ still_status still_prefill(const still_shape *shape, const still_bf16 *q, const 
     int32_t *status = (int32_t *)(base + L.status);
     float *scores = (float *)(base + L.scores);
     int32_t *fsel = (int32_t *)(base + L.fsel);
-    uint8_t *flag = (uint8_t *)(base + L.flag);
+    int32_t *kslot = (int32_t *)(base + L.kslot);
     uint16_t *phik = (uint16_t *)(base + L.phik);
     uint16_t *kk = (uint16_t *)(base + L.kk);
     uint16_t *vk = (uint16_t *)(base + L.vk);
@@ -271,13 +271,13 @@ still_status still_prefill(const still_shape *shape, const still_bf16 *q, const 
     float *dz = (float *)(base + L.dz);
     const bool tc = hybrid_tc_supported(dm);
     cudaError_t e = cudaMemsetAsync(base, 0, L.status + 256, s);
-    if (e == cudaSuccess) e = cudaMemsetAsync(flag, 0, (size_t)dm.B * dm.Hkv * dm.N, s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(kslot, 0xff, (size_t)dm.B * dm.Hkv * dm.N * 4, s);
     if (e == cudaSuccess) e = cudaMemsetAsync(kk, 0, L.kept_bytes, s);
     if (e == cudaSuccess && dm.lam > 0)
         e = score_tc_supported(dm) ? launch_score_tc(dm, q, k, scores, s) : launch_score(dm, q, k, scores, s);
-    if (e == cudaSuccess && dm.lam > 0) e = launch_select(dm, scores, sel_idx, fsel, flag, s);
-    if (e == cudaSuccess) e = launch_kept(dm, k, v, Wf, fsel, kk, vk, phk, wft, s);
-    if (e == cudaSuccess) e = launch_linstate_tc(dm, sp, k, v, wft, flag, phik, dS, dz, status, s);
+    if (e == cudaSuccess && dm.lam > 0) e = launch_select(dm, scores, sel_idx, fsel, kslot, s, k, v, kk, vk);
+    if (e == cudaSuccess) e = launch_wft(dm, Wf, wft, s);
+    if (e == cudaSuccess) e = launch_linstate_tc(dm, sp, k, v, wft, kslot, phik, phk, dS, dz, status, s);
     if (e == cudaSuccess) e = launch_scan(dm, sp, dS, dz, s);
     if (e == cudaSuccess) {
         if (tc) {

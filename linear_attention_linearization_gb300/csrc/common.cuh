@@ -139,15 +139,15 @@ struct KTimer {
 cudaError_t launch_score(const Dims &dm, const uint16_t *q, const uint16_t *k, float *scores, cudaStream_t s);
 bool score_tc_supported(const Dims &dm);
 cudaError_t launch_score_tc(const Dims &dm, const uint16_t *q, const uint16_t *k, float *scores, cudaStream_t s);
-cudaError_t launch_select(const Dims &dm, const float *scores, int32_t *sel_idx, int32_t *fsel, uint8_t *flag,
-                          cudaStream_t s);
+cudaError_t launch_select(const Dims &dm, const float *scores, int32_t *sel_idx, int32_t *fsel, int32_t *kslot,
+                          cudaStream_t s, const uint16_t *k = nullptr, const uint16_t *v = nullptr,
+                          uint16_t *kk = nullptr, uint16_t *vk = nullptr);
 cudaError_t launch_npmap(const uint16_t *x, long long rows, int d, const float *Wf, int df, float *phi,
                          cudaStream_t s);
-cudaError_t launch_kept(const Dims &dm, const uint16_t *k, const uint16_t *v, const float *Wf, const int32_t *fsel,
-                        uint16_t *kk, uint16_t *vk, uint16_t *phk, uint16_t *wft, cudaStream_t s);
+cudaError_t launch_wft(const Dims &dm, const float *Wf, uint16_t *wft, cudaStream_t s);
 cudaError_t launch_linstate_tc(const Dims &dm, const SegPlan &sp, const uint16_t *k, const uint16_t *v,
-                               const uint16_t *wft, const uint8_t *flag, uint16_t *phik, float *dS, float *dz,
-                               int32_t *status, cudaStream_t s);
+                               const uint16_t *wft, const int32_t *kslot, uint16_t *phik, uint16_t *phk, float *dS,
+                               float *dz, int32_t *status, cudaStream_t s);
 cudaError_t launch_scan(const Dims &dm, const SegPlan &sp, float *dS, float *dz, cudaStream_t s);
 cudaError_t launch_hybrid_general(const Dims &dm, const SegPlan &sp, const uint16_t *q, const uint16_t *k,
                                   const uint16_t *v, const float *Wf, const uint16_t *phik, const uint16_t *phkept,

@@ -8,7 +8,9 @@
 // CTA s of a (sequence, kv head) walks 128-key blocks of its key range:
 //   U    = K_blk Wf                          (tcgen05, TMEM)
 //   phi  = ||k|| u / ||u||, u = softmax(U)   (one thread per key row)
-//          -> the bf16 feature table (zero rows for slotted keys)
+//          -> the bf16 feature table (zero rows for slotted keys); a kept key
+//             also gets its unmasked phi in the kept table (the selection
+//             kernel copies its K and V rows there)
 //   dS  += phi_blk^T V_blk                   (tcgen05, accumulated in TMEM)
 //   dz  += column sums of phi_blk            (CUDA cores)
 // The range is [s*L - W, (s+1)*L - W) clipped to [0, N): the keys that leave
@@ -26,8 +28,8 @@ using namespace sm100;
 struct LinTCParams {
     Dims dm;
     SegPlan sp;
-    const uint8_t *flag;
-    uint16_t *phik;
+    const int32_t *kslot;   // per key: row of the kept tables, -1 when the key is in no budget slot
+    uint16_t *phik, *phk;
     float *dS;
     float *dz;
     int32_t *status;
@@ -180,7 +182,10 @@ __global__ void __launch_bounds__(128, 1) linstate_tc_kernel(const __grid_consta
         }
         const float sc = sqrtf(kn2) * rsqrtf(s2);
         const bool in_range = j < khi;
-        const bool slotted = in_range && P.flag[unit * dm.N + j] != 0;
+        const int kslot = in_range ? P.kslot[unit * dm.N + j] : -1;
+        const bool slotted = kslot >= 0;
+        const int KP = dm.T_max * dm.lam;
+        uint16_t *krow = slotted ? P.phk + (unit * KP + kslot) * DF : nullptr;
         const bool folded = j < fhi && !slotted;
         uint16_t *grow = P.phik + (unit * dm.N + (in_range ? j : 0)) * DF;
 #pragma unroll
@@ -200,6 +205,7 @@ __global__ void __launch_bounds__(128, 1) linstate_tc_kernel(const __grid_consta
                 const uint4 val = make_uint4(w4[0], w4[1], w4[2], w4[3]);
                 const uint4 zero = make_uint4(0, 0, 0, 0);
                 if (in_range) *reinterpret_cast<uint4 *>(grow + f0) = slotted ? zero : val;
+                if (slotted) *reinterpret_cast<uint4 *>(krow + f0) = val;   // kept: unmasked features
                 *reinterpret_cast<uint4 *>(sm + Lay::PHI + (f0 / 64) * 16384 + sw128(r, (f0 % 64) / 8)) =
                     folded ? val : zero;
             }
@@ -243,8 +249,8 @@ __global__ void __launch_bounds__(128, 1) linstate_tc_kernel(const __grid_consta
 }
 
 cudaError_t launch_linstate_tc(const Dims &dm, const SegPlan &sp, const uint16_t *k, const uint16_t *v,
-                               const uint16_t *wft, const uint8_t *flag, uint16_t *phik, float *dS, float *dz,
-                               int32_t *status, cudaStream_t s)
+                               const uint16_t *wft, const int32_t *kslot, uint16_t *phik, uint16_t *phk, float *dS,
+                               float *dz, int32_t *status, cudaStream_t s)
 {
     KTimer tm("features_linstate", s);
     LinTCMaps m;
@@ -257,7 +263,7 @@ cudaError_t launch_linstate_tc(const Dims &dm, const SegPlan &sp, const uint16_t
     uint32_t boxw[2] = {64, (uint32_t)DF};
     ok = ok && make_tma_map(&m.wft, wft, 2, dw, sw, boxw, true);
     if (!ok) return cudaErrorInvalidValue;
-    LinTCParams p{dm, sp, flag, phik, dS, dz, status};
+    LinTCParams p{dm, sp, kslot, phik, phk, dS, dz, status};
     dim3 grid(sp.nseg, dm.Hkv, dm.B);
     cudaError_t e;
 #define STILL_LIN(DD, FF)                                                                                     \

@@ -75,11 +75,15 @@ cudaError_t launch_score(const Dims &dm, const uint16_t *q, const uint16_t *k, f
 // a warp-wide arg-max under outranks(); winners are then written in ascending
 // position by a ballot compaction.  The unfinished tail chunk (when < T_max)
 // is ranked too: its current top-lambda goes to `fsel` (the internal table of
-// tokens kept out of the linear state) but not to the public sel_idx.
+// tokens kept out of the linear state) but not to the public sel_idx.  `kslot`
+// maps each such token to its row c*lambda + r of that table, and the token's
+// K and V rows are copied to the same row of the kept tables.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(32) select_kernel(const float *__restrict__ scores, Dims dm,
                                                     int32_t *__restrict__ sel_idx, int32_t *__restrict__ fsel,
-                                                    uint8_t *__restrict__ flag)
+                                                    int32_t *__restrict__ kslot, const uint16_t *__restrict__ k,
+                                                    const uint16_t *__restrict__ v, uint16_t *__restrict__ kk,
+                                                    uint16_t *__restrict__ vk)
 {
     extern __shared__ float sel_smem[];
     float *sc = sel_smem;
@@ -135,7 +139,7 @@ __global__ void __launch_bounds__(32) select_kernel(const float *__restrict__ sc
             const int p = outn + __popc(mask & ((1u << lane) - 1u));
             if (fsel) fsel[row + p] = base + i;
             if (sel_idx) sel_idx[row + p] = complete ? base + i : -1;
-            if (flag) flag[(size_t)(b * dm.Hkv + g) * dm.N + base + i] = 1;
+            if (kslot) kslot[(size_t)(b * dm.Hkv + g) * dm.N + base + i] = c * dm.lam + p;
         }
         outn += __popc(mask);
     }
@@ -145,10 +149,27 @@ __global__ void __launch_bounds__(32) select_kernel(const float *__restrict__ sc
     }
     if (!complete && sel_idx)
         for (int r = lane; r < outn; r += 32) sel_idx[row + r] = -1;
+    // K and V rows of the kept tokens into the kept tables (row c*lambda + r)
+    if (kk) {
+        __syncwarp();
+        const size_t ug = (size_t)b * dm.Hkv + g;
+        const int words = dm.d / 4;   // 8-byte words per row
+        for (int p = 0; p < outn; ++p) {
+            const int j = fsel[row + p];
+            const uint2 *ks = reinterpret_cast<const uint2 *>(k + (ug * dm.N + j) * dm.d);
+            const uint2 *vs = reinterpret_cast<const uint2 *>(v + (ug * dm.N + j) * dm.d);
+            uint2 *kd = reinterpret_cast<uint2 *>(kk + (row + p) * dm.d);
+            uint2 *vd = reinterpret_cast<uint2 *>(vk + (row + p) * dm.d);
+            for (int x = lane; x < words; x += 32) {
+                kd[x] = ks[x];
+                vd[x] = vs[x];
+            }
+        }
+    }
 }
 
-cudaError_t launch_select(const Dims &dm, const float *scores, int32_t *sel_idx, int32_t *fsel, uint8_t *flag,
-                          cudaStream_t s)
+cudaError_t launch_select(const Dims &dm, const float *scores, int32_t *sel_idx, int32_t *fsel, int32_t *kslot,
+                          cudaStream_t s, const uint16_t *k, const uint16_t *v, uint16_t *kk, uint16_t *vk)
 {
     if (dm.lam <= 0) return cudaSuccess;
     KTimer tm("select", s);
@@ -158,7 +179,7 @@ cudaError_t launch_select(const Dims &dm, const float *scores, int32_t *sel_idx,
         if (e != cudaSuccess) return e;
     }
     dim3 grid(dm.T_max, dm.Hkv, dm.B);
-    select_kernel<<<grid, 32, smem, s>>>(scores, dm, sel_idx, fsel, flag);
+    select_kernel<<<grid, 32, smem, s>>>(scores, dm, sel_idx, fsel, kslot, k, v, kk, vk);
     return cudaGetLastError();
 }
 

@@ -11,8 +11,9 @@
 // band of keys [t0 - Wr, t0 + 32) that holds every window of the tile.  The
 // logits stay in TMEM; 8 warps (two per TMEM lane quarter, each owning half of
 // the band columns) reduce each row to (max, off-diagonal mass, self mass).
-// Tiles are double-buffered: while the row warps reduce tile i, the MMA of
-// tile i+1 runs and the loads of tile i+2 are in flight.
+// Tiles are pipelined over up to four shared-memory / TMEM stages: while the
+// row warps reduce tile i, the MMA of tile i+1 runs and the loads of the
+// following tiles are in flight.
 #include "sm100.cuh"
 #include "tma_host.cuh"
 
@@ -21,14 +22,17 @@ namespace still {
 using namespace sm100;
 
 namespace {
-constexpr int SC_STAGE_COLS = 256;   // TMEM columns per stage
 constexpr int SC_MAX_NB = 8;         // band blocks of 32 keys (W <= 225)
+constexpr int SC_MAX_STAGES = 4;     // tiles in flight
+constexpr size_t SC_SMEM_CAP = 227 * 1024 - 4096;   // dynamic share of the 227 KB per-block limit
 }
 
 struct ScoreTCParams {
     Dims dm;
     int Wr, nb;        // band [t0 - Wr, t0 + 32), nb blocks of 32 keys
     int tiles_per_unit, total_tiles;
+    int stages;        // tiles in flight (shared-memory and TMEM stages)
+    uint32_t stage_bytes, tmem_stride;
     float *scores;
 };
 
@@ -40,18 +44,19 @@ template <int D>
 __global__ void __launch_bounds__(256, 1) score_tc_kernel(const __grid_constant__ ScoreTCMaps maps, ScoreTCParams P)
 {
     constexpr int CBD = D / 64;
-    constexpr uint32_t QB = CBD * 16384;               // Q tile bytes
-    constexpr uint32_t KB = SC_MAX_NB * 32 * D * 2;   // band bytes (max)
+    constexpr uint32_t QB = CBD * 16384;          // Q tile bytes
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     const uint32_t sb = smem_u32(sm);
-    __shared__ uint64_t bar_full[2], bar_mma[2];
+    __shared__ uint64_t bar_full[SC_MAX_STAGES], bar_mma[SC_MAX_STAGES];
     __shared__ uint32_t tmem_base;
     __shared__ float xch[2][128][3];
     __shared__ float hsc[4][32];
     __shared__ int s_abort;
 
     const Dims &dm = P.dm;
+    const int NS = P.stages;
+    const uint32_t STB = P.stage_bytes, KBB = P.nb * 4096;   // bytes of a stage, of one K column block
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int quarter = warp & 3, half = warp >> 2;
     const int r = quarter * 32 + lane, hh = r / 32, tt = r % 32;
@@ -64,15 +69,15 @@ __global__ void __launch_bounds__(256, 1) score_tc_kernel(const __grid_constant_
         tmem_relinquish();
     }
     if (tid == 0) {
-        for (int i = 0; i < 2; ++i) { mbar_init(&bar_full[i], 1); mbar_init(&bar_mma[i], 1); }
+        for (int i = 0; i < NS; ++i) { mbar_init(&bar_full[i], 1); mbar_init(&bar_mma[i], 1); }
         fence_barrier_init();
         s_abort = 0;
     }
-    // padding rows of absent heads: zero in both stage buffers, never written again
-    for (int st = 0; st < 2; ++st)
+    // padding rows of absent heads: zero in every stage buffer, never written again
+    for (int st = 0; st < NS; ++st)
         for (int i = tid; i < (int)(QB / 16); i += 256) {
             const int row = (i * 16 % 16384) / 128;
-            if (row >= dm.G * 32) reinterpret_cast<uint4 *>(sm + st * (QB + KB))[i] = make_uint4(0, 0, 0, 0);
+            if (row >= dm.G * 32) reinterpret_cast<uint4 *>(sm + st * STB)[i] = make_uint4(0, 0, 0, 0);
         }
     fence_async_smem();
     tc_fence_before();
@@ -84,6 +89,7 @@ __global__ void __launch_bounds__(256, 1) score_tc_kernel(const __grid_constant_
     const int first = blockIdx.x, step = gridDim.x;
     const int my_tiles = first < P.total_tiles ? (P.total_tiles - first + step - 1) / step : 0;
     const uint32_t idesc = idesc_bf16(128, ncols, 0, 0);
+    const uint64_t d0 = sdesc(sb, 16, 1024);
 
     auto tile_coords = [&](int i, int &unit, int &t0) {
         const int tile = first + i * step;
@@ -93,8 +99,8 @@ __global__ void __launch_bounds__(256, 1) score_tc_kernel(const __grid_constant_
     auto issue_load = [&](int i) {
         int unit, t0;
         tile_coords(i, unit, t0);
-        const int st = i & 1;
-        uint8_t *qd = sm + st * (QB + KB);
+        const int st = i % NS;
+        uint8_t *qd = sm + st * STB;
         uint8_t *kd = qd + QB;
         const int b = unit / dm.Hkv, g = unit % dm.Hkv;
         mbar_expect_tx(&bar_full[st], dm.G * CBD * 4096 + P.nb * CBD * 4096);
@@ -103,34 +109,33 @@ __global__ void __launch_bounds__(256, 1) score_tc_kernel(const __grid_constant_
                 tma_load_3d(qd + cb * 16384 + h * 4096, &maps.q, &bar_full[st], cb * 64, t0, b * dm.Hq + g * dm.G + h);
         for (int kb = 0; kb < P.nb; ++kb)
             for (int cb = 0; cb < CBD; ++cb)
-                tma_load_3d(kd + cb * (P.nb * 4096) + kb * 4096, &maps.k, &bar_full[st], cb * 64,
-                            t0 - P.Wr + 32 * kb, unit);
+                tma_load_3d(kd + cb * KBB + kb * 4096, &maps.k, &bar_full[st], cb * 64, t0 - P.Wr + 32 * kb, unit);
     };
-    uint32_t ph_full[2] = {0, 0}, ph_mma[2] = {0, 0};
+    uint32_t ph_full = 0, ph_mma = 0;   // one parity bit per stage
     auto issue_mma = [&](int i) {
-        const int st = i & 1;
-        if (!mbar_wait(&bar_full[st], ph_full[st], nullptr)) { s_abort = 1; return; }
-        ph_full[st] ^= 1;
+        const int st = i % NS;
+        if (!mbar_wait(&bar_full[st], (ph_full >> st) & 1u, nullptr)) { s_abort = 1; return; }
+        ph_full ^= 1u << st;
         tc_fence_after();
-        const uint32_t qa = sb + st * (QB + KB), ka = qa + QB;
+        const uint64_t qa = d0 + ((st * STB) >> 4), ka = qa + (QB >> 4);
+#pragma unroll
         for (int k = 0; k < D; k += 16)
-            mma_ss(tmem + st * SC_STAGE_COLS, sdesc(qa + (k / 64) * 16384 + (k % 64) * 2, 16, 1024),
-                   sdesc(ka + (k / 64) * (P.nb * 4096) + (k % 64) * 2, 16, 1024), idesc, k > 0);
+            mma_ss(tmem + st * P.tmem_stride, qa + (((k / 64) * 16384 + (k % 64) * 2) >> 4),
+                   ka + (((k / 64) * KBB + (k % 64) * 2) >> 4), idesc, k > 0);
         mma_commit(&bar_mma[st]);
     };
 
     if (tid == 0) {
-        if (my_tiles > 0) issue_load(0);
-        if (my_tiles > 1) issue_load(1);
+        for (int i = 0; i < NS && i < my_tiles; ++i) issue_load(i);
         if (my_tiles > 0) issue_mma(0);
     }
     for (int i = 0; i < my_tiles; ++i) {
-        const int st = i & 1;
+        const int st = i % NS;
         int unit, t0;
         tile_coords(i, unit, t0);
         if (tid == 0 && i + 1 < my_tiles && !s_abort) issue_mma(i + 1);
-        if (!mbar_wait(&bar_mma[st], ph_mma[st], nullptr)) s_abort = 1;
-        ph_mma[st] ^= 1;
+        if (!mbar_wait(&bar_mma[st], (ph_mma >> st) & 1u, nullptr)) s_abort = 1;
+        ph_mma ^= 1u << st;
         tc_fence_after();
 
         // row statistics over this thread's half of the band columns
@@ -142,7 +147,7 @@ __global__ void __launch_bounds__(256, 1) score_tc_kernel(const __grid_constant_
         float m = -INFINITY, oth = 0.f, slf = 0.f;
         for (int c0 = 0; c0 < hcols; c0 += 16) {
             float v[16];
-            tmem_ld16(tlane + st * SC_STAGE_COLS + c_beg + c0, v);
+            tmem_ld16(tlane + st * P.tmem_stride + c_beg + c0, v);
             tmem_ld_wait();
             float bm = -INFINITY;
 #pragma unroll
@@ -171,16 +176,17 @@ __global__ void __launch_bounds__(256, 1) score_tc_kernel(const __grid_constant_
         xch[half][r][2] = slf;
         tc_fence_before();
         __syncthreads();
+        if (s_abort) break;
         if (half == 0) {
             const float m1 = xch[1][r][0];
             const float M = fmaxf(m, m1);
-            float o = 0.f, s = 0.f;
+            float o = 0.f, sl = 0.f;
             if (M != -INFINITY) {
                 const float f0 = m == -INFINITY ? 0.f : exp2f(m - M), f1 = m1 == -INFINITY ? 0.f : exp2f(m1 - M);
                 o = oth * f0 + xch[1][r][1] * f1;
-                s = slf * f0 + xch[1][r][2] * f1;
+                sl = slf * f0 + xch[1][r][2] * f1;
             }
-            hsc[hh][tt] = (hh < dm.G && t < dm.N) ? saliency_from_stats(o, s) : 0.f;
+            hsc[hh][tt] = (hh < dm.G && t < dm.N) ? saliency_from_stats(o, sl) : 0.f;
         }
         __syncthreads();
         if (tid < 32 && t0 + tid < dm.N) {
@@ -188,9 +194,8 @@ __global__ void __launch_bounds__(256, 1) score_tc_kernel(const __grid_constant_
             for (int h = 0; h < dm.G; ++h) a += hsc[h][tid];
             P.scores[(size_t)unit * dm.N + t0 + tid] = a / dm.G;
         }
-        // stage st is free again: load tile i+2 into it
-        if (tid == 0 && i + 2 < my_tiles && !s_abort) issue_load(i + 2);
-        if (s_abort) break;
+        // stage st is free again: load tile i + NS into it
+        if (tid == 0 && i + NS < my_tiles && !s_abort) issue_load(i + NS);
     }
     tc_fence_before();
     __syncthreads();
@@ -225,11 +230,18 @@ cudaError_t launch_score_tc(const Dims &dm, const uint16_t *q, const uint16_t *k
     p.tiles_per_unit = (dm.N + 31) / 32;
     p.total_tiles = p.tiles_per_unit * dm.B * dm.Hkv;
     p.scores = scores;
+    const uint32_t qb = (uint32_t)(D / 64) * 16384, kbytes = (uint32_t)p.nb * 32 * D * 2;
+    p.stage_bytes = (qb + kbytes + 1023) & ~1023u;
+    p.tmem_stride = p.nb * 32 <= 128 ? 128 : 256;
+    int ns = (int)((SC_SMEM_CAP - 1024) / p.stage_bytes);
+    if (ns > SC_MAX_STAGES) ns = SC_MAX_STAGES;
+    if (ns > (int)(512 / p.tmem_stride)) ns = 512 / p.tmem_stride;
+    p.stages = ns;
     int dev = 0, nsm = 152;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
     const int grid = p.total_tiles < nsm ? p.total_tiles : nsm;
-    const size_t smem = 2 * ((size_t)(D / 64) * 16384 + (size_t)SC_MAX_NB * 32 * D * 2) + 1024;
+    const size_t smem = (size_t)ns * p.stage_bytes + 1024;
     cudaError_t e;
     if (D == 64) {
         e = cudaFuncSetAttribute(score_tc_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
