@@ -71,6 +71,23 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int32_
     return true;
 }
 
+// As mbar_wait, for long waits of whole blocks: the waiting threads back off
+// between polls so that they leave the issue slots to co-resident blocks.
+__device__ __forceinline__ bool mbar_wait_sleep(uint64_t *bar, uint32_t parity, int32_t *status,
+                                                long long limit_cycles = 4000000000LL)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    while (!mbar_try_wait(bar, parity)) {
+        __nanosleep(200);
+        if (clock64() - t0 > limit_cycles) {
+            set_status(status, STILL_ERR_TIMEOUT);
+            return false;
+        }
+    }
+    return true;
+}
+
 // ---- proxy fences ------------------------------------------------------------------
 // Generic-proxy writes to shared memory (st.shared) made visible to the async
 // proxy (tensor core operand reads, TMA stores).
@@ -98,6 +115,15 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, u
             smem_u32(dst)),
         "l"(map), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z)
         : "memory");
+}
+
+// Bulk copy of `bytes` (multiple of 16, 16-byte aligned ends) global -> shared.
+__device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_u32(dst)),
+                 "l"(src), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
 }
 
 __device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, const void *src, int x, int y, int z)
