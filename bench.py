@@ -110,7 +110,9 @@ def profile_traffic(kernel):
     path = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
     if not os.path.exists(path):
         return None
-    src_of = {"hybrid_attn": "hybrid.cu", "score": "score_select.cu", "linstate": "linstate.cu"}
+    src_of = {"hybrid_attn": "hybrid_tc.cu", "score": "score_tc.cu", "select": "score_select.cu",
+              "wf_transpose": "features.cu", "features_linstate": "linstate_tc.cu", "scan": "linstate.cu",
+              "decode_step": "decode.cu"}
     f = src_of.get(kernel)
     if not f:
         return None
