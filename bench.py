@@ -35,7 +35,7 @@ L2_BYTES = 129 * 1024 * 1024
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
-def parse():
+def parse(argv=None):
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
     p.add_argument("--steps", type=int, default=50)
@@ -46,7 +46,7 @@ def parse():
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--cpu-tokens", type=int, default=16384, help="tokens of the CPU-baseline sample")
     p.add_argument("--seed", type=int, default=0)
-    return p.parse_args()
+    return p.parse_args(argv)
 
 
 def peaks():
@@ -233,6 +233,15 @@ def reduce_max(pg, x, device):
     return float(t.item())
 
 
+def aggregate(pg, seconds, tokens_per_rank, steps, device):
+    """Whole-job throughput of `steps` timed steps: every rank processes
+    `tokens_per_rank` tokens per step; the job takes as long as its slowest
+    rank.  Returns (tokens/s over all ranks, ms per step, slowest seconds)."""
+    world = pg.get_world_size() if pg is not None else 1
+    t_max = reduce_max(pg, seconds, device)
+    return world * tokens_per_rank * steps / t_max, 1e3 * t_max / steps, t_max
+
+
 def run_reference(args):
     world, rank, local, pg = dist_setup()
     if rank != 0:
@@ -308,10 +317,7 @@ def run_ours(args):
     ktimes = still.timing_read()
     step_ms = [a.elapsed_time(b) for a, b in ev]
     t_total = sum(step_ms) / 1e3
-    t_max = reduce_max(pg, t_total, dev)
-    tokens_all = world * w.B * w.N * args.steps
-    value = tokens_all / t_max
-    ms_per_step = 1e3 * t_max / args.steps
+    value, ms_per_step, t_max = aggregate(pg, t_total, w.B * w.N, args.steps, dev)
 
     # -------- roofline of the dominant kernel --------
     pk, pk_kind = peaks()
@@ -382,8 +388,8 @@ def run_ours(args):
             e2e_step()
         b.record(stream)
         torch.cuda.synchronize(dev)
-        t_e2e = reduce_max(pg, a.elapsed_time(b) / 1e3, dev)
-        line["e2e"] = {"value": world * w.B * w.N * n_e2e / t_e2e, "unit": "tokens/s",
+        v_e2e, _, _ = aggregate(pg, a.elapsed_time(b) / 1e3, w.B * w.N, n_e2e, dev)
+        line["e2e"] = {"value": v_e2e, "unit": "tokens/s",
                        "h2d_bytes_per_step": int(hq.numel() * 2 + hk.numel() * 2 + hv.numel() * 2),
                        "d2h_bytes_per_step": int(hout.numel() * 2 + hsel.numel() * 4), "steps": n_e2e}
 

@@ -1,0 +1,84 @@
+"""Multi-rank host logic of bench.py on CPU: two gloo ranks.
+
+The bench runs one replica of the prefill per GPU (the path has no exchange
+step); the job's throughput counts every rank's tokens over the slowest
+rank's time, and the reference arm runs on rank 0 only."""
+import io
+import json
+import os
+import socket
+import sys
+import contextlib
+
+import pytest
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _env(rank, world, port):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world),
+                      LOCAL_RANK=str(rank))
+    sys.path.insert(0, ROOT)
+
+
+def _aggregate_worker(rank, world, port, q):
+    _env(rank, world, port)
+    import bench
+    import torch.distributed as dist
+    w, r, _, pg = bench.dist_setup()
+    assert (w, r) == (world, rank) and pg is not None
+    seconds = [1.0, 2.5][rank]
+    q.put((rank, bench.aggregate(pg, seconds, tokens_per_rank=1000, steps=4, device="cpu")))
+    dist.destroy_process_group()
+
+
+def _reference_worker(rank, world, port, q):
+    _env(rank, world, port)
+    import bench
+    import torch.distributed as dist
+    args = bench.parse(["--impl", "reference", "--steps", "1", "--warmup", "0", "--gpus", str(world)])
+    buf = io.StringIO()
+    with contextlib.redirect_stdout(buf):
+        bench.run_reference(args)
+    q.put((rank, buf.getvalue()))
+    if dist.is_initialized():
+        dist.destroy_process_group()
+
+
+def _run(target, world=2):
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=target, args=(r, world, port, q)) for r in range(world)]
+    for p in procs:
+        p.start()
+    out = dict(q.get(timeout=600) for _ in procs)
+    for p in procs:
+        p.join(timeout=120)
+        assert p.exitcode == 0
+    return out
+
+
+def test_aggregate_counts_all_ranks_over_slowest():
+    out = _run(_aggregate_worker)
+    for rank in (0, 1):
+        value, ms_per_step, t_max = out[rank]
+        assert t_max == 2.5
+        assert value == pytest.approx(2 * 1000 * 4 / 2.5)
+        assert ms_per_step == pytest.approx(2500.0 / 4)
+
+
+def test_reference_arm_runs_on_rank_zero_only():
+    out = _run(_reference_worker)
+    assert out[1] == ""
+    line = json.loads(out[0].strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["n_gpus"] == 2
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["value"] > 0
+    assert line["e2e"]["h2d_bytes_per_step"] == 0
