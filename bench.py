@@ -101,7 +101,7 @@ def kernel_bytes(w):
     q = 2.0 * B * Hq * N * d
     kv = 2.0 * B * Hkv * N * d
     return {"hybrid_attn": 2 * q + 2 * kv, "score": q + kv + 4.0 * B * Hkv * N,
-            "linstate": 2 * kv, "select": 4.0 * B * Hkv * N, "scan": 0.0}
+            "features_linstate": 2 * kv, "select": 4.0 * B * Hkv * N, "scan": 0.0}
 
 
 def profile_traffic(kernel):
