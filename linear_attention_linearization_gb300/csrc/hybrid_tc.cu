@@ -53,11 +53,11 @@ struct TCMaps {
     CUtensorMap q, k, v, kk, vk, vk16, phik, phk16, wft, out;
 };
 
-constexpr int TM_S = 0, TM_O = 320, TM_A = 448, TM_COLS = 512;
+constexpr int TM_S = 0, TM_O = 320, TM_A = 448, TM_X = 496, TM_COLS = 512;   // TM_X: row exchange
 constexpr int MAX_KEY_BLOCKS = 10;   // 320 logit columns
 constexpr int NX = 16;               // extra (kept, own chunk) rows per tile
 
-constexpr int RING_SLOTS = 8;        // K (then V) blocks of 32 keys in flight
+constexpr int RING_SLOTS = 9;        // K (then V) blocks of 32 keys in flight
 
 template <int D, int DF>
 struct TCLayout {
@@ -70,8 +70,7 @@ struct TCLayout {
     static constexpr uint32_t RSTRIDE = RING_SLOTS * 4096;     // bytes between the column-block regions
     static constexpr uint32_t PHIK = RING + CBD * RSTRIDE;
     static constexpr uint32_t VLAG = PHIK + CBF * 6144;
-    static constexpr uint32_t KPOS = VLAG + CBD * 6144;          // int32[MAX_KEY_BLOCKS * 32]
-    static constexpr uint32_t XPOS = KPOS + MAX_KEY_BLOCKS * 32 * 4;
+    static constexpr uint32_t XPOS = VLAG + CBD * 6144;
     static constexpr uint32_t ZRUN = XPOS + NX * 4;
     static constexpr uint32_t TOTAL = ZRUN + DF * 4;
 };
@@ -88,14 +87,13 @@ __global__ void __launch_bounds__(256, 1) hybrid_tc_kernel(const __grid_constant
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     const uint32_t sb = smem_u32(sm);
-    int32_t *kpos = (int32_t *)(sm + Lay::KPOS);
     int32_t *xpos = (int32_t *)(sm + Lay::XPOS);
     float *zrun = (float *)(sm + Lay::ZRUN);
 
-    __shared__ uint64_t bar_q, bar_wf, bar_lag, bar_mma, bar_ds, bar_full[RING_SLOTS], bar_free[RING_SLOTS];
+    __shared__ uint64_t bar_q, bar_wf, bar_lag, bar_u, bar_s, bar_a, bar_o, bar_ds, bar_full[RING_SLOTS],
+        bar_free[RING_SLOTS];
     __shared__ uint32_t tmem_base;
     __shared__ int s_abort;
-    __shared__ float xch[2][128][4];
 
     const Dims &dm = P.dm;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -117,7 +115,10 @@ __global__ void __launch_bounds__(256, 1) hybrid_tc_kernel(const __grid_constant
         mbar_init(&bar_q, 1);
         mbar_init(&bar_wf, 1);
         mbar_init(&bar_lag, 1);
-        mbar_init(&bar_mma, 1);
+        mbar_init(&bar_u, 1);
+        mbar_init(&bar_s, 1);
+        mbar_init(&bar_a, 1);
+        mbar_init(&bar_o, 1);
         mbar_init(&bar_ds, 1);
         for (int i = 0; i < RING_SLOTS; ++i) { mbar_init(&bar_full[i], 1); mbar_init(&bar_free[i], 1); }
         fence_barrier_init();
@@ -208,12 +209,11 @@ __global__ void __launch_bounds__(256, 1) hybrid_tc_kernel(const __grid_constant
     fence_async_smem();
     __syncthreads();
 
-    uint32_t ph_q = 0, ph_lag = 0, ph_mma = 0, ph_ds = 0;
+    uint32_t ph_q = 0, ph_lag = 0, ph_u = 0, ph_s = 0, ph_a = 0, ph_o = 0, ph_ds = 0;
     uint32_t ph_full = 0, ph_free = 0;   // one parity bit per ring slot (thread 0)
     bool wf_ready = false;
 
     const uint32_t id_u = idesc_bf16(128, DF, 0, 0);
-    const uint32_t id_s = idesc_bf16(128, 32, 0, 0);
     const uint32_t id_a = idesc_bf16(128, 32 + NX, 0, 0);
     const uint32_t id_o = idesc_bf16(128, D, 0, 1);
     const uint32_t id_ds = idesc_bf16(128, D, 1, 1);
@@ -235,6 +235,20 @@ __global__ void __launch_bounds__(256, 1) hybrid_tc_kernel(const __grid_constant
         phs ^= 1u << slot;
     };
 
+    // per-row values the two warps of a lane quarter exchange go through TMEM
+    // columns TM_X.. of the row's lane: half h writes [TM_X + 4h, +4) for the
+    // NP-Map statistics and [TM_X + 8 + 4h, +4) for the row maximum, later the
+    // denominator
+    auto xput = [&](int col, float a, float b, float c) {
+        const float v[4] = {a, b, c, 0.f};
+        tmem_st4(tlane + TM_X + col, v);
+        tmem_st_wait();
+    };
+    auto xget = [&](int col, float (&v)[4]) {
+        tmem_ld4(tlane + TM_X + col, v);
+        tmem_ld_wait();
+    };
+
     for (int it = 0; it < ntiles; ++it) {
         const int t0 = tbeg + it * 32;
         const int ct = t0 / C;
@@ -251,10 +265,9 @@ __global__ void __launch_bounds__(256, 1) hybrid_tc_kernel(const __grid_constant
         const int blo = row_ok ? max(t - W + 1, 0) - band_lo : 1, bhi = row_ok ? t - band_lo : 0;
         const int llo = max(0, W - t0), lhi = row_ok ? t - t0 : -1;
 
-        for (int e = tid; e < ngb * 32; e += 256) kpos[e] = e < nkg ? fs[e] : INT_MAX;
         if (tid < NX) xpos[tid] = (ct < dm.T_max && tid < lam) ? fs[ct * lam + tid] : INT_MAX;
 
-        // ---------------- S phase: U = Q Wf, S = Q K^T ----------------------------
+        // ---------------- U = Q Wf (own commit), S = Q K^T ------------------------------
         if (tid == 0 && !s_abort) {
             if (!wf_ready) {
                 uint32_t ph0 = 0;
@@ -267,16 +280,26 @@ __global__ void __launch_bounds__(256, 1) hybrid_tc_kernel(const __grid_constant
 #pragma unroll
             for (int k = 0; k < D; k += 16)
                 mma_ss(tmem + TM_O, dQ + koff(k, 16384), dWF + koff(k, DF * 128), id_u, k > 0);
-            // blocks 0 .. n1-1 sit in consecutive slots: one MMA of N = 32 n1 per K step
+            mma_commit(&bar_u);
+            // blocks 0 .. n1-1 sit in consecutive slots: one MMA of N = 32 min(n1, 8)
+            // per K step, and one more for a ninth slot
             const int n1 = nkb < RING_SLOTS ? nkb : RING_SLOTS;
             for (int kb = 0; kb < n1; ++kb) wait_slot(bar_full, ph_full, kb);
             tc_fence_after();
-            const uint32_t id_s1 = idesc_bf16(128, 32 * n1, 0, 0);
+            const int na = n1 < 8 ? n1 : 8;
+            const uint32_t id_sa = idesc_bf16(128, 32 * na, 0, 0);
 #pragma unroll
             for (int k = 0; k < D; k += 16)
-                mma_ss(tmem + TM_S, dQ + koff(k, 16384), dKR + koff(k, RSTRIDE), id_s1, k > 0);
+                mma_ss(tmem + TM_S, dQ + koff(k, 16384), dKR + koff(k, RSTRIDE), id_sa, k > 0);
+            if (n1 > 8) {
+                const uint32_t id_sb = idesc_bf16(128, 32 * (n1 - 8), 0, 0);
+#pragma unroll
+                for (int k = 0; k < D; k += 16)
+                    mma_ss(tmem + TM_S + 256, dQ + koff(k, 16384), dKR + koff(k, RSTRIDE) + (uint64_t)(8 * 4096 >> 4),
+                           id_sb, k > 0);
+            }
             if (nkb > RING_SLOTS) {
-                // the rest reuse the first slots once the wide MMA has read them
+                // the rest reuse the first slots once the MMAs above have read them
                 mma_commit(&bar_free[0]);
                 wait_slot(bar_free, ph_free, 0);
                 for (int kb = RING_SLOTS; kb < nkb; ++kb) load_blk(kb, t0, 0);
@@ -287,24 +310,10 @@ __global__ void __launch_bounds__(256, 1) hybrid_tc_kernel(const __grid_constant
                 for (int k = 0; k < D; k += 16)
                     mma_ss(tmem + TM_S + 32 * RING_SLOTS, dQ + koff(k, 16384), dKR + koff(k, RSTRIDE), id_s2, k > 0);
             }
-            mma_commit(&bar_mma);
-        }
-        __syncthreads();
-        if (s_abort) break;
-        // number of kept keys (ascending table) at or before t - W, own-chunk extras likewise
-        int nvk = 0, nvx = 0;
-        {
-            int lo = 0, hi = nkg;
-            while (lo < hi) {
-                const int mid = (lo + hi) >> 1;
-                if (kpos[mid] <= t - W) lo = mid + 1; else hi = mid;
-            }
-            nvk = row_ok ? lo : 0;
-            while (nvx < NX && xpos[nvx] <= t - W) ++nvx;
-            if (!row_ok) nvx = 0;
+            mma_commit(&bar_s);
         }
 
-        // ||q||^2 over this thread's half of the row (before the next Q overwrites it)
+        // ||q||^2 over this thread's half of the row (the MMAs read Q meanwhile)
         float qn2 = 0.f;
 #pragma unroll
         for (int c8 = 0; c8 < DH / 8; ++c8) {
@@ -317,14 +326,27 @@ __global__ void __launch_bounds__(256, 1) hybrid_tc_kernel(const __grid_constant
                 qn2 = fmaf(a0, a0, fmaf(a1, a1, qn2));
             }
         }
-        wait_all(&bar_mma, ph_mma);                 // U and S are in TMEM; Q and the ring are free
-        tc_fence_after();
+        __syncthreads();
+        if (s_abort) break;
+        // number of kept keys (ascending table) at or before t - W, own-chunk extras likewise
+        int nvk = 0, nvx = 0;
+        {
+            int lo = 0, hi = nkg;
+            while (lo < hi) {
+                const int mid = (lo + hi) >> 1;
+                if (__ldg(fs + mid) <= t - W) lo = mid + 1; else hi = mid;
+            }
+            nvk = row_ok ? lo : 0;
+            while (nvx < NX && xpos[nvx] <= t - W) ++nvx;
+            if (!row_ok) nvx = 0;
+        }
 
         // ---------------- phi(Q), pass 1: exponentials of my features (kept) ----------
+        wait_all(&bar_u, ph_u);
+        tc_fence_after();
         float eu[DFH];
-        float mu = -INFINITY;
+        float mu = -INFINITY, s2 = 0.f;
         {
-            float s2 = 0.f;
 #pragma unroll
             for (int c0 = 0; c0 < DFH; c0 += 16) tmem_ld16(tlane + TM_O + half * DFH + c0, *reinterpret_cast<float(*)[16]>(eu + c0));
             tmem_ld_wait();
@@ -335,27 +357,34 @@ __global__ void __launch_bounds__(256, 1) hybrid_tc_kernel(const __grid_constant
                 eu[i] = exp2f(fmaf(eu[i], LOG2E, -mu));
                 s2 = fmaf(eu[i], eu[i], s2);
             }
-            xch[half][r][0] = mu;
-            xch[half][r][1] = s2;
-            xch[half][r][2] = qn2;
+            xput(4 * half, mu, s2, qn2);
         }
+        tc_fence_before();
         __syncthreads();
+        tc_fence_after();
         if (s_abort) break;
         if (tid == 0) {
+            // S complete: Q and the ring are free
+            if (!mbar_wait(&bar_s, ph_s, P.status)) s_abort = 1;
             if (has_next) load_q(t0 + 32);
-            for (int kb = 0; kb < nkb && kb < RING_SLOTS; ++kb) load_blk(kb, t0, 1);   // the ring is free: V blocks
+            for (int kb = 0; kb < nkb && kb < RING_SLOTS; ++kb) load_blk(kb, t0, 1);   // V blocks
             tma_store_wait_read();                  // the previous tile's output left the staging buffer
         }
+        float xo[4];
+        xget(4 * (1 - half), xo);
         __syncthreads();
 
         // ---------------- phi(Q), pass 2: write my half of phi, phi . z ---------------
         float den = 0.f;
         {
-            const float m0 = xch[0][r][0], m1 = xch[1][r][0];
+            // (half 0's values, half 1's values) in the same order on both halves
+            const float m0 = half ? xo[0] : mu, m1 = half ? mu : xo[0];
+            const float a0 = half ? xo[1] : s2, a1 = half ? s2 : xo[1];
+            const float q0 = half ? xo[2] : qn2, q1 = half ? qn2 : xo[2];
             const float M = fmaxf(m0, m1);
-            const float s2 = xch[0][r][1] * exp2f(2.f * (m0 - M)) + xch[1][r][1] * exp2f(2.f * (m1 - M));
-            const float qn = sqrtf(xch[0][r][2] + xch[1][r][2]);
-            const float sc = qn * rsqrtf(s2) * exp2f(mu - M);   // my half's exponentials were taken against mu
+            const float ss = a0 * exp2f(2.f * (m0 - M)) + a1 * exp2f(2.f * (m1 - M));
+            const float qn = sqrtf(q0 + q1);
+            const float sc = qn * rsqrtf(ss) * exp2f(mu - M);   // my half's exponentials were taken against mu
 #pragma unroll
             for (int c0 = 0; c0 < DFH; c0 += 16) {
 #pragma unroll
@@ -381,17 +410,25 @@ __global__ void __launch_bounds__(256, 1) hybrid_tc_kernel(const __grid_constant
         tc_fence_before();
         __syncthreads();
 
-        // ---------------- A = phi(Q) [phi(K_lag) | phi(K_x)]^T ----------------------
+        // ---------------- A = phi(Q) [phi(K_lag) | phi(K_x)]^T; O = phi(Q) S_run -------
         if (tid == 0) {
             if (!mbar_wait(&bar_lag, ph_lag, P.status)) s_abort = 1;
             ph_lag ^= 1;
             tc_fence_after();
             for (int k = 0; k < DF; k += 16)
                 mma_ss(tmem + TM_A, kdesc(sb + Lay::PHIQ, k, 16384), kdesc(sb + Lay::PHIK, k, 6144), id_a, k > 0);
-            mma_commit(&bar_mma);
+            // U was read out by every row in pass 1: O starts as phi(Q) S_run
+            const uint64_t dPQ = sdesc(sb + Lay::PHIQ, 16, 1024), dSR = sdesc(sb + Lay::SRUN, DF * 128, 1024);
+#pragma unroll
+            for (int k = 0; k < DF; k += 16)
+                mma_ss(tmem + TM_O, dPQ + koff(k, 16384), dSR + (uint64_t)(k * 128 >> 4), id_o, k > 0);
+            mma_commit(&bar_a);
         }
 
         // ---------------- softmax pass 1: exact row maximum (blocks kb = half mod 2) ---
+        wait_all(&bar_s, ph_s);
+        tc_fence_after();
+        float cm;
         {
             float cmax = -INFINITY;
             for (int kb = half; kb < nkb; kb += 4) {
@@ -411,15 +448,19 @@ __global__ void __launch_bounds__(256, 1) hybrid_tc_kernel(const __grid_constant
                         if (i >= clo && i <= chi) cmax = fmaxf(cmax, sv[x][i]);
                 }
             }
-            xch[half][r][3] = cmax;
+            xput(8 + 4 * half, cmax, 0.f, 0.f);
+            tc_fence_before();
+            __syncthreads();
+            tc_fence_after();
+            float xc[4];
+            xget(8 + 4 * (1 - half), xc);
+            cmax = fmaxf(cmax, xc[0]);   // the row maximum (both halves agree)
+            cm = cmax == -INFINITY ? 0.f : cmax * l2s;   // no softmax key: every P is 0
         }
-        __syncthreads();
         if (s_abort) break;
-        const float cmr = fmaxf(xch[0][r][3], xch[1][r][3]);
-        const float cm = cmr == -INFINITY ? 0.f : cmr * l2s;   // no softmax key: every P is 0
 
         // ---------------- A: mask, row sum, bf16 pairs back into TMEM ------------------
-        wait_all(&bar_mma, ph_mma);
+        wait_all(&bar_a, ph_a);
         tc_fence_after();
         if (half == 0) {
             float a[32];
@@ -448,6 +489,17 @@ __global__ void __launch_bounds__(256, 1) hybrid_tc_kernel(const __grid_constant
             }
             tmem_st8(tlane + TM_A + 16, w);
         }
+        tmem_st_wait();
+        tc_fence_before();
+        __syncthreads();
+        if (tid == 0) {
+            // O += A V_lagx while the rows form P
+            tc_fence_after();
+            const uint64_t dVL = sdesc(sb + Lay::VLAG, 6144, 1024);
+#pragma unroll
+            for (int kk = 0; kk < 32 + NX; kk += 16)
+                mma_ts(tmem + TM_O, tmem + TM_A + kk / 2, dVL + (uint64_t)(kk * 128 >> 4), id_o, 1);
+        }
 
         // ---------------- softmax pass 2: P (bf16 pairs) over the logits, in place ------
         for (int kb = half; kb < nkb; kb += 2) {
@@ -467,18 +519,14 @@ __global__ void __launch_bounds__(256, 1) hybrid_tc_kernel(const __grid_constant
             tmem_st16(tlane + TM_S + 32 * kb, w);
         }
         tmem_st_wait();
-        xch[half][r][0] = den;
+        xput(8 + 4 * half, den, 0.f, 0.f);
         tc_fence_before();
         __syncthreads();
         if (s_abort) break;
 
-        // ---------------- O = A V_lagx + sum_kb P_kb V_kb + phi(Q) S_run ---------------
+        // ---------------- O += sum_kb P_kb V_kb ------------------------------------------
         if (tid == 0) {
             tc_fence_after();
-            const uint64_t dVL = sdesc(sb + Lay::VLAG, 6144, 1024);
-#pragma unroll
-            for (int kk = 0; kk < 32 + NX; kk += 16)
-                mma_ts(tmem + TM_O, tmem + TM_A + kk / 2, dVL + (uint64_t)(kk * 128 >> 4), id_o, kk > 0);
             const int n1 = nkb < RING_SLOTS ? nkb : RING_SLOTS;
             for (int kb = 0; kb < n1; ++kb) {
                 wait_slot(bar_full, ph_full, kb);
@@ -498,13 +546,13 @@ __global__ void __launch_bounds__(256, 1) hybrid_tc_kernel(const __grid_constant
                     mma_ts(tmem + TM_O, tmem + TM_S + 32 * kb + 8, dVR + (uint64_t)((slot * 4096 + 2048) >> 4), id_o, 1);
                 }
             }
-            const uint64_t dPQ = sdesc(sb + Lay::PHIQ, 16, 1024), dSR = sdesc(sb + Lay::SRUN, DF * 128, 1024);
-#pragma unroll
-            for (int k = 0; k < DF; k += 16)
-                mma_ss(tmem + TM_O, dPQ + koff(k, 16384), dSR + (uint64_t)(k * 128 >> 4), id_o, 1);
-            mma_commit(&bar_mma);
+            mma_commit(&bar_o);
         }
-        wait_all(&bar_mma, ph_mma);
+        tc_fence_after();
+        float xd[4];
+        xget(8 + 4 * (1 - half), xd);
+        const float dtot = den + xd[0];
+        wait_all(&bar_o, ph_o);
         tc_fence_after();
         if (tid == 0) {
             // dS = phi(K_lag)^T V_lag into the logit columns (every read of P is done)
@@ -516,7 +564,6 @@ __global__ void __launch_bounds__(256, 1) hybrid_tc_kernel(const __grid_constant
             if (has_next)
                 for (int kb = 0; kb < nkb_of(t0 + 32) && kb < RING_SLOTS; ++kb) load_blk(kb, t0 + 32, 0);
         }
-        const float dtot = xch[0][r][0] + xch[1][r][0];
 
         // ---------------- epilogue: y = O / den (my half of the columns) ---------------
         {
