@@ -57,7 +57,7 @@ constexpr int TM_S = 0, TM_O = 320, TM_A = 448, TM_X = 496, TM_COLS = 512;   // 
 constexpr int MAX_KEY_BLOCKS = 10;   // 320 logit columns
 constexpr int NX = 16;               // extra (kept, own chunk) rows per tile
 
-constexpr int RING_SLOTS = 9;        // K (then V) blocks of 32 keys in flight
+constexpr int RING_SLOTS = 9;        // K (then V) blocks of 32 keys resident
 
 template <int D, int DF>
 struct TCLayout {
@@ -75,8 +75,14 @@ struct TCLayout {
     static constexpr uint32_t TOTAL = ZRUN + DF * 4;
 };
 
+constexpr int HT_ROWS = 256;               // row threads: 8 warps, two per TMEM lane quarter
+constexpr int HT_THREADS = HT_ROWS + 128;  // and a warpgroup whose first thread issues every TMA copy and MMA
+// registers per thread after the split (launch: 168 x 384 = 64512; rows take
+// 208 x 256, the issuing warpgroup keeps 88 x 128: the same total)
+constexpr int HT_ROW_REGS = 208, HT_ISSUE_REGS = 88;
+
 template <int D, int DF>
-__global__ void __launch_bounds__(256, 1) hybrid_tc_kernel(const __grid_constant__ TCMaps maps, TCParams P)
+__global__ void __launch_bounds__(HT_THREADS, 1) hybrid_tc_kernel(const __grid_constant__ TCMaps maps, TCParams P)
 {
     using Lay = TCLayout<D, DF>;
     constexpr int CBD = Lay::CBD, CBF = Lay::CBF;
@@ -84,271 +90,338 @@ __global__ void __launch_bounds__(256, 1) hybrid_tc_kernel(const __grid_constant
     constexpr float LOG2E = 1.4426950408889634f;
     constexpr uint32_t SLOT = CBD * 4096;     // bytes of one ring slot (32 keys x D)
     constexpr uint32_t RSTRIDE = Lay::RSTRIDE;
+    constexpr long long WAIT_LIMIT = 4000000000LL;   // cycles
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     const uint32_t sb = smem_u32(sm);
     int32_t *xpos = (int32_t *)(sm + Lay::XPOS);
     float *zrun = (float *)(sm + Lay::ZRUN);
 
-    __shared__ uint64_t bar_q, bar_wf, bar_lag, bar_u, bar_s, bar_a, bar_o, bar_ds, bar_full[RING_SLOTS],
-        bar_free[RING_SLOTS];
+    // issuer -> rows: U, S, A (+ phi(Q) S_run), O, dS complete; rows -> issuer:
+    // phi(Q) written, A masked, P written, tile finished (O and dS read,
+    // output staged, S_run updated); issuer -> rows: output staging free
+    __shared__ uint64_t bar_q, bar_wf, bar_lag, bar_u, bar_s, bar_a, bar_o, bar_ds, bar_full[RING_SLOTS], bar_free;
+    __shared__ uint64_t rdy_phiq, rdy_a, rdy_p, rdy_epi, stg_free;
     __shared__ uint32_t tmem_base;
     __shared__ int s_abort;
 
     const Dims &dm = P.dm;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int quarter = warp & 3, half = warp >> 2;
-    const int r = quarter * 32 + lane;            // the tile row (and state row) this thread serves
     const int s = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
     const int unit = b * dm.Hkv + g;
     const int W = dm.W, C = dm.C, lam = dm.lam;
     const int tbeg = s * P.sp.L, tend = min((s + 1) * P.sp.L, dm.N);
     const int ntiles = (tend - tbeg + 31) / 32;
     const int32_t *fs = P.fsel + (size_t)unit * P.KP;
-    const float l2s = LOG2E * rsqrtf((float)D);
 
     if (warp == 0) {
         tmem_alloc(&tmem_base, TM_COLS);
         tmem_relinquish();
     }
     if (tid == 0) {
-        mbar_init(&bar_q, 1);
-        mbar_init(&bar_wf, 1);
-        mbar_init(&bar_lag, 1);
-        mbar_init(&bar_u, 1);
-        mbar_init(&bar_s, 1);
-        mbar_init(&bar_a, 1);
-        mbar_init(&bar_o, 1);
-        mbar_init(&bar_ds, 1);
-        for (int i = 0; i < RING_SLOTS; ++i) { mbar_init(&bar_full[i], 1); mbar_init(&bar_free[i], 1); }
+        for (uint64_t *bb : {&bar_q, &bar_wf, &bar_lag, &bar_u, &bar_s, &bar_a, &bar_o, &bar_ds, &bar_free, &stg_free})
+            mbar_init(bb, 1);
+        for (int i = 0; i < RING_SLOTS; ++i) mbar_init(&bar_full[i], 1);
+        for (uint64_t *bb : {&rdy_phiq, &rdy_a, &rdy_p, &rdy_epi}) mbar_init(bb, HT_ROWS);
         fence_barrier_init();
         s_abort = 0;
     }
     // padding rows of absent heads stay zero for the whole kernel
-    for (int i = tid; i < CBD * 16384 / 16; i += 256) {
+    for (int i = tid; i < CBD * 16384 / 16; i += HT_THREADS) {
         const int row = (i * 16 % 16384) / 128;
         if (row >= dm.G * 32) reinterpret_cast<uint4 *>(sm + Lay::Q)[i] = make_uint4(0, 0, 0, 0);
     }
+    fence_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = tmem_base;
-    const uint32_t tlane = tmem + ((uint32_t)(quarter * 32) << 16);   // this warp's TMEM lanes
 
-    // ---- running linear state: row f = r, columns [half*DH, half*DH + DH) in fp32
-    float srun[DH];
-    {
-        const float *S0 = P.dS + ((size_t)unit * (P.sp.nseg + 1) + s) * (size_t)(DF * D);
-        const int f = r;
-#pragma unroll
-        for (int c = 0; c < DH; ++c) srun[c] = f < DF ? S0[(size_t)f * D + half * DH + c] : 0.f;
-        if (f < DF && half == 0) zrun[f] = P.dz[((size_t)unit * (P.sp.nseg + 1) + s) * DF + f];
-        if (f < DF) {
-#pragma unroll
-            for (int c8 = 0; c8 < DH / 8; ++c8) {
-                const int c = half * DH + c8 * 8;
-                uint4 pk;
-                pk.x = pack_bf16(srun[c8 * 8 + 0], srun[c8 * 8 + 1]);
-                pk.y = pack_bf16(srun[c8 * 8 + 2], srun[c8 * 8 + 3]);
-                pk.z = pack_bf16(srun[c8 * 8 + 4], srun[c8 * 8 + 5]);
-                pk.w = pack_bf16(srun[c8 * 8 + 6], srun[c8 * 8 + 7]);
-                *reinterpret_cast<uint4 *>(sm + Lay::SRUN + (c / 64) * (DF * 128) + sw128(f, (c % 64) / 8)) = pk;
+    // bounded wait; gives up early once the other side has given up
+    auto wait = [&](uint64_t *bar, uint32_t parity) -> bool {
+        if (mbar_try_wait(bar, parity)) return true;
+        const long long c0 = clock64();
+        while (!mbar_try_wait(bar, parity)) {
+            if (*(volatile int *)&s_abort) return false;
+            if (clock64() - c0 > WAIT_LIMIT) {
+                set_status(P.status, STILL_ERR_TIMEOUT);
+                *(volatile int *)&s_abort = 1;
+                return false;
             }
         }
-    }
+        return true;
+    };
 
-    // ---- loads (issued by thread 0 only) -------------------------------------------
-    auto load_q = [&](int t0) {
-        mbar_expect_tx(&bar_q, dm.G * CBD * 4096);
-        for (int hh = 0; hh < dm.G; ++hh)
-            for (int cb = 0; cb < CBD; ++cb)
-                tma_load_3d(sm + Lay::Q + cb * 16384 + hh * 4096, &maps.q, &bar_q, cb * 64, t0,
-                            b * dm.Hq + g * dm.G + hh);
-    };
-    auto load_lag = [&](int t0) {
-        const int ct = t0 / C;
-        const int xrow = ct < dm.T_max ? ct * lam : P.KP;   // past the table: zero fill
-        mbar_expect_tx(&bar_lag, CBF * (4096 + 2048) + CBD * (4096 + 2048));
-        for (int cb = 0; cb < CBF; ++cb) {
-            tma_load_3d(sm + Lay::PHIK + cb * 6144, &maps.phik, &bar_lag, cb * 64, t0 - W, unit);
-            tma_load_3d(sm + Lay::PHIK + cb * 6144 + 4096, &maps.phk16, &bar_lag, cb * 64, xrow, unit);
-        }
-        for (int cb = 0; cb < CBD; ++cb) {
-            tma_load_3d(sm + Lay::VLAG + cb * 6144, &maps.v, &bar_lag, cb * 64, t0 - W, unit);
-            tma_load_3d(sm + Lay::VLAG + cb * 6144 + 4096, &maps.vk16, &bar_lag, cb * 64, xrow, unit);
-        }
-    };
-    // block kb (32 keys) of the key list of the tile at t0, K (kv = 0) or V (kv = 1), into ring slot kb % RING_SLOTS
-    auto load_blk = [&](int kb, int t0, int kv) {
-        const int slot = kb % RING_SLOTS;
-        uint8_t *dst = sm + Lay::RING + slot * 4096;
-        mbar_expect_tx(&bar_full[slot], SLOT);
-        const CUtensorMap *band = kv ? &maps.v : &maps.k;
-        const CUtensorMap *kept = kv ? &maps.vk : &maps.kk;
-        for (int cb = 0; cb < CBD; ++cb) {
-            if (kb < P.nb)
-                tma_load_3d(dst + cb * RSTRIDE, band, &bar_full[slot], cb * 64, t0 - P.Wr + 32 * kb, unit);
-            else
-                tma_load_3d(dst + cb * RSTRIDE, kept, &bar_full[slot], cb * 64, 32 * (kb - P.nb), unit);
-        }
-    };
-    auto nkb_of = [&](int t0) {
-        const int nkg = min(t0 / C, dm.T_max) * lam;
-        return P.nb + (nkg + 31) / 32;
-    };
-    if (tid == 0) {
-        tma_prefetch_desc(&maps.q);
-        mbar_expect_tx(&bar_wf, CBD * DF * 128);
-        for (int cb = 0; cb < CBD; ++cb) tma_load_2d(sm + Lay::WF + cb * DF * 128, &maps.wft, &bar_wf, cb * 64, 0);
-        if (ntiles > 0) {
+    if (warp >= HT_ROWS / 32) {
+        // ======================== the issuing warpgroup =========================
+        regs_dec<HT_ISSUE_REGS>();
+        if (warp == HT_ROWS / 32 && lane == 0 && ntiles > 0) {
+            auto load_q = [&](int t0) {
+                mbar_expect_tx(&bar_q, dm.G * CBD * 4096);
+                for (int hh = 0; hh < dm.G; ++hh)
+                    for (int cb = 0; cb < CBD; ++cb)
+                        tma_load_3d(sm + Lay::Q + cb * 16384 + hh * 4096, &maps.q, &bar_q, cb * 64, t0,
+                                    b * dm.Hq + g * dm.G + hh);
+            };
+            auto load_lag = [&](int t0) {
+                const int ct = t0 / C;
+                const int xrow = ct < dm.T_max ? ct * lam : P.KP;   // past the table: zero fill
+                mbar_expect_tx(&bar_lag, CBF * (4096 + 2048) + CBD * (4096 + 2048));
+                for (int cb = 0; cb < CBF; ++cb) {
+                    tma_load_3d(sm + Lay::PHIK + cb * 6144, &maps.phik, &bar_lag, cb * 64, t0 - W, unit);
+                    tma_load_3d(sm + Lay::PHIK + cb * 6144 + 4096, &maps.phk16, &bar_lag, cb * 64, xrow, unit);
+                }
+                for (int cb = 0; cb < CBD; ++cb) {
+                    tma_load_3d(sm + Lay::VLAG + cb * 6144, &maps.v, &bar_lag, cb * 64, t0 - W, unit);
+                    tma_load_3d(sm + Lay::VLAG + cb * 6144 + 4096, &maps.vk16, &bar_lag, cb * 64, xrow, unit);
+                }
+            };
+            // block kb (32 keys) of the key list of the tile at t0, K (kv = 0) or V (kv = 1), into ring slot kb % RING_SLOTS
+            auto load_blk = [&](int kb, int t0, int kv) {
+                const int slot = kb % RING_SLOTS;
+                uint8_t *dst = sm + Lay::RING + slot * 4096;
+                mbar_expect_tx(&bar_full[slot], SLOT);
+                const CUtensorMap *band = kv ? &maps.v : &maps.k;
+                const CUtensorMap *kept = kv ? &maps.vk : &maps.kk;
+                for (int cb = 0; cb < CBD; ++cb) {
+                    if (kb < P.nb)
+                        tma_load_3d(dst + cb * RSTRIDE, band, &bar_full[slot], cb * 64, t0 - P.Wr + 32 * kb, unit);
+                    else
+                        tma_load_3d(dst + cb * RSTRIDE, kept, &bar_full[slot], cb * 64, 32 * (kb - P.nb), unit);
+                }
+            };
+            auto nkb_of = [&](int t0) { return P.nb + (min(t0 / C, dm.T_max) * lam + 31) / 32; };
+            auto store_out = [&](int t0) {
+                for (int h2 = 0; h2 < dm.G; ++h2)
+                    for (int cb = 0; cb < CBD; ++cb)
+                        tma_store_3d(&maps.out, sm + Lay::PHIQ + cb * 16384 + h2 * 4096, cb * 64, t0,
+                                     b * dm.Hq + g * dm.G + h2);
+                tma_store_commit();
+            };
+            uint32_t ph_q = 0, ph_lag = 0, ph_s = 0, ph_o = 0, pe_phiq = 0, pe_a = 0, pe_p = 0, pe_epi = 0;
+            uint32_t ph_full = 0, ph_free = 0;   // one parity bit per ring slot
+            auto wait_slot = [&](int slot) {
+                const bool ok = wait(&bar_full[slot], (ph_full >> slot) & 1u);
+                ph_full ^= 1u << slot;
+                return ok;
+            };
+            const uint32_t id_u = idesc_bf16(128, DF, 0, 0);
+            const uint32_t id_a = idesc_bf16(128, 32 + NX, 0, 0);
+            const uint32_t id_o = idesc_bf16(128, D, 0, 1);
+            const uint32_t id_ds = idesc_bf16(128, D, 1, 1);
+            auto koff = [](int k, uint32_t blockbytes) { return (uint64_t)(((k / 64) * blockbytes + (k % 64) * 2) >> 4); };
+            auto kdesc = [&](uint32_t base, int k, uint32_t blockbytes) {   // K-major operand, K step k
+                return sdesc(base + (k / 64) * blockbytes + (k % 64) * 2, 16, 1024);
+            };
+            // descriptors advance by adding (byte offset >> 4) to the start-address field
+            const uint64_t dQ = sdesc(sb + Lay::Q, 16, 1024), dWF = sdesc(sb + Lay::WF, 16, 1024);
+            const uint64_t dKR = sdesc(sb + Lay::RING, 16, 1024);               // K-major ring (keys as N)
+            const uint64_t dVR = sdesc(sb + Lay::RING, RSTRIDE, 1024);          // MN-major ring (keys as K)
+            const uint64_t dVL = sdesc(sb + Lay::VLAG, 6144, 1024);
+            const uint64_t dPQ = sdesc(sb + Lay::PHIQ, 16, 1024), dSR = sdesc(sb + Lay::SRUN, DF * 128, 1024);
+
+            tma_prefetch_desc(&maps.q);
+            mbar_expect_tx(&bar_wf, CBD * DF * 128);
+            for (int cb = 0; cb < CBD; ++cb) tma_load_2d(sm + Lay::WF + cb * DF * 128, &maps.wft, &bar_wf, cb * 64, 0);
             load_q(tbeg);
             load_lag(tbeg);
             for (int kb = 0; kb < nkb_of(tbeg) && kb < RING_SLOTS; ++kb) load_blk(kb, tbeg, 0);
-        }
-    }
-    fence_async_smem();
-    __syncthreads();
+            mbar_arrive(&stg_free);   // the staging buffer starts free
+            bool ok = wait(&bar_wf, 0);
 
-    uint32_t ph_q = 0, ph_lag = 0, ph_u = 0, ph_s = 0, ph_a = 0, ph_o = 0, ph_ds = 0;
-    uint32_t ph_full = 0, ph_free = 0;   // one parity bit per ring slot (thread 0)
-    bool wf_ready = false;
-
-    const uint32_t id_u = idesc_bf16(128, DF, 0, 0);
-    const uint32_t id_a = idesc_bf16(128, 32 + NX, 0, 0);
-    const uint32_t id_o = idesc_bf16(128, D, 0, 1);
-    const uint32_t id_ds = idesc_bf16(128, D, 1, 1);
-
-    auto kdesc = [&](uint32_t base, int k, uint32_t blockbytes) {   // K-major operand, K step k
-        return sdesc(base + (k / 64) * blockbytes + (k % 64) * 2, 16, 1024);
-    };
-    // descriptors advance by adding (byte offset >> 4) to the start-address field
-    const uint64_t dQ = sdesc(sb + Lay::Q, 16, 1024), dWF = sdesc(sb + Lay::WF, 16, 1024);
-    const uint64_t dKR = sdesc(sb + Lay::RING, 16, 1024);               // K-major ring (keys as N)
-    const uint64_t dVR = sdesc(sb + Lay::RING, RSTRIDE, 1024);          // MN-major ring (keys as K)
-    auto koff = [](int k, uint32_t blockbytes) { return (uint64_t)(((k / 64) * blockbytes + (k % 64) * 2) >> 4); };
-    auto wait_all = [&](uint64_t *bar, uint32_t &ph) {
-        if (!mbar_wait(bar, ph, P.status)) s_abort = 1;
-        ph ^= 1;
-    };
-    auto wait_slot = [&](uint64_t *bars, uint32_t &phs, int slot) {   // thread 0 only
-        if (!mbar_wait(&bars[slot], (phs >> slot) & 1u, P.status)) s_abort = 1;
-        phs ^= 1u << slot;
-    };
-
-    // per-row values the two warps of a lane quarter exchange go through TMEM
-    // columns TM_X.. of the row's lane: half h writes [TM_X + 4h, +4) for the
-    // NP-Map statistics and [TM_X + 8 + 4h, +4) for the row maximum, later the
-    // denominator
-    auto xput = [&](int col, float a, float b, float c) {
-        const float v[4] = {a, b, c, 0.f};
-        tmem_st4(tlane + TM_X + col, v);
-        tmem_st_wait();
-    };
-    auto xget = [&](int col, float (&v)[4]) {
-        tmem_ld4(tlane + TM_X + col, v);
-        tmem_ld_wait();
-    };
-
-    for (int it = 0; it < ntiles; ++it) {
-        const int t0 = tbeg + it * 32;
-        const int ct = t0 / C;
-        const int nkg = min(ct, dm.T_max) * lam;
-        const int ngb = (nkg + 31) / 32;
-        const int nkb = P.nb + ngb;
-        const int band_lo = t0 - P.Wr;
-        const bool has_next = it + 1 < ntiles;
-
-        // row identity and its column ranges
-        const int hh = r / 32, t = t0 + (r % 32);
-        const bool row_ok = hh < dm.G && t < dm.N;
-        // softmax band columns [blo, bhi]; lag columns [llo, lhi] of A
-        const int blo = row_ok ? max(t - W + 1, 0) - band_lo : 1, bhi = row_ok ? t - band_lo : 0;
-        const int llo = max(0, W - t0), lhi = row_ok ? t - t0 : -1;
-
-        if (tid < NX) xpos[tid] = (ct < dm.T_max && tid < lam) ? fs[ct * lam + tid] : INT_MAX;
-
-        // ---------------- U = Q Wf (own commit), S = Q K^T ------------------------------
-        if (tid == 0 && !s_abort) {
-            if (!wf_ready) {
-                uint32_t ph0 = 0;
-                if (!mbar_wait(&bar_wf, ph0, P.status)) s_abort = 1;
-                wf_ready = true;
-            }
-            if (!mbar_wait(&bar_q, ph_q, P.status)) s_abort = 1;
-            ph_q ^= 1;
-            tc_fence_after();
-#pragma unroll
-            for (int k = 0; k < D; k += 16)
-                mma_ss(tmem + TM_O, dQ + koff(k, 16384), dWF + koff(k, DF * 128), id_u, k > 0);
-            mma_commit(&bar_u);
-            // blocks 0 .. n1-1 sit in consecutive slots: one MMA of N = 32 min(n1, 8)
-            // per K step, and one more for a ninth slot
-            const int n1 = nkb < RING_SLOTS ? nkb : RING_SLOTS;
-            for (int kb = 0; kb < n1; ++kb) wait_slot(bar_full, ph_full, kb);
-            tc_fence_after();
-            const int na = n1 < 8 ? n1 : 8;
-            const uint32_t id_sa = idesc_bf16(128, 32 * na, 0, 0);
-#pragma unroll
-            for (int k = 0; k < D; k += 16)
-                mma_ss(tmem + TM_S, dQ + koff(k, 16384), dKR + koff(k, RSTRIDE), id_sa, k > 0);
-            if (n1 > 8) {
-                const uint32_t id_sb = idesc_bf16(128, 32 * (n1 - 8), 0, 0);
-#pragma unroll
-                for (int k = 0; k < D; k += 16)
-                    mma_ss(tmem + TM_S + 256, dQ + koff(k, 16384), dKR + koff(k, RSTRIDE) + (uint64_t)(8 * 4096 >> 4),
-                           id_sb, k > 0);
-            }
-            if (nkb > RING_SLOTS) {
-                // the rest reuse the first slots once the MMAs above have read them
-                mma_commit(&bar_free[0]);
-                wait_slot(bar_free, ph_free, 0);
-                for (int kb = RING_SLOTS; kb < nkb; ++kb) load_blk(kb, t0, 0);
-                for (int kb = RING_SLOTS; kb < nkb; ++kb) wait_slot(bar_full, ph_full, kb - RING_SLOTS);
+            for (int it = 0; it < ntiles && ok; ++it) {
+                const int t0 = tbeg + it * 32;
+                const int nkb = nkb_of(t0);
+                const bool has_next = it + 1 < ntiles;
+                if (it > 0) {
+                    // the rows are done with the previous tile: its output leaves, this tile's lag comes in
+                    ok &= wait(&rdy_epi, pe_epi);
+                    pe_epi ^= 1;
+                    store_out(t0 - 32);
+                    load_lag(t0);
+                }
+                // U = Q Wf, then S = Q K^T: blocks 0 .. n1-1 in consecutive slots, one MMA of
+                // N = 32 min(n1, 8) per K step and one more for a ninth slot
+                ok &= wait(&bar_q, ph_q);
+                ph_q ^= 1;
                 tc_fence_after();
-                const uint32_t id_s2 = idesc_bf16(128, 32 * (nkb - RING_SLOTS), 0, 0);
-#pragma unroll
+#pragma unroll 1
                 for (int k = 0; k < D; k += 16)
-                    mma_ss(tmem + TM_S + 32 * RING_SLOTS, dQ + koff(k, 16384), dKR + koff(k, RSTRIDE), id_s2, k > 0);
+                    mma_ss(tmem + TM_O, dQ + koff(k, 16384), dWF + koff(k, DF * 128), id_u, k > 0);
+                mma_commit(&bar_u);
+                const int n1 = nkb < RING_SLOTS ? nkb : RING_SLOTS;
+                for (int kb = 0; kb < n1; ++kb) ok &= wait_slot(kb);
+                tc_fence_after();
+                const int na = n1 < 8 ? n1 : 8;
+                const uint32_t id_sa = idesc_bf16(128, 32 * na, 0, 0);
+#pragma unroll 1
+                for (int k = 0; k < D; k += 16)
+                    mma_ss(tmem + TM_S, dQ + koff(k, 16384), dKR + koff(k, RSTRIDE), id_sa, k > 0);
+                if (n1 > 8) {
+                    const uint32_t id_sb = idesc_bf16(128, 32 * (n1 - 8), 0, 0);
+#pragma unroll 1
+                    for (int k = 0; k < D; k += 16)
+                        mma_ss(tmem + TM_S + 256, dQ + koff(k, 16384), dKR + koff(k, RSTRIDE) + (uint64_t)(8 * 4096 >> 4),
+                               id_sb, k > 0);
+                }
+                if (nkb > RING_SLOTS) {
+                    // the rest reuse the first slots once the MMAs above have read them
+                    mma_commit(&bar_free);
+                    ok &= wait(&bar_free, ph_free);
+                    ph_free ^= 1;
+                    for (int kb = RING_SLOTS; kb < nkb; ++kb) load_blk(kb, t0, 0);
+                    for (int kb = RING_SLOTS; kb < nkb; ++kb) ok &= wait_slot(kb - RING_SLOTS);
+                    tc_fence_after();
+                    const uint32_t id_s2 = idesc_bf16(128, 32 * (nkb - RING_SLOTS), 0, 0);
+#pragma unroll 1
+                    for (int k = 0; k < D; k += 16)
+                        mma_ss(tmem + TM_S + 32 * RING_SLOTS, dQ + koff(k, 16384), dKR + koff(k, RSTRIDE), id_s2, k > 0);
+                }
+                mma_commit(&bar_s);
+                if (it > 0) {
+                    tma_store_wait_read();   // the previous output has left the staging buffer
+                    mbar_arrive(&stg_free);
+                }
+                // S complete: the ring takes this tile's V blocks
+                ok &= wait(&bar_s, ph_s);
+                ph_s ^= 1;
+                for (int kb = 0; kb < nkb && kb < RING_SLOTS; ++kb) load_blk(kb, t0, 1);
+                // phi(Q) written (and every row has read Q): A, O = phi(Q) S_run; the next Q
+                ok &= wait(&rdy_phiq, pe_phiq);
+                pe_phiq ^= 1;
+                if (has_next) load_q(t0 + 32);
+                ok &= wait(&bar_lag, ph_lag);
+                ph_lag ^= 1;
+                tc_fence_after();
+                for (int k = 0; k < DF; k += 16)
+                    mma_ss(tmem + TM_A, kdesc(sb + Lay::PHIQ, k, 16384), kdesc(sb + Lay::PHIK, k, 6144), id_a, k > 0);
+#pragma unroll 1
+                for (int k = 0; k < DF; k += 16)
+                    mma_ss(tmem + TM_O, dPQ + koff(k, 16384), dSR + (uint64_t)(k * 128 >> 4), id_o, k > 0);
+                mma_commit(&bar_a);
+                // A masked: O += A V_lagx
+                ok &= wait(&rdy_a, pe_a);
+                pe_a ^= 1;
+                tc_fence_after();
+#pragma unroll 1
+                for (int kk = 0; kk < 32 + NX; kk += 16)
+                    mma_ts(tmem + TM_O, tmem + TM_A + kk / 2, dVL + (uint64_t)(kk * 128 >> 4), id_o, 1);
+                // P written: O += sum_kb P_kb V_kb
+                ok &= wait(&rdy_p, pe_p);
+                pe_p ^= 1;
+                tc_fence_after();
+                for (int kb = 0; kb < n1; ++kb) {
+                    ok &= wait_slot(kb);
+                    tc_fence_after();
+                    mma_ts(tmem + TM_O, tmem + TM_S + 32 * kb, dVR + (uint64_t)(kb * 4096 >> 4), id_o, 1);
+                    mma_ts(tmem + TM_O, tmem + TM_S + 32 * kb + 8, dVR + (uint64_t)((kb * 4096 + 2048) >> 4), id_o, 1);
+                }
+                if (nkb > RING_SLOTS) {
+                    mma_commit(&bar_free);
+                    ok &= wait(&bar_free, ph_free);
+                    ph_free ^= 1;
+                    for (int kb = RING_SLOTS; kb < nkb; ++kb) load_blk(kb, t0, 1);
+                    for (int kb = RING_SLOTS; kb < nkb; ++kb) {
+                        const int slot = kb - RING_SLOTS;
+                        ok &= wait_slot(slot);
+                        tc_fence_after();
+                        mma_ts(tmem + TM_O, tmem + TM_S + 32 * kb, dVR + (uint64_t)(slot * 4096 >> 4), id_o, 1);
+                        mma_ts(tmem + TM_O, tmem + TM_S + 32 * kb + 8, dVR + (uint64_t)((slot * 4096 + 2048) >> 4), id_o, 1);
+                    }
+                }
+                mma_commit(&bar_o);
+                // every read of P and of the ring is done: dS into the logit columns, the next K blocks
+                ok &= wait(&bar_o, ph_o);
+                ph_o ^= 1;
+                tc_fence_after();
+                for (int kk = 0; kk < 32; kk += 16)
+                    mma_ss(tmem + TM_S, sdesc(sb + Lay::PHIK + kk * 128, 6144, 1024),
+                           sdesc(sb + Lay::VLAG + kk * 128, 6144, 1024), id_ds, kk > 0);
+                mma_commit(&bar_ds);
+                if (has_next)
+                    for (int kb = 0; kb < nkb_of(t0 + 32) && kb < RING_SLOTS; ++kb) load_blk(kb, t0 + 32, 0);
             }
-            mma_commit(&bar_s);
+            if (ok && wait(&rdy_epi, pe_epi)) store_out(tbeg + (ntiles - 1) * 32);
+            tma_store_wait_all();
         }
+        __syncwarp();
+    } else {
+        // ============================ the row warps =============================
+        regs_inc<HT_ROW_REGS>();
+        const int quarter = warp & 3, half = warp >> 2;
+        const int r = quarter * 32 + lane;            // the tile row (and state row) this thread serves
+        const float l2s = LOG2E * rsqrtf((float)D);
+        const uint32_t tlane = tmem + ((uint32_t)(quarter * 32) << 16);   // this warp's TMEM lanes
 
-        // ||q||^2 over this thread's half of the row (the MMAs read Q meanwhile)
-        float qn2 = 0.f;
-#pragma unroll
-        for (int c8 = 0; c8 < DH / 8; ++c8) {
-            const int c = half * DH + c8 * 8;
-            const uint4 pk = *reinterpret_cast<const uint4 *>(sm + Lay::Q + (c / 64) * 16384 + sw128(r, (c % 64) / 8));
-            const uint32_t w4[4] = {pk.x, pk.y, pk.z, pk.w};
-#pragma unroll
-            for (int h2 = 0; h2 < 4; ++h2) {
-                const float a0 = __uint_as_float(w4[h2] << 16), a1 = __uint_as_float(w4[h2] & 0xffff0000u);
-                qn2 = fmaf(a0, a0, fmaf(a1, a1, qn2));
-            }
-        }
-        __syncthreads();
-        if (s_abort) break;
-        // number of kept keys (ascending table) at or before t - W, own-chunk extras likewise
-        int nvk = 0, nvx = 0;
+        // running linear state: row f = r, columns [half*DH, half*DH + DH) in fp32
+        float srun[DH];
         {
-            int lo = 0, hi = nkg;
-            while (lo < hi) {
-                const int mid = (lo + hi) >> 1;
-                if (__ldg(fs + mid) <= t - W) lo = mid + 1; else hi = mid;
+            const float *S0 = P.dS + ((size_t)unit * (P.sp.nseg + 1) + s) * (size_t)(DF * D);
+            const int f = r;
+#pragma unroll
+            for (int c = 0; c < DH; ++c) srun[c] = f < DF ? S0[(size_t)f * D + half * DH + c] : 0.f;
+            if (f < DF && half == 0) zrun[f] = P.dz[((size_t)unit * (P.sp.nseg + 1) + s) * DF + f];
+            if (f < DF) {
+#pragma unroll
+                for (int c8 = 0; c8 < DH / 8; ++c8) {
+                    const int c = half * DH + c8 * 8;
+                    uint4 pk;
+                    pk.x = pack_bf16(srun[c8 * 8 + 0], srun[c8 * 8 + 1]);
+                    pk.y = pack_bf16(srun[c8 * 8 + 2], srun[c8 * 8 + 3]);
+                    pk.z = pack_bf16(srun[c8 * 8 + 4], srun[c8 * 8 + 5]);
+                    pk.w = pack_bf16(srun[c8 * 8 + 6], srun[c8 * 8 + 7]);
+                    *reinterpret_cast<uint4 *>(sm + Lay::SRUN + (c / 64) * (DF * 128) + sw128(f, (c % 64) / 8)) = pk;
+                }
             }
-            nvk = row_ok ? lo : 0;
-            while (nvx < NX && xpos[nvx] <= t - W) ++nvx;
-            if (!row_ok) nvx = 0;
         }
+        uint32_t ph_q = 0, ph_u = 0, ph_s = 0, ph_a = 0, ph_o = 0, ph_ds = 0, ph_stg = 0;
+        // per-row values the two warps of a lane quarter exchange go through
+        // TMEM columns TM_X.. of the row's lane: NP-Map statistics of half h at
+        // [TM_X + 4h, +3), its row maximum at TM_X + 8 + h, its denominator at
+        // TM_X + 10 + h
+        auto sync_rows = [&](bool bad) { return named_sync_or(1, HT_ROWS, bad || *(volatile int *)&s_abort); };
 
-        // ---------------- phi(Q), pass 1: exponentials of my features (kept) ----------
-        wait_all(&bar_u, ph_u);
-        tc_fence_after();
-        float eu[DFH];
-        float mu = -INFINITY, s2 = 0.f;
-        {
+        for (int it = 0; it < ntiles; ++it) {
+            const int t0 = tbeg + it * 32;
+            const int ct = t0 / C;
+            const int nkg = min(ct, dm.T_max) * lam;
+            const int nkb = P.nb + (nkg + 31) / 32;
+            const int band_lo = t0 - P.Wr;
+
+            // row identity and its column ranges
+            const int hh = r / 32, t = t0 + (r % 32);
+            const bool row_ok = hh < dm.G && t < dm.N;
+            // softmax band columns [blo, bhi]; lag columns [llo, lhi] of A
+            const int blo = row_ok ? max(t - W + 1, 0) - band_lo : 1, bhi = row_ok ? t - band_lo : 0;
+            const int llo = max(0, W - t0), lhi = row_ok ? t - t0 : -1;
+
+            if (tid < NX) xpos[tid] = (ct < dm.T_max && tid < lam) ? fs[ct * lam + tid] : INT_MAX;
+
+            // ---------------- ||q||^2 of my half of the row ----------------------------------
+            bool bad = !wait(&bar_q, ph_q);
+            ph_q ^= 1;
+            float qn2 = 0.f;
 #pragma unroll
-            for (int c0 = 0; c0 < DFH; c0 += 16) tmem_ld16(tlane + TM_O + half * DFH + c0, *reinterpret_cast<float(*)[16]>(eu + c0));
+            for (int c8 = 0; c8 < DH / 8; ++c8) {
+                const int c = half * DH + c8 * 8;
+                const uint4 pk = *reinterpret_cast<const uint4 *>(sm + Lay::Q + (c / 64) * 16384 + sw128(r, (c % 64) / 8));
+                const uint32_t w4[4] = {pk.x, pk.y, pk.z, pk.w};
+#pragma unroll
+                for (int h2 = 0; h2 < 4; ++h2) {
+                    const float a0 = __uint_as_float(w4[h2] << 16), a1 = __uint_as_float(w4[h2] & 0xffff0000u);
+                    qn2 = fmaf(a0, a0, fmaf(a1, a1, qn2));
+                }
+            }
+
+            // ---------------- phi(Q), pass 1: exponentials of my features (kept) ----------
+            bad |= !wait(&bar_u, ph_u);
+            ph_u ^= 1;
+            tc_fence_after();
+            float eu[DFH];
+            float mu = -INFINITY, s2 = 0.f;
+#pragma unroll
+            for (int c0 = 0; c0 < DFH; c0 += 16)
+                tmem_ld16(tlane + TM_O + half * DFH + c0, *reinterpret_cast<float(*)[16]>(eu + c0));
             tmem_ld_wait();
 #pragma unroll
             for (int i = 0; i < DFH; ++i) mu = fmaxf(mu, eu[i] * LOG2E);
@@ -357,79 +430,71 @@ __global__ void __launch_bounds__(256, 1) hybrid_tc_kernel(const __grid_constant
                 eu[i] = exp2f(fmaf(eu[i], LOG2E, -mu));
                 s2 = fmaf(eu[i], eu[i], s2);
             }
-            xput(4 * half, mu, s2, qn2);
-        }
-        tc_fence_before();
-        __syncthreads();
-        tc_fence_after();
-        if (s_abort) break;
-        if (tid == 0) {
-            // S complete: Q and the ring are free
-            if (!mbar_wait(&bar_s, ph_s, P.status)) s_abort = 1;
-            if (has_next) load_q(t0 + 32);
-            for (int kb = 0; kb < nkb && kb < RING_SLOTS; ++kb) load_blk(kb, t0, 1);   // V blocks
-            tma_store_wait_read();                  // the previous tile's output left the staging buffer
-        }
-        float xo[4];
-        xget(4 * (1 - half), xo);
-        __syncthreads();
+            {
+                const float v[4] = {mu, s2, qn2, 0.f};
+                tmem_st4(tlane + TM_X + 4 * half, v);
+                tmem_st_wait();
+            }
+            tc_fence_before();
+            if (sync_rows(bad)) break;
+            tc_fence_after();
+            // number of kept keys (ascending table) at or before t - W, own-chunk extras likewise
+            int nvk = 0, nvx = 0;
+            {
+                int lo = 0, hi = nkg;
+                while (lo < hi) {
+                    const int mid = (lo + hi) >> 1;
+                    if (__ldg(fs + mid) <= t - W) lo = mid + 1; else hi = mid;
+                }
+                nvk = row_ok ? lo : 0;
+                while (nvx < NX && xpos[nvx] <= t - W) ++nvx;
+                if (!row_ok) nvx = 0;
+            }
+            float xo[4];
+            tmem_ld4(tlane + TM_X + 4 * (1 - half), xo);
+            tmem_ld_wait();
 
-        // ---------------- phi(Q), pass 2: write my half of phi, phi . z ---------------
-        float den = 0.f;
-        {
-            // (half 0's values, half 1's values) in the same order on both halves
-            const float m0 = half ? xo[0] : mu, m1 = half ? mu : xo[0];
-            const float a0 = half ? xo[1] : s2, a1 = half ? s2 : xo[1];
-            const float q0 = half ? xo[2] : qn2, q1 = half ? qn2 : xo[2];
-            const float M = fmaxf(m0, m1);
-            const float ss = a0 * exp2f(2.f * (m0 - M)) + a1 * exp2f(2.f * (m1 - M));
-            const float qn = sqrtf(q0 + q1);
-            const float sc = qn * rsqrtf(ss) * exp2f(mu - M);   // my half's exponentials were taken against mu
+            // ---------------- phi(Q), pass 2: write my half of phi, phi . z ---------------
+            bad = !wait(&stg_free, ph_stg);    // the previous output has left the staging buffer
+            ph_stg ^= 1;
+            float den = 0.f;
+            {
+                // (half 0's values, half 1's values) in the same order on both halves
+                const float m0 = half ? xo[0] : mu, m1 = half ? mu : xo[0];
+                const float a0 = half ? xo[1] : s2, a1 = half ? s2 : xo[1];
+                const float q0 = half ? xo[2] : qn2, q1 = half ? qn2 : xo[2];
+                const float M = fmaxf(m0, m1);
+                const float ss = a0 * exp2f(2.f * (m0 - M)) + a1 * exp2f(2.f * (m1 - M));
+                const float qn = sqrtf(q0 + q1);
+                const float sc = qn * rsqrtf(ss) * exp2f(mu - M);   // my half's exponentials were taken against mu
 #pragma unroll
-            for (int c0 = 0; c0 < DFH; c0 += 16) {
+                for (int c0 = 0; c0 < DFH; c0 += 16) {
 #pragma unroll
-                for (int c8 = 0; c8 < 2; ++c8) {
-                    uint32_t w4[4];
+                    for (int c8 = 0; c8 < 2; ++c8) {
+                        uint32_t w4[4];
 #pragma unroll
-                    for (int h2 = 0; h2 < 4; ++h2) {
-                        const int i = c8 * 8 + h2 * 2;
-                        const float p0 = sc * eu[c0 + i];
-                        const float p1 = sc * eu[c0 + i + 1];
-                        w4[h2] = pack_bf16(p0, p1);
-                        const int f = half * DFH + c0 + i;
-                        den = fmaf(__uint_as_float(w4[h2] << 16), zrun[f], den);
-                        den = fmaf(__uint_as_float(w4[h2] & 0xffff0000u), zrun[f + 1], den);
+                        for (int h2 = 0; h2 < 4; ++h2) {
+                            const int i = c8 * 8 + h2 * 2;
+                            const float p0 = sc * eu[c0 + i];
+                            const float p1 = sc * eu[c0 + i + 1];
+                            w4[h2] = pack_bf16(p0, p1);
+                            const int f = half * DFH + c0 + i;
+                            den = fmaf(__uint_as_float(w4[h2] << 16), zrun[f], den);
+                            den = fmaf(__uint_as_float(w4[h2] & 0xffff0000u), zrun[f + 1], den);
+                        }
+                        const int f0 = half * DFH + c0 + c8 * 8;
+                        *reinterpret_cast<uint4 *>(sm + Lay::PHIQ + (f0 / 64) * 16384 + sw128(r, (f0 % 64) / 8)) =
+                            make_uint4(w4[0], w4[1], w4[2], w4[3]);
                     }
-                    const int f0 = half * DFH + c0 + c8 * 8;
-                    *reinterpret_cast<uint4 *>(sm + Lay::PHIQ + (f0 / 64) * 16384 + sw128(r, (f0 % 64) / 8)) =
-                        make_uint4(w4[0], w4[1], w4[2], w4[3]);
                 }
             }
-        }
-        fence_async_smem();
-        tc_fence_before();
-        __syncthreads();
+            fence_async_smem();
+            mbar_arrive(&rdy_phiq);
 
-        // ---------------- A = phi(Q) [phi(K_lag) | phi(K_x)]^T; O = phi(Q) S_run -------
-        if (tid == 0) {
-            if (!mbar_wait(&bar_lag, ph_lag, P.status)) s_abort = 1;
-            ph_lag ^= 1;
+            // ---------------- softmax pass 1: exact row maximum (blocks kb = half mod 2) ---
+            bad |= !wait(&bar_s, ph_s);
+            ph_s ^= 1;
             tc_fence_after();
-            for (int k = 0; k < DF; k += 16)
-                mma_ss(tmem + TM_A, kdesc(sb + Lay::PHIQ, k, 16384), kdesc(sb + Lay::PHIK, k, 6144), id_a, k > 0);
-            // U was read out by every row in pass 1: O starts as phi(Q) S_run
-            const uint64_t dPQ = sdesc(sb + Lay::PHIQ, 16, 1024), dSR = sdesc(sb + Lay::SRUN, DF * 128, 1024);
-#pragma unroll
-            for (int k = 0; k < DF; k += 16)
-                mma_ss(tmem + TM_O, dPQ + koff(k, 16384), dSR + (uint64_t)(k * 128 >> 4), id_o, k > 0);
-            mma_commit(&bar_a);
-        }
-
-        // ---------------- softmax pass 1: exact row maximum (blocks kb = half mod 2) ---
-        wait_all(&bar_s, ph_s);
-        tc_fence_after();
-        float cm;
-        {
             float cmax = -INFINITY;
             for (int kb = half; kb < nkb; kb += 4) {
                 float sv[2][32];
@@ -448,192 +513,144 @@ __global__ void __launch_bounds__(256, 1) hybrid_tc_kernel(const __grid_constant
                         if (i >= clo && i <= chi) cmax = fmaxf(cmax, sv[x][i]);
                 }
             }
-            xput(8 + 4 * half, cmax, 0.f, 0.f);
+            tmem_st1(tlane + TM_X + 8 + half, cmax);
+            tmem_st_wait();
             tc_fence_before();
-            __syncthreads();
+            if (sync_rows(bad)) break;
             tc_fence_after();
-            float xc[4];
-            xget(8 + 4 * (1 - half), xc);
-            cmax = fmaxf(cmax, xc[0]);   // the row maximum (both halves agree)
-            cm = cmax == -INFINITY ? 0.f : cmax * l2s;   // no softmax key: every P is 0
-        }
-        if (s_abort) break;
+            cmax = fmaxf(cmax, tmem_ld1(tlane + TM_X + 8 + (1 - half)));   // the row maximum (both halves agree)
+            tmem_ld_wait();
+            const float cm = cmax == -INFINITY ? 0.f : cmax * l2s;   // no softmax key: every P is 0
 
-        // ---------------- A: mask, row sum, bf16 pairs back into TMEM ------------------
-        wait_all(&bar_a, ph_a);
-        tc_fence_after();
-        if (half == 0) {
-            float a[32];
-            tmem_ld32(tlane + TM_A, a);
-            tmem_ld_wait();
-            uint32_t w[16];
-#pragma unroll
-            for (int i = 0; i < 32; i += 2) {
-                const float x0 = (i >= llo && i <= lhi) ? a[i] : 0.f;
-                const float x1 = (i + 1 >= llo && i + 1 <= lhi) ? a[i + 1] : 0.f;
-                den += x0 + x1;
-                w[i / 2] = pack_bf16(x0, x1);
-            }
-            tmem_st16(tlane + TM_A, w);
-        } else {
-            float a[16];
-            tmem_ld16(tlane + TM_A + 32, a);
-            tmem_ld_wait();
-            uint32_t w[8];
-#pragma unroll
-            for (int i = 0; i < 16; i += 2) {
-                const float x0 = i < nvx ? a[i] : 0.f;
-                const float x1 = i + 1 < nvx ? a[i + 1] : 0.f;
-                den += x0 + x1;
-                w[i / 2] = pack_bf16(x0, x1);
-            }
-            tmem_st8(tlane + TM_A + 16, w);
-        }
-        tmem_st_wait();
-        tc_fence_before();
-        __syncthreads();
-        if (tid == 0) {
-            // O += A V_lagx while the rows form P
+            // ---------------- A: mask, row sum, bf16 pairs back into TMEM ------------------
+            bad = !wait(&bar_a, ph_a);
+            ph_a ^= 1;
             tc_fence_after();
-            const uint64_t dVL = sdesc(sb + Lay::VLAG, 6144, 1024);
+            if (half == 0) {
+                float a[32];
+                tmem_ld32(tlane + TM_A, a);
+                tmem_ld_wait();
+                uint32_t w[16];
 #pragma unroll
-            for (int kk = 0; kk < 32 + NX; kk += 16)
-                mma_ts(tmem + TM_O, tmem + TM_A + kk / 2, dVL + (uint64_t)(kk * 128 >> 4), id_o, 1);
-        }
-
-        // ---------------- softmax pass 2: P (bf16 pairs) over the logits, in place ------
-        for (int kb = half; kb < nkb; kb += 2) {
-            float sv[32];
-            tmem_ld32(tlane + TM_S + 32 * kb, sv);
-            tmem_ld_wait();
-            const int clo = kb < P.nb ? blo - 32 * kb : 0;
-            const int chi = kb < P.nb ? bhi - 32 * kb : nvk - 1 - 32 * (kb - P.nb);
-            uint32_t w[16];
-#pragma unroll
-            for (int i = 0; i < 32; i += 2) {
-                const float p0 = (i >= clo && i <= chi) ? exp2f(fmaf(sv[i], l2s, -cm)) : 0.f;
-                const float p1 = (i + 1 >= clo && i + 1 <= chi) ? exp2f(fmaf(sv[i + 1], l2s, -cm)) : 0.f;
-                den += p0 + p1;
-                w[i / 2] = pack_bf16(p0, p1);
-            }
-            tmem_st16(tlane + TM_S + 32 * kb, w);
-        }
-        tmem_st_wait();
-        xput(8 + 4 * half, den, 0.f, 0.f);
-        tc_fence_before();
-        __syncthreads();
-        if (s_abort) break;
-
-        // ---------------- O += sum_kb P_kb V_kb ------------------------------------------
-        if (tid == 0) {
-            tc_fence_after();
-            const int n1 = nkb < RING_SLOTS ? nkb : RING_SLOTS;
-            for (int kb = 0; kb < n1; ++kb) {
-                wait_slot(bar_full, ph_full, kb);
-                tc_fence_after();
-                mma_ts(tmem + TM_O, tmem + TM_S + 32 * kb, dVR + (uint64_t)(kb * 4096 >> 4), id_o, 1);
-                mma_ts(tmem + TM_O, tmem + TM_S + 32 * kb + 8, dVR + (uint64_t)((kb * 4096 + 2048) >> 4), id_o, 1);
-            }
-            if (nkb > RING_SLOTS) {
-                mma_commit(&bar_free[0]);
-                wait_slot(bar_free, ph_free, 0);
-                for (int kb = RING_SLOTS; kb < nkb; ++kb) load_blk(kb, t0, 1);
-                for (int kb = RING_SLOTS; kb < nkb; ++kb) {
-                    const int slot = kb - RING_SLOTS;
-                    wait_slot(bar_full, ph_full, slot);
-                    tc_fence_after();
-                    mma_ts(tmem + TM_O, tmem + TM_S + 32 * kb, dVR + (uint64_t)(slot * 4096 >> 4), id_o, 1);
-                    mma_ts(tmem + TM_O, tmem + TM_S + 32 * kb + 8, dVR + (uint64_t)((slot * 4096 + 2048) >> 4), id_o, 1);
+                for (int i = 0; i < 32; i += 2) {
+                    const float x0 = (i >= llo && i <= lhi) ? a[i] : 0.f;
+                    const float x1 = (i + 1 >= llo && i + 1 <= lhi) ? a[i + 1] : 0.f;
+                    den += x0 + x1;
+                    w[i / 2] = pack_bf16(x0, x1);
                 }
-            }
-            mma_commit(&bar_o);
-        }
-        tc_fence_after();
-        float xd[4];
-        xget(8 + 4 * (1 - half), xd);
-        const float dtot = den + xd[0];
-        wait_all(&bar_o, ph_o);
-        tc_fence_after();
-        if (tid == 0) {
-            // dS = phi(K_lag)^T V_lag into the logit columns (every read of P is done)
-            for (int kk = 0; kk < 32; kk += 16)
-                mma_ss(tmem + TM_S, sdesc(sb + Lay::PHIK + kk * 128, 6144, 1024),
-                       sdesc(sb + Lay::VLAG + kk * 128, 6144, 1024), id_ds, kk > 0);
-            mma_commit(&bar_ds);
-            // the ring is free: the next tile's first K blocks
-            if (has_next)
-                for (int kb = 0; kb < nkb_of(t0 + 32) && kb < RING_SLOTS; ++kb) load_blk(kb, t0 + 32, 0);
-        }
-
-        // ---------------- epilogue: y = O / den (my half of the columns) ---------------
-        {
-            const float inv = dtot != 0.f ? 1.f / dtot : 0.f;
-            float ov[DH];
+                tmem_st16(tlane + TM_A, w);
+            } else {
+                float a[16];
+                tmem_ld16(tlane + TM_A + 32, a);
+                tmem_ld_wait();
+                uint32_t w[8];
 #pragma unroll
-            for (int c0 = 0; c0 < DH; c0 += 16) tmem_ld16(tlane + TM_O + half * DH + c0, *reinterpret_cast<float(*)[16]>(ov + c0));
-            tmem_ld_wait();
-#pragma unroll
-            for (int c0 = 0; c0 < DH; c0 += 16) {
-                const float *o = ov + c0;
-#pragma unroll
-                for (int c8 = 0; c8 < 2; ++c8) {
-                    uint4 pk;
-                    pk.x = pack_bf16(o[c8 * 8 + 0] * inv, o[c8 * 8 + 1] * inv);
-                    pk.y = pack_bf16(o[c8 * 8 + 2] * inv, o[c8 * 8 + 3] * inv);
-                    pk.z = pack_bf16(o[c8 * 8 + 4] * inv, o[c8 * 8 + 5] * inv);
-                    pk.w = pack_bf16(o[c8 * 8 + 6] * inv, o[c8 * 8 + 7] * inv);
-                    const int d0 = half * DH + c0 + c8 * 8;
-                    *reinterpret_cast<uint4 *>(sm + Lay::PHIQ + (d0 / 64) * 16384 + sw128(r, (d0 % 64) / 8)) = pk;
+                for (int i = 0; i < 16; i += 2) {
+                    const float x0 = i < nvx ? a[i] : 0.f;
+                    const float x1 = i + 1 < nvx ? a[i + 1] : 0.f;
+                    den += x0 + x1;
+                    w[i / 2] = pack_bf16(x0, x1);
                 }
+                tmem_st8(tlane + TM_A + 16, w);
             }
-        }
-        // ---------------- state update: S_run += dS, z_run += sum phi(K_lag) ------------
-        wait_all(&bar_ds, ph_ds);
-        tc_fence_after();
-        {
-            const int f = r;
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(&rdy_a);
+
+            // ---------------- softmax pass 2: P (bf16 pairs) over the logits, in place ------
+            for (int kb = half; kb < nkb; kb += 2) {
+                float sv[32];
+                tmem_ld32(tlane + TM_S + 32 * kb, sv);
+                tmem_ld_wait();
+                const int clo = kb < P.nb ? blo - 32 * kb : 0;
+                const int chi = kb < P.nb ? bhi - 32 * kb : nvk - 1 - 32 * (kb - P.nb);
+                uint32_t w[16];
+#pragma unroll
+                for (int i = 0; i < 32; i += 2) {
+                    const float p0 = (i >= clo && i <= chi) ? exp2f(fmaf(sv[i], l2s, -cm)) : 0.f;
+                    const float p1 = (i + 1 >= clo && i + 1 <= chi) ? exp2f(fmaf(sv[i + 1], l2s, -cm)) : 0.f;
+                    den += p0 + p1;
+                    w[i / 2] = pack_bf16(p0, p1);
+                }
+                tmem_st16(tlane + TM_S + 32 * kb, w);
+            }
+            tmem_st1(tlane + TM_X + 10 + half, den);
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(&rdy_p);
+            if (sync_rows(bad)) break;
+            tc_fence_after();
+            const float dtot = den + tmem_ld1(tlane + TM_X + 10 + (1 - half));
+            tmem_ld_wait();
+
+            // ---------------- epilogue: y = O / den (my half of the columns) ---------------
+            bad = !wait(&bar_o, ph_o);
+            ph_o ^= 1;
+            tc_fence_after();
             {
-                float ds[DH];
+                const float inv = dtot != 0.f ? 1.f / dtot : 0.f;
+                float ov[DH];
 #pragma unroll
-                for (int c0 = 0; c0 < DH; c0 += 16) tmem_ld16(tlane + TM_S + half * DH + c0, *reinterpret_cast<float(*)[16]>(ds + c0));
+                for (int c0 = 0; c0 < DH; c0 += 16)
+                    tmem_ld16(tlane + TM_O + half * DH + c0, *reinterpret_cast<float(*)[16]>(ov + c0));
                 tmem_ld_wait();
 #pragma unroll
-                for (int i = 0; i < DH; ++i) srun[i] += ds[i];
-            }
-            if (f < DF) {
+                for (int c0 = 0; c0 < DH; c0 += 16) {
+                    const float *o = ov + c0;
 #pragma unroll
-                for (int c8 = 0; c8 < DH / 8; ++c8) {
-                    const int c = half * DH + c8 * 8;
-                    uint4 pk;
-                    pk.x = pack_bf16(srun[c8 * 8 + 0], srun[c8 * 8 + 1]);
-                    pk.y = pack_bf16(srun[c8 * 8 + 2], srun[c8 * 8 + 3]);
-                    pk.z = pack_bf16(srun[c8 * 8 + 4], srun[c8 * 8 + 5]);
-                    pk.w = pack_bf16(srun[c8 * 8 + 6], srun[c8 * 8 + 7]);
-                    *reinterpret_cast<uint4 *>(sm + Lay::SRUN + (c / 64) * (DF * 128) + sw128(f, (c % 64) / 8)) = pk;
-                }
-                if (half == 0) {
-                    float za = 0.f;
-                    const int cb = f / 64, c8 = (f % 64) / 8, e = f % 8;
-                    for (int tok = 0; tok < 32; ++tok)
-                        za += bf2f(*reinterpret_cast<const uint16_t *>(sm + Lay::PHIK + cb * 6144 + sw128(tok, c8) + e * 2));
-                    zrun[f] += za;
+                    for (int c8 = 0; c8 < 2; ++c8) {
+                        uint4 pk;
+                        pk.x = pack_bf16(o[c8 * 8 + 0] * inv, o[c8 * 8 + 1] * inv);
+                        pk.y = pack_bf16(o[c8 * 8 + 2] * inv, o[c8 * 8 + 3] * inv);
+                        pk.z = pack_bf16(o[c8 * 8 + 4] * inv, o[c8 * 8 + 5] * inv);
+                        pk.w = pack_bf16(o[c8 * 8 + 6] * inv, o[c8 * 8 + 7] * inv);
+                        const int d0 = half * DH + c0 + c8 * 8;
+                        *reinterpret_cast<uint4 *>(sm + Lay::PHIQ + (d0 / 64) * 16384 + sw128(r, (d0 % 64) / 8)) = pk;
+                    }
                 }
             }
-        }
-        fence_async_smem();
-        tc_fence_before();
-        __syncthreads();
-        if (tid == 0) {
-            for (int h2 = 0; h2 < dm.G; ++h2)
-                for (int cb = 0; cb < CBD; ++cb)
-                    tma_store_3d(&maps.out, sm + Lay::PHIQ + cb * 16384 + h2 * 4096, cb * 64, t0,
-                                 b * dm.Hq + g * dm.G + h2);
-            tma_store_commit();
-            if (has_next) load_lag(t0 + 32);
+            // ---------------- state update: S_run += dS, z_run += sum phi(K_lag) ------------
+            bad |= !wait(&bar_ds, ph_ds);
+            ph_ds ^= 1;
+            tc_fence_after();
+            {
+                const int f = r;
+                {
+                    float ds[DH];
+#pragma unroll
+                    for (int c0 = 0; c0 < DH; c0 += 16)
+                        tmem_ld16(tlane + TM_S + half * DH + c0, *reinterpret_cast<float(*)[16]>(ds + c0));
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < DH; ++i) srun[i] += ds[i];
+                }
+                if (f < DF) {
+#pragma unroll
+                    for (int c8 = 0; c8 < DH / 8; ++c8) {
+                        const int c = half * DH + c8 * 8;
+                        uint4 pk;
+                        pk.x = pack_bf16(srun[c8 * 8 + 0], srun[c8 * 8 + 1]);
+                        pk.y = pack_bf16(srun[c8 * 8 + 2], srun[c8 * 8 + 3]);
+                        pk.z = pack_bf16(srun[c8 * 8 + 4], srun[c8 * 8 + 5]);
+                        pk.w = pack_bf16(srun[c8 * 8 + 6], srun[c8 * 8 + 7]);
+                        *reinterpret_cast<uint4 *>(sm + Lay::SRUN + (c / 64) * (DF * 128) + sw128(f, (c % 64) / 8)) = pk;
+                    }
+                    if (half == 0) {
+                        float za = 0.f;
+                        const int cb = f / 64, c8 = (f % 64) / 8, e = f % 8;
+                        for (int tok = 0; tok < 32; ++tok)
+                            za += bf2f(*reinterpret_cast<const uint16_t *>(sm + Lay::PHIK + cb * 6144 + sw128(tok, c8) + e * 2));
+                        zrun[f] += za;
+                    }
+                }
+            }
+            fence_async_smem();
+            tc_fence_before();
+            mbar_arrive(&rdy_epi);
+            if (bad) *(volatile int *)&s_abort = 1;
         }
     }
 
-    if (tid == 0) tma_store_wait_all();
     tc_fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tmem, TM_COLS);
@@ -706,11 +723,11 @@ cudaError_t launch_hybrid_tc(const Dims &dm, const SegPlan &sp, const TCBuffers 
     if (D == 64) {
         e = cudaFuncSetAttribute(hybrid_tc_kernel<64, 64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        hybrid_tc_kernel<64, 64><<<grid, 256, smem, s>>>(m, p);
+        hybrid_tc_kernel<64, 64><<<grid, HT_THREADS, smem, s>>>(m, p);
     } else {
         e = cudaFuncSetAttribute(hybrid_tc_kernel<128, 128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        hybrid_tc_kernel<128, 128><<<grid, 256, smem, s>>>(m, p);
+        hybrid_tc_kernel<128, 128><<<grid, HT_THREADS, smem, s>>>(m, p);
     }
     return cudaGetLastError();
 }
