@@ -72,6 +72,16 @@ __device__ __forceinline__ float saliency_from_stats(float oth, float self)
     return -logf(oth / tot + 1e-6f);
 }
 
+// ---- 2^x on the MUFU unit: the PTX ex2.approx instruction, results below
+// 2^-126 flushed to zero (the weights it forms are rounded to bf16 or summed
+// in fp32, where such values do not count)
+__device__ __forceinline__ float exp2_mufu(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 // ---- NP-Map of one row, by one warp -------------------------------------------
 // x: the row in shared memory (fp32, D values); Wf: global fp32 [D, DF].
 // Writes phi (DF values) to `phi` (shared or global).

@@ -49,12 +49,16 @@ struct TCParams {
     int32_t *status;
 };
 
+// q and out: boxes of 32 tokens x 64 columns x G heads.  kband / vband: the
+// nb band blocks of a tile in one box; kk<n> / vk<n>: n blocks of 32 rows of
+// the kept tables; v / phik: the 32 lag rows; vk16 / phk16: the 16 rows of
+// the own-chunk kept tokens.
 struct TCMaps {
-    CUtensorMap q, k, v, kk, vk, vk16, phik, phk16, wft, out;
+    CUtensorMap q, out, kband, vband, kk32, kk64, kk128, vk32, vk64, vk128, v, vk16, phik, phk16, wft;
 };
 
 constexpr int TM_S = 0, TM_O = 320, TM_A = 448, TM_X = 496, TM_COLS = 512;   // TM_X: row exchange
-constexpr int MAX_KEY_BLOCKS = 10;   // 320 logit columns
+constexpr int MAX_KEY_BLOCKS = 9;    // 288 logit columns: every block of a tile stays resident
 constexpr int NX = 16;               // extra (kept, own chunk) rows per tile
 
 constexpr int RING_SLOTS = 9;        // K (then V) blocks of 32 keys resident
@@ -78,8 +82,8 @@ struct TCLayout {
 constexpr int HT_ROWS = 256;               // row threads: 8 warps, two per TMEM lane quarter
 constexpr int HT_THREADS = HT_ROWS + 128;  // and a warpgroup whose first thread issues every TMA copy and MMA
 // registers per thread after the split (launch: 168 x 384 = 64512; rows take
-// 208 x 256, the issuing warpgroup keeps 88 x 128: the same total)
-constexpr int HT_ROW_REGS = 208, HT_ISSUE_REGS = 88;
+// 216 x 256, the issuing warpgroup keeps 72 x 128: 62976 of them)
+constexpr int HT_ROW_REGS = 216, HT_ISSUE_REGS = 72;
 
 template <int D, int DF>
 __global__ void __launch_bounds__(HT_THREADS, 1) hybrid_tc_kernel(const __grid_constant__ TCMaps maps, TCParams P)
@@ -100,7 +104,7 @@ __global__ void __launch_bounds__(HT_THREADS, 1) hybrid_tc_kernel(const __grid_c
     // issuer -> rows: U, S, A (+ phi(Q) S_run), O, dS complete; rows -> issuer:
     // phi(Q) written, A masked, P written, tile finished (O and dS read,
     // output staged, S_run updated); issuer -> rows: output staging free
-    __shared__ uint64_t bar_q, bar_wf, bar_lag, bar_u, bar_s, bar_a, bar_o, bar_ds, bar_full[RING_SLOTS], bar_free;
+    __shared__ uint64_t bar_q, bar_wf, bar_lag, bar_u, bar_s, bar_a, bar_o, bar_ds, bar_k, bar_v;
     __shared__ uint64_t rdy_phiq, rdy_a, rdy_p, rdy_epi, stg_free;
     __shared__ uint32_t tmem_base;
     __shared__ int s_abort;
@@ -119,9 +123,8 @@ __global__ void __launch_bounds__(HT_THREADS, 1) hybrid_tc_kernel(const __grid_c
         tmem_relinquish();
     }
     if (tid == 0) {
-        for (uint64_t *bb : {&bar_q, &bar_wf, &bar_lag, &bar_u, &bar_s, &bar_a, &bar_o, &bar_ds, &bar_free, &stg_free})
+        for (uint64_t *bb : {&bar_q, &bar_wf, &bar_lag, &bar_u, &bar_s, &bar_a, &bar_o, &bar_ds, &bar_k, &bar_v, &stg_free})
             mbar_init(bb, 1);
-        for (int i = 0; i < RING_SLOTS; ++i) mbar_init(&bar_full[i], 1);
         for (uint64_t *bb : {&rdy_phiq, &rdy_a, &rdy_p, &rdy_epi}) mbar_init(bb, HT_ROWS);
         fence_barrier_init();
         s_abort = 0;
@@ -158,10 +161,8 @@ __global__ void __launch_bounds__(HT_THREADS, 1) hybrid_tc_kernel(const __grid_c
         if (warp == HT_ROWS / 32 && lane == 0 && ntiles > 0) {
             auto load_q = [&](int t0) {
                 mbar_expect_tx(&bar_q, dm.G * CBD * 4096);
-                for (int hh = 0; hh < dm.G; ++hh)
-                    for (int cb = 0; cb < CBD; ++cb)
-                        tma_load_3d(sm + Lay::Q + cb * 16384 + hh * 4096, &maps.q, &bar_q, cb * 64, t0,
-                                    b * dm.Hq + g * dm.G + hh);
+                for (int cb = 0; cb < CBD; ++cb)
+                    tma_load_3d(sm + Lay::Q + cb * 16384, &maps.q, &bar_q, cb * 64, t0, b * dm.Hq + g * dm.G);
             };
             auto load_lag = [&](int t0) {
                 const int ct = t0 / C;
@@ -176,35 +177,32 @@ __global__ void __launch_bounds__(HT_THREADS, 1) hybrid_tc_kernel(const __grid_c
                     tma_load_3d(sm + Lay::VLAG + cb * 6144 + 4096, &maps.vk16, &bar_lag, cb * 64, xrow, unit);
                 }
             };
-            // block kb (32 keys) of the key list of the tile at t0, K (kv = 0) or V (kv = 1), into ring slot kb % RING_SLOTS
-            auto load_blk = [&](int kb, int t0, int kv) {
-                const int slot = kb % RING_SLOTS;
-                uint8_t *dst = sm + Lay::RING + slot * 4096;
-                mbar_expect_tx(&bar_full[slot], SLOT);
-                const CUtensorMap *band = kv ? &maps.v : &maps.k;
-                const CUtensorMap *kept = kv ? &maps.vk : &maps.kk;
+            // the key blocks of the tile at t0 into ring slots 0 .. nkb-1: K (kv = 0) or V (kv = 1);
+            // the band in one box per column block, the kept prefix in boxes of 4, 2 and 1 blocks
+            auto load_keys = [&](int t0, int nkb, int kv) {
+                uint64_t *bar = kv ? &bar_v : &bar_k;
+                mbar_expect_tx(bar, nkb * SLOT);
                 for (int cb = 0; cb < CBD; ++cb) {
-                    if (kb < P.nb)
-                        tma_load_3d(dst + cb * RSTRIDE, band, &bar_full[slot], cb * 64, t0 - P.Wr + 32 * kb, unit);
-                    else
-                        tma_load_3d(dst + cb * RSTRIDE, kept, &bar_full[slot], cb * 64, 32 * (kb - P.nb), unit);
+                    uint8_t *dst = sm + Lay::RING + cb * RSTRIDE;
+                    tma_load_3d(dst, kv ? &maps.vband : &maps.kband, bar, cb * 64, t0 - P.Wr, unit);
+                    int kb = P.nb;
+                    while (kb < nkb) {
+                        const int n = nkb - kb >= 4 ? 4 : (nkb - kb >= 2 ? 2 : 1);
+                        const CUtensorMap *mp = n == 4 ? (kv ? &maps.vk128 : &maps.kk128)
+                                              : n == 2 ? (kv ? &maps.vk64 : &maps.kk64) : (kv ? &maps.vk32 : &maps.kk32);
+                        tma_load_3d(dst + kb * 4096, mp, bar, cb * 64, 32 * (kb - P.nb), unit);
+                        kb += n;
+                    }
                 }
             };
-            auto nkb_of = [&](int t0) { return P.nb + (min(t0 / C, dm.T_max) * lam + 31) / 32; };
             auto store_out = [&](int t0) {
-                for (int h2 = 0; h2 < dm.G; ++h2)
-                    for (int cb = 0; cb < CBD; ++cb)
-                        tma_store_3d(&maps.out, sm + Lay::PHIQ + cb * 16384 + h2 * 4096, cb * 64, t0,
-                                     b * dm.Hq + g * dm.G + h2);
+                for (int cb = 0; cb < CBD; ++cb)
+                    tma_store_3d(&maps.out, sm + Lay::PHIQ + cb * 16384, cb * 64, t0, b * dm.Hq + g * dm.G);
                 tma_store_commit();
             };
-            uint32_t ph_q = 0, ph_lag = 0, ph_s = 0, ph_o = 0, pe_phiq = 0, pe_a = 0, pe_p = 0, pe_epi = 0;
-            uint32_t ph_full = 0, ph_free = 0;   // one parity bit per ring slot
-            auto wait_slot = [&](int slot) {
-                const bool ok = wait(&bar_full[slot], (ph_full >> slot) & 1u);
-                ph_full ^= 1u << slot;
-                return ok;
-            };
+            auto nkb_of = [&](int t0) { return P.nb + (min(t0 / C, dm.T_max) * lam + 31) / 32; };
+            uint32_t ph_q = 0, ph_lag = 0, ph_s = 0, ph_o = 0, ph_k = 0, ph_v = 0;
+            uint32_t pe_phiq = 0, pe_a = 0, pe_p = 0, pe_epi = 0;
             const uint32_t id_u = idesc_bf16(128, DF, 0, 0);
             const uint32_t id_a = idesc_bf16(128, 32 + NX, 0, 0);
             const uint32_t id_o = idesc_bf16(128, D, 0, 1);
@@ -225,7 +223,7 @@ __global__ void __launch_bounds__(HT_THREADS, 1) hybrid_tc_kernel(const __grid_c
             for (int cb = 0; cb < CBD; ++cb) tma_load_2d(sm + Lay::WF + cb * DF * 128, &maps.wft, &bar_wf, cb * 64, 0);
             load_q(tbeg);
             load_lag(tbeg);
-            for (int kb = 0; kb < nkb_of(tbeg) && kb < RING_SLOTS; ++kb) load_blk(kb, tbeg, 0);
+            load_keys(tbeg, nkb_of(tbeg), 0);
             mbar_arrive(&stg_free);   // the staging buffer starts free
             bool ok = wait(&bar_wf, 0);
 
@@ -234,14 +232,13 @@ __global__ void __launch_bounds__(HT_THREADS, 1) hybrid_tc_kernel(const __grid_c
                 const int nkb = nkb_of(t0);
                 const bool has_next = it + 1 < ntiles;
                 if (it > 0) {
-                    // the rows are done with the previous tile: its output leaves, this tile's lag comes in
+                    // the rows are done with the previous tile (O and dS read, output staged)
                     ok &= wait(&rdy_epi, pe_epi);
                     pe_epi ^= 1;
-                    store_out(t0 - 32);
-                    load_lag(t0);
                 }
-                // U = Q Wf, then S = Q K^T: blocks 0 .. n1-1 in consecutive slots, one MMA of
-                // N = 32 min(n1, 8) per K step and one more for a ninth slot
+                // U = Q Wf first (the rows wait on it), then the previous output leaves and
+                // S = Q K^T: blocks 0 .. n1-1 in consecutive slots, one MMA of N = 32 min(n1, 8)
+                // per K step and one more for a ninth slot
                 ok &= wait(&bar_q, ph_q);
                 ph_q ^= 1;
                 tc_fence_after();
@@ -249,43 +246,32 @@ __global__ void __launch_bounds__(HT_THREADS, 1) hybrid_tc_kernel(const __grid_c
                 for (int k = 0; k < D; k += 16)
                     mma_ss(tmem + TM_O, dQ + koff(k, 16384), dWF + koff(k, DF * 128), id_u, k > 0);
                 mma_commit(&bar_u);
-                const int n1 = nkb < RING_SLOTS ? nkb : RING_SLOTS;
-                for (int kb = 0; kb < n1; ++kb) ok &= wait_slot(kb);
+                if (it > 0) store_out(t0 - 32);
+                ok &= wait(&bar_k, ph_k);
+                ph_k ^= 1;
                 tc_fence_after();
-                const int na = n1 < 8 ? n1 : 8;
+                const int na = nkb < 8 ? nkb : 8;
                 const uint32_t id_sa = idesc_bf16(128, 32 * na, 0, 0);
 #pragma unroll 1
                 for (int k = 0; k < D; k += 16)
                     mma_ss(tmem + TM_S, dQ + koff(k, 16384), dKR + koff(k, RSTRIDE), id_sa, k > 0);
-                if (n1 > 8) {
-                    const uint32_t id_sb = idesc_bf16(128, 32 * (n1 - 8), 0, 0);
+                if (nkb > 8) {
+                    const uint32_t id_sb = idesc_bf16(128, 32 * (nkb - 8), 0, 0);
 #pragma unroll 1
                     for (int k = 0; k < D; k += 16)
                         mma_ss(tmem + TM_S + 256, dQ + koff(k, 16384), dKR + koff(k, RSTRIDE) + (uint64_t)(8 * 4096 >> 4),
                                id_sb, k > 0);
                 }
-                if (nkb > RING_SLOTS) {
-                    // the rest reuse the first slots once the MMAs above have read them
-                    mma_commit(&bar_free);
-                    ok &= wait(&bar_free, ph_free);
-                    ph_free ^= 1;
-                    for (int kb = RING_SLOTS; kb < nkb; ++kb) load_blk(kb, t0, 0);
-                    for (int kb = RING_SLOTS; kb < nkb; ++kb) ok &= wait_slot(kb - RING_SLOTS);
-                    tc_fence_after();
-                    const uint32_t id_s2 = idesc_bf16(128, 32 * (nkb - RING_SLOTS), 0, 0);
-#pragma unroll 1
-                    for (int k = 0; k < D; k += 16)
-                        mma_ss(tmem + TM_S + 32 * RING_SLOTS, dQ + koff(k, 16384), dKR + koff(k, RSTRIDE), id_s2, k > 0);
-                }
                 mma_commit(&bar_s);
                 if (it > 0) {
+                    load_lag(t0);            // the previous tile's A, dS and z_run are done with it
                     tma_store_wait_read();   // the previous output has left the staging buffer
                     mbar_arrive(&stg_free);
                 }
                 // S complete: the ring takes this tile's V blocks
                 ok &= wait(&bar_s, ph_s);
                 ph_s ^= 1;
-                for (int kb = 0; kb < nkb && kb < RING_SLOTS; ++kb) load_blk(kb, t0, 1);
+                load_keys(t0, nkb, 1);
                 // phi(Q) written (and every row has read Q): A, O = phi(Q) S_run; the next Q
                 ok &= wait(&rdy_phiq, pe_phiq);
                 pe_phiq ^= 1;
@@ -310,24 +296,12 @@ __global__ void __launch_bounds__(HT_THREADS, 1) hybrid_tc_kernel(const __grid_c
                 ok &= wait(&rdy_p, pe_p);
                 pe_p ^= 1;
                 tc_fence_after();
-                for (int kb = 0; kb < n1; ++kb) {
-                    ok &= wait_slot(kb);
-                    tc_fence_after();
+                ok &= wait(&bar_v, ph_v);
+                ph_v ^= 1;
+                tc_fence_after();
+                for (int kb = 0; kb < nkb; ++kb) {
                     mma_ts(tmem + TM_O, tmem + TM_S + 32 * kb, dVR + (uint64_t)(kb * 4096 >> 4), id_o, 1);
-                    mma_ts(tmem + TM_O, tmem + TM_S + 32 * kb + 8, dVR + (uint64_t)((kb * 4096 + 2048) >> 4), id_o, 1);
-                }
-                if (nkb > RING_SLOTS) {
-                    mma_commit(&bar_free);
-                    ok &= wait(&bar_free, ph_free);
-                    ph_free ^= 1;
-                    for (int kb = RING_SLOTS; kb < nkb; ++kb) load_blk(kb, t0, 1);
-                    for (int kb = RING_SLOTS; kb < nkb; ++kb) {
-                        const int slot = kb - RING_SLOTS;
-                        ok &= wait_slot(slot);
-                        tc_fence_after();
-                        mma_ts(tmem + TM_O, tmem + TM_S + 32 * kb, dVR + (uint64_t)(slot * 4096 >> 4), id_o, 1);
-                        mma_ts(tmem + TM_O, tmem + TM_S + 32 * kb + 8, dVR + (uint64_t)((slot * 4096 + 2048) >> 4), id_o, 1);
-                    }
+                    mma_ts(tmem + TM_O, tmem + TM_S + 32 * kb + 16, dVR + (uint64_t)((kb * 4096 + 2048) >> 4), id_o, 1);
                 }
                 mma_commit(&bar_o);
                 // every read of P and of the ring is done: dS into the logit columns, the next K blocks
@@ -338,8 +312,7 @@ __global__ void __launch_bounds__(HT_THREADS, 1) hybrid_tc_kernel(const __grid_c
                     mma_ss(tmem + TM_S, sdesc(sb + Lay::PHIK + kk * 128, 6144, 1024),
                            sdesc(sb + Lay::VLAG + kk * 128, 6144, 1024), id_ds, kk > 0);
                 mma_commit(&bar_ds);
-                if (has_next)
-                    for (int kb = 0; kb < nkb_of(t0 + 32) && kb < RING_SLOTS; ++kb) load_blk(kb, t0 + 32, 0);
+                if (has_next) load_keys(t0 + 32, nkb_of(t0 + 32), 0);
             }
             if (ok && wait(&rdy_epi, pe_epi)) store_out(tbeg + (ntiles - 1) * 32);
             tma_store_wait_all();
@@ -427,7 +400,7 @@ __global__ void __launch_bounds__(HT_THREADS, 1) hybrid_tc_kernel(const __grid_c
             for (int i = 0; i < DFH; ++i) mu = fmaxf(mu, eu[i] * LOG2E);
 #pragma unroll
             for (int i = 0; i < DFH; ++i) {
-                eu[i] = exp2f(fmaf(eu[i], LOG2E, -mu));
+                eu[i] = exp2_mufu(fmaf(eu[i], LOG2E, -mu));
                 s2 = fmaf(eu[i], eu[i], s2);
             }
             {
@@ -495,23 +468,49 @@ __global__ void __launch_bounds__(HT_THREADS, 1) hybrid_tc_kernel(const __grid_c
             bad |= !wait(&bar_s, ph_s);
             ph_s ^= 1;
             tc_fence_after();
+            // every 32-key block is split between the two halves: keys [16 half, 16 half + 16)
+            // of block kb are columns TM_S + 32 kb + 16 half ..; masks are row ranges, so a
+            // 16-key group is often fully in or fully out for the whole warp
+            auto key_range = [&](int kb, int &clo, int &chi) {
+                clo = (kb < P.nb ? blo - 32 * kb : 0) - 16 * half;
+                chi = (kb < P.nb ? bhi - 32 * kb : nvk - 1 - 32 * (kb - P.nb)) - 16 * half;
+            };
+            // the logits pass one block at a time through registers, software-pipelined:
+            // the next block's TMEM load is in flight while this one is worked on
+            struct Blk {
+                int clo, chi;
+                bool skip, full;
+            };
+            auto blk_load = [&](int kb, Blk &bi, float (&sv)[16]) {
+                key_range(kb, bi.clo, bi.chi);
+                bi.skip = __all_sync(0xffffffffu, bi.chi < 0 || bi.clo > 15);
+                bi.full = __all_sync(0xffffffffu, bi.clo <= 0 && bi.chi >= 15);
+                if (!bi.skip) tmem_ld16(tlane + TM_S + 32 * kb + 16 * half, sv);
+            };
+            float sva[16], svb[16];
+            Blk ba, bb;
             float cmax = -INFINITY;
-            for (int kb = half; kb < nkb; kb += 4) {
-                float sv[2][32];
-                const bool two = kb + 2 < nkb;
-                tmem_ld32(tlane + TM_S + 32 * kb, sv[0]);
-                if (two) tmem_ld32(tlane + TM_S + 32 * (kb + 2), sv[1]);
-                tmem_ld_wait();
+            auto cmax_blk = [&](const Blk &bi, const float (&sv)[16]) {
+                if (bi.skip) return;
+                if (bi.full) {
 #pragma unroll
-                for (int x = 0; x < 2; ++x) {
-                    if (x == 1 && !two) break;
-                    const int bk = kb + 2 * x;
-                    const int clo = bk < P.nb ? blo - 32 * bk : 0;
-                    const int chi = bk < P.nb ? bhi - 32 * bk : nvk - 1 - 32 * (bk - P.nb);
+                    for (int i = 0; i < 16; ++i) cmax = fmaxf(cmax, sv[i]);
+                } else {
 #pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        if (i >= clo && i <= chi) cmax = fmaxf(cmax, sv[x][i]);
+                    for (int i = 0; i < 16; ++i)
+                        if (i >= bi.clo && i <= bi.chi) cmax = fmaxf(cmax, sv[i]);
                 }
+            };
+            blk_load(0, ba, sva);
+            for (int kb = 0; kb < nkb;) {
+                tmem_ld_wait();
+                if (kb + 1 < nkb) blk_load(kb + 1, bb, svb);
+                cmax_blk(ba, sva);
+                if (++kb >= nkb) break;
+                tmem_ld_wait();
+                if (kb + 1 < nkb) blk_load(kb + 1, ba, sva);
+                cmax_blk(bb, svb);
+                ++kb;
             }
             tmem_st1(tlane + TM_X + 8 + half, cmax);
             tmem_st_wait();
@@ -558,21 +557,43 @@ __global__ void __launch_bounds__(HT_THREADS, 1) hybrid_tc_kernel(const __grid_c
             mbar_arrive(&rdy_a);
 
             // ---------------- softmax pass 2: P (bf16 pairs) over the logits, in place ------
-            for (int kb = half; kb < nkb; kb += 2) {
-                float sv[32];
-                tmem_ld32(tlane + TM_S + 32 * kb, sv);
-                tmem_ld_wait();
-                const int clo = kb < P.nb ? blo - 32 * kb : 0;
-                const int chi = kb < P.nb ? bhi - 32 * kb : nvk - 1 - 32 * (kb - P.nb);
-                uint32_t w[16];
+            // keys [16 half, 16 half + 16) of block kb become 8 packed columns at the start of
+            // the 16 they came from
+            auto p_blk = [&](int kb, const Blk &bi, const float (&sv)[16]) {
+                uint32_t w[8];
+                if (bi.skip) {
 #pragma unroll
-                for (int i = 0; i < 32; i += 2) {
-                    const float p0 = (i >= clo && i <= chi) ? exp2f(fmaf(sv[i], l2s, -cm)) : 0.f;
-                    const float p1 = (i + 1 >= clo && i + 1 <= chi) ? exp2f(fmaf(sv[i + 1], l2s, -cm)) : 0.f;
-                    den += p0 + p1;
-                    w[i / 2] = pack_bf16(p0, p1);
+                    for (int i = 0; i < 8; ++i) w[i] = 0u;
+                } else if (bi.full) {
+#pragma unroll
+                    for (int i = 0; i < 16; i += 2) {
+                        const float p0 = exp2_mufu(fmaf(sv[i], l2s, -cm));
+                        const float p1 = exp2_mufu(fmaf(sv[i + 1], l2s, -cm));
+                        den += p0 + p1;
+                        w[i / 2] = pack_bf16(p0, p1);
+                    }
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 16; i += 2) {
+                        const float p0 = (i >= bi.clo && i <= bi.chi) ? exp2_mufu(fmaf(sv[i], l2s, -cm)) : 0.f;
+                        const float p1 =
+                            (i + 1 >= bi.clo && i + 1 <= bi.chi) ? exp2_mufu(fmaf(sv[i + 1], l2s, -cm)) : 0.f;
+                        den += p0 + p1;
+                        w[i / 2] = pack_bf16(p0, p1);
+                    }
                 }
-                tmem_st16(tlane + TM_S + 32 * kb, w);
+                tmem_st8(tlane + TM_S + 32 * kb + 16 * half, w);
+            };
+            blk_load(0, ba, sva);
+            for (int kb = 0; kb < nkb;) {
+                tmem_ld_wait();
+                if (kb + 1 < nkb) blk_load(kb + 1, bb, svb);
+                p_blk(kb, ba, sva);
+                if (++kb >= nkb) break;
+                tmem_ld_wait();
+                if (kb + 1 < nkb) blk_load(kb + 1, ba, sva);
+                p_blk(kb, bb, svb);
+                ++kb;
             }
             tmem_st1(tlane + TM_X + 10 + half, den);
             tmem_st_wait();
@@ -666,6 +687,7 @@ bool hybrid_tc_supported(const Dims &dm)
     if (dm.C % 32 != 0 || dm.lam > NX) return false;
     const int Wr = dm.W >= 1 ? (dm.W - 1 + 31) / 32 * 32 : 0;
     const int nb = (Wr + 32) / 32;
+    if (nb > 8) return false;   // the band is one TMA box of at most 256 rows
     const int nchunks = (dm.N + dm.C - 1) / dm.C;
     const int maxg = dm.lam * min(dm.T_max, max(nchunks - 1, 0));
     return nb + (maxg + 31) / 32 <= MAX_KEY_BLOCKS;
@@ -686,19 +708,26 @@ cudaError_t launch_hybrid_tc(const Dims &dm, const SegPlan &sp, const TCBuffers 
     TCMaps m;
     bool ok = true;
     {
+        const int nb = dm.W >= 1 ? ((dm.W - 1 + 31) / 32 * 32 + 32) / 32 : 1;
         uint64_t dq[3] = {(uint64_t)D, (uint64_t)dm.N, heads}, sq[2] = {(uint64_t)D * 2, (uint64_t)D * 2 * dm.N};
-        uint32_t box[3] = {64, 32, 1};
-        ok &= make_tma_map(&m.q, bf.q, 3, dq, sq, box, true);
-        ok &= make_tma_map(&m.out, bf.out, 3, dq, sq, box, true);
+        uint32_t boxg[3] = {64, 32, (uint32_t)dm.G};
+        ok &= make_tma_map(&m.q, bf.q, 3, dq, sq, boxg, true);
+        ok &= make_tma_map(&m.out, bf.out, 3, dq, sq, boxg, true);
         uint64_t dk[3] = {(uint64_t)D, (uint64_t)dm.N, units};
-        ok &= make_tma_map(&m.k, bf.k, 3, dk, sq, box, true);
+        uint32_t box[3] = {64, 32, 1}, boxb[3] = {64, (uint32_t)(32 * nb), 1};
+        ok &= make_tma_map(&m.kband, bf.k, 3, dk, sq, boxb, true);
+        ok &= make_tma_map(&m.vband, bf.v, 3, dk, sq, boxb, true);
         ok &= make_tma_map(&m.v, bf.v, 3, dk, sq, box, true);
         uint64_t df3[3] = {(uint64_t)DF, (uint64_t)dm.N, units}, sf[2] = {(uint64_t)DF * 2, (uint64_t)DF * 2 * dm.N};
         ok &= make_tma_map(&m.phik, bf.phik, 3, df3, sf, box, true);
         uint64_t dkp[3] = {(uint64_t)D, (uint64_t)KP, units}, skp[2] = {(uint64_t)D * 2, (uint64_t)D * 2 * KP};
-        ok &= make_tma_map(&m.kk, bf.kk, 3, dkp, skp, box, true);
-        ok &= make_tma_map(&m.vk, bf.vk, 3, dkp, skp, box, true);
-        uint32_t box16[3] = {64, 16, 1};
+        uint32_t b32[3] = {64, 32, 1}, b64[3] = {64, 64, 1}, b128[3] = {64, 128, 1}, box16[3] = {64, 16, 1};
+        ok &= make_tma_map(&m.kk32, bf.kk, 3, dkp, skp, b32, true);
+        ok &= make_tma_map(&m.kk64, bf.kk, 3, dkp, skp, b64, true);
+        ok &= make_tma_map(&m.kk128, bf.kk, 3, dkp, skp, b128, true);
+        ok &= make_tma_map(&m.vk32, bf.vk, 3, dkp, skp, b32, true);
+        ok &= make_tma_map(&m.vk64, bf.vk, 3, dkp, skp, b64, true);
+        ok &= make_tma_map(&m.vk128, bf.vk, 3, dkp, skp, b128, true);
         ok &= make_tma_map(&m.vk16, bf.vk, 3, dkp, skp, box16, true);
         uint64_t dpk[3] = {(uint64_t)DF, (uint64_t)KP, units}, spk[2] = {(uint64_t)DF * 2, (uint64_t)DF * 2 * KP};
         ok &= make_tma_map(&m.phk16, bf.phk, 3, dpk, spk, box16, true);

@@ -176,7 +176,7 @@ __global__ void __launch_bounds__(128, 1) linstate_tc_kernel(const __grid_consta
             }
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
-                const float e = exp2f(fmaf(u[i], LOG2E, -mu));
+                const float e = exp2_mufu(fmaf(u[i], LOG2E, -mu));
                 s2 = fmaf(e, e, s2);
             }
         }
@@ -199,7 +199,7 @@ __global__ void __launch_bounds__(128, 1) linstate_tc_kernel(const __grid_consta
 #pragma unroll
                 for (int h2 = 0; h2 < 4; ++h2) {
                     const int i = c8 * 8 + h2 * 2;
-                    w4[h2] = pack_bf16(sc * exp2f(fmaf(u[i], LOG2E, -mu)), sc * exp2f(fmaf(u[i + 1], LOG2E, -mu)));
+                    w4[h2] = pack_bf16(sc * exp2_mufu(fmaf(u[i], LOG2E, -mu)), sc * exp2_mufu(fmaf(u[i + 1], LOG2E, -mu)));
                 }
                 const int f0 = c0 + c8 * 8;
                 const uint4 val = make_uint4(w4[0], w4[1], w4[2], w4[3]);

@@ -165,7 +165,7 @@ __global__ void __launch_bounds__(256, 1) score_tc_kernel(const __grid_constant_
             if (m != -INFINITY) {
 #pragma unroll
                 for (int x = 0; x < 16; ++x) {
-                    const float e = exp2f(v[x] - m);
+                    const float e = exp2_mufu(v[x] - m);
                     if (c_beg + c0 + x == self_c) slf += e;
                     else oth += e;
                 }
