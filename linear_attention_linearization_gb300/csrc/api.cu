@@ -100,17 +100,34 @@ SegPlan plan_segments(const Dims &dm)
     sp.T = 32;
     const int ntile = (dm.N + sp.T - 1) / sp.T;
     const int units = dm.B * dm.Hkv;
-    int target = 152 / units;
+    int target = MAX_SEGMENTS / (units > 0 ? units : 1);
     if (target < 1) target = 1;
     if (target > ntile) target = ntile;
     if (ntile == 0) {
-        sp.L = sp.T;
         sp.nseg = 1;
+        sp.begin[0] = 0;
+        sp.begin[1] = dm.N;
         return sp;
     }
-    const int tiles_per = (ntile + target - 1) / target;
-    sp.L = tiles_per * sp.T;
-    sp.nseg = (dm.N + sp.L - 1) / sp.L;
+    // work of a tile: a fixed part (NP-Map, epilogues, state update) worth about
+    // 512 keys, plus the softmax keys it attends (window and kept tokens)
+    auto cost = [&](int tile) {
+        const int ct = tile * sp.T / dm.C;
+        return 512.0 + dm.W + (double)(ct < dm.T_max ? ct : dm.T_max) * dm.lam;
+    };
+    double total = 0.0;
+    for (int i = 0; i < ntile; ++i) total += cost(i);
+    sp.nseg = target;
+    sp.begin[0] = 0;
+    double acc = 0.0;
+    int s = 1, i = 0;
+    for (; i < ntile && s < target; ++i) {
+        acc += cost(i);
+        // cut after tile i once this segment has its share, leaving a tile for each later one
+        if (acc >= total * s / target || ntile - (i + 1) == target - s) sp.begin[s++] = (i + 1) * sp.T;
+    }
+    sp.nseg = s;
+    sp.begin[s] = dm.N;
     return sp;
 }
 

@@ -19,12 +19,15 @@ struct Dims {
 };
 
 // Segment plan of the chunk-parallel prefill: CTA s of a (sequence, kv head)
-// walks query tiles [s*L, (s+1)*L) in order, starting from the linear state of
-// the keys that left the window before its first tile.
+// walks the query tiles of [begin[s], begin[s+1]) in order, starting from the
+// linear state of the keys that left the window before its first tile.
+// Segments are cut so that their attention work (not their token counts) is
+// even: tiles late in the sequence see more kept keys.
+constexpr int MAX_SEGMENTS = 152;
 struct SegPlan {
     int T;      // query tokens per tile
-    int L;      // tokens per segment (multiple of T)
     int nseg;   // segments per (sequence, kv head)
+    int begin[MAX_SEGMENTS + 1];   // first token of each segment (multiples of T); begin[nseg] = N
 };
 
 // ---- bf16 ------------------------------------------------------------------

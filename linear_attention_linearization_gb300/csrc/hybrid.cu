@@ -61,7 +61,7 @@ __global__ void __launch_bounds__(256) hybrid_kernel(const uint16_t *__restrict_
     }
     __syncthreads();
 
-    const int tbeg = s * sp.L, tend = min((s + 1) * sp.L, dm.N);
+    const int tbeg = sp.begin[s], tend = sp.begin[s + 1];
     for (int t0 = tbeg; t0 < tend; t0 += sp.T) {
         const int nt = min(sp.T, tend - t0);
         const int e0 = t0 - dm.W;

@@ -114,7 +114,7 @@ __global__ void __launch_bounds__(HT_THREADS, 1) hybrid_tc_kernel(const __grid_c
     const int s = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
     const int unit = b * dm.Hkv + g;
     const int W = dm.W, C = dm.C, lam = dm.lam;
-    const int tbeg = s * P.sp.L, tend = min((s + 1) * P.sp.L, dm.N);
+    const int tbeg = P.sp.begin[s], tend = P.sp.begin[s + 1];
     const int ntiles = (tend - tbeg + 31) / 32;
     const int32_t *fs = P.fsel + (size_t)unit * P.KP;
 
@@ -236,9 +236,11 @@ __global__ void __launch_bounds__(HT_THREADS, 1) hybrid_tc_kernel(const __grid_c
                     ok &= wait(&rdy_epi, pe_epi);
                     pe_epi ^= 1;
                 }
-                // U = Q Wf first (the rows wait on it), then the previous output leaves and
-                // S = Q K^T: blocks 0 .. n1-1 in consecutive slots, one MMA of N = 32 min(n1, 8)
-                // per K step and one more for a ninth slot
+                // the previous output leaves, U = Q Wf (the rows wait on it), the staging buffer
+                // is handed back once the store has read it, then S = Q K^T: blocks 0 .. nkb-1
+                // in consecutive slots, one MMA of N = 32 min(nkb, 8) per K step and one more for
+                // a ninth slot
+                if (it > 0) store_out(t0 - 32);
                 ok &= wait(&bar_q, ph_q);
                 ph_q ^= 1;
                 tc_fence_after();
@@ -246,7 +248,10 @@ __global__ void __launch_bounds__(HT_THREADS, 1) hybrid_tc_kernel(const __grid_c
                 for (int k = 0; k < D; k += 16)
                     mma_ss(tmem + TM_O, dQ + koff(k, 16384), dWF + koff(k, DF * 128), id_u, k > 0);
                 mma_commit(&bar_u);
-                if (it > 0) store_out(t0 - 32);
+                if (it > 0) {
+                    tma_store_wait_read();
+                    mbar_arrive(&stg_free);
+                }
                 ok &= wait(&bar_k, ph_k);
                 ph_k ^= 1;
                 tc_fence_after();
@@ -263,11 +268,7 @@ __global__ void __launch_bounds__(HT_THREADS, 1) hybrid_tc_kernel(const __grid_c
                                id_sb, k > 0);
                 }
                 mma_commit(&bar_s);
-                if (it > 0) {
-                    load_lag(t0);            // the previous tile's A, dS and z_run are done with it
-                    tma_store_wait_read();   // the previous output has left the staging buffer
-                    mbar_arrive(&stg_free);
-                }
+                if (it > 0) load_lag(t0);   // the previous tile's A, dS and z_run are done with it
                 // S complete: the ring takes this tile's V blocks
                 ok &= wait(&bar_s, ph_s);
                 ph_s ^= 1;

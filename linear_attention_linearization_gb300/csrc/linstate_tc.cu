@@ -13,9 +13,9 @@
 //             kernel copies its K and V rows there)
 //   dS  += phi_blk^T V_blk                   (tcgen05, accumulated in TMEM)
 //   dz  += column sums of phi_blk            (CUDA cores)
-// The range is [s*L - W, (s+1)*L - W) clipped to [0, N): the keys that leave
-// the window while segment s runs (the last segment also writes the features
-// of the final W keys).  Only keys below N - W enter dS: the others never
+// The range is [b_s - W, b_{s+1} - W) clipped to [0, N), b_s the first token
+// of segment s: the keys that leave the window while segment s runs (the last
+// segment also writes the features of the final W keys).  Only keys below N - W enter dS: the others never
 // leave the window.  An exclusive scan over segments then gives each
 // segment's starting state.
 #include "sm100.cuh"
@@ -67,8 +67,8 @@ __global__ void __launch_bounds__(128, 1) linstate_tc_kernel(const __grid_consta
     const int tid = threadIdx.x, warp = tid >> 5;
     const int s = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
     const size_t unit = (size_t)b * dm.Hkv + g;
-    const int klo = max(0, s * P.sp.L - dm.W);
-    const int fhi = min((s + 1) * P.sp.L, dm.N) - dm.W;                   // keys folded: [klo, fhi)
+    const int klo = max(0, P.sp.begin[s] - dm.W);
+    const int fhi = P.sp.begin[s + 1] - dm.W;                              // keys folded: [klo, fhi)
     const int khi = s == P.sp.nseg - 1 ? dm.N : max(fhi, klo);            // features written: [klo, khi)
     const int nblk = khi > klo ? (khi - klo + 127) / 128 : 0;
 
