@@ -8,12 +8,11 @@
 //
 // Persistent CTAs walk tiles of 32 tokens of one (sequence, kv head): the
 // G <= 4 query heads x 32 tokens form the M = 128 rows of one MMA against the
-// band of keys [t0 - Wr, t0 + 32) that holds every window of the tile.  The
-// logits stay in TMEM; 8 warps (two per TMEM lane quarter, each owning half of
-// the band columns) reduce each row to (max, off-diagonal mass, self mass).
-// Tiles are pipelined over up to four shared-memory / TMEM stages: while the
-// row warps reduce tile i, the MMA of tile i+1 runs and the loads of the
-// following tiles are in flight.
+// band of keys [t0 - Wr, t0 + 32) that holds every window of the tile.  One
+// thread of a fourth warpgroup issues the TMA copies and the MMAs, tiles
+// pipelined over up to four shared-memory / TMEM stages; 8 row warps (two per
+// TMEM lane quarter, each owning half of the band columns) reduce each row to
+// (max, off-diagonal mass, self mass) while the next tiles load and multiply.
 #include "sm100.cuh"
 #include "tma_host.cuh"
 
@@ -24,6 +23,8 @@ using namespace sm100;
 namespace {
 constexpr int SC_MAX_NB = 8;         // band blocks of 32 keys (W <= 225)
 constexpr int SC_MAX_STAGES = 4;     // tiles in flight
+constexpr int SC_ROWS = 256;         // row threads
+constexpr int SC_THREADS = SC_ROWS + 128;
 constexpr size_t SC_SMEM_CAP = 227 * 1024 - 4096;   // dynamic share of the 227 KB per-block limit
 }
 
@@ -36,21 +37,25 @@ struct ScoreTCParams {
     float *scores;
 };
 
+// q: boxes of 32 tokens x 64 columns x G heads; k: the nb band blocks in one box
 struct ScoreTCMaps {
     CUtensorMap q, k;
 };
 
-template <int D>
-__global__ void __launch_bounds__(256, 1) score_tc_kernel(const __grid_constant__ ScoreTCMaps maps, ScoreTCParams P)
+template <int D, int NB>
+__global__ void __launch_bounds__(SC_THREADS, 1) score_tc_kernel(const __grid_constant__ ScoreTCMaps maps, ScoreTCParams P)
 {
     constexpr int CBD = D / 64;
     constexpr uint32_t QB = CBD * 16384;          // Q tile bytes
+    constexpr long long WAIT_LIMIT = 4000000000LL;   // cycles
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     const uint32_t sb = smem_u32(sm);
-    __shared__ uint64_t bar_full[SC_MAX_STAGES], bar_mma[SC_MAX_STAGES];
+    // full: a stage's Q and K arrived; mma: its logits are in TMEM (and its
+    // shared memory is free); tfree: the rows have read its TMEM columns
+    __shared__ uint64_t bar_full[SC_MAX_STAGES], bar_mma[SC_MAX_STAGES], bar_tfree[SC_MAX_STAGES];
     __shared__ uint32_t tmem_base;
-    __shared__ float xch[2][128][3];
+    __shared__ float xch[128][3];
     __shared__ float hsc[4][32];
     __shared__ int s_abort;
 
@@ -58,24 +63,25 @@ __global__ void __launch_bounds__(256, 1) score_tc_kernel(const __grid_constant_
     const int NS = P.stages;
     const uint32_t STB = P.stage_bytes, KBB = P.nb * 4096;   // bytes of a stage, of one K column block
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int quarter = warp & 3, half = warp >> 2;
-    const int r = quarter * 32 + lane, hh = r / 32, tt = r % 32;
-    const int ncols = P.nb * 32, hcols = ncols / 2;
-    const int W = dm.W;
-    const float l2s = 1.4426950408889634f * rsqrtf((float)D);   // log2(e) / sqrt(d)
+    const int first = blockIdx.x, step = gridDim.x;
+    const int my_tiles = first < P.total_tiles ? (P.total_tiles - first + step - 1) / step : 0;
 
     if (warp == 0) {
         tmem_alloc(&tmem_base, 512);
         tmem_relinquish();
     }
     if (tid == 0) {
-        for (int i = 0; i < NS; ++i) { mbar_init(&bar_full[i], 1); mbar_init(&bar_mma[i], 1); }
+        for (int i = 0; i < NS; ++i) {
+            mbar_init(&bar_full[i], 1);
+            mbar_init(&bar_mma[i], 1);
+            mbar_init(&bar_tfree[i], SC_ROWS);
+        }
         fence_barrier_init();
         s_abort = 0;
     }
     // padding rows of absent heads: zero in every stage buffer, never written again
     for (int st = 0; st < NS; ++st)
-        for (int i = tid; i < (int)(QB / 16); i += 256) {
+        for (int i = tid; i < (int)(QB / 16); i += SC_THREADS) {
             const int row = (i * 16 % 16384) / 128;
             if (row >= dm.G * 32) reinterpret_cast<uint4 *>(sm + st * STB)[i] = make_uint4(0, 0, 0, 0);
         }
@@ -84,118 +90,144 @@ __global__ void __launch_bounds__(256, 1) score_tc_kernel(const __grid_constant_
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = tmem_base;
-    const uint32_t tlane = tmem + ((uint32_t)(quarter * 32) << 16);
 
-    const int first = blockIdx.x, step = gridDim.x;
-    const int my_tiles = first < P.total_tiles ? (P.total_tiles - first + step - 1) / step : 0;
-    const uint32_t idesc = idesc_bf16(128, ncols, 0, 0);
-    const uint64_t d0 = sdesc(sb, 16, 1024);
-
+    auto wait = [&](uint64_t *bar, uint32_t parity) -> bool {
+        if (mbar_try_wait(bar, parity)) return true;
+        const long long c0 = clock64();
+        while (!mbar_try_wait(bar, parity)) {
+            if (*(volatile int *)&s_abort) return false;
+            if (clock64() - c0 > WAIT_LIMIT) {
+                *(volatile int *)&s_abort = 1;
+                return false;
+            }
+        }
+        return true;
+    };
     auto tile_coords = [&](int i, int &unit, int &t0) {
         const int tile = first + i * step;
         unit = tile / P.tiles_per_unit;
         t0 = (tile % P.tiles_per_unit) * 32;
     };
-    auto issue_load = [&](int i) {
-        int unit, t0;
-        tile_coords(i, unit, t0);
-        const int st = i % NS;
-        uint8_t *qd = sm + st * STB;
-        uint8_t *kd = qd + QB;
-        const int b = unit / dm.Hkv, g = unit % dm.Hkv;
-        mbar_expect_tx(&bar_full[st], dm.G * CBD * 4096 + P.nb * CBD * 4096);
-        for (int h = 0; h < dm.G; ++h)
-            for (int cb = 0; cb < CBD; ++cb)
-                tma_load_3d(qd + cb * 16384 + h * 4096, &maps.q, &bar_full[st], cb * 64, t0, b * dm.Hq + g * dm.G + h);
-        for (int kb = 0; kb < P.nb; ++kb)
-            for (int cb = 0; cb < CBD; ++cb)
-                tma_load_3d(kd + cb * KBB + kb * 4096, &maps.k, &bar_full[st], cb * 64, t0 - P.Wr + 32 * kb, unit);
-    };
-    uint32_t ph_full = 0, ph_mma = 0;   // one parity bit per stage
-    auto issue_mma = [&](int i) {
-        const int st = i % NS;
-        if (!mbar_wait(&bar_full[st], (ph_full >> st) & 1u, nullptr)) { s_abort = 1; return; }
-        ph_full ^= 1u << st;
-        tc_fence_after();
-        const uint64_t qa = d0 + ((st * STB) >> 4), ka = qa + (QB >> 4);
+
+    if (warp >= SC_ROWS / 32) {
+        // ======================= the issuing warpgroup =======================
+        regs_dec<56>();
+        if (warp == SC_ROWS / 32 && lane == 0 && my_tiles > 0) {
+            const uint32_t idesc = idesc_bf16(128, P.nb * 32, 0, 0);
+            const uint64_t d0 = sdesc(sb, 16, 1024);
+            auto issue_load = [&](int i) {
+                int unit, t0;
+                tile_coords(i, unit, t0);
+                const int st = i % NS;
+                uint8_t *qd = sm + st * STB;
+                uint8_t *kd = qd + QB;
+                const int b = unit / dm.Hkv, g = unit % dm.Hkv;
+                mbar_expect_tx(&bar_full[st], dm.G * CBD * 4096 + P.nb * CBD * 4096);
+                for (int cb = 0; cb < CBD; ++cb) {
+                    tma_load_3d(qd + cb * 16384, &maps.q, &bar_full[st], cb * 64, t0, b * dm.Hq + g * dm.G);
+                    tma_load_3d(kd + cb * KBB, &maps.k, &bar_full[st], cb * 64, t0 - P.Wr, unit);
+                }
+            };
+            uint32_t ph_full = 0, ph_mma = 0, ph_tf = 0;   // one parity bit per stage
+            bool ok = true;
+            for (int i = 0; i < NS && i < my_tiles; ++i) issue_load(i);
+            for (int i = 0; i < my_tiles && ok; ++i) {
+                const int st = i % NS;
+                ok &= wait(&bar_full[st], (ph_full >> st) & 1u);
+                ph_full ^= 1u << st;
+                if (i >= NS) {   // the rows are done with tile i - NS in this TMEM stage
+                    ok &= wait(&bar_tfree[st], (ph_tf >> st) & 1u);
+                    ph_tf ^= 1u << st;
+                }
+                tc_fence_after();
+                const uint64_t qa = d0 + ((st * STB) >> 4), ka = qa + (QB >> 4);
+#pragma unroll 1
+                for (int k = 0; k < D; k += 16)
+                    mma_ss(tmem + st * P.tmem_stride, qa + (((k / 64) * 16384 + (k % 64) * 2) >> 4),
+                           ka + (((k / 64) * KBB + (k % 64) * 2) >> 4), idesc, k > 0);
+                mma_commit(&bar_mma[st]);
+                if (i + NS < my_tiles) {
+                    // the stage's shared memory is free once this MMA has read it
+                    ok &= wait(&bar_mma[st], (ph_mma >> st) & 1u);
+                    issue_load(i + NS);
+                }
+                ph_mma ^= 1u << st;
+            }
+        }
+        __syncwarp();
+    } else {
+        // ============================= the row warps =============================
+        regs_inc<224>();
+        const int quarter = warp & 3, half = warp >> 2;
+        const int r = quarter * 32 + lane, hh = r / 32, tt = r % 32;
+        constexpr int HC = NB * 16;   // band columns per half-row thread
+        const int W = dm.W;
+        const float l2s = 1.4426950408889634f * rsqrtf((float)D);   // log2(e) / sqrt(d)
+        const uint32_t tlane = tmem + ((uint32_t)(quarter * 32) << 16);
+        const int c_beg = half * HC;
+        uint32_t ph_mma = 0;
+        for (int i = 0; i < my_tiles; ++i) {
+            const int st = i % NS;
+            int unit, t0;
+            tile_coords(i, unit, t0);
+            bool bad = !wait(&bar_mma[st], (ph_mma >> st) & 1u);
+            ph_mma ^= 1u << st;
+            tc_fence_after();
+
+            // this thread's half of the band columns: all its TMEM loads, then one wait
+            float v[HC];
 #pragma unroll
-        for (int k = 0; k < D; k += 16)
-            mma_ss(tmem + st * P.tmem_stride, qa + (((k / 64) * 16384 + (k % 64) * 2) >> 4),
-                   ka + (((k / 64) * KBB + (k % 64) * 2) >> 4), idesc, k > 0);
-        mma_commit(&bar_mma[st]);
-    };
-
-    if (tid == 0) {
-        for (int i = 0; i < NS && i < my_tiles; ++i) issue_load(i);
-        if (my_tiles > 0) issue_mma(0);
-    }
-    for (int i = 0; i < my_tiles; ++i) {
-        const int st = i % NS;
-        int unit, t0;
-        tile_coords(i, unit, t0);
-        if (tid == 0 && i + 1 < my_tiles && !s_abort) issue_mma(i + 1);
-        if (!mbar_wait(&bar_mma[st], (ph_mma >> st) & 1u, nullptr)) s_abort = 1;
-        ph_mma ^= 1u << st;
-        tc_fence_after();
-
-        // row statistics over this thread's half of the band columns
-        const int t = t0 + tt;
-        const int band_lo = t0 - P.Wr;
-        const int lo = max(max(t - W + 1, 0) - band_lo, 0), hi = t - band_lo;   // window columns [lo, hi]
-        const int self_c = t - band_lo;
-        const int c_beg = half * hcols;
-        float m = -INFINITY, oth = 0.f, slf = 0.f;
-        for (int c0 = 0; c0 < hcols; c0 += 16) {
-            float v[16];
-            tmem_ld16(tlane + st * P.tmem_stride + c_beg + c0, v);
+            for (int c0 = 0; c0 < HC; c0 += 16)
+                tmem_ld16(tlane + st * P.tmem_stride + c_beg + c0, *reinterpret_cast<float(*)[16]>(v + c0));
             tmem_ld_wait();
-            float bm = -INFINITY;
+            tc_fence_before();
+            mbar_arrive(&bar_tfree[st]);
+
+            // row statistics: window columns [lo, hi], the token itself at self_c
+            const int t = t0 + tt;
+            const int band_lo = t0 - P.Wr;
+            const int lo = max(max(t - W + 1, 0) - band_lo, 0), hi = t - band_lo;
+            const int self_c = t - band_lo;
+            float m = -INFINITY;
 #pragma unroll
-            for (int x = 0; x < 16; ++x) {
-                const int c = c_beg + c0 + x;
+            for (int x = 0; x < HC; ++x) {
+                const int c = c_beg + x;
                 v[x] = (c >= lo && c <= hi) ? v[x] * l2s : -INFINITY;
-                bm = fmaxf(bm, v[x]);
+                m = fmaxf(m, v[x]);
             }
-            if (bm > m) {
-                const float sc = exp2f(m - bm);
-                oth *= sc;
-                slf *= sc;
-                m = bm;
-            }
+            float oth = 0.f, slf = 0.f;
             if (m != -INFINITY) {
 #pragma unroll
-                for (int x = 0; x < 16; ++x) {
+                for (int x = 0; x < HC; ++x) {
                     const float e = exp2_mufu(v[x] - m);
-                    if (c_beg + c0 + x == self_c) slf += e;
+                    if (c_beg + x == self_c) slf += e;
                     else oth += e;
                 }
             }
-        }
-        xch[half][r][0] = m;
-        xch[half][r][1] = oth;
-        xch[half][r][2] = slf;
-        tc_fence_before();
-        __syncthreads();
-        if (s_abort) break;
-        if (half == 0) {
-            const float m1 = xch[1][r][0];
-            const float M = fmaxf(m, m1);
-            float o = 0.f, sl = 0.f;
-            if (M != -INFINITY) {
-                const float f0 = m == -INFINITY ? 0.f : exp2f(m - M), f1 = m1 == -INFINITY ? 0.f : exp2f(m1 - M);
-                o = oth * f0 + xch[1][r][1] * f1;
-                sl = slf * f0 + xch[1][r][2] * f1;
+            if (half == 1) {
+                xch[r][0] = m;
+                xch[r][1] = oth;
+                xch[r][2] = slf;
             }
-            hsc[hh][tt] = (hh < dm.G && t < dm.N) ? saliency_from_stats(o, sl) : 0.f;
+            if (named_sync_or(1, SC_ROWS, bad || *(volatile int *)&s_abort)) break;
+            if (half == 0) {
+                const float m1 = xch[r][0];
+                const float M = fmaxf(m, m1);
+                float o = 0.f, sl = 0.f;
+                if (M != -INFINITY) {
+                    const float f0 = m == -INFINITY ? 0.f : exp2f(m - M), f1 = m1 == -INFINITY ? 0.f : exp2f(m1 - M);
+                    o = oth * f0 + xch[r][1] * f1;
+                    sl = slf * f0 + xch[r][2] * f1;
+                }
+                hsc[hh][tt] = (hh < dm.G && t < dm.N) ? saliency_from_stats(o, sl) : 0.f;
+            }
+            named_sync_or(1, SC_ROWS, false);
+            if (tid < 32 && t0 + tid < dm.N) {
+                float a = 0.f;
+                for (int h = 0; h < dm.G; ++h) a += hsc[h][tid];
+                P.scores[(size_t)unit * dm.N + t0 + tid] = a / dm.G;
+            }
         }
-        __syncthreads();
-        if (tid < 32 && t0 + tid < dm.N) {
-            float a = 0.f;
-            for (int h = 0; h < dm.G; ++h) a += hsc[h][tid];
-            P.scores[(size_t)unit * dm.N + t0 + tid] = a / dm.G;
-        }
-        // stage st is free again: load tile i + NS into it
-        if (tid == 0 && i + NS < my_tiles && !s_abort) issue_load(i + NS);
     }
     tc_fence_before();
     __syncthreads();
@@ -218,15 +250,15 @@ cudaError_t launch_score_tc(const Dims &dm, const uint16_t *q, const uint16_t *k
     const int D = dm.d;
     uint64_t dq[3] = {(uint64_t)D, (uint64_t)dm.N, (uint64_t)dm.B * dm.Hq};
     uint64_t sq[2] = {(uint64_t)D * 2, (uint64_t)D * 2 * dm.N};
-    uint32_t box[3] = {64, 32, 1};
-    bool ok = make_tma_map(&m.q, q, 3, dq, sq, box, true);
-    uint64_t dk[3] = {(uint64_t)D, (uint64_t)dm.N, (uint64_t)dm.B * dm.Hkv};
-    ok = ok && make_tma_map(&m.k, k, 3, dk, sq, box, true);
-    if (!ok) return cudaErrorInvalidValue;
     ScoreTCParams p;
     p.dm = dm;
     p.Wr = (dm.W - 1 + 31) / 32 * 32;
     p.nb = (p.Wr + 32) / 32;
+    uint32_t boxq[3] = {64, 32, (uint32_t)dm.G}, boxk[3] = {64, (uint32_t)(32 * p.nb), 1};
+    bool ok = make_tma_map(&m.q, q, 3, dq, sq, boxq, true);
+    uint64_t dk[3] = {(uint64_t)D, (uint64_t)dm.N, (uint64_t)dm.B * dm.Hkv};
+    ok = ok && make_tma_map(&m.k, k, 3, dk, sq, boxk, true);
+    if (!ok) return cudaErrorInvalidValue;
     p.tiles_per_unit = (dm.N + 31) / 32;
     p.total_tiles = p.tiles_per_unit * dm.B * dm.Hkv;
     p.scores = scores;
@@ -242,16 +274,26 @@ cudaError_t launch_score_tc(const Dims &dm, const uint16_t *q, const uint16_t *k
     cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
     const int grid = p.total_tiles < nsm ? p.total_tiles : nsm;
     const size_t smem = (size_t)ns * p.stage_bytes + 1024;
-    cudaError_t e;
-    if (D == 64) {
-        e = cudaFuncSetAttribute(score_tc_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        score_tc_kernel<64><<<grid, 256, smem, s>>>(m, p);
-    } else {
-        e = cudaFuncSetAttribute(score_tc_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        score_tc_kernel<128><<<grid, 256, smem, s>>>(m, p);
+    cudaError_t e = cudaSuccess;
+#define STILL_SCORE(DD, NBB)                                                                                    \
+    e = cudaFuncSetAttribute(score_tc_kernel<DD, NBB>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);  \
+    if (e != cudaSuccess) return e;                                                                             \
+    score_tc_kernel<DD, NBB><<<grid, SC_THREADS, smem, s>>>(m, p);
+#define STILL_SCORE_NB(DD)                                                                                      \
+    switch (p.nb) {                                                                                             \
+    case 1: STILL_SCORE(DD, 1) break;                                                                           \
+    case 2: STILL_SCORE(DD, 2) break;                                                                           \
+    case 3: STILL_SCORE(DD, 3) break;                                                                           \
+    case 4: STILL_SCORE(DD, 4) break;                                                                           \
+    case 5: STILL_SCORE(DD, 5) break;                                                                           \
+    case 6: STILL_SCORE(DD, 6) break;                                                                           \
+    case 7: STILL_SCORE(DD, 7) break;                                                                           \
+    default: STILL_SCORE(DD, 8) break;                                                                          \
     }
+    if (D == 64) { STILL_SCORE_NB(64) }
+    else { STILL_SCORE_NB(128) }
+#undef STILL_SCORE_NB
+#undef STILL_SCORE
     return cudaGetLastError();
 }
 
