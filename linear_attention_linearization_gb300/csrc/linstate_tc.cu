@@ -12,7 +12,9 @@
 //             also gets its unmasked phi in the kept table (the selection
 //             kernel copies its K and V rows there)
 //   dS  += phi_blk^T V_blk                   (tcgen05, accumulated in TMEM)
-//   dz  += column sums of phi_blk            (CUDA cores)
+//   dz  += phi_blk^T 1                       (tcgen05: an all-ones B operand)
+// U of the next block is issued with dS of this one, into the other half of
+// a double-buffered TMEM U, so that the rows go straight on to it.
 // The range is [b_s - W, b_{s+1} - W) clipped to [0, N), b_s the first token
 // of segment s: the keys that leave the window while segment s runs (the last
 // segment also writes the features of the final W keys).  Only keys below N - W enter dS: the others never
@@ -46,7 +48,8 @@ struct LinLayout {
     static constexpr uint32_t STAGE = WF + CBD * DF * 128;     // 2 x (K [128 x D] + V [128 x D])
     static constexpr uint32_t STAGE_BYTES = 2 * CBD * 16384;
     static constexpr uint32_t PHI = STAGE + 2 * STAGE_BYTES;   // [128 rows x DF], always 2 blocks
-    static constexpr uint32_t TOTAL = PHI + 2 * 16384;
+    static constexpr uint32_t ONES = PHI + 2 * 16384;          // [16 rows x 128 keys]: row 0 ones, K-major
+    static constexpr uint32_t TOTAL = ONES + 2 * 2048;
 };
 
 template <int D, int DF>
@@ -55,11 +58,11 @@ __global__ void __launch_bounds__(128, 1) linstate_tc_kernel(const __grid_consta
     using Lay = LinLayout<D, DF>;
     constexpr int CBD = Lay::CBD, CBF = Lay::CBF;
     constexpr float LOG2E = 1.4426950408889634f;
-    constexpr int TM_U = 0, TM_DS = 128;
+    constexpr int TM_U = 0, TM_DS = 256, TM_DZ = 384;   // U double-buffered at 0 and 128
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     const uint32_t sb = smem_u32(sm);
-    __shared__ uint64_t bar_wf, bar_full[2], bar_u, bar_ds;
+    __shared__ uint64_t bar_wf, bar_full[2], bar_u[2], bar_ds;
     __shared__ uint32_t tmem_base;
     __shared__ int s_abort;
 
@@ -73,14 +76,15 @@ __global__ void __launch_bounds__(128, 1) linstate_tc_kernel(const __grid_consta
     const int nblk = khi > klo ? (khi - klo + 127) / 128 : 0;
 
     if (warp == 0) {
-        tmem_alloc(&tmem_base, 256);
+        tmem_alloc(&tmem_base, 512);
         tmem_relinquish();
     }
     if (tid == 0) {
         mbar_init(&bar_wf, 1);
         mbar_init(&bar_full[0], 1);
         mbar_init(&bar_full[1], 1);
-        mbar_init(&bar_u, 1);
+        mbar_init(&bar_u[0], 1);
+        mbar_init(&bar_u[1], 1);
         mbar_init(&bar_ds, 1);
         fence_barrier_init();
         s_abort = 0;
@@ -88,6 +92,12 @@ __global__ void __launch_bounds__(128, 1) linstate_tc_kernel(const __grid_consta
     // the second feature block stays zero when d_f = 64 (it is read as padding rows of dS)
     if (CBF == 1)
         for (int i = tid; i < 16384 / 16; i += 128) reinterpret_cast<uint4 *>(sm + Lay::PHI + 16384)[i] = make_uint4(0, 0, 0, 0);
+    // the all-ones operand: row 0 of each 64-key block is ones, rows 1..15 zero
+    for (int i = tid; i < 2 * 2048 / 16; i += 128) {
+        const int row = (i * 16 % 2048) / 128;
+        const uint32_t one2 = 0x3f803f80u;   // two bf16 ones
+        reinterpret_cast<uint4 *>(sm + Lay::ONES)[i] = row == 0 ? make_uint4(one2, one2, one2, one2) : make_uint4(0, 0, 0, 0);
+    }
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
@@ -112,33 +122,37 @@ __global__ void __launch_bounds__(128, 1) linstate_tc_kernel(const __grid_consta
         if (nblk > 0) load_blk(0);
         if (nblk > 1) load_blk(1);
     }
-    uint32_t ph_full[2] = {0, 0}, ph_u = 0, ph_ds = 0;
+    uint32_t ph_full[2] = {0, 0}, ph_u[2] = {0, 0}, ph_ds = 0;   // ph_full: the issuing thread's waits
+    uint32_t ph_kf[2] = {0, 0};                                   // every thread's waits on the K copies
     const uint32_t id_u = idesc_bf16(128, DF, 0, 0);
     const uint32_t id_ds = idesc_bf16(128, D, 1, 1);
-    float zacc = 0.f;
+    const uint32_t id_dz = idesc_bf16(128, 16, 1, 0);
     const int r = tid;
+    // U of block blk = K_blk Wf into TMEM half blk & 1 (thread 0)
+    auto issue_u = [&](int blk) {
+        const int st = blk & 1;
+        if (!mbar_wait(&bar_full[st], ph_full[st], P.status)) s_abort = 1;
+        ph_full[st] ^= 1;
+        tc_fence_after();
+        const uint32_t ka = sb + Lay::STAGE + st * Lay::STAGE_BYTES;
+        for (int k = 0; k < D; k += 16)
+            mma_ss(tmem + TM_U + 128 * st, sdesc(ka + (k / 64) * 16384 + (k % 64) * 2, 16, 1024),
+                   sdesc(sb + Lay::WF + (k / 64) * (DF * 128) + (k % 64) * 2, 16, 1024), id_u, k > 0);
+        mma_commit(&bar_u[st]);
+    };
+    if (tid == 0 && nblk > 0) {
+        uint32_t ph0 = 0;
+        if (!mbar_wait(&bar_wf, ph0, P.status)) s_abort = 1;
+        issue_u(0);
+    }
 
     for (int blk = 0; blk < nblk; ++blk) {
         const int st = blk & 1;
         const int j = klo + 128 * blk + r;
         uint8_t *kd = sm + Lay::STAGE + st * Lay::STAGE_BYTES;
-        if (tid == 0) {
-            if (blk == 0) {
-                uint32_t ph0 = 0;
-                if (!mbar_wait(&bar_wf, ph0, P.status)) s_abort = 1;
-            }
-            if (!mbar_wait(&bar_full[st], ph_full[st], P.status)) s_abort = 1;
-            ph_full[st] ^= 1;
-            tc_fence_after();
-            const uint32_t ka = sb + Lay::STAGE + st * Lay::STAGE_BYTES;
-            for (int k = 0; k < D; k += 16)
-                mma_ss(tmem + TM_U, sdesc(ka + (k / 64) * 16384 + (k % 64) * 2, 16, 1024),
-                       sdesc(sb + Lay::WF + (k / 64) * (DF * 128) + (k % 64) * 2, 16, 1024), id_u, k > 0);
-            mma_commit(&bar_u);
-        }
-        __syncthreads();
-        if (s_abort) break;
-        // ||k|| of this row
+        // ||k|| of this row, once the block's K has arrived
+        if (!mbar_wait(&bar_full[st], ph_kf[st], P.status)) s_abort = 1;
+        ph_kf[st] ^= 1;
         float kn2 = 0.f;
 #pragma unroll
         for (int cb = 0; cb < CBD; ++cb)
@@ -152,35 +166,30 @@ __global__ void __launch_bounds__(128, 1) linstate_tc_kernel(const __grid_consta
                     kn2 = fmaf(a0, a0, fmaf(a1, a1, kn2));
                 }
             }
-        if (!mbar_wait(&bar_u, ph_u, P.status)) s_abort = 1;
-        ph_u ^= 1;
+        if (!mbar_wait(&bar_u[st], ph_u[st], P.status)) s_abort = 1;
+        ph_u[st] ^= 1;
         tc_fence_after();
-        // the previous block's dS MMA still reads the feature buffer
+        // phi of this row: the DF exponentials stay in registers
+        float u[DF];
+#pragma unroll
+        for (int c0 = 0; c0 < DF; c0 += 32) tmem_ld32(tlane + TM_U + 128 * st + c0, *reinterpret_cast<float(*)[32]>(u + c0));
+        tmem_ld_wait();
+        float mu = -INFINITY, s2 = 0.f;
+#pragma unroll
+        for (int i = 0; i < DF; ++i) mu = fmaxf(mu, u[i] * LOG2E);
+#pragma unroll
+        for (int i = 0; i < DF; ++i) {
+            u[i] = exp2_mufu(fmaf(u[i], LOG2E, -mu));
+            s2 = fmaf(u[i], u[i], s2);
+        }
+        const float sc = sqrtf(kn2) * rsqrtf(s2);
+        // the previous block's dS / dz MMAs still read the feature buffer; once they are
+        // done, that block's stage is free for block blk + 1
         if (blk > 0) {
             if (!mbar_wait(&bar_ds, ph_ds, P.status)) s_abort = 1;
             ph_ds ^= 1;
-            if (tid == 0 && blk + 1 < nblk) load_blk(blk + 1);   // stage of block blk-1 is free again
+            if (tid == 0 && blk + 1 < nblk) load_blk(blk + 1);
         }
-        float mu = -INFINITY, s2 = 0.f;
-#pragma unroll
-        for (int c0 = 0; c0 < DF; c0 += 32) {
-            float u[32];
-            tmem_ld32(tlane + TM_U + c0, u);
-            tmem_ld_wait();
-            float bm = -INFINITY;
-#pragma unroll
-            for (int i = 0; i < 32; ++i) bm = fmaxf(bm, u[i] * LOG2E);
-            if (bm > mu) {
-                s2 *= exp2f(2.f * (mu - bm));
-                mu = bm;
-            }
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                const float e = exp2_mufu(fmaf(u[i], LOG2E, -mu));
-                s2 = fmaf(e, e, s2);
-            }
-        }
-        const float sc = sqrtf(kn2) * rsqrtf(s2);
         const bool in_range = j < khi;
         const int kslot = in_range ? P.kslot[unit * dm.N + j] : -1;
         const bool slotted = kslot >= 0;
@@ -189,45 +198,32 @@ __global__ void __launch_bounds__(128, 1) linstate_tc_kernel(const __grid_consta
         const bool folded = j < fhi && !slotted;
         uint16_t *grow = P.phik + (unit * dm.N + (in_range ? j : 0)) * DF;
 #pragma unroll
-        for (int c0 = 0; c0 < DF; c0 += 32) {
-            float u[32];
-            tmem_ld32(tlane + TM_U + c0, u);
-            tmem_ld_wait();
+        for (int f0 = 0; f0 < DF; f0 += 8) {
+            uint32_t w4[4];
 #pragma unroll
-            for (int c8 = 0; c8 < 4; ++c8) {
-                uint32_t w4[4];
-#pragma unroll
-                for (int h2 = 0; h2 < 4; ++h2) {
-                    const int i = c8 * 8 + h2 * 2;
-                    w4[h2] = pack_bf16(sc * exp2_mufu(fmaf(u[i], LOG2E, -mu)), sc * exp2_mufu(fmaf(u[i + 1], LOG2E, -mu)));
-                }
-                const int f0 = c0 + c8 * 8;
-                const uint4 val = make_uint4(w4[0], w4[1], w4[2], w4[3]);
-                const uint4 zero = make_uint4(0, 0, 0, 0);
-                if (in_range) *reinterpret_cast<uint4 *>(grow + f0) = slotted ? zero : val;
-                if (slotted) *reinterpret_cast<uint4 *>(krow + f0) = val;   // kept: unmasked features
-                *reinterpret_cast<uint4 *>(sm + Lay::PHI + (f0 / 64) * 16384 + sw128(r, (f0 % 64) / 8)) =
-                    folded ? val : zero;
-            }
+            for (int h2 = 0; h2 < 4; ++h2) w4[h2] = pack_bf16(sc * u[f0 + 2 * h2], sc * u[f0 + 2 * h2 + 1]);
+            const uint4 val = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+            const uint4 zero = make_uint4(0, 0, 0, 0);
+            if (in_range) *reinterpret_cast<uint4 *>(grow + f0) = slotted ? zero : val;
+            if (slotted) *reinterpret_cast<uint4 *>(krow + f0) = val;   // kept: unmasked features
+            *reinterpret_cast<uint4 *>(sm + Lay::PHI + (f0 / 64) * 16384 + sw128(r, (f0 % 64) / 8)) = folded ? val : zero;
         }
         fence_async_smem();
         tc_fence_before();
         __syncthreads();
-        // dz: column f of the (masked) feature block
-        if (r < DF) {
-            const int cb = r / 64, c8 = (r % 64) / 8, e = r % 8;
-            for (int row = 0; row < 128; ++row)
-                zacc += bf2f(*reinterpret_cast<const uint16_t *>(sm + Lay::PHI + cb * 16384 + sw128(row, c8) + e * 2));
-        }
+        if (s_abort) break;
         if (tid == 0) {
             tc_fence_after();
             const uint32_t va = sb + Lay::STAGE + st * Lay::STAGE_BYTES + CBD * 16384;
-            for (int kk = 0; kk < 128; kk += 16)
-                mma_ss(tmem + TM_DS, sdesc(sb + Lay::PHI + kk * 128, 16384, 1024), sdesc(va + kk * 128, 16384, 1024),
-                       id_ds, (blk > 0 || kk > 0) ? 1u : 0u);
+            for (int kk = 0; kk < 128; kk += 16) {
+                const uint64_t a = sdesc(sb + Lay::PHI + kk * 128, 16384, 1024);
+                const uint32_t acc = (blk > 0 || kk > 0) ? 1u : 0u;
+                mma_ss(tmem + TM_DS, a, sdesc(va + kk * 128, 16384, 1024), id_ds, acc);
+                mma_ss(tmem + TM_DZ, a, sdesc(sb + Lay::ONES + (kk / 64) * 2048 + (kk % 64) * 2, 16, 1024), id_dz, acc);
+            }
             mma_commit(&bar_ds);
+            if (blk + 1 < nblk) issue_u(blk + 1);
         }
-        __syncthreads();   // zacc reads of the feature block end before it is rewritten
     }
     // write dS / dz of this segment
     if (nblk > 0 && !s_abort) {
@@ -242,10 +238,14 @@ __global__ void __launch_bounds__(128, 1) linstate_tc_kernel(const __grid_consta
         if (r < DF)
             for (int i = 0; i < 32; ++i) out[(size_t)r * D + c0 + i] = nblk > 0 ? v[i] : 0.f;
     }
-    if (r < DF) P.dz[(unit * (P.sp.nseg + 1) + s) * DF + r] = zacc;
+    {
+        const float zacc = tmem_ld1(tlane + TM_DZ);
+        tmem_ld_wait();
+        if (r < DF) P.dz[(unit * (P.sp.nseg + 1) + s) * DF + r] = nblk > 0 ? zacc : 0.f;
+    }
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tmem, 256);
+    if (warp == 0) tmem_dealloc(tmem, 512);
 }
 
 cudaError_t launch_linstate_tc(const Dims &dm, const SegPlan &sp, const uint16_t *k, const uint16_t *v,
