@@ -13,8 +13,9 @@
 //             kernel copies its K and V rows there)
 //   dS  += phi_blk^T V_blk                   (tcgen05, accumulated in TMEM)
 //   dz  += phi_blk^T 1                       (tcgen05: an all-ones B operand)
-// U of the next block is issued with dS of this one, into the other half of
-// a double-buffered TMEM U, so that the rows go straight on to it.
+// A fifth warp issues the TMA copies and the MMAs: U runs two blocks ahead of
+// the rows in a double-buffered TMEM U, dS and dz as soon as a block's
+// features are in shared memory.
 // The range is [b_s - W, b_{s+1} - W) clipped to [0, N), b_s the first token
 // of segment s: the keys that leave the window while segment s runs (the last
 // segment also writes the features of the final W keys).  Only keys below N - W enter dS: the others never
@@ -53,7 +54,7 @@ struct LinLayout {
 };
 
 template <int D, int DF>
-__global__ void __launch_bounds__(128, 1) linstate_tc_kernel(const __grid_constant__ LinTCMaps maps, LinTCParams P)
+__global__ void __launch_bounds__(160, 1) linstate_tc_kernel(const __grid_constant__ LinTCMaps maps, LinTCParams P)
 {
     using Lay = LinLayout<D, DF>;
     constexpr int CBD = Lay::CBD, CBF = Lay::CBF;
@@ -62,7 +63,7 @@ __global__ void __launch_bounds__(128, 1) linstate_tc_kernel(const __grid_consta
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     const uint32_t sb = smem_u32(sm);
-    __shared__ uint64_t bar_wf, bar_full[2], bar_u[2], bar_ds;
+    __shared__ uint64_t bar_wf, bar_full[2], bar_u[2], bar_ds, rdy_phi;
     __shared__ uint32_t tmem_base;
     __shared__ int s_abort;
 
@@ -86,14 +87,15 @@ __global__ void __launch_bounds__(128, 1) linstate_tc_kernel(const __grid_consta
         mbar_init(&bar_u[0], 1);
         mbar_init(&bar_u[1], 1);
         mbar_init(&bar_ds, 1);
+        mbar_init(&rdy_phi, 128);
         fence_barrier_init();
         s_abort = 0;
     }
     // the second feature block stays zero when d_f = 64 (it is read as padding rows of dS)
     if (CBF == 1)
-        for (int i = tid; i < 16384 / 16; i += 128) reinterpret_cast<uint4 *>(sm + Lay::PHI + 16384)[i] = make_uint4(0, 0, 0, 0);
+        for (int i = tid; i < 16384 / 16; i += 160) reinterpret_cast<uint4 *>(sm + Lay::PHI + 16384)[i] = make_uint4(0, 0, 0, 0);
     // the all-ones operand: row 0 of each 64-key block is ones, rows 1..15 zero
-    for (int i = tid; i < 2 * 2048 / 16; i += 128) {
+    for (int i = tid; i < 2 * 2048 / 16; i += 160) {
         const int row = (i * 16 % 2048) / 128;
         const uint32_t one2 = 0x3f803f80u;   // two bf16 ones
         reinterpret_cast<uint4 *>(sm + Lay::ONES)[i] = row == 0 ? make_uint4(one2, one2, one2, one2) : make_uint4(0, 0, 0, 0);
@@ -116,129 +118,160 @@ __global__ void __launch_bounds__(128, 1) linstate_tc_kernel(const __grid_consta
             tma_load_3d(vd + cb * 16384, &maps.v, &bar_full[st], cb * 64, j0, (int)unit);
         }
     };
-    if (tid == 0) {
-        mbar_expect_tx(&bar_wf, CBD * DF * 128);
-        for (int cb = 0; cb < CBD; ++cb) tma_load_2d(sm + Lay::WF + cb * DF * 128, &maps.wft, &bar_wf, cb * 64, 0);
-        if (nblk > 0) load_blk(0);
-        if (nblk > 1) load_blk(1);
-    }
-    uint32_t ph_full[2] = {0, 0}, ph_u[2] = {0, 0}, ph_ds = 0;   // ph_full: the issuing thread's waits
-    uint32_t ph_kf[2] = {0, 0};                                   // every thread's waits on the K copies
     const uint32_t id_u = idesc_bf16(128, DF, 0, 0);
     const uint32_t id_ds = idesc_bf16(128, D, 1, 1);
     const uint32_t id_dz = idesc_bf16(128, 16, 1, 0);
-    const int r = tid;
-    // U of block blk = K_blk Wf into TMEM half blk & 1 (thread 0)
-    auto issue_u = [&](int blk) {
-        const int st = blk & 1;
-        if (!mbar_wait(&bar_full[st], ph_full[st], P.status)) s_abort = 1;
-        ph_full[st] ^= 1;
-        tc_fence_after();
-        const uint32_t ka = sb + Lay::STAGE + st * Lay::STAGE_BYTES;
-        for (int k = 0; k < D; k += 16)
-            mma_ss(tmem + TM_U + 128 * st, sdesc(ka + (k / 64) * 16384 + (k % 64) * 2, 16, 1024),
-                   sdesc(sb + Lay::WF + (k / 64) * (DF * 128) + (k % 64) * 2, 16, 1024), id_u, k > 0);
-        mma_commit(&bar_u[st]);
-    };
-    if (tid == 0 && nblk > 0) {
-        uint32_t ph0 = 0;
-        if (!mbar_wait(&bar_wf, ph0, P.status)) s_abort = 1;
-        issue_u(0);
-    }
+    uint32_t ph_ds = 0;
 
-    for (int blk = 0; blk < nblk; ++blk) {
-        const int st = blk & 1;
-        const int j = klo + 128 * blk + r;
-        uint8_t *kd = sm + Lay::STAGE + st * Lay::STAGE_BYTES;
-        // ||k|| of this row, once the block's K has arrived
-        if (!mbar_wait(&bar_full[st], ph_kf[st], P.status)) s_abort = 1;
-        ph_kf[st] ^= 1;
-        float kn2 = 0.f;
+    if (warp == 4) {
+        // ============================ the issuing warp ============================
+        if (tid == 128) {
+            uint32_t ph_full[2] = {0, 0}, pe_phi = 0;
+            // U of block blk = K_blk Wf into TMEM half blk & 1
+            auto issue_u = [&](int blk) {
+                const int st = blk & 1;
+                if (!mbar_wait(&bar_full[st], ph_full[st], P.status)) s_abort = 1;
+                ph_full[st] ^= 1;
+                tc_fence_after();
+                const uint32_t ka = sb + Lay::STAGE + st * Lay::STAGE_BYTES;
+                for (int k = 0; k < D; k += 16)
+                    mma_ss(tmem + TM_U + 128 * st, sdesc(ka + (k / 64) * 16384 + (k % 64) * 2, 16, 1024),
+                           sdesc(sb + Lay::WF + (k / 64) * (DF * 128) + (k % 64) * 2, 16, 1024), id_u, k > 0);
+                mma_commit(&bar_u[st]);
+            };
+            mbar_expect_tx(&bar_wf, CBD * DF * 128);
+            for (int cb = 0; cb < CBD; ++cb) tma_load_2d(sm + Lay::WF + cb * DF * 128, &maps.wft, &bar_wf, cb * 64, 0);
+            if (nblk > 0) load_blk(0);
+            if (nblk > 1) load_blk(1);
+            if (nblk > 0) {
+                uint32_t ph0 = 0;
+                if (!mbar_wait(&bar_wf, ph0, P.status)) s_abort = 1;
+                issue_u(0);
+            }
+            if (nblk > 1) issue_u(1);
+            for (int blk = 0; blk < nblk && !*(volatile int *)&s_abort; ++blk) {
+                const int st = blk & 1;
+                // the block's features are in shared memory (and the rows are done with its U and K)
+                if (!mbar_wait(&rdy_phi, pe_phi, P.status)) s_abort = 1;
+                pe_phi ^= 1;
+                tc_fence_after();
+                const uint32_t va = sb + Lay::STAGE + st * Lay::STAGE_BYTES + CBD * 16384;
+                for (int kk = 0; kk < 128; kk += 16) {
+                    const uint64_t a = sdesc(sb + Lay::PHI + kk * 128, 16384, 1024);
+                    const uint32_t acc = (blk > 0 || kk > 0) ? 1u : 0u;
+                    mma_ss(tmem + TM_DS, a, sdesc(va + kk * 128, 16384, 1024), id_ds, acc);
+                    mma_ss(tmem + TM_DZ, a, sdesc(sb + Lay::ONES + (kk / 64) * 2048 + (kk % 64) * 2, 16, 1024), id_dz, acc);
+                }
+                mma_commit(&bar_ds);
+                if (blk + 2 < nblk) {
+                    // this stage is free once dS has read its V: block blk + 2 comes in, its U follows
+                    if (!mbar_wait(&bar_ds, ph_ds, P.status)) s_abort = 1;
+                    load_blk(blk + 2);
+                    issue_u(blk + 2);
+                }
+                ph_ds ^= 1;
+            }
+        }
+        __syncwarp();
+    } else {
+        // ============================== the row warps ==============================
+        uint32_t ph_u[2] = {0, 0}, ph_kf[2] = {0, 0};
+        const int r = tid;
+        for (int blk = 0; blk < nblk; ++blk) {
+            const int st = blk & 1;
+            const int j = klo + 128 * blk + r;
+            uint8_t *kd = sm + Lay::STAGE + st * Lay::STAGE_BYTES;
+            const bool in_range = j < khi;
+            const int kslot = in_range ? __ldg(P.kslot + unit * dm.N + j) : -1;   // in flight behind the waits
+            // ||k|| of this row, once the block's K has arrived
+            bool bad = !mbar_wait(&bar_full[st], ph_kf[st], P.status);
+            ph_kf[st] ^= 1;
+            float kn2 = 0.f;
 #pragma unroll
-        for (int cb = 0; cb < CBD; ++cb)
+            for (int cb = 0; cb < CBD; ++cb)
 #pragma unroll
-            for (int c8 = 0; c8 < 8; ++c8) {
-                const uint4 pk = *reinterpret_cast<const uint4 *>(kd + cb * 16384 + sw128(r, c8));
-                const uint32_t w4[4] = {pk.x, pk.y, pk.z, pk.w};
+                for (int c8 = 0; c8 < 8; ++c8) {
+                    const uint4 pk = *reinterpret_cast<const uint4 *>(kd + cb * 16384 + sw128(r, c8));
+                    const uint32_t w4[4] = {pk.x, pk.y, pk.z, pk.w};
 #pragma unroll
-                for (int h2 = 0; h2 < 4; ++h2) {
-                    const float a0 = __uint_as_float(w4[h2] << 16), a1 = __uint_as_float(w4[h2] & 0xffff0000u);
-                    kn2 = fmaf(a0, a0, fmaf(a1, a1, kn2));
+                    for (int h2 = 0; h2 < 4; ++h2) {
+                        const float a0 = __uint_as_float(w4[h2] << 16), a1 = __uint_as_float(w4[h2] & 0xffff0000u);
+                        kn2 = fmaf(a0, a0, fmaf(a1, a1, kn2));
+                    }
+                }
+            bad |= !mbar_wait(&bar_u[st], ph_u[st], P.status);
+            ph_u[st] ^= 1;
+            tc_fence_after();
+            // phi of this row: the DF exponentials stay in registers
+            float u[DF];
+#pragma unroll
+            for (int c0 = 0; c0 < DF; c0 += 32) tmem_ld32(tlane + TM_U + 128 * st + c0, *reinterpret_cast<float(*)[32]>(u + c0));
+            tmem_ld_wait();
+            float mu = -INFINITY, s2 = 0.f;
+#pragma unroll
+            for (int i = 0; i < DF; ++i) mu = fmaxf(mu, u[i] * LOG2E);
+#pragma unroll
+            for (int i = 0; i < DF; ++i) {
+                u[i] = exp2_mufu(fmaf(u[i], LOG2E, -mu));
+                s2 = fmaf(u[i], u[i], s2);
+            }
+            const float sc = sqrtf(kn2) * rsqrtf(s2);
+            // the previous block's dS / dz MMAs are done with the feature buffer
+            if (blk > 0) {
+                bad |= !mbar_wait(&bar_ds, ph_ds, P.status);
+                ph_ds ^= 1;
+            }
+            const bool slotted = kslot >= 0;
+            const int KP = dm.T_max * dm.lam;
+            uint16_t *krow = slotted ? P.phk + (unit * KP + kslot) * DF : nullptr;
+            const bool folded = j < fhi && !slotted;
+            // keys that stay in the window to the end (the last segment's tail) go to the
+            // table from here; every other row of the table is copied from the block below
+            const bool tail = in_range && j >= fhi;
+            uint16_t *grow = P.phik + (unit * dm.N + (in_range ? j : 0)) * DF;
+#pragma unroll
+            for (int f0 = 0; f0 < DF; f0 += 8) {
+                uint32_t w4[4];
+#pragma unroll
+                for (int h2 = 0; h2 < 4; ++h2) w4[h2] = pack_bf16(sc * u[f0 + 2 * h2], sc * u[f0 + 2 * h2 + 1]);
+                const uint4 val = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+                const uint4 zero = make_uint4(0, 0, 0, 0);
+                if (tail) *reinterpret_cast<uint4 *>(grow + f0) = slotted ? zero : val;
+                if (slotted) *reinterpret_cast<uint4 *>(krow + f0) = val;   // kept: unmasked features
+                *reinterpret_cast<uint4 *>(sm + Lay::PHI + (f0 / 64) * 16384 + sw128(r, (f0 % 64) / 8)) = folded ? val : zero;
+            }
+            fence_async_smem();
+            tc_fence_before();
+            mbar_arrive(&rdy_phi);
+            if (named_sync_or(1, 128, bad || *(volatile int *)&s_abort)) break;
+            {
+                // rows below fhi: the block holds exactly the table's values (phi, or zero for
+                // slotted keys); each warp stores two 256-byte rows per instruction
+                const int j0 = klo + 128 * blk;
+                const int nrow = max(0, min(128, min(khi, fhi) - j0));
+                constexpr int CH = DF / 8;   // 16-byte chunks per row
+                uint16_t *gbase = P.phik + (unit * dm.N + j0) * DF;
+                for (int e = tid; e < nrow * CH; e += 128) {
+                    const int row = e / CH, ch = e % CH;
+                    const uint4 x = *reinterpret_cast<const uint4 *>(sm + Lay::PHI + (ch / 8) * 16384 + sw128(row, ch % 8));
+                    *reinterpret_cast<uint4 *>(gbase + (size_t)row * DF + ch * 8) = x;
                 }
             }
-        if (!mbar_wait(&bar_u[st], ph_u[st], P.status)) s_abort = 1;
-        ph_u[st] ^= 1;
-        tc_fence_after();
-        // phi of this row: the DF exponentials stay in registers
-        float u[DF];
-#pragma unroll
-        for (int c0 = 0; c0 < DF; c0 += 32) tmem_ld32(tlane + TM_U + 128 * st + c0, *reinterpret_cast<float(*)[32]>(u + c0));
-        tmem_ld_wait();
-        float mu = -INFINITY, s2 = 0.f;
-#pragma unroll
-        for (int i = 0; i < DF; ++i) mu = fmaxf(mu, u[i] * LOG2E);
-#pragma unroll
-        for (int i = 0; i < DF; ++i) {
-            u[i] = exp2_mufu(fmaf(u[i], LOG2E, -mu));
-            s2 = fmaf(u[i], u[i], s2);
+            named_sync_or(1, 128, false);   // the copy's reads end before the buffer is rewritten
         }
-        const float sc = sqrtf(kn2) * rsqrtf(s2);
-        // the previous block's dS / dz MMAs still read the feature buffer; once they are
-        // done, that block's stage is free for block blk + 1
-        if (blk > 0) {
+        // dS / dz of this segment
+        if (nblk > 0 && !*(volatile int *)&s_abort) {
             if (!mbar_wait(&bar_ds, ph_ds, P.status)) s_abort = 1;
-            ph_ds ^= 1;
-            if (tid == 0 && blk + 1 < nblk) load_blk(blk + 1);
-        }
-        const bool in_range = j < khi;
-        const int kslot = in_range ? P.kslot[unit * dm.N + j] : -1;
-        const bool slotted = kslot >= 0;
-        const int KP = dm.T_max * dm.lam;
-        uint16_t *krow = slotted ? P.phk + (unit * KP + kslot) * DF : nullptr;
-        const bool folded = j < fhi && !slotted;
-        uint16_t *grow = P.phik + (unit * dm.N + (in_range ? j : 0)) * DF;
-#pragma unroll
-        for (int f0 = 0; f0 < DF; f0 += 8) {
-            uint32_t w4[4];
-#pragma unroll
-            for (int h2 = 0; h2 < 4; ++h2) w4[h2] = pack_bf16(sc * u[f0 + 2 * h2], sc * u[f0 + 2 * h2 + 1]);
-            const uint4 val = make_uint4(w4[0], w4[1], w4[2], w4[3]);
-            const uint4 zero = make_uint4(0, 0, 0, 0);
-            if (in_range) *reinterpret_cast<uint4 *>(grow + f0) = slotted ? zero : val;
-            if (slotted) *reinterpret_cast<uint4 *>(krow + f0) = val;   // kept: unmasked features
-            *reinterpret_cast<uint4 *>(sm + Lay::PHI + (f0 / 64) * 16384 + sw128(r, (f0 % 64) / 8)) = folded ? val : zero;
-        }
-        fence_async_smem();
-        tc_fence_before();
-        __syncthreads();
-        if (s_abort) break;
-        if (tid == 0) {
             tc_fence_after();
-            const uint32_t va = sb + Lay::STAGE + st * Lay::STAGE_BYTES + CBD * 16384;
-            for (int kk = 0; kk < 128; kk += 16) {
-                const uint64_t a = sdesc(sb + Lay::PHI + kk * 128, 16384, 1024);
-                const uint32_t acc = (blk > 0 || kk > 0) ? 1u : 0u;
-                mma_ss(tmem + TM_DS, a, sdesc(va + kk * 128, 16384, 1024), id_ds, acc);
-                mma_ss(tmem + TM_DZ, a, sdesc(sb + Lay::ONES + (kk / 64) * 2048 + (kk % 64) * 2, 16, 1024), id_dz, acc);
-            }
-            mma_commit(&bar_ds);
-            if (blk + 1 < nblk) issue_u(blk + 1);
         }
-    }
-    // write dS / dz of this segment
-    if (nblk > 0 && !s_abort) {
-        if (!mbar_wait(&bar_ds, ph_ds, P.status)) s_abort = 1;
-        tc_fence_after();
-    }
-    float *out = P.dS + (unit * (P.sp.nseg + 1) + s) * (size_t)(DF * D);
-    for (int c0 = 0; c0 < D; c0 += 32) {
-        float v[32];
-        tmem_ld32(tlane + TM_DS + c0, v);
-        tmem_ld_wait();
-        if (r < DF)
-            for (int i = 0; i < 32; ++i) out[(size_t)r * D + c0 + i] = nblk > 0 ? v[i] : 0.f;
-    }
-    {
+        float *out = P.dS + (unit * (P.sp.nseg + 1) + s) * (size_t)(DF * D);
+        for (int c0 = 0; c0 < D; c0 += 32) {
+            float v[32];
+            tmem_ld32(tlane + TM_DS + c0, v);
+            tmem_ld_wait();
+            if (r < DF)
+                for (int i = 0; i < 32; ++i) out[(size_t)r * D + c0 + i] = nblk > 0 ? v[i] : 0.f;
+        }
         const float zacc = tmem_ld1(tlane + TM_DZ);
         tmem_ld_wait();
         if (r < DF) P.dz[(unit * (P.sp.nseg + 1) + s) * DF + r] = nblk > 0 ? zacc : 0.f;
@@ -272,7 +305,7 @@ cudaError_t launch_linstate_tc(const Dims &dm, const SegPlan &sp, const uint16_t
         e = cudaFuncSetAttribute(linstate_tc_kernel<DD, FF>, cudaFuncAttributeMaxDynamicSharedMemorySize,     \
                                  (int)smem);                                                                  \
         if (e != cudaSuccess) return e;                                                                       \
-        linstate_tc_kernel<DD, FF><<<grid, 128, smem, s>>>(m, p);                                            \
+        linstate_tc_kernel<DD, FF><<<grid, 160, smem, s>>>(m, p);                                            \
     }
     if (D == 64 && DF == 64) STILL_LIN(64, 64)
     else if (D == 64) STILL_LIN(64, 128)
