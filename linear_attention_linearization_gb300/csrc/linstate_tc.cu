@@ -13,9 +13,10 @@
 //             kernel copies its K and V rows there)
 //   dS  += phi_blk^T V_blk                   (tcgen05, accumulated in TMEM)
 //   dz  += phi_blk^T 1                       (tcgen05: an all-ones B operand)
-// A fifth warp issues the TMA copies and the MMAs: U runs two blocks ahead of
-// the rows in a double-buffered TMEM U, dS and dz as soon as a block's
-// features are in shared memory.
+// Two row threads share a key (each takes half of its features and of its
+// dimensions); a ninth warp issues the TMA copies and the MMAs: U runs two
+// blocks ahead of the rows in a double-buffered TMEM U, dS and dz as soon as
+// a block's features are in shared memory.
 // The range is [b_s - W, b_{s+1} - W) clipped to [0, N), b_s the first token
 // of segment s: the keys that leave the window while segment s runs (the last
 // segment also writes the features of the final W keys).  Only keys below N - W enter dS: the others never
@@ -54,7 +55,7 @@ struct LinLayout {
 };
 
 template <int D, int DF>
-__global__ void __launch_bounds__(160, 1) linstate_tc_kernel(const __grid_constant__ LinTCMaps maps, LinTCParams P)
+__global__ void __launch_bounds__(288, 1) linstate_tc_kernel(const __grid_constant__ LinTCMaps maps, LinTCParams P)
 {
     using Lay = LinLayout<D, DF>;
     constexpr int CBD = Lay::CBD, CBF = Lay::CBF;
@@ -64,6 +65,7 @@ __global__ void __launch_bounds__(160, 1) linstate_tc_kernel(const __grid_consta
     uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     const uint32_t sb = smem_u32(sm);
     __shared__ uint64_t bar_wf, bar_full[2], bar_u[2], bar_ds, rdy_phi;
+    __shared__ float xch[2][128][3];   // per key row and half: max, sum of squares, ||k||^2 part
     __shared__ uint32_t tmem_base;
     __shared__ int s_abort;
 
@@ -87,15 +89,15 @@ __global__ void __launch_bounds__(160, 1) linstate_tc_kernel(const __grid_consta
         mbar_init(&bar_u[0], 1);
         mbar_init(&bar_u[1], 1);
         mbar_init(&bar_ds, 1);
-        mbar_init(&rdy_phi, 128);
+        mbar_init(&rdy_phi, 256);
         fence_barrier_init();
         s_abort = 0;
     }
     // the second feature block stays zero when d_f = 64 (it is read as padding rows of dS)
     if (CBF == 1)
-        for (int i = tid; i < 16384 / 16; i += 160) reinterpret_cast<uint4 *>(sm + Lay::PHI + 16384)[i] = make_uint4(0, 0, 0, 0);
+        for (int i = tid; i < 16384 / 16; i += 288) reinterpret_cast<uint4 *>(sm + Lay::PHI + 16384)[i] = make_uint4(0, 0, 0, 0);
     // the all-ones operand: row 0 of each 64-key block is ones, rows 1..15 zero
-    for (int i = tid; i < 2 * 2048 / 16; i += 160) {
+    for (int i = tid; i < 2 * 2048 / 16; i += 288) {
         const int row = (i * 16 % 2048) / 128;
         const uint32_t one2 = 0x3f803f80u;   // two bf16 ones
         reinterpret_cast<uint4 *>(sm + Lay::ONES)[i] = row == 0 ? make_uint4(one2, one2, one2, one2) : make_uint4(0, 0, 0, 0);
@@ -105,7 +107,7 @@ __global__ void __launch_bounds__(160, 1) linstate_tc_kernel(const __grid_consta
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = tmem_base;
-    const uint32_t tlane = tmem + ((uint32_t)(warp * 32) << 16);
+    const uint32_t tlane = tmem + ((uint32_t)((warp & 3) * 32) << 16);
 
     auto load_blk = [&](int blk) {
         const int st = blk & 1;
@@ -123,9 +125,9 @@ __global__ void __launch_bounds__(160, 1) linstate_tc_kernel(const __grid_consta
     const uint32_t id_dz = idesc_bf16(128, 16, 1, 0);
     uint32_t ph_ds = 0;
 
-    if (warp == 4) {
+    if (warp == 8) {
         // ============================ the issuing warp ============================
-        if (tid == 128) {
+        if (tid == 256) {
             uint32_t ph_full[2] = {0, 0}, pe_phi = 0;
             // U of block blk = K_blk Wf into TMEM half blk & 1
             auto issue_u = [&](int blk) {
@@ -163,11 +165,12 @@ __global__ void __launch_bounds__(160, 1) linstate_tc_kernel(const __grid_consta
                     mma_ss(tmem + TM_DZ, a, sdesc(sb + Lay::ONES + (kk / 64) * 2048 + (kk % 64) * 2, 16, 1024), id_dz, acc);
                 }
                 mma_commit(&bar_ds);
+                // the next block's U (its K came in one block ago; U of block 1 went out first)
+                if (blk >= 1 && blk + 1 < nblk) issue_u(blk + 1);
                 if (blk + 2 < nblk) {
-                    // this stage is free once dS has read its V: block blk + 2 comes in, its U follows
+                    // this stage is free once dS has read its V: block blk + 2 comes in
                     if (!mbar_wait(&bar_ds, ph_ds, P.status)) s_abort = 1;
                     load_blk(blk + 2);
-                    issue_u(blk + 2);
                 }
                 ph_ds ^= 1;
             }
@@ -175,50 +178,64 @@ __global__ void __launch_bounds__(160, 1) linstate_tc_kernel(const __grid_consta
         __syncwarp();
     } else {
         // ============================== the row warps ==============================
+        constexpr int DFH = DF / 2, CH8 = CBD * 4;   // features per half; 16-byte K chunks per half
         uint32_t ph_u[2] = {0, 0}, ph_kf[2] = {0, 0};
-        const int r = tid;
+        const int r = tid & 127, half = tid >> 7;   // key row of the block; which half of it
         for (int blk = 0; blk < nblk; ++blk) {
             const int st = blk & 1;
             const int j = klo + 128 * blk + r;
             uint8_t *kd = sm + Lay::STAGE + st * Lay::STAGE_BYTES;
             const bool in_range = j < khi;
             const int kslot = in_range ? __ldg(P.kslot + unit * dm.N + j) : -1;   // in flight behind the waits
-            // ||k|| of this row, once the block's K has arrived
+            // ||k||^2 over my half of the dimensions, once the block's K has arrived
             bool bad = !mbar_wait(&bar_full[st], ph_kf[st], P.status);
             ph_kf[st] ^= 1;
             float kn2 = 0.f;
 #pragma unroll
-            for (int cb = 0; cb < CBD; ++cb)
+            for (int q = 0; q < CH8; ++q) {
+                const int c = half * CH8 + q;   // 16-byte chunk of the row, 8 per 64-column block
+                const uint4 pk = *reinterpret_cast<const uint4 *>(kd + (c / 8) * 16384 + sw128(r, c % 8));
+                const uint32_t w4[4] = {pk.x, pk.y, pk.z, pk.w};
 #pragma unroll
-                for (int c8 = 0; c8 < 8; ++c8) {
-                    const uint4 pk = *reinterpret_cast<const uint4 *>(kd + cb * 16384 + sw128(r, c8));
-                    const uint32_t w4[4] = {pk.x, pk.y, pk.z, pk.w};
-#pragma unroll
-                    for (int h2 = 0; h2 < 4; ++h2) {
-                        const float a0 = __uint_as_float(w4[h2] << 16), a1 = __uint_as_float(w4[h2] & 0xffff0000u);
-                        kn2 = fmaf(a0, a0, fmaf(a1, a1, kn2));
-                    }
+                for (int h2 = 0; h2 < 4; ++h2) {
+                    const float a0 = __uint_as_float(w4[h2] << 16), a1 = __uint_as_float(w4[h2] & 0xffff0000u);
+                    kn2 = fmaf(a0, a0, fmaf(a1, a1, kn2));
                 }
+            }
             bad |= !mbar_wait(&bar_u[st], ph_u[st], P.status);
             ph_u[st] ^= 1;
             tc_fence_after();
-            // phi of this row: the DF exponentials stay in registers
-            float u[DF];
+            // my half of the features: exponentials against my half's maximum, in registers
+            float u[DFH];
 #pragma unroll
-            for (int c0 = 0; c0 < DF; c0 += 32) tmem_ld32(tlane + TM_U + 128 * st + c0, *reinterpret_cast<float(*)[32]>(u + c0));
+            for (int c0 = 0; c0 < DFH; c0 += 32)
+                tmem_ld32(tlane + TM_U + 128 * st + half * DFH + c0, *reinterpret_cast<float(*)[32]>(u + c0));
             tmem_ld_wait();
             float mu = -INFINITY, s2 = 0.f;
 #pragma unroll
-            for (int i = 0; i < DF; ++i) mu = fmaxf(mu, u[i] * LOG2E);
+            for (int i = 0; i < DFH; ++i) mu = fmaxf(mu, u[i] * LOG2E);
 #pragma unroll
-            for (int i = 0; i < DF; ++i) {
+            for (int i = 0; i < DFH; ++i) {
                 u[i] = exp2_mufu(fmaf(u[i], LOG2E, -mu));
                 s2 = fmaf(u[i], u[i], s2);
             }
-            const float sc = sqrtf(kn2) * rsqrtf(s2);
+            xch[half][r][0] = mu;
+            xch[half][r][1] = s2;
+            xch[half][r][2] = kn2;
+            tc_fence_before();
+            if (named_sync_or(1, 256, bad || *(volatile int *)&s_abort)) break;
+            float sc;
+            {
+                // both halves combine (half 0, half 1) in the same order
+                const float m0 = xch[0][r][0], m1 = xch[1][r][0];
+                const float M = fmaxf(m0, m1);
+                const float ss = xch[0][r][1] * exp2f(2.f * (m0 - M)) + xch[1][r][1] * exp2f(2.f * (m1 - M));
+                const float kk = xch[0][r][2] + xch[1][r][2];
+                sc = sqrtf(kk) * rsqrtf(ss) * exp2f(mu - M);
+            }
             // the previous block's dS / dz MMAs are done with the feature buffer
             if (blk > 0) {
-                bad |= !mbar_wait(&bar_ds, ph_ds, P.status);
+                bad = !mbar_wait(&bar_ds, ph_ds, P.status);
                 ph_ds ^= 1;
             }
             const bool slotted = kslot >= 0;
@@ -230,10 +247,11 @@ __global__ void __launch_bounds__(160, 1) linstate_tc_kernel(const __grid_consta
             const bool tail = in_range && j >= fhi;
             uint16_t *grow = P.phik + (unit * dm.N + (in_range ? j : 0)) * DF;
 #pragma unroll
-            for (int f0 = 0; f0 < DF; f0 += 8) {
+            for (int q = 0; q < DFH; q += 8) {
+                const int f0 = half * DFH + q;
                 uint32_t w4[4];
 #pragma unroll
-                for (int h2 = 0; h2 < 4; ++h2) w4[h2] = pack_bf16(sc * u[f0 + 2 * h2], sc * u[f0 + 2 * h2 + 1]);
+                for (int h2 = 0; h2 < 4; ++h2) w4[h2] = pack_bf16(sc * u[q + 2 * h2], sc * u[q + 2 * h2 + 1]);
                 const uint4 val = make_uint4(w4[0], w4[1], w4[2], w4[3]);
                 const uint4 zero = make_uint4(0, 0, 0, 0);
                 if (tail) *reinterpret_cast<uint4 *>(grow + f0) = slotted ? zero : val;
@@ -241,9 +259,8 @@ __global__ void __launch_bounds__(160, 1) linstate_tc_kernel(const __grid_consta
                 *reinterpret_cast<uint4 *>(sm + Lay::PHI + (f0 / 64) * 16384 + sw128(r, (f0 % 64) / 8)) = folded ? val : zero;
             }
             fence_async_smem();
-            tc_fence_before();
             mbar_arrive(&rdy_phi);
-            if (named_sync_or(1, 128, bad || *(volatile int *)&s_abort)) break;
+            if (named_sync_or(1, 256, bad || *(volatile int *)&s_abort)) break;
             {
                 // rows below fhi: the block holds exactly the table's values (phi, or zero for
                 // slotted keys); each warp stores two 256-byte rows per instruction
@@ -251,21 +268,21 @@ __global__ void __launch_bounds__(160, 1) linstate_tc_kernel(const __grid_consta
                 const int nrow = max(0, min(128, min(khi, fhi) - j0));
                 constexpr int CH = DF / 8;   // 16-byte chunks per row
                 uint16_t *gbase = P.phik + (unit * dm.N + j0) * DF;
-                for (int e = tid; e < nrow * CH; e += 128) {
+                for (int e = tid; e < nrow * CH; e += 256) {
                     const int row = e / CH, ch = e % CH;
                     const uint4 x = *reinterpret_cast<const uint4 *>(sm + Lay::PHI + (ch / 8) * 16384 + sw128(row, ch % 8));
                     *reinterpret_cast<uint4 *>(gbase + (size_t)row * DF + ch * 8) = x;
                 }
             }
-            named_sync_or(1, 128, false);   // the copy's reads end before the buffer is rewritten
+            named_sync_or(1, 256, false);   // the copy's reads end before the buffer is rewritten
         }
-        // dS / dz of this segment
+        // dS / dz of this segment: row r, my half of the columns
         if (nblk > 0 && !*(volatile int *)&s_abort) {
             if (!mbar_wait(&bar_ds, ph_ds, P.status)) s_abort = 1;
             tc_fence_after();
         }
         float *out = P.dS + (unit * (P.sp.nseg + 1) + s) * (size_t)(DF * D);
-        for (int c0 = 0; c0 < D; c0 += 32) {
+        for (int c0 = half * (D / 2); c0 < (half + 1) * (D / 2); c0 += 32) {
             float v[32];
             tmem_ld32(tlane + TM_DS + c0, v);
             tmem_ld_wait();
@@ -274,7 +291,7 @@ __global__ void __launch_bounds__(160, 1) linstate_tc_kernel(const __grid_consta
         }
         const float zacc = tmem_ld1(tlane + TM_DZ);
         tmem_ld_wait();
-        if (r < DF) P.dz[(unit * (P.sp.nseg + 1) + s) * DF + r] = nblk > 0 ? zacc : 0.f;
+        if (r < DF && half == 0) P.dz[(unit * (P.sp.nseg + 1) + s) * DF + r] = nblk > 0 ? zacc : 0.f;
     }
     tc_fence_before();
     __syncthreads();
@@ -305,7 +322,7 @@ cudaError_t launch_linstate_tc(const Dims &dm, const SegPlan &sp, const uint16_t
         e = cudaFuncSetAttribute(linstate_tc_kernel<DD, FF>, cudaFuncAttributeMaxDynamicSharedMemorySize,     \
                                  (int)smem);                                                                  \
         if (e != cudaSuccess) return e;                                                                       \
-        linstate_tc_kernel<DD, FF><<<grid, 160, smem, s>>>(m, p);                                            \
+        linstate_tc_kernel<DD, FF><<<grid, 288, smem, s>>>(m, p);                                            \
     }
     if (D == 64 && DF == 64) STILL_LIN(64, 64)
     else if (D == 64) STILL_LIN(64, 128)
