@@ -40,7 +40,7 @@ struct LinTCParams {
 };
 
 struct LinTCMaps {
-    CUtensorMap k, v, wft;
+    CUtensorMap k, v, wft, phik;   // phik: the feature table, boxes of 128 keys x 64 features
 };
 
 template <int D, int DF>
@@ -64,7 +64,7 @@ __global__ void __launch_bounds__(288, 1) linstate_tc_kernel(const __grid_consta
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     const uint32_t sb = smem_u32(sm);
-    __shared__ uint64_t bar_wf, bar_full[2], bar_u[2], bar_ds, rdy_phi;
+    __shared__ uint64_t bar_wf, bar_full[2], bar_u[2], bar_ds, rdy_phi, phi_free;
     __shared__ float xch[2][128][3];   // per key row and half: max, sum of squares, ||k||^2 part
     __shared__ uint32_t tmem_base;
     __shared__ int s_abort;
@@ -90,6 +90,7 @@ __global__ void __launch_bounds__(288, 1) linstate_tc_kernel(const __grid_consta
         mbar_init(&bar_u[1], 1);
         mbar_init(&bar_ds, 1);
         mbar_init(&rdy_phi, 256);
+        mbar_init(&phi_free, 1);
         fence_barrier_init();
         s_abort = 0;
     }
@@ -165,28 +166,45 @@ __global__ void __launch_bounds__(288, 1) linstate_tc_kernel(const __grid_consta
                     mma_ss(tmem + TM_DZ, a, sdesc(sb + Lay::ONES + (kk / 64) * 2048 + (kk % 64) * 2, 16, 1024), id_dz, acc);
                 }
                 mma_commit(&bar_ds);
+                // a full block of table rows leaves straight from the feature buffer
+                const int j0 = klo + 128 * blk;
+                const bool full = min(khi, fhi) - j0 >= 128;
+                if (full) {
+                    for (int cb = 0; cb < CBF; ++cb)
+                        tma_store_3d(&maps.phik, sm + Lay::PHI + cb * 16384, cb * 64, j0, (int)unit);
+                    tma_store_commit();
+                }
                 // the next block's U (its K came in one block ago; U of block 1 went out first)
                 if (blk >= 1 && blk + 1 < nblk) issue_u(blk + 1);
-                if (blk + 2 < nblk) {
-                    // this stage is free once dS has read its V: block blk + 2 comes in
-                    if (!mbar_wait(&bar_ds, ph_ds, P.status)) s_abort = 1;
-                    load_blk(blk + 2);
-                }
+                // this stage is free once dS has read its V: block blk + 2 comes in; the
+                // feature buffer is free once dS, dz and the store have read it
+                if (!mbar_wait(&bar_ds, ph_ds, P.status)) s_abort = 1;
                 ph_ds ^= 1;
+                if (blk + 2 < nblk) load_blk(blk + 2);
+                if (full) tma_store_wait_read();
+                mbar_arrive(&phi_free);
             }
+            tma_store_wait_all();
         }
         __syncwarp();
     } else {
         // ============================== the row warps ==============================
         constexpr int DFH = DF / 2, CH8 = CBD * 4;   // features per half; 16-byte K chunks per half
-        uint32_t ph_u[2] = {0, 0}, ph_kf[2] = {0, 0};
+        uint32_t ph_u[2] = {0, 0}, ph_kf[2] = {0, 0}, ph_pf = 0;
         const int r = tid & 127, half = tid >> 7;   // key row of the block; which half of it
+        // kept-slot index of this thread's key, one block ahead
+        auto slot_of = [&](int blk) {
+            const int jj = klo + 128 * blk + r;
+            return blk < nblk && jj < khi ? __ldg(P.kslot + unit * dm.N + jj) : -1;
+        };
+        int kslot_next = slot_of(0);
         for (int blk = 0; blk < nblk; ++blk) {
             const int st = blk & 1;
             const int j = klo + 128 * blk + r;
             uint8_t *kd = sm + Lay::STAGE + st * Lay::STAGE_BYTES;
             const bool in_range = j < khi;
-            const int kslot = in_range ? __ldg(P.kslot + unit * dm.N + j) : -1;   // in flight behind the waits
+            const int kslot = kslot_next;
+            kslot_next = slot_of(blk + 1);
             // ||k||^2 over my half of the dimensions, once the block's K has arrived
             bool bad = !mbar_wait(&bar_full[st], ph_kf[st], P.status);
             ph_kf[st] ^= 1;
@@ -233,10 +251,10 @@ __global__ void __launch_bounds__(288, 1) linstate_tc_kernel(const __grid_consta
                 const float kk = xch[0][r][2] + xch[1][r][2];
                 sc = sqrtf(kk) * rsqrtf(ss) * exp2f(mu - M);
             }
-            // the previous block's dS / dz MMAs are done with the feature buffer
+            // the previous block's dS / dz MMAs and table store are done with the feature buffer
             if (blk > 0) {
-                bad = !mbar_wait(&bar_ds, ph_ds, P.status);
-                ph_ds ^= 1;
+                bad = !mbar_wait(&phi_free, ph_pf, P.status);
+                ph_pf ^= 1;
             }
             const bool slotted = kslot >= 0;
             const int KP = dm.T_max * dm.lam;
@@ -260,12 +278,13 @@ __global__ void __launch_bounds__(288, 1) linstate_tc_kernel(const __grid_consta
             }
             fence_async_smem();
             mbar_arrive(&rdy_phi);
-            if (named_sync_or(1, 256, bad || *(volatile int *)&s_abort)) break;
-            {
-                // rows below fhi: the block holds exactly the table's values (phi, or zero for
-                // slotted keys); each warp stores two 256-byte rows per instruction
-                const int j0 = klo + 128 * blk;
-                const int nrow = max(0, min(128, min(khi, fhi) - j0));
+            if (bad) *(volatile int *)&s_abort = 1;
+            const int j0 = klo + 128 * blk;
+            const int nrow = max(0, min(128, min(khi, fhi) - j0));
+            if (nrow > 0 && nrow < 128) {
+                // a partial block: rows below fhi hold exactly the table's values (phi, or zero
+                // for slotted keys); each warp stores two 256-byte rows per instruction
+                if (named_sync_or(1, 256, *(volatile int *)&s_abort)) break;
                 constexpr int CH = DF / 8;   // 16-byte chunks per row
                 uint16_t *gbase = P.phik + (unit * dm.N + j0) * DF;
                 for (int e = tid; e < nrow * CH; e += 256) {
@@ -273,12 +292,12 @@ __global__ void __launch_bounds__(288, 1) linstate_tc_kernel(const __grid_consta
                     const uint4 x = *reinterpret_cast<const uint4 *>(sm + Lay::PHI + (ch / 8) * 16384 + sw128(row, ch % 8));
                     *reinterpret_cast<uint4 *>(gbase + (size_t)row * DF + ch * 8) = x;
                 }
+                named_sync_or(1, 256, false);   // the copy's reads end before the buffer is rewritten
             }
-            named_sync_or(1, 256, false);   // the copy's reads end before the buffer is rewritten
         }
-        // dS / dz of this segment: row r, my half of the columns
+        // dS / dz of this segment: row r, my half of the columns (the last block's MMAs)
         if (nblk > 0 && !*(volatile int *)&s_abort) {
-            if (!mbar_wait(&bar_ds, ph_ds, P.status)) s_abort = 1;
+            if (!mbar_wait(&bar_ds, (uint32_t)((nblk - 1) & 1), P.status)) s_abort = 1;
             tc_fence_after();
         }
         float *out = P.dS + (unit * (P.sp.nseg + 1) + s) * (size_t)(DF * D);
@@ -312,6 +331,8 @@ cudaError_t launch_linstate_tc(const Dims &dm, const SegPlan &sp, const uint16_t
     uint64_t dw[2] = {(uint64_t)D, (uint64_t)DF}, sw[1] = {(uint64_t)D * 2};
     uint32_t boxw[2] = {64, (uint32_t)DF};
     ok = ok && make_tma_map(&m.wft, wft, 2, dw, sw, boxw, true);
+    uint64_t dp[3] = {(uint64_t)DF, (uint64_t)dm.N, units}, sp2[2] = {(uint64_t)DF * 2, (uint64_t)DF * 2 * dm.N};
+    ok = ok && make_tma_map(&m.phik, phik, 3, dp, sp2, box, true);
     if (!ok) return cudaErrorInvalidValue;
     LinTCParams p{dm, sp, kslot, phik, phk, dS, dz, status};
     dim3 grid(sp.nseg, dm.Hkv, dm.B);
