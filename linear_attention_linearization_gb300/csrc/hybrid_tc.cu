@@ -82,8 +82,8 @@ struct TCLayout {
 constexpr int HT_ROWS = 256;               // row threads: 8 warps, two per TMEM lane quarter
 constexpr int HT_THREADS = HT_ROWS + 128;  // and a warpgroup whose first thread issues every TMA copy and MMA
 // registers per thread after the split (launch: 168 x 384 = 64512; rows take
-// 216 x 256, the issuing warpgroup keeps 72 x 128: 62976 of them)
-constexpr int HT_ROW_REGS = 216, HT_ISSUE_REGS = 72;
+// 200 x 256, the issuing warpgroup keeps 104 x 128: 64512 of them)
+constexpr int HT_ROW_REGS = 192, HT_ISSUE_REGS = 120;
 
 template <int D, int DF>
 __global__ void __launch_bounds__(HT_THREADS, 1) hybrid_tc_kernel(const __grid_constant__ TCMaps maps, TCParams P)
@@ -105,7 +105,7 @@ __global__ void __launch_bounds__(HT_THREADS, 1) hybrid_tc_kernel(const __grid_c
     // phi(Q) written, A masked, P written, tile finished (O and dS read,
     // output staged, S_run updated); issuer -> rows: output staging free
     __shared__ uint64_t bar_q, bar_wf, bar_lag, bar_u, bar_s, bar_a, bar_o, bar_ds, bar_k, bar_v;
-    __shared__ uint64_t rdy_phiq, rdy_a, rdy_p, rdy_epi, stg_free;
+    __shared__ uint64_t rdy_phiq, rdy_a, rdy_p1, rdy_p, rdy_epi, stg_free;
     __shared__ uint32_t tmem_base;
     __shared__ int s_abort;
 
@@ -125,7 +125,7 @@ __global__ void __launch_bounds__(HT_THREADS, 1) hybrid_tc_kernel(const __grid_c
     if (tid == 0) {
         for (uint64_t *bb : {&bar_q, &bar_wf, &bar_lag, &bar_u, &bar_s, &bar_a, &bar_o, &bar_ds, &bar_k, &bar_v, &stg_free})
             mbar_init(bb, 1);
-        for (uint64_t *bb : {&rdy_phiq, &rdy_a, &rdy_p, &rdy_epi}) mbar_init(bb, HT_ROWS);
+        for (uint64_t *bb : {&rdy_phiq, &rdy_a, &rdy_p1, &rdy_p, &rdy_epi}) mbar_init(bb, HT_ROWS);
         fence_barrier_init();
         s_abort = 0;
     }
@@ -202,7 +202,7 @@ __global__ void __launch_bounds__(HT_THREADS, 1) hybrid_tc_kernel(const __grid_c
             };
             auto nkb_of = [&](int t0) { return P.nb + (min(t0 / C, dm.T_max) * lam + 31) / 32; };
             uint32_t ph_q = 0, ph_lag = 0, ph_s = 0, ph_o = 0, ph_k = 0, ph_v = 0;
-            uint32_t pe_phiq = 0, pe_a = 0, pe_p = 0, pe_epi = 0;
+            uint32_t pe_phiq = 0, pe_a = 0, pe_p1 = 0, pe_p = 0, pe_epi = 0;
             const uint32_t id_u = idesc_bf16(128, DF, 0, 0);
             const uint32_t id_a = idesc_bf16(128, 32 + NX, 0, 0);
             const uint32_t id_o = idesc_bf16(128, D, 0, 1);
@@ -293,14 +293,21 @@ __global__ void __launch_bounds__(HT_THREADS, 1) hybrid_tc_kernel(const __grid_c
 #pragma unroll 1
                 for (int kk = 0; kk < 32 + NX; kk += 16)
                     mma_ts(tmem + TM_O, tmem + TM_A + kk / 2, dVL + (uint64_t)(kk * 128 >> 4), id_o, 1);
-                // P written: O += sum_kb P_kb V_kb
+                // P written, first the blocks below the split, then the rest: O += sum_kb P_kb V_kb
+                const int split = nkb / 2;
+                ok &= wait(&bar_v, ph_v);
+                ph_v ^= 1;
+                ok &= wait(&rdy_p1, pe_p1);
+                pe_p1 ^= 1;
+                tc_fence_after();
+                for (int kb = 0; kb < split; ++kb) {
+                    mma_ts(tmem + TM_O, tmem + TM_S + 32 * kb, dVR + (uint64_t)(kb * 4096 >> 4), id_o, 1);
+                    mma_ts(tmem + TM_O, tmem + TM_S + 32 * kb + 16, dVR + (uint64_t)((kb * 4096 + 2048) >> 4), id_o, 1);
+                }
                 ok &= wait(&rdy_p, pe_p);
                 pe_p ^= 1;
                 tc_fence_after();
-                ok &= wait(&bar_v, ph_v);
-                ph_v ^= 1;
-                tc_fence_after();
-                for (int kb = 0; kb < nkb; ++kb) {
+                for (int kb = split; kb < nkb; ++kb) {
                     mma_ts(tmem + TM_O, tmem + TM_S + 32 * kb, dVR + (uint64_t)(kb * 4096 >> 4), id_o, 1);
                     mma_ts(tmem + TM_O, tmem + TM_S + 32 * kb + 16, dVR + (uint64_t)((kb * 4096 + 2048) >> 4), id_o, 1);
                 }
@@ -441,6 +448,7 @@ __global__ void __launch_bounds__(HT_THREADS, 1) hybrid_tc_kernel(const __grid_c
                 const float ss = a0 * exp2f(2.f * (m0 - M)) + a1 * exp2f(2.f * (m1 - M));
                 const float qn = sqrtf(q0 + q1);
                 const float sc = qn * rsqrtf(ss) * exp2f(mu - M);   // my half's exponentials were taken against mu
+                float2 dz2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
                 for (int c0 = 0; c0 < DFH; c0 += 16) {
 #pragma unroll
@@ -453,14 +461,17 @@ __global__ void __launch_bounds__(HT_THREADS, 1) hybrid_tc_kernel(const __grid_c
                             const float p1 = sc * eu[c0 + i + 1];
                             w4[h2] = pack_bf16(p0, p1);
                             const int f = half * DFH + c0 + i;
-                            den = fmaf(__uint_as_float(w4[h2] << 16), zrun[f], den);
-                            den = fmaf(__uint_as_float(w4[h2] & 0xffff0000u), zrun[f + 1], den);
+                            const float2 zz = *reinterpret_cast<const float2 *>(zrun + f);
+                            dz2[h2 & 1] = __ffma2_rn(make_float2(__uint_as_float(w4[h2] << 16),
+                                                                 __uint_as_float(w4[h2] & 0xffff0000u)),
+                                                     zz, dz2[h2 & 1]);
                         }
                         const int f0 = half * DFH + c0 + c8 * 8;
                         *reinterpret_cast<uint4 *>(sm + Lay::PHIQ + (f0 / 64) * 16384 + sw128(r, (f0 % 64) / 8)) =
                             make_uint4(w4[0], w4[1], w4[2], w4[3]);
                     }
                 }
+                den = (dz2[0].x + dz2[0].y) + (dz2[1].x + dz2[1].y);
             }
             fence_async_smem();
             mbar_arrive(&rdy_phiq);
@@ -585,16 +596,27 @@ __global__ void __launch_bounds__(HT_THREADS, 1) hybrid_tc_kernel(const __grid_c
                 }
                 tmem_st8(tlane + TM_S + 32 * kb + 16 * half, w);
             };
+            // blocks below the split go to the tensor cores while the rest are formed
+            const int split = nkb / 2;
+            auto p_split = [&](int kb_done) {
+                if (kb_done == split) {
+                    tmem_st_wait();
+                    tc_fence_before();
+                    mbar_arrive(&rdy_p1);
+                }
+            };
+            p_split(0);
             blk_load(0, ba, sva);
             for (int kb = 0; kb < nkb;) {
                 tmem_ld_wait();
                 if (kb + 1 < nkb) blk_load(kb + 1, bb, svb);
                 p_blk(kb, ba, sva);
-                if (++kb >= nkb) break;
+                p_split(++kb);
+                if (kb >= nkb) break;
                 tmem_ld_wait();
                 if (kb + 1 < nkb) blk_load(kb + 1, ba, sva);
                 p_blk(kb, bb, svb);
-                ++kb;
+                p_split(++kb);
             }
             tmem_st1(tlane + TM_X + 10 + half, den);
             tmem_st_wait();
@@ -658,11 +680,12 @@ __global__ void __launch_bounds__(HT_THREADS, 1) hybrid_tc_kernel(const __grid_c
                         *reinterpret_cast<uint4 *>(sm + Lay::SRUN + (c / 64) * (DF * 128) + sw128(f, (c % 64) / 8)) = pk;
                     }
                     if (half == 0) {
-                        float za = 0.f;
+                        float za[4] = {0.f, 0.f, 0.f, 0.f};
                         const int cb = f / 64, c8 = (f % 64) / 8, e = f % 8;
+#pragma unroll
                         for (int tok = 0; tok < 32; ++tok)
-                            za += bf2f(*reinterpret_cast<const uint16_t *>(sm + Lay::PHIK + cb * 6144 + sw128(tok, c8) + e * 2));
-                        zrun[f] += za;
+                            za[tok & 3] += bf2f(*reinterpret_cast<const uint16_t *>(sm + Lay::PHIK + cb * 6144 + sw128(tok, c8) + e * 2));
+                        zrun[f] += (za[0] + za[1]) + (za[2] + za[3]);
                     }
                 }
             }
