@@ -111,7 +111,7 @@ def profile_traffic(kernel):
     if not os.path.exists(path):
         return None
     src_of = {"hybrid_attn": "hybrid_tc.cu", "score": "score_tc.cu", "select": "score_select.cu",
-              "wf_transpose": "features.cu", "features_linstate": "linstate_tc.cu", "scan": "linstate.cu",
+              "prep": "features.cu", "features_linstate": "linstate_tc.cu", "scan": "linstate.cu",
               "decode_step": "decode.cu"}
     f = src_of.get(kernel)
     if not f:

@@ -287,13 +287,10 @@ still_status still_prefill(const still_shape *shape, const still_bf16 *q, const 
     float *dS = (float *)(base + L.dS);
     float *dz = (float *)(base + L.dz);
     const bool tc = hybrid_tc_supported(dm);
-    cudaError_t e = cudaMemsetAsync(base, 0, L.status + 256, s);
-    if (e == cudaSuccess) e = cudaMemsetAsync(kslot, 0xff, (size_t)dm.B * dm.Hkv * dm.N * 4, s);
-    if (e == cudaSuccess) e = cudaMemsetAsync(kk, 0, L.kept_bytes, s);
+    cudaError_t e = launch_prep(dm, Wf, wft, status, kslot, kk, L.kept_bytes, s);
     if (e == cudaSuccess && dm.lam > 0)
         e = score_tc_supported(dm) ? launch_score_tc(dm, q, k, scores, s) : launch_score(dm, q, k, scores, s);
     if (e == cudaSuccess && dm.lam > 0) e = launch_select(dm, scores, sel_idx, fsel, kslot, s, k, v, kk, vk);
-    if (e == cudaSuccess) e = launch_wft(dm, Wf, wft, s);
     if (e == cudaSuccess) e = launch_linstate_tc(dm, sp, k, v, wft, kslot, phik, phk, dS, dz, status, s);
     if (e == cudaSuccess) e = launch_scan(dm, sp, dS, dz, s);
     if (e == cudaSuccess) {

@@ -30,6 +30,34 @@ struct SegPlan {
     int begin[MAX_SEGMENTS + 1];   // first token of each segment (multiples of T); begin[nseg] = N
 };
 
+// ---- programmatic dependent launch ---------------------------------------------
+// Every kernel of the library is launched so that it may be scheduled while
+// the previous kernel on the stream is still finishing; before it touches
+// global memory it waits for that kernel's completion (and the visibility of
+// its writes), then lets the next kernel be scheduled in turn.
+__device__ __forceinline__ void grid_dep_sync()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                                 Args... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
 // ---- bf16 ------------------------------------------------------------------
 __device__ __forceinline__ float bf2f(uint16_t x) { return __uint_as_float(((uint32_t)x) << 16); }
 
@@ -157,7 +185,8 @@ cudaError_t launch_select(const Dims &dm, const float *scores, int32_t *sel_idx,
                           uint16_t *kk = nullptr, uint16_t *vk = nullptr);
 cudaError_t launch_npmap(const uint16_t *x, long long rows, int d, const float *Wf, int df, float *phi,
                          cudaStream_t s);
-cudaError_t launch_wft(const Dims &dm, const float *Wf, uint16_t *wft, cudaStream_t s);
+cudaError_t launch_prep(const Dims &dm, const float *Wf, uint16_t *wft, int32_t *status, int32_t *kslot, void *kept,
+                        size_t kept_bytes, cudaStream_t s);
 cudaError_t launch_linstate_tc(const Dims &dm, const SegPlan &sp, const uint16_t *k, const uint16_t *v,
                                const uint16_t *wft, const int32_t *kslot, uint16_t *phik, uint16_t *phk, float *dS,
                                float *dz, int32_t *status, cudaStream_t s);

@@ -74,6 +74,7 @@ __global__ void __launch_bounds__(256) decode_general_kernel(still_decode_state 
                                                      const uint16_t *__restrict__ v_t, const float *__restrict__ Wf,
                                                      Dims dm, DecodeGeneralSmem L, uint16_t *__restrict__ out_t)
 {
+    grid_dep_sync();
     constexpr int PARTS = 256 / D;
     extern __shared__ __align__(16) unsigned char dsm[];
     float *qs = reinterpret_cast<float *>(dsm + L.off_qs);
@@ -606,6 +607,7 @@ __global__ void __launch_bounds__(DS_THREADS, 2)
                   const uint16_t *__restrict__ v_t, const float *__restrict__ Wf, Dims dm, DecodeSmem L,
                   uint16_t *__restrict__ out_t)
 {
+    grid_dep_sync();
     using namespace sm100;
     constexpr int C4 = D / 4;              // 4-column groups of an output row
     constexpr int RG = DS_THREADS / C4;    // thread rows: S rows / slots handled in parallel
@@ -1150,7 +1152,8 @@ cudaError_t launch_decode(const Dims &dm, const still_decode_state &st, const ui
             if (dev >= 0 && dev < 64) set_bytes[dev] = L.total;                                                \
         }                                                                                                      \
     }                                                                                                          \
-    decode_kernel<DD, FF, GG><<<grid, DS_THREADS, L.total, s>>>(mk, mv, st, q_t, k_t, v_t, Wf, dm, L, out_t);
+    e = launch_kernel(decode_kernel<DD, FF, GG>, grid, dim3(DS_THREADS), L.total, s, mk, mv, st, q_t, k_t, v_t, Wf, dm, \
+                      L, out_t);
 #define STILL_DECODE_G(DD, FF)                                                                                 \
     switch (dm.G) {                                                                                              \
     case 1: STILL_DECODE(DD, FF, 1) break;                                                                       \
@@ -1171,7 +1174,7 @@ cudaError_t launch_decode(const Dims &dm, const still_decode_state &st, const ui
     e = cudaFuncSetAttribute(decode_general_kernel<DD, FF>, cudaFuncAttributeMaxDynamicSharedMemorySize,         \
                              (int)L.total);                                                                      \
     if (e != cudaSuccess) return e;                                                                              \
-    decode_general_kernel<DD, FF><<<grid, 256, L.total, s>>>(st, q_t, k_t, v_t, Wf, dm, L, out_t);
+    e = launch_kernel(decode_general_kernel<DD, FF>, grid, dim3(256), L.total, s, st, q_t, k_t, v_t, Wf, dm, L, out_t);
     if (dm.d == 64 && dm.df == 64) { STILL_DECODE(64, 64) }
     else if (dm.d == 64) { STILL_DECODE(64, 128) }
     else if (dm.df == 64) { STILL_DECODE(128, 64) }
@@ -1201,6 +1204,7 @@ __global__ void __launch_bounds__(256) export_kernel(const uint16_t *__restrict_
                                                      size_t pstride, size_t zstride, Dims dm,
                                                      still_decode_state st)
 {
+    grid_dep_sync();
     const int g = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
     const size_t ug = (size_t)b * dm.Hkv + g;
     const int W = dm.W, C = dm.C, lam = dm.lam, m = dm.m, N = dm.N;
@@ -1280,10 +1284,10 @@ cudaError_t launch_export(const Dims &dm, const SegPlan &sp, const uint16_t *k, 
     const size_t pstride = (size_t)(sp.nseg + 1) * dm.df * dm.d, zstride = (size_t)(sp.nseg + 1) * dm.df;
     const float *Pt = dS + (size_t)sp.nseg * dm.df * dm.d;
     const float *Zt = dz + (size_t)sp.nseg * dm.df;
-    if (dm.d == 64 && dm.df == 64) export_kernel<64, 64><<<grid, 256, 0, s>>>(k, v, scores, fsel, Pt, Zt, pstride, zstride, dm, st);
-    else if (dm.d == 64) export_kernel<64, 128><<<grid, 256, 0, s>>>(k, v, scores, fsel, Pt, Zt, pstride, zstride, dm, st);
-    else if (dm.df == 64) export_kernel<128, 64><<<grid, 256, 0, s>>>(k, v, scores, fsel, Pt, Zt, pstride, zstride, dm, st);
-    else export_kernel<128, 128><<<grid, 256, 0, s>>>(k, v, scores, fsel, Pt, Zt, pstride, zstride, dm, st);
+    auto kern = dm.d == 64 ? (dm.df == 64 ? export_kernel<64, 64> : export_kernel<64, 128>)
+                           : (dm.df == 64 ? export_kernel<128, 64> : export_kernel<128, 128>);
+    const cudaError_t e = launch_kernel(kern, grid, dim3(256), 0, s, k, v, scores, fsel, Pt, Zt, pstride, zstride, dm, st);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

@@ -31,6 +31,7 @@ __global__ void __launch_bounds__(256) hybrid_kernel(const uint16_t *__restrict_
                                                      const float *__restrict__ dz, Dims dm, SegPlan sp,
                                                      uint16_t *__restrict__ out, int32_t *status)
 {
+    grid_dep_sync();
     constexpr int PD = D / 32;          // output dims per lane
     constexpr int PER = DF * D / 256;   // state elements per thread
     constexpr int RSTEP = 256 / D;
@@ -197,7 +198,9 @@ static cudaError_t launch_hybrid_t(const Dims &dm, const SegPlan &sp, const uint
     cudaError_t e = cudaFuncSetAttribute(hybrid_kernel<D, DF>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     dim3 grid(sp.nseg, dm.Hkv, dm.B);
-    hybrid_kernel<D, DF><<<grid, 256, smem, s>>>(q, k, v, Wf, phik, phkept, fsel, dS, dz, dm, sp, out, status);
+    e = launch_kernel(hybrid_kernel<D, DF>, grid, dim3(256), smem, s, q, k, v, Wf, phik, phkept, fsel, dS, dz, dm, sp,
+                      out, status);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

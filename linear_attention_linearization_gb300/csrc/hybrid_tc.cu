@@ -139,6 +139,7 @@ __global__ void __launch_bounds__(HT_THREADS, 1) hybrid_tc_kernel(const __grid_c
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = tmem_base;
+    grid_dep_sync();   // the previous kernel's writes are visible from here on
 
     // bounded wait; gives up early once the other side has given up
     auto wait = [&](uint64_t *bar, uint32_t parity) -> bool {
@@ -776,11 +777,13 @@ cudaError_t launch_hybrid_tc(const Dims &dm, const SegPlan &sp, const TCBuffers 
     if (D == 64) {
         e = cudaFuncSetAttribute(hybrid_tc_kernel<64, 64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        hybrid_tc_kernel<64, 64><<<grid, HT_THREADS, smem, s>>>(m, p);
+        e = launch_kernel(hybrid_tc_kernel<64, 64>, grid, dim3(HT_THREADS), smem, s, m, p);
+        if (e != cudaSuccess) return e;
     } else {
         e = cudaFuncSetAttribute(hybrid_tc_kernel<128, 128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        hybrid_tc_kernel<128, 128><<<grid, HT_THREADS, smem, s>>>(m, p);
+        e = launch_kernel(hybrid_tc_kernel<128, 128>, grid, dim3(HT_THREADS), smem, s, m, p);
+        if (e != cudaSuccess) return e;
     }
     return cudaGetLastError();
 }

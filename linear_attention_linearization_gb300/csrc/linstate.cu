@@ -11,6 +11,7 @@ namespace still {
 // slot nseg receives the total.
 __global__ void scan_kernel(float *__restrict__ dS, float *__restrict__ dz, int nseg, int nel_s, int nel_z)
 {
+    grid_dep_sync();
     const int e = blockIdx.x * blockDim.x + threadIdx.x;
     const size_t ug = blockIdx.y;
     float *p;
@@ -43,7 +44,8 @@ cudaError_t launch_scan(const Dims &dm, const SegPlan &sp, float *dS, float *dz,
     KTimer tm("scan", s);
     const int nel_s = dm.df * dm.d, nel_z = dm.df;
     dim3 grid((nel_s + nel_z + 255) / 256, dm.B * dm.Hkv);
-    scan_kernel<<<grid, 256, 0, s>>>(dS, dz, sp.nseg, nel_s, nel_z);
+    const cudaError_t e = launch_kernel(scan_kernel, grid, dim3(256), 0, s, dS, dz, sp.nseg, nel_s, nel_z);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

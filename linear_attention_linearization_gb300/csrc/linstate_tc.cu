@@ -108,6 +108,7 @@ __global__ void __launch_bounds__(288, 1) linstate_tc_kernel(const __grid_consta
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = tmem_base;
+    grid_dep_sync();   // the previous kernel's writes are visible from here on
     const uint32_t tlane = tmem + ((uint32_t)((warp & 3) * 32) << 16);
 
     auto load_blk = [&](int blk) {
@@ -343,7 +344,8 @@ cudaError_t launch_linstate_tc(const Dims &dm, const SegPlan &sp, const uint16_t
         e = cudaFuncSetAttribute(linstate_tc_kernel<DD, FF>, cudaFuncAttributeMaxDynamicSharedMemorySize,     \
                                  (int)smem);                                                                  \
         if (e != cudaSuccess) return e;                                                                       \
-        linstate_tc_kernel<DD, FF><<<grid, 288, smem, s>>>(m, p);                                            \
+        e = launch_kernel(linstate_tc_kernel<DD, FF>, grid, dim3(288), smem, s, m, p);                     \
+        if (e != cudaSuccess) return e;                                                                    \
     }
     if (D == 64 && DF == 64) STILL_LIN(64, 64)
     else if (D == 64) STILL_LIN(64, 128)

@@ -22,6 +22,7 @@ __global__ void __launch_bounds__(256) score_kernel(const uint16_t *__restrict__
                                                     const uint16_t *__restrict__ k, Dims dm,
                                                     float *__restrict__ scores)
 {
+    grid_dep_sync();
     const int g = blockIdx.y, b = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     __shared__ float qs[8][D];
@@ -65,8 +66,9 @@ cudaError_t launch_score(const Dims &dm, const uint16_t *q, const uint16_t *k, f
 {
     KTimer tm("score", s);
     dim3 grid((dm.N + 63) / 64, dm.Hkv, dm.B);
-    if (dm.d == 64) score_kernel<64><<<grid, 256, 0, s>>>(q, k, dm, scores);
-    else score_kernel<128><<<grid, 256, 0, s>>>(q, k, dm, scores);
+    const cudaError_t e = launch_kernel(dm.d == 64 ? score_kernel<64> : score_kernel<128>, grid, dim3(256), 0, s, q, k,
+                                        dm, scores);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
@@ -85,6 +87,7 @@ __global__ void __launch_bounds__(32) select_kernel(const float *__restrict__ sc
                                                     const uint16_t *__restrict__ v, uint16_t *__restrict__ kk,
                                                     uint16_t *__restrict__ vk)
 {
+    grid_dep_sync();
     extern __shared__ float sel_smem[];
     float *sc = sel_smem;
     uint8_t *taken = reinterpret_cast<uint8_t *>(sc + dm.C);
@@ -179,7 +182,8 @@ cudaError_t launch_select(const Dims &dm, const float *scores, int32_t *sel_idx,
         if (e != cudaSuccess) return e;
     }
     dim3 grid(dm.T_max, dm.Hkv, dm.B);
-    select_kernel<<<grid, 32, smem, s>>>(scores, dm, sel_idx, fsel, kslot, k, v, kk, vk);
+    const cudaError_t e = launch_kernel(select_kernel, grid, dim3(32), smem, s, scores, dm, sel_idx, fsel, kslot, k, v, kk, vk);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
@@ -190,6 +194,7 @@ template <int D, int DF>
 __global__ void __launch_bounds__(256) npmap_kernel(const uint16_t *__restrict__ x, long long rows,
                                                     const float *__restrict__ Wf, float *__restrict__ phi)
 {
+    grid_dep_sync();
     __shared__ float xs[8][D];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     for (long long r = (long long)blockIdx.x * 8 + warp; r < rows; r += (long long)gridDim.x * 8) {
@@ -206,10 +211,10 @@ cudaError_t launch_npmap(const uint16_t *x, long long rows, int d, const float *
     KTimer tm("npmap", s);
     long long blocks = (rows + 7) / 8;
     int grid = (int)(blocks < 152 * 16 ? blocks : 152 * 16);
-    if (d == 64 && df == 64) npmap_kernel<64, 64><<<grid, 256, 0, s>>>(x, rows, Wf, phi);
-    else if (d == 64 && df == 128) npmap_kernel<64, 128><<<grid, 256, 0, s>>>(x, rows, Wf, phi);
-    else if (d == 128 && df == 64) npmap_kernel<128, 64><<<grid, 256, 0, s>>>(x, rows, Wf, phi);
-    else npmap_kernel<128, 128><<<grid, 256, 0, s>>>(x, rows, Wf, phi);
+    auto kern = d == 64 ? (df == 64 ? npmap_kernel<64, 64> : npmap_kernel<64, 128>)
+                        : (df == 64 ? npmap_kernel<128, 64> : npmap_kernel<128, 128>);
+    const cudaError_t e = launch_kernel(kern, grid, dim3(256), 0, s, x, rows, Wf, phi);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

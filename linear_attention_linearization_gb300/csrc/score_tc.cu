@@ -90,6 +90,7 @@ __global__ void __launch_bounds__(SC_THREADS, 1) score_tc_kernel(const __grid_co
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = tmem_base;
+    grid_dep_sync();   // the previous kernel's writes are visible from here on
 
     auto wait = [&](uint64_t *bar, uint32_t parity) -> bool {
         if (mbar_try_wait(bar, parity)) return true;
@@ -278,7 +279,8 @@ cudaError_t launch_score_tc(const Dims &dm, const uint16_t *q, const uint16_t *k
 #define STILL_SCORE(DD, NBB)                                                                                    \
     e = cudaFuncSetAttribute(score_tc_kernel<DD, NBB>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);  \
     if (e != cudaSuccess) return e;                                                                             \
-    score_tc_kernel<DD, NBB><<<grid, SC_THREADS, smem, s>>>(m, p);
+    e = launch_kernel(score_tc_kernel<DD, NBB>, grid, dim3(SC_THREADS), smem, s, m, p);                       \
+    if (e != cudaSuccess) return e;
 #define STILL_SCORE_NB(DD)                                                                                      \
     switch (p.nb) {                                                                                             \
     case 1: STILL_SCORE(DD, 1) break;                                                                           \
