@@ -341,7 +341,14 @@ __global__ void __launch_bounds__(HT_THREADS, 1) hybrid_tc_kernel(const __grid_c
             const float *S0 = P.dS + ((size_t)unit * (P.sp.nseg + 1) + s) * (size_t)(DF * D);
             const int f = r;
 #pragma unroll
-            for (int c = 0; c < DH; ++c) srun[c] = f < DF ? S0[(size_t)f * D + half * DH + c] : 0.f;
+            for (int c = 0; c < DH; c += 4) {
+                const float4 x = f < DF ? *reinterpret_cast<const float4 *>(S0 + (size_t)f * D + half * DH + c)
+                                        : make_float4(0.f, 0.f, 0.f, 0.f);
+                srun[c] = x.x;
+                srun[c + 1] = x.y;
+                srun[c + 2] = x.z;
+                srun[c + 3] = x.w;
+            }
             if (f < DF && half == 0) zrun[f] = P.dz[((size_t)unit * (P.sp.nseg + 1) + s) * DF + f];
             if (f < DF) {
 #pragma unroll
