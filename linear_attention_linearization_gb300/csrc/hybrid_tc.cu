@@ -22,7 +22,8 @@
 //   O   = A V_lagx + sum_kb P_kb V_kb + phi(Q) S_run                       (TMEM)
 //         P = exp(S - c) masked, c = exact row maximum over the softmax keys;
 //         masked A and P are written back to TMEM as bf16 pairs over the
-//         columns they came from and feed the MMAs from there
+//         columns they came from (each thread within the columns it read
+//         itself) and feed the MMAs from there
 //   dS  = phi(K_lag)^T V_lag -> S_run += dS (fp32 in registers, bf16 copy in smem)
 //   y   = O / (sum P + sum A + phi(Q).z_run)                              (TMA store)
 // Masks (window, causal lag, chunk of the kept tokens) are applied to the
@@ -291,9 +292,11 @@ __global__ void __launch_bounds__(HT_THREADS, 1) hybrid_tc_kernel(const __grid_c
                 ok &= wait(&rdy_a, pe_a);
                 pe_a ^= 1;
                 tc_fence_after();
+                // packed lag pairs in columns 0 .. 15 of A, packed extras in 32 .. 39 (each half
+                // packs within the columns it read, so neither overwrites what the other reads)
 #pragma unroll 1
                 for (int kk = 0; kk < 32 + NX; kk += 16)
-                    mma_ts(tmem + TM_O, tmem + TM_A + kk / 2, dVL + (uint64_t)(kk * 128 >> 4), id_o, 1);
+                    mma_ts(tmem + TM_O, tmem + TM_A + (kk < 32 ? kk / 2 : kk), dVL + (uint64_t)(kk * 128 >> 4), id_o, 1);
                 // P written, first the blocks below the split, then the rest: O += sum_kb P_kb V_kb
                 const int split = nkb / 2;
                 ok &= wait(&bar_v, ph_v);
@@ -570,7 +573,7 @@ __global__ void __launch_bounds__(HT_THREADS, 1) hybrid_tc_kernel(const __grid_c
                     den += x0 + x1;
                     w[i / 2] = pack_bf16(x0, x1);
                 }
-                tmem_st8(tlane + TM_A + 16, w);
+                tmem_st8(tlane + TM_A + 32, w);
             }
             tmem_st_wait();
             tc_fence_before();

@@ -306,11 +306,12 @@ __global__ void __launch_bounds__(288, 1) linstate_tc_kernel(const __grid_consta
             float v[32];
             tmem_ld32(tlane + TM_DS + c0, v);
             tmem_ld_wait();
-            if (r < DF)
+            if (r < DF) {
 #pragma unroll
                 for (int i = 0; i < 32; i += 4)
                     *reinterpret_cast<float4 *>(out + (size_t)r * D + c0 + i) =
                         nblk > 0 ? make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
         }
         const float zacc = tmem_ld1(tlane + TM_DZ);
         tmem_ld_wait();

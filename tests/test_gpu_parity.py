@@ -305,3 +305,25 @@ def test_decode_step_16k_batch128():
         yr = ref.decode_step(st_ref, to_f64(qt[b:b + 1]), to_f64(kt[b:b + 1]), to_f64(vt[b:b + 1]), Wa,
                              w.W, w.C, w.m, w.T_max)
         assert np.abs(to_f64(yt[b:b + 1]) - yr).max() <= OUT_TOL * np.abs(yr).max()
+
+
+def test_prefill_repeated_calls_stable():
+    """Many prefills of alternating shapes in one process, each compared with
+    the oracle: a race between the warps that share a row (which show up only
+    under some interleavings) or a dependence on what an earlier call left in
+    reused device memory fails here even when a single call passes."""
+    s = still()
+    cases = [custom(1, 4, 2, 64, 301, 16, 32, 16 + 3 * 8, 8), custom(1, 2, 1, 128, 120, 20, 6, 20 + 1 * 30, 30),
+             custom(2, 8, 2, 128, 260, 64, 64, 64 + 2 * 4, 4)]
+    prepared = []
+    for w in cases:
+        q, k, v, Wf = inputs.make_inputs(w, seed=4)
+        y_ref, _, _ = ref.prefill(*(to_f64(t) for t in (q, k, v, Wf)), w.W, w.C, w.m, w.T_max)
+        prepared.append((w, tuple(t.to(DEV) for t in (q, k, v, Wf)), y_ref))
+    for rep in range(24):
+        for w, (qd, kd, vd, Wd), y_ref in prepared:
+            st = s.DecodeState(w.B, w.Hkv, w.d, w.df, w.C, w.m) if rep % 2 else None
+            out, _ = s.prefill(qd, kd, vd, Wd, w.W, w.C, w.m, w.T_max, export_state=st)
+            torch.cuda.synchronize()
+            err = np.abs(to_f64(out) - y_ref).max()
+            assert err <= OUT_TOL * np.abs(y_ref).max(), (rep, w.N, err)
