@@ -491,7 +491,7 @@ struct DecodeSmem {
     int nslot;      // W + lambda * T_max slots in use
     int R;          // slot rows held in the buffer (nslot rounded up to DS_BOX_ROWS)
     int xrows;      // feature rows: G query heads + at most lambda + 1 linear keys
-    size_t off_buf, off_x, off_phi, off_np, off_w, off_pos, off_kv, off_lin, off_small, total;
+    size_t off_buf, off_x, off_phi, off_np, off_w, off_pos, off_kv, off_lin, off_small, off_qb, total;
 };
 
 static DecodeSmem decode_smem(const Dims &dm)
@@ -509,7 +509,8 @@ static DecodeSmem decode_smem(const Dims &dm)
         return r;
     };
     size_t buf = (size_t)L.R * dm.d * 2;
-    buf = buf > 4ull * rg * dm.G * dm.d ? buf : 4ull * rg * dm.G * dm.d;                 // partial outputs
+    const size_t parts = (size_t)rg + 8 / (dm.d / 16);                                    // + the MMA's slot splits
+    buf = buf > 4ull * parts * dm.G * dm.d ? buf : 4ull * parts * dm.G * dm.d;           // partial outputs
     const size_t fin = (dm.C <= 4096 ? 4ull * dm.C : 0) + 4ull * (dm.lam + 1) + 16;      // chunk completion
     buf = buf > fin ? buf : fin;
     L.off_buf = take(buf, 1024);
@@ -523,8 +524,33 @@ static DecodeSmem decode_smem(const Dims &dm)
     L.off_kv = take(8ull * dm.d, 16);
     L.off_lin = take(4ull * (dm.lam + 1) * (dm.G + 1), 16);
     L.off_small = take(16ull * (dm.lam + 2), 16);
+    L.off_qb = take(2ull * 8 * dm.d, 16);   // bf16 query rows, 8 heads (zero past G): the MMA's B operand
     L.total = o + 1024;   // room to align the base to 1024 bytes
     return L;
+}
+
+// Warp-level bf16 MMA (m16n8k16, fp32 accumulation) and the 8x8 shared-memory
+// matrix loads that feed it.  The decode step's two contractions (q K^T over
+// the slots, and V^T P^T) are too small for the asynchronous tensor-core
+// path; these replace long per-thread dot-product loops.
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4])
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t (&r)[4])
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(addr));
+}
+
+__device__ __forceinline__ void mma_16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1)
+{
+    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+                 "{%8, %9}, {%0, %1, %2, %3};"
+                 : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+                 : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
 // Byte offset of element (row, col) in the staged buffer: 64-column blocks of
@@ -667,6 +693,8 @@ __global__ void __launch_bounds__(DS_THREADS, 2)
     const int c4 = tid % C4, part = tid / C4;
     const float zo = tid < DF ? z[tid] : 0.f;
     for (int i = tid; i < G * D; i += DS_THREADS) xs[i] = bf2f(q_t[((size_t)b * dm.Hq + (size_t)g * G) * D + i]);
+    uint16_t *qb = reinterpret_cast<uint16_t *>(dsm + L.off_qb);
+    for (int i = tid; i < 8 * D; i += DS_THREADS) qb[i] = i < G * D ? q_t[((size_t)b * dm.Hq + (size_t)g * G) * D + i] : (uint16_t)0;
     for (int i = tid; i < D; i += DS_THREADS) {
         ktf[i] = bf2f(k_t[ug * D + i]);
         vtf[i] = bf2f(v_t[ug * D + i]);
@@ -801,6 +829,11 @@ __global__ void __launch_bounds__(DS_THREADS, 2)
         xs[(G + l) * D + x] = src >= 0 ? bf2f(*reinterpret_cast<const uint16_t *>(buf + ds_off(R, src, x))) : ktf[x];
     }
     __syncthreads();
+    // every read of the staged K before this step is done: the window slot of t
+    // takes k_t, so that every slot is a plain row for the logits (the NP-Map's
+    // barriers order these writes before them)
+    if (nslot > 0 && tslot >= 0)
+        for (int x = tid; x < D; x += DS_THREADS) *reinterpret_cast<uint16_t *>(buf + ds_off(R, tslot, x)) = k_t[ug * D + x];
     block_npmap<D, DF>(xs, G + nlin, Wf, phs, npart);
 
     // the linear state S (fp32) into registers; the loads complete behind the logits
@@ -809,48 +842,44 @@ __global__ void __launch_bounds__(DS_THREADS, 2)
     for (int k = 0; k < SR; ++k) Sreg[k] = *reinterpret_cast<const float4 *>(S + (size_t)(part + RG * k) * D + 4 * c4);
 
     // ---- (4)-(5) softmax logits: window (slot t % W now holds t) and kept slots ----
-    for (int sl = tid; sl < nslot; sl += DS_THREADS) {
-        const int p = spos[sl];
-        bool sa;
-        if (sl < W) sa = sl == tslot || p >= 0;
-        else sa = p >= 0 && p / C < ct && p <= t - W;
-        float2 lg[G];
+    // [16 slots x 8 heads] += K[16 slots x 16 dims] q^T[16 dims x 8 heads] per MMA,
+    // one group of 16 slots per warp at a time; heads past G are zero columns
+    {
+        const int g8 = lane >> 2, t4 = lane & 3, mi = lane >> 3;
+        uint32_t qf[D / 16][2];
 #pragma unroll
-        for (int hh = 0; hh < G; ++hh) lg[hh] = make_float2(0.f, 0.f);
-        if (sa) {
-            if (sl == tslot) {
-                for (int x = 0; x < D; x += 2)
+        for (int ks = 0; ks < D / 16; ++ks) {
+            qf[ks][0] = *reinterpret_cast<const uint32_t *>(qb + g8 * D + ks * 16 + 2 * t4);
+            qf[ks][1] = *reinterpret_cast<const uint32_t *>(qb + g8 * D + ks * 16 + 2 * t4 + 8);
+        }
+        const uint32_t bufa = smem_u32(buf);
+        for (int grp = warp; grp * 16 < nslot; grp += DS_THREADS / 32) {
+            // this lane's row address: 8x8 matrix mi holds slots +8 (mi & 1), dims +8 (mi >> 1)
+            const uint32_t row = (uint32_t)(grp * 16 + (mi & 1) * 8 + (lane & 7));
+            float c[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                    for (int hh = 0; hh < G; ++hh)
-                        lg[hh] = __ffma2_rn(make_float2(ktf[x], ktf[x + 1]), make_float2(xs[hh * D + x], xs[hh * D + x + 1]),
-                                            lg[hh]);
-            } else {
-                const unsigned char *rowp = buf + (uint32_t)sl * 128u;
-                const uint32_t r7 = (uint32_t)sl & 7u;
+            for (int ks = 0; ks < D / 16; ++ks) {
+                const uint32_t j = (uint32_t)(2 * ks + (mi >> 1));   // 16-byte chunk of the row
+                uint32_t a[4];
+                ldsm_x4(bufa + (j >> 3) * (uint32_t)R * 128u + sw128(row, j & 7u), a);
+                mma_16816(c, a, qf[ks][0], qf[ks][1]);
+            }
+            // c[2 hf + e]: slot grp*16 + g8 + 8 hf, head 2 t4 + e
 #pragma unroll
-                for (int c = 0; c < D / 8; ++c) {
-                    const uint4 pk = *reinterpret_cast<const uint4 *>(rowp + (uint32_t)(c >> 3) * (uint32_t)R * 128u +
-                                                                      ((((uint32_t)c & 7u) ^ r7) << 4));
-                    const float2 k01 = make_float2(__uint_as_float(pk.x << 16), __uint_as_float(pk.x & 0xffff0000u));
-                    const float2 k23 = make_float2(__uint_as_float(pk.y << 16), __uint_as_float(pk.y & 0xffff0000u));
-                    const float2 k45 = make_float2(__uint_as_float(pk.z << 16), __uint_as_float(pk.z & 0xffff0000u));
-                    const float2 k67 = make_float2(__uint_as_float(pk.w << 16), __uint_as_float(pk.w & 0xffff0000u));
+            for (int hf = 0; hf < 2; ++hf) {
+                const int sl = grp * 16 + g8 + 8 * hf;
+                if (sl >= nslot) continue;
+                const int p = spos[sl];
+                bool sa;
+                if (sl < W) sa = sl == tslot || p >= 0;
+                else sa = p >= 0 && p / C < ct && p <= t - W;
 #pragma unroll
-                    for (int hh = 0; hh < G; ++hh) {
-                        const float4 qa = *reinterpret_cast<const float4 *>(xs + hh * D + 8 * c);
-                        const float4 qb = *reinterpret_cast<const float4 *>(xs + hh * D + 8 * c + 4);
-                        float2 a = lg[hh];
-                        a = __ffma2_rn(k01, make_float2(qa.x, qa.y), a);
-                        a = __ffma2_rn(k23, make_float2(qa.z, qa.w), a);
-                        a = __ffma2_rn(k45, make_float2(qb.x, qb.y), a);
-                        a = __ffma2_rn(k67, make_float2(qb.z, qb.w), a);
-                        lg[hh] = a;
-                    }
+                for (int e2 = 0; e2 < 2; ++e2) {
+                    const int hh = 2 * t4 + e2;
+                    if (hh < G) wsa[hh * nslot + sl] = sa ? c[2 * hf + e2] * inv : -INFINITY;
                 }
             }
         }
-#pragma unroll
-        for (int hh = 0; hh < G; ++hh) wsa[hh * nslot + sl] = sa ? (lg[hh].x + lg[hh].y) * inv : -INFINITY;
     }
     __syncthreads();
     // every read of K in the buffer is done: V takes its place
@@ -927,28 +956,6 @@ __global__ void __launch_bounds__(DS_THREADS, 2)
         v01 = make_float2(__uint_as_float(pk.x << 16), __uint_as_float(pk.x & 0xffff0000u));
         v23 = make_float2(__uint_as_float(pk.y << 16), __uint_as_float(pk.y & 0xffff0000u));
     };
-    // softmax keys (slot sl = part + RG*k; RG is a multiple of 8, so the
-    // swizzle phase sl & 7 is fixed per thread): the window slot of t holds t,
-    // whose row is v_t
-    {
-        const uint32_t vcol = (uint32_t)(c4 >> 4) * (uint32_t)R * 128u +
-                              ((((uint32_t)(c4 >> 1) & 7u) ^ ((uint32_t)part & 7u)) << 4) + (uint32_t)(c4 & 1) * 8u;
-        for (int sl = part; sl < nslot; sl += RG) {
-            float2 v01, v23;
-            if (sl == tslot) {
-                v01 = make_float2(vtf[4 * c4], vtf[4 * c4 + 1]);
-                v23 = make_float2(vtf[4 * c4 + 2], vtf[4 * c4 + 3]);
-            } else {
-                vbuf4(vcol + (uint32_t)sl * 128u, v01, v23);
-            }
-#pragma unroll
-            for (int hh = 0; hh < G; ++hh) {
-                const float w = wsa[hh * nslot + sl];
-                acc[hh][0] = __ffma2_rn(make_float2(w, w), v01, acc[hh][0]);
-                acc[hh][1] = __ffma2_rn(make_float2(w, w), v23, acc[hh][1]);
-            }
-        }
-    }
     // linear keys: a slot of the buffer as it was before this step (the window
     // slot of t still holds the token leaving the window), or v_t when W = 0
     auto vlin4 = [&](int src, float2 &v01, float2 &v23) {
@@ -984,17 +991,60 @@ __global__ void __launch_bounds__(DS_THREADS, 2)
 #pragma unroll
         for (int k = 0; k < SR; ++k) *reinterpret_cast<float4 *>(S + (size_t)(part + RG * k) * D + 4 * c4) = Sreg[k];
     }
+    // ---- softmax keys: V^T P^T on the tensor cores ----------------------------------
+    // The window slot of t takes v_t (the linear keys above have read the token
+    // that left it).  Warp w: output dims [16 (w % MT), +16) over every KSPLIT-th
+    // group of 16 slots; V^T comes from the slot rows by transposing 8x8 loads,
+    // P^T as bf16 pairs of consecutive slots of one head.
+    constexpr int MT = D / 16, KSPLIT = (DS_THREADS / 32) / MT;
+    __syncthreads();
+    if (nslot > 0 && tslot >= 0)
+        for (int x = tid; x < D; x += DS_THREADS) *reinterpret_cast<uint16_t *>(buf + ds_off(R, tslot, x)) = v_t[ug * D + x];
+    __syncthreads();
+    const int mt = warp % MT, kp = warp / MT;
+    float pv[4] = {0.f, 0.f, 0.f, 0.f};
+    {
+        const int g8 = lane >> 2, t4 = lane & 3, mi = lane >> 3;
+        const uint32_t bufa = smem_u32(buf);
+        const uint32_t j = (uint32_t)(2 * mt + (mi & 1));   // 16-byte chunk of the slot row
+        for (int ks = kp; ks * 16 < nslot; ks += KSPLIT) {
+            const int k0 = ks * 16;
+            const uint32_t row = (uint32_t)(k0 + (mi >> 1) * 8 + (lane & 7));
+            uint32_t a[4];
+            ldsm_x4_trans(bufa + (j >> 3) * (uint32_t)R * 128u + sw128(row, j & 7u), a);
+            uint32_t bb[2];
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+                const int s0 = k0 + 2 * t4 + 8 * hf;
+                const float w0 = (g8 < G && s0 < nslot) ? wsa[g8 * nslot + s0] : 0.f;
+                const float w1 = (g8 < G && s0 + 1 < nslot) ? wsa[g8 * nslot + s0 + 1] : 0.f;
+                bb[hf] = pack_bf16(w0, w1);
+            }
+            mma_16816(pv, a, bb[0], bb[1]);
+        }
+    }
     __syncthreads();   // all reads of V in the buffer are done: partial outputs take its place
     float *red = reinterpret_cast<float *>(buf);
 #pragma unroll
     for (int hh = 0; hh < G; ++hh)
         *reinterpret_cast<float4 *>(red + ((size_t)part * G + hh) * D + 4 * c4) =
             make_float4(acc[hh][0].x, acc[hh][0].y, acc[hh][1].x, acc[hh][1].y);
+    {
+        // pv[2 hf + e]: dim 16 mt + g8 + 8 hf, head 2 t4 + e
+        const int g8 = lane >> 2, t4 = lane & 3;
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf)
+#pragma unroll
+            for (int e2 = 0; e2 < 2; ++e2) {
+                const int hh = 2 * t4 + e2;
+                if (hh < G) red[((size_t)(RG + kp) * G + hh) * D + 16 * mt + g8 + 8 * hf] = pv[2 * hf + e2];
+            }
+    }
     __syncthreads();
     for (int i = tid; i < G * D; i += DS_THREADS) {
         const int hh = i / D, c = i % D;
         float num = 0.f;
-        for (int p2 = 0; p2 < RG; ++p2) num += red[((size_t)p2 * G + hh) * D + c];
+        for (int p2 = 0; p2 < RG + KSPLIT; ++p2) num += red[((size_t)p2 * G + hh) * D + c];
         const float den = s_den[hh];
         out_t[((size_t)b * dm.Hq + (size_t)g * G + hh) * D + c] = f2bf(den != 0.f ? num / den : 0.f);
     }

@@ -61,6 +61,9 @@ struct TCMaps {
 constexpr int TM_S = 0, TM_O = 320, TM_A = 448, TM_X = 496, TM_COLS = 512;   // TM_X: row exchange
 constexpr int MAX_KEY_BLOCKS = 9;    // 288 logit columns: every block of a tile stays resident
 constexpr int NX = 16;               // extra (kept, own chunk) rows per tile
+// kept positions a CTA reads: the kept prefix of at most 256 softmax keys plus
+// the lambda <= NX of the tile's own chunk
+constexpr int FSEL_MAX = (MAX_KEY_BLOCKS - 1) * 32 + NX;
 
 constexpr int RING_SLOTS = 9;        // K (then V) blocks of 32 keys resident
 
@@ -75,8 +78,8 @@ struct TCLayout {
     static constexpr uint32_t RSTRIDE = RING_SLOTS * 4096;     // bytes between the column-block regions
     static constexpr uint32_t PHIK = RING + CBD * RSTRIDE;
     static constexpr uint32_t VLAG = PHIK + CBF * 6144;
-    static constexpr uint32_t XPOS = VLAG + CBD * 6144;
-    static constexpr uint32_t ZRUN = XPOS + NX * 4;
+    static constexpr uint32_t FSEL = VLAG + CBD * 6144;       // kept positions, chunk-major
+    static constexpr uint32_t ZRUN = FSEL + FSEL_MAX * 4;
     static constexpr uint32_t TOTAL = ZRUN + DF * 4;
 };
 
@@ -99,7 +102,7 @@ __global__ void __launch_bounds__(HT_THREADS, 1) hybrid_tc_kernel(const __grid_c
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     const uint32_t sb = smem_u32(sm);
-    int32_t *xpos = (int32_t *)(sm + Lay::XPOS);
+    int32_t *fsm = (int32_t *)(sm + Lay::FSEL);
     float *zrun = (float *)(sm + Lay::ZRUN);
 
     // issuer -> rows: U, S, A (+ phi(Q) S_run), O, dS complete; rows -> issuer:
@@ -333,6 +336,12 @@ __global__ void __launch_bounds__(HT_THREADS, 1) hybrid_tc_kernel(const __grid_c
     } else {
         // ============================ the row warps =============================
         regs_inc<HT_ROW_REGS>();
+        // the kept positions of every chunk this CTA can see, once (read after the first row sync)
+        {
+            const int nch = (dm.N + C - 1) / C;
+            const int nfs = min(dm.T_max, nch) * lam;
+            for (int i = tid; i < nfs; i += HT_ROWS) fsm[i] = __ldg(fs + i);
+        }
         const int quarter = warp & 3, half = warp >> 2;
         const int r = quarter * 32 + lane;            // the tile row (and state row) this thread serves
         const float l2s = LOG2E * rsqrtf((float)D);
@@ -387,7 +396,6 @@ __global__ void __launch_bounds__(HT_THREADS, 1) hybrid_tc_kernel(const __grid_c
             const int blo = row_ok ? max(t - W + 1, 0) - band_lo : 1, bhi = row_ok ? t - band_lo : 0;
             const int llo = max(0, W - t0), lhi = row_ok ? t - t0 : -1;
 
-            if (tid < NX) xpos[tid] = (ct < dm.T_max && tid < lam) ? fs[ct * lam + tid] : INT_MAX;
 
             // ---------------- ||q||^2 of my half of the row ----------------------------------
             bool bad = !wait(&bar_q, ph_q);
@@ -436,10 +444,11 @@ __global__ void __launch_bounds__(HT_THREADS, 1) hybrid_tc_kernel(const __grid_c
                 int lo = 0, hi = nkg;
                 while (lo < hi) {
                     const int mid = (lo + hi) >> 1;
-                    if (__ldg(fs + mid) <= t - W) lo = mid + 1; else hi = mid;
+                    if (fsm[mid] <= t - W) lo = mid + 1; else hi = mid;
                 }
                 nvk = row_ok ? lo : 0;
-                while (nvx < NX && xpos[nvx] <= t - W) ++nvx;
+                if (ct < dm.T_max)
+                    while (nvx < lam && fsm[ct * lam + nvx] <= t - W) ++nvx;
                 if (!row_ok) nvx = 0;
             }
             float xo[4];
@@ -725,6 +734,7 @@ bool hybrid_tc_supported(const Dims &dm)
     if (nb > 8) return false;   // the band is one TMA box of at most 256 rows
     const int nchunks = (dm.N + dm.C - 1) / dm.C;
     const int maxg = dm.lam * min(dm.T_max, max(nchunks - 1, 0));
+    if (dm.lam * min(dm.T_max, nchunks) > FSEL_MAX) return false;   // the shared copy of the kept positions
     return nb + (maxg + 31) / 32 <= MAX_KEY_BLOCKS;
 }
 
