@@ -24,7 +24,8 @@
 //         masked A and P are written back to TMEM as bf16 pairs over the
 //         columns they came from (each thread within the columns it read
 //         itself) and feed the MMAs from there
-//   dS  = phi(K_lag)^T V_lag -> S_run += dS (fp32 in registers, bf16 copy in smem)
+//   dS  = phi(K_lag)^T V_lag, dz = phi(K_lag)^T 1 -> S_run += dS, z_run += dz
+//         (fp32 in registers and shared memory, bf16 copy of S_run in smem)
 //   y   = O / (sum P + sum A + phi(Q).z_run)                              (TMA store)
 // Masks (window, causal lag, chunk of the kept tokens) are applied to the
 // logits in TMEM by the row threads -- two warps per TMEM lane quarter, each
@@ -58,12 +59,10 @@ struct TCMaps {
     CUtensorMap q, out, kband, vband, kk32, kk64, kk128, vk32, vk64, vk128, v, vk16, phik, phk16, wft;
 };
 
-constexpr int TM_S = 0, TM_O = 320, TM_A = 448, TM_X = 496, TM_COLS = 512;   // TM_X: row exchange
+// logits (and, once P V is done, dS at 0 and dz at TM_DZ), row exchange, O, A
+constexpr int TM_S = 0, TM_DZ = 256, TM_X = 288, TM_O = 320, TM_A = 448, TM_COLS = 512;
 constexpr int MAX_KEY_BLOCKS = 9;    // 288 logit columns: every block of a tile stays resident
 constexpr int NX = 16;               // extra (kept, own chunk) rows per tile
-// kept positions a CTA reads: the kept prefix of at most 256 softmax keys plus
-// the lambda <= NX of the tile's own chunk
-constexpr int FSEL_MAX = (MAX_KEY_BLOCKS - 1) * 32 + NX;
 
 constexpr int RING_SLOTS = 9;        // K (then V) blocks of 32 keys resident
 
@@ -76,10 +75,13 @@ struct TCLayout {
     static constexpr uint32_t SRUN = PHIQ + (CBD > CBF ? CBD : CBF) * 16384;
     static constexpr uint32_t RING = SRUN + CBD * DF * 128;   // CBD regions of RING_SLOTS x 32 rows x 128 B
     static constexpr uint32_t RSTRIDE = RING_SLOTS * 4096;     // bytes between the column-block regions
-    static constexpr uint32_t PHIK = RING + CBD * RSTRIDE;
+    // one 1024-byte swizzle atom whose row 0 is 64 bf16 ones: the B operand of
+    // phi(K_lag)^T 1 (rows 1..15 feed output columns that are never read)
+    static constexpr uint32_t ONES = RING + CBD * RSTRIDE;
+    static constexpr uint32_t PHIK = ONES + 1024;
     static constexpr uint32_t VLAG = PHIK + CBF * 6144;
-    static constexpr uint32_t FSEL = VLAG + CBD * 6144;       // kept positions, chunk-major
-    static constexpr uint32_t ZRUN = FSEL + FSEL_MAX * 4;
+    static constexpr uint32_t XPOS = VLAG + CBD * 6144;
+    static constexpr uint32_t ZRUN = XPOS + NX * 4;
     static constexpr uint32_t TOTAL = ZRUN + DF * 4;
 };
 
@@ -102,7 +104,7 @@ __global__ void __launch_bounds__(HT_THREADS, 1) hybrid_tc_kernel(const __grid_c
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     const uint32_t sb = smem_u32(sm);
-    int32_t *fsm = (int32_t *)(sm + Lay::FSEL);
+    int32_t *xpos = (int32_t *)(sm + Lay::XPOS);
     float *zrun = (float *)(sm + Lay::ZRUN);
 
     // issuer -> rows: U, S, A (+ phi(Q) S_run), O, dS complete; rows -> issuer:
@@ -132,6 +134,11 @@ __global__ void __launch_bounds__(HT_THREADS, 1) hybrid_tc_kernel(const __grid_c
         for (uint64_t *bb : {&rdy_phiq, &rdy_a, &rdy_p1, &rdy_p, &rdy_epi}) mbar_init(bb, HT_ROWS);
         fence_barrier_init();
         s_abort = 0;
+    }
+    // the ones row (and zero rows below it)
+    for (int i = tid; i < 1024 / 16; i += HT_THREADS) {
+        const uint32_t one2 = 0x3f803f80u;   // two bf16 ones
+        reinterpret_cast<uint4 *>(sm + Lay::ONES)[i] = i < 8 ? make_uint4(one2, one2, one2, one2) : make_uint4(0, 0, 0, 0);
     }
     // padding rows of absent heads stay zero for the whole kernel
     for (int i = tid; i < CBD * 16384 / 16; i += HT_THREADS) {
@@ -212,6 +219,7 @@ __global__ void __launch_bounds__(HT_THREADS, 1) hybrid_tc_kernel(const __grid_c
             const uint32_t id_a = idesc_bf16(128, 32 + NX, 0, 0);
             const uint32_t id_o = idesc_bf16(128, D, 0, 1);
             const uint32_t id_ds = idesc_bf16(128, D, 1, 1);
+            const uint32_t id_dz = idesc_bf16(128, 16, 1, 0);   // phi(K_lag)^T 1
             auto koff = [](int k, uint32_t blockbytes) { return (uint64_t)(((k / 64) * blockbytes + (k % 64) * 2) >> 4); };
             auto kdesc = [&](uint32_t base, int k, uint32_t blockbytes) {   // K-major operand, K step k
                 return sdesc(base + (k / 64) * blockbytes + (k % 64) * 2, 16, 1024);
@@ -323,9 +331,11 @@ __global__ void __launch_bounds__(HT_THREADS, 1) hybrid_tc_kernel(const __grid_c
                 ok &= wait(&bar_o, ph_o);
                 ph_o ^= 1;
                 tc_fence_after();
-                for (int kk = 0; kk < 32; kk += 16)
-                    mma_ss(tmem + TM_S, sdesc(sb + Lay::PHIK + kk * 128, 6144, 1024),
-                           sdesc(sb + Lay::VLAG + kk * 128, 6144, 1024), id_ds, kk > 0);
+                for (int kk = 0; kk < 32; kk += 16) {
+                    const uint64_t dphi = sdesc(sb + Lay::PHIK + kk * 128, 6144, 1024);
+                    mma_ss(tmem + TM_S, dphi, sdesc(sb + Lay::VLAG + kk * 128, 6144, 1024), id_ds, kk > 0);
+                    mma_ss(tmem + TM_DZ, dphi, sdesc(sb + Lay::ONES + kk * 2, 16, 1024), id_dz, kk > 0);
+                }
                 mma_commit(&bar_ds);
                 if (has_next) load_keys(t0 + 32, nkb_of(t0 + 32), 0);
             }
@@ -336,12 +346,6 @@ __global__ void __launch_bounds__(HT_THREADS, 1) hybrid_tc_kernel(const __grid_c
     } else {
         // ============================ the row warps =============================
         regs_inc<HT_ROW_REGS>();
-        // the kept positions of every chunk this CTA can see, once (read after the first row sync)
-        {
-            const int nch = (dm.N + C - 1) / C;
-            const int nfs = min(dm.T_max, nch) * lam;
-            for (int i = tid; i < nfs; i += HT_ROWS) fsm[i] = __ldg(fs + i);
-        }
         const int quarter = warp & 3, half = warp >> 2;
         const int r = quarter * 32 + lane;            // the tile row (and state row) this thread serves
         const float l2s = LOG2E * rsqrtf((float)D);
@@ -378,8 +382,8 @@ __global__ void __launch_bounds__(HT_THREADS, 1) hybrid_tc_kernel(const __grid_c
         uint32_t ph_q = 0, ph_u = 0, ph_s = 0, ph_a = 0, ph_o = 0, ph_ds = 0, ph_stg = 0;
         // per-row values the two warps of a lane quarter exchange go through
         // TMEM columns TM_X.. of the row's lane: NP-Map statistics of half h at
-        // [TM_X + 4h, +3), its row maximum at TM_X + 8 + h, its denominator at
-        // TM_X + 10 + h
+        // [TM_X + 4h, +3), its row maximum at TM_X + 8 + h, its share of the
+        // denominator at TM_X + 10 + h
         auto sync_rows = [&](bool bad) { return named_sync_or(1, HT_ROWS, bad || *(volatile int *)&s_abort); };
 
         for (int it = 0; it < ntiles; ++it) {
@@ -396,6 +400,7 @@ __global__ void __launch_bounds__(HT_THREADS, 1) hybrid_tc_kernel(const __grid_c
             const int blo = row_ok ? max(t - W + 1, 0) - band_lo : 1, bhi = row_ok ? t - band_lo : 0;
             const int llo = max(0, W - t0), lhi = row_ok ? t - t0 : -1;
 
+            if (tid < NX) xpos[tid] = (ct < dm.T_max && tid < lam) ? fs[ct * lam + tid] : INT_MAX;
 
             // ---------------- ||q||^2 of my half of the row ----------------------------------
             bool bad = !wait(&bar_q, ph_q);
@@ -444,11 +449,10 @@ __global__ void __launch_bounds__(HT_THREADS, 1) hybrid_tc_kernel(const __grid_c
                 int lo = 0, hi = nkg;
                 while (lo < hi) {
                     const int mid = (lo + hi) >> 1;
-                    if (fsm[mid] <= t - W) lo = mid + 1; else hi = mid;
+                    if (__ldg(fs + mid) <= t - W) lo = mid + 1; else hi = mid;
                 }
                 nvk = row_ok ? lo : 0;
-                if (ct < dm.T_max)
-                    while (nvx < lam && fsm[ct * lam + nvx] <= t - W) ++nvx;
+                while (nvx < NX && xpos[nvx] <= t - W) ++nvx;
                 if (!row_ok) nvx = 0;
             }
             float xo[4];
@@ -638,26 +642,26 @@ __global__ void __launch_bounds__(HT_THREADS, 1) hybrid_tc_kernel(const __grid_c
                 p_blk(kb, bb, svb);
                 p_split(++kb);
             }
+            // my share of the denominator goes with P: the partner reads it once the
+            // P V MMAs, which every row's P precedes, are complete
             tmem_st1(tlane + TM_X + 10 + half, den);
             tmem_st_wait();
             tc_fence_before();
             mbar_arrive(&rdy_p);
-            if (sync_rows(bad)) break;
-            tc_fence_after();
-            const float dtot = den + tmem_ld1(tlane + TM_X + 10 + (1 - half));
-            tmem_ld_wait();
 
             // ---------------- epilogue: y = O / den (my half of the columns) ---------------
-            bad = !wait(&bar_o, ph_o);
+            bad |= !wait(&bar_o, ph_o);
             ph_o ^= 1;
             tc_fence_after();
             {
-                const float inv = dtot != 0.f ? 1.f / dtot : 0.f;
                 float ov[DH];
 #pragma unroll
                 for (int c0 = 0; c0 < DH; c0 += 16)
                     tmem_ld16(tlane + TM_O + half * DH + c0, *reinterpret_cast<float(*)[16]>(ov + c0));
+                const float dpart = tmem_ld1(tlane + TM_X + 10 + (1 - half));
                 tmem_ld_wait();
+                const float dtot = den + dpart;
+                const float inv = dtot != 0.f ? 1.f / dtot : 0.f;
 #pragma unroll
                 for (int c0 = 0; c0 < DH; c0 += 16) {
                     const float *o = ov + c0;
@@ -679,11 +683,13 @@ __global__ void __launch_bounds__(HT_THREADS, 1) hybrid_tc_kernel(const __grid_c
             tc_fence_after();
             {
                 const int f = r;
+                float dzf;
                 {
                     float ds[DH];
 #pragma unroll
                     for (int c0 = 0; c0 < DH; c0 += 16)
                         tmem_ld16(tlane + TM_S + half * DH + c0, *reinterpret_cast<float(*)[16]>(ds + c0));
+                    dzf = tmem_ld1(tlane + TM_DZ);
                     tmem_ld_wait();
 #pragma unroll
                     for (int i = 0; i < DH; ++i) srun[i] += ds[i];
@@ -699,14 +705,7 @@ __global__ void __launch_bounds__(HT_THREADS, 1) hybrid_tc_kernel(const __grid_c
                         pk.w = pack_bf16(srun[c8 * 8 + 6], srun[c8 * 8 + 7]);
                         *reinterpret_cast<uint4 *>(sm + Lay::SRUN + (c / 64) * (DF * 128) + sw128(f, (c % 64) / 8)) = pk;
                     }
-                    if (half == 0) {
-                        float za[4] = {0.f, 0.f, 0.f, 0.f};
-                        const int cb = f / 64, c8 = (f % 64) / 8, e = f % 8;
-#pragma unroll
-                        for (int tok = 0; tok < 32; ++tok)
-                            za[tok & 3] += bf2f(*reinterpret_cast<const uint16_t *>(sm + Lay::PHIK + cb * 6144 + sw128(tok, c8) + e * 2));
-                        zrun[f] += (za[0] + za[1]) + (za[2] + za[3]);
-                    }
+                    if (half == 0) zrun[f] += dzf;
                 }
             }
             fence_async_smem();
@@ -734,7 +733,6 @@ bool hybrid_tc_supported(const Dims &dm)
     if (nb > 8) return false;   // the band is one TMA box of at most 256 rows
     const int nchunks = (dm.N + dm.C - 1) / dm.C;
     const int maxg = dm.lam * min(dm.T_max, max(nchunks - 1, 0));
-    if (dm.lam * min(dm.T_max, nchunks) > FSEL_MAX) return false;   // the shared copy of the kept positions
     return nb + (maxg + 31) / 32 <= MAX_KEY_BLOCKS;
 }
 
