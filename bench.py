@@ -16,6 +16,7 @@ runs it.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import os
@@ -42,6 +43,9 @@ def parse(argv=None):
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--no-decode", action="store_true", help="skip the decode-step measurement")
+    p.add_argument("--decode-seqs", type=int, default=0,
+                   help="sequences of the decode workload (default: the workload's 128); a smaller batch "
+                        "keeps an ncu capture of the decode kernel to a few GB of device memory")
     p.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--cpu-tokens", type=int, default=16384, help="tokens of the CPU-baseline sample")
@@ -415,6 +419,8 @@ def run_ours(args):
 def bench_decode(still, inputs, dev, stream, pk, pk_kind, args):
     import torch
     w = inputs.WORKLOADS[DECODE_WORKLOAD]
+    if args.decode_seqs > 0:
+        w = dataclasses.replace(w, B=args.decode_seqs)
     q, k, v, Wf = inputs.make_inputs(w, seed=args.seed + 7, device=dev)
     st = still.DecodeState(w.B, w.Hkv, w.d, w.df, w.C, w.m, device=dev)
     still.prefill(q, k, v, Wf, w.W, w.C, w.m, w.T_max, export_state=st, stream=stream)

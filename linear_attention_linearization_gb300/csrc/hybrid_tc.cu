@@ -28,8 +28,9 @@
 //         (fp32 in registers and shared memory, bf16 copy of S_run in smem)
 //   y   = O / (sum P + sum A + phi(Q).z_run)                              (TMA store)
 // Masks (window, causal lag, chunk of the kept tokens) are applied to the
-// logits in TMEM by the row threads -- two warps per TMEM lane quarter, each
-// owning half of a row's columns -- and one thread issues every TMA and MMA.
+// logits in TMEM by the row threads -- four warps per TMEM lane quarter, each
+// owning a quarter of U, O and dS and every fourth block of 32 keys -- and one
+// thread issues every TMA and MMA.
 #include <climits>
 
 #include "sm100.cuh"
@@ -59,8 +60,9 @@ struct TCMaps {
     CUtensorMap q, out, kband, vband, kk32, kk64, kk128, vk32, vk64, vk128, v, vk16, phik, phk16, wft;
 };
 
-// logits (and, once P V is done, dS at 0 and dz at TM_DZ), row exchange, O, A
-constexpr int TM_S = 0, TM_DZ = 256, TM_X = 288, TM_O = 320, TM_A = 448, TM_COLS = 512;
+// logits (and, once P V is done, dS at 0 and dz at TM_DZ), row exchange (NP-Map
+// statistics at TM_X, row maxima and denominator shares at TM_X2), O, A
+constexpr int TM_S = 0, TM_DZ = 256, TM_X = 288, TM_X2 = 304, TM_O = 320, TM_A = 448, TM_COLS = 512;
 constexpr int MAX_KEY_BLOCKS = 9;    // 288 logit columns: every block of a tile stays resident
 constexpr int NX = 16;               // extra (kept, own chunk) rows per tile
 
@@ -85,18 +87,20 @@ struct TCLayout {
     static constexpr uint32_t TOTAL = ZRUN + DF * 4;
 };
 
-constexpr int HT_ROWS = 256;               // row threads: 8 warps, two per TMEM lane quarter
+constexpr int HT_PARTS = 4;                // row warps per TMEM lane quarter
+constexpr int HT_ROWS = 128 * HT_PARTS;    // row threads: 16 warps
 constexpr int HT_THREADS = HT_ROWS + 128;  // and a warpgroup whose first thread issues every TMA copy and MMA
-// registers per thread after the split (launch: 168 x 384 = 64512; rows take
-// 200 x 256, the issuing warpgroup keeps 104 x 128: 64512 of them)
-constexpr int HT_ROW_REGS = 192, HT_ISSUE_REGS = 120;
+// registers per thread after the split: the launch gives 96 x 640 = 61440; the
+// row warps take 104 x 512 = 53248 and the issuing warpgroup keeps 64 x 128 = 8192
+constexpr int HT_LAUNCH_REGS = 96, HT_ROW_REGS = 104, HT_ISSUE_REGS = 64;
+static_assert(HT_ROWS * HT_ROW_REGS + 128 * HT_ISSUE_REGS <= HT_THREADS * HT_LAUNCH_REGS,
+              "the register split exceeds what the block is launched with");
 
 template <int D, int DF>
 __global__ void __launch_bounds__(HT_THREADS, 1) hybrid_tc_kernel(const __grid_constant__ TCMaps maps, TCParams P)
 {
     using Lay = TCLayout<D, DF>;
     constexpr int CBD = Lay::CBD, CBF = Lay::CBF;
-    constexpr int DH = D / 2, DFH = DF / 2;   // columns per half-row thread
     constexpr float LOG2E = 1.4426950408889634f;
     constexpr uint32_t SLOT = CBD * 4096;     // bytes of one ring slot (32 keys x D)
     constexpr uint32_t RSTRIDE = Lay::RSTRIDE;
@@ -345,31 +349,36 @@ __global__ void __launch_bounds__(HT_THREADS, 1) hybrid_tc_kernel(const __grid_c
         __syncwarp();
     } else {
         // ============================ the row warps =============================
+        // Four warps per TMEM lane quarter.  Part p of a row owns the columns
+        // [p DQ, (p + 1) DQ) of U, O and dS, the 32-key logit blocks kb = p mod 4
+        // (so a block's P is packed over the columns its own thread read), and
+        // one piece of A (part 0 the lag keys, part 1 the own-chunk extras).
         regs_inc<HT_ROW_REGS>();
-        const int quarter = warp & 3, half = warp >> 2;
+        constexpr int DQ = D / HT_PARTS, FQ = DF / HT_PARTS;
+        const int quarter = warp & 3, part = warp >> 2;
         const int r = quarter * 32 + lane;            // the tile row (and state row) this thread serves
         const float l2s = LOG2E * rsqrtf((float)D);
         const uint32_t tlane = tmem + ((uint32_t)(quarter * 32) << 16);   // this warp's TMEM lanes
 
-        // running linear state: row f = r, columns [half*DH, half*DH + DH) in fp32
-        float srun[DH];
+        // running linear state: row f = r, columns [part*DQ, part*DQ + DQ) in fp32
+        float srun[DQ];
         {
             const float *S0 = P.dS + ((size_t)unit * (P.sp.nseg + 1) + s) * (size_t)(DF * D);
             const int f = r;
 #pragma unroll
-            for (int c = 0; c < DH; c += 4) {
-                const float4 x = f < DF ? *reinterpret_cast<const float4 *>(S0 + (size_t)f * D + half * DH + c)
+            for (int c = 0; c < DQ; c += 4) {
+                const float4 x = f < DF ? *reinterpret_cast<const float4 *>(S0 + (size_t)f * D + part * DQ + c)
                                         : make_float4(0.f, 0.f, 0.f, 0.f);
                 srun[c] = x.x;
                 srun[c + 1] = x.y;
                 srun[c + 2] = x.z;
                 srun[c + 3] = x.w;
             }
-            if (f < DF && half == 0) zrun[f] = P.dz[((size_t)unit * (P.sp.nseg + 1) + s) * DF + f];
+            if (f < DF && part == 0) zrun[f] = P.dz[((size_t)unit * (P.sp.nseg + 1) + s) * DF + f];
             if (f < DF) {
 #pragma unroll
-                for (int c8 = 0; c8 < DH / 8; ++c8) {
-                    const int c = half * DH + c8 * 8;
+                for (int c8 = 0; c8 < DQ / 8; ++c8) {
+                    const int c = part * DQ + c8 * 8;
                     uint4 pk;
                     pk.x = pack_bf16(srun[c8 * 8 + 0], srun[c8 * 8 + 1]);
                     pk.y = pack_bf16(srun[c8 * 8 + 2], srun[c8 * 8 + 3]);
@@ -380,10 +389,9 @@ __global__ void __launch_bounds__(HT_THREADS, 1) hybrid_tc_kernel(const __grid_c
             }
         }
         uint32_t ph_q = 0, ph_u = 0, ph_s = 0, ph_a = 0, ph_o = 0, ph_ds = 0, ph_stg = 0;
-        // per-row values the two warps of a lane quarter exchange go through
-        // TMEM columns TM_X.. of the row's lane: NP-Map statistics of half h at
-        // [TM_X + 4h, +3), its row maximum at TM_X + 8 + h, its share of the
-        // denominator at TM_X + 10 + h
+        // per-row values the four parts exchange go through TMEM columns of the
+        // row's lane: NP-Map statistics of part p at [TM_X + 4p, +3), its row
+        // maximum at TM_X2 + p, its share of the denominator at TM_X2 + 4 + p
         auto sync_rows = [&](bool bad) { return named_sync_or(1, HT_ROWS, bad || *(volatile int *)&s_abort); };
 
         for (int it = 0; it < ntiles; ++it) {
@@ -402,42 +410,45 @@ __global__ void __launch_bounds__(HT_THREADS, 1) hybrid_tc_kernel(const __grid_c
 
             if (tid < NX) xpos[tid] = (ct < dm.T_max && tid < lam) ? fs[ct * lam + tid] : INT_MAX;
 
-            // ---------------- ||q||^2 of my half of the row ----------------------------------
+            // ---------------- ||q||^2 of my quarter of the row -------------------------------
             bool bad = !wait(&bar_q, ph_q);
             ph_q ^= 1;
-            float qn2 = 0.f;
+            float qa[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int c8 = 0; c8 < DH / 8; ++c8) {
-                const int c = half * DH + c8 * 8;
+            for (int c8 = 0; c8 < DQ / 8; ++c8) {
+                const int c = part * DQ + c8 * 8;
                 const uint4 pk = *reinterpret_cast<const uint4 *>(sm + Lay::Q + (c / 64) * 16384 + sw128(r, (c % 64) / 8));
                 const uint32_t w4[4] = {pk.x, pk.y, pk.z, pk.w};
 #pragma unroll
                 for (int h2 = 0; h2 < 4; ++h2) {
                     const float a0 = __uint_as_float(w4[h2] << 16), a1 = __uint_as_float(w4[h2] & 0xffff0000u);
-                    qn2 = fmaf(a0, a0, fmaf(a1, a1, qn2));
+                    qa[h2] = fmaf(a0, a0, fmaf(a1, a1, qa[h2]));
                 }
             }
+            const float qn2 = (qa[0] + qa[1]) + (qa[2] + qa[3]);
 
             // ---------------- phi(Q), pass 1: exponentials of my features (kept) ----------
             bad |= !wait(&bar_u, ph_u);
             ph_u ^= 1;
             tc_fence_after();
-            float eu[DFH];
-            float mu = -INFINITY, s2 = 0.f;
+            float eu[FQ];
 #pragma unroll
-            for (int c0 = 0; c0 < DFH; c0 += 16)
-                tmem_ld16(tlane + TM_O + half * DFH + c0, *reinterpret_cast<float(*)[16]>(eu + c0));
+            for (int c0 = 0; c0 < FQ; c0 += 16)
+                tmem_ld16(tlane + TM_O + part * FQ + c0, *reinterpret_cast<float(*)[16]>(eu + c0));
             tmem_ld_wait();
+            float mx = eu[0];
 #pragma unroll
-            for (int i = 0; i < DFH; ++i) mu = fmaxf(mu, eu[i] * LOG2E);
+            for (int i = 1; i < FQ; ++i) mx = fmaxf(mx, eu[i]);
+            const float mu = mx * LOG2E;   // = max(u log2 e): scaling by a positive constant is monotone
+            float s2 = 0.f;
 #pragma unroll
-            for (int i = 0; i < DFH; ++i) {
+            for (int i = 0; i < FQ; ++i) {
                 eu[i] = exp2_mufu(fmaf(eu[i], LOG2E, -mu));
                 s2 = fmaf(eu[i], eu[i], s2);
             }
             {
                 const float v[4] = {mu, s2, qn2, 0.f};
-                tmem_st4(tlane + TM_X + 4 * half, v);
+                tmem_st4(tlane + TM_X + 4 * part, v);
                 tmem_st_wait();
             }
             tc_fence_before();
@@ -455,229 +466,222 @@ __global__ void __launch_bounds__(HT_THREADS, 1) hybrid_tc_kernel(const __grid_c
                 while (nvx < NX && xpos[nvx] <= t - W) ++nvx;
                 if (!row_ok) nvx = 0;
             }
-            float xo[4];
-            tmem_ld4(tlane + TM_X + 4 * (1 - half), xo);
+            float xs[16];
+            tmem_ld16(tlane + TM_X, xs);
             tmem_ld_wait();
 
-            // ---------------- phi(Q), pass 2: write my half of phi, phi . z ---------------
+            // ---------------- phi(Q), pass 2: write my quarter of phi, phi . z --------------
             bad = !wait(&stg_free, ph_stg);    // the previous output has left the staging buffer
             ph_stg ^= 1;
-            float den = 0.f;
+            float den = 0.f;   // my share of the denominator: phi . z here, then my A and P sums
             {
-                // (half 0's values, half 1's values) in the same order on both halves
-                const float m0 = half ? xo[0] : mu, m1 = half ? mu : xo[0];
-                const float a0 = half ? xo[1] : s2, a1 = half ? s2 : xo[1];
-                const float q0 = half ? xo[2] : qn2, q1 = half ? qn2 : xo[2];
-                const float M = fmaxf(m0, m1);
-                const float ss = a0 * exp2f(2.f * (m0 - M)) + a1 * exp2f(2.f * (m1 - M));
-                const float qn = sqrtf(q0 + q1);
-                const float sc = qn * rsqrtf(ss) * exp2f(mu - M);   // my half's exponentials were taken against mu
+                // the four parts' statistics, combined in part order on every part
+                float M = xs[0];
+#pragma unroll
+                for (int q4 = 1; q4 < HT_PARTS; ++q4) M = fmaxf(M, xs[4 * q4]);
+                float ss = 0.f, qq = 0.f;
+#pragma unroll
+                for (int q4 = 0; q4 < HT_PARTS; ++q4) {
+                    ss += xs[4 * q4 + 1] * exp2f(2.f * (xs[4 * q4] - M));
+                    qq += xs[4 * q4 + 2];
+                }
+                const float sc = sqrtf(qq) * rsqrtf(ss) * exp2f(mu - M);   // my exponentials were taken against mu
                 float2 dz2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
-                for (int c0 = 0; c0 < DFH; c0 += 16) {
+                for (int c8 = 0; c8 < FQ / 8; ++c8) {
+                    uint32_t w4[4];
 #pragma unroll
-                    for (int c8 = 0; c8 < 2; ++c8) {
-                        uint32_t w4[4];
-#pragma unroll
-                        for (int h2 = 0; h2 < 4; ++h2) {
-                            const int i = c8 * 8 + h2 * 2;
-                            const float p0 = sc * eu[c0 + i];
-                            const float p1 = sc * eu[c0 + i + 1];
-                            w4[h2] = pack_bf16(p0, p1);
-                            const int f = half * DFH + c0 + i;
-                            const float2 zz = *reinterpret_cast<const float2 *>(zrun + f);
-                            dz2[h2 & 1] = __ffma2_rn(make_float2(__uint_as_float(w4[h2] << 16),
-                                                                 __uint_as_float(w4[h2] & 0xffff0000u)),
-                                                     zz, dz2[h2 & 1]);
-                        }
-                        const int f0 = half * DFH + c0 + c8 * 8;
-                        *reinterpret_cast<uint4 *>(sm + Lay::PHIQ + (f0 / 64) * 16384 + sw128(r, (f0 % 64) / 8)) =
-                            make_uint4(w4[0], w4[1], w4[2], w4[3]);
+                    for (int h2 = 0; h2 < 4; ++h2) {
+                        const int i = c8 * 8 + h2 * 2;
+                        w4[h2] = pack_bf16(sc * eu[i], sc * eu[i + 1]);
+                        const int f = part * FQ + i;
+                        const float2 zz = *reinterpret_cast<const float2 *>(zrun + f);
+                        dz2[h2 & 1] = __ffma2_rn(make_float2(__uint_as_float(w4[h2] << 16),
+                                                             __uint_as_float(w4[h2] & 0xffff0000u)),
+                                                 zz, dz2[h2 & 1]);
                     }
+                    const int f0 = part * FQ + c8 * 8;
+                    *reinterpret_cast<uint4 *>(sm + Lay::PHIQ + (f0 / 64) * 16384 + sw128(r, (f0 % 64) / 8)) =
+                        make_uint4(w4[0], w4[1], w4[2], w4[3]);
                 }
                 den = (dz2[0].x + dz2[0].y) + (dz2[1].x + dz2[1].y);
             }
             fence_async_smem();
             mbar_arrive(&rdy_phiq);
 
-            // ---------------- softmax pass 1: exact row maximum (blocks kb = half mod 2) ---
+            // ---------------- softmax pass 1: exact row maximum over my blocks ---------------
             bad |= !wait(&bar_s, ph_s);
             ph_s ^= 1;
             tc_fence_after();
-            // every 32-key block is split between the two halves: keys [16 half, 16 half + 16)
-            // of block kb are columns TM_S + 32 kb + 16 half ..; masks are row ranges, so a
-            // 16-key group is often fully in or fully out for the whole warp
+            // key columns of block kb this row may use: [clo, chi] (0..31); masks are row
+            // ranges, so a 16-key half is often fully in or fully out for the whole warp
             auto key_range = [&](int kb, int &clo, int &chi) {
-                clo = (kb < P.nb ? blo - 32 * kb : 0) - 16 * half;
-                chi = (kb < P.nb ? bhi - 32 * kb : nvk - 1 - 32 * (kb - P.nb)) - 16 * half;
+                clo = kb < P.nb ? blo - 32 * kb : 0;
+                chi = kb < P.nb ? bhi - 32 * kb : nvk - 1 - 32 * (kb - P.nb);
             };
-            // the logits pass one block at a time through registers, software-pipelined:
-            // the next block's TMEM load is in flight while this one is worked on
-            struct Blk {
-                int clo, chi;
-                bool skip, full;
-            };
-            auto blk_load = [&](int kb, Blk &bi, float (&sv)[16]) {
-                key_range(kb, bi.clo, bi.chi);
-                bi.skip = __all_sync(0xffffffffu, bi.chi < 0 || bi.clo > 15);
-                bi.full = __all_sync(0xffffffffu, bi.clo <= 0 && bi.chi >= 15);
-                if (!bi.skip) tmem_ld16(tlane + TM_S + 32 * kb + 16 * half, sv);
-            };
-            float sva[16], svb[16];
-            Blk ba, bb;
             float cmax = -INFINITY;
-            auto cmax_blk = [&](const Blk &bi, const float (&sv)[16]) {
-                if (bi.skip) return;
-                if (bi.full) {
+            for (int kb = part; kb < nkb; kb += HT_PARTS) {
+                int clo, chi;
+                key_range(kb, clo, chi);
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) cmax = fmaxf(cmax, sv[i]);
-                } else {
+                for (int h = 0; h < 2; ++h) {
+                    const int lo = clo - 16 * h, hi = chi - 16 * h;   // this half's keys: [lo, hi] of 0..15
+                    if (__all_sync(0xffffffffu, hi < 0 || lo > 15)) continue;
+                    float sv[16];
+                    tmem_ld16(tlane + TM_S + 32 * kb + 16 * h, sv);
+                    tmem_ld_wait();
+                    if (__all_sync(0xffffffffu, lo <= 0 && hi >= 15)) {
+                        float m4[4];
 #pragma unroll
-                    for (int i = 0; i < 16; ++i)
-                        if (i >= bi.clo && i <= bi.chi) cmax = fmaxf(cmax, sv[i]);
+                        for (int j = 0; j < 4; ++j) m4[j] = fmaxf(fmaxf(sv[j], sv[j + 4]), fmaxf(sv[j + 8], sv[j + 12]));
+                        cmax = fmaxf(cmax, fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])));
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i)
+                            if (i >= lo && i <= hi) cmax = fmaxf(cmax, sv[i]);
+                    }
                 }
-            };
-            blk_load(0, ba, sva);
-            for (int kb = 0; kb < nkb;) {
-                tmem_ld_wait();
-                if (kb + 1 < nkb) blk_load(kb + 1, bb, svb);
-                cmax_blk(ba, sva);
-                if (++kb >= nkb) break;
-                tmem_ld_wait();
-                if (kb + 1 < nkb) blk_load(kb + 1, ba, sva);
-                cmax_blk(bb, svb);
-                ++kb;
             }
-            tmem_st1(tlane + TM_X + 8 + half, cmax);
+            tmem_st1(tlane + TM_X2 + part, cmax);
             tmem_st_wait();
             tc_fence_before();
             if (sync_rows(bad)) break;
             tc_fence_after();
-            cmax = fmaxf(cmax, tmem_ld1(tlane + TM_X + 8 + (1 - half)));   // the row maximum (both halves agree)
-            tmem_ld_wait();
+            {
+                float c4[4];
+                tmem_ld4(tlane + TM_X2, c4);
+                tmem_ld_wait();
+                cmax = fmaxf(fmaxf(c4[0], c4[1]), fmaxf(c4[2], c4[3]));   // the row maximum (all parts agree)
+            }
             const float cm = cmax == -INFINITY ? 0.f : cmax * l2s;   // no softmax key: every P is 0
 
             // ---------------- A: mask, row sum, bf16 pairs back into TMEM ------------------
             bad = !wait(&bar_a, ph_a);
             ph_a ^= 1;
             tc_fence_after();
-            if (half == 0) {
+            if (part == 0) {
                 float a[32];
                 tmem_ld32(tlane + TM_A, a);
                 tmem_ld_wait();
                 uint32_t w[16];
+                float d4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                 for (int i = 0; i < 32; i += 2) {
                     const float x0 = (i >= llo && i <= lhi) ? a[i] : 0.f;
                     const float x1 = (i + 1 >= llo && i + 1 <= lhi) ? a[i + 1] : 0.f;
-                    den += x0 + x1;
+                    d4[(i / 2) & 3] += x0 + x1;
                     w[i / 2] = pack_bf16(x0, x1);
                 }
+                den += (d4[0] + d4[1]) + (d4[2] + d4[3]);
                 tmem_st16(tlane + TM_A, w);
-            } else {
+                tmem_st_wait();
+            } else if (part == 1) {
                 float a[16];
                 tmem_ld16(tlane + TM_A + 32, a);
                 tmem_ld_wait();
                 uint32_t w[8];
+                float d4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                 for (int i = 0; i < 16; i += 2) {
                     const float x0 = i < nvx ? a[i] : 0.f;
                     const float x1 = i + 1 < nvx ? a[i + 1] : 0.f;
-                    den += x0 + x1;
+                    d4[(i / 2) & 3] += x0 + x1;
                     w[i / 2] = pack_bf16(x0, x1);
                 }
+                den += (d4[0] + d4[1]) + (d4[2] + d4[3]);
                 tmem_st8(tlane + TM_A + 32, w);
+                tmem_st_wait();
             }
-            tmem_st_wait();
             tc_fence_before();
             mbar_arrive(&rdy_a);
 
-            // ---------------- softmax pass 2: P (bf16 pairs) over the logits, in place ------
-            // keys [16 half, 16 half + 16) of block kb become 8 packed columns at the start of
-            // the 16 they came from
-            auto p_blk = [&](int kb, const Blk &bi, const float (&sv)[16]) {
-                uint32_t w[8];
-                if (bi.skip) {
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) w[i] = 0u;
-                } else if (bi.full) {
-#pragma unroll
-                    for (int i = 0; i < 16; i += 2) {
-                        const float p0 = exp2_mufu(fmaf(sv[i], l2s, -cm));
-                        const float p1 = exp2_mufu(fmaf(sv[i + 1], l2s, -cm));
-                        den += p0 + p1;
-                        w[i / 2] = pack_bf16(p0, p1);
-                    }
-                } else {
-#pragma unroll
-                    for (int i = 0; i < 16; i += 2) {
-                        const float p0 = (i >= bi.clo && i <= bi.chi) ? exp2_mufu(fmaf(sv[i], l2s, -cm)) : 0.f;
-                        const float p1 =
-                            (i + 1 >= bi.clo && i + 1 <= bi.chi) ? exp2_mufu(fmaf(sv[i + 1], l2s, -cm)) : 0.f;
-                        den += p0 + p1;
-                        w[i / 2] = pack_bf16(p0, p1);
-                    }
-                }
-                tmem_st8(tlane + TM_S + 32 * kb + 16 * half, w);
-            };
-            // blocks below the split go to the tensor cores while the rest are formed
+            // ---------------- softmax pass 2: P (bf16 pairs) over my blocks, in place -------
+            // keys [0, 16) and [16, 32) of block kb become 8 packed columns at the start of
+            // the 16 they came from; blocks below the split go to the tensor cores first
             const int split = nkb / 2;
-            auto p_split = [&](int kb_done) {
-                if (kb_done == split) {
-                    tmem_st_wait();
-                    tc_fence_before();
-                    mbar_arrive(&rdy_p1);
-                }
+            bool p1_sent = false;
+            auto send_p1 = [&]() {
+                tmem_st_wait();
+                tc_fence_before();
+                mbar_arrive(&rdy_p1);
+                p1_sent = true;
             };
-            p_split(0);
-            blk_load(0, ba, sva);
-            for (int kb = 0; kb < nkb;) {
-                tmem_ld_wait();
-                if (kb + 1 < nkb) blk_load(kb + 1, bb, svb);
-                p_blk(kb, ba, sva);
-                p_split(++kb);
-                if (kb >= nkb) break;
-                tmem_ld_wait();
-                if (kb + 1 < nkb) blk_load(kb + 1, ba, sva);
-                p_blk(kb, bb, svb);
-                p_split(++kb);
+            for (int kb = part; kb < nkb; kb += HT_PARTS) {
+                if (kb >= split && !p1_sent) send_p1();
+                int clo, chi;
+                key_range(kb, clo, chi);
+                float d4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int lo = clo - 16 * h, hi = chi - 16 * h;   // this half's keys: [lo, hi] of 0..15
+                    const bool skip = __all_sync(0xffffffffu, hi < 0 || lo > 15);
+                    const bool full = __all_sync(0xffffffffu, lo <= 0 && hi >= 15);
+                    uint32_t w[8];
+                    if (skip) {
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) w[i] = 0u;
+                    } else {
+                        float sv[16];
+                        tmem_ld16(tlane + TM_S + 32 * kb + 16 * h, sv);
+                        tmem_ld_wait();
+                        if (full) {
+#pragma unroll
+                            for (int i = 0; i < 16; i += 2) {
+                                const float p0 = exp2_mufu(fmaf(sv[i], l2s, -cm));
+                                const float p1 = exp2_mufu(fmaf(sv[i + 1], l2s, -cm));
+                                d4[(i / 2) & 3] += p0 + p1;
+                                w[i / 2] = pack_bf16(p0, p1);
+                            }
+                        } else {
+#pragma unroll
+                            for (int i = 0; i < 16; i += 2) {
+                                const float p0 = (i >= lo && i <= hi) ? exp2_mufu(fmaf(sv[i], l2s, -cm)) : 0.f;
+                                const float p1 = (i + 1 >= lo && i + 1 <= hi) ? exp2_mufu(fmaf(sv[i + 1], l2s, -cm)) : 0.f;
+                                d4[(i / 2) & 3] += p0 + p1;
+                                w[i / 2] = pack_bf16(p0, p1);
+                            }
+                        }
+                    }
+                    tmem_st8(tlane + TM_S + 32 * kb + 16 * h, w);
+                }
+                den += (d4[0] + d4[1]) + (d4[2] + d4[3]);
             }
-            // my share of the denominator goes with P: the partner reads it once the
+            if (!p1_sent) send_p1();
+            // my share of the denominator goes with P: the other parts read it once the
             // P V MMAs, which every row's P precedes, are complete
-            tmem_st1(tlane + TM_X + 10 + half, den);
+            tmem_st1(tlane + TM_X2 + 4 + part, den);
             tmem_st_wait();
             tc_fence_before();
             mbar_arrive(&rdy_p);
 
-            // ---------------- epilogue: y = O / den (my half of the columns) ---------------
+            // ---------------- epilogue: y = O / den (my quarter of the columns) --------------
             bad |= !wait(&bar_o, ph_o);
             ph_o ^= 1;
             tc_fence_after();
             {
-                float ov[DH];
-#pragma unroll
-                for (int c0 = 0; c0 < DH; c0 += 16)
-                    tmem_ld16(tlane + TM_O + half * DH + c0, *reinterpret_cast<float(*)[16]>(ov + c0));
-                const float dpart = tmem_ld1(tlane + TM_X + 10 + (1 - half));
+                float d4[4];
+                tmem_ld4(tlane + TM_X2 + 4, d4);
                 tmem_ld_wait();
-                const float dtot = den + dpart;
+                const float dtot = (d4[0] + d4[1]) + (d4[2] + d4[3]);
                 const float inv = dtot != 0.f ? 1.f / dtot : 0.f;
+                float ov[16];   // 16 columns at a time: two groups of 8
 #pragma unroll
-                for (int c0 = 0; c0 < DH; c0 += 16) {
-                    const float *o = ov + c0;
-#pragma unroll
-                    for (int c8 = 0; c8 < 2; ++c8) {
-                        uint4 pk;
-                        pk.x = pack_bf16(o[c8 * 8 + 0] * inv, o[c8 * 8 + 1] * inv);
-                        pk.y = pack_bf16(o[c8 * 8 + 2] * inv, o[c8 * 8 + 3] * inv);
-                        pk.z = pack_bf16(o[c8 * 8 + 4] * inv, o[c8 * 8 + 5] * inv);
-                        pk.w = pack_bf16(o[c8 * 8 + 6] * inv, o[c8 * 8 + 7] * inv);
-                        const int d0 = half * DH + c0 + c8 * 8;
-                        *reinterpret_cast<uint4 *>(sm + Lay::PHIQ + (d0 / 64) * 16384 + sw128(r, (d0 % 64) / 8)) = pk;
+                for (int c8 = 0; c8 < DQ / 8; ++c8) {
+                    if (c8 % 2 == 0) {
+                        tmem_ld16(tlane + TM_O + part * DQ + c8 * 8, ov);
+                        tmem_ld_wait();
                     }
+                    const float *o = ov + (c8 % 2) * 8;
+                    uint4 pk;
+                    pk.x = pack_bf16(o[0] * inv, o[1] * inv);
+                    pk.y = pack_bf16(o[2] * inv, o[3] * inv);
+                    pk.z = pack_bf16(o[4] * inv, o[5] * inv);
+                    pk.w = pack_bf16(o[6] * inv, o[7] * inv);
+                    const int d0 = part * DQ + c8 * 8;
+                    *reinterpret_cast<uint4 *>(sm + Lay::PHIQ + (d0 / 64) * 16384 + sw128(r, (d0 % 64) / 8)) = pk;
                 }
             }
-            // ---------------- state update: S_run += dS, z_run += sum phi(K_lag) ------------
+            // ---------------- state update: S_run += dS, z_run += dz --------------------------
             bad |= !wait(&bar_ds, ph_ds);
             ph_ds ^= 1;
             tc_fence_after();
@@ -685,19 +689,19 @@ __global__ void __launch_bounds__(HT_THREADS, 1) hybrid_tc_kernel(const __grid_c
                 const int f = r;
                 float dzf;
                 {
-                    float ds[DH];
+                    float ds[DQ];
 #pragma unroll
-                    for (int c0 = 0; c0 < DH; c0 += 16)
-                        tmem_ld16(tlane + TM_S + half * DH + c0, *reinterpret_cast<float(*)[16]>(ds + c0));
+                    for (int c0 = 0; c0 < DQ; c0 += 16)
+                        tmem_ld16(tlane + TM_S + part * DQ + c0, *reinterpret_cast<float(*)[16]>(ds + c0));
                     dzf = tmem_ld1(tlane + TM_DZ);
                     tmem_ld_wait();
 #pragma unroll
-                    for (int i = 0; i < DH; ++i) srun[i] += ds[i];
+                    for (int i = 0; i < DQ; ++i) srun[i] += ds[i];
                 }
                 if (f < DF) {
 #pragma unroll
-                    for (int c8 = 0; c8 < DH / 8; ++c8) {
-                        const int c = half * DH + c8 * 8;
+                    for (int c8 = 0; c8 < DQ / 8; ++c8) {
+                        const int c = part * DQ + c8 * 8;
                         uint4 pk;
                         pk.x = pack_bf16(srun[c8 * 8 + 0], srun[c8 * 8 + 1]);
                         pk.y = pack_bf16(srun[c8 * 8 + 2], srun[c8 * 8 + 3]);
@@ -705,7 +709,7 @@ __global__ void __launch_bounds__(HT_THREADS, 1) hybrid_tc_kernel(const __grid_c
                         pk.w = pack_bf16(srun[c8 * 8 + 6], srun[c8 * 8 + 7]);
                         *reinterpret_cast<uint4 *>(sm + Lay::SRUN + (c / 64) * (DF * 128) + sw128(f, (c % 64) / 8)) = pk;
                     }
-                    if (half == 0) zrun[f] += dzf;
+                    if (part == 0) zrun[f] += dzf;
                 }
             }
             fence_async_smem();
@@ -792,6 +796,13 @@ cudaError_t launch_hybrid_tc(const Dims &dm, const SegPlan &sp, const TCBuffers 
     dim3 grid(sp.nseg, dm.Hkv, dm.B);
     const size_t smem = hybrid_tc_smem(dm);
     cudaError_t e;
+    // the warpgroups' register split draws on what the block is launched with
+    auto regs_ok = [](const void *kern) {
+        cudaFuncAttributes fa;
+        return cudaFuncGetAttributes(&fa, kern) == cudaSuccess && fa.numRegs >= HT_LAUNCH_REGS;
+    };
+    if (!regs_ok(D == 64 ? (const void *)hybrid_tc_kernel<64, 64> : (const void *)hybrid_tc_kernel<128, 128>))
+        return cudaErrorInvalidConfiguration;
     if (D == 64) {
         e = cudaFuncSetAttribute(hybrid_tc_kernel<64, 64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
