@@ -110,10 +110,11 @@ SegPlan plan_segments(const Dims &dm)
         return sp;
     }
     // work of a tile: a fixed part (NP-Map, epilogues, state update) worth about
-    // 512 keys, plus the softmax keys it attends (window and kept tokens)
+    // 600 keys (fitted to measured segment times), plus the softmax keys it
+    // attends (window and kept tokens)
     auto cost = [&](int tile) {
         const int ct = tile * sp.T / dm.C;
-        return 512.0 + dm.W + (double)(ct < dm.T_max ? ct : dm.T_max) * dm.lam;
+        return 600.0 + dm.W + (double)(ct < dm.T_max ? ct : dm.T_max) * dm.lam;
     };
     double total = 0.0;
     for (int i = 0; i < ntile; ++i) total += cost(i);
