@@ -288,9 +288,16 @@ still_status still_prefill(const still_shape *shape, const still_bf16 *q, const 
     float *dS = (float *)(base + L.dS);
     float *dz = (float *)(base + L.dz);
     const bool tc = hybrid_tc_supported(dm);
-    cudaError_t e = launch_prep(dm, Wf, wft, status, kslot, kk, L.kept_bytes, s);
-    if (e == cudaSuccess && dm.lam > 0)
-        e = score_tc_supported(dm) ? launch_score_tc(dm, q, k, scores, s) : launch_score(dm, q, k, scores, s);
+    // the set-up pass rides on the tensor-core score kernel when that one runs
+    const bool fused_prep = dm.lam > 0 && score_tc_supported(dm);
+    cudaError_t e = cudaSuccess;
+    if (fused_prep) {
+        const PrepArgs pa{Wf, wft, status, kslot, kk, L.kept_bytes};
+        e = launch_score_tc(dm, q, k, scores, s, &pa);
+    } else {
+        e = launch_prep(dm, Wf, wft, status, kslot, kk, L.kept_bytes, s);
+        if (e == cudaSuccess && dm.lam > 0) e = launch_score(dm, q, k, scores, s);
+    }
     if (e == cudaSuccess && dm.lam > 0) e = launch_select(dm, scores, sel_idx, fsel, kslot, s, k, v, kk, vk);
     if (e == cudaSuccess) e = launch_linstate_tc(dm, sp, k, v, wft, kslot, phik, phk, dS, dz, status, s);
     if (e == cudaSuccess) e = launch_scan(dm, sp, dS, dz, s);

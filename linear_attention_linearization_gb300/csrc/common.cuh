@@ -179,7 +179,16 @@ struct KTimer {
 // ---- launchers (one per kernel family) ----------------------------------------
 cudaError_t launch_score(const Dims &dm, const uint16_t *q, const uint16_t *k, float *scores, cudaStream_t s);
 bool score_tc_supported(const Dims &dm);
-cudaError_t launch_score_tc(const Dims &dm, const uint16_t *q, const uint16_t *k, float *scores, cudaStream_t s);
+// The prefill's set-up pass (see prep_kernel), folded into the score kernel.
+struct PrepArgs {
+    const float *Wf;
+    uint16_t *wft;
+    int32_t *status, *kslot;
+    void *kept;
+    size_t kept_bytes;
+};
+cudaError_t launch_score_tc(const Dims &dm, const uint16_t *q, const uint16_t *k, float *scores, cudaStream_t s,
+                            const PrepArgs *prep = nullptr);
 cudaError_t launch_select(const Dims &dm, const float *scores, int32_t *sel_idx, int32_t *fsel, int32_t *kslot,
                           cudaStream_t s, const uint16_t *k = nullptr, const uint16_t *v = nullptr,
                           uint16_t *kk = nullptr, uint16_t *vk = nullptr);

@@ -35,6 +35,13 @@ struct ScoreTCParams {
     int stages;        // tiles in flight (shared-memory and TMEM stages)
     uint32_t stage_bytes, tmem_stride;
     float *scores;
+    // the prefill's set-up, done by this kernel's threads when kslot is set:
+    // status word = 0, slot map = -1, kept tables = 0, W_f^T in bf16
+    const float *Wf;
+    uint16_t *wft;
+    int32_t *status, *kslot;
+    size_t nkslot, nkept16;
+    uint4 *kept;
 };
 
 // q: boxes of 32 tokens x 64 columns x G heads; k: the nb band blocks in one box
@@ -91,6 +98,17 @@ __global__ void __launch_bounds__(SC_THREADS, 1) score_tc_kernel(const __grid_co
     tc_fence_after();
     const uint32_t tmem = tmem_base;
     grid_dep_sync();   // the previous kernel's writes are visible from here on
+    if (P.kslot) {
+        const size_t gt = (size_t)blockIdx.x * SC_THREADS + tid, nt = (size_t)gridDim.x * SC_THREADS;
+        if (gt == 0) *P.status = 0;
+        for (size_t i = gt; i < P.nkslot / 4; i += nt) reinterpret_cast<int4 *>(P.kslot)[i] = make_int4(-1, -1, -1, -1);
+        for (size_t i = P.nkslot / 4 * 4 + gt; i < P.nkslot; i += nt) P.kslot[i] = -1;
+        for (size_t i = gt; i < P.nkept16; i += nt) P.kept[i] = make_uint4(0, 0, 0, 0);
+        for (size_t i = gt; i < (size_t)dm.d * dm.df; i += nt) {
+            const int f = (int)(i / dm.d), e = (int)(i % dm.d);
+            P.wft[i] = f2bf(P.Wf[(size_t)e * dm.df + f]);
+        }
+    }
 
     auto wait = [&](uint64_t *bar, uint32_t parity) -> bool {
         if (mbar_try_wait(bar, parity)) return true;
@@ -244,7 +262,8 @@ bool score_tc_supported(const Dims &dm)
     return (Wr + 32) / 32 <= SC_MAX_NB;
 }
 
-cudaError_t launch_score_tc(const Dims &dm, const uint16_t *q, const uint16_t *k, float *scores, cudaStream_t s)
+cudaError_t launch_score_tc(const Dims &dm, const uint16_t *q, const uint16_t *k, float *scores, cudaStream_t s,
+                            const PrepArgs *prep)
 {
     KTimer tm("score", s);
     ScoreTCMaps m;
@@ -263,6 +282,13 @@ cudaError_t launch_score_tc(const Dims &dm, const uint16_t *q, const uint16_t *k
     p.tiles_per_unit = (dm.N + 31) / 32;
     p.total_tiles = p.tiles_per_unit * dm.B * dm.Hkv;
     p.scores = scores;
+    p.Wf = prep ? prep->Wf : nullptr;
+    p.wft = prep ? prep->wft : nullptr;
+    p.status = prep ? prep->status : nullptr;
+    p.kslot = prep ? prep->kslot : nullptr;
+    p.nkslot = prep ? (size_t)dm.B * dm.Hkv * dm.N : 0;
+    p.kept = prep ? reinterpret_cast<uint4 *>(prep->kept) : nullptr;
+    p.nkept16 = prep ? prep->kept_bytes / 16 : 0;
     const uint32_t qb = (uint32_t)(D / 64) * 16384, kbytes = (uint32_t)p.nb * 32 * D * 2;
     p.stage_bytes = (qb + kbytes + 1023) & ~1023u;
     p.tmem_stride = p.nb * 32 <= 128 ? 128 : 256;
