@@ -90,7 +90,8 @@ __global__ void __launch_bounds__(32) select_kernel(const float *__restrict__ sc
     grid_dep_sync();
     extern __shared__ float sel_smem[];
     float *sc = sel_smem;
-    uint8_t *taken = reinterpret_cast<uint8_t *>(sc + dm.C);
+    int *kidx = reinterpret_cast<int *>(sc + dm.C);            // chunk offsets of the kept tokens, in order
+    uint8_t *taken = reinterpret_cast<uint8_t *>(kidx + dm.lam);
     const int c = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
     const int lane = threadIdx.x;
     const size_t row = ((size_t)(b * dm.Hkv + g) * dm.T_max + c) * dm.lam;
@@ -140,6 +141,7 @@ __global__ void __launch_bounds__(32) select_kernel(const float *__restrict__ sc
         const unsigned mask = __ballot_sync(0xffffffffu, f);
         if (f) {
             const int p = outn + __popc(mask & ((1u << lane) - 1u));
+            kidx[p] = i;
             if (fsel) fsel[row + p] = base + i;
             if (sel_idx) sel_idx[row + p] = complete ? base + i : -1;
             if (kslot) kslot[(size_t)(b * dm.Hkv + g) * dm.N + base + i] = c * dm.lam + p;
@@ -152,20 +154,33 @@ __global__ void __launch_bounds__(32) select_kernel(const float *__restrict__ sc
     }
     if (!complete && sel_idx)
         for (int r = lane; r < outn; r += 32) sel_idx[row + r] = -1;
-    // K and V rows of the kept tokens into the kept tables (row c*lambda + r)
+    // K and V rows of the kept tokens into the kept tables (row c*lambda + r):
+    // (token, 16-byte word) pairs spread over the lanes, every load issued
+    // before the stores
     if (kk) {
         __syncwarp();
         const size_t ug = (size_t)b * dm.Hkv + g;
-        const int words = dm.d / 4;   // 8-byte words per row
-        for (int p = 0; p < outn; ++p) {
-            const int j = fsel[row + p];
-            const uint2 *ks = reinterpret_cast<const uint2 *>(k + (ug * dm.N + j) * dm.d);
-            const uint2 *vs = reinterpret_cast<const uint2 *>(v + (ug * dm.N + j) * dm.d);
-            uint2 *kd = reinterpret_cast<uint2 *>(kk + (row + p) * dm.d);
-            uint2 *vd = reinterpret_cast<uint2 *>(vk + (row + p) * dm.d);
-            for (int x = lane; x < words; x += 32) {
-                kd[x] = ks[x];
-                vd[x] = vs[x];
+        const int words = dm.d / 8;   // 16-byte words per row
+        const int total = outn * words;
+        for (int e0 = 0; e0 < total; e0 += 128) {
+            uint4 kv[4][2];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int e = e0 + u * 32 + lane;
+                if (e < total) {
+                    const size_t j = (size_t)(base + kidx[e / words]);
+                    kv[u][0] = reinterpret_cast<const uint4 *>(k + (ug * dm.N + j) * dm.d)[e % words];
+                    kv[u][1] = reinterpret_cast<const uint4 *>(v + (ug * dm.N + j) * dm.d)[e % words];
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int e = e0 + u * 32 + lane;
+                if (e < total) {
+                    const size_t dst = (row + (size_t)(e / words)) * dm.d;
+                    reinterpret_cast<uint4 *>(kk + dst)[e % words] = kv[u][0];
+                    reinterpret_cast<uint4 *>(vk + dst)[e % words] = kv[u][1];
+                }
             }
         }
     }
@@ -176,7 +191,7 @@ cudaError_t launch_select(const Dims &dm, const float *scores, int32_t *sel_idx,
 {
     if (dm.lam <= 0) return cudaSuccess;
     KTimer tm("select", s);
-    const size_t smem = (size_t)dm.C * (sizeof(float) + 1);
+    const size_t smem = (size_t)dm.C * (sizeof(float) + 1) + sizeof(int) * dm.lam;
     if (smem > 48 * 1024) {
         cudaError_t e = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
