@@ -523,24 +523,21 @@ __global__ void __launch_bounds__(HT_THREADS, 1) hybrid_tc_kernel(const __grid_c
             for (int kb = part; kb < nkb; kb += HT_PARTS) {
                 int clo, chi;
                 key_range(kb, clo, chi);
+                if (__all_sync(0xffffffffu, chi < 0 || clo > 31)) continue;
+                float sv[32];   // the block's 32 logits in one TMEM round trip
+                tmem_ld16(tlane + TM_S + 32 * kb, *reinterpret_cast<float(*)[16]>(sv));
+                tmem_ld16(tlane + TM_S + 32 * kb + 16, *reinterpret_cast<float(*)[16]>(sv + 16));
+                tmem_ld_wait();
+                float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+                if (__all_sync(0xffffffffu, clo <= 0 && chi >= 31)) {
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const int lo = clo - 16 * h, hi = chi - 16 * h;   // this half's keys: [lo, hi] of 0..15
-                    if (__all_sync(0xffffffffu, hi < 0 || lo > 15)) continue;
-                    float sv[16];
-                    tmem_ld16(tlane + TM_S + 32 * kb + 16 * h, sv);
-                    tmem_ld_wait();
-                    if (__all_sync(0xffffffffu, lo <= 0 && hi >= 15)) {
-                        float m4[4];
+                    for (int i = 0; i < 32; ++i) m4[i & 3] = fmaxf(m4[i & 3], sv[i]);
+                } else {
 #pragma unroll
-                        for (int j = 0; j < 4; ++j) m4[j] = fmaxf(fmaxf(sv[j], sv[j + 4]), fmaxf(sv[j + 8], sv[j + 12]));
-                        cmax = fmaxf(cmax, fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])));
-                    } else {
-#pragma unroll
-                        for (int i = 0; i < 16; ++i)
-                            if (i >= lo && i <= hi) cmax = fmaxf(cmax, sv[i]);
-                    }
+                    for (int i = 0; i < 32; ++i)
+                        if (i >= clo && i <= chi) m4[i & 3] = fmaxf(m4[i & 3], sv[i]);
                 }
+                cmax = fmaxf(cmax, fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])));
             }
             tmem_st1(tlane + TM_X2 + part, cmax);
             tmem_st_wait();
@@ -659,19 +656,17 @@ __global__ void __launch_bounds__(HT_THREADS, 1) hybrid_tc_kernel(const __grid_c
             ph_o ^= 1;
             tc_fence_after();
             {
-                float d4[4];
+                float d4[4], ov[DQ];   // the denominator shares and my output columns in one round trip
                 tmem_ld4(tlane + TM_X2 + 4, d4);
+#pragma unroll
+                for (int c0 = 0; c0 < DQ; c0 += 16)
+                    tmem_ld16(tlane + TM_O + part * DQ + c0, *reinterpret_cast<float(*)[16]>(ov + c0));
                 tmem_ld_wait();
                 const float dtot = (d4[0] + d4[1]) + (d4[2] + d4[3]);
                 const float inv = dtot != 0.f ? 1.f / dtot : 0.f;
-                float ov[16];   // 16 columns at a time: two groups of 8
 #pragma unroll
                 for (int c8 = 0; c8 < DQ / 8; ++c8) {
-                    if (c8 % 2 == 0) {
-                        tmem_ld16(tlane + TM_O + part * DQ + c8 * 8, ov);
-                        tmem_ld_wait();
-                    }
-                    const float *o = ov + (c8 % 2) * 8;
+                    const float *o = ov + c8 * 8;
                     uint4 pk;
                     pk.x = pack_bf16(o[0] * inv, o[1] * inv);
                     pk.y = pack_bf16(o[2] * inv, o[3] * inv);
