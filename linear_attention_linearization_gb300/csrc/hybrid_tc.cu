@@ -350,9 +350,11 @@ __global__ void __launch_bounds__(HT_THREADS, 1) hybrid_tc_kernel(const __grid_c
     } else {
         // ============================ the row warps =============================
         // Four warps per TMEM lane quarter.  Part p of a row owns the columns
-        // [p DQ, (p + 1) DQ) of U, O and dS, the 32-key logit blocks kb = p mod 4
-        // (so a block's P is packed over the columns its own thread read), and
-        // one piece of A (part 0 the lag keys, part 1 the own-chunk extras).
+        // [p DQ, (p + 1) DQ) of U, O and dS, the 16-key halves u = p mod 4 of the
+        // logit blocks (half u = 2 kb + h: a half's P is packed over the first 8
+        // of the 16 columns its own thread read), and, on the parts with the
+        // fewest halves, one piece of A (part 3 the lag keys, part 2 the
+        // own-chunk extras).
         regs_inc<HT_ROW_REGS>();
         constexpr int DQ = D / HT_PARTS, FQ = DF / HT_PARTS;
         const int quarter = warp & 3, part = warp >> 2;
@@ -509,7 +511,7 @@ __global__ void __launch_bounds__(HT_THREADS, 1) hybrid_tc_kernel(const __grid_c
             fence_async_smem();
             mbar_arrive(&rdy_phiq);
 
-            // ---------------- softmax pass 1: exact row maximum over my blocks ---------------
+            // ---------------- softmax pass 1: exact row maximum over my halves ---------------
             bad |= !wait(&bar_s, ph_s);
             ph_s ^= 1;
             tc_fence_after();
@@ -520,22 +522,23 @@ __global__ void __launch_bounds__(HT_THREADS, 1) hybrid_tc_kernel(const __grid_c
                 chi = kb < P.nb ? bhi - 32 * kb : nvk - 1 - 32 * (kb - P.nb);
             };
             float cmax = -INFINITY;
-            for (int kb = part; kb < nkb; kb += HT_PARTS) {
+            for (int u = part; u < 2 * nkb; u += HT_PARTS) {
+                const int kb = u >> 1, h = u & 1;
                 int clo, chi;
                 key_range(kb, clo, chi);
-                if (__all_sync(0xffffffffu, chi < 0 || clo > 31)) continue;
-                float sv[32];   // the block's 32 logits in one TMEM round trip
-                tmem_ld16(tlane + TM_S + 32 * kb, *reinterpret_cast<float(*)[16]>(sv));
-                tmem_ld16(tlane + TM_S + 32 * kb + 16, *reinterpret_cast<float(*)[16]>(sv + 16));
+                const int lo = clo - 16 * h, hi = chi - 16 * h;   // this half's keys: [lo, hi] of 0..15
+                if (__all_sync(0xffffffffu, hi < 0 || lo > 15)) continue;
+                float sv[16];
+                tmem_ld16(tlane + TM_S + 16 * u, sv);
                 tmem_ld_wait();
                 float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-                if (__all_sync(0xffffffffu, clo <= 0 && chi >= 31)) {
+                if (__all_sync(0xffffffffu, lo <= 0 && hi >= 15)) {
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) m4[i & 3] = fmaxf(m4[i & 3], sv[i]);
+                    for (int i = 0; i < 16; ++i) m4[i & 3] = fmaxf(m4[i & 3], sv[i]);
                 } else {
 #pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        if (i >= clo && i <= chi) m4[i & 3] = fmaxf(m4[i & 3], sv[i]);
+                    for (int i = 0; i < 16; ++i)
+                        if (i >= lo && i <= hi) m4[i & 3] = fmaxf(m4[i & 3], sv[i]);
                 }
                 cmax = fmaxf(cmax, fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])));
             }
@@ -556,7 +559,7 @@ __global__ void __launch_bounds__(HT_THREADS, 1) hybrid_tc_kernel(const __grid_c
             bad = !wait(&bar_a, ph_a);
             ph_a ^= 1;
             tc_fence_after();
-            if (part == 0) {
+            if (part == HT_PARTS - 1) {
                 float a[32];
                 tmem_ld32(tlane + TM_A, a);
                 tmem_ld_wait();
@@ -572,7 +575,7 @@ __global__ void __launch_bounds__(HT_THREADS, 1) hybrid_tc_kernel(const __grid_c
                 den += (d4[0] + d4[1]) + (d4[2] + d4[3]);
                 tmem_st16(tlane + TM_A, w);
                 tmem_st_wait();
-            } else if (part == 1) {
+            } else if (part == HT_PARTS - 2) {
                 float a[16];
                 tmem_ld16(tlane + TM_A + 32, a);
                 tmem_ld_wait();
@@ -592,9 +595,9 @@ __global__ void __launch_bounds__(HT_THREADS, 1) hybrid_tc_kernel(const __grid_c
             tc_fence_before();
             mbar_arrive(&rdy_a);
 
-            // ---------------- softmax pass 2: P (bf16 pairs) over my blocks, in place -------
-            // keys [0, 16) and [16, 32) of block kb become 8 packed columns at the start of
-            // the 16 they came from; blocks below the split go to the tensor cores first
+            // ---------------- softmax pass 2: P (bf16 pairs) over my halves, in place -------
+            // the 16 keys of half u become 8 packed columns at the start of the 16 they
+            // came from; blocks below the split go to the tensor cores first
             const int split = nkb / 2;
             bool p1_sent = false;
             auto send_p1 = [&]() {
@@ -603,44 +606,42 @@ __global__ void __launch_bounds__(HT_THREADS, 1) hybrid_tc_kernel(const __grid_c
                 mbar_arrive(&rdy_p1);
                 p1_sent = true;
             };
-            for (int kb = part; kb < nkb; kb += HT_PARTS) {
+            for (int u = part; u < 2 * nkb; u += HT_PARTS) {
+                const int kb = u >> 1, h = u & 1;
                 if (kb >= split && !p1_sent) send_p1();
                 int clo, chi;
                 key_range(kb, clo, chi);
+                const int lo = clo - 16 * h, hi = chi - 16 * h;   // this half's keys: [lo, hi] of 0..15
+                const bool skip = __all_sync(0xffffffffu, hi < 0 || lo > 15);
+                const bool full = __all_sync(0xffffffffu, lo <= 0 && hi >= 15);
+                uint32_t w[8];
                 float d4[4] = {0.f, 0.f, 0.f, 0.f};
+                if (skip) {
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const int lo = clo - 16 * h, hi = chi - 16 * h;   // this half's keys: [lo, hi] of 0..15
-                    const bool skip = __all_sync(0xffffffffu, hi < 0 || lo > 15);
-                    const bool full = __all_sync(0xffffffffu, lo <= 0 && hi >= 15);
-                    uint32_t w[8];
-                    if (skip) {
+                    for (int i = 0; i < 8; ++i) w[i] = 0u;
+                } else {
+                    float sv[16];
+                    tmem_ld16(tlane + TM_S + 16 * u, sv);
+                    tmem_ld_wait();
+                    if (full) {
 #pragma unroll
-                        for (int i = 0; i < 8; ++i) w[i] = 0u;
+                        for (int i = 0; i < 16; i += 2) {
+                            const float p0 = exp2_mufu(fmaf(sv[i], l2s, -cm));
+                            const float p1 = exp2_mufu(fmaf(sv[i + 1], l2s, -cm));
+                            d4[(i / 2) & 3] += p0 + p1;
+                            w[i / 2] = pack_bf16(p0, p1);
+                        }
                     } else {
-                        float sv[16];
-                        tmem_ld16(tlane + TM_S + 32 * kb + 16 * h, sv);
-                        tmem_ld_wait();
-                        if (full) {
 #pragma unroll
-                            for (int i = 0; i < 16; i += 2) {
-                                const float p0 = exp2_mufu(fmaf(sv[i], l2s, -cm));
-                                const float p1 = exp2_mufu(fmaf(sv[i + 1], l2s, -cm));
-                                d4[(i / 2) & 3] += p0 + p1;
-                                w[i / 2] = pack_bf16(p0, p1);
-                            }
-                        } else {
-#pragma unroll
-                            for (int i = 0; i < 16; i += 2) {
-                                const float p0 = (i >= lo && i <= hi) ? exp2_mufu(fmaf(sv[i], l2s, -cm)) : 0.f;
-                                const float p1 = (i + 1 >= lo && i + 1 <= hi) ? exp2_mufu(fmaf(sv[i + 1], l2s, -cm)) : 0.f;
-                                d4[(i / 2) & 3] += p0 + p1;
-                                w[i / 2] = pack_bf16(p0, p1);
-                            }
+                        for (int i = 0; i < 16; i += 2) {
+                            const float p0 = (i >= lo && i <= hi) ? exp2_mufu(fmaf(sv[i], l2s, -cm)) : 0.f;
+                            const float p1 = (i + 1 >= lo && i + 1 <= hi) ? exp2_mufu(fmaf(sv[i + 1], l2s, -cm)) : 0.f;
+                            d4[(i / 2) & 3] += p0 + p1;
+                            w[i / 2] = pack_bf16(p0, p1);
                         }
                     }
-                    tmem_st8(tlane + TM_S + 32 * kb + 16 * h, w);
                 }
+                tmem_st8(tlane + TM_S + 16 * u, w);
                 den += (d4[0] + d4[1]) + (d4[2] + d4[3]);
             }
             if (!p1_sent) send_p1();
