@@ -10,9 +10,10 @@
 // G <= 4 query heads x 32 tokens form the M = 128 rows of one MMA against the
 // band of keys [t0 - Wr, t0 + 32) that holds every window of the tile.  One
 // thread of a fourth warpgroup issues the TMA copies and the MMAs, tiles
-// pipelined over up to four shared-memory / TMEM stages; 8 row warps (two per
-// TMEM lane quarter, each owning half of the band columns) reduce each row to
-// (max, off-diagonal mass, self mass) while the next tiles load and multiply.
+// pipelined over up to four shared-memory / TMEM stages; two groups of four
+// row warps take alternate tiles, one thread per row, and reduce each row to its
+// off-diagonal window mass relative to the token's own logit while the next
+// tiles load and multiply.
 #include "sm100.cuh"
 #include "tma_host.cuh"
 
@@ -23,7 +24,8 @@ using namespace sm100;
 namespace {
 constexpr int SC_MAX_NB = 8;         // band blocks of 32 keys (W <= 225)
 constexpr int SC_MAX_STAGES = 4;     // tiles in flight
-constexpr int SC_ROWS = 256;         // row threads
+constexpr int SC_ROWS = 256;         // row threads: SC_GROUPS groups of four warps
+constexpr int SC_GROUPS = 2;
 constexpr int SC_THREADS = SC_ROWS + 128;
 constexpr size_t SC_SMEM_CAP = 227 * 1024 - 4096;   // dynamic share of the 227 KB per-block limit
 }
@@ -62,8 +64,7 @@ __global__ void __launch_bounds__(SC_THREADS, 1) score_tc_kernel(const __grid_co
     // shared memory is free); tfree: the rows have read its TMEM columns
     __shared__ uint64_t bar_full[SC_MAX_STAGES], bar_mma[SC_MAX_STAGES], bar_tfree[SC_MAX_STAGES];
     __shared__ uint32_t tmem_base;
-    __shared__ float xch[128][3];
-    __shared__ float hsc[4][32];
+    __shared__ float hsc[SC_GROUPS][2][4 * 32];   // per group, two tiles: head scores by (head, token)
     __shared__ int s_abort;
 
     const Dims &dm = P.dm;
@@ -81,7 +82,7 @@ __global__ void __launch_bounds__(SC_THREADS, 1) score_tc_kernel(const __grid_co
         for (int i = 0; i < NS; ++i) {
             mbar_init(&bar_full[i], 1);
             mbar_init(&bar_mma[i], 1);
-            mbar_init(&bar_tfree[i], SC_ROWS);
+            mbar_init(&bar_tfree[i], SC_ROWS / SC_GROUPS);
         }
         fence_barrier_init();
         s_abort = 0;
@@ -176,75 +177,66 @@ __global__ void __launch_bounds__(SC_THREADS, 1) score_tc_kernel(const __grid_co
         __syncwarp();
     } else {
         // ============================= the row warps =============================
+        // Two groups of four warps take alternate tiles; in a group, warp q
+        // serves TMEM lane quarter q (query head q of the tile) and each thread
+        // one whole row, so the only exchange is the head mean.
         regs_inc<224>();
-        const int quarter = warp & 3, half = warp >> 2;
-        const int r = quarter * 32 + lane, hh = r / 32, tt = r % 32;
-        constexpr int HC = NB * 16;   // band columns per half-row thread
+        const int quarter = warp & 3, grp = warp >> 2;
+        const int hh = quarter, tt = lane;
+        constexpr int BC = NB * 32;   // band columns
         const int W = dm.W;
         const float l2s = 1.4426950408889634f * rsqrtf((float)D);   // log2(e) / sqrt(d)
         const uint32_t tlane = tmem + ((uint32_t)(quarter * 32) << 16);
-        const int c_beg = half * HC;
-        uint32_t ph_mma = 0;
-        for (int i = 0; i < my_tiles; ++i) {
+        for (int i = grp, n = 0; i < my_tiles; i += SC_GROUPS, ++n) {
             const int st = i % NS;
             int unit, t0;
             tile_coords(i, unit, t0);
-            bool bad = !wait(&bar_mma[st], (ph_mma >> st) & 1u);
-            ph_mma ^= 1u << st;
+            // the k-th use of a stage completes phase k of its barrier; this group
+            // has seen tile i - 2 complete, so every earlier use of the stage has too
+            bool bad = !wait(&bar_mma[st], (uint32_t)(i / NS) & 1u);
             tc_fence_after();
-
-            // this thread's half of the band columns: all its TMEM loads, then one wait
-            float v[HC];
+            float v[BC];
 #pragma unroll
-            for (int c0 = 0; c0 < HC; c0 += 16)
-                tmem_ld16(tlane + st * P.tmem_stride + c_beg + c0, *reinterpret_cast<float(*)[16]>(v + c0));
+            for (int c0 = 0; c0 < BC; c0 += 32)
+                tmem_ld32(tlane + st * P.tmem_stride + c0, *reinterpret_cast<float(*)[32]>(v + c0));
             tmem_ld_wait();
             tc_fence_before();
             mbar_arrive(&bar_tfree[st]);
 
-            // row statistics: window columns [lo, hi], the token itself at self_c
+            // window columns [lo, self_c): the keys other than the token itself; the
+            // token's own logit is at self_c = Wr + tt, in the last band block.  The
+            // masses are taken relative to the token's own logit, so no row maximum
+            // is needed: a mass that overflows to +inf gives p = 0 exactly.
             const int t = t0 + tt;
             const int band_lo = t0 - P.Wr;
-            const int lo = max(max(t - W + 1, 0) - band_lo, 0), hi = t - band_lo;
-            const int self_c = t - band_lo;
-            float m = -INFINITY;
+            const int lo = max(max(t - W + 1, 0) - band_lo, 0);
+            const int self_c = P.Wr + tt;
+            float sself = 0.f;
 #pragma unroll
-            for (int x = 0; x < HC; ++x) {
-                const int c = c_beg + x;
-                v[x] = (c >= lo && c <= hi) ? v[x] * l2s : -INFINITY;
-                m = fmaxf(m, v[x]);
-            }
-            float oth = 0.f, slf = 0.f;
-            if (m != -INFINITY) {
+            for (int x = BC - 32; x < BC; ++x)
+                if (x == self_c) sself = v[x];
+            const float ms = sself * l2s;
+            float o4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                for (int x = 0; x < HC; ++x) {
-                    const float e = exp2_mufu(v[x] - m);
-                    if (c_beg + x == self_c) slf += e;
-                    else oth += e;
-                }
+            for (int x = 0; x < BC - 32; ++x) {   // before the last block: every column is below self_c
+                const float e = exp2_mufu(fmaf(v[x], l2s, -ms));
+                o4[x & 3] += x >= lo ? e : 0.f;
             }
-            if (half == 1) {
-                xch[r][0] = m;
-                xch[r][1] = oth;
-                xch[r][2] = slf;
+#pragma unroll
+            for (int x = BC - 32; x < BC; ++x) {
+                const float e = exp2_mufu(fmaf(v[x], l2s, -ms));
+                o4[x & 3] += (x >= lo && x < self_c) ? e : 0.f;
             }
-            if (named_sync_or(1, SC_ROWS, bad || *(volatile int *)&s_abort)) break;
-            if (half == 0) {
-                const float m1 = xch[r][0];
-                const float M = fmaxf(m, m1);
-                float o = 0.f, sl = 0.f;
-                if (M != -INFINITY) {
-                    const float f0 = m == -INFINITY ? 0.f : exp2f(m - M), f1 = m1 == -INFINITY ? 0.f : exp2f(m1 - M);
-                    o = oth * f0 + xch[r][1] * f1;
-                    sl = slf * f0 + xch[r][2] * f1;
-                }
-                hsc[hh][tt] = (hh < dm.G && t < dm.N) ? saliency_from_stats(o, sl) : 0.f;
-            }
-            named_sync_or(1, SC_ROWS, false);
-            if (tid < 32 && t0 + tid < dm.N) {
+            const float oth = (o4[0] + o4[1]) + (o4[2] + o4[3]);
+            float *hs = hsc[grp][n & 1];
+            hs[hh * 32 + tt] = (hh < dm.G && t < dm.N) ? saliency_from_stats(oth, 1.f) : 0.f;
+            // the group's four heads are in; the other half of hsc[grp] was read
+            // before this barrier by the warp that reads this half after it
+            if (named_sync_or(1 + grp, 128, bad || *(volatile int *)&s_abort)) break;
+            if (quarter == 0 && t < dm.N) {
                 float a = 0.f;
-                for (int h = 0; h < dm.G; ++h) a += hsc[h][tid];
-                P.scores[(size_t)unit * dm.N + t0 + tid] = a / dm.G;
+                for (int h = 0; h < dm.G; ++h) a += hs[h * 32 + tt];
+                P.scores[(size_t)unit * dm.N + t] = a / dm.G;
             }
         }
     }
