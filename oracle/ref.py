@@ -47,6 +47,8 @@ def lib():
             L.oref_npmap.argtypes = [_D, ct.c_long, ct.c_int, _D, ct.c_int, _D]
             L.oref_scores.restype = None
             L.oref_scores.argtypes = [_D, _D] + [ct.c_int] * 5 + [_D, _D]
+            L.oref_metric_scores.restype = None
+            L.oref_metric_scores.argtypes = [_D, _D] + [ct.c_int] * 8 + [ct.c_uint64, ct.c_long, _D]
             L.oref_select.restype = None
             L.oref_select.argtypes = [_D] + [ct.c_int] * 5 + [_I32]
             L.oref_state_init.restype = None
@@ -103,6 +105,40 @@ def scores(q, k, W):
     s = np.empty((Hkv, N))
     lib().oref_scores(_d(q), _d(k), Hq, Hkv, N, d, W, _d(hs), _d(s))
     return hs, s
+
+
+# routing metrics of the ablation (the ids of still_metric in include/still.h are
+# the library's; these are the oracle's own, written out here)
+METRICS = {"self_saliency": 0, "diagonal": 1, "qk": 2, "key_norm": 3, "uniform": 4, "random": 5}
+
+
+def metric_scores(q, k, W, C, lam, metric, seed=0, unit0=0):
+    """Routing-metric scores of one sequence: q [Hq,N,d], k [Hkv,N,d] -> [Hkv,N].
+    unit0 = b * Hkv places the sequence in the random metric's counter."""
+    if metric == "self_saliency":
+        return scores(q, k, W)[1]
+    q, k = _f64(q), _f64(k)
+    Hq, N, d = q.shape
+    Hkv = k.shape[0]
+    out = np.empty((Hkv, N))
+    lib().oref_metric_scores(_d(q), _d(k), Hq, Hkv, N, d, W, C, lam, METRICS[metric], ct.c_uint64(seed),
+                             int(unit0), _d(out))
+    return out
+
+
+def prefill_routed(q, k, v, Wf, W, C, m, T_max, metric, seed=0, sel=None, threads=0):
+    """The layer with its chunks ranked by a routing metric: the metric's scores,
+    the top-lambda of every completed chunk, then the prefill with that
+    selection.  sel (optional [B,Hkv,T_max,lam]) replaces the selection.
+    Returns (y [B,Hq,N,d], metric scores [B,Hkv,N], selection)."""
+    q, k = _f64(q), _f64(k)
+    B, Hkv = q.shape[0], k.shape[1]
+    lam = lam_of(m, W, T_max)
+    sc = np.stack([metric_scores(q[b], k[b], W, C, lam, metric, seed, b * Hkv) for b in range(B)])
+    if sel is None:
+        sel = np.stack([select(sc[b], C, lam, T_max) for b in range(B)])
+    y, _, _ = prefill(q, k, v, Wf, W, C, m, T_max, sel_override=sel if lam > 0 else None, threads=threads)
+    return y, sc, sel
 
 
 def select(scores_kv, C, lam, T_max):

@@ -160,6 +160,78 @@ void oref_scores(const double *q, const double *k, int Hq, int Hkv, int N, int d
     free(keys);
 }
 
+/* ---- routing metrics of the ablation ("Ablation Studies", routing metric
+ * comparison): other per-token scores ranked by the same chunk selection.
+ * The pages name them without formulas; each is written out from its plain
+ * reading.  1 diagonal: mean over the G heads of the self probability p_t of
+ * the window softmax; 2 q.k / sqrt(d), mean over the G heads; 3 ||k_t||;
+ * 4 uniform: 1 at the lambda evenly spaced offsets floor((r + 1/2) C / lambda)
+ * of each chunk; 5 random: SplitMix64 (Steele, Lea, Flood 2014), the stream
+ * that starts at `seed`, draw number i + 1 for the token with flat index
+ * i = (unit0 + g) N + t, its top 24 bits over 2^24. */
+
+static uint64_t oref_splitmix64_next(uint64_t *x)
+{
+    uint64_t z = (*x += 0x9E3779B97F4A7C15ull);
+    z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+    z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+    return z ^ (z >> 31);
+}
+
+void oref_metric_scores(const double *q, const double *k, int Hq, int Hkv, int N, int d, int W, int C, int lam,
+                        int metric, uint64_t seed, long unit0, double *scores)
+{
+    int G = Hq / Hkv;
+    double sc = 1.0 / sqrt((double)d);
+    for (long i = 0; i < (long)Hkv * N; ++i) scores[i] = 0.0;
+    if (metric == 5) {
+        uint64_t x = seed;
+        for (long j = 0; j < unit0 * (long)N; ++j) oref_splitmix64_next(&x);   /* earlier sequences' draws */
+        for (long i = 0; i < (long)Hkv * N; ++i) scores[i] = (double)(oref_splitmix64_next(&x) >> 40) / 16777216.0;
+        return;
+    }
+    for (int g = 0; g < Hkv; ++g)
+        for (long t = 0; t < N; ++t) {
+            const double *kt = k + ((long)g * N + t) * d;
+            double v = 0.0;
+            if (metric == 3) {
+                for (int e = 0; e < d; ++e) v += kt[e] * kt[e];
+                v = sqrt(v);
+            } else if (metric == 4) {
+                long off = t % C;
+                if (lam >= C) v = 1.0;
+                for (int r = 0; r < lam && r < C; ++r)
+                    if (((2L * r + 1) * C) / (2L * lam) == off) v = 1.0;
+            } else {
+                for (int h = g * G; h < (g + 1) * G; ++h) {
+                    const double *qt = q + ((long)h * N + t) * d;
+                    if (metric == 2) {
+                        double a = 0.0;
+                        for (int e = 0; e < d; ++e) a += qt[e] * kt[e];
+                        v += a * sc / G;
+                    } else { /* 1: softmax over keys [max(0, t-W+1), t], the weight of key t */
+                        long lo = t - W + 1 < 0 ? 0 : t - W + 1;
+                        double mx = -INFINITY, tot = 0.0, self = 0.0;
+                        for (long j = lo; j <= t; ++j) {
+                            double a = 0.0;
+                            for (int e = 0; e < d; ++e) a += qt[e] * k[((long)g * N + j) * d + e];
+                            if (a * sc > mx) mx = a * sc;
+                        }
+                        for (long j = lo; j <= t; ++j) {
+                            double a = 0.0;
+                            for (int e = 0; e < d; ++e) a += qt[e] * k[((long)g * N + j) * d + e];
+                            double w = exp(a * sc - mx);
+                            tot += w;
+                            if (j == t) self = w;
+                        }
+                        v += self / tot / G;
+                    }
+                }
+            }
+            scores[(long)g * N + t] = v;
+        }
+}
+
 /* Top-lambda of each completed chunk c < T_max, ascending positions, -1 pad.
  * scores [Hkv, N] -> sel [Hkv, T_max, lam]. */
 void oref_select(const double *scores, int Hkv, int N, int C, int lam, int T_max, int32_t *sel)
