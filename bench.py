@@ -47,6 +47,7 @@ def parse(argv=None):
                    help="sequences of the decode workload (default: the workload's 128); a smaller batch "
                         "keeps an ncu capture of the decode kernel to a few GB of device memory")
     p.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
+    p.add_argument("--no-routing", action="store_true", help="skip the routing-metric measurements")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--cpu-tokens", type=int, default=16384, help="tokens of the CPU-baseline sample")
     p.add_argument("--seed", type=int, default=0)
@@ -303,10 +304,11 @@ def run_ours(args):
         if pg is not None:
             pg.barrier()
         torch.cuda.synchronize(dev)
-        still.timing_read()
-        still.timing_enable(True)
         ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
               for _ in range(args.steps)]
+        # the headline: the step as a caller runs it (the library's per-kernel
+        # timers put an event between launches, which would serialise the
+        # programmatic dependent launches; they run in a second pass below)
         wall0 = time.perf_counter()
         for i in range(args.steps):
             flush.fill_(float(i))              # evict the previous step's data from L2
@@ -315,10 +317,23 @@ def run_ours(args):
             ev[i][1].record(stream)
         torch.cuda.synchronize(dev)
         wall = time.perf_counter() - wall0
-        still.timing_enable(False)
         if pg is not None:
             pg.barrier()
+    # the same steps again with a CUDA event pair around every kernel: the
+    # per-kernel times and the roofline of the dominant kernel
+    still.timing_read()
+    still.timing_enable(True)
+    ev_k = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for _ in range(args.steps)]
+    for i in range(args.steps):
+        flush.fill_(float(i))
+        ev_k[i][0].record(stream)
+        step()
+        ev_k[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    still.timing_enable(False)
     ktimes = still.timing_read()
+    step_ms_timed_kernels = statistics.mean(a.elapsed_time(b) for a, b in ev_k)
     step_ms = [a.elapsed_time(b) for a, b in ev]
     t_total = sum(step_ms) / 1e3
     value, ms_per_step, t_max = aggregate(pg, t_total, w.B * w.N, args.steps, dev)
@@ -361,7 +376,10 @@ def run_ours(args):
                               "roofline_ms": step_roof_s * 1e3, "frac_of_roofline": step_roof_s * 1e3 / ms_per_step,
                               "mean_softmax_keys_per_query": alg["mean_sa_keys"], "peak_source": pk_kind},
             "kernels": {k2: {"launches": n, "ms_per_launch": ms / n} for k2, (n, ms) in ktimes.items()},
+            # the kernel pass runs the same steps through the same path, so it
+            # launches what the headline pass did
             "gpu_launches": launches, "wall_s_timed_region": wall,
+            "ms_per_step_with_kernel_timers": step_ms_timed_kernels,
             "clocks": clk.summary()}
 
     # -------- end to end through host buffers --------
@@ -422,6 +440,10 @@ def run_ours(args):
                        "d2h_bytes_per_step": int(hout.numel() * 2 + hsel.numel() * 4), "steps": n_e2e,
                        "overlap": "upload, layer and download on three streams, double-buffered"}
 
+    # -------- routing metrics of the ablation (16K layer) --------
+    if not args.no_routing and rank == 0:
+        line["routing_metrics"] = bench_routing(still, w, (q, k, v, Wf), dev, stream, pk, pk_kind)
+
     # -------- decode step (128 sequences at 16K) --------
     if not args.no_decode and rank == 0:
         line["decode_step"] = bench_decode(still, inputs, dev, stream, pk, pk_kind, args)
@@ -439,6 +461,53 @@ def run_ours(args):
         print(json.dumps(line), flush=True)
     if pg is not None:
         pg.destroy_process_group()
+
+
+def bench_routing(still, w, qkvw, dev, stream, pk, pk_kind, launches=10):
+    """Each routing metric's score kernel on the 16K layer (library event timers,
+    L2 flushed before every launch) against its algorithmic bytes, and the whole
+    layer routed by it (CUDA events around the call)."""
+    import torch
+    q, k, v, Wf = qkvw
+    qb, kb, sb = 2.0 * w.B * w.Hq * w.N * w.d, 2.0 * w.B * w.Hkv * w.N * w.d, 4.0 * w.B * w.Hkv * w.N
+    need = {"diagonal": qb + kb, "qk": qb + kb, "key_norm": kb, "uniform": 0.0, "random": 0.0}
+    scores = torch.empty((w.B, w.Hkv, w.N), dtype=torch.float32, device=dev)
+    out = torch.empty_like(q)
+    sel = torch.empty((w.B, w.Hkv, w.T_max, w.lam), dtype=torch.int32, device=dev)
+    ws = torch.empty(still.workspace_size(q, k, Wf, w.W, w.C, w.m, w.T_max), dtype=torch.uint8, device=dev)
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+    res = {}
+    for metric, inb in need.items():
+        for i in range(3):
+            still.score_metric(q, k, w.W, w.C, w.m, w.T_max, metric, seed=i, scores=scores, stream=stream)
+        torch.cuda.synchronize(dev)
+        still.timing_read()
+        still.timing_enable(True)
+        for i in range(launches):
+            flush.fill_(float(i))
+            still.score_metric(q, k, w.W, w.C, w.m, w.T_max, metric, seed=i, scores=scores, stream=stream)
+        torch.cuda.synchronize(dev)
+        still.timing_enable(False)
+        t = still.timing_read()
+        n, ms = t.get("routing_metric", t.get("score", (0, 0.0)))
+        per = ms / max(n, 1) / 1e3
+        by = inb + sb
+        ach = by / per / 1e9
+        pre = []
+        for i in range(5):
+            flush.fill_(float(i))
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            still.prefill_routed(q, k, v, Wf, w.W, w.C, w.m, w.T_max, metric, seed=i, out=out, sel_idx=sel,
+                                 workspace=ws, stream=stream)
+            b.record(stream)
+            pre.append((a, b))
+        torch.cuda.synchronize(dev)
+        res[metric] = {"ms_per_launch": per * 1e3, "launches": n, "algorithmic_bytes": by,
+                       "roofline": {"bound": "hbm", "achieved": ach, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                                    "frac": ach / pk["hbm_gbs"], "peak_source": pk_kind},
+                       "routed_prefill_ms": statistics.median(a.elapsed_time(b) for a, b in pre[2:])}
+    return res
 
 
 def bench_decode(still, inputs, dev, stream, pk, pk_kind, args):

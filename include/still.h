@@ -113,6 +113,46 @@ still_status still_score(const still_shape *shape, const still_bf16 *q, const st
                          float *scores, still_stream_t stream);
 
 /*
+ * Routing metrics (section "Ablation Studies", routing metric comparison: the
+ * fixed-budget selection run with other per-token scores in place of the
+ * Self-Saliency Score).  Every metric yields one fp32 score per (sequence, kv
+ * head, token), [B, Hkv, N]; a higher score ranks higher in the chunk's
+ * top-lambda.  The pages name the metrics but print no formula; the readings:
+ *   SELF_SALIENCY  the Self-Saliency Score, as still_score
+ *   DIAGONAL       mean over the G query heads of p_t, the token's own weight in
+ *                  the softmax over its causal window of W keys (a^diag_t)
+ *   QK             mean over the G query heads of q_t . k_t / sqrt(d)
+ *   KEY_NORM       ||k_t|| (two-norm over d)
+ *   UNIFORM        1 at the lambda evenly spaced offsets floor((r + 1/2) C /
+ *                  lambda), r < lambda, of every chunk, 0 elsewhere (every
+ *                  offset when lambda >= C)
+ *   RANDOM         SplitMix64 (Steele, Lea, Flood 2014) as a counter-based
+ *                  generator: z = seed + (i + 1) * 0x9E3779B97F4A7C15, then its
+ *                  published output mix, with i = (b Hkv + g) N + t; the score
+ *                  is (z >> 40) * 2^-24 in [0, 1)
+ */
+typedef enum {
+    STILL_METRIC_SELF_SALIENCY = 0,
+    STILL_METRIC_DIAGONAL = 1,
+    STILL_METRIC_QK = 2,
+    STILL_METRIC_KEY_NORM = 3,
+    STILL_METRIC_UNIFORM = 4,
+    STILL_METRIC_RANDOM = 5
+} still_metric;
+
+/*
+ * Scores of one routing metric.  q [B,Hq,N,d] bf16 (read by SELF_SALIENCY,
+ * DIAGONAL and QK; may be NULL otherwise), k [B,Hkv,N,d] bf16 (read by all but
+ * UNIFORM and RANDOM; may be NULL for those two) -> scores fp32 [B,Hkv,N].  W is
+ * the window of SELF_SALIENCY and DIAGONAL (>= 1 for them); C, m and T_max
+ * give UNIFORM its lambda and are checked as for still_select; seed is read by
+ * RANDOM only.  An unknown metric returns STILL_ERR_INVALID_ARG.
+ */
+still_status still_score_metric(const still_shape *shape, const still_bf16 *q, const still_bf16 *k, int W, int C,
+                                int m, int T_max, still_metric metric, uint64_t seed, float *scores,
+                                still_stream_t stream);
+
+/*
  * Delayed chunk-level selection (section "Delayed Chunk-Level Selection for
  * Unified Training-Inference Parallelism"): each completed chunk c < T_max
  * (tokens [cC, cC + C), all < N) keeps its top-lambda tokens by score, an
@@ -154,6 +194,18 @@ still_status still_prefill(const still_shape *shape, const still_bf16 *q, const 
                            const still_bf16 *v, const float *Wf, int W, int C, int m, int T_max,
                            still_bf16 *out, int32_t *sel_idx, void *workspace, size_t workspace_bytes,
                            const still_decode_state *export_state, still_stream_t stream);
+
+/*
+ * The prefill above with the chunk selection ranked by another routing metric
+ * (see still_metric); everything after the scores is the same layer.  With
+ * STILL_METRIC_SELF_SALIENCY it computes exactly what still_prefill does.  No
+ * decode state is exported: the decode step ranks by the Self-Saliency Score.
+ * workspace as for still_prefill (still_prefill_workspace_size bytes, or NULL).
+ */
+still_status still_prefill_routed(const still_shape *shape, const still_bf16 *q, const still_bf16 *k,
+                                  const still_bf16 *v, const float *Wf, int W, int C, int m, int T_max,
+                                  still_metric metric, uint64_t seed, still_bf16 *out, int32_t *sel_idx,
+                                  void *workspace, size_t workspace_bytes, still_stream_t stream);
 
 /*
  * The prefill above with its scratch memory taken from a fixed array inside

@@ -246,10 +246,17 @@ size_t still_prefill_workspace_size(const still_shape *shape, int W, int C, int 
     return ws_layout(dm, plan_segments(dm)).total;
 }
 
-still_status still_prefill(const still_shape *shape, const still_bf16 *q, const still_bf16 *k, const still_bf16 *v,
-                           const float *Wf, int W, int C, int m, int T_max, still_bf16 *out, int32_t *sel_idx,
-                           void *workspace, size_t workspace_bytes, const still_decode_state *export_state,
-                           still_stream_t stream)
+}  // extern "C"
+
+namespace {
+
+// The prefill, its chunks ranked by `metric`.  The Self-Saliency path runs the
+// set-up pass inside the tensor-core score kernel; other metrics run it as a
+// kernel of its own before their scores.
+still_status prefill_impl(const still_shape *shape, const still_bf16 *q, const still_bf16 *k, const still_bf16 *v,
+                          const float *Wf, int W, int C, int m, int T_max, int metric, unsigned long long seed,
+                          still_bf16 *out, int32_t *sel_idx, void *workspace, size_t workspace_bytes,
+                          const still_decode_state *export_state, still_stream_t stream)
 {
     Dims dm;
     still_status st = make_dims(shape, W, C, m, T_max, &dm);
@@ -289,14 +296,14 @@ still_status still_prefill(const still_shape *shape, const still_bf16 *q, const 
     float *dz = (float *)(base + L.dz);
     const bool tc = hybrid_tc_supported(dm);
     // the set-up pass rides on the tensor-core score kernel when that one runs
-    const bool fused_prep = dm.lam > 0 && score_tc_supported(dm);
+    const bool fused_prep = dm.lam > 0 && score_tc_supported(dm) && metric == STILL_METRIC_SELF_SALIENCY;
     cudaError_t e = cudaSuccess;
     if (fused_prep) {
         const PrepArgs pa{Wf, wft, status, kslot, kk, L.kept_bytes};
         e = launch_score_tc(dm, q, k, scores, s, &pa);
     } else {
         e = launch_prep(dm, Wf, wft, status, kslot, kk, L.kept_bytes, s);
-        if (e == cudaSuccess && dm.lam > 0) e = launch_score(dm, q, k, scores, s);
+        if (e == cudaSuccess && dm.lam > 0) e = launch_metric(dm, metric, seed, q, k, scores, s);
     }
     if (e == cudaSuccess && dm.lam > 0) e = launch_select(dm, scores, sel_idx, fsel, kslot, s, k, v, kk, vk);
     if (e == cudaSuccess) e = launch_linstate_tc(dm, sp, k, v, wft, kslot, phik, phk, dS, dz, status, s);
@@ -315,6 +322,49 @@ still_status still_prefill(const still_shape *shape, const still_bf16 *q, const 
         if (e == cudaSuccess) e = e2;
     }
     return cuda_status(e);
+}
+
+bool metric_ok(int metric) { return metric >= STILL_METRIC_SELF_SALIENCY && metric <= STILL_METRIC_RANDOM; }
+
+}  // namespace
+
+extern "C" {
+
+still_status still_prefill(const still_shape *shape, const still_bf16 *q, const still_bf16 *k, const still_bf16 *v,
+                           const float *Wf, int W, int C, int m, int T_max, still_bf16 *out, int32_t *sel_idx,
+                           void *workspace, size_t workspace_bytes, const still_decode_state *export_state,
+                           still_stream_t stream)
+{
+    return prefill_impl(shape, q, k, v, Wf, W, C, m, T_max, STILL_METRIC_SELF_SALIENCY, 0, out, sel_idx, workspace,
+                        workspace_bytes, export_state, stream);
+}
+
+still_status still_prefill_routed(const still_shape *shape, const still_bf16 *q, const still_bf16 *k,
+                                  const still_bf16 *v, const float *Wf, int W, int C, int m, int T_max,
+                                  still_metric metric, uint64_t seed, still_bf16 *out, int32_t *sel_idx,
+                                  void *workspace, size_t workspace_bytes, still_stream_t stream)
+{
+    if (!metric_ok(metric)) return STILL_ERR_INVALID_ARG;
+    return prefill_impl(shape, q, k, v, Wf, W, C, m, T_max, metric, seed, out, sel_idx, workspace, workspace_bytes,
+                        nullptr, stream);
+}
+
+still_status still_score_metric(const still_shape *shape, const still_bf16 *q, const still_bf16 *k, int W, int C,
+                                int m, int T_max, still_metric metric, uint64_t seed, float *scores,
+                                still_stream_t stream)
+{
+    if (!metric_ok(metric)) return STILL_ERR_INVALID_ARG;
+    const bool windowed = metric == STILL_METRIC_SELF_SALIENCY || metric == STILL_METRIC_DIAGONAL;
+    const bool needs_q = windowed || metric == STILL_METRIC_QK;
+    const bool needs_k = needs_q || metric == STILL_METRIC_KEY_NORM;
+    Dims dm;
+    const still_status st = make_dims(shape, W, C, m, T_max, &dm);   // the routing parameters, as still_select
+    if (st != STILL_OK) return st;
+    if (windowed && W < 1) return STILL_ERR_INVALID_ARG;
+    if (!scores || !aligned16(scores)) return STILL_ERR_INVALID_ARG;
+    if ((needs_q && (!q || !aligned16(q))) || (needs_k && (!k || !aligned16(k)))) return STILL_ERR_INVALID_ARG;
+    if (dm.N == 0) return STILL_OK;
+    return cuda_status(launch_metric(dm, metric, seed, q, k, scores, (cudaStream_t)stream));
 }
 
 still_status still_decode_state_init(const still_shape *shape, const still_decode_state *state, int W, int C, int m,

@@ -177,7 +177,9 @@ struct KTimer {
 };
 
 // ---- launchers (one per kernel family) ----------------------------------------
-cudaError_t launch_score(const Dims &dm, const uint16_t *q, const uint16_t *k, float *scores, cudaStream_t s);
+// diag = 1: the mean self probability p_t (the diagonal-attention routing metric)
+cudaError_t launch_score(const Dims &dm, const uint16_t *q, const uint16_t *k, float *scores, cudaStream_t s,
+                         int diag = 0);
 bool score_tc_supported(const Dims &dm);
 // The prefill's set-up pass (see prep_kernel), folded into the score kernel.
 struct PrepArgs {
@@ -188,7 +190,10 @@ struct PrepArgs {
     size_t kept_bytes;
 };
 cudaError_t launch_score_tc(const Dims &dm, const uint16_t *q, const uint16_t *k, float *scores, cudaStream_t s,
-                            const PrepArgs *prep = nullptr);
+                            const PrepArgs *prep = nullptr, int diag = 0);
+// Routing metrics (routing.cu); metric is a still_metric value.
+cudaError_t launch_metric(const Dims &dm, int metric, unsigned long long seed, const uint16_t *q, const uint16_t *k,
+                          float *scores, cudaStream_t s);
 cudaError_t launch_select(const Dims &dm, const float *scores, int32_t *sel_idx, int32_t *fsel, int32_t *kslot,
                           cudaStream_t s, const uint16_t *k = nullptr, const uint16_t *v = nullptr,
                           uint16_t *kk = nullptr, uint16_t *vk = nullptr);

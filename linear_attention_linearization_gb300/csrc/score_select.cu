@@ -20,7 +20,7 @@ namespace still {
 template <int D>
 __global__ void __launch_bounds__(256) score_kernel(const uint16_t *__restrict__ q,
                                                     const uint16_t *__restrict__ k, Dims dm,
-                                                    float *__restrict__ scores)
+                                                    float *__restrict__ scores, int diag)
 {
     grid_dep_sync();
     const int g = blockIdx.y, b = blockIdx.z;
@@ -56,18 +56,18 @@ __global__ void __launch_bounds__(256) score_kernel(const uint16_t *__restrict__
             const float f = (ml == -INFINITY) ? 0.f : expf(ml - M);
             const float oth = warp_sum(tl * f);
             const float self = warp_sum(sl * f);
-            acc += saliency_from_stats(oth, self);
+            acc += diag ? self / (oth + self) : saliency_from_stats(oth, self);
         }
         if (lane == 0) scores[(size_t)(b * dm.Hkv + g) * dm.N + t] = acc / dm.G;
     }
 }
 
-cudaError_t launch_score(const Dims &dm, const uint16_t *q, const uint16_t *k, float *scores, cudaStream_t s)
+cudaError_t launch_score(const Dims &dm, const uint16_t *q, const uint16_t *k, float *scores, cudaStream_t s, int diag)
 {
     KTimer tm("score", s);
     dim3 grid((dm.N + 63) / 64, dm.Hkv, dm.B);
     const cudaError_t e = launch_kernel(dm.d == 64 ? score_kernel<64> : score_kernel<128>, grid, dim3(256), 0, s, q, k,
-                                        dm, scores);
+                                        dm, scores, diag);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }

@@ -37,6 +37,7 @@ struct ScoreTCParams {
     int stages;        // tiles in flight (shared-memory and TMEM stages)
     uint32_t stage_bytes, tmem_stride;
     float *scores;
+    int diag;          // 1: write the mean self probability p_t (diagonal attention) instead of the score
     // the prefill's set-up, done by this kernel's threads when kslot is set:
     // status word = 0, slot map = -1, kept tables = 0, W_f^T in bf16
     const float *Wf;
@@ -229,7 +230,7 @@ __global__ void __launch_bounds__(SC_THREADS, 1) score_tc_kernel(const __grid_co
             }
             const float oth = (o4[0] + o4[1]) + (o4[2] + o4[3]);
             float *hs = hsc[grp][n & 1];
-            hs[hh * 32 + tt] = (hh < dm.G && t < dm.N) ? saliency_from_stats(oth, 1.f) : 0.f;
+            hs[hh * 32 + tt] = (hh < dm.G && t < dm.N) ? (P.diag ? 1.f / (1.f + oth) : saliency_from_stats(oth, 1.f)) : 0.f;
             // the group's four heads are in; the other half of hsc[grp] was read
             // before this barrier by the warp that reads this half after it
             if (named_sync_or(1 + grp, 128, bad || *(volatile int *)&s_abort)) break;
@@ -255,7 +256,7 @@ bool score_tc_supported(const Dims &dm)
 }
 
 cudaError_t launch_score_tc(const Dims &dm, const uint16_t *q, const uint16_t *k, float *scores, cudaStream_t s,
-                            const PrepArgs *prep)
+                            const PrepArgs *prep, int diag)
 {
     KTimer tm("score", s);
     ScoreTCMaps m;
@@ -274,6 +275,7 @@ cudaError_t launch_score_tc(const Dims &dm, const uint16_t *q, const uint16_t *k
     p.tiles_per_unit = (dm.N + 31) / 32;
     p.total_tiles = p.tiles_per_unit * dm.B * dm.Hkv;
     p.scores = scores;
+    p.diag = diag;
     p.Wf = prep ? prep->Wf : nullptr;
     p.wft = prep ? prep->wft : nullptr;
     p.status = prep ? prep->status : nullptr;

@@ -15,6 +15,9 @@ import torch
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libstill.so")
 
+# still_metric (include/still.h): routing metrics of the chunk selection
+METRICS = {"self_saliency": 0, "diagonal": 1, "qk": 2, "key_norm": 3, "uniform": 4, "random": 5}
+
 STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported shape", 3: "CUDA error",
           4: "device wait timed out", 5: "index out of bounds", 6: "workspace too small"}
 
@@ -49,6 +52,8 @@ SIGNATURES = {
                                ct.c_void_p]),
     "still_select": (ct.c_int, [ct.POINTER(Shape), ct.c_void_p, ct.c_int, ct.c_int, ct.c_int, ct.c_int,
                                 ct.c_void_p, ct.c_void_p]),
+    "still_score_metric": (ct.c_int, [ct.POINTER(Shape), ct.c_void_p, ct.c_void_p, ct.c_int, ct.c_int, ct.c_int,
+                                      ct.c_int, ct.c_int, ct.c_uint64, ct.c_void_p, ct.c_void_p]),
     "still_npmap": (ct.c_int, [ct.c_void_p, ct.c_longlong, ct.c_int, ct.c_void_p, ct.c_int, ct.c_void_p,
                                ct.c_void_p]),
     "still_prefill_workspace_size": (ct.c_size_t, [ct.POINTER(Shape), ct.c_int, ct.c_int, ct.c_int,
@@ -56,6 +61,9 @@ SIGNATURES = {
     "still_prefill": (ct.c_int, [ct.POINTER(Shape), ct.c_void_p, ct.c_void_p, ct.c_void_p, ct.c_void_p,
                                  ct.c_int, ct.c_int, ct.c_int, ct.c_int, ct.c_void_p, ct.c_void_p,
                                  ct.c_void_p, ct.c_size_t, ct.POINTER(DecodeStateC), ct.c_void_p]),
+    "still_prefill_routed": (ct.c_int, [ct.POINTER(Shape), ct.c_void_p, ct.c_void_p, ct.c_void_p, ct.c_void_p,
+                                        ct.c_int, ct.c_int, ct.c_int, ct.c_int, ct.c_int, ct.c_uint64,
+                                        ct.c_void_p, ct.c_void_p, ct.c_void_p, ct.c_size_t, ct.c_void_p]),
     "still_prefill_noalloc_max_bytes": (ct.c_size_t, []),
     "still_prefill_noalloc": (ct.c_int, [ct.POINTER(Shape), ct.c_void_p, ct.c_void_p, ct.c_void_p, ct.c_void_p,
                                          ct.c_int, ct.c_int, ct.c_int, ct.c_int, ct.c_void_p, ct.c_void_p,
@@ -142,6 +150,26 @@ def select(scores, Hq, d, W, C, m, T_max, sel_idx=None, stream=None):
     return sel_idx
 
 
+def score_metric(q, k, W, C, m, T_max, metric, seed=0, B=None, Hq=None, Hkv=None, N=None, d=None,
+                 scores=None, stream=None):
+    """Scores [B, Hkv, N] (fp32) of one routing metric (a name of METRICS).  q and
+    k are bf16 [B,Hq,N,d] / [B,Hkv,N,d]; either may be None for the metrics that do
+    not read it, and the sizes are then taken from the keyword arguments."""
+    mid = METRICS[metric]
+    if q is not None:
+        B, Hq, N, d = q.shape
+    if k is not None:
+        B, Hkv, N, d = k.shape
+    sh = Shape(B, Hq, Hkv, N, d, d)
+    dev = q.device if q is not None else (k.device if k is not None else torch.device("cuda"))
+    if scores is None:
+        scores = torch.empty((B, Hkv, N), dtype=torch.float32, device=dev)
+    _check(lib().still_score_metric(ct.byref(sh), _ptr(q, torch.bfloat16, "q"), _ptr(k, torch.bfloat16, "k"), W, C,
+                                    m, T_max, mid, ct.c_uint64(seed), _ptr(scores, torch.float32, "scores"),
+                                    _stream(stream)), "still_score_metric")
+    return scores
+
+
 def npmap(x, Wf, stream=None):
     """NP-Map of the rows of bf16 x [..., d] with fp32 Wf [d, d_f] -> fp32 [..., d_f]."""
     d, df = Wf.shape
@@ -211,6 +239,28 @@ def prefill(q, k, v, Wf, W, C, m, T_max, out=None, sel_idx=None, workspace=None,
                                _ptr(out, torch.bfloat16, "out"),
                                _ptr(sel_idx, torch.int32, "sel_idx") if sel_idx.numel() else None,
                                ws_ptr, ws_bytes, st, _stream(stream)), "still_prefill")
+    return out, sel_idx
+
+
+def prefill_routed(q, k, v, Wf, W, C, m, T_max, metric, seed=0, out=None, sel_idx=None, workspace=None,
+                   stream=None):
+    """The prefill with the chunk selection ranked by a routing metric (a name of
+    METRICS).  Returns (out [B,Hq,N,d] bf16, sel_idx)."""
+    B, Hq, N, d = q.shape
+    lam = lam_of(W, m, T_max)
+    sh = shape_of(q, k, Wf)
+    if out is None:
+        out = torch.empty_like(q)
+    if sel_idx is None:
+        sel_idx = torch.empty((B, k.shape[1], T_max, max(lam, 0)), dtype=torch.int32, device=q.device)
+    ws_ptr, ws_bytes = None, 0
+    if workspace is not None:
+        ws_ptr, ws_bytes = _ptr(workspace, torch.uint8, "workspace"), workspace.numel()
+    _check(lib().still_prefill_routed(ct.byref(sh), _ptr(q, torch.bfloat16, "q"), _ptr(k, torch.bfloat16, "k"),
+                                      _ptr(v, torch.bfloat16, "v"), _ptr(Wf, torch.float32, "Wf"), W, C, m, T_max,
+                                      METRICS[metric], ct.c_uint64(seed), _ptr(out, torch.bfloat16, "out"),
+                                      _ptr(sel_idx, torch.int32, "sel_idx") if sel_idx.numel() else None,
+                                      ws_ptr, ws_bytes, _stream(stream)), "still_prefill_routed")
     return out, sel_idx
 
 

@@ -72,6 +72,18 @@ def test_workspace_size_and_argument_errors(lib):
     st = DecodeStateC()
     assert lib.still_decode_step(ct.byref(sh), ct.byref(st), p, p, p, p, 64, 256, 288, 64, p, None) == 1
     assert lib.still_score(ct.byref(sh), p, p, 0, p, None) == 1
+    # routing metrics: unknown metric, missing inputs, windowed metric without a window
+    assert lib.still_score_metric(ct.byref(sh), p, p, 64, 256, 288, 64, 6, 0, p, None) == 1
+    assert lib.still_score_metric(ct.byref(sh), p, p, 64, 256, 288, 64, -1, 0, p, None) == 1
+    assert lib.still_score_metric(ct.byref(sh), None, p, 64, 256, 288, 64, 2, 0, p, None) == 1   # q.k without q
+    assert lib.still_score_metric(ct.byref(sh), p, None, 64, 256, 288, 64, 3, 0, p, None) == 1   # key norm without k
+    assert lib.still_score_metric(ct.byref(sh), p, p, 64, 256, 288, 64, 4, 0, None, None) == 1   # no scores
+    assert lib.still_score_metric(ct.byref(sh), p, p, 0, 256, 0, 64, 1, 0, p, None) == 1         # diagonal, W = 0
+    assert lib.still_score_metric(ct.byref(sh), p, p, 64, 256, 32, 64, 4, 0, p, None) == 1       # m < W
+    rargs = lambda metric, q: (ct.byref(sh), q, p, p, p, 64, 256, 288, 64, metric, 0, p, None, None, 0, None)
+    assert lib.still_prefill_routed(*rargs(7, p)) == 1
+    assert lib.still_prefill_routed(*rargs(2, None)) == 1
+    assert lib.still_prefill_routed(*rargs(2, bad)) == 1
 
 
 def test_oracle_library_shares_nothing_with_cuda_path():
