@@ -7,6 +7,13 @@ in libstill's kernels, on seeded synthetic inputs resident in HBM.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
+The headline steps run as a caller runs them (one CUDA event pair per step);
+a second pass of the same steps with an event pair around every kernel gives
+the per-kernel times and the roofline of the dominant kernel.  Further legs:
+end to end through pinned host buffers, the 128-sequence decode step, the
+routing metrics of the ablation (score kernel per metric and the layer routed
+by it), and the CPU oracle on a sample of the same layer.
+
 Under torchrun (N > 1) every rank runs its own layer (its own seed): weak
 scaling, no collective on the data path; value = all ranks' tokens / the max
 over ranks of the timed region.  --impl reference times the CPU oracle (the
