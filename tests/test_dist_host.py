@@ -82,3 +82,19 @@ def test_reference_arm_runs_on_rank_zero_only():
     assert line["impl"] == "reference" and line["n_gpus"] == 2
     assert line["cpu_baseline"]["kind"] == "oracle" and line["value"] > 0
     assert line["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_cpu_baseline_reports_all_cores_and_one_core():
+    """The CPU-baseline leg on a small layer: both runs time the oracle as it
+    stands, the one-core figure comes from one unit scaled to all of them."""
+    sys.path.insert(0, ROOT)
+    import bench
+    from linear_attention_linearization_gb300 import inputs
+    w = inputs.Workload("case", 2, 4, 2, 16, 96, 8, 16, 8 + 2 * 6, 6, 16)
+    q, k, v, Wf = inputs.make_inputs(w, seed=1)
+    r = bench.cpu_baseline(q, k, v, Wf, w, 64)
+    assert r["kind"] == "oracle" and r["unit"] == "tokens/s" and r["value"] > 0
+    assert 1 <= r["cores"] <= w.B * w.Hkv and r["seconds"] > 0
+    one = r["one_core"]
+    assert one["cores"] == 1 and one["value"] > 0 and one["unit"] == "tokens/s"
+    json.dumps(r)
