@@ -530,6 +530,36 @@ def bench_routing(still, w, qkvw, dev, stream, pk, pk_kind, launches=10):
     return res
 
 
+def cpu_decode_baseline(w, seed, steps=10):
+    """The oracle's decode step on the host cores: one sequence's state built by
+    the oracle's prefill over the workload's context, then `steps` decode steps
+    of that sequence (its kv heads over the host threads); the decode state is
+    bounded, so a step costs the same at any sequence of the batch, and the
+    batch's step is the sequence's time x B."""
+    import numpy as np
+    from linear_attention_linearization_gb300.inputs import to_f64
+    from oracle import ref
+    q, k, v, Wf = (to_f64(t) for t in inputs_cpu(w, seed))
+    thr = cpu_threads(w.Hkv)
+    _, _, st = ref.prefill(q, k, v, Wf, w.W, w.C, w.m, w.T_max, threads=thr)
+    rng = np.random.default_rng(seed + 1)
+    rows = lambda h: rng.standard_normal((steps, 1, h, w.d)).astype(np.float64)
+    qt, kt, vt = rows(w.Hq), rows(w.Hkv), rows(w.Hkv)
+    t0 = time.perf_counter()
+    for i in range(steps):
+        ref.decode_step(st, qt[i], kt[i], vt[i], Wf, w.W, w.C, w.m, w.T_max, threads=thr)
+    per_seq = (time.perf_counter() - t0) / steps
+    return {"value": 1.0 / per_seq, "unit": "tokens/s", "cores": thr, "kind": "oracle",
+            "ms_per_step": per_seq * w.B * 1e3,
+            "sample": f"one sequence's state from the oracle's prefill over {w.N} tokens, {steps} decode steps of it "
+                      f"({w.Hkv} kv heads over {thr} threads); a step of the {w.B}-sequence batch = its time x {w.B}"}
+
+
+def inputs_cpu(w, seed):
+    from linear_attention_linearization_gb300 import inputs
+    return inputs.make_inputs(w, seed=seed, B=1)
+
+
 def bench_decode(still, inputs, dev, stream, pk, pk_kind, args):
     import torch
     w = inputs.WORKLOADS[DECODE_WORKLOAD]
@@ -576,13 +606,16 @@ def bench_decode(still, inputs, dev, stream, pk, pk_kind, args):
     by_valid = units * (2.0 * valid * w.d * 2 + 2.0 * w.df * w.d * 4 + 2.0 * w.df * 4) + \
         w.B * (2.0 * w.Hq * w.d * 2 + 2.0 * w.Hkv * w.d * 2)
     ach = by_valid / per / 1e9
-    return {"workload": DECODE_WORKLOAD, "sequences": w.B, "context": w.N, "ms_per_step": per * 1e3,
+    res = {"workload": DECODE_WORKLOAD, "sequences": w.B, "context": w.N, "ms_per_step": per * 1e3,
             "ms_per_call_with_host_launch": step_ms, "kernel_launches_timed": kt_launches,
             "tokens_per_s": w.B / per, "valid_slots": valid, "algorithmic_bytes_per_step": by_valid,
             "roofline": {"kernel": "decode_step", "bound": "hbm", "achieved": ach, "peak": pk["hbm_gbs"],
                          "unit": "GB/s", "frac": ach / pk["hbm_gbs"], "peak_source": pk_kind,
                          "traffic": profile_traffic("decode_step")},
             "state_bytes": st.nbytes()}
+    if not args.no_cpu:
+        res["cpu_baseline"] = cpu_decode_baseline(w, args.seed + 7)
+    return res
 
 
 def main():

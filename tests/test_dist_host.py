@@ -98,3 +98,14 @@ def test_cpu_baseline_reports_all_cores_and_one_core():
     one = r["one_core"]
     assert one["cores"] == 1 and one["value"] > 0 and one["unit"] == "tokens/s"
     json.dumps(r)
+
+
+def test_cpu_decode_baseline_runs_the_oracle_decode_step():
+    sys.path.insert(0, ROOT)
+    import bench
+    from linear_attention_linearization_gb300 import inputs
+    w = inputs.Workload("case", 16, 4, 2, 16, 200, 8, 16, 8 + 2 * 6, 6, 16)
+    r = bench.cpu_decode_baseline(w, seed=3, steps=4)
+    assert r["kind"] == "oracle" and r["unit"] == "tokens/s" and r["value"] > 0 and r["ms_per_step"] > 0
+    assert 1 <= r["cores"] <= w.Hkv
+    json.dumps(r)
