@@ -195,8 +195,10 @@ class ClockSampler:
 # CPU oracle
 # ---------------------------------------------------------------------------
 
-def oracle_sample(q, k, v, Wf, w, tokens, threads):
-    """Run the fp64 streaming oracle over `tokens` tokens of every kv head."""
+def oracle_sample(q, k, v, Wf, w, tokens, threads, keep=None):
+    """Run the fp64 streaming oracle over `tokens` tokens of every kv head; the
+    time it took.  With a dict `keep`, the oracle's output and scores are
+    stored there (key "y", "scores") for the parity check."""
     from linear_attention_linearization_gb300.inputs import to_f64
     from oracle import ref
     qa = to_f64(q[:, :, :tokens])
@@ -204,8 +206,45 @@ def oracle_sample(q, k, v, Wf, w, tokens, threads):
     va = to_f64(v[:, :, :tokens])
     Wa = to_f64(Wf)
     t0 = time.perf_counter()
-    ref.prefill(qa, ka, va, Wa, w.W, w.C, w.m, w.T_max, threads=threads)
-    return time.perf_counter() - t0
+    y, sc, _ = ref.prefill(qa, ka, va, Wa, w.W, w.C, w.m, w.T_max, threads=threads)
+    secs = time.perf_counter() - t0
+    if keep is not None:
+        keep.update(y=y, scores=sc, inputs=(qa, ka, va, Wa))
+    return secs
+
+
+def parity_vs_oracle(out, sel, w, toks, keep, threads):
+    """The benchmarked layer's output and selection against the oracle's run of
+    the CPU-baseline leg on the same inputs (tokens 0..toks-1): the largest
+    output error relative to the largest oracle output; selected sets exact
+    outside near-tie chunks (lambda-th and (lambda+1)-th oracle scores within
+    1e-5 relative), where the GPU's set must be a valid top-lambda and the
+    oracle is re-run with it."""
+    import numpy as np
+    from linear_attention_linearization_gb300.inputs import to_f64
+    from oracle import brute, ref
+    y_ref, sc = keep["y"], keep["scores"]
+    sel_g = sel.cpu().numpy()
+    n_ties = n_diff = 0
+    exact_outside = True
+    n_chunks = min(toks // w.C, w.T_max)
+    for b in range(w.B):
+        ties = set(brute.near_ties(sc[b], w.C, w.lam, w.T_max))
+        n_ties += len(ties)
+        sref = brute.select(sc[b], w.C, w.lam, w.T_max)
+        for g, c in np.argwhere((sel_g[b, :, :n_chunks] != sref[:, :n_chunks]).any(axis=-1)):
+            n_diff += 1
+            if (g, c) not in ties:
+                exact_outside = False
+    if n_diff and exact_outside and toks == w.N:
+        qa, ka, va, Wa = keep["inputs"]
+        y_ref, _, _ = ref.prefill(qa, ka, va, Wa, w.W, w.C, w.m, w.T_max, sel_override=sel_g, threads=threads)
+    y = to_f64(out[:, :, :toks])
+    err = float(np.abs(y - y_ref).max() / np.abs(y_ref).max())
+    return {"max_err_rel": err, "tolerance": 1e-2, "within_tolerance": err <= 1e-2,
+            "near_tie_chunks": n_ties, "sel_differs_in_near_ties": n_diff if exact_outside else None,
+            "sel_exact_outside_ties": exact_outside,
+            "compared": f"every output element and selected index of tokens 0..{toks - 1}, all heads"}
 
 
 def cpu_threads(units):
@@ -222,7 +261,8 @@ def cpu_baseline(q, k, v, Wf, w, toks):
     heads on one thread, its time scaled by the number of kv heads and
     sequences (the units are independent and cost the same)."""
     thr = cpu_threads(w.B * w.Hkv)
-    secs = oracle_sample(q, k, v, Wf, w, toks, thr)
+    keep = {}
+    secs = oracle_sample(q, k, v, Wf, w, toks, thr, keep)
     G = w.Hq // w.Hkv
     w1 = dataclasses.replace(w, B=1, Hq=G, Hkv=1)
     secs1 = oracle_sample(q[:1, :G], k[:1, :1], v[:1, :1], Wf, w1, toks, 1) * w.B * w.Hkv
@@ -232,7 +272,7 @@ def cpu_baseline(q, k, v, Wf, w, toks):
             "seconds": secs,
             "one_core": {"value": w.B * toks / secs1, "unit": "tokens/s", "cores": 1,
                          "sample": f"kv head 0 of sequence 0 with its {G} query heads over the same tokens on one "
-                                   f"thread, time x {w.B * w.Hkv} units"}}
+                                   f"thread, time x {w.B * w.Hkv} units"}}, keep, thr
 
 
 # ---------------------------------------------------------------------------
@@ -476,7 +516,10 @@ def run_ours(args):
 
     # -------- CPU oracle baseline --------
     if not args.no_cpu and rank == 0 and world == 1:
-        line["cpu_baseline"] = cpu_baseline(q.cpu(), k.cpu(), v.cpu(), Wf.cpu(), w, min(args.cpu_tokens, w.N))
+        toks = min(args.cpu_tokens, w.N)
+        line["cpu_baseline"], keep, thr = cpu_baseline(q.cpu(), k.cpu(), v.cpu(), Wf.cpu(), w, toks)
+        # the last timed step's output against that oracle run (outside the timed regions)
+        line["parity"] = parity_vs_oracle(out, sel, w, toks, keep, thr)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if pg is not None:

@@ -250,6 +250,20 @@ still_status still_decode_step(const still_shape *shape, const still_decode_stat
                                const float *Wf, int W, int C, int m, int T_max, still_bf16 *out_t,
                                still_stream_t stream);
 
+/*
+ * Failure-path testing.  The tensor-core prefill kernels bound every wait on
+ * the device: a row warp waiting for a copy or a tensor-core result gives up
+ * after a limit of clock cycles, writes STILL_ERR_TIMEOUT to the prefill's
+ * status word (still_read_status on the first int32 of the workspace), lets
+ * its block finish the copies and MMAs it already issued, and returns without
+ * trapping.  This call sets that limit for kernels launched afterwards by
+ * this process (cycles <= 0 restores the default of 4e9 cycles, about 2 s);
+ * a limit far below a kernel's normal waiting time (a few hundred cycles)
+ * makes the failure path run.  The outputs of a call that timed out are
+ * undefined; the CUDA context stays usable.  Not for production use.
+ */
+void still_debug_set_wait_limit(long long cycles);
+
 /* Synchronise `stream` and read a device status word (the one in a decode
  * state, or the first int32 of a prefill workspace). */
 still_status still_read_status(const int32_t *status_word, still_stream_t stream, int32_t *host_value);

@@ -1,4 +1,5 @@
 // C ABI of libstill: argument checks, workspace plan, launch order, timing.
+#include <atomic>
 #include <cstdio>
 #include <cstring>
 #include <mutex>
@@ -56,6 +57,16 @@ void timing_end(cudaStream_t s)
 }
 
 size_t decode_smem_bytes(const Dims &dm);
+
+namespace {
+std::atomic<long long> g_consumer_wait_limit{0};   // 0: WAIT_LIMIT_CYCLES
+}
+
+long long consumer_wait_limit()
+{
+    const long long v = g_consumer_wait_limit.load();
+    return v > 0 ? v : WAIT_LIMIT_CYCLES;
+}
 
 }  // namespace still
 
@@ -239,6 +250,18 @@ still_status still_npmap(const still_bf16 *x, long long rows, int d, const float
     return cuda_status(launch_npmap(x, rows, d, Wf, d_f, phi, (cudaStream_t)stream));
 }
 
+}  // extern "C"
+
+namespace still {
+still_status check_prefill_sizes(const still_shape *shape, int W, int C, int m, int T_max)
+{
+    Dims dm;
+    return make_dims(shape, W, C, m, T_max, &dm);
+}
+}  // namespace still
+
+extern "C" {
+
 size_t still_prefill_workspace_size(const still_shape *shape, int W, int C, int m, int T_max)
 {
     Dims dm;
@@ -294,6 +317,12 @@ still_status prefill_impl(const still_shape *shape, const still_bf16 *q, const s
     uint16_t *wft = (uint16_t *)(base + L.wft);
     float *dS = (float *)(base + L.dS);
     float *dz = (float *)(base + L.dz);
+    // the status word starts at zero before any kernel of this call can write it
+    cudaError_t e0 = cudaMemsetAsync(status, 0, 4, s);
+    if (e0 != cudaSuccess) {
+        if (!workspace) cudaFreeAsync(ws, s);
+        return cuda_status(e0);
+    }
     const bool tc = hybrid_tc_supported(dm);
     // the set-up pass rides on the tensor-core score kernel when that one runs
     const bool fused_prep = dm.lam > 0 && score_tc_supported(dm) && metric == STILL_METRIC_SELF_SALIENCY;
@@ -415,6 +444,8 @@ still_status still_read_status(const int32_t *status_word, still_stream_t stream
     if (e == cudaSuccess) e = cudaStreamSynchronize((cudaStream_t)stream);
     return cuda_status(e);
 }
+
+void still_debug_set_wait_limit(long long cycles) { g_consumer_wait_limit.store(cycles > 0 ? cycles : 0); }
 
 void still_timing_enable(int on)
 {

@@ -90,6 +90,15 @@ __device__ __forceinline__ void set_status(int32_t *status, int code)
     if (status) atomicCAS(status, 0, code);
 }
 
+// Bounded device-side waits: clock cycles a wait may spin before it gives up
+// (about 2 s at the GB300's 2.07 GHz), setting STILL_ERR_TIMEOUT.
+constexpr long long WAIT_LIMIT_CYCLES = 4000000000LL;
+
+// Limit of the consumer-side waits (row warps waiting for a copy or an MMA) of
+// the tensor-core prefill kernels: WAIT_LIMIT_CYCLES unless a test lowered it
+// with still_debug_set_wait_limit (api.cu).
+long long consumer_wait_limit();
+
 // Self-Saliency score from the window's softmax statistics: oth = sum of
 // e^{s-M} over the window without the token itself, self = e^{s_tt - M}.
 // -log(1 - p + eps) is taken through log1p while p is small, so that small
@@ -175,6 +184,10 @@ struct KTimer {
     KTimer(const char *name, cudaStream_t st) : s(st) { timing_begin(name, st); }
     ~KTimer() { timing_end(s); }
 };
+
+// The status still_prefill returns for these sizes and routing parameters
+// before it looks at any pointer (STILL_OK when they are valid).
+still_status check_prefill_sizes(const still_shape *shape, int W, int C, int m, int T_max);
 
 // ---- launchers (one per kernel family) ----------------------------------------
 // diag = 1: the mean self probability p_t (the diagonal-attention routing metric)

@@ -57,8 +57,10 @@ still_status still_prefill_noalloc(const still_shape *shape, const still_bf16 *q
                                    still_bf16 *out, int32_t *sel_idx, const still_decode_state *export_state,
                                    still_stream_t stream)
 {
+    // sizes or a budget still_prefill refuses are refused with the same status
+    const still_status chk = still::check_prefill_sizes(shape, W, C, m, T_max);
+    if (chk != STILL_OK) return chk;
     const size_t need = still_prefill_workspace_size(shape, W, C, m, T_max);
-    if (need == 0) return STILL_ERR_INVALID_ARG;          // the shape or budget itself is invalid
     if (need > STILL_NOALLOC_SCRATCH_BYTES) {
         fprintf(stderr,
                 "libstill: still_prefill_noalloc needs %zu bytes of scratch for this size, more than its fixed "

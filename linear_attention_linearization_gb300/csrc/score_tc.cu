@@ -42,7 +42,12 @@ struct ScoreTCParams {
     // status word = 0, slot map = -1, kept tables = 0, W_f^T in bf16
     const float *Wf;
     uint16_t *wft;
-    int32_t *status, *kslot;
+    int32_t *kslot;
+    // device status word (nullable): a bounded wait that gives up writes
+    // STILL_ERR_TIMEOUT here; the row warps' waits give up after
+    // row_wait_limit cycles, the issuing thread's after WAIT_LIMIT_CYCLES
+    int32_t *status;
+    long long row_wait_limit;
     size_t nkslot, nkept16;
     uint4 *kept;
 };
@@ -57,13 +62,12 @@ __global__ void __launch_bounds__(SC_THREADS, 1) score_tc_kernel(const __grid_co
 {
     constexpr int CBD = D / 64;
     constexpr uint32_t QB = CBD * 16384;          // Q tile bytes
-    constexpr long long WAIT_LIMIT = 4000000000LL;   // cycles
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     const uint32_t sb = smem_u32(sm);
     // full: a stage's Q and K arrived; mma: its logits are in TMEM (and its
     // shared memory is free); tfree: the rows have read its TMEM columns
-    __shared__ uint64_t bar_full[SC_MAX_STAGES], bar_mma[SC_MAX_STAGES], bar_tfree[SC_MAX_STAGES];
+    __shared__ uint64_t bar_full[SC_MAX_STAGES], bar_mma[SC_MAX_STAGES], bar_tfree[SC_MAX_STAGES], bar_drain;
     __shared__ uint32_t tmem_base;
     __shared__ float hsc[SC_GROUPS][2][4 * 32];   // per group, two tiles: head scores by (head, token)
     __shared__ int s_abort;
@@ -85,6 +89,7 @@ __global__ void __launch_bounds__(SC_THREADS, 1) score_tc_kernel(const __grid_co
             mbar_init(&bar_mma[i], 1);
             mbar_init(&bar_tfree[i], SC_ROWS / SC_GROUPS);
         }
+        mbar_init(&bar_drain, 1);
         fence_barrier_init();
         s_abort = 0;
     }
@@ -102,7 +107,6 @@ __global__ void __launch_bounds__(SC_THREADS, 1) score_tc_kernel(const __grid_co
     grid_dep_sync();   // the previous kernel's writes are visible from here on
     if (P.kslot) {
         const size_t gt = (size_t)blockIdx.x * SC_THREADS + tid, nt = (size_t)gridDim.x * SC_THREADS;
-        if (gt == 0) *P.status = 0;
         for (size_t i = gt; i < P.nkslot / 4; i += nt) reinterpret_cast<int4 *>(P.kslot)[i] = make_int4(-1, -1, -1, -1);
         for (size_t i = P.nkslot / 4 * 4 + gt; i < P.nkslot; i += nt) P.kslot[i] = -1;
         for (size_t i = gt; i < P.nkept16; i += nt) P.kept[i] = make_uint4(0, 0, 0, 0);
@@ -112,12 +116,14 @@ __global__ void __launch_bounds__(SC_THREADS, 1) score_tc_kernel(const __grid_co
         }
     }
 
-    auto wait = [&](uint64_t *bar, uint32_t parity) -> bool {
+    // bounded wait; gives up early once another thread has given up
+    auto wait = [&](uint64_t *bar, uint32_t parity, long long limit) -> bool {
         if (mbar_try_wait(bar, parity)) return true;
         const long long c0 = clock64();
         while (!mbar_try_wait(bar, parity)) {
             if (*(volatile int *)&s_abort) return false;
-            if (clock64() - c0 > WAIT_LIMIT) {
+            if (clock64() - c0 > limit) {
+                set_status(P.status, STILL_ERR_TIMEOUT);
                 *(volatile int *)&s_abort = 1;
                 return false;
             }
@@ -150,14 +156,18 @@ __global__ void __launch_bounds__(SC_THREADS, 1) score_tc_kernel(const __grid_co
                 }
             };
             uint32_t ph_full = 0, ph_mma = 0, ph_tf = 0;   // one parity bit per stage
+            int loaded = 0, arrived = 0;                  // tiles whose copies were issued / waited for
             bool ok = true;
-            for (int i = 0; i < NS && i < my_tiles; ++i) issue_load(i);
+            for (int i = 0; i < NS && i < my_tiles; ++i, ++loaded) issue_load(i);
             for (int i = 0; i < my_tiles && ok; ++i) {
                 const int st = i % NS;
-                ok &= wait(&bar_full[st], (ph_full >> st) & 1u);
+                ok &= wait(&bar_full[st], (ph_full >> st) & 1u, WAIT_LIMIT_CYCLES);
+                if (!ok) break;
+                ++arrived;
                 ph_full ^= 1u << st;
                 if (i >= NS) {   // the rows are done with tile i - NS in this TMEM stage
-                    ok &= wait(&bar_tfree[st], (ph_tf >> st) & 1u);
+                    ok &= wait(&bar_tfree[st], (ph_tf >> st) & 1u, WAIT_LIMIT_CYCLES);
+                    if (!ok) break;
                     ph_tf ^= 1u << st;
                 }
                 tc_fence_after();
@@ -169,11 +179,19 @@ __global__ void __launch_bounds__(SC_THREADS, 1) score_tc_kernel(const __grid_co
                 mma_commit(&bar_mma[st]);
                 if (i + NS < my_tiles) {
                     // the stage's shared memory is free once this MMA has read it
-                    ok &= wait(&bar_mma[st], (ph_mma >> st) & 1u);
+                    ok &= wait(&bar_mma[st], (ph_mma >> st) & 1u, WAIT_LIMIT_CYCLES);
+                    if (!ok) break;
                     issue_load(i + NS);
+                    ++loaded;
                 }
                 ph_mma ^= 1u << st;
             }
+            // Every MMA and copy this thread issued completes before the block's shared and
+            // tensor memory are released, also when the block gave up (these waits ignore the
+            // abort flag; on the normal path they find everything complete).
+            mma_commit(&bar_drain);
+            mbar_wait(&bar_drain, 0, P.status);
+            for (int j = arrived; j < loaded; ++j) mbar_wait(&bar_full[j % NS], (uint32_t)(j / NS) & 1u, P.status);
         }
         __syncwarp();
     } else {
@@ -194,7 +212,7 @@ __global__ void __launch_bounds__(SC_THREADS, 1) score_tc_kernel(const __grid_co
             tile_coords(i, unit, t0);
             // the k-th use of a stage completes phase k of its barrier; this group
             // has seen tile i - 2 complete, so every earlier use of the stage has too
-            bool bad = !wait(&bar_mma[st], (uint32_t)(i / NS) & 1u);
+            bool bad = !wait(&bar_mma[st], (uint32_t)(i / NS) & 1u, P.row_wait_limit);
             tc_fence_after();
             float v[BC];
 #pragma unroll
@@ -279,6 +297,7 @@ cudaError_t launch_score_tc(const Dims &dm, const uint16_t *q, const uint16_t *k
     p.Wf = prep ? prep->Wf : nullptr;
     p.wft = prep ? prep->wft : nullptr;
     p.status = prep ? prep->status : nullptr;
+    p.row_wait_limit = consumer_wait_limit();
     p.kslot = prep ? prep->kslot : nullptr;
     p.nkslot = prep ? (size_t)dm.B * dm.Hkv * dm.N : 0;
     p.kept = prep ? reinterpret_cast<uint4 *>(prep->kept) : nullptr;

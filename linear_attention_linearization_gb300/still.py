@@ -74,6 +74,7 @@ SIGNATURES = {
                                      ct.c_void_p, ct.c_void_p, ct.c_int, ct.c_int, ct.c_int, ct.c_int,
                                      ct.c_void_p, ct.c_void_p]),
     "still_read_status": (ct.c_int, [ct.c_void_p, ct.c_void_p, ct.POINTER(ct.c_int32)]),
+    "still_debug_set_wait_limit": (None, [ct.c_longlong]),
     "still_timing_enable": (None, [ct.c_int]),
     "still_timing_read": (ct.c_int, [ct.POINTER(KernelTime), ct.c_int]),
 }
@@ -282,6 +283,21 @@ def prefill_noalloc(q, k, v, Wf, W, C, m, T_max, out=None, sel_idx=None, export_
                                        _ptr(sel_idx, torch.int32, "sel_idx") if sel_idx.numel() else None,
                                        st, _stream(stream)), "still_prefill_noalloc")
     return out, sel_idx
+
+
+def workspace_status(workspace, stream=None):
+    """The device status word of a prefill (the first int32 of its workspace),
+    read after synchronising `stream`: 0, or the still_status a kernel found."""
+    val = ct.c_int32(0)
+    _check(lib().still_read_status(ct.c_void_p(_ptr(workspace, torch.uint8, "workspace")), _stream(stream),
+                                   ct.byref(val)), "still_read_status")
+    return int(val.value)
+
+
+def debug_set_wait_limit(cycles):
+    """Wait limit (clock cycles) of the prefill kernels' row-side waits; 0 restores
+    the default.  For tests of the timeout path only."""
+    lib().still_debug_set_wait_limit(int(cycles))
 
 
 def decode_state_init(state: DecodeState, Hq, W, C, m, T_max, stream=None):

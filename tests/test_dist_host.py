@@ -92,7 +92,8 @@ def test_cpu_baseline_reports_all_cores_and_one_core():
     from linear_attention_linearization_gb300 import inputs
     w = inputs.Workload("case", 2, 4, 2, 16, 96, 8, 16, 8 + 2 * 6, 6, 16)
     q, k, v, Wf = inputs.make_inputs(w, seed=1)
-    r = bench.cpu_baseline(q, k, v, Wf, w, 64)
+    r, keep, thr = bench.cpu_baseline(q, k, v, Wf, w, 64)
+    assert keep["y"].shape == (w.B, w.Hq, 64, w.d) and thr == r["cores"]
     assert r["kind"] == "oracle" and r["unit"] == "tokens/s" and r["value"] > 0
     assert 1 <= r["cores"] <= w.B * w.Hkv and r["seconds"] > 0
     one = r["one_core"]
@@ -109,3 +110,33 @@ def test_cpu_decode_baseline_runs_the_oracle_decode_step():
     assert r["kind"] == "oracle" and r["unit"] == "tokens/s" and r["value"] > 0 and r["ms_per_step"] > 0
     assert 1 <= r["cores"] <= w.Hkv
     json.dumps(r)
+
+
+def test_parity_object_of_the_bench_line():
+    """The bench's parity check on the host: the oracle's own output rounded to
+    bf16 and its own selection pass; a selection changed outside a near tie is
+    flagged, and a perturbed output shows its relative error."""
+    sys.path.insert(0, ROOT)
+    import numpy as np
+    import torch
+    import bench
+    from linear_attention_linearization_gb300 import inputs
+    from oracle import brute
+    w = inputs.Workload("case", 1, 4, 2, 16, 96, 8, 16, 8 + 2 * 6, 6, 16)
+    q, k, v, Wf = inputs.make_inputs(w, seed=2)
+    keep = {}
+    bench.oracle_sample(q, k, v, Wf, w, w.N, 1, keep)
+    out = torch.from_numpy(keep["y"]).to(torch.bfloat16)
+    sel = torch.from_numpy(np.stack([brute.select(keep["scores"][b], w.C, w.lam, w.T_max)
+                                     for b in range(w.B)]).astype(np.int32))
+    p = bench.parity_vs_oracle(out, sel, w, w.N, keep, 1)
+    assert p["within_tolerance"] and p["max_err_rel"] < 2 ** -8 and p["sel_exact_outside_ties"]
+    assert p["sel_differs_in_near_ties"] == 0
+    bad = sel.clone()
+    bad[0, 0, 0, 0] = next(x for x in range(w.C) if x not in sel[0, 0, 0].tolist())
+    p = bench.parity_vs_oracle(out, bad, w, w.N, keep, 1)
+    assert not p["sel_exact_outside_ties"]
+    out2 = out.clone()
+    out2[0, 1, 50, 3] += 0.5 * float(np.abs(keep["y"]).max())
+    p = bench.parity_vs_oracle(out2, sel, w, w.N, keep, 1)
+    assert 0.45 < p["max_err_rel"] < 0.55 and not p["within_tolerance"]

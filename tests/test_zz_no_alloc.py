@@ -5,8 +5,11 @@ whose execution step must not allocate, latency-critical code); for them the
 library offers the prefill with its scratch in a fixed array of its own.  This
 file checks, through the C ABI, that it gives the same result as still_prefill
 with a caller workspace on two calls in a row, and that sizes needing more
-scratch than the array holds are refused without launching anything.  It is
-named so that pytest collects it last.
+scratch than the array holds are refused without launching anything, that
+sizes still_prefill refuses are refused with the same status, and that the
+call takes nothing from the device's stream-ordered memory pool (the one a
+workspace-less still_prefill draws from).  It is named so that pytest collects
+it last.
 """
 import ctypes as ct
 
@@ -30,6 +33,32 @@ def still(cuda_ok):
     return s
 
 
+class _PoolProbe:
+    """High-water mark of the memory pool cudaMallocAsync uses on the current
+    device (CUDA driver API: CU_MEMPOOL_ATTR_USED_MEM_HIGH / _CURRENT)."""
+    USED_CURRENT, USED_HIGH = 7, 8
+
+    def __init__(self):
+        self.cu = ct.CDLL("libcuda.so.1")
+        dev = ct.c_int(0)
+        assert self.cu.cuCtxGetDevice(ct.byref(dev)) == 0
+        self.pool = ct.c_void_p()
+        assert self.cu.cuDeviceGetMemPool(ct.byref(self.pool), dev) == 0
+
+    def _get(self, attr):
+        v = ct.c_uint64(0)
+        assert self.cu.cuMemPoolGetAttribute(self.pool, attr, ct.byref(v)) == 0
+        return v.value
+
+    def reset(self):
+        zero = ct.c_uint64(0)
+        assert self.cu.cuMemPoolSetAttribute(self.pool, self.USED_HIGH, ct.byref(zero)) == 0
+        return self._get(self.USED_CURRENT)
+
+    def high(self):
+        return self._get(self.USED_HIGH)
+
+
 @pytest.mark.parametrize("name", ["tiny_prefill_n512", "llama32_1b_layer_prefill_4k"])
 def test_noalloc_matches_prefill_twice(still, name):
     w = inputs.WORKLOADS[name]
@@ -40,8 +69,13 @@ def test_noalloc_matches_prefill_twice(still, name):
         assert still.workspace_size(q, k, Wf, w.W, w.C, w.m, w.T_max) <= still.lib().still_prefill_noalloc_max_bytes()
         ws = torch.empty(still.workspace_size(q, k, Wf, w.W, w.C, w.m, w.T_max), dtype=torch.uint8, device=dev)
         ref_out, ref_sel = still.prefill(q, k, v, Wf, w.W, w.C, w.m, w.T_max, workspace=ws)
-        out, sel = still.prefill_noalloc(q, k, v, Wf, w.W, w.C, w.m, w.T_max)
+        out, sel = torch.empty_like(ref_out), torch.empty_like(ref_sel)
         torch.cuda.synchronize()
+        probe = _PoolProbe()
+        base = probe.reset()
+        still.prefill_noalloc(q, k, v, Wf, w.W, w.C, w.m, w.T_max, out=out, sel_idx=sel)
+        torch.cuda.synchronize()
+        assert probe.high() == base, "still_prefill_noalloc took memory from the stream-ordered pool"
         a, b = to_f64(out), to_f64(ref_out)
         assert np.abs(a - b).max() <= OUT_TOL * np.abs(b).max()
         assert torch.equal(sel.cpu(), ref_sel.cpu())
@@ -54,3 +88,24 @@ def test_noalloc_refuses_sizes_beyond_its_array(still):
     p = ct.c_void_p(256)                                          # never dereferenced: refused on the host
     rc = still.lib().still_prefill_noalloc(ct.byref(sh), p, p, p, p, w.W, w.C, w.m, w.T_max, p, None, None, None)
     assert rc == 6                                                # STILL_ERR_WORKSPACE
+
+
+def test_noalloc_refuses_what_prefill_refuses(still):
+    """d outside {64, 128}: both entry points answer STILL_ERR_UNSUPPORTED."""
+    sh = still.Shape(1, 2, 2, 64, 96, 96)
+    p = ct.c_void_p(256)                                          # never dereferenced: refused on the host
+    assert still.lib().still_prefill(ct.byref(sh), p, p, p, p, 8, 8, 16, 1, p, None, None, 0, None, None) == 2
+    assert still.lib().still_prefill_noalloc(ct.byref(sh), p, p, p, p, 8, 8, 16, 1, p, None, None, None) == 2
+
+
+def test_pool_probe_sees_a_workspace_allocation(still):
+    """The probe above is live: a still_prefill without a workspace takes its
+    workspace from that pool, and the high-water mark shows it."""
+    w = inputs.WORKLOADS["tiny_prefill_n512"]
+    q, k, v, Wf = (t.to("cuda") for t in inputs.make_inputs(w, seed=23))
+    torch.cuda.synchronize()
+    probe = _PoolProbe()
+    base = probe.reset()
+    still.prefill(q, k, v, Wf, w.W, w.C, w.m, w.T_max)
+    torch.cuda.synchronize()
+    assert probe.high() >= base + still.workspace_size(q, k, Wf, w.W, w.C, w.m, w.T_max)
