@@ -116,11 +116,14 @@ __global__ void __launch_bounds__(SC_THREADS, 1) score_tc_kernel(const __grid_co
         }
     }
 
-    // bounded wait; gives up early once another thread has given up
+    // bounded wait; gives up early once another thread has given up.  A limit
+    // below the default (a test of this path) polls without the suspension
+    // mbarrier.try_wait may take, so that the clock limit is what decides.
     auto wait = [&](uint64_t *bar, uint32_t parity, long long limit) -> bool {
-        if (mbar_try_wait(bar, parity)) return true;
+        const bool poll = limit < WAIT_LIMIT_CYCLES;
+        if (poll ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity)) return true;
         const long long c0 = clock64();
-        while (!mbar_try_wait(bar, parity)) {
+        while (!(poll ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity))) {
             if (*(volatile int *)&s_abort) return false;
             if (clock64() - c0 > limit) {
                 set_status(P.status, STILL_ERR_TIMEOUT);

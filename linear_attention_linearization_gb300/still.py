@@ -289,8 +289,8 @@ def workspace_status(workspace, stream=None):
     """The device status word of a prefill (the first int32 of its workspace),
     read after synchronising `stream`: 0, or the still_status a kernel found."""
     val = ct.c_int32(0)
-    _check(lib().still_read_status(ct.c_void_p(_ptr(workspace, torch.uint8, "workspace")), _stream(stream),
-                                   ct.byref(val)), "still_read_status")
+    _check(lib().still_read_status(_ptr(workspace, torch.uint8, "workspace"), _stream(stream), ct.byref(val)),
+           "still_read_status")
     return int(val.value)
 
 

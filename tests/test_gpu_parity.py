@@ -20,7 +20,7 @@ pytestmark = pytest.mark.gpu
 
 OUT_TOL = 1e-2
 DEV = "cuda"
-U_BF16 = 2.0 ** -9      # unit roundoff of bf16 (8 significant bits, round to nearest)
+U_BF16 = 2.0 ** -8      # unit roundoff of bf16: 8 significant bits, round to nearest
 U_F32 = 2.0 ** -24
 
 
@@ -244,8 +244,9 @@ def state_tolerance(kg, vg, Wf, folded, pre_folded):
       is computed exactly here: phi~ = the oracle's NP-Map fed bf16(Wf), and
       |S~ - S_ref| with S~ = sum phi~ v^T is part of the bound.  The bf16
       rounding of each phi~ element is an independent error of at most
-      u = 2^-9 relative (uniform, variance (u phi~)^2 / 3); their sum over the
-      folded keys is bounded by 6 standard deviations.
+      u = 2^-8 relative (half an ulp of 8 significant bits; uniform, variance
+      at most (u phi~)^2 / 3); their sum over the folded keys is bounded by 6
+      standard deviations.
     * keys folded by the decode step use fp32 features from the fp32 Wf.
     * fp32 accumulation of the sums: 8 u32 sqrt(n) max|S|.
     Returns (tol_S [d_f, d], tol_z [d_f], S_model, z_model) where the model
