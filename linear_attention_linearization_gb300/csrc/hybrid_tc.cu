@@ -50,6 +50,7 @@ struct TCParams {
     const float *dS;
     const float *dz;
     int32_t *status;
+    long long row_wait_limit;   // limit of the row warps' waits (the issuing thread's: WAIT_LIMIT_CYCLES)
 };
 
 // q and out: boxes of 32 tokens x 64 columns x G heads.  kband / vband: the
@@ -60,13 +61,14 @@ struct TCMaps {
     CUtensorMap q, out, kband, vband, kk32, kk64, kk128, vk32, vk64, vk128, v, vk16, phik, phk16, wft;
 };
 
-// logits (and, once P V is done, dS at 0 and dz at TM_DZ), row exchange (NP-Map
-// statistics at TM_X, row maxima and denominator shares at TM_X2), O, A
-constexpr int TM_S = 0, TM_DZ = 256, TM_X = 288, TM_X2 = 304, TM_O = 320, TM_A = 448, TM_COLS = 512;
-constexpr int MAX_KEY_BLOCKS = 9;    // 288 logit columns: every block of a tile stays resident
+// logits (and, once P V is done, dS at 0 and dz at TM_DZ), O, A, row exchange:
+// the NP-Map statistics at TM_X share the A columns (they are read before the
+// A MMA is issued), row maxima and denominator shares at TM_X2
+constexpr int TM_S = 0, TM_DZ = 256, TM_O = 320, TM_A = 448, TM_X = 448, TM_X2 = 496, TM_COLS = 512;
+constexpr int MAX_KEY_BLOCKS = 10;   // 320 logit columns: every block of a tile stays resident
 constexpr int NX = 16;               // extra (kept, own chunk) rows per tile
 
-constexpr int RING_SLOTS = 9;        // K (then V) blocks of 32 keys resident
+constexpr int RING_SLOTS = 9;        // K (then V) blocks of 32 keys resident; more come in a second batch
 
 template <int D, int DF>
 struct TCLayout {
@@ -104,7 +106,6 @@ __global__ void __launch_bounds__(HT_THREADS, 1) hybrid_tc_kernel(const __grid_c
     constexpr float LOG2E = 1.4426950408889634f;
     constexpr uint32_t SLOT = CBD * 4096;     // bytes of one ring slot (32 keys x D)
     constexpr uint32_t RSTRIDE = Lay::RSTRIDE;
-    constexpr long long WAIT_LIMIT = 4000000000LL;   // cycles
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     const uint32_t sb = smem_u32(sm);
@@ -115,6 +116,7 @@ __global__ void __launch_bounds__(HT_THREADS, 1) hybrid_tc_kernel(const __grid_c
     // phi(Q) written, A masked, P written, tile finished (O and dS read,
     // output staged, S_run updated); issuer -> rows: output staging free
     __shared__ uint64_t bar_q, bar_wf, bar_lag, bar_u, bar_s, bar_a, bar_o, bar_ds, bar_k, bar_v;
+    __shared__ uint64_t bar_s1, bar_pv1, bar_drain;   // the issuer's own: first-batch S and P V, the drain
     __shared__ uint64_t rdy_phiq, rdy_a, rdy_p1, rdy_p, rdy_epi, stg_free;
     __shared__ uint32_t tmem_base;
     __shared__ int s_abort;
@@ -133,7 +135,8 @@ __global__ void __launch_bounds__(HT_THREADS, 1) hybrid_tc_kernel(const __grid_c
         tmem_relinquish();
     }
     if (tid == 0) {
-        for (uint64_t *bb : {&bar_q, &bar_wf, &bar_lag, &bar_u, &bar_s, &bar_a, &bar_o, &bar_ds, &bar_k, &bar_v, &stg_free})
+        for (uint64_t *bb : {&bar_q, &bar_wf, &bar_lag, &bar_u, &bar_s, &bar_a, &bar_o, &bar_ds, &bar_k, &bar_v, &stg_free,
+                             &bar_s1, &bar_pv1, &bar_drain})
             mbar_init(bb, 1);
         for (uint64_t *bb : {&rdy_phiq, &rdy_a, &rdy_p1, &rdy_p, &rdy_epi}) mbar_init(bb, HT_ROWS);
         fence_barrier_init();
@@ -156,13 +159,19 @@ __global__ void __launch_bounds__(HT_THREADS, 1) hybrid_tc_kernel(const __grid_c
     const uint32_t tmem = tmem_base;
     grid_dep_sync();   // the previous kernel's writes are visible from here on
 
-    // bounded wait; gives up early once the other side has given up
+    // bounded wait; gives up early once the other side has given up.  The row
+    // warps wait at most P.row_wait_limit cycles, the issuing thread
+    // WAIT_LIMIT_CYCLES; a limit below the default (a test of this path) polls
+    // without the suspension mbarrier.try_wait may take.
+    const bool is_row = warp < HT_ROWS / 32;
+    const long long limit = is_row ? P.row_wait_limit : WAIT_LIMIT_CYCLES;
+    const bool poll = limit < WAIT_LIMIT_CYCLES;
     auto wait = [&](uint64_t *bar, uint32_t parity) -> bool {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (poll ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity)) return true;
         const long long c0 = clock64();
-        while (!mbar_try_wait(bar, parity)) {
+        while (!(poll ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity))) {
             if (*(volatile int *)&s_abort) return false;
-            if (clock64() - c0 > WAIT_LIMIT) {
+            if (clock64() - c0 > limit) {
                 set_status(P.status, STILL_ERR_TIMEOUT);
                 *(volatile int *)&s_abort = 1;
                 return false;
@@ -175,7 +184,9 @@ __global__ void __launch_bounds__(HT_THREADS, 1) hybrid_tc_kernel(const __grid_c
         // ======================== the issuing warpgroup =========================
         regs_dec<HT_ISSUE_REGS>();
         if (warp == HT_ROWS / 32 && lane == 0 && ntiles > 0) {
+            int loads_q = 0, loads_lag = 0;   // copies issued per barrier (for the drain)
             auto load_q = [&](int t0) {
+                ++loads_q;
                 mbar_expect_tx(&bar_q, dm.G * CBD * 4096);
                 for (int cb = 0; cb < CBD; ++cb)
                     tma_load_3d(sm + Lay::Q + cb * 16384, &maps.q, &bar_q, cb * 64, t0, b * dm.Hq + g * dm.G);
@@ -183,6 +194,7 @@ __global__ void __launch_bounds__(HT_THREADS, 1) hybrid_tc_kernel(const __grid_c
             auto load_lag = [&](int t0) {
                 const int ct = t0 / C;
                 const int xrow = ct < dm.T_max ? ct * lam : P.KP;   // past the table: zero fill
+                ++loads_lag;
                 mbar_expect_tx(&bar_lag, CBF * (4096 + 2048) + CBD * (4096 + 2048));
                 for (int cb = 0; cb < CBF; ++cb) {
                     tma_load_3d(sm + Lay::PHIK + cb * 6144, &maps.phik, &bar_lag, cb * 64, t0 - W, unit);
@@ -193,20 +205,23 @@ __global__ void __launch_bounds__(HT_THREADS, 1) hybrid_tc_kernel(const __grid_c
                     tma_load_3d(sm + Lay::VLAG + cb * 6144 + 4096, &maps.vk16, &bar_lag, cb * 64, xrow, unit);
                 }
             };
-            // the key blocks of the tile at t0 into ring slots 0 .. nkb-1: K (kv = 0) or V (kv = 1);
-            // the band in one box per column block, the kept prefix in boxes of 4, 2 and 1 blocks
-            auto load_keys = [&](int t0, int nkb, int kv) {
+            // key blocks [k0, k1) of the tile at t0 into ring slots 0 .. k1-k0-1: K (kv = 0) or
+            // V (kv = 1); the band (blocks below nb, first batch only) in one box per column
+            // block, the kept prefix in boxes of 4, 2 and 1 blocks
+            int loads_k = 0, loads_v = 0;   // copies issued per barrier (for the drain)
+            auto load_keys = [&](int t0, int k0, int k1, int kv) {
                 uint64_t *bar = kv ? &bar_v : &bar_k;
-                mbar_expect_tx(bar, nkb * SLOT);
+                ++(kv ? loads_v : loads_k);
+                mbar_expect_tx(bar, (k1 - k0) * SLOT);
                 for (int cb = 0; cb < CBD; ++cb) {
                     uint8_t *dst = sm + Lay::RING + cb * RSTRIDE;
-                    tma_load_3d(dst, kv ? &maps.vband : &maps.kband, bar, cb * 64, t0 - P.Wr, unit);
-                    int kb = P.nb;
-                    while (kb < nkb) {
-                        const int n = nkb - kb >= 4 ? 4 : (nkb - kb >= 2 ? 2 : 1);
+                    if (k0 == 0) tma_load_3d(dst, kv ? &maps.vband : &maps.kband, bar, cb * 64, t0 - P.Wr, unit);
+                    int kb = max(k0, P.nb);
+                    while (kb < k1) {
+                        const int n = k1 - kb >= 4 ? 4 : (k1 - kb >= 2 ? 2 : 1);
                         const CUtensorMap *mp = n == 4 ? (kv ? &maps.vk128 : &maps.kk128)
                                               : n == 2 ? (kv ? &maps.vk64 : &maps.kk64) : (kv ? &maps.vk32 : &maps.kk32);
-                        tma_load_3d(dst + kb * 4096, mp, bar, cb * 64, 32 * (kb - P.nb), unit);
+                        tma_load_3d(dst + (kb - k0) * 4096, mp, bar, cb * 64, 32 * (kb - P.nb), unit);
                         kb += n;
                     }
                 }
@@ -240,25 +255,27 @@ __global__ void __launch_bounds__(HT_THREADS, 1) hybrid_tc_kernel(const __grid_c
             for (int cb = 0; cb < CBD; ++cb) tma_load_2d(sm + Lay::WF + cb * DF * 128, &maps.wft, &bar_wf, cb * 64, 0);
             load_q(tbeg);
             load_lag(tbeg);
-            load_keys(tbeg, nkb_of(tbeg), 0);
+            load_keys(tbeg, 0, min(nkb_of(tbeg), RING_SLOTS), 0);
             mbar_arrive(&stg_free);   // the staging buffer starts free
             bool ok = wait(&bar_wf, 0);
+            uint32_t ph_s1 = 0, ph_pv1 = 0;
 
             for (int it = 0; it < ntiles && ok; ++it) {
                 const int t0 = tbeg + it * 32;
                 const int nkb = nkb_of(t0);
+                const int B1 = min(nkb, RING_SLOTS);   // blocks of the first batch through the ring
                 const bool has_next = it + 1 < ntiles;
                 if (it > 0) {
                     // the rows are done with the previous tile (O and dS read, output staged)
-                    ok &= wait(&rdy_epi, pe_epi);
+                    if (!(ok = wait(&rdy_epi, pe_epi))) break;
                     pe_epi ^= 1;
                 }
                 // the previous output leaves, U = Q Wf (the rows wait on it), the staging buffer
-                // is handed back once the store has read it, then S = Q K^T: blocks 0 .. nkb-1
-                // in consecutive slots, one MMA of N = 32 min(nkb, 8) per K step and one more for
-                // a ninth slot
+                // is handed back once the store has read it, then S = Q K^T: blocks 0 .. B1-1
+                // in consecutive slots, one MMA of N = 32 min(B1, 8) per K step and one more for
+                // a ninth slot; blocks past the ring come in a second batch once these are read
                 if (it > 0) store_out(t0 - 32);
-                ok &= wait(&bar_q, ph_q);
+                if (!(ok = wait(&bar_q, ph_q))) break;
                 ph_q ^= 1;
                 tc_fence_after();
 #pragma unroll 1
@@ -269,32 +286,46 @@ __global__ void __launch_bounds__(HT_THREADS, 1) hybrid_tc_kernel(const __grid_c
                     tma_store_wait_read();
                     mbar_arrive(&stg_free);
                 }
-                ok &= wait(&bar_k, ph_k);
+                if (!(ok = wait(&bar_k, ph_k))) break;
                 ph_k ^= 1;
                 tc_fence_after();
-                const int na = nkb < 8 ? nkb : 8;
+                const int na = B1 < 8 ? B1 : 8;
                 const uint32_t id_sa = idesc_bf16(128, 32 * na, 0, 0);
 #pragma unroll 1
                 for (int k = 0; k < D; k += 16)
                     mma_ss(tmem + TM_S, dQ + koff(k, 16384), dKR + koff(k, RSTRIDE), id_sa, k > 0);
-                if (nkb > 8) {
-                    const uint32_t id_sb = idesc_bf16(128, 32 * (nkb - 8), 0, 0);
+                if (B1 > 8) {
+                    const uint32_t id_sb = idesc_bf16(128, 32 * (B1 - 8), 0, 0);
 #pragma unroll 1
                     for (int k = 0; k < D; k += 16)
                         mma_ss(tmem + TM_S + 256, dQ + koff(k, 16384), dKR + koff(k, RSTRIDE) + (uint64_t)(8 * 4096 >> 4),
                                id_sb, k > 0);
                 }
+                if (nkb > B1) {
+                    // the second batch: its K blocks replace the first batch's once those are read
+                    mma_commit(&bar_s1);
+                    if (!(ok = wait(&bar_s1, ph_s1))) break;
+                    ph_s1 ^= 1;
+                    load_keys(t0, B1, nkb, 0);
+                    if (!(ok = wait(&bar_k, ph_k))) break;
+                    ph_k ^= 1;
+                    tc_fence_after();
+                    const uint32_t id_sc = idesc_bf16(128, 32 * (nkb - B1), 0, 0);
+#pragma unroll 1
+                    for (int k = 0; k < D; k += 16)
+                        mma_ss(tmem + TM_S + 32 * B1, dQ + koff(k, 16384), dKR + koff(k, RSTRIDE), id_sc, k > 0);
+                }
                 mma_commit(&bar_s);
                 if (it > 0) load_lag(t0);   // the previous tile's A, dS and z_run are done with it
-                // S complete: the ring takes this tile's V blocks
-                ok &= wait(&bar_s, ph_s);
+                // S complete: the ring takes this tile's V blocks (the first batch)
+                if (!(ok = wait(&bar_s, ph_s))) break;
                 ph_s ^= 1;
-                load_keys(t0, nkb, 1);
+                load_keys(t0, 0, B1, 1);
                 // phi(Q) written (and every row has read Q): A, O = phi(Q) S_run; the next Q
-                ok &= wait(&rdy_phiq, pe_phiq);
+                if (!(ok = wait(&rdy_phiq, pe_phiq))) break;
                 pe_phiq ^= 1;
                 if (has_next) load_q(t0 + 32);
-                ok &= wait(&bar_lag, ph_lag);
+                if (!(ok = wait(&bar_lag, ph_lag))) break;
                 ph_lag ^= 1;
                 tc_fence_after();
                 for (int k = 0; k < DF; k += 16)
@@ -304,7 +335,7 @@ __global__ void __launch_bounds__(HT_THREADS, 1) hybrid_tc_kernel(const __grid_c
                     mma_ss(tmem + TM_O, dPQ + koff(k, 16384), dSR + (uint64_t)(k * 128 >> 4), id_o, k > 0);
                 mma_commit(&bar_a);
                 // A masked: O += A V_lagx
-                ok &= wait(&rdy_a, pe_a);
+                if (!(ok = wait(&rdy_a, pe_a))) break;
                 pe_a ^= 1;
                 tc_fence_after();
                 // packed lag pairs in columns 0 .. 15 of A, packed extras in 32 .. 39 (each half
@@ -313,26 +344,35 @@ __global__ void __launch_bounds__(HT_THREADS, 1) hybrid_tc_kernel(const __grid_c
                 for (int kk = 0; kk < 32 + NX; kk += 16)
                     mma_ts(tmem + TM_O, tmem + TM_A + (kk < 32 ? kk / 2 : kk), dVL + (uint64_t)(kk * 128 >> 4), id_o, 1);
                 // P written, first the blocks below the split, then the rest: O += sum_kb P_kb V_kb
+                // (blocks of the second batch once the first batch's V has been read)
                 const int split = nkb / 2;
-                ok &= wait(&bar_v, ph_v);
+                auto pv = [&](int kb, int slot) {
+                    mma_ts(tmem + TM_O, tmem + TM_S + 32 * kb, dVR + (uint64_t)(slot * 4096 >> 4), id_o, 1);
+                    mma_ts(tmem + TM_O, tmem + TM_S + 32 * kb + 16, dVR + (uint64_t)((slot * 4096 + 2048) >> 4), id_o, 1);
+                };
+                if (!(ok = wait(&bar_v, ph_v))) break;
                 ph_v ^= 1;
-                ok &= wait(&rdy_p1, pe_p1);
+                if (!(ok = wait(&rdy_p1, pe_p1))) break;
                 pe_p1 ^= 1;
                 tc_fence_after();
-                for (int kb = 0; kb < split; ++kb) {
-                    mma_ts(tmem + TM_O, tmem + TM_S + 32 * kb, dVR + (uint64_t)(kb * 4096 >> 4), id_o, 1);
-                    mma_ts(tmem + TM_O, tmem + TM_S + 32 * kb + 16, dVR + (uint64_t)((kb * 4096 + 2048) >> 4), id_o, 1);
-                }
-                ok &= wait(&rdy_p, pe_p);
+                for (int kb = 0; kb < min(split, B1); ++kb) pv(kb, kb);
+                if (!(ok = wait(&rdy_p, pe_p))) break;
                 pe_p ^= 1;
                 tc_fence_after();
-                for (int kb = split; kb < nkb; ++kb) {
-                    mma_ts(tmem + TM_O, tmem + TM_S + 32 * kb, dVR + (uint64_t)(kb * 4096 >> 4), id_o, 1);
-                    mma_ts(tmem + TM_O, tmem + TM_S + 32 * kb + 16, dVR + (uint64_t)((kb * 4096 + 2048) >> 4), id_o, 1);
+                for (int kb = min(split, B1); kb < B1; ++kb) pv(kb, kb);
+                if (nkb > B1) {
+                    mma_commit(&bar_pv1);
+                    if (!(ok = wait(&bar_pv1, ph_pv1))) break;
+                    ph_pv1 ^= 1;
+                    load_keys(t0, B1, nkb, 1);
+                    if (!(ok = wait(&bar_v, ph_v))) break;
+                    ph_v ^= 1;
+                    tc_fence_after();
+                    for (int kb = B1; kb < nkb; ++kb) pv(kb, kb - B1);
                 }
                 mma_commit(&bar_o);
                 // every read of P and of the ring is done: dS into the logit columns, the next K blocks
-                ok &= wait(&bar_o, ph_o);
+                if (!(ok = wait(&bar_o, ph_o))) break;
                 ph_o ^= 1;
                 tc_fence_after();
                 for (int kk = 0; kk < 32; kk += 16) {
@@ -341,10 +381,20 @@ __global__ void __launch_bounds__(HT_THREADS, 1) hybrid_tc_kernel(const __grid_c
                     mma_ss(tmem + TM_DZ, dphi, sdesc(sb + Lay::ONES + kk * 2, 16, 1024), id_dz, kk > 0);
                 }
                 mma_commit(&bar_ds);
-                if (has_next) load_keys(t0 + 32, nkb_of(t0 + 32), 0);
+                if (has_next) load_keys(t0 + 32, 0, min(nkb_of(t0 + 32), RING_SLOTS), 0);
             }
             if (ok && wait(&rdy_epi, pe_epi)) store_out(tbeg + (ntiles - 1) * 32);
             tma_store_wait_all();
+            // Every MMA and copy this thread issued completes before the block releases its
+            // shared and tensor memory, also when the block gave up (these waits ignore the
+            // abort flag; on the normal path they find everything complete).
+            mma_commit(&bar_drain);
+            mbar_wait(&bar_drain, 0, P.status);
+            mbar_wait(&bar_wf, 0, P.status);
+            if (loads_q > 0) mbar_wait(&bar_q, (uint32_t)(loads_q - 1) & 1u, P.status);
+            if (loads_lag > 0) mbar_wait(&bar_lag, (uint32_t)(loads_lag - 1) & 1u, P.status);
+            if (loads_k > 0) mbar_wait(&bar_k, (uint32_t)(loads_k - 1) & 1u, P.status);
+            if (loads_v > 0) mbar_wait(&bar_v, (uint32_t)(loads_v - 1) & 1u, P.status);
         }
         __syncwarp();
     } else {
@@ -789,6 +839,7 @@ cudaError_t launch_hybrid_tc(const Dims &dm, const SegPlan &sp, const TCBuffers 
     p.dS = dS;
     p.dz = dz;
     p.status = status;
+    p.row_wait_limit = consumer_wait_limit();
     dim3 grid(sp.nseg, dm.Hkv, dm.B);
     const size_t smem = hybrid_tc_smem(dm);
     cudaError_t e;

@@ -436,3 +436,23 @@ def test_prefill_repeated_calls_stable():
             torch.cuda.synchronize()
             err = np.abs(to_f64(out) - y_ref).max()
             assert err <= OUT_TOL * np.abs(y_ref).max(), (rep, w.N, err)
+
+
+@pytest.mark.parametrize("name", ["tiny_prefill_n512", "llama32_1b_layer_prefill_4k",
+                                  "llama3_8b_layer_prefill_16k", "train_b8_n1k_chunk_parallel"])
+def test_every_prefill_workload_takes_the_tensor_core_kernels(name):
+    """The kernels a workload's prefill launches, by the library's timer names:
+    the tensor-core score and attention kernels, never the CUDA-core fallbacks."""
+    w = inputs.WORKLOADS[name]
+    s = still()
+    q, k, v, Wf = (t.to(DEV) for t in inputs.make_inputs(w, seed=1))
+    s.timing_read()
+    s.timing_enable(True)
+    try:
+        s.prefill(q, k, v, Wf, w.W, w.C, w.m, w.T_max)
+        torch.cuda.synchronize()
+    finally:
+        s.timing_enable(False)
+    names = set(s.timing_read())
+    assert "hybrid_attn" in names and "hybrid_attn_general" not in names, names
+    assert "score" in names and "features_linstate" in names, names
