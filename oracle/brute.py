@@ -134,8 +134,10 @@ def route_masks(kept_g: np.ndarray, N: int, W: int, C: int):
     return sa, la
 
 
-def prefill(q, k, v, Wf, W, C, m, T_max, sel=None):
+def prefill(q, k, v, Wf, W, C, m, T_max, sel=None, gate=None):
     """Full output [Hq, N, d] of one sequence; O(N^2), tiny inputs only.
+    gate (optional [Hq, N, d]): pre-activations of the linear branch's gate,
+    y = (softmax numerator + sigmoid(gate) * linear numerator) / (both denominators).
 
     Returns (y, kv scores, sel)."""
     Hq, N, d = q.shape
@@ -157,9 +159,9 @@ def prefill(q, k, v, Wf, W, C, m, T_max, sel=None):
             c = np.where(np.isfinite(c), c, 0.0)
             e = np.where(sa, np.exp(s_sa - c), 0.0)
             a = np.where(la, npmap(q[h], Wf) @ phk.T, 0.0)
-            wgt = e + a
-            den = wgt.sum(axis=1, keepdims=True)
-            num = wgt @ v[g]
+            den = (e + a).sum(axis=1, keepdims=True)
+            g_h = 1.0 / (1.0 + np.exp(-gate[h])) if gate is not None else 1.0
+            num = e @ v[g] + g_h * (a @ v[g])
             y[h] = np.where(den != 0, num / np.where(den != 0, den, 1.0), 0.0)
     return y, scores, sel
 

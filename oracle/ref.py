@@ -54,10 +54,10 @@ def lib():
             L.oref_state_init.restype = None
             L.oref_state_init.argtypes = [ct.c_int] * 6 + [_D, _D, _I32, _I32, _D, _D, _D, _D]
             L.oref_prefill.restype = ct.c_int
-            L.oref_prefill.argtypes = ([ct.c_int] * 10 + [_D, _D, _D, _D, _I32, _D, _D]
+            L.oref_prefill.argtypes = ([ct.c_int] * 10 + [_D, _D, _D, _D, _I32, _D, _D, _D]
                                        + [_D, _D, _I32, _I32, _D, _D, _D, _D, ct.c_int])
             L.oref_decode_step.restype = ct.c_int
-            L.oref_decode_step.argtypes = ([ct.c_int] * 9 + [_I64, _D, _D, _D, _D, _D]
+            L.oref_decode_step.argtypes = ([ct.c_int] * 9 + [_I64, _D, _D, _D, _D, _D, _D]
                                            + [_D, _D, _I32, _I32, _D, _D, _D, _D, ct.c_int])
             L.oref_max_threads.restype = ct.c_int
             _lib = L
@@ -175,9 +175,13 @@ class State:
         return o
 
 
-def prefill(q, k, v, Wf, W, C, m, T_max, sel_override=None, threads=0):
-    """q [B,Hq,N,d], k,v [B,Hkv,N,d] -> (y [B,Hq,N,d], scores [B,Hkv,N], State)."""
+def prefill(q, k, v, Wf, W, C, m, T_max, sel_override=None, threads=0, gate=None):
+    """q [B,Hq,N,d], k,v [B,Hkv,N,d] -> (y [B,Hq,N,d], scores [B,Hkv,N], State).
+    gate (optional [B,Hq,N,d]): pre-activations of the linear branch's gate."""
     q, k, v, Wf = _f64(q), _f64(k), _f64(v), _f64(Wf)
+    gt = _f64(gate) if gate is not None else None
+    if gt is not None:
+        assert gt.shape == q.shape
     B, Hq, N, d = q.shape
     Hkv = k.shape[1]
     df = Wf.shape[1]
@@ -192,7 +196,8 @@ def prefill(q, k, v, Wf, W, C, m, T_max, sel_override=None, threads=0):
         ovr = np.ascontiguousarray(sel_override, dtype=np.int32)
         assert ovr.shape == (B, Hkv, T_max, lam)
     rc = lib().oref_prefill(B, Hq, Hkv, N, d, df, W, C, m, T_max, _d(q), _d(k), _d(v), _d(Wf),
-                            _i32(ovr) if ovr is not None else None, _d(y), _d(sc),
+                            _i32(ovr) if ovr is not None else None, _d(gt) if gt is not None else None,
+                            _d(y), _d(sc),
                             *st.ptrs(), int(threads))
     if rc != 0:
         raise RuntimeError(f"oracle prefill failed ({rc})")
@@ -200,15 +205,18 @@ def prefill(q, k, v, Wf, W, C, m, T_max, sel_override=None, threads=0):
     return y, sc, st
 
 
-def decode_step(st: State, q_t, k_t, v_t, Wf, W, C, m, T_max, threads=0):
-    """One token for every sequence; updates `st` in place and returns y [B,Hq,d]."""
+def decode_step(st: State, q_t, k_t, v_t, Wf, W, C, m, T_max, threads=0, gate_t=None):
+    """One token for every sequence; updates `st` in place and returns y [B,Hq,d].
+    gate_t (optional [B,Hq,d]): pre-activations of the linear branch's gate."""
     q_t, k_t, v_t, Wf = _f64(q_t), _f64(k_t), _f64(v_t), _f64(Wf)
+    gt = _f64(gate_t) if gate_t is not None else None
     B, Hq, d = q_t.shape
     Hkv = k_t.shape[1]
     df = Wf.shape[1]
     y = np.empty_like(q_t)
     rc = lib().oref_decode_step(B, Hq, Hkv, d, df, W, C, m, T_max, st.t.ctypes.data_as(_I64),
-                                _d(q_t), _d(k_t), _d(v_t), _d(Wf), _d(y), *st.ptrs(), int(threads))
+                                _d(q_t), _d(k_t), _d(v_t), _d(Wf), _d(gt) if gt is not None else None, _d(y),
+                                *st.ptrs(), int(threads))
     if rc != 0:
         raise RuntimeError(f"oracle decode step failed ({rc})")
     st.t += 1

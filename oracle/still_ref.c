@@ -32,6 +32,14 @@
  *   - One shared normalisation of both branches:
  *       y_t = (sum_SA e^{s-c} v + phi(q)^T S) / (sum_SA e^{s-c} + phi(q)^T z),
  *     c = the maximum logit over the softmax keys of the row.
+ *   - The gate of the linear branch (section "NP-Map: Norm-Preserving Feature
+ *     Map": a gating mechanism raises the rank of the linear branch; its
+ *     equation did not survive extraction).  Reading taken by this library: a
+ *     per-channel sigmoid gate on the linear branch's numerator,
+ *       y_t = (sum_SA e^{s-c} v + g_t * (phi(q)^T S)) / (sum_SA e^{s-c} + phi(q)^T z),
+ *     g_t = 1 / (1 + exp(-a_t)) elementwise over the d channels, a_t the
+ *     gate pre-activation of the query head at token t (an input of the
+ *     layer).  Without a gate (g = 1) this is the layer above.
  *
  * The implementation is the decode recurrence (one token at a time, bounded
  * m-slot cache plus (S, z)), and the prefill is that recurrence run N times
@@ -299,8 +307,8 @@ static int in_override(const prm_t *P, const int32_t *ovr, long c, long pos)
  * ovr (nullable) [T_max, lam] replaces the score ranking by a given selection.
  * Returns 0, or a negative code if an internal invariant breaks. */
 static int step_unit(const prm_t *P, unit_t *u, long t, const double *q, const double *kt,
-                     const double *vt, const double *Wf, const int32_t *ovr, double *y,
-                     double *score_out)
+                     const double *vt, const double *Wf, const int32_t *ovr, const double *gate,
+                     double *y, double *score_out)
 {
     const int W = P->W, C = P->C, lam = P->lam, d = P->d, df = P->df, G = P->G;
     const long ct = t / C;
@@ -387,6 +395,7 @@ static int step_unit(const prm_t *P, unit_t *u, long t, const double *q, const d
         char *is_sa = (char *)malloc((size_t)(nslot > 0 ? nslot : 1));
         double *phq = (double *)malloc(sizeof(double) * (size_t)df);
         double *phk = (double *)malloc(sizeof(double) * (size_t)df);
+        double *ylin = (double *)malloc(sizeof(double) * (size_t)d);   /* the linear branch's numerator */
         for (int s = 0; s < nslot; ++s) {
             int p = u->pos[s];
             if (s < W) is_sa[s] = p >= 0;
@@ -411,9 +420,10 @@ static int step_unit(const prm_t *P, unit_t *u, long t, const double *q, const d
                 for (int e2 = 0; e2 < d; ++e2) yh[e2] += w * u->V[(long)s * d + e2];
             }
             oref_npmap(qh, 1, d, Wf, df, phq);
+            for (int e2 = 0; e2 < d; ++e2) ylin[e2] = 0.0;
             for (int i = 0; i < df; ++i) {
                 den += phq[i] * u->z[i];
-                for (int e2 = 0; e2 < d; ++e2) yh[e2] += phq[i] * u->S[(long)i * d + e2];
+                for (int e2 = 0; e2 < d; ++e2) ylin[e2] += phq[i] * u->S[(long)i * d + e2];
             }
             for (int s = W; s < nslot; ++s) {
                 int p = u->pos[s];
@@ -422,14 +432,19 @@ static int step_unit(const prm_t *P, unit_t *u, long t, const double *q, const d
                 double a = 0.0;
                 for (int i = 0; i < df; ++i) a += phq[i] * phk[i];
                 den += a;
-                for (int e2 = 0; e2 < d; ++e2) yh[e2] += a * u->V[(long)s * d + e2];
+                for (int e2 = 0; e2 < d; ++e2) ylin[e2] += a * u->V[(long)s * d + e2];
             }
-            for (int e2 = 0; e2 < d; ++e2) yh[e2] = den != 0.0 ? yh[e2] / den : 0.0;
+            for (int e2 = 0; e2 < d; ++e2) {
+                const double gch = gate ? 1.0 / (1.0 + exp(-gate[(long)h * d + e2])) : 1.0;
+                yh[e2] += gch * ylin[e2];
+                yh[e2] = den != 0.0 ? yh[e2] / den : 0.0;
+            }
         }
         free(logit);
         free(is_sa);
         free(phq);
         free(phk);
+        free(ylin);
     }
 
     /* (6) chunk ct is complete after token t: its top-lambda are kept for good */
@@ -520,10 +535,12 @@ void oref_state_init(int B, int Hkv, int d, int df, int C, int m, double *K, dou
 /* Prefill of B sequences of N tokens = N streaming steps from an empty state.
  * q [B,Hq,N,d], k,v [B,Hkv,N,d], Wf [d,df] -> y [B,Hq,N,d], scores [B,Hkv,N]
  * (nullable) and the state after N tokens.  sel_override [B,Hkv,T_max,lam] is
- * nullable.  nthreads <= 0 uses the OpenMP default.  Returns 0 or an error. */
+ * nullable; gate [B,Hq,N,d] (nullable: no gate) holds the gate pre-activations
+ * of the linear branch.  nthreads <= 0 uses the OpenMP default.  Returns 0 or
+ * an error. */
 int oref_prefill(int B, int Hq, int Hkv, int N, int d, int df, int W, int C, int m, int T_max,
                  const double *q, const double *k, const double *v, const double *Wf,
-                 const int32_t *sel_override, double *y, double *scores, double *K, double *V,
+                 const int32_t *sel_override, const double *gate, double *y, double *scores, double *K, double *V,
                  int32_t *pos, int32_t *cnt, double *ssc, double *S, double *z, double *ring,
                  int nthreads)
 {
@@ -542,17 +559,22 @@ int oref_prefill(int B, int Hq, int Hkv, int N, int d, int df, int W, int C, int
         int g = (int)(ug % Hkv);
         unit_t u = unit_at(&P, b, g, K, V, pos, cnt, ssc, S, z, ring);
         double *qbuf = (double *)malloc(sizeof(double) * (size_t)(P.G * d));
+        double *gbuf = gate ? (double *)malloc(sizeof(double) * (size_t)(P.G * d)) : NULL;
         double *ybuf = (double *)malloc(sizeof(double) * (size_t)(P.G * d));
         const int32_t *ovr = sel_override ? sel_override + ug * T_max * (P.lam > 0 ? P.lam : 1) : NULL;
         if (P.lam == 0) ovr = NULL;
         for (long t = 0; t < N; ++t) {
-            for (int h = 0; h < P.G; ++h)
+            for (int h = 0; h < P.G; ++h) {
                 memcpy(qbuf + (long)h * d, q + (((b * Hq) + g * P.G + h) * (long)N + t) * d,
                        sizeof(double) * (size_t)d);
+                if (gbuf)
+                    memcpy(gbuf + (long)h * d, gate + (((b * Hq) + g * P.G + h) * (long)N + t) * d,
+                           sizeof(double) * (size_t)d);
+            }
             const double *kt = k + ((b * Hkv + g) * (long)N + t) * d;
             const double *vt = v + ((b * Hkv + g) * (long)N + t) * d;
             double st;
-            int r = step_unit(&P, &u, t, qbuf, kt, vt, Wf, ovr, ybuf, &st);
+            int r = step_unit(&P, &u, t, qbuf, kt, vt, Wf, ovr, gbuf, ybuf, &st);
             if (r < err) err = r;
             if (scores) scores[(b * Hkv + g) * (long)N + t] = st;
             for (int h = 0; h < P.G; ++h)
@@ -560,6 +582,7 @@ int oref_prefill(int B, int Hq, int Hkv, int N, int d, int df, int W, int C, int
                        sizeof(double) * (size_t)d);
         }
         free(qbuf);
+        free(gbuf);
         free(ybuf);
     }
     return err;
@@ -567,10 +590,11 @@ int oref_prefill(int B, int Hq, int Hkv, int N, int d, int df, int W, int C, int
 
 /* One decode step for B sequences: token position t[b] of each sequence
  * (t[b] tokens already absorbed).  q_t [B,Hq,d], k_t,v_t [B,Hkv,d] -> y
- * [B,Hq,d]; the state is updated in place.  The caller advances t. */
+ * [B,Hq,d]; gate_t [B,Hq,d] (nullable) the gate pre-activations of the
+ * linear branch; the state is updated in place.  The caller advances t. */
 int oref_decode_step(int B, int Hq, int Hkv, int d, int df, int W, int C, int m, int T_max,
                      const int64_t *t, const double *q_t, const double *k_t, const double *v_t,
-                     const double *Wf, double *y, double *K, double *V, int32_t *pos,
+                     const double *Wf, const double *gate_t, double *y, double *K, double *V, int32_t *pos,
                      int32_t *cnt, double *ssc, double *S, double *z, double *ring, int nthreads)
 {
     prm_t P;
@@ -588,6 +612,7 @@ int oref_decode_step(int B, int Hq, int Hkv, int d, int df, int W, int C, int m,
         unit_t u = unit_at(&P, b, g, K, V, pos, cnt, ssc, S, z, ring);
         int r = step_unit(&P, &u, (long)t[b], q_t + (b * Hq + g * P.G) * (long)d,
                           k_t + (b * Hkv + g) * (long)d, v_t + (b * Hkv + g) * (long)d, Wf, NULL,
+                          gate_t ? gate_t + (b * Hq + g * P.G) * (long)d : NULL,
                           y + (b * Hq + g * P.G) * (long)d, NULL);
         if (r < err) err = r;
     }
