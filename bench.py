@@ -12,7 +12,10 @@ a second pass of the same steps with an event pair around every kernel gives
 the per-kernel times and the roofline of the dominant kernel.  Further legs:
 end to end through pinned host buffers, the 128-sequence decode step, the
 routing metrics of the ablation (score kernel per metric and the layer routed
-by it), and the CPU oracle on a sample of the same layer.
+by it), the other prefill workloads (the Llama-3.2-1B-shaped layer at 4K and
+the training-shaped batch of eight 1K sequences, each with its roofline, its
+CPU-oracle time and its parity), and the CPU oracle on the 16K layer with the
+parity of the benchmarked output against it.
 
 Under torchrun (N > 1) every rank runs its own layer (its own seed): weak
 scaling, no collective on the data path; value = all ranks' tokens / the max
@@ -56,6 +59,8 @@ def parse(argv=None):
     p.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
     p.add_argument("--no-routing", action="store_true", help="skip the routing-metric measurements")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-workloads", action="store_true",
+                   help="skip the 1B-shaped 4K and training-shaped prefill legs")
     p.add_argument("--cpu-tokens", type=int, default=16384, help="tokens of the CPU-baseline sample")
     p.add_argument("--seed", type=int, default=0)
     return p.parse_args(argv)
@@ -195,7 +200,7 @@ class ClockSampler:
 # CPU oracle
 # ---------------------------------------------------------------------------
 
-def oracle_sample(q, k, v, Wf, w, tokens, threads, keep=None):
+def oracle_sample(q, k, v, Wf, w, tokens, threads, keep=None, gate=None):
     """Run the fp64 streaming oracle over `tokens` tokens of every kv head; the
     time it took.  With a dict `keep`, the oracle's output and scores are
     stored there (key "y", "scores") for the parity check."""
@@ -206,10 +211,11 @@ def oracle_sample(q, k, v, Wf, w, tokens, threads, keep=None):
     va = to_f64(v[:, :, :tokens])
     Wa = to_f64(Wf)
     t0 = time.perf_counter()
-    y, sc, _ = ref.prefill(qa, ka, va, Wa, w.W, w.C, w.m, w.T_max, threads=threads)
+    ga = to_f64(gate[:, :, :tokens]) if gate is not None else None
+    y, sc, _ = ref.prefill(qa, ka, va, Wa, w.W, w.C, w.m, w.T_max, threads=threads, gate=ga)
     secs = time.perf_counter() - t0
     if keep is not None:
-        keep.update(y=y, scores=sc, inputs=(qa, ka, va, Wa))
+        keep.update(y=y, scores=sc, inputs=(qa, ka, va, Wa), gate=ga)
     return secs
 
 
@@ -238,7 +244,8 @@ def parity_vs_oracle(out, sel, w, toks, keep, threads):
                 exact_outside = False
     if n_diff and exact_outside and toks == w.N:
         qa, ka, va, Wa = keep["inputs"]
-        y_ref, _, _ = ref.prefill(qa, ka, va, Wa, w.W, w.C, w.m, w.T_max, sel_override=sel_g, threads=threads)
+        y_ref, _, _ = ref.prefill(qa, ka, va, Wa, w.W, w.C, w.m, w.T_max, sel_override=sel_g, threads=threads,
+                                  gate=keep.get("gate"))
     y = to_f64(out[:, :, :toks])
     err = float(np.abs(y - y_ref).max() / np.abs(y_ref).max())
     return {"max_err_rel": err, "tolerance": 1e-2, "within_tolerance": err <= 1e-2,
@@ -255,14 +262,14 @@ def cpu_threads(units):
     return max(1, min(n, units))
 
 
-def cpu_baseline(q, k, v, Wf, w, toks):
+def cpu_baseline(q, k, v, Wf, w, toks, gate=None):
     """The oracle on the host cores over tokens 0..toks-1 of every kv head (one
     thread per kv head), and on one core: the first kv head with its query
     heads on one thread, its time scaled by the number of kv heads and
     sequences (the units are independent and cost the same)."""
     thr = cpu_threads(w.B * w.Hkv)
     keep = {}
-    secs = oracle_sample(q, k, v, Wf, w, toks, thr, keep)
+    secs = oracle_sample(q, k, v, Wf, w, toks, thr, keep, gate=gate)
     G = w.Hq // w.Hkv
     w1 = dataclasses.replace(w, B=1, Hq=G, Hkv=1)
     secs1 = oracle_sample(q[:1, :G], k[:1, :1], v[:1, :1], Wf, w1, toks, 1) * w.B * w.Hkv
@@ -510,6 +517,14 @@ def run_ours(args):
     if not args.no_routing and rank == 0:
         line["routing_metrics"] = bench_routing(still, w, (q, k, v, Wf), dev, stream, pk, pk_kind)
 
+    # -------- the other prefill workloads --------
+    if not args.no_workloads and rank == 0:
+        line["workloads"] = {nm: bench_workload(still, nm, dev, stream, pk, pk_kind, args.seed + 11,
+                                                cpu=not args.no_cpu)
+                             for nm in ("llama32_1b_layer_prefill_4k", "train_b8_n1k_chunk_parallel")}
+        line["workloads"]["llama3_8b_layer_prefill_16k_gated"] = bench_workload(
+            still, WORKLOAD, dev, stream, pk, pk_kind, args.seed + 12, steps=20, cpu=not args.no_cpu, gated=True)
+
     # -------- decode step (128 sequences at 16K) --------
     if not args.no_decode and rank == 0:
         line["decode_step"] = bench_decode(still, inputs, dev, stream, pk, pk_kind, args)
@@ -570,6 +585,85 @@ def bench_routing(still, w, qkvw, dev, stream, pk, pk_kind, launches=10):
                        "roofline": {"bound": "hbm", "achieved": ach, "peak": pk["hbm_gbs"], "unit": "GB/s",
                                     "frac": ach / pk["hbm_gbs"], "peak_source": pk_kind},
                        "routed_prefill_ms": statistics.median(a.elapsed_time(b) for a, b in pre[2:])}
+    return res
+
+
+def bench_workload(still, name, dev, stream, pk, pk_kind, seed, steps=50, cpu=True, gated=False):
+    """Another prefill workload of the pages' set (the 1B-shaped layer at 4K, the
+    training-shaped batch of eight 1K sequences): `steps` timed prefills after 3
+    warm-up ones, L2 flushed before each (CUDA events around every call), the
+    step against its roofline, the kernels' times from a second pass with the
+    library's event timers, and -- unless cpu is False -- the oracle over the
+    whole workload on the host cores and the parity of the GPU's output with it.
+    gated: the layer with the per-channel sigmoid gate on the linear branch
+    (still_prefill_gated), its pre-activations drawn by inputs.make_gate."""
+    import torch
+    from linear_attention_linearization_gb300 import inputs
+    w = inputs.WORKLOADS[name]
+    q, k, v, Wf = inputs.make_inputs(w, seed=seed, device=dev)
+    gate = inputs.make_gate(w, seed=seed, device=dev) if gated else None
+    out = torch.empty_like(q)
+    sel = torch.empty((w.B, w.Hkv, w.T_max, w.lam), dtype=torch.int32, device=dev)
+    ws = torch.empty(still.workspace_size(q, k, Wf, w.W, w.C, w.m, w.T_max), dtype=torch.uint8, device=dev)
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def step():
+        if gated:
+            still.prefill_gated(q, k, v, gate, Wf, w.W, w.C, w.m, w.T_max, out=out, sel_idx=sel, workspace=ws,
+                                stream=stream)
+        else:
+            still.prefill(q, k, v, Wf, w.W, w.C, w.m, w.T_max, out=out, sel_idx=sel, workspace=ws, stream=stream)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize(dev)
+    ev = []
+    for i in range(steps):
+        flush.fill_(float(i))
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        step()
+        b.record(stream)
+        ev.append((a, b))
+    torch.cuda.synchronize(dev)
+    ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    still.timing_read()
+    still.timing_enable(True)
+    for i in range(10):
+        flush.fill_(float(i))
+        step()
+    torch.cuda.synchronize(dev)
+    still.timing_enable(False)
+    kt = still.timing_read()
+    alg = algorithmic(w, sel.cpu().numpy())
+    t_roof = max(alg["flops"] / (pk["bf16_tflops"] * 1e12), alg["bytes"] / (pk["hbm_gbs"] * 1e9))
+    kb = kernel_bytes(w)
+    att_name = "hybrid_attn_gated" if gated else "hybrid_attn"
+    n_att, ms_att = kt.get(att_name, (0, 0.0))
+    att = None
+    if n_att:
+        per = ms_att / n_att / 1e3
+        by = kb["hybrid_attn"] + (2.0 * w.B * w.Hq * w.N * w.d if gated else 0.0)   # + the gate read once
+        att = {"ms_per_launch": per * 1e3, "achieved": by / per / 1e9, "peak": pk["hbm_gbs"], "algorithmic_bytes": by,
+               "unit": "GB/s", "frac": by / per / 1e9 / pk["hbm_gbs"], "bound": "hbm", "peak_source": pk_kind}
+    res = {"config": {"workload": name, **w.asdict()}, "metric": "prefill tokens/s", "unit": "tokens/s",
+           "value": w.B * w.N / (ms / 1e3), "ms_per_step": ms, "steps": steps,
+           "l2": "flushed (258 MB write) before every timed step",
+           "step_roofline": {"algorithmic_flops": alg["flops"], "algorithmic_bytes": alg["bytes"],
+                             "roofline_ms": t_roof * 1e3, "frac_of_roofline": t_roof * 1e3 / ms, "peak_source": pk_kind},
+           "attention_roofline": att,
+           "kernels": {k2: {"launches": n, "ms_per_launch": m / n} for k2, (n, m) in kt.items()},
+           "attention_on_tensor_cores": att_name in kt and not any(n.startswith("hybrid_attn_general") for n in kt)}
+    if gated:
+        res["layer"] = "gated: per-channel sigmoid gate on the linear branch's numerator"
+    if cpu:
+        toks = w.N
+        if gated:
+            res["cpu_baseline"], keep, thr = cpu_baseline(q.cpu(), k.cpu(), v.cpu(), Wf.cpu(), w, toks,
+                                                          gate=gate.cpu())
+        else:
+            res["cpu_baseline"], keep, thr = cpu_baseline(q.cpu(), k.cpu(), v.cpu(), Wf.cpu(), w, toks)
+        res["parity"] = parity_vs_oracle(out, sel, w, toks, keep, thr)
     return res
 
 

@@ -208,6 +208,27 @@ still_status still_prefill_routed(const still_shape *shape, const still_bf16 *q,
                                   void *workspace, size_t workspace_bytes, still_stream_t stream);
 
 /*
+ * The prefill above with a gate on the linear branch (section "NP-Map:
+ * Norm-Preserving Feature Map": a gating mechanism raises the linear branch's
+ * rank; the ablation loses 5.8 points without it).  The pages lost its
+ * equation; the reading this library takes is a per-channel sigmoid gate on
+ * the linear branch's numerator, the shared denominator ungated:
+ *   y_t = (sum_SA e^{s-c} v + g_t * (phi(q)^T S_LA)) / (sum_SA e^{s-c} + phi(q)^T z_LA),
+ *   g_t = 1 / (1 + exp(-a_t)) elementwise,
+ * where a = gate, bf16 [B,Hq,N,d] (the layout of q), holds the pre-activation
+ * of query head h at token t (the linear part of y includes the own-chunk and
+ * lagged linear keys, gated alike).  A gate of +inf everywhere gives
+ * still_prefill's layer.  Everything else -- routing, selection, workspace
+ * (still_prefill_workspace_size bytes, or NULL) -- is as for still_prefill.
+ * No decode state is exported: the decode step of the gated layer is not
+ * provided.
+ */
+still_status still_prefill_gated(const still_shape *shape, const still_bf16 *q, const still_bf16 *k,
+                                 const still_bf16 *v, const still_bf16 *gate, const float *Wf, int W, int C, int m,
+                                 int T_max, still_bf16 *out, int32_t *sel_idx, void *workspace,
+                                 size_t workspace_bytes, still_stream_t stream);
+
+/*
  * The prefill above with its scratch memory taken from a fixed array inside
  * the library instead of a workspace argument.  The pages have no counterpart:
  * this entry point exists for callers that may not allocate device memory

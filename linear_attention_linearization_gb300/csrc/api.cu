@@ -279,7 +279,8 @@ namespace {
 still_status prefill_impl(const still_shape *shape, const still_bf16 *q, const still_bf16 *k, const still_bf16 *v,
                           const float *Wf, int W, int C, int m, int T_max, int metric, unsigned long long seed,
                           still_bf16 *out, int32_t *sel_idx, void *workspace, size_t workspace_bytes,
-                          const still_decode_state *export_state, still_stream_t stream)
+                          const still_decode_state *export_state, still_stream_t stream,
+                          const still_bf16 *gate = nullptr)
 {
     Dims dm;
     still_status st = make_dims(shape, W, C, m, T_max, &dm);
@@ -339,10 +340,10 @@ still_status prefill_impl(const still_shape *shape, const still_bf16 *q, const s
     if (e == cudaSuccess) e = launch_scan(dm, sp, dS, dz, s);
     if (e == cudaSuccess) {
         if (tc) {
-            TCBuffers bf{q, k, v, kk, vk, phik, phk, wft, out};
+            TCBuffers bf{q, k, v, kk, vk, phik, phk, wft, out, gate};
             e = launch_hybrid_tc(dm, sp, bf, fsel, dS, dz, status, s);
         } else {
-            e = launch_hybrid_general(dm, sp, q, k, v, Wf, phik, phk, fsel, dS, dz, out, status, s);
+            e = launch_hybrid_general(dm, sp, q, k, v, Wf, phik, phk, fsel, dS, dz, out, status, s, gate);
         }
     }
     if (e == cudaSuccess && export_state) e = launch_export(dm, sp, k, v, scores, fsel, dS, dz, *export_state, s);
@@ -376,6 +377,16 @@ still_status still_prefill_routed(const still_shape *shape, const still_bf16 *q,
     if (!metric_ok(metric)) return STILL_ERR_INVALID_ARG;
     return prefill_impl(shape, q, k, v, Wf, W, C, m, T_max, metric, seed, out, sel_idx, workspace, workspace_bytes,
                         nullptr, stream);
+}
+
+still_status still_prefill_gated(const still_shape *shape, const still_bf16 *q, const still_bf16 *k,
+                                 const still_bf16 *v, const still_bf16 *gate, const float *Wf, int W, int C, int m,
+                                 int T_max, still_bf16 *out, int32_t *sel_idx, void *workspace,
+                                 size_t workspace_bytes, still_stream_t stream)
+{
+    if (shape && shape->N > 0 && (!gate || !aligned16(gate))) return STILL_ERR_INVALID_ARG;
+    return prefill_impl(shape, q, k, v, Wf, W, C, m, T_max, STILL_METRIC_SELF_SALIENCY, 0, out, sel_idx, workspace,
+                        workspace_bytes, nullptr, stream, gate);
 }
 
 still_status still_score_metric(const still_shape *shape, const still_bf16 *q, const still_bf16 *k, int W, int C,

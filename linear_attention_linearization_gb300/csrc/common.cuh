@@ -221,10 +221,11 @@ cudaError_t launch_scan(const Dims &dm, const SegPlan &sp, float *dS, float *dz,
 cudaError_t launch_hybrid_general(const Dims &dm, const SegPlan &sp, const uint16_t *q, const uint16_t *k,
                                   const uint16_t *v, const float *Wf, const uint16_t *phik, const uint16_t *phkept,
                                   const int32_t *fsel, const float *dS, const float *dz, uint16_t *out,
-                                  int32_t *status, cudaStream_t s);
+                                  int32_t *status, cudaStream_t s, const uint16_t *gate = nullptr);
 struct TCBuffers {
     const uint16_t *q, *k, *v, *kk, *vk, *phik, *phk, *wft;
     uint16_t *out;
+    const uint16_t *gate;   // nullable: pre-activations of the linear branch's gate, [B, Hq, N, d]
 };
 bool hybrid_tc_supported(const Dims &dm);
 cudaError_t launch_hybrid_tc(const Dims &dm, const SegPlan &sp, const TCBuffers &bf, const int32_t *fsel,

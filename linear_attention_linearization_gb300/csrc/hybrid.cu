@@ -29,7 +29,8 @@ __global__ void __launch_bounds__(256) hybrid_kernel(const uint16_t *__restrict_
                                                      const uint16_t *__restrict__ phik, const uint16_t *__restrict__ phkept,
                                                      const int32_t *__restrict__ fsel, const float *__restrict__ dS,
                                                      const float *__restrict__ dz, Dims dm, SegPlan sp,
-                                                     uint16_t *__restrict__ out, int32_t *status)
+                                                     uint16_t *__restrict__ out, int32_t *status,
+                                                     const uint16_t *__restrict__ gate)
 {
     grid_dep_sync();
     constexpr int PD = D / 32;          // output dims per lane
@@ -159,8 +160,13 @@ __global__ void __launch_bounds__(256) hybrid_kernel(const uint16_t *__restrict_
             }
             const float den = l + dl;
             uint16_t *orow = out + ((size_t)(b * dm.Hq + h) * dm.N + t) * D;
+            // the gated layer: sigmoid(gate) on the linear numerator, channel by channel
+            const uint16_t *grow = gate ? gate + ((size_t)(b * dm.Hq + h) * dm.N + t) * D : nullptr;
 #pragma unroll
-            for (int r = 0; r < PD; ++r) orow[lane + 32 * r] = f2bf(den != 0.f ? (acc[r] + la[r]) / den : 0.f);
+            for (int r = 0; r < PD; ++r) {
+                const float gch = grow ? 1.f / (1.f + expf(-bf2f(grow[lane + 32 * r]))) : 1.f;
+                orow[lane + 32 * r] = f2bf(den != 0.f ? fmaf(gch, la[r], acc[r]) / den : 0.f);
+            }
         }
         __syncthreads();
 
@@ -192,14 +198,14 @@ template <int D, int DF>
 static cudaError_t launch_hybrid_t(const Dims &dm, const SegPlan &sp, const uint16_t *q, const uint16_t *k,
                                    const uint16_t *v, const float *Wf, const uint16_t *phik,
                                    const uint16_t *phkept, const int32_t *fsel, const float *dS, const float *dz,
-                                   uint16_t *out, int32_t *status, cudaStream_t s)
+                                   uint16_t *out, int32_t *status, cudaStream_t s, const uint16_t *gate)
 {
     const size_t smem = sizeof(float) * ((size_t)DF * D + DF + 8 * D + 8 * DF + (size_t)sp.T * (DF + D));
     cudaError_t e = cudaFuncSetAttribute(hybrid_kernel<D, DF>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     dim3 grid(sp.nseg, dm.Hkv, dm.B);
     e = launch_kernel(hybrid_kernel<D, DF>, grid, dim3(256), smem, s, q, k, v, Wf, phik, phkept, fsel, dS, dz, dm, sp,
-                      out, status);
+                      out, status, gate);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
@@ -207,14 +213,16 @@ static cudaError_t launch_hybrid_t(const Dims &dm, const SegPlan &sp, const uint
 cudaError_t launch_hybrid_general(const Dims &dm, const SegPlan &sp, const uint16_t *q, const uint16_t *k,
                                   const uint16_t *v, const float *Wf, const uint16_t *phik, const uint16_t *phkept,
                                   const int32_t *fsel, const float *dS, const float *dz, uint16_t *out,
-                                  int32_t *status, cudaStream_t s)
+                                  int32_t *status, cudaStream_t s, const uint16_t *gate)
 {
-    KTimer tm("hybrid_attn_general", s);
+    KTimer tm(gate ? "hybrid_attn_general_gated" : "hybrid_attn_general", s);
     if (dm.d == 64 && dm.df == 64)
-        return launch_hybrid_t<64, 64>(dm, sp, q, k, v, Wf, phik, phkept, fsel, dS, dz, out, status, s);
-    if (dm.d == 64) return launch_hybrid_t<64, 128>(dm, sp, q, k, v, Wf, phik, phkept, fsel, dS, dz, out, status, s);
-    if (dm.df == 64) return launch_hybrid_t<128, 64>(dm, sp, q, k, v, Wf, phik, phkept, fsel, dS, dz, out, status, s);
-    return launch_hybrid_t<128, 128>(dm, sp, q, k, v, Wf, phik, phkept, fsel, dS, dz, out, status, s);
+        return launch_hybrid_t<64, 64>(dm, sp, q, k, v, Wf, phik, phkept, fsel, dS, dz, out, status, s, gate);
+    if (dm.d == 64)
+        return launch_hybrid_t<64, 128>(dm, sp, q, k, v, Wf, phik, phkept, fsel, dS, dz, out, status, s, gate);
+    if (dm.df == 64)
+        return launch_hybrid_t<128, 64>(dm, sp, q, k, v, Wf, phik, phkept, fsel, dS, dz, out, status, s, gate);
+    return launch_hybrid_t<128, 128>(dm, sp, q, k, v, Wf, phik, phkept, fsel, dS, dz, out, status, s, gate);
 }
 
 }  // namespace still

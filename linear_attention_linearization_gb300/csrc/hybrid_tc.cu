@@ -51,6 +51,9 @@ struct TCParams {
     const float *dz;
     int32_t *status;
     long long row_wait_limit;   // limit of the row warps' waits (the issuing thread's: WAIT_LIMIT_CYCLES)
+    // gated layer (nullable): pre-activations of the linear branch's per-channel gate,
+    // [B, Hq, N, d] bf16; y = (softmax numerator + sigmoid(gate) * linear numerator) / den
+    const uint16_t *gate;
 };
 
 // q and out: boxes of 32 tokens x 64 columns x G heads.  kband / vband: the
@@ -65,6 +68,9 @@ struct TCMaps {
 // the NP-Map statistics at TM_X share the A columns (they are read before the
 // A MMA is issued), row maxima and denominator shares at TM_X2
 constexpr int TM_S = 0, TM_DZ = 256, TM_O = 320, TM_A = 448, TM_X = 448, TM_X2 = 496, TM_COLS = 512;
+// the gated layer's linear numerator, in logit columns free once P V is done
+// (dS takes 0 .. 127 and dz 256 .. 271)
+constexpr int TM_LIN = 128;
 constexpr int MAX_KEY_BLOCKS = 10;   // 320 logit columns: every block of a tile stays resident
 constexpr int NX = 16;               // extra (kept, own chunk) rows per tile
 
@@ -98,7 +104,7 @@ constexpr int HT_LAUNCH_REGS = 96, HT_ROW_REGS = 104, HT_ISSUE_REGS = 64;
 static_assert(HT_ROWS * HT_ROW_REGS + 128 * HT_ISSUE_REGS <= HT_THREADS * HT_LAUNCH_REGS,
               "the register split exceeds what the block is launched with");
 
-template <int D, int DF>
+template <int D, int DF, bool GATED>
 __global__ void __launch_bounds__(HT_THREADS, 1) hybrid_tc_kernel(const __grid_constant__ TCMaps maps, TCParams P)
 {
     using Lay = TCLayout<D, DF>;
@@ -129,6 +135,7 @@ __global__ void __launch_bounds__(HT_THREADS, 1) hybrid_tc_kernel(const __grid_c
     const int tbeg = P.sp.begin[s], tend = P.sp.begin[s + 1];
     const int ntiles = (tend - tbeg + 31) / 32;
     const int32_t *fs = P.fsel + (size_t)unit * P.KP;
+    constexpr bool gated = GATED;
 
     if (warp == 0) {
         tmem_alloc(&tmem_base, TM_COLS);
@@ -330,25 +337,36 @@ __global__ void __launch_bounds__(HT_THREADS, 1) hybrid_tc_kernel(const __grid_c
                 tc_fence_after();
                 for (int k = 0; k < DF; k += 16)
                     mma_ss(tmem + TM_A, kdesc(sb + Lay::PHIQ, k, 16384), kdesc(sb + Lay::PHIK, k, 6144), id_a, k > 0);
+                // the linear numerator: phi(Q) S_run, then (once A is masked) A V_lagx -- into O
+                // with the softmax part, or, for the gated layer, into logit columns of its own
+                // once every P V MMA has been issued
+                auto lin_state = [&](uint32_t d, uint32_t acc0) {
 #pragma unroll 1
-                for (int k = 0; k < DF; k += 16)
-                    mma_ss(tmem + TM_O, dPQ + koff(k, 16384), dSR + (uint64_t)(k * 128 >> 4), id_o, k > 0);
+                    for (int k = 0; k < DF; k += 16)
+                        mma_ss(d, dPQ + koff(k, 16384), dSR + (uint64_t)(k * 128 >> 4), id_o, k > 0 ? 1u : acc0);
+                };
+                auto lin_lag = [&](uint32_t d) {
+                    // packed lag pairs in columns 0 .. 15 of A, packed extras in 32 .. 39 (each half
+                    // packs within the columns it read, so neither overwrites what the other reads)
+#pragma unroll 1
+                    for (int kk = 0; kk < 32 + NX; kk += 16)
+                        mma_ts(d, tmem + TM_A + (kk < 32 ? kk / 2 : kk), dVL + (uint64_t)(kk * 128 >> 4), id_o, 1);
+                };
+                if (!gated) lin_state(tmem + TM_O, 0);
                 mma_commit(&bar_a);
-                // A masked: O += A V_lagx
                 if (!(ok = wait(&rdy_a, pe_a))) break;
                 pe_a ^= 1;
                 tc_fence_after();
-                // packed lag pairs in columns 0 .. 15 of A, packed extras in 32 .. 39 (each half
-                // packs within the columns it read, so neither overwrites what the other reads)
-#pragma unroll 1
-                for (int kk = 0; kk < 32 + NX; kk += 16)
-                    mma_ts(tmem + TM_O, tmem + TM_A + (kk < 32 ? kk / 2 : kk), dVL + (uint64_t)(kk * 128 >> 4), id_o, 1);
+                if (!gated) lin_lag(tmem + TM_O);
                 // P written, first the blocks below the split, then the rest: O += sum_kb P_kb V_kb
-                // (blocks of the second batch once the first batch's V has been read)
+                // (blocks of the second batch once the first batch's V has been read); the gated
+                // layer's first P V starts O
                 const int split = nkb / 2;
+                uint32_t o_acc = gated ? 0u : 1u;
                 auto pv = [&](int kb, int slot) {
-                    mma_ts(tmem + TM_O, tmem + TM_S + 32 * kb, dVR + (uint64_t)(slot * 4096 >> 4), id_o, 1);
+                    mma_ts(tmem + TM_O, tmem + TM_S + 32 * kb, dVR + (uint64_t)(slot * 4096 >> 4), id_o, o_acc);
                     mma_ts(tmem + TM_O, tmem + TM_S + 32 * kb + 16, dVR + (uint64_t)((slot * 4096 + 2048) >> 4), id_o, 1);
+                    o_acc = 1u;
                 };
                 if (!(ok = wait(&bar_v, ph_v))) break;
                 ph_v ^= 1;
@@ -370,17 +388,23 @@ __global__ void __launch_bounds__(HT_THREADS, 1) hybrid_tc_kernel(const __grid_c
                     tc_fence_after();
                     for (int kb = B1; kb < nkb; ++kb) pv(kb, kb - B1);
                 }
+                if (gated) {
+                    // the gated layer's linear numerator, behind the P V MMAs (which have read P)
+                    lin_state(tmem + TM_S + TM_LIN, 0);
+                    lin_lag(tmem + TM_S + TM_LIN);
+                }
                 mma_commit(&bar_o);
-                // every read of P and of the ring is done: dS into the logit columns, the next K blocks
-                if (!(ok = wait(&bar_o, ph_o))) break;
-                ph_o ^= 1;
-                tc_fence_after();
+                // dS into the logit columns right behind the P V MMAs (the tensor pipe runs its
+                // MMAs in issue order, so they have read P first), then the next K blocks once
+                // every read of the ring is done
                 for (int kk = 0; kk < 32; kk += 16) {
                     const uint64_t dphi = sdesc(sb + Lay::PHIK + kk * 128, 6144, 1024);
                     mma_ss(tmem + TM_S, dphi, sdesc(sb + Lay::VLAG + kk * 128, 6144, 1024), id_ds, kk > 0);
                     mma_ss(tmem + TM_DZ, dphi, sdesc(sb + Lay::ONES + kk * 2, 16, 1024), id_dz, kk > 0);
                 }
                 mma_commit(&bar_ds);
+                if (!(ok = wait(&bar_o, ph_o))) break;
+                ph_o ^= 1;
                 if (has_next) load_keys(t0 + 32, 0, min(nkb_of(t0 + 32), RING_SLOTS), 0);
             }
             if (ok && wait(&rdy_epi, pe_epi)) store_out(tbeg + (ntiles - 1) * 32);
@@ -534,10 +558,10 @@ __global__ void __launch_bounds__(HT_THREADS, 1) hybrid_tc_kernel(const __grid_c
                 float ss = 0.f, qq = 0.f;
 #pragma unroll
                 for (int q4 = 0; q4 < HT_PARTS; ++q4) {
-                    ss += xs[4 * q4 + 1] * exp2f(2.f * (xs[4 * q4] - M));
+                    ss += xs[4 * q4 + 1] * exp2_mufu(2.f * (xs[4 * q4] - M));
                     qq += xs[4 * q4 + 2];
                 }
-                const float sc = sqrtf(qq) * rsqrtf(ss) * exp2f(mu - M);   // my exponentials were taken against mu
+                const float sc = sqrtf(qq) * rsqrtf(ss) * exp2_mufu(mu - M);   // my exponentials were taken against mu
                 float2 dz2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
                 for (int c8 = 0; c8 < FQ / 8; ++c8) {
@@ -703,10 +727,51 @@ __global__ void __launch_bounds__(HT_THREADS, 1) hybrid_tc_kernel(const __grid_c
             mbar_arrive(&rdy_p);
 
             // ---------------- epilogue: y = O / den (my quarter of the columns) --------------
+            // the gated layer: y = (O + sigmoid(a) * O_lin) / den, the gate pre-activations of
+            // my columns fetched before the wait
+            uint4 gq[DQ / 8];
+            if (gated) {
+                const uint16_t *gp = P.gate + ((size_t)(b * dm.Hq + g * dm.G + hh) * dm.N + t) * D + part * DQ;
+#pragma unroll
+                for (int i = 0; i < DQ / 8; ++i)
+                    gq[i] = row_ok ? __ldg(reinterpret_cast<const uint4 *>(gp) + i) : make_uint4(0, 0, 0, 0);
+            }
             bad |= !wait(&bar_o, ph_o);
             ph_o ^= 1;
             tc_fence_after();
-            {
+            if (gated) {
+                float d4[4];
+                tmem_ld4(tlane + TM_X2 + 4, d4);
+                tmem_ld_wait();
+                const float dtot = (d4[0] + d4[1]) + (d4[2] + d4[3]);
+                const float inv = dtot != 0.f ? 1.f / dtot : 0.f;
+#pragma unroll
+                for (int c0 = 0; c0 < DQ; c0 += 16) {
+                    float ov[16], lv[16];
+                    tmem_ld16(tlane + TM_O + part * DQ + c0, ov);
+                    tmem_ld16(tlane + TM_S + TM_LIN + part * DQ + c0, lv);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int c8 = 0; c8 < 16; c8 += 8) {
+                        const uint4 ga = gq[(c0 + c8) / 8];
+                        const uint32_t gw[4] = {ga.x, ga.y, ga.z, ga.w};
+                        float yv[8];
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            const float a = __uint_as_float(i & 1 ? gw[i / 2] & 0xffff0000u : gw[i / 2] << 16);
+                            const float gate = __frcp_rn(1.f + exp2_mufu(-a * LOG2E));
+                            yv[i] = fmaf(gate, lv[c8 + i], ov[c8 + i]) * inv;
+                        }
+                        uint4 pk;
+                        pk.x = pack_bf16(yv[0], yv[1]);
+                        pk.y = pack_bf16(yv[2], yv[3]);
+                        pk.z = pack_bf16(yv[4], yv[5]);
+                        pk.w = pack_bf16(yv[6], yv[7]);
+                        const int d0 = part * DQ + c0 + c8;
+                        *reinterpret_cast<uint4 *>(sm + Lay::PHIQ + (d0 / 64) * 16384 + sw128(r, (d0 % 64) / 8)) = pk;
+                    }
+                }
+            } else {
                 float d4[4], ov[DQ];   // the denominator shares and my output columns in one round trip
                 tmem_ld4(tlane + TM_X2 + 4, d4);
 #pragma unroll
@@ -794,7 +859,7 @@ size_t hybrid_tc_smem(const Dims &dm)
 cudaError_t launch_hybrid_tc(const Dims &dm, const SegPlan &sp, const TCBuffers &bf, const int32_t *fsel,
                              const float *dS, const float *dz, int32_t *status, cudaStream_t s)
 {
-    KTimer tm("hybrid_attn", s);
+    KTimer tm(bf.gate ? "hybrid_attn_gated" : "hybrid_attn", s);
     const int D = dm.d, DF = dm.df;
     const uint64_t units = (uint64_t)dm.B * dm.Hkv, heads = (uint64_t)dm.B * dm.Hq;
     const int KP = dm.T_max * dm.lam > 0 ? dm.T_max * dm.lam : 1;
@@ -840,6 +905,7 @@ cudaError_t launch_hybrid_tc(const Dims &dm, const SegPlan &sp, const TCBuffers 
     p.dz = dz;
     p.status = status;
     p.row_wait_limit = consumer_wait_limit();
+    p.gate = bf.gate;
     dim3 grid(sp.nseg, dm.Hkv, dm.B);
     const size_t smem = hybrid_tc_smem(dm);
     cudaError_t e;
@@ -848,19 +914,15 @@ cudaError_t launch_hybrid_tc(const Dims &dm, const SegPlan &sp, const TCBuffers 
         cudaFuncAttributes fa;
         return cudaFuncGetAttributes(&fa, kern) == cudaSuccess && fa.numRegs >= HT_LAUNCH_REGS;
     };
-    if (!regs_ok(D == 64 ? (const void *)hybrid_tc_kernel<64, 64> : (const void *)hybrid_tc_kernel<128, 128>))
-        return cudaErrorInvalidConfiguration;
-    if (D == 64) {
-        e = cudaFuncSetAttribute(hybrid_tc_kernel<64, 64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        e = launch_kernel(hybrid_tc_kernel<64, 64>, grid, dim3(HT_THREADS), smem, s, m, p);
-        if (e != cudaSuccess) return e;
-    } else {
-        e = cudaFuncSetAttribute(hybrid_tc_kernel<128, 128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        e = launch_kernel(hybrid_tc_kernel<128, 128>, grid, dim3(HT_THREADS), smem, s, m, p);
-        if (e != cudaSuccess) return e;
-    }
+    auto go = [&](auto kern) -> cudaError_t {
+        if (!regs_ok((const void *)kern)) return cudaErrorInvalidConfiguration;
+        cudaError_t e2 = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e2 != cudaSuccess) return e2;
+        return launch_kernel(kern, grid, dim3(HT_THREADS), smem, s, m, p);
+    };
+    if (D == 64) e = p.gate ? go(hybrid_tc_kernel<64, 64, true>) : go(hybrid_tc_kernel<64, 64, false>);
+    else e = p.gate ? go(hybrid_tc_kernel<128, 128, true>) : go(hybrid_tc_kernel<128, 128, false>);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

@@ -122,6 +122,23 @@ def make_inputs(w: Workload, seed: int = 0, device="cpu", B: int | None = None, 
     return (q.to(torch.bfloat16), k.to(torch.bfloat16), v.to(torch.bfloat16), Wf)
 
 
+def make_gate(w: Workload, seed: int = 0, device="cpu", B: int | None = None, N: int | None = None,
+              scale: float = 2.0):
+    """Gate pre-activations of the linear branch, bf16 [B,Hq,N,d]: i.i.d.
+    N(0, scale^2), so that the sigmoid gates spread over (0, 1) (about 0.02 to
+    0.98 at two standard deviations).  Seeded apart from make_inputs."""
+    B = w.B if B is None else B
+    N = w.N if N is None else N
+    dev = torch.device(device)
+    if dev.type == "cpu":
+        rng = np.random.Generator(np.random.PCG64(seed + 7919))
+        a = rng.standard_normal((B, w.Hq, N, w.d), dtype=np.float32) * np.float32(scale)
+        return torch.from_numpy(a).to(torch.bfloat16)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(seed + 7919)
+    return (torch.randn((B, w.Hq, N, w.d), generator=gen, device=dev) * scale).to(torch.bfloat16)
+
+
 def to_f64(t: torch.Tensor) -> np.ndarray:
     """Exact float64 copy of a (bf16/fp32) tensor, on the host."""
     return t.detach().to("cpu", torch.float64).numpy()

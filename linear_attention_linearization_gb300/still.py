@@ -64,6 +64,9 @@ SIGNATURES = {
     "still_prefill_routed": (ct.c_int, [ct.POINTER(Shape), ct.c_void_p, ct.c_void_p, ct.c_void_p, ct.c_void_p,
                                         ct.c_int, ct.c_int, ct.c_int, ct.c_int, ct.c_int, ct.c_uint64,
                                         ct.c_void_p, ct.c_void_p, ct.c_void_p, ct.c_size_t, ct.c_void_p]),
+    "still_prefill_gated": (ct.c_int, [ct.POINTER(Shape), ct.c_void_p, ct.c_void_p, ct.c_void_p, ct.c_void_p,
+                                       ct.c_void_p, ct.c_int, ct.c_int, ct.c_int, ct.c_int, ct.c_void_p,
+                                       ct.c_void_p, ct.c_void_p, ct.c_size_t, ct.c_void_p]),
     "still_prefill_noalloc_max_bytes": (ct.c_size_t, []),
     "still_prefill_noalloc": (ct.c_int, [ct.POINTER(Shape), ct.c_void_p, ct.c_void_p, ct.c_void_p, ct.c_void_p,
                                          ct.c_int, ct.c_int, ct.c_int, ct.c_int, ct.c_void_p, ct.c_void_p,
@@ -262,6 +265,29 @@ def prefill_routed(q, k, v, Wf, W, C, m, T_max, metric, seed=0, out=None, sel_id
                                       METRICS[metric], ct.c_uint64(seed), _ptr(out, torch.bfloat16, "out"),
                                       _ptr(sel_idx, torch.int32, "sel_idx") if sel_idx.numel() else None,
                                       ws_ptr, ws_bytes, _stream(stream)), "still_prefill_routed")
+    return out, sel_idx
+
+
+def prefill_gated(q, k, v, gate, Wf, W, C, m, T_max, out=None, sel_idx=None, workspace=None, stream=None):
+    """The layer with a per-channel sigmoid gate on the linear branch's numerator:
+    gate [B,Hq,N,d] bf16 holds the pre-activations (see still_prefill_gated)."""
+    B, Hq, N, d = q.shape
+    if tuple(gate.shape) != tuple(q.shape):
+        raise ValueError("gate must have the shape of q")
+    lam = lam_of(W, m, T_max)
+    sh = shape_of(q, k, Wf)
+    if out is None:
+        out = torch.empty_like(q)
+    if sel_idx is None:
+        sel_idx = torch.empty((B, k.shape[1], T_max, max(lam, 0)), dtype=torch.int32, device=q.device)
+    ws_ptr, ws_bytes = None, 0
+    if workspace is not None:
+        ws_ptr, ws_bytes = _ptr(workspace, torch.uint8, "workspace"), workspace.numel()
+    _check(lib().still_prefill_gated(ct.byref(sh), _ptr(q, torch.bfloat16, "q"), _ptr(k, torch.bfloat16, "k"),
+                                     _ptr(v, torch.bfloat16, "v"), _ptr(gate, torch.bfloat16, "gate"),
+                                     _ptr(Wf, torch.float32, "Wf"), W, C, m, T_max, _ptr(out, torch.bfloat16, "out"),
+                                     _ptr(sel_idx, torch.int32, "sel_idx") if sel_idx.numel() else None,
+                                     ws_ptr, ws_bytes, _stream(stream)), "still_prefill_gated")
     return out, sel_idx
 
 
