@@ -13,10 +13,11 @@
 //             kernel copies its K and V rows there)
 //   dS  += phi_blk^T V_blk                   (tcgen05, accumulated in TMEM)
 //   dz  += phi_blk^T 1                       (tcgen05: an all-ones B operand)
-// Two row threads share a key (each takes half of its features and of its
-// dimensions); a ninth warp issues the TMA copies and the MMAs: U runs two
-// blocks ahead of the rows in a double-buffered TMEM U, dS and dz as soon as
-// a block's features are in shared memory.
+// Four row threads share a key (each takes a quarter of its features and of
+// its dimensions); a seventeenth warp issues the TMA copies and the MMAs: U runs
+// two blocks ahead of the rows in a double-buffered TMEM U (the U of block b+2
+// is issued as soon as the rows are done with block b and its K has come in),
+// dS and dz as soon as a block's features are in shared memory.
 // The range is [b_s - W, b_{s+1} - W) clipped to [0, N), b_s the first token
 // of segment s: the keys that leave the window while segment s runs (the last
 // segment also writes the features of the final W keys).  Only keys below N - W enter dS: the others never
@@ -54,8 +55,12 @@ struct LinLayout {
     static constexpr uint32_t TOTAL = ONES + 2 * 2048;
 };
 
+constexpr int LS_PARTS = 4;                   // row threads per key
+constexpr int LS_ROWS = 128 * LS_PARTS;       // row threads: 16 warps
+constexpr int LS_THREADS = LS_ROWS + 32;      // and the issuing warp
+
 template <int D, int DF>
-__global__ void __launch_bounds__(288, 1) linstate_tc_kernel(const __grid_constant__ LinTCMaps maps, LinTCParams P)
+__global__ void __launch_bounds__(LS_THREADS, 1) linstate_tc_kernel(const __grid_constant__ LinTCMaps maps, LinTCParams P)
 {
     using Lay = LinLayout<D, DF>;
     constexpr int CBD = Lay::CBD, CBF = Lay::CBF;
@@ -65,7 +70,7 @@ __global__ void __launch_bounds__(288, 1) linstate_tc_kernel(const __grid_consta
     uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     const uint32_t sb = smem_u32(sm);
     __shared__ uint64_t bar_wf, bar_full[2], bar_u[2], bar_ds, rdy_phi, phi_free;
-    __shared__ float xch[2][128][3];   // per key row and half: max, sum of squares, ||k||^2 part
+    __shared__ float xch[LS_PARTS][128][3];   // per key row and part: max, sum of squares, ||k||^2 part
     __shared__ uint32_t tmem_base;
     __shared__ int s_abort;
 
@@ -89,16 +94,16 @@ __global__ void __launch_bounds__(288, 1) linstate_tc_kernel(const __grid_consta
         mbar_init(&bar_u[0], 1);
         mbar_init(&bar_u[1], 1);
         mbar_init(&bar_ds, 1);
-        mbar_init(&rdy_phi, 256);
+        mbar_init(&rdy_phi, LS_ROWS);
         mbar_init(&phi_free, 1);
         fence_barrier_init();
         s_abort = 0;
     }
     // the second feature block stays zero when d_f = 64 (it is read as padding rows of dS)
     if (CBF == 1)
-        for (int i = tid; i < 16384 / 16; i += 288) reinterpret_cast<uint4 *>(sm + Lay::PHI + 16384)[i] = make_uint4(0, 0, 0, 0);
+        for (int i = tid; i < 16384 / 16; i += LS_THREADS) reinterpret_cast<uint4 *>(sm + Lay::PHI + 16384)[i] = make_uint4(0, 0, 0, 0);
     // the all-ones operand: row 0 of each 64-key block is ones, rows 1..15 zero
-    for (int i = tid; i < 2 * 2048 / 16; i += 288) {
+    for (int i = tid; i < 2 * 2048 / 16; i += LS_THREADS) {
         const int row = (i * 16 % 2048) / 128;
         const uint32_t one2 = 0x3f803f80u;   // two bf16 ones
         reinterpret_cast<uint4 *>(sm + Lay::ONES)[i] = row == 0 ? make_uint4(one2, one2, one2, one2) : make_uint4(0, 0, 0, 0);
@@ -127,9 +132,9 @@ __global__ void __launch_bounds__(288, 1) linstate_tc_kernel(const __grid_consta
     const uint32_t id_dz = idesc_bf16(128, 16, 1, 0);
     uint32_t ph_ds = 0;
 
-    if (warp == 8) {
+    if (warp == LS_ROWS / 32) {
         // ============================ the issuing warp ============================
-        if (tid == 256) {
+        if (tid == LS_ROWS) {
             uint32_t ph_full[2] = {0, 0}, pe_phi = 0;
             // U of block blk = K_blk Wf into TMEM half blk & 1
             auto issue_u = [&](int blk) {
@@ -175,8 +180,6 @@ __global__ void __launch_bounds__(288, 1) linstate_tc_kernel(const __grid_consta
                         tma_store_3d(&maps.phik, sm + Lay::PHI + cb * 16384, cb * 64, j0, (int)unit);
                     tma_store_commit();
                 }
-                // the next block's U (its K came in one block ago; U of block 1 went out first)
-                if (blk >= 1 && blk + 1 < nblk) issue_u(blk + 1);
                 // this stage is free once dS has read its V: block blk + 2 comes in; the
                 // feature buffer is free once dS, dz and the store have read it
                 if (!mbar_wait(&bar_ds, ph_ds, P.status)) s_abort = 1;
@@ -184,15 +187,18 @@ __global__ void __launch_bounds__(288, 1) linstate_tc_kernel(const __grid_consta
                 if (blk + 2 < nblk) load_blk(blk + 2);
                 if (full) tma_store_wait_read();
                 mbar_arrive(&phi_free);
+                // U of block blk + 2 into the TMEM half the rows are done with (block blk's):
+                // it is ready long before the rows get there
+                if (blk + 2 < nblk) issue_u(blk + 2);
             }
             tma_store_wait_all();
         }
         __syncwarp();
     } else {
         // ============================== the row warps ==============================
-        constexpr int DFH = DF / 2, CH8 = CBD * 4;   // features per half; 16-byte K chunks per half
+        constexpr int DFH = DF / LS_PARTS, CH8 = CBD * 8 / LS_PARTS;   // features per part; 16-byte K chunks per part
         uint32_t ph_u[2] = {0, 0}, ph_kf[2] = {0, 0}, ph_pf = 0;
-        const int r = tid & 127, half = tid >> 7;   // key row of the block; which half of it
+        const int r = tid & 127, part = tid >> 7;   // key row of the block; which part of it
         // kept-slot index of this thread's key, one block ahead
         auto slot_of = [&](int blk) {
             const int jj = klo + 128 * blk + r;
@@ -206,13 +212,13 @@ __global__ void __launch_bounds__(288, 1) linstate_tc_kernel(const __grid_consta
             const bool in_range = j < khi;
             const int kslot = kslot_next;
             kslot_next = slot_of(blk + 1);
-            // ||k||^2 over my half of the dimensions, once the block's K has arrived
+            // ||k||^2 over my part of the dimensions, once the block's K has arrived
             bool bad = !mbar_wait(&bar_full[st], ph_kf[st], P.status);
             ph_kf[st] ^= 1;
             float kn2 = 0.f;
 #pragma unroll
             for (int q = 0; q < CH8; ++q) {
-                const int c = half * CH8 + q;   // 16-byte chunk of the row, 8 per 64-column block
+                const int c = part * CH8 + q;   // 16-byte chunk of the row, 8 per 64-column block
                 const uint4 pk = *reinterpret_cast<const uint4 *>(kd + (c / 8) * 16384 + sw128(r, c % 8));
                 const uint32_t w4[4] = {pk.x, pk.y, pk.z, pk.w};
 #pragma unroll
@@ -224,11 +230,11 @@ __global__ void __launch_bounds__(288, 1) linstate_tc_kernel(const __grid_consta
             bad |= !mbar_wait(&bar_u[st], ph_u[st], P.status);
             ph_u[st] ^= 1;
             tc_fence_after();
-            // my half of the features: exponentials against my half's maximum, in registers
+            // my part of the features: exponentials against my part's maximum, in registers
             float u[DFH];
 #pragma unroll
-            for (int c0 = 0; c0 < DFH; c0 += 32)
-                tmem_ld32(tlane + TM_U + 128 * st + half * DFH + c0, *reinterpret_cast<float(*)[32]>(u + c0));
+            for (int c0 = 0; c0 < DFH; c0 += 16)
+                tmem_ld16(tlane + TM_U + 128 * st + part * DFH + c0, *reinterpret_cast<float(*)[16]>(u + c0));
             tmem_ld_wait();
             float mu = -INFINITY, s2 = 0.f;
 #pragma unroll
@@ -238,19 +244,24 @@ __global__ void __launch_bounds__(288, 1) linstate_tc_kernel(const __grid_consta
                 u[i] = exp2_mufu(fmaf(u[i], LOG2E, -mu));
                 s2 = fmaf(u[i], u[i], s2);
             }
-            xch[half][r][0] = mu;
-            xch[half][r][1] = s2;
-            xch[half][r][2] = kn2;
+            xch[part][r][0] = mu;
+            xch[part][r][1] = s2;
+            xch[part][r][2] = kn2;
             tc_fence_before();
-            if (named_sync_or(1, 256, bad || *(volatile int *)&s_abort)) break;
+            if (named_sync_or(1, LS_ROWS, bad || *(volatile int *)&s_abort)) break;
             float sc;
             {
-                // both halves combine (half 0, half 1) in the same order
-                const float m0 = xch[0][r][0], m1 = xch[1][r][0];
-                const float M = fmaxf(m0, m1);
-                const float ss = xch[0][r][1] * exp2f(2.f * (m0 - M)) + xch[1][r][1] * exp2f(2.f * (m1 - M));
-                const float kk = xch[0][r][2] + xch[1][r][2];
-                sc = sqrtf(kk) * rsqrtf(ss) * exp2f(mu - M);
+                // the parts' statistics, combined in part order on every part
+                float M = xch[0][r][0];
+#pragma unroll
+                for (int p = 1; p < LS_PARTS; ++p) M = fmaxf(M, xch[p][r][0]);
+                float ss = 0.f, kk = 0.f;
+#pragma unroll
+                for (int p = 0; p < LS_PARTS; ++p) {
+                    ss += xch[p][r][1] * exp2_mufu(2.f * (xch[p][r][0] - M));
+                    kk += xch[p][r][2];
+                }
+                sc = sqrtf(kk) * rsqrtf(ss) * exp2_mufu(mu - M);
             }
             // the previous block's dS / dz MMAs and table store are done with the feature buffer
             if (blk > 0) {
@@ -267,7 +278,7 @@ __global__ void __launch_bounds__(288, 1) linstate_tc_kernel(const __grid_consta
             uint16_t *grow = P.phik + (unit * dm.N + (in_range ? j : 0)) * DF;
 #pragma unroll
             for (int q = 0; q < DFH; q += 8) {
-                const int f0 = half * DFH + q;
+                const int f0 = part * DFH + q;
                 uint32_t w4[4];
 #pragma unroll
                 for (int h2 = 0; h2 < 4; ++h2) w4[h2] = pack_bf16(sc * u[q + 2 * h2], sc * u[q + 2 * h2 + 1]);
@@ -285,37 +296,37 @@ __global__ void __launch_bounds__(288, 1) linstate_tc_kernel(const __grid_consta
             if (nrow > 0 && nrow < 128) {
                 // a partial block: rows below fhi hold exactly the table's values (phi, or zero
                 // for slotted keys); each warp stores two 256-byte rows per instruction
-                if (named_sync_or(1, 256, *(volatile int *)&s_abort)) break;
+                if (named_sync_or(1, LS_ROWS, *(volatile int *)&s_abort)) break;
                 constexpr int CH = DF / 8;   // 16-byte chunks per row
                 uint16_t *gbase = P.phik + (unit * dm.N + j0) * DF;
-                for (int e = tid; e < nrow * CH; e += 256) {
+                for (int e = tid; e < nrow * CH; e += LS_ROWS) {
                     const int row = e / CH, ch = e % CH;
                     const uint4 x = *reinterpret_cast<const uint4 *>(sm + Lay::PHI + (ch / 8) * 16384 + sw128(row, ch % 8));
                     *reinterpret_cast<uint4 *>(gbase + (size_t)row * DF + ch * 8) = x;
                 }
-                named_sync_or(1, 256, false);   // the copy's reads end before the buffer is rewritten
+                named_sync_or(1, LS_ROWS, false);   // the copy's reads end before the buffer is rewritten
             }
         }
-        // dS / dz of this segment: row r, my half of the columns (the last block's MMAs)
+        // dS / dz of this segment: row r, my part of the columns (the last block's MMAs)
         if (nblk > 0 && !*(volatile int *)&s_abort) {
             if (!mbar_wait(&bar_ds, (uint32_t)((nblk - 1) & 1), P.status)) s_abort = 1;
             tc_fence_after();
         }
         float *out = P.dS + (unit * (P.sp.nseg + 1) + s) * (size_t)(DF * D);
-        for (int c0 = half * (D / 2); c0 < (half + 1) * (D / 2); c0 += 32) {
-            float v[32];
-            tmem_ld32(tlane + TM_DS + c0, v);
+        for (int c0 = part * (D / LS_PARTS); c0 < (part + 1) * (D / LS_PARTS); c0 += 16) {
+            float v[16];
+            tmem_ld16(tlane + TM_DS + c0, v);
             tmem_ld_wait();
             if (r < DF) {
 #pragma unroll
-                for (int i = 0; i < 32; i += 4)
+                for (int i = 0; i < 16; i += 4)
                     *reinterpret_cast<float4 *>(out + (size_t)r * D + c0 + i) =
                         nblk > 0 ? make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]) : make_float4(0.f, 0.f, 0.f, 0.f);
             }
         }
         const float zacc = tmem_ld1(tlane + TM_DZ);
         tmem_ld_wait();
-        if (r < DF && half == 0) P.dz[(unit * (P.sp.nseg + 1) + s) * DF + r] = nblk > 0 ? zacc : 0.f;
+        if (r < DF && part == 0) P.dz[(unit * (P.sp.nseg + 1) + s) * DF + r] = nblk > 0 ? zacc : 0.f;
     }
     tc_fence_before();
     __syncthreads();
@@ -348,7 +359,7 @@ cudaError_t launch_linstate_tc(const Dims &dm, const SegPlan &sp, const uint16_t
         e = cudaFuncSetAttribute(linstate_tc_kernel<DD, FF>, cudaFuncAttributeMaxDynamicSharedMemorySize,     \
                                  (int)smem);                                                                  \
         if (e != cudaSuccess) return e;                                                                       \
-        e = launch_kernel(linstate_tc_kernel<DD, FF>, grid, dim3(288), smem, s, m, p);                     \
+        e = launch_kernel(linstate_tc_kernel<DD, FF>, grid, dim3(LS_THREADS), smem, s, m, p);              \
         if (e != cudaSuccess) return e;                                                                    \
     }
     if (D == 64 && DF == 64) STILL_LIN(64, 64)
