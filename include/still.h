@@ -229,6 +229,40 @@ still_status still_prefill_gated(const still_shape *shape, const still_bf16 *q, 
                                  size_t workspace_bytes, still_stream_t stream);
 
 /*
+ * Backward pass of the layer (still_prefill's forward, ungated) with the
+ * routing held fixed: given the selection sel_idx the forward made and the
+ * upstream gradient dout = dL/dy, writes dL/dq, dL/dk, dL/dv and dL/dWf.
+ * Section "Experiments" of "STILL: Content-Aware Intra-Layer Hybrid Attention
+ * for Efficient LLM Linearization" trains through the layer; the selection is
+ * a discrete choice and carries no gradient.  The stabiliser c_t (the row
+ * maximum over the softmax keys) is part of the output -- the linear terms are
+ * not scaled by it -- so its gradient goes to the logit of the key where the
+ * maximum is attained (the lowest position among equal maxima).
+ *   q, k, v, Wf   as for still_prefill (bf16 [B,H,N,d], fp32 [d,d_f])
+ *   sel_idx       int32 [B,Hkv,T_max,lambda], the table still_prefill wrote
+ *                 (-1 = no token); entries must be positions of completed
+ *                 chunks c < T_max in ascending order within their chunk
+ *   dout          bf16 [B,Hq,N,d]
+ *   dq            fp32 [B,Hq,N,d]; dk, dv fp32 [B,Hkv,N,d]; dWf fp32 [d,d_f]:
+ *                 overwritten (no accumulation into what they held)
+ *   cmax_idx      nullable int32 [B,Hq,N]: the key position whose logit the
+ *                 row maximum c_t took (the key that received c's gradient)
+ *   workspace     still_backward_workspace_size() bytes, 16-byte aligned, or
+ *                 NULL for a stream-ordered allocation inside the call
+ * Supported: d == d_f in {64, 128}, G = Hq/Hkv in {1, 2, 4}, and W >= C (the
+ * pages' routing rule, under which a kept key is a softmax key of every later
+ * query outside its window and never a linear key); other shapes return
+ * STILL_ERR_UNSUPPORTED.  All device pointers 16-byte aligned.  The call is
+ * asynchronous on `stream`; dk and dWf receive atomic additions, so their
+ * low-order bits may differ between runs.
+ */
+size_t still_backward_workspace_size(const still_shape *shape, int W, int C, int m, int T_max);
+still_status still_backward(const still_shape *shape, const still_bf16 *q, const still_bf16 *k, const still_bf16 *v,
+                            const float *Wf, int W, int C, int m, int T_max, const int32_t *sel_idx,
+                            const still_bf16 *dout, float *dq, float *dk, float *dv, float *dWf, int32_t *cmax_idx,
+                            void *workspace, size_t workspace_bytes, still_stream_t stream);
+
+/*
  * The prefill above with its scratch memory taken from a fixed array inside
  * the library instead of a workspace argument.  The pages have no counterpart:
  * this entry point exists for callers that may not allocate device memory

@@ -389,6 +389,48 @@ still_status still_prefill_gated(const still_shape *shape, const still_bf16 *q, 
                         workspace_bytes, nullptr, stream, gate);
 }
 
+size_t still_backward_workspace_size(const still_shape *shape, int W, int C, int m, int T_max)
+{
+    Dims dm;
+    if (make_dims(shape, W, C, m, T_max, &dm) != STILL_OK) return 0;
+    return bwd_layout(dm).total;
+}
+
+still_status still_backward(const still_shape *shape, const still_bf16 *q, const still_bf16 *k, const still_bf16 *v,
+                            const float *Wf, int W, int C, int m, int T_max, const int32_t *sel_idx,
+                            const still_bf16 *dout, float *dq, float *dk, float *dv, float *dWf, int32_t *cmax_idx,
+                            void *workspace, size_t workspace_bytes, still_stream_t stream)
+{
+    Dims dm;
+    still_status st = make_dims(shape, W, C, m, T_max, &dm);
+    if (st != STILL_OK) return st;
+    if (!backward_supported(dm)) return STILL_ERR_UNSUPPORTED;
+    if (!dWf || !aligned16(dWf) || !Wf || !aligned16(Wf)) return STILL_ERR_INVALID_ARG;
+    cudaStream_t s = (cudaStream_t)stream;
+    if (dm.N == 0) return cuda_status(cudaMemsetAsync(dWf, 0, (size_t)dm.d * dm.df * 4, s));
+    const void *ptrs[] = {q, k, v, dout, dq, dk, dv};
+    for (const void *p : ptrs)
+        if (!p || !aligned16(p)) return STILL_ERR_INVALID_ARG;
+    if ((dm.lam > 0 && (!sel_idx || !aligned16(sel_idx))) || (cmax_idx && !aligned16(cmax_idx)) ||
+        (workspace && !aligned16(workspace)))
+        return STILL_ERR_INVALID_ARG;
+    const BwdLayout L = bwd_layout(dm);
+    if (workspace && workspace_bytes < L.total) return STILL_ERR_WORKSPACE;
+    void *ws = workspace;
+    if (!ws) {
+        cudaError_t e = cudaMallocAsync(&ws, L.total, s);
+        if (e != cudaSuccess) return cuda_status(e);
+    }
+    BwdInputs in{(const uint16_t *)q, (const uint16_t *)k, (const uint16_t *)v, (const uint16_t *)dout, Wf, sel_idx,
+                 dq, dk, dv, dWf, cmax_idx, s};
+    cudaError_t e = launch_backward(dm, in, ws);
+    if (!workspace) {
+        const cudaError_t ef = cudaFreeAsync(ws, s);
+        if (e == cudaSuccess) e = ef;
+    }
+    return cuda_status(e);
+}
+
 still_status still_score_metric(const still_shape *shape, const still_bf16 *q, const still_bf16 *k, int W, int C,
                                 int m, int T_max, still_metric metric, uint64_t seed, float *scores,
                                 still_stream_t stream)

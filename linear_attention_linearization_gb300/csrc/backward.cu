@@ -1,0 +1,1269 @@
+// Chunk-parallel backward pass of the layer, the routing (the kept set) held
+// fixed: gradients of sum(dy * y) with respect to q, k, v and Wf.
+//
+// "STILL: Content-Aware Intra-Layer Hybrid Attention for Efficient LLM
+// Linearization", sections "Content-Aware Routing with Fixed Budget" and
+// "NP-Map: Norm-Preserving Feature Map" define the forward
+//   y_t = (N_SA + phi(q_t)^T S_t) / (D_SA + phi(q_t).z_t),
+//   N_SA = sum_SA p_tj v_j, D_SA = sum_SA p_tj, p_tj = e^{s_tj - c_t},
+//   s_tj = q_t.k_j / sqrt(d), c_t = max_SA s_tj,
+//   S_t = sum_LA phi(k_j) v_j^T, z_t = sum_LA phi(k_j),
+// and its "Experiments" section trains through it.  With g_t = dy_t / D_t and
+// delta_t = g_t . y_t (D_t the whole denominator):
+//   softmax keys:  dp_tj = g_t.v_j - delta_t,  ds_tj = p_tj dp_tj,
+//                  plus -sum_j ds_tj at the row-max key (c_t is part of the
+//                  output: the linear terms are not scaled by it);
+//                  dq_t += sum ds_tj k_j / sqrt(d), dk_j += ds_tj q_t / sqrt(d),
+//                  dv_j += p_tj g_t
+//   linear keys:   dphi(q_t) = S_t g_t - delta_t z_t,
+//                  dphi(k_j) = R_j v_j - r_j,  dv_j += R_j^T phi(k_j),
+//                  R_j = sum_{t : j in LA(t)} phi(q_t) g_t^T, r_j = sum delta_t phi(q_t)
+//   NP-Map:        phi = ||x|| u/||u||, u = softmax(x Wf):
+//                  dl = phi * (dphi - a phi/||x||), a = dphi.phi/||x||,
+//                  dx = a x/||x|| + Wf dl, dWf += x dl^T
+// (the softmax term <du, u> of the NP-Map's chain vanishes because u/||u|| has
+// unit norm).  The routing rule used here is the one for W >= C: every key at
+// or before t - W lies in an earlier chunk, so a kept key is a softmax key of
+// every later query outside its window and never a linear key.
+//
+// Passes (one sequence and kv head per unit, states at 32-token blocks):
+//   mark_kept, phik     the kept flags and phi(k) (kept rows zero)
+//   blocksum, scan      S, z before every 32-key block (forward state)
+//   query               per 16-row warp tile: c, P V, the linear branch, y,
+//                       g, delta, dP, dS, dq (complete, NP-Map included)
+//   blocksum, scan      R, r after every 32-token block (reverse state)
+//   key                 per 16-key warp tile: dk, dv from the window queries
+//                       and the linear branch (NP-Map included)
+//   kept                dk, dv of the kept keys from the queries of later
+//                       chunks outside their window (atomic adds)
+//   dwf                 dWf = sum over q and k rows of x dl^T
+// The contractions run as warp MMAs (bf16 operands, fp32 accumulation).
+#include <climits>
+
+#include "common.cuh"
+#include "warp_mma.cuh"
+
+namespace still {
+
+__global__ void scan_kernel(float *__restrict__ dS, float *__restrict__ dz, int nseg, int nel_s, int nel_z);
+
+namespace {
+
+using namespace wmma16;
+
+constexpr int BT = 32;             // tokens per state block
+constexpr int BQ_THREADS = 128;    // four warps of 16 rows (query pass) or 16 keys (key passes)
+
+struct BwdArgs {
+    Dims dm;
+    int nblk;            // state blocks: ceil(N / BT)
+    float scale;         // 1 / sqrt(d)
+    const uint16_t *q, *k, *v, *dy;
+    const float *Wf;
+    const int32_t *sel;  // [B, Hkv, T_max * lam]
+    const uint8_t *kept; // [B, Hkv, N]
+    const uint16_t *phk; // [B, Hkv, N, DF], kept rows zero
+    const float *Sp, *zp;   // [units][nblk + 1][DF * D], [units][nblk + 1][DF]: state before block i
+    const float *Rs, *rs;   // the same layout, reversed blocks: index nblk - i holds the sums over t >= BT i
+    uint16_t *g, *phq;               // g = dy / den (bf16, for the reverse state), phi(q) [B, Hq, N, *]
+    float *phq32, *phk32;            // phi(q), phi(k) in fp32 (for the NP-Map backward)
+    float *dlq, *dlk;                // dl of the q rows [B, Hq, N, DF] and of the k rows [B, Hkv, N, DF]
+    float *rc, *rdelta, *rds, *rinv; // per query row: c, delta, sum of its softmax ds, 1 / den
+    int32_t *rjs;                    // per query row: the key position of c
+    float *dq, *dk, *dv, *dWf;
+    int32_t *cidx;                   // nullable copy of rjs for the caller
+};
+
+__device__ __forceinline__ uint32_t ld_pair(const uint16_t *row, int col) { return *reinterpret_cast<const uint32_t *>(row + col); }
+
+// 16-byte rows of a bf16 tile: rows [0, nrows) of `src` (rows of `width` elements,
+// `valid(r)` false -> zero row) into a shared tile of stride `ld`, by all threads.
+template <int WIDTH, typename RowPtr>
+__device__ __forceinline__ void stage_rows(uint16_t *dst, int ld, int nrows, RowPtr rowptr)
+{
+    constexpr int V = WIDTH / 8;
+    for (int i = threadIdx.x; i < nrows * V; i += blockDim.x) {
+        const int r = i / V, c = i % V;
+        const uint16_t *src = rowptr(r);
+        uint4 x = make_uint4(0, 0, 0, 0);
+        if (src) x = __ldg(reinterpret_cast<const uint4 *>(src) + c);
+        *reinterpret_cast<uint4 *>(dst + r * ld + c * 8) = x;
+    }
+}
+
+// fp32 [rows][cols] global -> bf16 shared tile of stride ld
+__device__ __forceinline__ void stage_f32(uint16_t *dst, int ld, const float *src, int rows, int cols)
+{
+    const int n4 = rows * cols / 4;
+    for (int i = threadIdx.x; i < n4; i += blockDim.x) {
+        const int r = i / (cols / 4), c = (i % (cols / 4)) * 4;
+        const float4 x = __ldg(reinterpret_cast<const float4 *>(src + (size_t)r * cols + c));
+        uint2 p;
+        p.x = pack(x.x, x.y);
+        p.y = pack(x.z, x.w);
+        *reinterpret_cast<uint2 *>(dst + r * ld + c) = p;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// kept flags and phi(k)
+// ---------------------------------------------------------------------------
+__global__ void mark_kept_kernel(const int32_t *__restrict__ sel, int KP, int N, uint8_t *__restrict__ kept)
+{
+    grid_dep_sync();
+    const int unit = blockIdx.y;
+    const int e = blockIdx.x * blockDim.x + threadIdx.x;
+    if (e >= KP) return;
+    const int p = sel[(size_t)unit * KP + e];
+    if (p >= 0 && p < N) kept[(size_t)unit * N + p] = 1;
+}
+
+template <int D, int DF>
+__global__ void __launch_bounds__(256) phik_kernel(BwdArgs A, uint16_t *__restrict__ phk, float *__restrict__ phk32)
+{
+    grid_dep_sync();
+    __shared__ float xs[8][D];
+    __shared__ float ph[8][DF];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const long long rows = (long long)A.dm.B * A.dm.Hkv * A.dm.N;
+    for (long long r = (long long)blockIdx.x * 8 + warp; r < rows; r += (long long)gridDim.x * 8) {
+        __syncwarp();
+        for (int e = lane; e < D; e += 32) xs[warp][e] = bf2f(A.k[r * D + e]);
+        __syncwarp();
+        warp_npmap<D, DF>(xs[warp], A.Wf, ph[warp], lane);
+        __syncwarp();
+        const bool kp = A.kept[r] != 0;
+        for (int e = lane; e < DF; e += 32) {
+            phk[r * DF + e] = kp ? (uint16_t)0 : f2bf(ph[warp][e]);
+            phk32[r * DF + e] = kp ? 0.f : ph[warp][e];
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// block sums of outer products: out[f][d] = sum_rows a[row][f] b[row][d],
+// zo[f] = sum_rows w[row] a[row][f], for the rows of one 32-token block
+// (forward: the block's keys, a = phi(k), b = v, w = 1; reverse: the block's
+// tokens x the group's heads, a = phi(q), b = g, w = delta; stored reversed)
+// ---------------------------------------------------------------------------
+template <int D, int DF>
+struct BSLayout {
+    static constexpr int LDA = DF + 8, LDB = D + 8, ROWS = 4 * BT;
+    static constexpr int A = 0, B = A + ROWS * LDA * 2, W = B + ROWS * LDB * 2, TOTAL = W + ROWS * 4;
+};
+
+template <int D, int DF, bool REV>
+__global__ void __launch_bounds__(256) blocksum_kernel(BwdArgs P, float *__restrict__ out, float *__restrict__ zo)
+{
+    grid_dep_sync();
+    using L = BSLayout<D, DF>;
+    extern __shared__ __align__(16) uint8_t smem[];
+    uint16_t *sa = (uint16_t *)(smem + L::A), *sb = (uint16_t *)(smem + L::B);
+    float *sw = (float *)(smem + L::W);
+    const Dims &dm = P.dm;
+    const int blk = blockIdx.x, unit = blockIdx.y, b = unit / dm.Hkv, gq = unit % dm.Hkv;
+    const int G = REV ? dm.G : 1;
+    const int rows = BT * G;   // row r: head r / BT, token blk * BT + r % BT
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    auto tok = [&](int r) { return blk * BT + r % BT; };
+    auto base_row = [&](int r) -> size_t {
+        return REV ? ((size_t)(b * dm.Hq + gq * dm.G + r / BT) * dm.N + tok(r)) : ((size_t)unit * dm.N + tok(r));
+    };
+    const uint16_t *ga = REV ? P.phq : P.phk;
+    const uint16_t *gb = REV ? P.g : P.v;
+    stage_rows<DF>(sa, L::LDA, rows, [&](int r) -> const uint16_t * {
+        return tok(r) < dm.N ? ga + base_row(r) * DF : nullptr;
+    });
+    stage_rows<D>(sb, L::LDB, rows, [&](int r) -> const uint16_t * {
+        return tok(r) < dm.N ? gb + base_row(r) * D : nullptr;
+    });
+    for (int r = threadIdx.x; r < rows; r += blockDim.x)
+        sw[r] = tok(r) < dm.N ? (REV ? P.rdelta[base_row(r)] : 1.f) : 0.f;
+    __syncthreads();
+    const int slot = REV ? P.nblk - 1 - blk : blk;
+    float *o = out + ((size_t)unit * (P.nblk + 1) + slot) * DF * D;
+    if (warp < DF / 16) {
+        constexpr int NT = D / 8;
+        float acc[NT][4];
+        zero(acc);
+        for (int k0 = 0; k0 < rows; k0 += 16) {
+            uint32_t a[1][4];
+            load_a_t(sa, L::LDA, warp * 16, k0, a[0]);   // A(m = f, k = row) from [row][f]
+            mma_tile<1, NT, true>(acc, a, sb, L::LDB, 0, k0);
+        }
+        const int gid = lane >> 2, tig = lane & 3;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            const int col = nt * 8 + 2 * tig;
+            *reinterpret_cast<float2 *>(o + (size_t)(warp * 16 + gid) * D + col) = make_float2(acc[nt][0], acc[nt][1]);
+            *reinterpret_cast<float2 *>(o + (size_t)(warp * 16 + gid + 8) * D + col) = make_float2(acc[nt][2], acc[nt][3]);
+        }
+    }
+    for (int f = threadIdx.x; f < DF; f += blockDim.x) {
+        float s = 0.f;
+        for (int r = 0; r < rows; ++r) s = fmaf(sw[r], bf2f(sa[r * L::LDA + f]), s);
+        zo[((size_t)unit * (P.nblk + 1) + slot) * DF + f] = s;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// query pass
+// ---------------------------------------------------------------------------
+template <int D>
+struct QLayout {
+    static constexpr int LD = D + 8, T32 = BT * LD * 2;
+    static constexpr int K = 0, V = K + T32, PK = V + T32, VL = PK + T32;
+    static constexpr int WF = VL + T32;            // Wf [d][df] bf16
+    static constexpr int SP = WF + D * LD * 2;     // S before the lag keys, [df][d] bf16
+    static constexpr int ZP = SP + D * LD * 2;     // z, fp32 [df]
+    static constexpr int POS = ZP + D * 4;         // positions of the staged key block / lag block
+    static constexpr int TOTAL = POS + 2 * BT * 4;
+};
+
+// The thread's two accumulator rows are gid and gid + 8; element (nt, 2r + e)
+// of an accumulator is (row gid + 8r, column 8nt + 2tig + e).
+template <int D, int G>
+__global__ void __launch_bounds__(BQ_THREADS, 2) query_kernel(BwdArgs P)
+{
+    grid_dep_sync();
+    constexpr int LD = D + 8, KC = D / 16, NT = D / 8;
+    constexpr int TOK = 16 * (4 / G);   // tokens per CTA
+    using L = QLayout<D>;
+    extern __shared__ __align__(16) uint8_t smem[];
+    uint16_t *sK = (uint16_t *)(smem + L::K), *sV = (uint16_t *)(smem + L::V);
+    uint16_t *sPK = (uint16_t *)(smem + L::PK), *sVL = (uint16_t *)(smem + L::VL);
+    uint16_t *sWF = (uint16_t *)(smem + L::WF), *sSP = (uint16_t *)(smem + L::SP);
+    float *sZ = (float *)(smem + L::ZP);
+    int *sPos = (int *)(smem + L::POS), *sLag = sPos + BT;
+
+    const Dims &dm = P.dm;
+    const int N = dm.N, W = dm.W, C = dm.C;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gid = lane >> 2, tig = lane & 3;
+    const int unit = blockIdx.y, b = unit / dm.Hkv, gq = unit % dm.Hkv;
+    const int t0 = blockIdx.x * TOK;
+    const int h = gq * G + warp % G;
+    const int tw = t0 + 16 * (warp / G);
+    const int tr[2] = {tw + gid, tw + gid + 8};
+    const size_t qrow0 = (size_t)(b * dm.Hq + h) * N;
+    const size_t krow0 = (size_t)unit * N;
+    const float scale = P.scale;
+
+    // ---- Wf as a bf16 pair hi (sWF, resident) + lo (in the S region until S is staged):
+    // U = q Wf to about 16 significant bits of Wf
+    for (int i = threadIdx.x; i < D * D / 4; i += blockDim.x) {
+        const int r = i / (D / 4), c = (i % (D / 4)) * 4;
+        const float4 x = __ldg(reinterpret_cast<const float4 *>(P.Wf) + i);
+        const uint32_t h0 = pack(x.x, x.y), h1 = pack(x.z, x.w);
+        *reinterpret_cast<uint2 *>(sWF + r * LD + c) = make_uint2(h0, h1);
+        *reinterpret_cast<uint2 *>(sSP + r * LD + c) =
+            make_uint2(pack(x.x - lo_f(h0), x.y - hi_f(h0)), pack(x.z - lo_f(h1), x.w - hi_f(h1)));
+    }
+    // the linear state before the lag keys: keys < BT * i0
+    const int i0 = t0 - W > 0 ? (t0 - W) / BT : 0;
+    const int lag0 = BT * i0, lag1 = min(t0 + TOK - W, N);   // lag keys [lag0, lag1)
+    const int nlag = lag1 > lag0 ? (lag1 - lag0 + BT - 1) / BT : 0;
+    for (int f = threadIdx.x; f < D; f += blockDim.x) sZ[f] = P.zp[((size_t)unit * (P.nblk + 1) + i0) * D + f];
+
+    uint32_t qa[KC][4];
+    {
+        const uint16_t *r0 = P.q + (qrow0 + tr[0]) * D, *r1 = P.q + (qrow0 + tr[1]) * D;
+        const bool v0 = tr[0] < N, v1 = tr[1] < N;
+#pragma unroll
+        for (int kc = 0; kc < KC; ++kc) {
+            qa[kc][0] = v0 ? ld_pair(r0, 16 * kc + 2 * tig) : 0u;
+            qa[kc][1] = v1 ? ld_pair(r1, 16 * kc + 2 * tig) : 0u;
+            qa[kc][2] = v0 ? ld_pair(r0, 16 * kc + 8 + 2 * tig) : 0u;
+            qa[kc][3] = v1 ? ld_pair(r1, 16 * kc + 8 + 2 * tig) : 0u;
+        }
+    }
+    __syncthreads();
+
+    // ---- NP-Map of the query rows: u = softmax(q Wf), phi = ||q|| u / ||u||
+    float nq[2];
+    uint32_t pa[KC][4];
+    {
+        float u[NT][4];
+        zero(u);
+        mma_tile<KC, NT, true>(u, qa, sWF, LD, 0, 0);
+        mma_tile<KC, NT, true>(u, qa, sSP, LD, 0, 0);
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            float mx = -INFINITY;
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) mx = fmaxf(mx, fmaxf(u[nt][2 * r], u[nt][2 * r + 1]));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+            float s2 = 0.f, x2 = 0.f;
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                u[nt][2 * r] = expf(u[nt][2 * r] - mx);
+                u[nt][2 * r + 1] = expf(u[nt][2 * r + 1] - mx);
+                s2 = fmaf(u[nt][2 * r], u[nt][2 * r], fmaf(u[nt][2 * r + 1], u[nt][2 * r + 1], s2));
+            }
+#pragma unroll
+            for (int kc = 0; kc < KC; ++kc) {
+                const uint32_t a0 = qa[kc][r], a1 = qa[kc][r + 2];
+                x2 = fmaf(lo_f(a0), lo_f(a0), fmaf(hi_f(a0), hi_f(a0), x2));
+                x2 = fmaf(lo_f(a1), lo_f(a1), fmaf(hi_f(a1), hi_f(a1), x2));
+            }
+            s2 = quad_sum(s2);
+            x2 = quad_sum(x2);
+            nq[r] = sqrtf(x2);
+            const float sc = s2 > 0.f ? nq[r] * rsqrtf(s2) : 0.f;
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                u[nt][2 * r] *= sc;
+                u[nt][2 * r + 1] *= sc;
+            }
+        }
+#pragma unroll
+        for (int r = 0; r < 2; ++r)
+            if (tr[r] < N) {
+                uint16_t *dst = P.phq + (qrow0 + tr[r]) * D;
+                float *d32 = P.phq32 + (qrow0 + tr[r]) * D;
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    *reinterpret_cast<uint32_t *>(dst + nt * 8 + 2 * tig) = pack(u[nt][2 * r], u[nt][2 * r + 1]);
+                    *reinterpret_cast<float2 *>(d32 + nt * 8 + 2 * tig) = make_float2(u[nt][2 * r], u[nt][2 * r + 1]);
+                }
+            }
+        acc_to_a<NT>(u, pa);
+    }
+    // the linear state before the lag keys replaces Wf's low part
+    __syncthreads();
+    stage_f32(sSP, LD, P.Sp + ((size_t)unit * (P.nblk + 1) + i0) * D * D, D, D);
+    __syncthreads();
+
+    // ---- the softmax keys: kept keys of earlier chunks, then the band
+    const int tlast = min(t0 + TOK, N) - 1;
+    const int KP = dm.T_max * dm.lam;
+    const int ck = min(tlast / C, dm.T_max);
+    const int nk = dm.lam * ck;                       // kept entries of chunks before the last row's
+    const int nkb = (nk + BT - 1) / BT;
+    const int bs = max(t0 - W + 1, 0), be = tlast + 1;
+    const int nbb = (be - bs + BT - 1) / BT;
+    const int nblk = nkb + nbb;
+    const int32_t *selu = P.sel + (size_t)unit * KP;
+    auto key_pos = [&](int blk, int i) -> int {
+        if (blk < nkb) {
+            const int e = blk * BT + i;
+            const int p = e < nk ? selu[e] : -1;
+            return p < N ? p : -1;
+        }
+        const int p = bs + (blk - nkb) * BT + i;
+        return p < be ? p : -1;
+    };
+    auto stage_keys = [&](int blk, bool with_v) {
+        __syncthreads();
+        for (int i = threadIdx.x; i < BT; i += blockDim.x) sPos[i] = key_pos(blk, i);
+        __syncthreads();
+        stage_rows<D>(sK, LD, BT, [&](int r) -> const uint16_t * {
+            const int p = sPos[r];
+            return p >= 0 ? P.k + (krow0 + p) * D : nullptr;
+        });
+        if (with_v)
+            stage_rows<D>(sV, LD, BT, [&](int r) -> const uint16_t * {
+                const int p = sPos[r];
+                return p >= 0 ? P.v + (krow0 + p) * D : nullptr;
+            });
+        __syncthreads();
+    };
+    auto in_sa = [&](int t, int p, bool kept_blk) -> bool {
+        if (p < 0 || t >= N) return false;
+        if (kept_blk) return p <= t - W && p / C < t / C;
+        return p <= t && p > t - W;
+    };
+    auto logits = [&](float (&s)[4][4]) {
+        zero(s);
+        mma_tile<KC, 4, false>(s, qa, sK, LD, 0, 0);
+    };
+
+    // pass 1: c = the row maximum, at the lowest position among equal maxima
+    float cm[2] = {-INFINITY, -INFINITY};
+    int cj[2] = {INT_MAX, INT_MAX};
+    for (int blk = 0; blk < nblk; ++blk) {
+        stage_keys(blk, false);
+        float s[4][4];
+        logits(s);
+        const bool kb = blk < nkb;
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int p = sPos[nt * 8 + 2 * tig + e];
+#pragma unroll
+                for (int r = 0; r < 2; ++r) {
+                    const float x = s[nt][2 * r + e] * scale;
+                    if (in_sa(tr[r], p, kb) && (x > cm[r] || (x == cm[r] && p < cj[r]))) {
+                        cm[r] = x;
+                        cj[r] = p;
+                    }
+                }
+            }
+    }
+#pragma unroll
+    for (int r = 0; r < 2; ++r)
+#pragma unroll
+        for (int o = 1; o <= 2; o <<= 1) {
+            const float x = __shfl_xor_sync(0xffffffffu, cm[r], o);
+            const int p = __shfl_xor_sync(0xffffffffu, cj[r], o);
+            if (x > cm[r] || (x == cm[r] && p < cj[r])) {
+                cm[r] = x;
+                cj[r] = p;
+            }
+        }
+
+    // pass 2: O = P V, D_SA = sum P
+    float o[NT][4];
+    zero(o);
+    float dsa[2] = {0.f, 0.f};
+    for (int blk = 0; blk < nblk; ++blk) {
+        stage_keys(blk, true);
+        float s[4][4];
+        logits(s);
+        const bool kb = blk < nkb;
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int p = sPos[nt * 8 + 2 * tig + e];
+#pragma unroll
+                for (int r = 0; r < 2; ++r) {
+                    const float x = s[nt][2 * r + e] * scale;
+                    const float pe = in_sa(tr[r], p, kb) ? expf(x - cm[r]) : 0.f;
+                    s[nt][2 * r + e] = pe;
+                    dsa[r] += pe;
+                }
+            }
+        uint32_t pf[2][4];
+        acc_to_a<4>(s, pf);
+        mma_tile<2, NT, true>(o, pf, sV, LD, 0, 0);
+    }
+
+    // ---- the linear branch: phi(q) S + the lag keys [lag0, t - W]
+    mma_tile<KC, NT, true>(o, pa, sSP, LD, 0, 0);
+    float dlin[2] = {0.f, 0.f};
+    {
+        float ph[NT][4];   // phi back from its bf16 copy (the MMA operand)
+#pragma unroll
+        for (int kc = 0; kc < KC; ++kc) {
+            ph[2 * kc][0] = lo_f(pa[kc][0]); ph[2 * kc][1] = hi_f(pa[kc][0]);
+            ph[2 * kc][2] = lo_f(pa[kc][1]); ph[2 * kc][3] = hi_f(pa[kc][1]);
+            ph[2 * kc + 1][0] = lo_f(pa[kc][2]); ph[2 * kc + 1][1] = hi_f(pa[kc][2]);
+            ph[2 * kc + 1][2] = lo_f(pa[kc][3]); ph[2 * kc + 1][3] = hi_f(pa[kc][3]);
+        }
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const float z = sZ[nt * 8 + 2 * tig + e];
+                dlin[0] = fmaf(ph[nt][e], z, dlin[0]);
+                dlin[1] = fmaf(ph[nt][2 + e], z, dlin[1]);
+            }
+    }
+    auto stage_lag = [&](int lb) {
+        __syncthreads();
+        for (int i = threadIdx.x; i < BT; i += blockDim.x) {
+            const int p = lag0 + lb * BT + i;
+            sLag[i] = p < lag1 ? p : -1;
+        }
+        __syncthreads();
+        stage_rows<D>(sPK, LD, BT, [&](int r) -> const uint16_t * {
+            const int p = sLag[r];
+            return p >= 0 ? P.phk + (krow0 + p) * D : nullptr;
+        });
+        stage_rows<D>(sVL, LD, BT, [&](int r) -> const uint16_t * {
+            const int p = sLag[r];
+            return p >= 0 ? P.v + (krow0 + p) * D : nullptr;
+        });
+        __syncthreads();
+    };
+    for (int lb = 0; lb < nlag; ++lb) {
+        stage_lag(lb);
+        float a[4][4];
+        zero(a);
+        mma_tile<KC, 4, false>(a, pa, sPK, LD, 0, 0);
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int p = sLag[nt * 8 + 2 * tig + e];
+#pragma unroll
+                for (int r = 0; r < 2; ++r) {
+                    const bool in = p >= 0 && p <= tr[r] - W && tr[r] < N;
+                    const float x = in ? a[nt][2 * r + e] : 0.f;
+                    a[nt][2 * r + e] = x;
+                    dlin[r] += x;
+                }
+            }
+        uint32_t af[2][4];
+        acc_to_a<4>(a, af);
+        mma_tile<2, NT, true>(o, af, sVL, LD, 0, 0);
+    }
+
+    // ---- y, g = dy / den, delta = g . y
+    float den[2], inv[2], delta[2];
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+        den[r] = quad_sum(dsa[r]) + quad_sum(dlin[r]);
+        inv[r] = den[r] != 0.f ? 1.f / den[r] : 0.f;
+    }
+    {
+        float dd[2] = {0.f, 0.f};
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            const uint16_t *dyr = P.dy + (qrow0 + tr[r]) * D;
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                const uint32_t pr = tr[r] < N ? ld_pair(dyr, nt * 8 + 2 * tig) : 0u;
+                const float g0 = lo_f(pr) * inv[r], g1 = hi_f(pr) * inv[r];
+                dd[r] = fmaf(g0, o[nt][2 * r] * inv[r], fmaf(g1, o[nt][2 * r + 1] * inv[r], dd[r]));
+                o[nt][2 * r] = g0;
+                o[nt][2 * r + 1] = g1;
+            }
+            delta[r] = quad_sum(dd[r]);
+        }
+    }
+#pragma unroll
+    for (int r = 0; r < 2; ++r)
+        if (tr[r] < N) {
+            uint16_t *dst = P.g + (qrow0 + tr[r]) * D;
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+                *reinterpret_cast<uint32_t *>(dst + nt * 8 + 2 * tig) = pack(o[nt][2 * r], o[nt][2 * r + 1]);
+        }
+    // dy itself (exact in bf16) is the MMA operand; 1/den scales the products
+    uint32_t ya[KC][4];
+    {
+        const uint16_t *r0 = P.dy + (qrow0 + tr[0]) * D, *r1 = P.dy + (qrow0 + tr[1]) * D;
+        const bool v0 = tr[0] < N, v1 = tr[1] < N;
+#pragma unroll
+        for (int kc = 0; kc < KC; ++kc) {
+            ya[kc][0] = v0 ? ld_pair(r0, 16 * kc + 2 * tig) : 0u;
+            ya[kc][1] = v1 ? ld_pair(r1, 16 * kc + 2 * tig) : 0u;
+            ya[kc][2] = v0 ? ld_pair(r0, 16 * kc + 8 + 2 * tig) : 0u;
+            ya[kc][3] = v1 ? ld_pair(r1, 16 * kc + 8 + 2 * tig) : 0u;
+        }
+    }
+
+    // pass 3: dP = g V^T = (dy V^T) / den, dS = P (dP - delta), dq = dS K
+    float dq[NT][4];
+    zero(dq);
+    float dss[2] = {0.f, 0.f};
+    for (int blk = 0; blk < nblk; ++blk) {
+        stage_keys(blk, true);
+        float s[4][4], dp[4][4];
+        logits(s);
+        zero(dp);
+        mma_tile<KC, 4, false>(dp, ya, sV, LD, 0, 0);
+        const bool kb = blk < nkb;
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int p = sPos[nt * 8 + 2 * tig + e];
+#pragma unroll
+                for (int r = 0; r < 2; ++r) {
+                    const float x = s[nt][2 * r + e] * scale;
+                    const float pe = in_sa(tr[r], p, kb) ? expf(x - cm[r]) : 0.f;
+                    const float ds = pe * (dp[nt][2 * r + e] * inv[r] - delta[r]);
+                    s[nt][2 * r + e] = ds;
+                    dss[r] += ds;
+                }
+            }
+        uint32_t sf[2][4];
+        acc_to_a<4>(s, sf);
+        mma_tile<2, NT, true>(dq, sf, sK, LD, 0, 0);
+    }
+    // the stabiliser's gradient at the row-max key, then the 1/sqrt(d) of the logits
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+        dss[r] = quad_sum(dss[r]);
+        const bool ok = tr[r] < N && cj[r] >= 0 && cj[r] < N;
+        const uint16_t *kr = P.k + (krow0 + (ok ? cj[r] : 0)) * D;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            const uint32_t pr = ok ? ld_pair(kr, nt * 8 + 2 * tig) : 0u;
+            dq[nt][2 * r] = (dq[nt][2 * r] - dss[r] * lo_f(pr)) * scale;
+            dq[nt][2 * r + 1] = (dq[nt][2 * r + 1] - dss[r] * hi_f(pr)) * scale;
+        }
+    }
+
+    // ---- dphi(q) = S g - delta z + sum_lag phi(k) (g . v - delta)
+    {
+        float dph[NT][4];
+        zero(dph);
+        mma_tile<KC, NT, false>(dph, ya, sSP, LD, 0, 0);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const float z = sZ[nt * 8 + 2 * tig + e];
+                dph[nt][e] = dph[nt][e] * inv[0] - delta[0] * z;
+                dph[nt][2 + e] = dph[nt][2 + e] * inv[1] - delta[1] * z;
+            }
+        for (int lb = 0; lb < nlag; ++lb) {
+            stage_lag(lb);
+            float da[4][4];
+            zero(da);
+            mma_tile<KC, 4, false>(da, ya, sVL, LD, 0, 0);
+#pragma unroll
+            for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int p = sLag[nt * 8 + 2 * tig + e];
+#pragma unroll
+                    for (int r = 0; r < 2; ++r) {
+                        const bool in = p >= 0 && p <= tr[r] - W && tr[r] < N;
+                        da[nt][2 * r + e] = in ? da[nt][2 * r + e] * inv[r] - delta[r] : 0.f;
+                    }
+                }
+            uint32_t df[2][4];
+            acc_to_a<4>(da, df);
+            mma_tile<2, NT, true>(dph, df, sPK, LD, 0, 0);
+        }
+        // NP-Map backward: dl = phi (dphi - a phi / ||q||), a = dphi . phi / ||q||, with the
+        // fp32 phi this thread wrote
+        float ph[NT][4];
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            const float *src = P.phq32 + (qrow0 + (tr[r] < N ? tr[r] : 0)) * D;
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                const float2 x = tr[r] < N ? *reinterpret_cast<const float2 *>(src + nt * 8 + 2 * tig) : make_float2(0.f, 0.f);
+                ph[nt][2 * r] = x.x;
+                ph[nt][2 * r + 1] = x.y;
+            }
+        }
+        float an[2];
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            float a = 0.f;
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) a = fmaf(dph[nt][2 * r], ph[nt][2 * r], fmaf(dph[nt][2 * r + 1], ph[nt][2 * r + 1], a));
+            const float iq = nq[r] > 0.f ? 1.f / nq[r] : 0.f;
+            a = quad_sum(a) * iq;
+            an[r] = a * iq;
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int e = 0; e < 2; ++e)
+                    dph[nt][2 * r + e] = ph[nt][2 * r + e] * (dph[nt][2 * r + e] - an[r] * ph[nt][2 * r + e]);
+        }
+#pragma unroll
+        for (int r = 0; r < 2; ++r)
+            if (tr[r] < N) {
+                float *dst = P.dlq + (qrow0 + tr[r]) * D;
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+                    *reinterpret_cast<float2 *>(dst + nt * 8 + 2 * tig) = make_float2(dph[nt][2 * r], dph[nt][2 * r + 1]);
+            }
+        // dq += a x / ||x|| + dl Wf^T
+#pragma unroll
+        for (int kc = 0; kc < KC; ++kc)
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                dq[2 * kc][2 * r] += an[r] * lo_f(qa[kc][r]);
+                dq[2 * kc][2 * r + 1] += an[r] * hi_f(qa[kc][r]);
+                dq[2 * kc + 1][2 * r] += an[r] * lo_f(qa[kc][r + 2]);
+                dq[2 * kc + 1][2 * r + 1] += an[r] * hi_f(qa[kc][r + 2]);
+            }
+        uint32_t lf[KC][4];
+        acc_to_a<NT>(dph, lf);
+        mma_tile<KC, NT, false>(dq, lf, sWF, LD, 0, 0);
+    }
+
+    // ---- outputs
+#pragma unroll
+    for (int r = 0; r < 2; ++r)
+        if (tr[r] < N) {
+            float *dst = P.dq + (qrow0 + tr[r]) * D;
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+                *reinterpret_cast<float2 *>(dst + nt * 8 + 2 * tig) = make_float2(dq[nt][2 * r], dq[nt][2 * r + 1]);
+            if (tig == 0) {
+                const size_t ri = qrow0 + tr[r];
+                P.rc[ri] = cm[r];
+                P.rdelta[ri] = delta[r];
+                P.rds[ri] = dss[r];
+                P.rinv[ri] = inv[r];
+                P.rjs[ri] = cj[r];
+                if (P.cidx) P.cidx[ri] = cj[r];
+            }
+        }
+}
+
+// ---------------------------------------------------------------------------
+// key passes: a warp owns 16 keys (rows of the transposed products)
+// ---------------------------------------------------------------------------
+template <int D>
+struct KLayout {
+    static constexpr int LD = D + 8, T32 = BT * LD * 2;
+    static constexpr int K = 0, V = K + 2 * T32, PK = V + 2 * T32;   // 64 keys each
+    static constexpr int Q = PK + 2 * T32, G = Q + T32, PQ = G + T32;  // one 32-row query block
+    static constexpr int R = PQ + T32;        // R [df][d] bf16 of the linear pass, then Wf [d][df]
+    static constexpr int RV = R + D * LD * 2; // r, fp32 [df]
+    static constexpr int ROW = RV + D * 4;    // per query row: token, c, delta, ds sum, 1/den, c position
+    static constexpr int KPOS = ROW + 6 * BT * 4;   // positions of the 64 keys
+    static constexpr int TOTAL = KPOS + 64 * 4;
+};
+
+// The query rows of one block (32 rows of one head), their scalars, and the
+// rows of q, g (and phi(q)) in shared memory.
+struct QRows {
+    int *tok;
+    float *c, *delta, *dss, *inv;
+    int *js;
+};
+
+template <int D>
+__device__ __forceinline__ void stage_qblock(const BwdArgs &P, int b, int h, int tq0, int tq1, bool with_phq,
+                                             uint16_t *sQ, uint16_t *sG, uint16_t *sPQ, QRows R)
+{
+    constexpr int LD = D + 8;
+    const Dims &dm = P.dm;
+    const size_t row0 = (size_t)(b * dm.Hq + h) * dm.N;
+    __syncthreads();
+    for (int i = threadIdx.x; i < BT; i += blockDim.x) {
+        const int t = tq0 + i;
+        const bool ok = t < tq1 && t < dm.N;
+        R.tok[i] = ok ? t : -1;
+        R.c[i] = ok ? P.rc[row0 + t] : 0.f;
+        R.delta[i] = ok ? P.rdelta[row0 + t] : 0.f;
+        R.dss[i] = ok ? P.rds[row0 + t] : 0.f;
+        R.inv[i] = ok ? P.rinv[row0 + t] : 0.f;
+        R.js[i] = ok ? P.rjs[row0 + t] : -1;
+    }
+    __syncthreads();
+    stage_rows<D>(sQ, LD, BT, [&](int r) -> const uint16_t * { return R.tok[r] >= 0 ? P.q + (row0 + R.tok[r]) * D : nullptr; });
+    stage_rows<D>(sG, LD, BT, [&](int r) -> const uint16_t * { return R.tok[r] >= 0 ? P.dy + (row0 + R.tok[r]) * D : nullptr; });
+    if (with_phq)
+        stage_rows<D>(sPQ, LD, BT, [&](int r) -> const uint16_t * { return R.tok[r] >= 0 ? P.phq + (row0 + R.tok[r]) * D : nullptr; });
+    __syncthreads();
+}
+
+// dK += dS^T Q, dV += P^T G over one staged query block for the warp's 16 keys
+// (sG holds dy: G = dy / den, the row's 1/den applied to the products)
+// (rows key0 .. key0+15 of sK / sV at positions kpos[]); `pair(t, p)` says
+// whether key p is a softmax key of query t in this pass.
+template <int D, typename Pair>
+__device__ __forceinline__ void kv_block(const uint16_t *sK, const uint16_t *sV, int key0, const int *kpos,
+                                         const uint16_t *sQ, const uint16_t *sG, QRows R, float scale,
+                                         float (&dK)[D / 8][4], float (&dV)[D / 8][4], Pair pair)
+{
+    constexpr int LD = D + 8, KC = D / 16, NT = D / 8;
+    const int lane = threadIdx.x & 31, gid = lane >> 2, tig = lane & 3;
+    float s[4][4], dp[4][4];
+    zero(s);
+    zero(dp);
+#pragma unroll
+    for (int kc = 0; kc < KC; ++kc) {
+        uint32_t ka[4], va[4];
+        load_a(sK, LD, key0, kc * 16, ka);
+        load_a(sV, LD, key0, kc * 16, va);
+#pragma unroll
+        for (int nt = 0; nt < 4; nt += 2) {
+            uint32_t f[4];
+            load_b(sQ, LD, nt * 8, kc * 16, f);
+            mma(s[nt], ka, f[0], f[1]);
+            mma(s[nt + 1], ka, f[2], f[3]);
+            load_b(sG, LD, nt * 8, kc * 16, f);
+            mma(dp[nt], va, f[0], f[1]);
+            mma(dp[nt + 1], va, f[2], f[3]);
+        }
+    }
+    const int kp[2] = {kpos[key0 + gid], kpos[key0 + gid + 8]};
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int qi = nt * 8 + 2 * tig + e;
+            const int t = R.tok[qi];
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                const bool in = t >= 0 && kp[r] >= 0 && pair(t, kp[r]);
+                const float pe = in ? expf(s[nt][2 * r + e] * scale - R.c[qi]) : 0.f;
+                float ds = pe * (dp[nt][2 * r + e] * R.inv[qi] - R.delta[qi]);
+                if (in && R.js[qi] == kp[r]) ds -= R.dss[qi];
+                s[nt][2 * r + e] = pe * R.inv[qi];
+                dp[nt][2 * r + e] = ds;
+            }
+        }
+    uint32_t pf[2][4], sf[2][4];
+    acc_to_a<4>(s, pf);
+    acc_to_a<4>(dp, sf);
+    mma_tile<2, NT, true>(dK, sf, sQ, LD, 0, 0);
+    mma_tile<2, NT, true>(dV, pf, sG, LD, 0, 0);
+}
+
+template <int D, int G>
+__global__ void __launch_bounds__(BQ_THREADS, 1) key_kernel(BwdArgs P)
+{
+    grid_dep_sync();
+    constexpr int LD = D + 8, KC = D / 16, NT = D / 8;
+    using L = KLayout<D>;
+    extern __shared__ __align__(16) uint8_t smem[];
+    uint16_t *sK = (uint16_t *)(smem + L::K), *sV = (uint16_t *)(smem + L::V), *sPK = (uint16_t *)(smem + L::PK);
+    uint16_t *sQ = (uint16_t *)(smem + L::Q), *sG = (uint16_t *)(smem + L::G), *sPQ = (uint16_t *)(smem + L::PQ);
+    uint16_t *sR = (uint16_t *)(smem + L::R);
+    float *sRV = (float *)(smem + L::RV);
+    int *rowi = (int *)(smem + L::ROW);
+    QRows R{rowi, (float *)(rowi + BT), (float *)(rowi + 2 * BT), (float *)(rowi + 3 * BT), (float *)(rowi + 4 * BT),
+            rowi + 5 * BT};
+    int *kpos = (int *)(smem + L::KPOS);
+
+    const Dims &dm = P.dm;
+    const int N = dm.N, W = dm.W;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gid = lane >> 2, tig = lane & 3;
+    const int unit = blockIdx.y, b = unit / dm.Hkv, gq = unit % dm.Hkv;
+    const int j0 = blockIdx.x * 64;
+    const size_t krow0 = (size_t)unit * N;
+    const int key0 = warp * 16;
+    const int kr[2] = {j0 + key0 + gid, j0 + key0 + gid + 8};
+
+    for (int i = threadIdx.x; i < 64; i += blockDim.x) kpos[i] = j0 + i < N ? j0 + i : -1;
+    __syncthreads();
+    stage_rows<D>(sK, LD, 64, [&](int r) -> const uint16_t * { return kpos[r] >= 0 ? P.k + (krow0 + kpos[r]) * D : nullptr; });
+    stage_rows<D>(sV, LD, 64, [&](int r) -> const uint16_t * { return kpos[r] >= 0 ? P.v + (krow0 + kpos[r]) * D : nullptr; });
+    stage_rows<D>(sPK, LD, 64, [&](int r) -> const uint16_t * { return kpos[r] >= 0 ? P.phk + (krow0 + kpos[r]) * D : nullptr; });
+
+    // ---- window queries: t in [j, j + W - 1]
+    float dK[NT][4], dV[NT][4];
+    zero(dK);
+    zero(dV);
+    const int tq_end = min(j0 + 64 + W - 1, N);
+    for (int hh = 0; hh < G; ++hh) {
+        const int h = gq * G + hh;
+        for (int tq0 = j0; tq0 < tq_end; tq0 += BT) {
+            stage_qblock<D>(P, b, h, tq0, tq_end, false, sQ, sG, sPQ, R);
+            kv_block<D>(sK, sV, key0, kpos, sQ, sG, R, P.scale, dK, dV,
+                        [&](int t, int p) { return p <= t && p > t - W; });
+        }
+    }
+#pragma unroll
+    for (int r = 0; r < 2; ++r)
+        if (kr[r] < N) {
+            float *dst = P.dk + (krow0 + kr[r]) * D;
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+                *reinterpret_cast<float2 *>(dst + nt * 8 + 2 * tig) = make_float2(dK[nt][0 + 2 * r] * P.scale, dK[nt][1 + 2 * r] * P.scale);
+        }
+
+    // ---- linear branch: R, r over the queries t >= U1, then the lag queries [j + W, U1)
+    const int U1 = ((j0 + 63 + W + BT - 1) / BT) * BT;
+    const int ub = min(U1 / BT, P.nblk);
+    const size_t rslot = (size_t)unit * (P.nblk + 1) + (P.nblk - ub);
+    __syncthreads();
+    stage_f32(sR, LD, P.Rs + rslot * D * D, D, D);
+    for (int f = threadIdx.x; f < D; f += blockDim.x) sRV[f] = P.rs[rslot * D + f];
+    __syncthreads();
+    const bool kk[2] = {kr[0] < N && P.kept[krow0 + kr[0]] != 0, kr[1] < N && P.kept[krow0 + kr[1]] != 0};
+    float dph[NT][4];
+    zero(dph);
+    {
+        uint32_t va[KC][4], pk[KC][4];
+#pragma unroll
+        for (int kc = 0; kc < KC; ++kc) {
+            load_a(sV, LD, key0, kc * 16, va[kc]);
+            load_a(sPK, LD, key0, kc * 16, pk[kc]);
+        }
+        mma_tile<KC, NT, false>(dph, va, sR, LD, 0, 0);   // V R^T: B(k = d, n = f) = R[f][d]
+        mma_tile<KC, NT, true>(dV, pk, sR, LD, 0, 0);     // phi(K) R: B(k = f, n = d) = R[f][d]
+    }
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const float rv = sRV[nt * 8 + 2 * tig + e];
+            dph[nt][e] -= rv;
+            dph[nt][2 + e] -= rv;
+        }
+    const int lq0 = j0 + W, lq1 = min(U1, N);
+    for (int hh = 0; hh < G; ++hh) {
+        const int h = gq * G + hh;
+        for (int tq0 = lq0; tq0 < lq1; tq0 += BT) {
+            stage_qblock<D>(P, b, h, tq0, lq1, true, sQ, sG, sPQ, R);
+            float dat[4][4], at[4][4];
+            zero(dat);
+            zero(at);
+#pragma unroll
+            for (int kc = 0; kc < KC; ++kc) {
+                uint32_t va[4], pk[4];
+                load_a(sV, LD, key0, kc * 16, va);
+                load_a(sPK, LD, key0, kc * 16, pk);
+#pragma unroll
+                for (int nt = 0; nt < 4; nt += 2) {
+                    uint32_t f[4];
+                    load_b(sG, LD, nt * 8, kc * 16, f);
+                    mma(dat[nt], va, f[0], f[1]);
+                    mma(dat[nt + 1], va, f[2], f[3]);
+                    load_b(sPQ, LD, nt * 8, kc * 16, f);
+                    mma(at[nt], pk, f[0], f[1]);
+                    mma(at[nt + 1], pk, f[2], f[3]);
+                }
+            }
+#pragma unroll
+            for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int qi = nt * 8 + 2 * tig + e;
+                    const int t = R.tok[qi];
+#pragma unroll
+                    for (int r = 0; r < 2; ++r) {
+                        const bool in = t >= 0 && kr[r] < N && t >= kr[r] + W;
+                        dat[nt][2 * r + e] = in ? dat[nt][2 * r + e] * R.inv[qi] - R.delta[qi] : 0.f;
+                        at[nt][2 * r + e] = in ? at[nt][2 * r + e] * R.inv[qi] : 0.f;
+                    }
+                }
+            uint32_t df[2][4], af[2][4];
+            acc_to_a<4>(dat, df);
+            acc_to_a<4>(at, af);
+            mma_tile<2, NT, true>(dph, df, sPQ, LD, 0, 0);
+            mma_tile<2, NT, true>(dV, af, sG, LD, 0, 0);
+        }
+    }
+    // kept keys have no linear role
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int r = 0; r < 2; ++r)
+            if (kk[r] || kr[r] >= N) dph[nt][2 * r] = dph[nt][2 * r + 1] = 0.f;
+
+    // ---- NP-Map backward of the key rows (Wf replaces R in shared memory)
+    __syncthreads();
+    for (int i = threadIdx.x; i < D * D / 4; i += blockDim.x) {
+        const int r = i / (D / 4), c = (i % (D / 4)) * 4;
+        const float4 x = __ldg(reinterpret_cast<const float4 *>(P.Wf) + i);
+        *reinterpret_cast<uint2 *>(sR + r * LD + c) = make_uint2(pack(x.x, x.y), pack(x.z, x.w));
+    }
+    __syncthreads();
+    float ph[NT][4], xk[NT][4];
+    float an[2];
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+        const int row = key0 + gid + 8 * r;
+        float a = 0.f, x2 = 0.f;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int col = nt * 8 + 2 * tig + e;
+                ph[nt][2 * r + e] = kr[r] < N ? P.phk32[(krow0 + kr[r]) * D + col] : 0.f;
+                xk[nt][2 * r + e] = bf2f(sK[row * LD + col]);
+                a = fmaf(dph[nt][2 * r + e], ph[nt][2 * r + e], a);
+                x2 = fmaf(xk[nt][2 * r + e], xk[nt][2 * r + e], x2);
+            }
+        const float nk = sqrtf(quad_sum(x2));
+        const float ik = nk > 0.f ? 1.f / nk : 0.f;
+        an[r] = quad_sum(a) * ik * ik;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int e = 0; e < 2; ++e)
+                dph[nt][2 * r + e] = ph[nt][2 * r + e] * (dph[nt][2 * r + e] - an[r] * ph[nt][2 * r + e]);
+    }
+    float dkn[NT][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) dkn[nt][i] = an[i >> 1] * xk[nt][i];
+    uint32_t lf[KC][4];
+    acc_to_a<NT>(dph, lf);
+    mma_tile<KC, NT, false>(dkn, lf, sR, LD, 0, 0);   // dl Wf^T: B(k = f, n = i) = Wf[i][f]
+#pragma unroll
+    for (int r = 0; r < 2; ++r)
+        if (kr[r] < N) {
+            float *dst = P.dk + (krow0 + kr[r]) * D;
+            float *dvd = P.dv + (krow0 + kr[r]) * D;
+            float *dl = P.dlk + (krow0 + kr[r]) * D;
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                float2 *p2 = reinterpret_cast<float2 *>(dst + nt * 8 + 2 * tig);
+                const float2 old = *p2;
+                *p2 = make_float2(old.x + dkn[nt][2 * r], old.y + dkn[nt][2 * r + 1]);
+                *reinterpret_cast<float2 *>(dvd + nt * 8 + 2 * tig) = make_float2(dV[nt][2 * r], dV[nt][2 * r + 1]);
+                *reinterpret_cast<float2 *>(dl + nt * 8 + 2 * tig) = make_float2(dph[nt][2 * r], dph[nt][2 * r + 1]);
+            }
+        }
+}
+
+// dk, dv of the kept keys from the queries of later chunks outside the window:
+// CTA = 64 entries of the kept table x one range of query tokens.
+constexpr int KEPT_TOKENS = 256;
+
+template <int D, int G>
+__global__ void __launch_bounds__(BQ_THREADS, 2) kept_kernel(BwdArgs P)
+{
+    grid_dep_sync();
+    constexpr int LD = D + 8, NT = D / 8;
+    using L = KLayout<D>;
+    extern __shared__ __align__(16) uint8_t smem[];
+    uint16_t *sK = (uint16_t *)(smem + L::K), *sV = (uint16_t *)(smem + L::V);
+    uint16_t *sQ = (uint16_t *)(smem + L::Q), *sG = (uint16_t *)(smem + L::G), *sPQ = (uint16_t *)(smem + L::PQ);
+    int *rowi = (int *)(smem + L::ROW);
+    QRows R{rowi, (float *)(rowi + BT), (float *)(rowi + 2 * BT), (float *)(rowi + 3 * BT), (float *)(rowi + 4 * BT),
+            rowi + 5 * BT};
+    int *kpos = (int *)(smem + L::KPOS);
+
+    const Dims &dm = P.dm;
+    const int N = dm.N, W = dm.W, C = dm.C;
+    const int KP = dm.T_max * dm.lam;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gid = lane >> 2, tig = lane & 3;
+    const int unit = blockIdx.y, b = unit / dm.Hkv, gq = unit % dm.Hkv;
+    const int e0 = blockIdx.x * 64;
+    const size_t krow0 = (size_t)unit * N;
+    const int key0 = warp * 16;
+    // queries of this CTA: tokens [tq_lo, tq_hi), from the end of the first entry's chunk on
+    auto entry = [&](int e) -> int {
+        const int p = e < KP ? P.sel[(size_t)unit * KP + e] : -1;
+        return p < N ? p : -1;
+    };
+    int first = -1;
+    for (int i = 0; i < 64 && first < 0; ++i) first = entry(e0 + i);
+    if (first < 0) return;
+    const int start = (first / C + 1) * C;
+    const int tq_lo = start + blockIdx.z * KEPT_TOKENS, tq_hi = min(tq_lo + KEPT_TOKENS, N);
+    if (tq_lo >= tq_hi) return;
+
+    for (int i = threadIdx.x; i < 64; i += blockDim.x) kpos[i] = entry(e0 + i);
+    __syncthreads();
+    stage_rows<D>(sK, LD, 64, [&](int r) -> const uint16_t * { return kpos[r] >= 0 ? P.k + (krow0 + kpos[r]) * D : nullptr; });
+    stage_rows<D>(sV, LD, 64, [&](int r) -> const uint16_t * { return kpos[r] >= 0 ? P.v + (krow0 + kpos[r]) * D : nullptr; });
+
+    float dK[NT][4], dV[NT][4];
+    zero(dK);
+    zero(dV);
+    for (int hh = 0; hh < G; ++hh) {
+        const int h = gq * G + hh;
+        for (int tq0 = tq_lo; tq0 < tq_hi; tq0 += BT) {
+            stage_qblock<D>(P, b, h, tq0, tq_hi, false, sQ, sG, sPQ, R);
+            kv_block<D>(sK, sV, key0, kpos, sQ, sG, R, P.scale, dK, dV,
+                        [&](int t, int p) { return p <= t - W && p / C < t / C; });
+        }
+    }
+    const int kp[2] = {kpos[key0 + gid], kpos[key0 + gid + 8]};
+#pragma unroll
+    for (int r = 0; r < 2; ++r)
+        if (kp[r] >= 0) {
+            float *dk = P.dk + (krow0 + kp[r]) * D, *dv = P.dv + (krow0 + kp[r]) * D;
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                const int col = nt * 8 + 2 * tig;
+                atomicAdd(dk + col, dK[nt][2 * r] * P.scale);
+                atomicAdd(dk + col + 1, dK[nt][2 * r + 1] * P.scale);
+                atomicAdd(dv + col, dV[nt][2 * r]);
+                atomicAdd(dv + col + 1, dV[nt][2 * r + 1]);
+            }
+        }
+}
+
+// dWf = sum_rows x^T dl over the q rows and the k rows: CTA = a range of rows,
+// warp w the Wf rows [16w, 16w + 16); partial sums added atomically.  dl is
+// fp32; it enters the MMAs as a bf16 pair hi + lo (hi = bf16(dl), lo =
+// bf16(dl - hi)), about 16 significant bits.
+constexpr int DWF_ROWS = 1024;
+
+template <int D, int DF>
+__global__ void __launch_bounds__(256) dwf_kernel(const uint16_t *__restrict__ x, const float *__restrict__ dl,
+                                                  long long rows, float *__restrict__ dWf)
+{
+    grid_dep_sync();
+    constexpr int LDX = D + 8, LDL = DF + 8, NT = DF / 8;
+    __shared__ __align__(16) uint16_t sx[BT * LDX];
+    __shared__ __align__(16) uint16_t sl[BT * LDL];
+    __shared__ __align__(16) uint16_t sl2[BT * LDL];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gid = lane >> 2, tig = lane & 3;
+    const long long r0 = (long long)blockIdx.x * DWF_ROWS;
+    const long long r1 = min(r0 + DWF_ROWS, rows);
+    float acc[NT][4];
+    zero(acc);
+    for (long long rb = r0; rb < r1; rb += BT) {
+        __syncthreads();
+        stage_rows<D>(sx, LDX, BT, [&](int r) -> const uint16_t * { return rb + r < r1 ? x + (rb + r) * D : nullptr; });
+        for (int i = threadIdx.x; i < BT * DF / 4; i += blockDim.x) {
+            const int r = i / (DF / 4), c = (i % (DF / 4)) * 4;
+            float4 f = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (rb + r < r1) f = __ldg(reinterpret_cast<const float4 *>(dl + (rb + r) * DF + c));
+            const uint32_t h0 = pack(f.x, f.y), h1 = pack(f.z, f.w);
+            *reinterpret_cast<uint2 *>(sl + r * LDL + c) = make_uint2(h0, h1);
+            *reinterpret_cast<uint2 *>(sl2 + r * LDL + c) =
+                make_uint2(pack(f.x - lo_f(h0), f.y - hi_f(h0)), pack(f.z - lo_f(h1), f.w - hi_f(h1)));
+        }
+        __syncthreads();
+        if (warp < D / 16) {
+#pragma unroll
+            for (int k0 = 0; k0 < BT; k0 += 16) {
+                uint32_t a[1][4];
+                load_a_t(sx, LDX, warp * 16, k0, a[0]);
+                mma_tile<1, NT, true>(acc, a, sl, LDL, 0, k0);
+                mma_tile<1, NT, true>(acc, a, sl2, LDL, 0, k0);
+            }
+        }
+    }
+    if (warp < D / 16) {
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            const int col = nt * 8 + 2 * tig;
+            float *o0 = dWf + (size_t)(warp * 16 + gid) * DF + col, *o1 = o0 + 8 * DF;
+            atomicAdd(o0, acc[nt][0]);
+            atomicAdd(o0 + 1, acc[nt][1]);
+            atomicAdd(o1, acc[nt][2]);
+            atomicAdd(o1 + 1, acc[nt][3]);
+        }
+    }
+}
+
+struct BwdBuffers {
+    uint8_t *kept;
+    uint16_t *phk;
+    float *phk32;
+    float *Sp, *zp, *Rs, *rs;
+};
+
+template <typename K>
+cudaError_t set_smem(K kern, size_t bytes)
+{
+    return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+}
+
+template <int D, int G>
+cudaError_t run(const BwdArgs &A, const BwdBuffers &bb, cudaStream_t s)
+{
+    const Dims &dm = A.dm;
+    const int units = dm.B * dm.Hkv;
+    const int KP = dm.T_max * dm.lam;
+    cudaError_t e = cudaSuccess;
+    auto chk = [&](cudaError_t x) {
+        if (e == cudaSuccess && x != cudaSuccess) e = x;
+        if (e == cudaSuccess) e = cudaGetLastError();
+    };
+    {
+        KTimer tm("bwd_prep", s);
+        chk(cudaMemsetAsync(bb.kept, 0, (size_t)units * dm.N, s));
+        if (KP > 0) chk(launch_kernel(mark_kept_kernel, dim3((KP + 255) / 256, units), dim3(256), 0, s, A.sel, KP, dm.N, bb.kept));
+        const long long rows = (long long)units * dm.N;
+        const int grid = (int)min((rows + 7) / 8, 152LL * 16);
+        chk(launch_kernel(phik_kernel<D, D>, dim3(grid), dim3(256), 0, s, A, bb.phk, bb.phk32));
+    }
+    const size_t bs_smem = BSLayout<D, D>::TOTAL;
+    const int nel_s = D * D, nel_z = D;
+    {
+        KTimer tm("bwd_state", s);
+        chk(set_smem(blocksum_kernel<D, D, false>, bs_smem));
+        chk(launch_kernel(blocksum_kernel<D, D, false>, dim3(A.nblk, units), dim3(256), bs_smem, s, A, bb.Sp, bb.zp));
+        chk(launch_kernel(scan_kernel, dim3((nel_s + nel_z + 255) / 256, units), dim3(256), 0, s, bb.Sp, bb.zp, A.nblk,
+                          nel_s, nel_z));
+    }
+    {
+        KTimer tm("bwd_query", s);
+        constexpr int TOK = 16 * (4 / G);
+        chk(set_smem(query_kernel<D, G>, QLayout<D>::TOTAL));
+        chk(launch_kernel(query_kernel<D, G>, dim3((dm.N + TOK - 1) / TOK, units), dim3(BQ_THREADS), QLayout<D>::TOTAL, s, A));
+    }
+    {
+        KTimer tm("bwd_rstate", s);
+        chk(set_smem(blocksum_kernel<D, D, true>, bs_smem));
+        chk(launch_kernel(blocksum_kernel<D, D, true>, dim3(A.nblk, units), dim3(256), bs_smem, s, A, bb.Rs, bb.rs));
+        chk(launch_kernel(scan_kernel, dim3((nel_s + nel_z + 255) / 256, units), dim3(256), 0, s, bb.Rs, bb.rs, A.nblk,
+                          nel_s, nel_z));
+    }
+    {
+        KTimer tm("bwd_key", s);
+        chk(set_smem(key_kernel<D, G>, KLayout<D>::TOTAL));
+        chk(launch_kernel(key_kernel<D, G>, dim3((dm.N + 63) / 64, units), dim3(BQ_THREADS), KLayout<D>::TOTAL, s, A));
+    }
+    if (KP > 0) {
+        KTimer tm("bwd_kept", s);
+        chk(set_smem(kept_kernel<D, G>, KLayout<D>::TOTAL));
+        const int nsplit = (dm.N + KEPT_TOKENS - 1) / KEPT_TOKENS;
+        chk(launch_kernel(kept_kernel<D, G>, dim3((KP + 63) / 64, units, nsplit), dim3(BQ_THREADS), KLayout<D>::TOTAL, s, A));
+    }
+    {
+        KTimer tm("bwd_dwf", s);
+        chk(cudaMemsetAsync(A.dWf, 0, (size_t)D * D * 4, s));
+        const long long rq = (long long)dm.B * dm.Hq * dm.N, rk = (long long)units * dm.N;
+        chk(launch_kernel(dwf_kernel<D, D>, dim3((unsigned)((rq + DWF_ROWS - 1) / DWF_ROWS)), dim3(256), 0, s, A.q,
+                          (const float *)A.dlq, rq, A.dWf));
+        chk(launch_kernel(dwf_kernel<D, D>, dim3((unsigned)((rk + DWF_ROWS - 1) / DWF_ROWS)), dim3(256), 0, s, A.k,
+                          (const float *)A.dlk, rk, A.dWf));
+    }
+    return e;
+}
+
+}  // namespace
+
+BwdLayout bwd_layout(const Dims &dm)
+{
+    auto al = [](size_t x) { return (x + 255) & ~size_t(255); };
+    BwdLayout L;
+    const size_t units = (size_t)dm.B * dm.Hkv, rows_q = (size_t)dm.B * dm.Hq * dm.N, rows_k = units * dm.N;
+    const int nblk = (dm.N + BT - 1) / BT;
+    size_t o = 0;
+    L.kept = o; o += al(rows_k);
+    L.phk = o; o += al(rows_k * dm.df * 2);
+    L.Sp = o; o += al(units * (nblk + 1) * (size_t)dm.df * dm.d * 4);
+    L.zp = o; o += al(units * (nblk + 1) * (size_t)dm.df * 4);
+    L.Rs = o; o += al(units * (nblk + 1) * (size_t)dm.df * dm.d * 4);
+    L.rs = o; o += al(units * (nblk + 1) * (size_t)dm.df * 4);
+    L.g = o; o += al(rows_q * dm.d * 2);
+    L.phq = o; o += al(rows_q * dm.df * 2);
+    L.phq32 = o; o += al(rows_q * dm.df * 4);
+    L.phk32 = o; o += al(rows_k * dm.df * 4);
+    L.dlq = o; o += al(rows_q * dm.df * 4);
+    L.dlk = o; o += al(rows_k * dm.df * 4);
+    L.rc = o; o += al(rows_q * 4);
+    L.rinv = o; o += al(rows_q * 4);
+    L.rdelta = o; o += al(rows_q * 4);
+    L.rds = o; o += al(rows_q * 4);
+    L.rjs = o; o += al(rows_q * 4);
+    L.total = o;
+    return L;
+}
+
+bool backward_supported(const Dims &dm)
+{
+    return dm.d == dm.df && (dm.d == 64 || dm.d == 128) && (dm.G == 1 || dm.G == 2 || dm.G == 4) && dm.W >= dm.C;
+}
+
+cudaError_t launch_backward(const Dims &dm, const BwdInputs &in, void *ws)
+{
+    const BwdLayout L = bwd_layout(dm);
+    char *base = (char *)ws;
+    BwdArgs A{};
+    A.dm = dm;
+    A.nblk = (dm.N + BT - 1) / BT;
+    A.scale = 1.f / sqrtf((float)dm.d);
+    A.q = in.q; A.k = in.k; A.v = in.v; A.dy = in.dy; A.Wf = in.Wf; A.sel = in.sel;
+    BwdBuffers bb;
+    bb.kept = (uint8_t *)(base + L.kept);
+    bb.Sp = (float *)(base + L.Sp); bb.zp = (float *)(base + L.zp);
+    bb.Rs = (float *)(base + L.Rs); bb.rs = (float *)(base + L.rs);
+    A.kept = bb.kept;
+    bb.phk = (uint16_t *)(base + L.phk);
+    A.phk = bb.phk;
+    A.Sp = bb.Sp; A.zp = bb.zp; A.Rs = bb.Rs; A.rs = bb.rs;
+    A.g = (uint16_t *)(base + L.g);
+    A.phq = (uint16_t *)(base + L.phq);
+    A.phq32 = (float *)(base + L.phq32);
+    bb.phk32 = (float *)(base + L.phk32);
+    A.phk32 = bb.phk32;
+    A.dlq = (float *)(base + L.dlq);
+    A.dlk = (float *)(base + L.dlk);
+    A.rinv = (float *)(base + L.rinv);
+    A.rc = (float *)(base + L.rc);
+    A.rdelta = (float *)(base + L.rdelta);
+    A.rds = (float *)(base + L.rds);
+    A.rjs = (int32_t *)(base + L.rjs);
+    A.dq = in.dq; A.dk = in.dk; A.dv = in.dv; A.dWf = in.dWf; A.cidx = in.cidx;
+    cudaStream_t s = in.stream;
+    if (dm.d == 128) {
+        if (dm.G == 4) return run<128, 4>(A, bb, s);
+        if (dm.G == 2) return run<128, 2>(A, bb, s);
+        return run<128, 1>(A, bb, s);
+    }
+    if (dm.G == 4) return run<64, 4>(A, bb, s);
+    if (dm.G == 2) return run<64, 2>(A, bb, s);
+    return run<64, 1>(A, bb, s);
+}
+
+}  // namespace still

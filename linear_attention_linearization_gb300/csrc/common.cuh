@@ -237,4 +237,22 @@ cudaError_t launch_decode(const Dims &dm, const still_decode_state &st, const ui
                           const uint16_t *k_t, const uint16_t *v_t, const float *Wf, uint16_t *out_t,
                           cudaStream_t s);
 
+
+// ---- backward pass (backward.cu) ----------------------------------------------
+struct BwdInputs {
+    const uint16_t *q, *k, *v, *dy;
+    const float *Wf;
+    const int32_t *sel;
+    float *dq, *dk, *dv, *dWf;
+    int32_t *cidx;   // nullable
+    cudaStream_t stream;
+};
+// byte offsets of the backward pass's workspace pieces
+struct BwdLayout {
+    size_t kept, phk, Sp, zp, Rs, rs, g, phq, phq32, phk32, dlq, dlk, rc, rinv, rdelta, rds, rjs, total;
+};
+BwdLayout bwd_layout(const Dims &dm);
+bool backward_supported(const Dims &dm);
+cudaError_t launch_backward(const Dims &dm, const BwdInputs &in, void *ws);
+
 }  // namespace still

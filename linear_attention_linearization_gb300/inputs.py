@@ -139,6 +139,21 @@ def make_gate(w: Workload, seed: int = 0, device="cpu", B: int | None = None, N:
     return (torch.randn((B, w.Hq, N, w.d), generator=gen, device=dev) * scale).to(torch.bfloat16)
 
 
+def make_dout(w: Workload, seed: int = 0, device="cpu", B: int | None = None, N: int | None = None):
+    """Upstream gradient dL/dy of the layer output for the backward pass, bf16
+    [B,Hq,N,d]: i.i.d. N(0, 1).  Seeded apart from make_inputs and make_gate."""
+    B = w.B if B is None else B
+    N = w.N if N is None else N
+    dev = torch.device(device)
+    if dev.type == "cpu":
+        rng = np.random.Generator(np.random.PCG64(seed + 104729))
+        a = rng.standard_normal((B, w.Hq, N, w.d), dtype=np.float32)
+        return torch.from_numpy(a).to(torch.bfloat16)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(seed + 104729)
+    return torch.randn((B, w.Hq, N, w.d), generator=gen, device=dev).to(torch.bfloat16)
+
+
 def to_f64(t: torch.Tensor) -> np.ndarray:
     """Exact float64 copy of a (bf16/fp32) tensor, on the host."""
     return t.detach().to("cpu", torch.float64).numpy()

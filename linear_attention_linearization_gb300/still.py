@@ -67,6 +67,11 @@ SIGNATURES = {
     "still_prefill_gated": (ct.c_int, [ct.POINTER(Shape), ct.c_void_p, ct.c_void_p, ct.c_void_p, ct.c_void_p,
                                        ct.c_void_p, ct.c_int, ct.c_int, ct.c_int, ct.c_int, ct.c_void_p,
                                        ct.c_void_p, ct.c_void_p, ct.c_size_t, ct.c_void_p]),
+    "still_backward_workspace_size": (ct.c_size_t, [ct.POINTER(Shape), ct.c_int, ct.c_int, ct.c_int, ct.c_int]),
+    "still_backward": (ct.c_int, [ct.POINTER(Shape), ct.c_void_p, ct.c_void_p, ct.c_void_p, ct.c_void_p,
+                                  ct.c_int, ct.c_int, ct.c_int, ct.c_int, ct.c_void_p, ct.c_void_p,
+                                  ct.c_void_p, ct.c_void_p, ct.c_void_p, ct.c_void_p, ct.c_void_p,
+                                  ct.c_void_p, ct.c_size_t, ct.c_void_p]),
     "still_prefill_noalloc_max_bytes": (ct.c_size_t, []),
     "still_prefill_noalloc": (ct.c_int, [ct.POINTER(Shape), ct.c_void_p, ct.c_void_p, ct.c_void_p, ct.c_void_p,
                                          ct.c_int, ct.c_int, ct.c_int, ct.c_int, ct.c_void_p, ct.c_void_p,
@@ -289,6 +294,38 @@ def prefill_gated(q, k, v, gate, Wf, W, C, m, T_max, out=None, sel_idx=None, wor
                                      _ptr(sel_idx, torch.int32, "sel_idx") if sel_idx.numel() else None,
                                      ws_ptr, ws_bytes, _stream(stream)), "still_prefill_gated")
     return out, sel_idx
+
+
+def backward_workspace_size(q, k, Wf, W, C, m, T_max):
+    sh = shape_of(q, k, Wf)
+    return lib().still_backward_workspace_size(ct.byref(sh), W, C, m, T_max)
+
+
+def backward(q, k, v, Wf, W, C, m, T_max, sel_idx, dout, grads=None, cmax_idx=None, workspace=None, stream=None):
+    """Gradients of sum(dout * y) for the layer still_prefill computed with the
+    selection sel_idx held fixed (see still_backward).  grads (optional) is a
+    tuple (dq, dk, dv, dWf) of fp32 tensors to write; cmax_idx (optional) an
+    int32 [B,Hq,N] tensor that receives the row-max key positions.
+    Returns (dq, dk, dv, dWf)."""
+    sh = shape_of(q, k, Wf)
+    if grads is None:
+        grads = (torch.empty(q.shape, dtype=torch.float32, device=q.device),
+                 torch.empty(k.shape, dtype=torch.float32, device=q.device),
+                 torch.empty(v.shape, dtype=torch.float32, device=q.device),
+                 torch.empty(Wf.shape, dtype=torch.float32, device=q.device))
+    dq, dk, dv, dWf = grads
+    ws_ptr, ws_bytes = None, 0
+    if workspace is not None:
+        ws_ptr, ws_bytes = _ptr(workspace, torch.uint8, "workspace"), workspace.numel()
+    _check(lib().still_backward(ct.byref(sh), _ptr(q, torch.bfloat16, "q"), _ptr(k, torch.bfloat16, "k"),
+                                _ptr(v, torch.bfloat16, "v"), _ptr(Wf, torch.float32, "Wf"), W, C, m, T_max,
+                                _ptr(sel_idx, torch.int32, "sel_idx") if sel_idx.numel() else None,
+                                _ptr(dout, torch.bfloat16, "dout"), _ptr(dq, torch.float32, "dq"),
+                                _ptr(dk, torch.float32, "dk"), _ptr(dv, torch.float32, "dv"),
+                                _ptr(dWf, torch.float32, "dWf"),
+                                _ptr(cmax_idx, torch.int32, "cmax_idx") if cmax_idx is not None else None,
+                                ws_ptr, ws_bytes, _stream(stream)), "still_backward")
+    return dq, dk, dv, dWf
 
 
 def prefill_noalloc(q, k, v, Wf, W, C, m, T_max, out=None, sel_idx=None, export_state=None, stream=None):

@@ -113,9 +113,8 @@ def layer_grad(q, k, v, Wf, W, C, sel, dy, cidx=None):
 
 def max_gaps(q, k, W, C, sel):
     """Per row, the gap between the largest and the second largest logit over
-    SA(t), relative to max(1, |largest|) (inf where SA(t) has one key or
-    none): rows whose gap is below the logits' rounding can take c from
-    either position.  Returns [B, Hq, N]."""
+    SA(t) (inf where SA(t) has one key or none): rows whose gap is below the
+    logits' rounding can take c from either position.  Returns [B, Hq, N]."""
     q, k = (np.asarray(a, dtype=np.float64) for a in (q, k))
     B, Hq, N, d = q.shape
     Hkv = k.shape[1]
@@ -129,5 +128,5 @@ def max_gaps(q, k, W, C, sel):
                 s = np.where(sa, q[b, h] @ k[b, g].T / np.sqrt(d), -np.inf)
                 top2 = -np.sort(-s, axis=-1)[:, :2]
                 ok = np.isfinite(top2[:, 1])
-                out[b, h, ok] = (top2[ok, 0] - top2[ok, 1]) / np.maximum(1.0, np.abs(top2[ok, 0]))
+                out[b, h, ok] = top2[ok, 0] - top2[ok, 1]
     return out

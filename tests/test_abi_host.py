@@ -86,6 +86,27 @@ def test_workspace_size_and_argument_errors(lib):
     assert lib.still_prefill_routed(*rargs(2, bad)) == 1
 
 
+
+def test_backward_argument_errors(lib):
+    from linear_attention_linearization_gb300.still import Shape
+    p = ct.c_void_p(16)
+    bad = ct.c_void_p(18)
+    tr = Shape(8, 32, 8, 1024, 128, 128)
+    assert lib.still_backward_workspace_size(ct.byref(tr), 64, 64, 288, 16) > 0
+    assert lib.still_backward_workspace_size(ct.byref(tr), 64, 64, 32, 16) == 0          # m < W
+    args = lambda sh, W, C, q, dWf: (ct.byref(sh), q, p, p, p, W, C, 288, 16, p, p, p, p, p, dWf, None, None, 0,
+                                     None)
+    assert lib.still_backward(*args(tr, 64, 256, p, p)) == 2          # W < C: not covered
+    assert lib.still_backward(*args(Shape(1, 24, 3, 64, 128, 128), 64, 64, p, p)) == 2   # G = 8
+    assert lib.still_backward(*args(Shape(1, 8, 2, 64, 128, 64), 64, 64, p, p)) == 2     # d != d_f
+    assert lib.still_backward(*args(tr, 64, 64, None, p)) == 1        # null q
+    assert lib.still_backward(*args(tr, 64, 64, bad, p)) == 1         # misaligned q
+    assert lib.still_backward(*args(tr, 64, 64, p, None)) == 1        # null dWf
+    assert lib.still_backward(ct.byref(tr), p, p, p, p, 64, 64, 288, 16, None, p, p, p, p, p, None, None, 0,
+                              None) == 1                              # no selection with lambda > 0
+    assert lib.still_backward(ct.byref(tr), p, p, p, p, 64, 64, 288, 16, p, p, p, p, p, p, None, p, 100,
+                              None) == 6                              # workspace too small
+
 def test_oracle_library_shares_nothing_with_cuda_path():
     """The oracle is built from its own C file and links no CUDA library."""
     from oracle import ref

@@ -156,5 +156,5 @@ def test_max_gaps_flags_equal_maxima():
     gaps = grad.max_gaps(q, k, 2, 4, np.full((1, 1, 1, 0), -1))
     assert gaps[0, 0, 0] == np.inf           # one key
     assert gaps[0, 0, 1] == pytest.approx(0.5)
-    assert gaps[0, 0, 2] == pytest.approx(0.5)
+    assert gaps[0, 0, 2] == pytest.approx(1.0)
     assert gaps[0, 0, 3] == 0.0
