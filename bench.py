@@ -61,6 +61,7 @@ def parse(argv=None):
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-workloads", action="store_true",
                    help="skip the 1B-shaped 4K and training-shaped prefill legs")
+    p.add_argument("--no-backward", action="store_true", help="skip the backward-pass leg (training-shaped batch)")
     p.add_argument("--cpu-tokens", type=int, default=16384, help="tokens of the CPU-baseline sample")
     p.add_argument("--seed", type=int, default=0)
     return p.parse_args(argv)
@@ -518,6 +519,8 @@ def run_ours(args):
         line["routing_metrics"] = bench_routing(still, w, (q, k, v, Wf), dev, stream, pk, pk_kind)
 
     # -------- the other prefill workloads --------
+    if not args.no_backward and rank == 0:
+        line["backward"] = bench_backward(still, dev, stream, pk, pk_kind, args.seed + 13, cpu=not args.no_cpu)
     if not args.no_workloads and rank == 0:
         line["workloads"] = {nm: bench_workload(still, nm, dev, stream, pk, pk_kind, args.seed + 11,
                                                 cpu=not args.no_cpu)
@@ -664,6 +667,115 @@ def bench_workload(still, name, dev, stream, pk, pk_kind, seed, steps=50, cpu=Tr
         else:
             res["cpu_baseline"], keep, thr = cpu_baseline(q.cpu(), k.cpu(), v.cpu(), Wf.cpu(), w, toks)
         res["parity"] = parity_vs_oracle(out, sel, w, toks, keep, thr)
+    return res
+
+
+BACKWARD_WORKLOAD = "train_b8_n1k_chunk_parallel"
+
+
+def backward_algorithmic(w, sel_idx):
+    """Algorithmic work of one backward pass (routing fixed): per softmax pair
+    (t, j) the logit recomputation and the four gradient contractions (dP, dq,
+    dk, dv: 2d flops each), per query row phi(q) S for y, S g for dphi(q) and
+    its share of the reverse state sum phi(q) g^T, per linear key phi(k) v^T
+    for the forward state, R v and R^T phi(k), per q and k row the NP-Map
+    (x Wf, dl Wf^T, x dl^T); bytes: q, k, v, dy read once (bf16), dq, dk, dv
+    written once (fp32), Wf read and dWf written."""
+    a = algorithmic(w, sel_idx)
+    N, d, df, Hq, Hkv, B = w.N, w.d, w.df, w.Hq, w.Hkv, w.B
+    sa_keys = a["mean_sa_keys"] * Hq * B * N
+    kept = float((sel_idx >= 0).sum())
+    rows_q, rows_k = Hq * B * N, Hkv * B * N
+    lin_keys = max(rows_k - kept - Hkv * B * w.W, 0.0)
+    F_soft = 10.0 * d * sa_keys
+    F_lin = 3 * 2.0 * df * d * rows_q + 3 * 2.0 * df * d * lin_keys
+    F_np = 6.0 * d * df * (rows_q + rows_k)
+    by = 2.0 * d * (2 * rows_q + 2 * rows_k) + 4.0 * d * (rows_q + 2 * rows_k) + 8.0 * d * df
+    return {"flops": F_soft + F_lin + F_np, "F_softmax": F_soft, "F_linear": F_lin, "F_npmap": F_np, "bytes": by}
+
+
+def bench_backward(still, dev, stream, pk, pk_kind, seed, steps=20, cpu=True):
+    """The backward pass (still_backward, routing held fixed) of the
+    training-shaped batch: `steps` timed calls after 3 warm-up ones, L2 flushed
+    before each (CUDA events around every call), the step against its roofline,
+    its kernels' times from the library's event timers, and -- unless cpu is
+    False -- the gradient oracle on one sequence of the batch on the host
+    cores, with the parity of the GPU's dq, dk, dv for that sequence."""
+    import numpy as np
+    import torch
+    from linear_attention_linearization_gb300 import inputs
+    from linear_attention_linearization_gb300.inputs import to_f64
+    w = inputs.WORKLOADS[BACKWARD_WORKLOAD]
+    q, k, v, Wf = inputs.make_inputs(w, seed=seed, device=dev)
+    dy = inputs.make_dout(w, seed=seed, device=dev)
+    _, sel = still.prefill(q, k, v, Wf, w.W, w.C, w.m, w.T_max, stream=stream)
+    grads = (torch.empty(q.shape, dtype=torch.float32, device=dev), torch.empty(k.shape, dtype=torch.float32, device=dev),
+             torch.empty(v.shape, dtype=torch.float32, device=dev), torch.empty(Wf.shape, dtype=torch.float32, device=dev))
+    ws = torch.empty(still.backward_workspace_size(q, k, Wf, w.W, w.C, w.m, w.T_max), dtype=torch.uint8, device=dev)
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def step():
+        still.backward(q, k, v, Wf, w.W, w.C, w.m, w.T_max, sel, dy, grads=grads, workspace=ws, stream=stream)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize(dev)
+    ev = []
+    for i in range(steps):
+        flush.fill_(float(i))
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        step()
+        b.record(stream)
+        ev.append((a, b))
+    torch.cuda.synchronize(dev)
+    ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    still.timing_read()
+    still.timing_enable(True)
+    for i in range(5):
+        flush.fill_(float(i))
+        step()
+    torch.cuda.synchronize(dev)
+    still.timing_enable(False)
+    kt = still.timing_read()
+    sel_h = sel.cpu().numpy()
+    alg = backward_algorithmic(w, sel_h)
+    t_flop = alg["flops"] / (pk["bf16_tflops"] * 1e12)
+    t_hbm = alg["bytes"] / (pk["hbm_gbs"] * 1e9)
+    res = {"config": {"workload": w.name, **w.asdict()}, "metric": "backward tokens/s", "unit": "tokens/s",
+           "value": w.B * w.N / (ms / 1e3), "ms_per_step": ms, "steps": steps, "dtype": "bf16 operands, fp32 gradients",
+           "l2": "flushed (258 MB write) before every timed step",
+           "roofline": {"bound": "tensor" if t_flop >= t_hbm else "hbm", "algorithmic_flops": alg["flops"],
+                        "algorithmic_bytes": alg["bytes"], "roofline_ms": max(t_flop, t_hbm) * 1e3,
+                        "achieved_tflops": alg["flops"] / (ms / 1e3) / 1e12, "peak_tflops": pk["bf16_tflops"],
+                        "frac": max(t_flop, t_hbm) * 1e3 / ms, "peak_source": pk_kind,
+                        "split": {k2: alg[k2] for k2 in ("F_softmax", "F_linear", "F_npmap")}},
+           "kernels": {k2: {"launches": n, "ms_per_launch": m / n} for k2, (n, m) in kt.items()},
+           "gpu_launches_per_step": 11}
+    if cpu:
+        from oracle import grad
+        torch_threads = torch.get_num_threads()
+        hq, hk, hv, hW, hdy = (to_f64(t[:1]) if t.dim() == 4 else to_f64(t) for t in (q, k, v, Wf, dy))
+        cidx = torch.empty((w.B, w.Hq, w.N), dtype=torch.int32, device=dev)
+        still.backward(q, k, v, Wf, w.W, w.C, w.m, w.T_max, sel, dy, grads=grads, cmax_idx=cidx, workspace=ws,
+                       stream=stream)
+        torch.cuda.synchronize(dev)
+        t0 = time.perf_counter()
+        _, dq_r, dk_r, dv_r, _, c_r = grad.layer_grad(hq, hk, hv, hW, w.W, w.C, sel_h[:1], hdy)
+        sec = time.perf_counter() - t0
+        c_g = cidx[:1].cpu().numpy().astype(np.int64)
+        moved = int((c_g != c_r).sum())
+        if moved:   # near-equal row maxima: the oracle takes the GPU's choice of the key that holds c
+            _, dq_r, dk_r, dv_r, _, _ = grad.layer_grad(hq, hk, hv, hW, w.W, w.C, sel_h[:1], hdy, cidx=c_g)
+        res["cpu_baseline"] = {"value": w.N / sec, "unit": "tokens/s", "cores": torch_threads, "kind": "oracle",
+                               "sample": f"the gradient oracle (fp64) on sequence 0 of the {w.B} ({w.N} tokens, "
+                                         f"{w.Hq} heads), {sec:.2f} s"}
+        par = {}
+        for nm, g_gpu, g_ref in (("dq", grads[0][:1], dq_r), ("dk", grads[1][:1], dk_r), ("dv", grads[2][:1], dv_r)):
+            par[f"{nm}_err_rel"] = float(np.abs(g_gpu.cpu().double().numpy() - g_ref).max() / np.abs(g_ref).max())
+        par["rows_row_max_differs"] = moved
+        par["tolerance"] = "max|g_gpu - g_ref| <= 1e-2 max|g_ref| per tensor"
+        res["parity"] = par
     return res
 
 
