@@ -209,36 +209,53 @@ __global__ void __launch_bounds__(256) blocksum_kernel(BwdArgs P, float *__restr
 // ---------------------------------------------------------------------------
 // query pass
 // ---------------------------------------------------------------------------
+constexpr int BQ8_THREADS = 256;   // the query pass: eight warps of 16 rows
+constexpr int KEPT_MAX = 1024;     // kept positions of a CTA held in shared memory (more: read from global)
+
+__device__ __forceinline__ void cp_async16(void *dst, const void *src, int src_bytes)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_addr(dst)), "l"(src), "r"(src_bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
 template <int D>
 struct QLayout {
     static constexpr int LD = D + 8, T32 = BT * LD * 2;
-    static constexpr int K = 0, V = K + T32, PK = V + T32, VL = PK + T32;
+    static constexpr int K = 0, V = K + 2 * T32, PK = V + 2 * T32, VL = PK + T32;   // K, V: two buffers each
     static constexpr int WF = VL + T32;            // Wf [d][df] bf16
     static constexpr int SP = WF + D * LD * 2;     // S before the lag keys, [df][d] bf16
     static constexpr int ZP = SP + D * LD * 2;     // z, fp32 [df]
-    static constexpr int POS = ZP + D * 4;         // positions of the staged key block / lag block
-    static constexpr int TOTAL = POS + 2 * BT * 4;
+    static constexpr int POS = ZP + D * 4;         // positions of the two staged key blocks and of the lag block
+    static constexpr int KEPT = POS + 3 * BT * 4;  // the CTA's kept positions
+    static constexpr int TOTAL = KEPT + KEPT_MAX * 4;
 };
 
 // The thread's two accumulator rows are gid and gid + 8; element (nt, 2r + e)
-// of an accumulator is (row gid + 8r, column 8nt + 2tig + e).
+// of an accumulator is (row gid + 8r, column 8nt + 2tig + e).  Eight warps: G
+// heads x 8/G token tiles of 16.
 template <int D, int G>
-__global__ void __launch_bounds__(BQ_THREADS, 2) query_kernel(BwdArgs P)
+__global__ void __launch_bounds__(BQ8_THREADS, 1) query_kernel(BwdArgs P)
 {
     grid_dep_sync();
     constexpr int LD = D + 8, KC = D / 16, NT = D / 8;
-    constexpr int TOK = 16 * (4 / G);   // tokens per CTA
+    constexpr int TOK = 16 * (8 / G);   // tokens per CTA
+    constexpr int T32E = BT * LD;       // elements of one 32-row tile
     using L = QLayout<D>;
     extern __shared__ __align__(16) uint8_t smem[];
-    uint16_t *sK = (uint16_t *)(smem + L::K), *sV = (uint16_t *)(smem + L::V);
+    uint16_t *sKb = (uint16_t *)(smem + L::K), *sVb = (uint16_t *)(smem + L::V);
     uint16_t *sPK = (uint16_t *)(smem + L::PK), *sVL = (uint16_t *)(smem + L::VL);
     uint16_t *sWF = (uint16_t *)(smem + L::WF), *sSP = (uint16_t *)(smem + L::SP);
     float *sZ = (float *)(smem + L::ZP);
-    int *sPos = (int *)(smem + L::POS), *sLag = sPos + BT;
+    int *sPosb = (int *)(smem + L::POS), *sLag = sPosb + 2 * BT;
+    int *sKept = (int *)(smem + L::KEPT);
 
     const Dims &dm = P.dm;
     const int N = dm.N, W = dm.W, C = dm.C;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gid = lane >> 2, tig = lane & 3;
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31, gid = lane >> 2, tig = lane & 3;
     const int unit = blockIdx.y, b = unit / dm.Hkv, gq = unit % dm.Hkv;
     const int t0 = blockIdx.x * TOK;
     const int h = gq * G + warp % G;
@@ -250,7 +267,7 @@ __global__ void __launch_bounds__(BQ_THREADS, 2) query_kernel(BwdArgs P)
 
     // ---- Wf as a bf16 pair hi (sWF, resident) + lo (in the S region until S is staged):
     // U = q Wf to about 16 significant bits of Wf
-    for (int i = threadIdx.x; i < D * D / 4; i += blockDim.x) {
+    for (int i = tid; i < D * D / 4; i += BQ8_THREADS) {
         const int r = i / (D / 4), c = (i % (D / 4)) * 4;
         const float4 x = __ldg(reinterpret_cast<const float4 *>(P.Wf) + i);
         const uint32_t h0 = pack(x.x, x.y), h1 = pack(x.z, x.w);
@@ -262,7 +279,19 @@ __global__ void __launch_bounds__(BQ_THREADS, 2) query_kernel(BwdArgs P)
     const int i0 = t0 - W > 0 ? (t0 - W) / BT : 0;
     const int lag0 = BT * i0, lag1 = min(t0 + TOK - W, N);   // lag keys [lag0, lag1)
     const int nlag = lag1 > lag0 ? (lag1 - lag0 + BT - 1) / BT : 0;
-    for (int f = threadIdx.x; f < D; f += blockDim.x) sZ[f] = P.zp[((size_t)unit * (P.nblk + 1) + i0) * D + f];
+    for (int f = tid; f < D; f += BQ8_THREADS) sZ[f] = P.zp[((size_t)unit * (P.nblk + 1) + i0) * D + f];
+    // the softmax keys: kept keys of chunks before the last row's, then the band
+    const int tlast = min(t0 + TOK, N) - 1;
+    const int KP = dm.T_max * dm.lam;
+    const int nk = dm.lam * min(tlast / C, dm.T_max);
+    const int nkb = (nk + BT - 1) / BT;
+    const int bs = max(t0 - W + 1, 0), be = tlast + 1;
+    const int nblk = nkb + (be - bs + BT - 1) / BT;
+    const int32_t *selu = P.sel + (size_t)unit * KP;
+    for (int e = tid; e < min(nk, KEPT_MAX); e += BQ8_THREADS) {
+        const int p = selu[e];
+        sKept[e] = p < N ? p : -1;
+    }
 
     uint32_t qa[KC][4];
     {
@@ -277,6 +306,56 @@ __global__ void __launch_bounds__(BQ_THREADS, 2) query_kernel(BwdArgs P)
         }
     }
     __syncthreads();
+
+    auto key_pos = [&](int blk, int i) -> int {
+        if (blk < nkb) {
+            const int e = blk * BT + i;
+            if (e >= nk) return -1;
+            if (e < KEPT_MAX) return sKept[e];
+            const int p = selu[e];
+            return p < N ? p : -1;
+        }
+        const int p = bs + (blk - nkb) * BT + i;
+        return p < be ? p : -1;
+    };
+    // key block blk into buffer buf (K, and V when with_v) by cp.async, one commit group
+    auto issue = [&](int blk, int buf, bool with_v) {
+        int *pos = sPosb + buf * BT;
+        for (int i = tid; i < BT; i += BQ8_THREADS) pos[i] = key_pos(blk, i);
+        constexpr int V8 = D / 8, NE = BT * V8;
+        for (int i = tid; i < NE * (with_v ? 2 : 1); i += BQ8_THREADS) {
+            const int which = i / NE, j = i % NE, r = j / V8, c = j % V8;
+            const int p = key_pos(blk, r);
+            const uint16_t *src = (which ? P.v : P.k) + (krow0 + (p >= 0 ? p : 0)) * D + c * 8;
+            cp_async16((which ? sVb : sKb) + buf * T32E + r * LD + c * 8, src, p >= 0 ? 16 : 0);
+        }
+        cp_commit();
+    };
+    // for each key block: wait for its copies, run body(buf), prefetch the next one
+    auto key_loop = [&](bool with_v, auto body) {
+        issue(0, 0, with_v);
+        for (int blk = 0; blk < nblk; ++blk) {
+            const int buf = blk & 1;
+            if (blk + 1 < nblk) {
+                issue(blk + 1, buf ^ 1, with_v);
+                cp_wait<1>();
+            } else {
+                cp_wait<0>();
+            }
+            __syncthreads();
+            body(blk, buf);
+            __syncthreads();
+        }
+    };
+    auto in_sa = [&](int t, int p, bool kept_blk) -> bool {
+        if (p < 0 || t >= N) return false;
+        if (kept_blk) return p <= t - W && p / C < t / C;
+        return p <= t && p > t - W;
+    };
+    auto logits = [&](float (&s)[4][4], int buf) {
+        zero(s);
+        mma_tile<KC, 4, false>(s, qa, sKb + buf * T32E, LD, 0, 0);
+    };
 
     // ---- NP-Map of the query rows: u = softmax(q Wf), phi = ||q|| u / ||u||
     float nq[2];
@@ -334,111 +413,79 @@ __global__ void __launch_bounds__(BQ_THREADS, 2) query_kernel(BwdArgs P)
     stage_f32(sSP, LD, P.Sp + ((size_t)unit * (P.nblk + 1) + i0) * D * D, D, D);
     __syncthreads();
 
-    // ---- the softmax keys: kept keys of earlier chunks, then the band
-    const int tlast = min(t0 + TOK, N) - 1;
-    const int KP = dm.T_max * dm.lam;
-    const int ck = min(tlast / C, dm.T_max);
-    const int nk = dm.lam * ck;                       // kept entries of chunks before the last row's
-    const int nkb = (nk + BT - 1) / BT;
-    const int bs = max(t0 - W + 1, 0), be = tlast + 1;
-    const int nbb = (be - bs + BT - 1) / BT;
-    const int nblk = nkb + nbb;
-    const int32_t *selu = P.sel + (size_t)unit * KP;
-    auto key_pos = [&](int blk, int i) -> int {
-        if (blk < nkb) {
-            const int e = blk * BT + i;
-            const int p = e < nk ? selu[e] : -1;
-            return p < N ? p : -1;
-        }
-        const int p = bs + (blk - nkb) * BT + i;
-        return p < be ? p : -1;
-    };
-    auto stage_keys = [&](int blk, bool with_v) {
-        __syncthreads();
-        for (int i = threadIdx.x; i < BT; i += blockDim.x) sPos[i] = key_pos(blk, i);
-        __syncthreads();
-        stage_rows<D>(sK, LD, BT, [&](int r) -> const uint16_t * {
-            const int p = sPos[r];
-            return p >= 0 ? P.k + (krow0 + p) * D : nullptr;
-        });
-        if (with_v)
-            stage_rows<D>(sV, LD, BT, [&](int r) -> const uint16_t * {
-                const int p = sPos[r];
-                return p >= 0 ? P.v + (krow0 + p) * D : nullptr;
-            });
-        __syncthreads();
-    };
-    auto in_sa = [&](int t, int p, bool kept_blk) -> bool {
-        if (p < 0 || t >= N) return false;
-        if (kept_blk) return p <= t - W && p / C < t / C;
-        return p <= t && p > t - W;
-    };
-    auto logits = [&](float (&s)[4][4]) {
-        zero(s);
-        mma_tile<KC, 4, false>(s, qa, sK, LD, 0, 0);
-    };
-
-    // pass 1: c = the row maximum, at the lowest position among equal maxima
+    // pass 1: O = P V and D_SA = sum P with a running row maximum (O and the sums
+    // rescaled when it grows); at the end it is c, the exact row maximum, and the
+    // lowest position among equal maxima holds it
+    float o[NT][4];
+    zero(o);
+    float dsa[2] = {0.f, 0.f};
+    float mrun[2] = {-INFINITY, -INFINITY};
     float cm[2] = {-INFINITY, -INFINITY};
     int cj[2] = {INT_MAX, INT_MAX};
-    for (int blk = 0; blk < nblk; ++blk) {
-        stage_keys(blk, false);
+    key_loop(true, [&](int blk, int buf) {
+        const int *pos = sPosb + buf * BT;
         float s[4][4];
-        logits(s);
+        logits(s, buf);
         const bool kb = blk < nkb;
+        float bm[2] = {-INFINITY, -INFINITY};
 #pragma unroll
         for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
-                const int p = sPos[nt * 8 + 2 * tig + e];
+                const int p = pos[nt * 8 + 2 * tig + e];
 #pragma unroll
                 for (int r = 0; r < 2; ++r) {
-                    const float x = s[nt][2 * r + e] * scale;
-                    if (in_sa(tr[r], p, kb) && (x > cm[r] || (x == cm[r] && p < cj[r]))) {
+                    const bool in = in_sa(tr[r], p, kb);
+                    const float x = in ? s[nt][2 * r + e] * scale : -INFINITY;
+                    s[nt][2 * r + e] = x;
+                    bm[r] = fmaxf(bm[r], x);
+                    if (in && (x > cm[r] || (x == cm[r] && p < cj[r]))) {
                         cm[r] = x;
                         cj[r] = p;
                     }
                 }
             }
-    }
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            bm[r] = fmaxf(bm[r], __shfl_xor_sync(0xffffffffu, bm[r], 1));
+            bm[r] = fmaxf(bm[r], __shfl_xor_sync(0xffffffffu, bm[r], 2));
+            if (bm[r] > mrun[r]) {
+                const float f = mrun[r] == -INFINITY ? 0.f : expf(mrun[r] - bm[r]);
+                dsa[r] *= f;
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    o[nt][2 * r] *= f;
+                    o[nt][2 * r + 1] *= f;
+                }
+                mrun[r] = bm[r];
+            }
+        }
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+            for (int e = 0; e < 2; ++e)
+#pragma unroll
+                for (int r = 0; r < 2; ++r) {
+                    const float x = s[nt][2 * r + e];
+                    const float pe = x == -INFINITY ? 0.f : expf(x - mrun[r]);
+                    s[nt][2 * r + e] = pe;
+                    dsa[r] += pe;
+                }
+        uint32_t pf[2][4];
+        acc_to_a<4>(s, pf);
+        mma_tile<2, NT, true>(o, pf, sVb + buf * T32E, LD, 0, 0);
+    });
 #pragma unroll
     for (int r = 0; r < 2; ++r)
 #pragma unroll
-        for (int o = 1; o <= 2; o <<= 1) {
-            const float x = __shfl_xor_sync(0xffffffffu, cm[r], o);
-            const int p = __shfl_xor_sync(0xffffffffu, cj[r], o);
+        for (int sh = 1; sh <= 2; sh <<= 1) {
+            const float x = __shfl_xor_sync(0xffffffffu, cm[r], sh);
+            const int p = __shfl_xor_sync(0xffffffffu, cj[r], sh);
             if (x > cm[r] || (x == cm[r] && p < cj[r])) {
                 cm[r] = x;
                 cj[r] = p;
             }
         }
-
-    // pass 2: O = P V, D_SA = sum P
-    float o[NT][4];
-    zero(o);
-    float dsa[2] = {0.f, 0.f};
-    for (int blk = 0; blk < nblk; ++blk) {
-        stage_keys(blk, true);
-        float s[4][4];
-        logits(s);
-        const bool kb = blk < nkb;
-#pragma unroll
-        for (int nt = 0; nt < 4; ++nt)
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                const int p = sPos[nt * 8 + 2 * tig + e];
-#pragma unroll
-                for (int r = 0; r < 2; ++r) {
-                    const float x = s[nt][2 * r + e] * scale;
-                    const float pe = in_sa(tr[r], p, kb) ? expf(x - cm[r]) : 0.f;
-                    s[nt][2 * r + e] = pe;
-                    dsa[r] += pe;
-                }
-            }
-        uint32_t pf[2][4];
-        acc_to_a<4>(s, pf);
-        mma_tile<2, NT, true>(o, pf, sV, LD, 0, 0);
-    }
 
     // ---- the linear branch: phi(q) S + the lag keys [lag0, t - W]
     mma_tile<KC, NT, true>(o, pa, sSP, LD, 0, 0);
@@ -546,22 +593,22 @@ __global__ void __launch_bounds__(BQ_THREADS, 2) query_kernel(BwdArgs P)
         }
     }
 
-    // pass 3: dP = g V^T = (dy V^T) / den, dS = P (dP - delta), dq = dS K
+    // pass 2: dP = g V^T = (dy V^T) / den, dS = P (dP - delta), dq = dS K
     float dq[NT][4];
     zero(dq);
     float dss[2] = {0.f, 0.f};
-    for (int blk = 0; blk < nblk; ++blk) {
-        stage_keys(blk, true);
+    key_loop(true, [&](int blk, int buf) {
+        const int *pos = sPosb + buf * BT;
         float s[4][4], dp[4][4];
-        logits(s);
+        logits(s, buf);
         zero(dp);
-        mma_tile<KC, 4, false>(dp, ya, sV, LD, 0, 0);
+        mma_tile<KC, 4, false>(dp, ya, sVb + buf * T32E, LD, 0, 0);
         const bool kb = blk < nkb;
 #pragma unroll
         for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
-                const int p = sPos[nt * 8 + 2 * tig + e];
+                const int p = pos[nt * 8 + 2 * tig + e];
 #pragma unroll
                 for (int r = 0; r < 2; ++r) {
                     const float x = s[nt][2 * r + e] * scale;
@@ -573,8 +620,8 @@ __global__ void __launch_bounds__(BQ_THREADS, 2) query_kernel(BwdArgs P)
             }
         uint32_t sf[2][4];
         acc_to_a<4>(s, sf);
-        mma_tile<2, NT, true>(dq, sf, sK, LD, 0, 0);
-    }
+        mma_tile<2, NT, true>(dq, sf, sKb + buf * T32E, LD, 0, 0);
+    });
     // the stabiliser's gradient at the row-max key, then the 1/sqrt(d) of the logits
 #pragma unroll
     for (int r = 0; r < 2; ++r) {
@@ -1156,9 +1203,9 @@ cudaError_t run(const BwdArgs &A, const BwdBuffers &bb, cudaStream_t s)
     }
     {
         KTimer tm("bwd_query", s);
-        constexpr int TOK = 16 * (4 / G);
+        constexpr int TOK = 16 * (8 / G);
         chk(set_smem(query_kernel<D, G>, QLayout<D>::TOTAL));
-        chk(launch_kernel(query_kernel<D, G>, dim3((dm.N + TOK - 1) / TOK, units), dim3(BQ_THREADS), QLayout<D>::TOTAL, s, A));
+        chk(launch_kernel(query_kernel<D, G>, dim3((dm.N + TOK - 1) / TOK, units), dim3(BQ8_THREADS), QLayout<D>::TOTAL, s, A));
     }
     {
         KTimer tm("bwd_rstate", s);
