@@ -52,7 +52,6 @@ namespace {
 using namespace wmma16;
 
 constexpr int BT = 32;             // tokens per state block
-constexpr int BQ_THREADS = 128;    // four warps of 16 rows (query pass) or 16 keys (key passes)
 
 struct BwdArgs {
     Dims dm;
@@ -217,6 +216,11 @@ __device__ __forceinline__ void cp_async16(void *dst, const void *src, int src_b
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_addr(dst)), "l"(src), "r"(src_bytes)
                  : "memory");
 }
+__device__ __forceinline__ void cp_async4(void *dst, const void *src, int src_bytes)
+{
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(smem_addr(dst)), "l"(src), "r"(src_bytes)
+                 : "memory");
+}
 __device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
 __device__ __forceinline__ void cp_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
@@ -243,6 +247,7 @@ __global__ void __launch_bounds__(BQ8_THREADS, 1) query_kernel(BwdArgs P)
     constexpr int LD = D + 8, KC = D / 16, NT = D / 8;
     constexpr int TOK = 16 * (8 / G);   // tokens per CTA
     constexpr int T32E = BT * LD;       // elements of one 32-row tile
+    constexpr float LOG2E = 1.4426950408889634f;
     using L = QLayout<D>;
     extern __shared__ __align__(16) uint8_t smem[];
     uint16_t *sKb = (uint16_t *)(smem + L::K), *sVb = (uint16_t *)(smem + L::V);
@@ -347,9 +352,10 @@ __global__ void __launch_bounds__(BQ8_THREADS, 1) query_kernel(BwdArgs P)
             __syncthreads();
         }
     };
+    // (with W >= C a kept key at or before t - W is of an earlier chunk than t)
     auto in_sa = [&](int t, int p, bool kept_blk) -> bool {
         if (p < 0 || t >= N) return false;
-        if (kept_blk) return p <= t - W && p / C < t / C;
+        if (kept_blk) return p <= t - W;
         return p <= t && p > t - W;
     };
     auto logits = [&](float (&s)[4][4], int buf) {
@@ -467,7 +473,7 @@ __global__ void __launch_bounds__(BQ8_THREADS, 1) query_kernel(BwdArgs P)
 #pragma unroll
                 for (int r = 0; r < 2; ++r) {
                     const float x = s[nt][2 * r + e];
-                    const float pe = x == -INFINITY ? 0.f : expf(x - mrun[r]);
+                    const float pe = x == -INFINITY ? 0.f : exp2_mufu((x - mrun[r]) * LOG2E);
                     s[nt][2 * r + e] = pe;
                     dsa[r] += pe;
                 }
@@ -594,6 +600,8 @@ __global__ void __launch_bounds__(BQ8_THREADS, 1) query_kernel(BwdArgs P)
     }
 
     // pass 2: dP = g V^T = (dy V^T) / den, dS = P (dP - delta), dq = dS K
+    const float scale_l2 = scale * LOG2E;
+    const float cl2[2] = {cm[0] * LOG2E, cm[1] * LOG2E};
     float dq[NT][4];
     zero(dq);
     float dss[2] = {0.f, 0.f};
@@ -611,8 +619,7 @@ __global__ void __launch_bounds__(BQ8_THREADS, 1) query_kernel(BwdArgs P)
                 const int p = pos[nt * 8 + 2 * tig + e];
 #pragma unroll
                 for (int r = 0; r < 2; ++r) {
-                    const float x = s[nt][2 * r + e] * scale;
-                    const float pe = in_sa(tr[r], p, kb) ? expf(x - cm[r]) : 0.f;
+                    const float pe = in_sa(tr[r], p, kb) ? exp2_mufu(fmaf(s[nt][2 * r + e], scale_l2, -cl2[r])) : 0.f;
                     const float ds = pe * (dp[nt][2 * r + e] * inv[r] - delta[r]);
                     s[nt][2 * r + e] = ds;
                     dss[r] += ds;
@@ -743,55 +750,94 @@ __global__ void __launch_bounds__(BQ8_THREADS, 1) query_kernel(BwdArgs P)
 // ---------------------------------------------------------------------------
 // key passes: a warp owns 16 keys (rows of the transposed products)
 // ---------------------------------------------------------------------------
+constexpr int BK_KEYS = 128;   // keys (or kept-table entries) per CTA: eight warps of 16
+
 template <int D>
 struct KLayout {
     static constexpr int LD = D + 8, T32 = BT * LD * 2;
-    static constexpr int K = 0, V = K + 2 * T32, PK = V + 2 * T32;   // 64 keys each
-    static constexpr int Q = PK + 2 * T32, G = Q + T32, PQ = G + T32;  // one 32-row query block
-    static constexpr int R = PQ + T32;        // R [df][d] bf16 of the linear pass, then Wf [d][df]
-    static constexpr int RV = R + D * LD * 2; // r, fp32 [df]
-    static constexpr int ROW = RV + D * 4;    // per query row: token, c, delta, ds sum, 1/den, c position
-    static constexpr int KPOS = ROW + 6 * BT * 4;   // positions of the 64 keys
-    static constexpr int TOTAL = KPOS + 64 * 4;
+    static constexpr int NR = 6;                            // per query row: token, c, delta, ds sum, 1/den, c position
+    static constexpr int K = 0, V = K + 4 * T32, PK = V + 4 * T32;   // the CTA's 128 keys
+    static constexpr int QB = PK + 4 * T32;                 // two buffers of one query block: q, dy, phi(q)
+    static constexpr int R = QB + 6 * T32;                  // R [df][d] bf16 of the linear pass, then Wf [d][df]
+    static constexpr int RV = R + D * LD * 2;               // r, fp32 [df]
+    static constexpr int ROW = RV + D * 4;                  // two buffers of the rows' scalars
+    static constexpr int KPOS = ROW + 2 * NR * BT * 4;      // positions of the keys
+    static constexpr int TOTAL = KPOS + BK_KEYS * 4;
 };
 
-// The query rows of one block (32 rows of one head), their scalars, and the
-// rows of q, g (and phi(q)) in shared memory.
+// The query rows of one block (32 tokens of one head) and their scalars in
+// shared memory.
 struct QRows {
     int *tok;
     float *c, *delta, *dss, *inv;
     int *js;
 };
 
-template <int D>
-__device__ __forceinline__ void stage_qblock(const BwdArgs &P, int b, int h, int tq0, int tq1, bool with_phq,
-                                             uint16_t *sQ, uint16_t *sG, uint16_t *sPQ, QRows R)
+__device__ __forceinline__ QRows qrows_at(int *base)
 {
-    constexpr int LD = D + 8;
+    return QRows{base, (float *)(base + BT), (float *)(base + 2 * BT), (float *)(base + 3 * BT),
+                 (float *)(base + 4 * BT), base + 5 * BT};
+}
+
+// Query blocks (head, tokens [tq0, tq1)) streamed through two shared buffers by
+// cp.async: q and dy rows (and phi(q) rows), the rows' scalars; tokens past
+// tq1 are zero rows with token -1.  body(i, sQ, sG, sPQ, R) runs on block i once
+// its copies have landed, while block i + 1 is being copied.
+template <int D, typename BlockOf, typename Body>
+__device__ __forceinline__ void query_blocks(const BwdArgs &P, int b, int nqb, bool with_phq, uint8_t *smem,
+                                             BlockOf block_of, Body body)
+{
+    using L = KLayout<D>;
+    constexpr int LD = D + 8, T32E = BT * LD, V8 = D / 8, NE = BT * V8;
     const Dims &dm = P.dm;
-    const size_t row0 = (size_t)(b * dm.Hq + h) * dm.N;
-    __syncthreads();
-    for (int i = threadIdx.x; i < BT; i += blockDim.x) {
-        const int t = tq0 + i;
-        const bool ok = t < tq1 && t < dm.N;
-        R.tok[i] = ok ? t : -1;
-        R.c[i] = ok ? P.rc[row0 + t] : 0.f;
-        R.delta[i] = ok ? P.rdelta[row0 + t] : 0.f;
-        R.dss[i] = ok ? P.rds[row0 + t] : 0.f;
-        R.inv[i] = ok ? P.rinv[row0 + t] : 0.f;
-        R.js[i] = ok ? P.rjs[row0 + t] : -1;
+    const int tid = threadIdx.x, nth = blockDim.x;
+    uint16_t *qb = (uint16_t *)(smem + L::QB);
+    int *rows = (int *)(smem + L::ROW);
+    auto issue = [&](int i, int buf) {
+        int h, tq0, tq1;
+        block_of(i, h, tq0, tq1);
+        const size_t row0 = (size_t)(b * dm.Hq + h) * dm.N;
+        uint16_t *dst = qb + buf * 3 * T32E;
+        QRows R = qrows_at(rows + buf * L::NR * BT);
+        for (int r = tid; r < BT; r += nth) R.tok[r] = tq0 + r < tq1 ? tq0 + r : -1;
+        const int nm = with_phq ? 3 : 2;
+        for (int e = tid; e < NE * nm; e += nth) {
+            const int which = e / NE, j = e % NE, r = j / V8, c = j % V8;
+            const bool ok = tq0 + r < tq1;
+            const uint16_t *src = (which == 0 ? P.q : which == 1 ? P.dy : P.phq) + (row0 + (ok ? tq0 + r : 0)) * D + c * 8;
+            cp_async16(dst + which * T32E + r * LD + c * 8, src, ok ? 16 : 0);
+        }
+        // scalars: 5 arrays of 32 values, one 4-byte copy each (a token's row need not
+        // start on a 16-byte boundary), the rows past tq1 zero-filled
+        for (int e = tid; e < 5 * BT; e += nth) {
+            const int a = e / BT, r = e % BT;
+            const bool ok = tq0 + r < tq1;
+            const float *arr = a == 0 ? P.rc : a == 1 ? P.rdelta : a == 2 ? P.rds : a == 3 ? P.rinv : (const float *)P.rjs;
+            float *d = a == 0 ? R.c : a == 1 ? R.delta : a == 2 ? R.dss : a == 3 ? R.inv : (float *)R.js;
+            cp_async4(d + r, arr + (ok ? row0 + tq0 + r : 0), ok ? 4 : 0);
+        }
+        cp_commit();
+    };
+    if (nqb <= 0) return;
+    issue(0, 0);
+    for (int i = 0; i < nqb; ++i) {
+        const int buf = i & 1;
+        if (i + 1 < nqb) {
+            issue(i + 1, buf ^ 1);
+            cp_wait<1>();
+        } else {
+            cp_wait<0>();
+        }
+        __syncthreads();
+        uint16_t *q = qb + buf * 3 * T32E;
+        body(i, q, q + T32E, q + 2 * T32E, qrows_at(rows + buf * L::NR * BT));
+        __syncthreads();
     }
-    __syncthreads();
-    stage_rows<D>(sQ, LD, BT, [&](int r) -> const uint16_t * { return R.tok[r] >= 0 ? P.q + (row0 + R.tok[r]) * D : nullptr; });
-    stage_rows<D>(sG, LD, BT, [&](int r) -> const uint16_t * { return R.tok[r] >= 0 ? P.dy + (row0 + R.tok[r]) * D : nullptr; });
-    if (with_phq)
-        stage_rows<D>(sPQ, LD, BT, [&](int r) -> const uint16_t * { return R.tok[r] >= 0 ? P.phq + (row0 + R.tok[r]) * D : nullptr; });
-    __syncthreads();
 }
 
 // dK += dS^T Q, dV += P^T G over one staged query block for the warp's 16 keys
-// (sG holds dy: G = dy / den, the row's 1/den applied to the products)
-// (rows key0 .. key0+15 of sK / sV at positions kpos[]); `pair(t, p)` says
+// (rows key0 .. key0+15 of sK / sV at positions kpos[]); sG holds dy, and
+// G = dy / den takes the row's 1/den after the products.  `pair(t, p)` says
 // whether key p is a softmax key of query t in this pass.
 template <int D, typename Pair>
 __device__ __forceinline__ void kv_block(const uint16_t *sK, const uint16_t *sV, int key0, const int *kpos,
@@ -829,7 +875,7 @@ __device__ __forceinline__ void kv_block(const uint16_t *sK, const uint16_t *sV,
 #pragma unroll
             for (int r = 0; r < 2; ++r) {
                 const bool in = t >= 0 && kp[r] >= 0 && pair(t, kp[r]);
-                const float pe = in ? expf(s[nt][2 * r + e] * scale - R.c[qi]) : 0.f;
+                const float pe = in ? exp2_mufu((s[nt][2 * r + e] * scale - R.c[qi]) * 1.4426950408889634f) : 0.f;
                 float ds = pe * (dp[nt][2 * r + e] * R.inv[qi] - R.delta[qi]);
                 if (in && R.js[qi] == kp[r]) ds -= R.dss[qi];
                 s[nt][2 * r + e] = pe * R.inv[qi];
@@ -844,48 +890,50 @@ __device__ __forceinline__ void kv_block(const uint16_t *sK, const uint16_t *sV,
 }
 
 template <int D, int G>
-__global__ void __launch_bounds__(BQ_THREADS, 1) key_kernel(BwdArgs P)
+__global__ void __launch_bounds__(BQ8_THREADS, 1) key_kernel(BwdArgs P)
 {
     grid_dep_sync();
     constexpr int LD = D + 8, KC = D / 16, NT = D / 8;
     using L = KLayout<D>;
     extern __shared__ __align__(16) uint8_t smem[];
     uint16_t *sK = (uint16_t *)(smem + L::K), *sV = (uint16_t *)(smem + L::V), *sPK = (uint16_t *)(smem + L::PK);
-    uint16_t *sQ = (uint16_t *)(smem + L::Q), *sG = (uint16_t *)(smem + L::G), *sPQ = (uint16_t *)(smem + L::PQ);
     uint16_t *sR = (uint16_t *)(smem + L::R);
     float *sRV = (float *)(smem + L::RV);
-    int *rowi = (int *)(smem + L::ROW);
-    QRows R{rowi, (float *)(rowi + BT), (float *)(rowi + 2 * BT), (float *)(rowi + 3 * BT), (float *)(rowi + 4 * BT),
-            rowi + 5 * BT};
     int *kpos = (int *)(smem + L::KPOS);
 
     const Dims &dm = P.dm;
     const int N = dm.N, W = dm.W;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gid = lane >> 2, tig = lane & 3;
     const int unit = blockIdx.y, b = unit / dm.Hkv, gq = unit % dm.Hkv;
-    const int j0 = blockIdx.x * 64;
+    const int j0 = blockIdx.x * BK_KEYS;
     const size_t krow0 = (size_t)unit * N;
     const int key0 = warp * 16;
     const int kr[2] = {j0 + key0 + gid, j0 + key0 + gid + 8};
 
-    for (int i = threadIdx.x; i < 64; i += blockDim.x) kpos[i] = j0 + i < N ? j0 + i : -1;
+    for (int i = threadIdx.x; i < BK_KEYS; i += blockDim.x) kpos[i] = j0 + i < N ? j0 + i : -1;
     __syncthreads();
-    stage_rows<D>(sK, LD, 64, [&](int r) -> const uint16_t * { return kpos[r] >= 0 ? P.k + (krow0 + kpos[r]) * D : nullptr; });
-    stage_rows<D>(sV, LD, 64, [&](int r) -> const uint16_t * { return kpos[r] >= 0 ? P.v + (krow0 + kpos[r]) * D : nullptr; });
-    stage_rows<D>(sPK, LD, 64, [&](int r) -> const uint16_t * { return kpos[r] >= 0 ? P.phk + (krow0 + kpos[r]) * D : nullptr; });
+    stage_rows<D>(sK, LD, BK_KEYS, [&](int r) -> const uint16_t * { return kpos[r] >= 0 ? P.k + (krow0 + kpos[r]) * D : nullptr; });
+    stage_rows<D>(sV, LD, BK_KEYS, [&](int r) -> const uint16_t * { return kpos[r] >= 0 ? P.v + (krow0 + kpos[r]) * D : nullptr; });
+    stage_rows<D>(sPK, LD, BK_KEYS, [&](int r) -> const uint16_t * { return kpos[r] >= 0 ? P.phk + (krow0 + kpos[r]) * D : nullptr; });
+    __syncthreads();
 
     // ---- window queries: t in [j, j + W - 1]
     float dK[NT][4], dV[NT][4];
     zero(dK);
     zero(dV);
-    const int tq_end = min(j0 + 64 + W - 1, N);
-    for (int hh = 0; hh < G; ++hh) {
-        const int h = gq * G + hh;
-        for (int tq0 = j0; tq0 < tq_end; tq0 += BT) {
-            stage_qblock<D>(P, b, h, tq0, tq_end, false, sQ, sG, sPQ, R);
-            kv_block<D>(sK, sV, key0, kpos, sQ, sG, R, P.scale, dK, dV,
-                        [&](int t, int p) { return p <= t && p > t - W; });
-        }
+    {
+        const int tq_end = min(j0 + BK_KEYS + W - 1, N);
+        const int per = (tq_end - j0 + BT - 1) / BT;
+        query_blocks<D>(P, b, G * per, false, smem,
+                        [&](int i, int &h, int &tq0, int &tq1) {
+                            h = gq * G + i / per;
+                            tq0 = j0 + (i % per) * BT;
+                            tq1 = tq_end;
+                        },
+                        [&](int, const uint16_t *sQ, const uint16_t *sG, const uint16_t *, QRows R) {
+                            kv_block<D>(sK, sV, key0, kpos, sQ, sG, R, P.scale, dK, dV,
+                                        [&](int t, int p) { return p <= t && p > t - W; });
+                        });
     }
 #pragma unroll
     for (int r = 0; r < 2; ++r)
@@ -897,10 +945,9 @@ __global__ void __launch_bounds__(BQ_THREADS, 1) key_kernel(BwdArgs P)
         }
 
     // ---- linear branch: R, r over the queries t >= U1, then the lag queries [j + W, U1)
-    const int U1 = ((j0 + 63 + W + BT - 1) / BT) * BT;
+    const int U1 = ((j0 + BK_KEYS - 1 + W + BT - 1) / BT) * BT;
     const int ub = min(U1 / BT, P.nblk);
     const size_t rslot = (size_t)unit * (P.nblk + 1) + (P.nblk - ub);
-    __syncthreads();
     stage_f32(sR, LD, P.Rs + rslot * D * D, D, D);
     for (int f = threadIdx.x; f < D; f += blockDim.x) sRV[f] = P.rs[rslot * D + f];
     __syncthreads();
@@ -925,49 +972,54 @@ __global__ void __launch_bounds__(BQ_THREADS, 1) key_kernel(BwdArgs P)
             dph[nt][e] -= rv;
             dph[nt][2 + e] -= rv;
         }
-    const int lq0 = j0 + W, lq1 = min(U1, N);
-    for (int hh = 0; hh < G; ++hh) {
-        const int h = gq * G + hh;
-        for (int tq0 = lq0; tq0 < lq1; tq0 += BT) {
-            stage_qblock<D>(P, b, h, tq0, lq1, true, sQ, sG, sPQ, R);
-            float dat[4][4], at[4][4];
-            zero(dat);
-            zero(at);
+    {
+        const int lq0 = j0 + W, lq1 = min(U1, N);
+        const int per = lq1 > lq0 ? (lq1 - lq0 + BT - 1) / BT : 0;
+        query_blocks<D>(P, b, G * per, true, smem,
+                        [&](int i, int &h, int &tq0, int &tq1) {
+                            h = gq * G + i / per;
+                            tq0 = lq0 + (i % per) * BT;
+                            tq1 = lq1;
+                        },
+                        [&](int, const uint16_t *, const uint16_t *sG, const uint16_t *sPQ, QRows R) {
+                            float dat[4][4], at[4][4];
+                            zero(dat);
+                            zero(at);
 #pragma unroll
-            for (int kc = 0; kc < KC; ++kc) {
-                uint32_t va[4], pk[4];
-                load_a(sV, LD, key0, kc * 16, va);
-                load_a(sPK, LD, key0, kc * 16, pk);
+                            for (int kc = 0; kc < KC; ++kc) {
+                                uint32_t va[4], pk[4];
+                                load_a(sV, LD, key0, kc * 16, va);
+                                load_a(sPK, LD, key0, kc * 16, pk);
 #pragma unroll
-                for (int nt = 0; nt < 4; nt += 2) {
-                    uint32_t f[4];
-                    load_b(sG, LD, nt * 8, kc * 16, f);
-                    mma(dat[nt], va, f[0], f[1]);
-                    mma(dat[nt + 1], va, f[2], f[3]);
-                    load_b(sPQ, LD, nt * 8, kc * 16, f);
-                    mma(at[nt], pk, f[0], f[1]);
-                    mma(at[nt + 1], pk, f[2], f[3]);
-                }
-            }
+                                for (int nt = 0; nt < 4; nt += 2) {
+                                    uint32_t f[4];
+                                    load_b(sG, LD, nt * 8, kc * 16, f);
+                                    mma(dat[nt], va, f[0], f[1]);
+                                    mma(dat[nt + 1], va, f[2], f[3]);
+                                    load_b(sPQ, LD, nt * 8, kc * 16, f);
+                                    mma(at[nt], pk, f[0], f[1]);
+                                    mma(at[nt + 1], pk, f[2], f[3]);
+                                }
+                            }
 #pragma unroll
-            for (int nt = 0; nt < 4; ++nt)
+                            for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const int qi = nt * 8 + 2 * tig + e;
-                    const int t = R.tok[qi];
+                                for (int e = 0; e < 2; ++e) {
+                                    const int qi = nt * 8 + 2 * tig + e;
+                                    const int t = R.tok[qi];
 #pragma unroll
-                    for (int r = 0; r < 2; ++r) {
-                        const bool in = t >= 0 && kr[r] < N && t >= kr[r] + W;
-                        dat[nt][2 * r + e] = in ? dat[nt][2 * r + e] * R.inv[qi] - R.delta[qi] : 0.f;
-                        at[nt][2 * r + e] = in ? at[nt][2 * r + e] * R.inv[qi] : 0.f;
-                    }
-                }
-            uint32_t df[2][4], af[2][4];
-            acc_to_a<4>(dat, df);
-            acc_to_a<4>(at, af);
-            mma_tile<2, NT, true>(dph, df, sPQ, LD, 0, 0);
-            mma_tile<2, NT, true>(dV, af, sG, LD, 0, 0);
-        }
+                                    for (int r = 0; r < 2; ++r) {
+                                        const bool in = t >= 0 && kr[r] < N && t >= kr[r] + W;
+                                        dat[nt][2 * r + e] = in ? dat[nt][2 * r + e] * R.inv[qi] - R.delta[qi] : 0.f;
+                                        at[nt][2 * r + e] = in ? at[nt][2 * r + e] * R.inv[qi] : 0.f;
+                                    }
+                                }
+                            uint32_t df[2][4], af[2][4];
+                            acc_to_a<4>(dat, df);
+                            acc_to_a<4>(at, af);
+                            mma_tile<2, NT, true>(dph, df, sPQ, LD, 0, 0);
+                            mma_tile<2, NT, true>(dV, af, sG, LD, 0, 0);
+                        });
     }
     // kept keys have no linear role
 #pragma unroll
@@ -1035,21 +1087,17 @@ __global__ void __launch_bounds__(BQ_THREADS, 1) key_kernel(BwdArgs P)
 }
 
 // dk, dv of the kept keys from the queries of later chunks outside the window:
-// CTA = 64 entries of the kept table x one range of query tokens.
+// CTA = 128 entries of the kept table x one range of query tokens.
 constexpr int KEPT_TOKENS = 256;
 
 template <int D, int G>
-__global__ void __launch_bounds__(BQ_THREADS, 2) kept_kernel(BwdArgs P)
+__global__ void __launch_bounds__(BQ8_THREADS, 1) kept_kernel(BwdArgs P)
 {
     grid_dep_sync();
     constexpr int LD = D + 8, NT = D / 8;
     using L = KLayout<D>;
     extern __shared__ __align__(16) uint8_t smem[];
     uint16_t *sK = (uint16_t *)(smem + L::K), *sV = (uint16_t *)(smem + L::V);
-    uint16_t *sQ = (uint16_t *)(smem + L::Q), *sG = (uint16_t *)(smem + L::G), *sPQ = (uint16_t *)(smem + L::PQ);
-    int *rowi = (int *)(smem + L::ROW);
-    QRows R{rowi, (float *)(rowi + BT), (float *)(rowi + 2 * BT), (float *)(rowi + 3 * BT), (float *)(rowi + 4 * BT),
-            rowi + 5 * BT};
     int *kpos = (int *)(smem + L::KPOS);
 
     const Dims &dm = P.dm;
@@ -1057,37 +1105,41 @@ __global__ void __launch_bounds__(BQ_THREADS, 2) kept_kernel(BwdArgs P)
     const int KP = dm.T_max * dm.lam;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gid = lane >> 2, tig = lane & 3;
     const int unit = blockIdx.y, b = unit / dm.Hkv, gq = unit % dm.Hkv;
-    const int e0 = blockIdx.x * 64;
+    const int e0 = blockIdx.x * BK_KEYS;
     const size_t krow0 = (size_t)unit * N;
     const int key0 = warp * 16;
-    // queries of this CTA: tokens [tq_lo, tq_hi), from the end of the first entry's chunk on
     auto entry = [&](int e) -> int {
         const int p = e < KP ? P.sel[(size_t)unit * KP + e] : -1;
         return p < N ? p : -1;
     };
+    // queries of this CTA: tokens [tq_lo, tq_hi), from the end of the first entry's chunk on
     int first = -1;
-    for (int i = 0; i < 64 && first < 0; ++i) first = entry(e0 + i);
+    for (int i = 0; i < BK_KEYS && first < 0; ++i) first = entry(e0 + i);
     if (first < 0) return;
     const int start = (first / C + 1) * C;
     const int tq_lo = start + blockIdx.z * KEPT_TOKENS, tq_hi = min(tq_lo + KEPT_TOKENS, N);
     if (tq_lo >= tq_hi) return;
 
-    for (int i = threadIdx.x; i < 64; i += blockDim.x) kpos[i] = entry(e0 + i);
+    for (int i = threadIdx.x; i < BK_KEYS; i += blockDim.x) kpos[i] = entry(e0 + i);
     __syncthreads();
-    stage_rows<D>(sK, LD, 64, [&](int r) -> const uint16_t * { return kpos[r] >= 0 ? P.k + (krow0 + kpos[r]) * D : nullptr; });
-    stage_rows<D>(sV, LD, 64, [&](int r) -> const uint16_t * { return kpos[r] >= 0 ? P.v + (krow0 + kpos[r]) * D : nullptr; });
+    stage_rows<D>(sK, LD, BK_KEYS, [&](int r) -> const uint16_t * { return kpos[r] >= 0 ? P.k + (krow0 + kpos[r]) * D : nullptr; });
+    stage_rows<D>(sV, LD, BK_KEYS, [&](int r) -> const uint16_t * { return kpos[r] >= 0 ? P.v + (krow0 + kpos[r]) * D : nullptr; });
+    __syncthreads();
 
     float dK[NT][4], dV[NT][4];
     zero(dK);
     zero(dV);
-    for (int hh = 0; hh < G; ++hh) {
-        const int h = gq * G + hh;
-        for (int tq0 = tq_lo; tq0 < tq_hi; tq0 += BT) {
-            stage_qblock<D>(P, b, h, tq0, tq_hi, false, sQ, sG, sPQ, R);
-            kv_block<D>(sK, sV, key0, kpos, sQ, sG, R, P.scale, dK, dV,
-                        [&](int t, int p) { return p <= t - W && p / C < t / C; });
-        }
-    }
+    const int per = (tq_hi - tq_lo + BT - 1) / BT;
+    query_blocks<D>(P, b, G * per, false, smem,
+                    [&](int i, int &h, int &tq0, int &tq1) {
+                        h = gq * G + i / per;
+                        tq0 = tq_lo + (i % per) * BT;
+                        tq1 = tq_hi;
+                    },
+                    [&](int, const uint16_t *sQ, const uint16_t *sG, const uint16_t *, QRows R) {
+                        kv_block<D>(sK, sV, key0, kpos, sQ, sG, R, P.scale, dK, dV,
+                                    [&](int t, int p) { return p <= t - W; });   // W >= C: an earlier chunk
+                    });
     const int kp[2] = {kpos[key0 + gid], kpos[key0 + gid + 8]};
 #pragma unroll
     for (int r = 0; r < 2; ++r)
@@ -1104,6 +1156,7 @@ __global__ void __launch_bounds__(BQ_THREADS, 2) kept_kernel(BwdArgs P)
         }
 }
 
+// ---------------------------------------------------------------------------
 // dWf = sum_rows x^T dl over the q rows and the k rows: CTA = a range of rows,
 // warp w the Wf rows [16w, 16w + 16); partial sums added atomically.  dl is
 // fp32; it enters the MMAs as a bf16 pair hi + lo (hi = bf16(dl), lo =
@@ -1217,13 +1270,15 @@ cudaError_t run(const BwdArgs &A, const BwdBuffers &bb, cudaStream_t s)
     {
         KTimer tm("bwd_key", s);
         chk(set_smem(key_kernel<D, G>, KLayout<D>::TOTAL));
-        chk(launch_kernel(key_kernel<D, G>, dim3((dm.N + 63) / 64, units), dim3(BQ_THREADS), KLayout<D>::TOTAL, s, A));
+        chk(launch_kernel(key_kernel<D, G>, dim3((dm.N + BK_KEYS - 1) / BK_KEYS, units), dim3(BQ8_THREADS), KLayout<D>::TOTAL,
+                          s, A));
     }
     if (KP > 0) {
         KTimer tm("bwd_kept", s);
         chk(set_smem(kept_kernel<D, G>, KLayout<D>::TOTAL));
         const int nsplit = (dm.N + KEPT_TOKENS - 1) / KEPT_TOKENS;
-        chk(launch_kernel(kept_kernel<D, G>, dim3((KP + 63) / 64, units, nsplit), dim3(BQ_THREADS), KLayout<D>::TOTAL, s, A));
+        chk(launch_kernel(kept_kernel<D, G>, dim3((KP + BK_KEYS - 1) / BK_KEYS, units, nsplit), dim3(BQ8_THREADS),
+                          KLayout<D>::TOTAL, s, A));
     }
     {
         KTimer tm("bwd_dwf", s);
