@@ -117,28 +117,6 @@ __global__ void mark_kept_kernel(const int32_t *__restrict__ sel, int KP, int N,
     if (p >= 0 && p < N) kept[(size_t)unit * N + p] = 1;
 }
 
-template <int D, int DF>
-__global__ void __launch_bounds__(256) phik_kernel(BwdArgs A, uint16_t *__restrict__ phk, float *__restrict__ phk32)
-{
-    grid_dep_sync();
-    __shared__ float xs[8][D];
-    __shared__ float ph[8][DF];
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const long long rows = (long long)A.dm.B * A.dm.Hkv * A.dm.N;
-    for (long long r = (long long)blockIdx.x * 8 + warp; r < rows; r += (long long)gridDim.x * 8) {
-        __syncwarp();
-        for (int e = lane; e < D; e += 32) xs[warp][e] = bf2f(A.k[r * D + e]);
-        __syncwarp();
-        warp_npmap<D, DF>(xs[warp], A.Wf, ph[warp], lane);
-        __syncwarp();
-        const bool kp = A.kept[r] != 0;
-        for (int e = lane; e < DF; e += 32) {
-            phk[r * DF + e] = kp ? (uint16_t)0 : f2bf(ph[warp][e]);
-            phk32[r * DF + e] = kp ? 0.f : ph[warp][e];
-        }
-    }
-}
-
 // ---------------------------------------------------------------------------
 // block sums of outer products: out[f][d] = sum_rows a[row][f] b[row][d],
 // zo[f] = sum_rows w[row] a[row][f], for the rows of one 32-token block
@@ -225,6 +203,102 @@ __device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_grou
 template <int N>
 __device__ __forceinline__ void cp_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
+// NP-Map of a warp's 16 rows x (A fragments xa, bf16): U = x Wf with Wf as a bf16
+// pair (hi, lo: shared tiles [d][df]), u = softmax(U), phi = ||x|| u / ||u|| into
+// phi (accumulator layout), ||x|| of the thread's two rows into nx.
+template <int D>
+__device__ __forceinline__ void warp_npmap_rows(const uint32_t (&xa)[D / 16][4], const uint16_t *wf_hi,
+                                                const uint16_t *wf_lo, float (&phi)[D / 8][4], float (&nx)[2])
+{
+    constexpr int LD = D + 8, KC = D / 16, NT = D / 8;
+    zero(phi);
+    mma_tile<KC, NT, true>(phi, xa, wf_hi, LD, 0, 0);
+    mma_tile<KC, NT, true>(phi, xa, wf_lo, LD, 0, 0);
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+        float mx = -INFINITY;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) mx = fmaxf(mx, fmaxf(phi[nt][2 * r], phi[nt][2 * r + 1]));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+        float s2 = 0.f, x2 = 0.f;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            phi[nt][2 * r] = expf(phi[nt][2 * r] - mx);
+            phi[nt][2 * r + 1] = expf(phi[nt][2 * r + 1] - mx);
+            s2 = fmaf(phi[nt][2 * r], phi[nt][2 * r], fmaf(phi[nt][2 * r + 1], phi[nt][2 * r + 1], s2));
+        }
+#pragma unroll
+        for (int kc = 0; kc < KC; ++kc) {
+            const uint32_t a0 = xa[kc][r], a1 = xa[kc][r + 2];
+            x2 = fmaf(lo_f(a0), lo_f(a0), fmaf(hi_f(a0), hi_f(a0), x2));
+            x2 = fmaf(lo_f(a1), lo_f(a1), fmaf(hi_f(a1), hi_f(a1), x2));
+        }
+        s2 = quad_sum(s2);
+        x2 = quad_sum(x2);
+        nx[r] = sqrtf(x2);
+        const float sc = s2 > 0.f ? nx[r] * rsqrtf(s2) : 0.f;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            phi[nt][2 * r] *= sc;
+            phi[nt][2 * r + 1] *= sc;
+        }
+    }
+}
+
+// Wf [d][df] fp32 -> two shared bf16 tiles hi = bf16(Wf), lo = bf16(Wf - hi)
+template <int D>
+__device__ __forceinline__ void stage_wf_pair(const float *__restrict__ Wf, uint16_t *hi, uint16_t *lo)
+{
+    constexpr int LD = D + 8;
+    for (int i = threadIdx.x; i < D * D / 4; i += blockDim.x) {
+        const int r = i / (D / 4), c = (i % (D / 4)) * 4;
+        const float4 x = __ldg(reinterpret_cast<const float4 *>(Wf) + i);
+        const uint32_t h0 = pack(x.x, x.y), h1 = pack(x.z, x.w);
+        *reinterpret_cast<uint2 *>(hi + r * LD + c) = make_uint2(h0, h1);
+        *reinterpret_cast<uint2 *>(lo + r * LD + c) =
+            make_uint2(pack(x.x - lo_f(h0), x.y - hi_f(h0)), pack(x.z - lo_f(h1), x.w - hi_f(h1)));
+    }
+}
+
+// phi(k) of 128 key rows per CTA (eight warps of 16 rows) on warp MMAs, fp32 and
+// bf16 copies, kept keys' rows zero
+template <int D>
+__global__ void __launch_bounds__(256) phik_mma_kernel(BwdArgs A, uint16_t *__restrict__ phk, float *__restrict__ phk32)
+{
+    grid_dep_sync();
+    constexpr int LD = D + 8, KC = D / 16, NT = D / 8;
+    extern __shared__ __align__(16) uint8_t smem[];
+    uint16_t *hi = (uint16_t *)smem, *lo = hi + D * LD;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gid = lane >> 2, tig = lane & 3;
+    const long long rows = (long long)A.dm.B * A.dm.Hkv * A.dm.N;
+    const long long r0 = (long long)blockIdx.x * 128 + warp * 16;
+    stage_wf_pair<D>(A.Wf, hi, lo);
+    __syncthreads();
+    const long long rr[2] = {r0 + gid, r0 + gid + 8};
+    uint32_t xa[KC][4];
+#pragma unroll
+    for (int kc = 0; kc < KC; ++kc)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const long long row = rr[i & 1];
+            xa[kc][i] = row < rows ? ld_pair(A.k + row * D, 16 * kc + 8 * (i >> 1) + 2 * tig) : 0u;
+        }
+    float ph[NT][4], nx[2];
+    warp_npmap_rows<D>(xa, hi, lo, ph, nx);
+#pragma unroll
+    for (int r = 0; r < 2; ++r)
+        if (rr[r] < rows) {
+            const bool kp = A.kept[rr[r]] != 0;
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                const float a = kp ? 0.f : ph[nt][2 * r], b = kp ? 0.f : ph[nt][2 * r + 1];
+                *reinterpret_cast<uint32_t *>(phk + rr[r] * D + nt * 8 + 2 * tig) = pack(a, b);
+                *reinterpret_cast<float2 *>(phk32 + rr[r] * D + nt * 8 + 2 * tig) = make_float2(a, b);
+            }
+        }
+}
+
 template <int D>
 struct QLayout {
     static constexpr int LD = D + 8, T32 = BT * LD * 2;
@@ -272,14 +346,7 @@ __global__ void __launch_bounds__(BQ8_THREADS, 1) query_kernel(BwdArgs P)
 
     // ---- Wf as a bf16 pair hi (sWF, resident) + lo (in the S region until S is staged):
     // U = q Wf to about 16 significant bits of Wf
-    for (int i = tid; i < D * D / 4; i += BQ8_THREADS) {
-        const int r = i / (D / 4), c = (i % (D / 4)) * 4;
-        const float4 x = __ldg(reinterpret_cast<const float4 *>(P.Wf) + i);
-        const uint32_t h0 = pack(x.x, x.y), h1 = pack(x.z, x.w);
-        *reinterpret_cast<uint2 *>(sWF + r * LD + c) = make_uint2(h0, h1);
-        *reinterpret_cast<uint2 *>(sSP + r * LD + c) =
-            make_uint2(pack(x.x - lo_f(h0), x.y - hi_f(h0)), pack(x.z - lo_f(h1), x.w - hi_f(h1)));
-    }
+    stage_wf_pair<D>(P.Wf, sWF, sSP);
     // the linear state before the lag keys: keys < BT * i0
     const int i0 = t0 - W > 0 ? (t0 - W) / BT : 0;
     const int lag0 = BT * i0, lag1 = min(t0 + TOK - W, N);   // lag keys [lag0, lag1)
@@ -368,39 +435,7 @@ __global__ void __launch_bounds__(BQ8_THREADS, 1) query_kernel(BwdArgs P)
     uint32_t pa[KC][4];
     {
         float u[NT][4];
-        zero(u);
-        mma_tile<KC, NT, true>(u, qa, sWF, LD, 0, 0);
-        mma_tile<KC, NT, true>(u, qa, sSP, LD, 0, 0);
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-            float mx = -INFINITY;
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt) mx = fmaxf(mx, fmaxf(u[nt][2 * r], u[nt][2 * r + 1]));
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-            float s2 = 0.f, x2 = 0.f;
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
-                u[nt][2 * r] = expf(u[nt][2 * r] - mx);
-                u[nt][2 * r + 1] = expf(u[nt][2 * r + 1] - mx);
-                s2 = fmaf(u[nt][2 * r], u[nt][2 * r], fmaf(u[nt][2 * r + 1], u[nt][2 * r + 1], s2));
-            }
-#pragma unroll
-            for (int kc = 0; kc < KC; ++kc) {
-                const uint32_t a0 = qa[kc][r], a1 = qa[kc][r + 2];
-                x2 = fmaf(lo_f(a0), lo_f(a0), fmaf(hi_f(a0), hi_f(a0), x2));
-                x2 = fmaf(lo_f(a1), lo_f(a1), fmaf(hi_f(a1), hi_f(a1), x2));
-            }
-            s2 = quad_sum(s2);
-            x2 = quad_sum(x2);
-            nq[r] = sqrtf(x2);
-            const float sc = s2 > 0.f ? nq[r] * rsqrtf(s2) : 0.f;
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
-                u[nt][2 * r] *= sc;
-                u[nt][2 * r + 1] *= sc;
-            }
-        }
+        warp_npmap_rows<D>(qa, sWF, sSP, u, nq);
 #pragma unroll
         for (int r = 0; r < 2; ++r)
             if (tr[r] < N) {
@@ -1161,20 +1196,29 @@ __global__ void __launch_bounds__(BQ8_THREADS, 1) kept_kernel(BwdArgs P)
 // warp w the Wf rows [16w, 16w + 16); partial sums added atomically.  dl is
 // fp32; it enters the MMAs as a bf16 pair hi + lo (hi = bf16(dl), lo =
 // bf16(dl - hi)), about 16 significant bits.
-constexpr int DWF_ROWS = 1024;
+constexpr int DWF_ROWS_Q = 1024, DWF_ROWS_K = 256;   // rows per CTA of the q rows and of the k rows
 
 template <int D, int DF>
-__global__ void __launch_bounds__(256) dwf_kernel(const uint16_t *__restrict__ x, const float *__restrict__ dl,
-                                                  long long rows, float *__restrict__ dWf)
+__global__ void __launch_bounds__(256) dwf_kernel(const uint16_t *__restrict__ xq, const float *__restrict__ dlq,
+                                                  long long rows_q, const uint16_t *__restrict__ xk,
+                                                  const float *__restrict__ dlk, long long rows_k, int ctas_q,
+                                                  float *__restrict__ dWf)
 {
     grid_dep_sync();
+    // CTAs [0, ctas_q) take the q rows, the others the k rows
+    const bool kq = (int)blockIdx.x < ctas_q;
+    const uint16_t *x = kq ? xq : xk;
+    const float *dl = kq ? dlq : dlk;
+    const long long rows = kq ? rows_q : rows_k;
+    const long long per = kq ? DWF_ROWS_Q : DWF_ROWS_K;
+    const long long cta = kq ? blockIdx.x : blockIdx.x - ctas_q;
     constexpr int LDX = D + 8, LDL = DF + 8, NT = DF / 8;
     __shared__ __align__(16) uint16_t sx[BT * LDX];
     __shared__ __align__(16) uint16_t sl[BT * LDL];
     __shared__ __align__(16) uint16_t sl2[BT * LDL];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gid = lane >> 2, tig = lane & 3;
-    const long long r0 = (long long)blockIdx.x * DWF_ROWS;
-    const long long r1 = min(r0 + DWF_ROWS, rows);
+    const long long r0 = cta * per;
+    const long long r1 = min(r0 + per, rows);
     float acc[NT][4];
     zero(acc);
     for (long long rb = r0; rb < r1; rb += BT) {
@@ -1242,8 +1286,9 @@ cudaError_t run(const BwdArgs &A, const BwdBuffers &bb, cudaStream_t s)
         chk(cudaMemsetAsync(bb.kept, 0, (size_t)units * dm.N, s));
         if (KP > 0) chk(launch_kernel(mark_kept_kernel, dim3((KP + 255) / 256, units), dim3(256), 0, s, A.sel, KP, dm.N, bb.kept));
         const long long rows = (long long)units * dm.N;
-        const int grid = (int)min((rows + 7) / 8, 152LL * 16);
-        chk(launch_kernel(phik_kernel<D, D>, dim3(grid), dim3(256), 0, s, A, bb.phk, bb.phk32));
+        const size_t sm = 2 * (size_t)D * (D + 8) * 2;
+        chk(set_smem(phik_mma_kernel<D>, sm));
+        chk(launch_kernel(phik_mma_kernel<D>, dim3((unsigned)((rows + 127) / 128)), dim3(256), sm, s, A, bb.phk, bb.phk32));
     }
     const size_t bs_smem = BSLayout<D, D>::TOTAL;
     const int nel_s = D * D, nel_z = D;
@@ -1284,10 +1329,9 @@ cudaError_t run(const BwdArgs &A, const BwdBuffers &bb, cudaStream_t s)
         KTimer tm("bwd_dwf", s);
         chk(cudaMemsetAsync(A.dWf, 0, (size_t)D * D * 4, s));
         const long long rq = (long long)dm.B * dm.Hq * dm.N, rk = (long long)units * dm.N;
-        chk(launch_kernel(dwf_kernel<D, D>, dim3((unsigned)((rq + DWF_ROWS - 1) / DWF_ROWS)), dim3(256), 0, s, A.q,
-                          (const float *)A.dlq, rq, A.dWf));
-        chk(launch_kernel(dwf_kernel<D, D>, dim3((unsigned)((rk + DWF_ROWS - 1) / DWF_ROWS)), dim3(256), 0, s, A.k,
-                          (const float *)A.dlk, rk, A.dWf));
+        const int cq = (int)((rq + DWF_ROWS_Q - 1) / DWF_ROWS_Q), ck = (int)((rk + DWF_ROWS_K - 1) / DWF_ROWS_K);
+        chk(launch_kernel(dwf_kernel<D, D>, dim3((unsigned)(cq + ck)), dim3(256), 0, s, A.q, (const float *)A.dlq, rq,
+                          A.k, (const float *)A.dlk, rk, cq, A.dWf));
     }
     return e;
 }
