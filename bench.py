@@ -751,7 +751,7 @@ def bench_backward(still, dev, stream, pk, pk_kind, seed, steps=20, cpu=True):
                         "frac": max(t_flop, t_hbm) * 1e3 / ms, "peak_source": pk_kind,
                         "split": {k2: alg[k2] for k2 in ("F_softmax", "F_linear", "F_npmap")}},
            "kernels": {k2: {"launches": n, "ms_per_launch": m / n} for k2, (n, m) in kt.items()},
-           "gpu_launches_per_step": 11}
+           "gpu_launches_per_step": 10}
     if cpu:
         from oracle import grad
         torch_threads = torch.get_num_threads()
