@@ -188,6 +188,7 @@ __global__ void __launch_bounds__(256) blocksum_kernel(BwdArgs P, float *__restr
 // ---------------------------------------------------------------------------
 constexpr int BQ8_THREADS = 256;   // the query pass: eight warps of 16 rows
 constexpr int KEPT_MAX = 1024;     // kept positions of a CTA held in shared memory (more: read from global)
+constexpr int PKEEP = 10;          // key blocks whose P the query pass keeps for its second pass
 
 __device__ __forceinline__ void cp_async16(void *dst, const void *src, int src_bytes)
 {
@@ -308,7 +309,12 @@ struct QLayout {
     static constexpr int ZP = SP + D * LD * 2;     // z, fp32 [df]
     static constexpr int POS = ZP + D * 4;         // positions of the two staged key blocks and of the lag block
     static constexpr int KEPT = POS + 3 * BT * 4;  // the CTA's kept positions
-    static constexpr int TOTAL = KEPT + KEPT_MAX * 4;
+    // pass 1's P of the first PKEEP key blocks, per warp in A-fragment order
+    // ([block][register][lane] uint32: bf16 pairs), and the running maximum each
+    // block's P was taken against ([block][row] fp32)
+    static constexpr int PST = KEPT + KEPT_MAX * 4;
+    static constexpr int MST = PST + 8 * PKEEP * 8 * 32 * 4;
+    static constexpr int TOTAL = MST + 8 * PKEEP * 16 * 4;
 };
 
 // The thread's two accumulator rows are gid and gid + 8; element (nt, 2r + e)
@@ -335,6 +341,8 @@ __global__ void __launch_bounds__(BQ8_THREADS, 1) query_kernel(BwdArgs P)
     const int N = dm.N, W = dm.W, C = dm.C;
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31, gid = lane >> 2, tig = lane & 3;
+    uint32_t *sPst = (uint32_t *)(smem + L::PST) + (size_t)warp * PKEEP * 8 * 32;
+    float *sMst = (float *)(smem + L::MST) + (size_t)warp * PKEEP * 16;
     const int unit = blockIdx.y, b = unit / dm.Hkv, gq = unit % dm.Hkv;
     const int t0 = blockIdx.x * TOK;
     const int h = gq * G + warp % G;
@@ -514,6 +522,14 @@ __global__ void __launch_bounds__(BQ8_THREADS, 1) query_kernel(BwdArgs P)
                 }
         uint32_t pf[2][4];
         acc_to_a<4>(s, pf);
+        if (blk < PKEEP) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) sPst[(blk * 8 + i) * 32 + lane] = pf[i >> 2][i & 3];
+            if (tig == 0) {
+                sMst[blk * 16 + gid] = mrun[0];
+                sMst[blk * 16 + gid + 8] = mrun[1];
+            }
+        }
         mma_tile<2, NT, true>(o, pf, sVb + buf * T32E, LD, 0, 0);
     });
 #pragma unroll
@@ -643,23 +659,57 @@ __global__ void __launch_bounds__(BQ8_THREADS, 1) query_kernel(BwdArgs P)
     key_loop(true, [&](int blk, int buf) {
         const int *pos = sPosb + buf * BT;
         float s[4][4], dp[4][4];
-        logits(s, buf);
         zero(dp);
         mma_tile<KC, 4, false>(dp, ya, sVb + buf * T32E, LD, 0, 0);
-        const bool kb = blk < nkb;
+        if (blk < PKEEP) {
+            // P of pass 1 (bf16, masked keys zero), taken against the running maximum of
+            // its block: rescaled to c
+            float f[2];
 #pragma unroll
-        for (int nt = 0; nt < 4; ++nt)
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                const int p = pos[nt * 8 + 2 * tig + e];
-#pragma unroll
-                for (int r = 0; r < 2; ++r) {
-                    const float pe = in_sa(tr[r], p, kb) ? exp2_mufu(fmaf(s[nt][2 * r + e], scale_l2, -cl2[r])) : 0.f;
-                    const float ds = pe * (dp[nt][2 * r + e] * inv[r] - delta[r]);
-                    s[nt][2 * r + e] = ds;
-                    dss[r] += ds;
-                }
+            for (int r = 0; r < 2; ++r) {
+                const float mb = sMst[blk * 16 + gid + 8 * r];
+                f[r] = mb == -INFINITY ? 0.f : exp2_mufu((mb - cm[r]) * LOG2E);
             }
+#pragma unroll
+            for (int kc = 0; kc < 2; ++kc) {
+                const uint32_t w0 = sPst[(blk * 8 + kc * 4 + 0) * 32 + lane], w1 = sPst[(blk * 8 + kc * 4 + 1) * 32 + lane];
+                const uint32_t w2 = sPst[(blk * 8 + kc * 4 + 2) * 32 + lane], w3 = sPst[(blk * 8 + kc * 4 + 3) * 32 + lane];
+                s[2 * kc][0] = lo_f(w0) * f[0];
+                s[2 * kc][1] = hi_f(w0) * f[0];
+                s[2 * kc][2] = lo_f(w1) * f[1];
+                s[2 * kc][3] = hi_f(w1) * f[1];
+                s[2 * kc + 1][0] = lo_f(w2) * f[0];
+                s[2 * kc + 1][1] = hi_f(w2) * f[0];
+                s[2 * kc + 1][2] = lo_f(w3) * f[1];
+                s[2 * kc + 1][3] = hi_f(w3) * f[1];
+            }
+#pragma unroll
+            for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+                for (int e = 0; e < 2; ++e)
+#pragma unroll
+                    for (int r = 0; r < 2; ++r) {
+                        const float ds = s[nt][2 * r + e] * (dp[nt][2 * r + e] * inv[r] - delta[r]);
+                        s[nt][2 * r + e] = ds;
+                        dss[r] += ds;
+                    }
+        } else {
+            logits(s, buf);
+            const bool kb = blk < nkb;
+#pragma unroll
+            for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int p = pos[nt * 8 + 2 * tig + e];
+#pragma unroll
+                    for (int r = 0; r < 2; ++r) {
+                        const float pe = in_sa(tr[r], p, kb) ? exp2_mufu(fmaf(s[nt][2 * r + e], scale_l2, -cl2[r])) : 0.f;
+                        const float ds = pe * (dp[nt][2 * r + e] * inv[r] - delta[r]);
+                        s[nt][2 * r + e] = ds;
+                        dss[r] += ds;
+                    }
+                }
+        }
         uint32_t sf[2][4];
         acc_to_a<4>(s, sf);
         mma_tile<2, NT, true>(dq, sf, sKb + buf * T32E, LD, 0, 0);
