@@ -1009,13 +1009,17 @@ __global__ void __launch_bounds__(BQ8_THREADS, 1) key_kernel(BwdArgs P)
     {
         const int tq_end = min(j0 + BK_KEYS + W - 1, N);
         const int per = (tq_end - j0 + BT - 1) / BT;
+        // a warp's keys [jw, jw + 16) see the queries [jw, jw + 15 + W): it skips the other blocks
+        const int jw = j0 + key0;
         query_blocks<D>(P, b, G * per, false, smem,
                         [&](int i, int &h, int &tq0, int &tq1) {
                             h = gq * G + i / per;
                             tq0 = j0 + (i % per) * BT;
                             tq1 = tq_end;
                         },
-                        [&](int, const uint16_t *sQ, const uint16_t *sG, const uint16_t *, QRows R) {
+                        [&](int i, const uint16_t *sQ, const uint16_t *sG, const uint16_t *, QRows R) {
+                            const int tq0 = j0 + (i % per) * BT;
+                            if (tq0 + BT - 1 < jw || tq0 > jw + 15 + W - 1) return;
                             kv_block<D>(sK, sV, key0, kpos, sQ, sG, R, P.scale, dK, dV,
                                         [&](int t, int p) { return p <= t && p > t - W; });
                         });
@@ -1214,6 +1218,14 @@ __global__ void __launch_bounds__(BQ8_THREADS, 1) kept_kernel(BwdArgs P)
     float dK[NT][4], dV[NT][4];
     zero(dK);
     zero(dV);
+    // the warp's first live query: the smallest p + W over its entries (entries ascend,
+    // so the first valid one), or none
+    int wfirst = INT_MAX;
+    for (int i = 0; i < 16; ++i)
+        if (kpos[key0 + i] >= 0) {
+            wfirst = kpos[key0 + i] + W;
+            break;
+        }
     const int per = (tq_hi - tq_lo + BT - 1) / BT;
     query_blocks<D>(P, b, G * per, false, smem,
                     [&](int i, int &h, int &tq0, int &tq1) {
@@ -1221,7 +1233,8 @@ __global__ void __launch_bounds__(BQ8_THREADS, 1) kept_kernel(BwdArgs P)
                         tq0 = tq_lo + (i % per) * BT;
                         tq1 = tq_hi;
                     },
-                    [&](int, const uint16_t *sQ, const uint16_t *sG, const uint16_t *, QRows R) {
+                    [&](int i, const uint16_t *sQ, const uint16_t *sG, const uint16_t *, QRows R) {
+                        if (tq_lo + (i % per) * BT + BT - 1 < wfirst) return;
                         kv_block<D>(sK, sV, key0, kpos, sQ, sG, R, P.scale, dK, dV,
                                     [&](int t, int p) { return p <= t - W; });   // W >= C: an earlier chunk
                     });
