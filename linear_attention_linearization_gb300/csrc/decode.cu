@@ -576,7 +576,7 @@ __device__ void block_npmap(const float *x, int nrows, const float *__restrict__
         float4 acc[DS_NP_ROWS];
 #pragma unroll
         for (int r = 0; r < DS_NP_ROWS; ++r) acc[r] = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
+#pragma unroll 8
         for (int i = 0; i < IS; ++i) {
             const float4 w = __ldg(reinterpret_cast<const float4 *>(Wf + (size_t)(sl * IS + i) * DF) + c4);
 #pragma unroll
