@@ -153,3 +153,39 @@ def test_backward_of_an_empty_sequence_zeroes_dwf(still):
                           torch.empty_like(k, dtype=torch.float32), dWf))
     torch.cuda.synchronize()
     assert (dWf == 0).all()
+
+
+def test_backward_repeated_calls_and_workspace(still):
+    # dq has no atomic additions: bit-identical across calls; dk, dv, dWf take atomic
+    # additions in an unspecified order: equal to within fp32 reassociation
+    w = Workload("rep", 2, 8, 2, 128, 300, 64, 64, 288, 16, 128, "dirnorm", 0.05)
+    q, k, v, Wf = (t.to(DEV) for t in inputs.make_inputs(w, seed=8))
+    dy = inputs.make_dout(w, seed=8).to(DEV)
+    _, sel = still.prefill(q, k, v, Wf, w.W, w.C, w.m, w.T_max)
+    ws = torch.empty(still.backward_workspace_size(q, k, Wf, w.W, w.C, w.m, w.T_max), dtype=torch.uint8, device=DEV)
+    a = [t.clone() for t in still.backward(q, k, v, Wf, w.W, w.C, w.m, w.T_max, sel, dy)]
+    b = still.backward(q, k, v, Wf, w.W, w.C, w.m, w.T_max, sel, dy, workspace=ws)
+    c = still.backward(q, k, v, Wf, w.W, w.C, w.m, w.T_max, sel, dy, workspace=ws)
+    torch.cuda.synchronize()
+    for x, y, z in zip(a, b, c):
+        scale = x.abs().max().item()
+        assert (x - y).abs().max().item() <= 1e-5 * scale and (y - z).abs().max().item() <= 1e-5 * scale
+    assert torch.equal(a[0], b[0]) and torch.equal(b[0], c[0])
+
+
+def test_backward_ignores_selection_entries_out_of_range(still):
+    # an entry past the sequence is no token (as -1): the kernels never read its row
+    w = Workload("oor", 1, 4, 2, 64, 256, 32, 32, 32 + 4 * 8, 8, 64)
+    q, k, v, Wf = (t.to(DEV) for t in inputs.make_inputs(w, seed=9))
+    dy = inputs.make_dout(w, seed=9).to(DEV)
+    _, sel = still.prefill(q, k, v, Wf, w.W, w.C, w.m, w.T_max)
+    sel_a = sel.clone()
+    sel_a[:, :, 2, 1] = -1
+    sel_b = sel.clone()
+    sel_b[:, :, 2, 1] = w.N + 1000
+    ga = still.backward(q, k, v, Wf, w.W, w.C, w.m, w.T_max, sel_a, dy)
+    gb = still.backward(q, k, v, Wf, w.W, w.C, w.m, w.T_max, sel_b, dy)
+    torch.cuda.synchronize()
+    assert torch.equal(ga[0], gb[0])
+    for x, y in zip(ga[1:], gb[1:]):
+        assert (x - y).abs().max().item() <= 1e-5 * x.abs().max().item()
