@@ -249,10 +249,9 @@ still_status still_prefill_gated(const still_shape *shape, const still_bf16 *q, 
  *                 row maximum c_t took (the key that received c's gradient)
  *   workspace     still_backward_workspace_size() bytes, 16-byte aligned, or
  *                 NULL for a stream-ordered allocation inside the call
- * Supported: d == d_f in {64, 128}, G = Hq/Hkv in {1, 2, 4}, and W >= C (then
- * a kept key older than the window is always of an earlier chunk: a softmax
- * key of every later query outside its window and never a linear key); other
- * shapes return STILL_ERR_UNSUPPORTED.  All device pointers 16-byte aligned.
+ * Supported: d == d_f in {64, 128}, G = Hq/Hkv in {1, 2, 4}, and lambda <= 128
+ * when W < C (a kept key is then a linear key of the later queries of its own
+ * chunk until the chunk completes); other shapes return STILL_ERR_UNSUPPORTED.  All device pointers 16-byte aligned.
  * The call is asynchronous on `stream`; dk, dv and dWf receive atomic
  * additions, so their low-order bits may differ between runs.
  */

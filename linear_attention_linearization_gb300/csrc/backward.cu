@@ -22,20 +22,23 @@
 //                  dl = phi * (dphi - a phi/||x||), a = dphi.phi/||x||,
 //                  dx = a x/||x|| + Wf dl, dWf += x dl^T
 // (the softmax term <du, u> of the NP-Map's chain vanishes because u/||u|| has
-// unit norm).  The routing rule used here is the one for W >= C: every key at
-// or before t - W lies in an earlier chunk, so a kept key is a softmax key of
-// every later query outside its window and never a linear key.
+// unit norm).  A kept key is a softmax key of the queries of later chunks
+// outside its window; when W < C it is also a linear key of the later queries
+// of its own chunk (t >= j + W) until that chunk completes.
 //
 // Passes (one sequence and kv head per unit, states at 32-token blocks):
-//   mark_kept, phik     the kept flags and phi(k) (kept rows zero)
+//   mark_kept, phik     each key's kept-table entry, phi(k) (kept rows zero in
+//                       the key table, kept in a table of their own)
 //   blocksum, scan      S, z before every 32-key block (forward state)
 //   query               per 16-row warp tile: c, P V, the linear branch, y,
 //                       g, delta, dP, dS, dq (complete, NP-Map included)
 //   blocksum, scan      R, r after every 32-token block (reverse state)
 //   key                 per 16-key warp tile: dk, dv from the window queries
-//                       and the linear branch (NP-Map included)
+//                       and, for unkept keys, the linear branch (NP-Map included)
 //   kept                dk, dv of the kept keys from the queries of later
 //                       chunks outside their window (atomic adds)
+//   kept_lin (W < C)    the kept keys as linear keys of their own chunk,
+//                       with their NP-Map backward (atomic adds)
 //   dwf                 dWf = sum over q and k rows of x dl^T
 // The contractions run as warp MMAs (bf16 operands, fp32 accumulation).
 #include <climits>
@@ -60,8 +63,10 @@ struct BwdArgs {
     const uint16_t *q, *k, *v, *dy;
     const float *Wf;
     const int32_t *sel;  // [B, Hkv, T_max * lam]
-    const uint8_t *kept; // [B, Hkv, N]
+    const int32_t *kslot; // [B, Hkv, N]: the kept-table entry of a kept key, else -1
     const uint16_t *phk; // [B, Hkv, N, DF], kept rows zero
+    const uint16_t *phkk; // [B, Hkv, T_max * lam, DF]: phi(k) of the kept entries (bf16)
+    const float *phkk32;  // the same in fp32
     const float *Sp, *zp;   // [units][nblk + 1][DF * D], [units][nblk + 1][DF]: state before block i
     const float *Rs, *rs;   // the same layout, reversed blocks: index nblk - i holds the sums over t >= BT i
     uint16_t *g, *phq;               // g = dy / den (bf16, for the reverse state), phi(q) [B, Hq, N, *]
@@ -107,14 +112,14 @@ __device__ __forceinline__ void stage_f32(uint16_t *dst, int ld, const float *sr
 // ---------------------------------------------------------------------------
 // kept flags and phi(k)
 // ---------------------------------------------------------------------------
-__global__ void mark_kept_kernel(const int32_t *__restrict__ sel, int KP, int N, uint8_t *__restrict__ kept)
+__global__ void mark_kept_kernel(const int32_t *__restrict__ sel, int KP, int N, int32_t *__restrict__ kslot)
 {
     grid_dep_sync();
     const int unit = blockIdx.y;
     const int e = blockIdx.x * blockDim.x + threadIdx.x;
     if (e >= KP) return;
     const int p = sel[(size_t)unit * KP + e];
-    if (p >= 0 && p < N) kept[(size_t)unit * N + p] = 1;
+    if (p >= 0 && p < N) kslot[(size_t)unit * N + p] = e;
 }
 
 // ---------------------------------------------------------------------------
@@ -265,7 +270,8 @@ __device__ __forceinline__ void stage_wf_pair(const float *__restrict__ Wf, uint
 // phi(k) of 128 key rows per CTA (eight warps of 16 rows) on warp MMAs, fp32 and
 // bf16 copies, kept keys' rows zero
 template <int D>
-__global__ void __launch_bounds__(256) phik_mma_kernel(BwdArgs A, uint16_t *__restrict__ phk, float *__restrict__ phk32)
+__global__ void __launch_bounds__(256) phik_mma_kernel(BwdArgs A, uint16_t *__restrict__ phk, float *__restrict__ phk32,
+                                                       uint16_t *__restrict__ phkk, float *__restrict__ phkk32)
 {
     grid_dep_sync();
     constexpr int LD = D + 8, KC = D / 16, NT = D / 8;
@@ -287,15 +293,25 @@ __global__ void __launch_bounds__(256) phik_mma_kernel(BwdArgs A, uint16_t *__re
         }
     float ph[NT][4], nx[2];
     warp_npmap_rows<D>(xa, hi, lo, ph, nx);
+    const int KP = A.dm.T_max * A.dm.lam;
 #pragma unroll
     for (int r = 0; r < 2; ++r)
         if (rr[r] < rows) {
-            const bool kp = A.kept[rr[r]] != 0;
+            const int e = A.kslot[rr[r]];
+            const bool kp = e >= 0;
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
                 const float a = kp ? 0.f : ph[nt][2 * r], b = kp ? 0.f : ph[nt][2 * r + 1];
                 *reinterpret_cast<uint32_t *>(phk + rr[r] * D + nt * 8 + 2 * tig) = pack(a, b);
                 *reinterpret_cast<float2 *>(phk32 + rr[r] * D + nt * 8 + 2 * tig) = make_float2(a, b);
+            }
+            if (kp) {   // the kept entry's own features, unmasked
+                const size_t kr = ((size_t)(rr[r] / A.dm.N) * KP + e) * D;
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    *reinterpret_cast<uint32_t *>(phkk + kr + nt * 8 + 2 * tig) = pack(ph[nt][2 * r], ph[nt][2 * r + 1]);
+                    *reinterpret_cast<float2 *>(phkk32 + kr + nt * 8 + 2 * tig) = make_float2(ph[nt][2 * r], ph[nt][2 * r + 1]);
+                }
             }
         }
 }
@@ -427,10 +443,13 @@ __global__ void __launch_bounds__(BQ8_THREADS, 1) query_kernel(BwdArgs P)
             __syncthreads();
         }
     };
-    // (with W >= C a kept key at or before t - W is of an earlier chunk than t)
-    auto in_sa = [&](int t, int p, bool kept_blk) -> bool {
+    // the first token of each row's chunk: a kept key of an earlier chunk lies below it
+    // (with W >= C every key at or before t - W does)
+    const int tcs[2] = {tr[0] - tr[0] % C, tr[1] - tr[1] % C};
+    auto in_sa = [&](int r, int p, bool kept_blk) -> bool {
+        const int t = tr[r];
         if (p < 0 || t >= N) return false;
-        if (kept_blk) return p <= t - W;
+        if (kept_blk) return p <= t - W && p < tcs[r];
         return p <= t && p > t - W;
     };
     auto logits = [&](float (&s)[4][4], int buf) {
@@ -484,7 +503,7 @@ __global__ void __launch_bounds__(BQ8_THREADS, 1) query_kernel(BwdArgs P)
                 const int p = pos[nt * 8 + 2 * tig + e];
 #pragma unroll
                 for (int r = 0; r < 2; ++r) {
-                    const bool in = in_sa(tr[r], p, kb);
+                    const bool in = in_sa(r, p, kb);
                     const float x = in ? s[nt][2 * r + e] * scale : -INFINITY;
                     s[nt][2 * r + e] = x;
                     bm[r] = fmaxf(bm[r], x);
@@ -565,16 +584,32 @@ __global__ void __launch_bounds__(BQ8_THREADS, 1) query_kernel(BwdArgs P)
                 dlin[1] = fmaf(ph[nt][2 + e], z, dlin[1]);
             }
     }
+    // linear keys past the state: the lag keys [lag0, lag1) (kept keys are zero rows of the
+    // feature table), then -- when W < C -- the kept entries of the rows' own chunks, which
+    // stay linear keys until their chunk completes (blocks nlag .. nlag + nxb - 1)
+    const int xc0 = t0 / C, xc1 = min(tlast / C, dm.T_max - 1);
+    const int xe0 = xc0 * dm.lam, nx = W < C && dm.lam > 0 && xc1 >= xc0 ? (xc1 - xc0 + 1) * dm.lam : 0;
+    const int nxb = (nx + BT - 1) / BT;
     auto stage_lag = [&](int lb) {
+        const bool ex = lb >= nlag;
         __syncthreads();
         for (int i = threadIdx.x; i < BT; i += blockDim.x) {
-            const int p = lag0 + lb * BT + i;
-            sLag[i] = p < lag1 ? p : -1;
+            int p;
+            if (!ex) {
+                p = lag0 + lb * BT + i;
+                p = p < lag1 ? p : -1;
+            } else {
+                const int e = (lb - nlag) * BT + i;
+                p = e < nx ? selu[xe0 + e] : -1;
+                p = p < N ? p : -1;
+            }
+            sLag[i] = p;
         }
         __syncthreads();
         stage_rows<D>(sPK, LD, BT, [&](int r) -> const uint16_t * {
             const int p = sLag[r];
-            return p >= 0 ? P.phk + (krow0 + p) * D : nullptr;
+            if (p < 0) return nullptr;
+            return ex ? P.phkk + ((size_t)unit * KP + xe0 + (lb - nlag) * BT + r) * D : P.phk + (krow0 + p) * D;
         });
         stage_rows<D>(sVL, LD, BT, [&](int r) -> const uint16_t * {
             const int p = sLag[r];
@@ -582,8 +617,13 @@ __global__ void __launch_bounds__(BQ8_THREADS, 1) query_kernel(BwdArgs P)
         });
         __syncthreads();
     };
-    for (int lb = 0; lb < nlag; ++lb) {
+    auto lin_key = [&](int r, int p, bool ex) -> bool {
+        const int t = tr[r];
+        return p >= 0 && t < N && p <= t - W && (!ex || p >= tcs[r]);
+    };
+    for (int lb = 0; lb < nlag + nxb; ++lb) {
         stage_lag(lb);
+        const bool ex = lb >= nlag;
         float a[4][4];
         zero(a);
         mma_tile<KC, 4, false>(a, pa, sPK, LD, 0, 0);
@@ -594,7 +634,7 @@ __global__ void __launch_bounds__(BQ8_THREADS, 1) query_kernel(BwdArgs P)
                 const int p = sLag[nt * 8 + 2 * tig + e];
 #pragma unroll
                 for (int r = 0; r < 2; ++r) {
-                    const bool in = p >= 0 && p <= tr[r] - W && tr[r] < N;
+                    const bool in = lin_key(r, p, ex);
                     const float x = in ? a[nt][2 * r + e] : 0.f;
                     a[nt][2 * r + e] = x;
                     dlin[r] += x;
@@ -703,7 +743,7 @@ __global__ void __launch_bounds__(BQ8_THREADS, 1) query_kernel(BwdArgs P)
                     const int p = pos[nt * 8 + 2 * tig + e];
 #pragma unroll
                     for (int r = 0; r < 2; ++r) {
-                        const float pe = in_sa(tr[r], p, kb) ? exp2_mufu(fmaf(s[nt][2 * r + e], scale_l2, -cl2[r])) : 0.f;
+                        const float pe = in_sa(r, p, kb) ? exp2_mufu(fmaf(s[nt][2 * r + e], scale_l2, -cl2[r])) : 0.f;
                         const float ds = pe * (dp[nt][2 * r + e] * inv[r] - delta[r]);
                         s[nt][2 * r + e] = ds;
                         dss[r] += ds;
@@ -741,8 +781,9 @@ __global__ void __launch_bounds__(BQ8_THREADS, 1) query_kernel(BwdArgs P)
                 dph[nt][e] = dph[nt][e] * inv[0] - delta[0] * z;
                 dph[nt][2 + e] = dph[nt][2 + e] * inv[1] - delta[1] * z;
             }
-        for (int lb = 0; lb < nlag; ++lb) {
+        for (int lb = 0; lb < nlag + nxb; ++lb) {
             stage_lag(lb);
+            const bool ex = lb >= nlag;
             float da[4][4];
             zero(da);
             mma_tile<KC, 4, false>(da, ya, sVL, LD, 0, 0);
@@ -753,7 +794,7 @@ __global__ void __launch_bounds__(BQ8_THREADS, 1) query_kernel(BwdArgs P)
                     const int p = sLag[nt * 8 + 2 * tig + e];
 #pragma unroll
                     for (int r = 0; r < 2; ++r) {
-                        const bool in = p >= 0 && p <= tr[r] - W && tr[r] < N;
+                        const bool in = lin_key(r, p, ex);
                         da[nt][2 * r + e] = in ? da[nt][2 * r + e] * inv[r] - delta[r] : 0.f;
                     }
                 }
@@ -1040,7 +1081,7 @@ __global__ void __launch_bounds__(BQ8_THREADS, 1) key_kernel(BwdArgs P)
     stage_f32(sR, LD, P.Rs + rslot * D * D, D, D);
     for (int f = threadIdx.x; f < D; f += blockDim.x) sRV[f] = P.rs[rslot * D + f];
     __syncthreads();
-    const bool kk[2] = {kr[0] < N && P.kept[krow0 + kr[0]] != 0, kr[1] < N && P.kept[krow0 + kr[1]] != 0};
+    const bool kk[2] = {kr[0] < N && P.kslot[krow0 + kr[0]] >= 0, kr[1] < N && P.kslot[krow0 + kr[1]] >= 0};
     float dph[NT][4];
     zero(dph);
     {
@@ -1236,7 +1277,7 @@ __global__ void __launch_bounds__(BQ8_THREADS, 1) kept_kernel(BwdArgs P)
                     [&](int i, const uint16_t *sQ, const uint16_t *sG, const uint16_t *, QRows R) {
                         if (tq_lo + (i % per) * BT + BT - 1 < wfirst) return;
                         kv_block<D>(sK, sV, key0, kpos, sQ, sG, R, P.scale, dK, dV,
-                                    [&](int t, int p) { return p <= t - W; });   // W >= C: an earlier chunk
+                                    [&](int t, int p) { return p <= t - W && (W >= C || p / C < t / C); });
                     });
     const int kp[2] = {kpos[key0 + gid], kpos[key0 + gid + 8]};
 #pragma unroll
@@ -1250,6 +1291,157 @@ __global__ void __launch_bounds__(BQ8_THREADS, 1) kept_kernel(BwdArgs P)
                 atomicAdd(dk + col + 1, dK[nt][2 * r + 1] * P.scale);
                 atomicAdd(dv + col, dV[nt][2 * r]);
                 atomicAdd(dv + col + 1, dV[nt][2 * r + 1]);
+            }
+        }
+}
+
+// When W < C a kept key is a linear key of the later queries of its own chunk
+// (t >= j + W, t in chunk(j)) until the chunk completes.  CTA = one chunk c of one
+// (sequence, kv head): its kept entries (warp w: entries [16w, 16w + 16)) against
+// the queries [cC + W, (c + 1)C): dphi(k) = sum phi(q) (g.v - delta) and
+// dv += sum (phi(q).phi(k)) g, then the NP-Map backward of those keys; dk, dv
+// by atomic additions, dl of their rows written for the dWf pass.
+template <int D, int G>
+__global__ void __launch_bounds__(BQ8_THREADS, 1) kept_lin_kernel(BwdArgs P)
+{
+    grid_dep_sync();
+    constexpr int LD = D + 8, KC = D / 16, NT = D / 8;
+    using L = KLayout<D>;
+    extern __shared__ __align__(16) uint8_t smem[];
+    uint16_t *sK = (uint16_t *)(smem + L::K), *sV = (uint16_t *)(smem + L::V), *sPK = (uint16_t *)(smem + L::PK);
+    uint16_t *sR = (uint16_t *)(smem + L::R);
+    int *kpos = (int *)(smem + L::KPOS);
+
+    const Dims &dm = P.dm;
+    const int N = dm.N, W = dm.W, C = dm.C, lam = dm.lam;
+    const int KP = dm.T_max * lam;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gid = lane >> 2, tig = lane & 3;
+    const int c = blockIdx.x, unit = blockIdx.y, b = unit / dm.Hkv, gq = unit % dm.Hkv;
+    const size_t krow0 = (size_t)unit * N;
+    const int key0 = warp * 16;
+    const int e0 = c * lam;
+    const int tq_lo = c * C + W, tq_hi = min((c + 1) * C, N);
+    if (tq_lo >= tq_hi) return;
+    for (int i = threadIdx.x; i < BK_KEYS; i += blockDim.x) {
+        int p = i < lam ? P.sel[(size_t)unit * KP + e0 + i] : -1;
+        kpos[i] = p >= 0 && p < N ? p : -1;
+    }
+    __syncthreads();
+    stage_rows<D>(sK, LD, BK_KEYS, [&](int r) -> const uint16_t * { return kpos[r] >= 0 ? P.k + (krow0 + kpos[r]) * D : nullptr; });
+    stage_rows<D>(sV, LD, BK_KEYS, [&](int r) -> const uint16_t * { return kpos[r] >= 0 ? P.v + (krow0 + kpos[r]) * D : nullptr; });
+    stage_rows<D>(sPK, LD, BK_KEYS, [&](int r) -> const uint16_t * {
+        return kpos[r] >= 0 ? P.phkk + ((size_t)unit * KP + e0 + r) * D : nullptr;
+    });
+    __syncthreads();
+    const bool active = key0 < lam;
+    const int kr[2] = {kpos[key0 + gid], kpos[key0 + gid + 8]};
+
+    float dph[NT][4], dV[NT][4];
+    zero(dph);
+    zero(dV);
+    const int per = (tq_hi - tq_lo + BT - 1) / BT;
+    query_blocks<D>(P, b, G * per, true, smem,
+                    [&](int i, int &h, int &tq0, int &tq1) {
+                        h = gq * G + i / per;
+                        tq0 = tq_lo + (i % per) * BT;
+                        tq1 = tq_hi;
+                    },
+                    [&](int, const uint16_t *, const uint16_t *sG, const uint16_t *sPQ, QRows R) {
+                        if (!active) return;
+                        float dat[4][4], at[4][4];
+                        zero(dat);
+                        zero(at);
+#pragma unroll
+                        for (int kc = 0; kc < KC; ++kc) {
+                            uint32_t va[4], pk[4];
+                            load_a(sV, LD, key0, kc * 16, va);
+                            load_a(sPK, LD, key0, kc * 16, pk);
+#pragma unroll
+                            for (int nt = 0; nt < 4; nt += 2) {
+                                uint32_t f[4];
+                                load_b(sG, LD, nt * 8, kc * 16, f);
+                                mma(dat[nt], va, f[0], f[1]);
+                                mma(dat[nt + 1], va, f[2], f[3]);
+                                load_b(sPQ, LD, nt * 8, kc * 16, f);
+                                mma(at[nt], pk, f[0], f[1]);
+                                mma(at[nt + 1], pk, f[2], f[3]);
+                            }
+                        }
+#pragma unroll
+                        for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+                            for (int e = 0; e < 2; ++e) {
+                                const int qi = nt * 8 + 2 * tig + e;
+                                const int t = R.tok[qi];
+#pragma unroll
+                                for (int r = 0; r < 2; ++r) {
+                                    const bool in = t >= 0 && kr[r] >= 0 && t >= kr[r] + W;
+                                    dat[nt][2 * r + e] = in ? dat[nt][2 * r + e] * R.inv[qi] - R.delta[qi] : 0.f;
+                                    at[nt][2 * r + e] = in ? at[nt][2 * r + e] * R.inv[qi] : 0.f;
+                                }
+                            }
+                        uint32_t df[2][4], af[2][4];
+                        acc_to_a<4>(dat, df);
+                        acc_to_a<4>(at, af);
+                        mma_tile<2, NT, true>(dph, df, sPQ, LD, 0, 0);
+                        mma_tile<2, NT, true>(dV, af, sG, LD, 0, 0);
+                    });
+
+    // ---- NP-Map backward of these keys' rows (Wf in shared memory)
+    __syncthreads();
+    for (int i = threadIdx.x; i < D * D / 4; i += blockDim.x) {
+        const int r = i / (D / 4), cc = (i % (D / 4)) * 4;
+        const float4 x = __ldg(reinterpret_cast<const float4 *>(P.Wf) + i);
+        *reinterpret_cast<uint2 *>(sR + r * LD + cc) = make_uint2(pack(x.x, x.y), pack(x.z, x.w));
+    }
+    __syncthreads();
+    if (!active) return;
+    float ph[NT][4], xk[NT][4];
+    float an[2];
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+        const int row = key0 + gid + 8 * r;
+        float a = 0.f, x2 = 0.f;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int col = nt * 8 + 2 * tig + e;
+                ph[nt][2 * r + e] = kr[r] >= 0 ? P.phkk32[((size_t)unit * KP + e0 + row) * D + col] : 0.f;
+                xk[nt][2 * r + e] = bf2f(sK[row * LD + col]);
+                a = fmaf(dph[nt][2 * r + e], ph[nt][2 * r + e], a);
+                x2 = fmaf(xk[nt][2 * r + e], xk[nt][2 * r + e], x2);
+            }
+        const float nk = sqrtf(quad_sum(x2));
+        const float ik = nk > 0.f ? 1.f / nk : 0.f;
+        an[r] = quad_sum(a) * ik * ik;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int e = 0; e < 2; ++e)
+                dph[nt][2 * r + e] = ph[nt][2 * r + e] * (dph[nt][2 * r + e] - an[r] * ph[nt][2 * r + e]);
+    }
+    float dkn[NT][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) dkn[nt][i] = an[i >> 1] * xk[nt][i];
+    uint32_t lf[KC][4];
+    acc_to_a<NT>(dph, lf);
+    mma_tile<KC, NT, false>(dkn, lf, sR, LD, 0, 0);   // dl Wf^T: B(k = f, n = i) = Wf[i][f]
+#pragma unroll
+    for (int r = 0; r < 2; ++r)
+        if (kr[r] >= 0) {
+            float *dk = P.dk + (krow0 + kr[r]) * D, *dv = P.dv + (krow0 + kr[r]) * D;
+            float *dl = P.dlk + (krow0 + kr[r]) * D;
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                const int col = nt * 8 + 2 * tig;
+                atomicAdd(dk + col, dkn[nt][2 * r]);
+                atomicAdd(dk + col + 1, dkn[nt][2 * r + 1]);
+                atomicAdd(dv + col, dV[nt][2 * r]);
+                atomicAdd(dv + col + 1, dV[nt][2 * r + 1]);
+                *reinterpret_cast<float2 *>(dl + col) = make_float2(dph[nt][2 * r], dph[nt][2 * r + 1]);
             }
         }
 }
@@ -1321,7 +1513,9 @@ __global__ void __launch_bounds__(256) dwf_kernel(const uint16_t *__restrict__ x
 }
 
 struct BwdBuffers {
-    uint8_t *kept;
+    int32_t *kslot;
+    uint16_t *phkk;
+    float *phkk32;
     uint16_t *phk;
     float *phk32;
     float *Sp, *zp, *Rs, *rs;
@@ -1346,12 +1540,13 @@ cudaError_t run(const BwdArgs &A, const BwdBuffers &bb, cudaStream_t s)
     };
     {
         KTimer tm("bwd_prep", s);
-        chk(cudaMemsetAsync(bb.kept, 0, (size_t)units * dm.N, s));
-        if (KP > 0) chk(launch_kernel(mark_kept_kernel, dim3((KP + 255) / 256, units), dim3(256), 0, s, A.sel, KP, dm.N, bb.kept));
+        chk(cudaMemsetAsync(bb.kslot, 0xff, (size_t)units * dm.N * 4, s));
+        if (KP > 0) chk(launch_kernel(mark_kept_kernel, dim3((KP + 255) / 256, units), dim3(256), 0, s, A.sel, KP, dm.N, bb.kslot));
         const long long rows = (long long)units * dm.N;
         const size_t sm = 2 * (size_t)D * (D + 8) * 2;
         chk(set_smem(phik_mma_kernel<D>, sm));
-        chk(launch_kernel(phik_mma_kernel<D>, dim3((unsigned)((rows + 127) / 128)), dim3(256), sm, s, A, bb.phk, bb.phk32));
+        chk(launch_kernel(phik_mma_kernel<D>, dim3((unsigned)((rows + 127) / 128)), dim3(256), sm, s, A, bb.phk, bb.phk32,
+                          bb.phkk, bb.phkk32));
     }
     const size_t bs_smem = BSLayout<D, D>::TOTAL;
     const int nel_s = D * D, nel_z = D;
@@ -1388,6 +1583,11 @@ cudaError_t run(const BwdArgs &A, const BwdBuffers &bb, cudaStream_t s)
         chk(launch_kernel(kept_kernel<D, G>, dim3((KP + BK_KEYS - 1) / BK_KEYS, units, nsplit), dim3(BQ8_THREADS),
                           KLayout<D>::TOTAL, s, A));
     }
+    if (KP > 0 && dm.W < dm.C) {
+        KTimer tm("bwd_kept_lin", s);
+        chk(set_smem(kept_lin_kernel<D, G>, KLayout<D>::TOTAL));
+        chk(launch_kernel(kept_lin_kernel<D, G>, dim3(dm.T_max, units), dim3(BQ8_THREADS), KLayout<D>::TOTAL, s, A));
+    }
     {
         KTimer tm("bwd_dwf", s);
         chk(cudaMemsetAsync(A.dWf, 0, (size_t)D * D * 4, s));
@@ -1408,7 +1608,10 @@ BwdLayout bwd_layout(const Dims &dm)
     const size_t units = (size_t)dm.B * dm.Hkv, rows_q = (size_t)dm.B * dm.Hq * dm.N, rows_k = units * dm.N;
     const int nblk = (dm.N + BT - 1) / BT;
     size_t o = 0;
-    L.kept = o; o += al(rows_k);
+    const size_t KPs = (size_t)dm.T_max * dm.lam > 0 ? (size_t)dm.T_max * dm.lam : 1;
+    L.kslot = o; o += al(rows_k * 4);
+    L.phkk = o; o += al(units * KPs * dm.df * 2);
+    L.phkk32 = o; o += al(units * KPs * dm.df * 4);
     L.phk = o; o += al(rows_k * dm.df * 2);
     L.Sp = o; o += al(units * (nblk + 1) * (size_t)dm.df * dm.d * 4);
     L.zp = o; o += al(units * (nblk + 1) * (size_t)dm.df * 4);
@@ -1431,7 +1634,9 @@ BwdLayout bwd_layout(const Dims &dm)
 
 bool backward_supported(const Dims &dm)
 {
-    return dm.d == dm.df && (dm.d == 64 || dm.d == 128) && (dm.G == 1 || dm.G == 2 || dm.G == 4) && dm.W >= dm.C;
+    // lambda <= 128: the kept entries of a chunk fit the eight warps of the own-chunk pass
+    return dm.d == dm.df && (dm.d == 64 || dm.d == 128) && (dm.G == 1 || dm.G == 2 || dm.G == 4) &&
+           (dm.W >= dm.C || dm.lam <= BK_KEYS);
 }
 
 cudaError_t launch_backward(const Dims &dm, const BwdInputs &in, void *ws)
@@ -1444,10 +1649,14 @@ cudaError_t launch_backward(const Dims &dm, const BwdInputs &in, void *ws)
     A.scale = 1.f / sqrtf((float)dm.d);
     A.q = in.q; A.k = in.k; A.v = in.v; A.dy = in.dy; A.Wf = in.Wf; A.sel = in.sel;
     BwdBuffers bb;
-    bb.kept = (uint8_t *)(base + L.kept);
+    bb.kslot = (int32_t *)(base + L.kslot);
+    bb.phkk = (uint16_t *)(base + L.phkk);
+    bb.phkk32 = (float *)(base + L.phkk32);
     bb.Sp = (float *)(base + L.Sp); bb.zp = (float *)(base + L.zp);
     bb.Rs = (float *)(base + L.Rs); bb.rs = (float *)(base + L.rs);
-    A.kept = bb.kept;
+    A.kslot = bb.kslot;
+    A.phkk = bb.phkk;
+    A.phkk32 = bb.phkk32;
     bb.phk = (uint16_t *)(base + L.phk);
     A.phk = bb.phk;
     A.Sp = bb.Sp; A.zp = bb.zp; A.Rs = bb.Rs; A.rs = bb.rs;

@@ -249,7 +249,7 @@ struct BwdInputs {
 };
 // byte offsets of the backward pass's workspace pieces
 struct BwdLayout {
-    size_t kept, phk, Sp, zp, Rs, rs, g, phq, phq32, phk32, dlq, dlk, rc, rinv, rdelta, rds, rjs, total;
+    size_t kslot, phkk, phkk32, phk, Sp, zp, Rs, rs, g, phq, phq32, phk32, dlq, dlk, rc, rinv, rdelta, rds, rjs, total;
 };
 BwdLayout bwd_layout(const Dims &dm);
 bool backward_supported(const Dims &dm);

@@ -96,7 +96,9 @@ def test_backward_argument_errors(lib):
     assert lib.still_backward_workspace_size(ct.byref(tr), 64, 64, 32, 16) == 0          # m < W
     args = lambda sh, W, C, q, dWf: (ct.byref(sh), q, p, p, p, W, C, 288, 16, p, p, p, p, p, dWf, None, None, 0,
                                      None)
-    assert lib.still_backward(*args(tr, 64, 256, p, p)) == 2          # W < C: not covered
+    tr_big = Shape(1, 32, 8, 1024, 128, 128)
+    assert lib.still_backward(ct.byref(tr_big), p, p, p, p, 64, 256, 64 + 16 * 129, 16, p, p, p, p, p, p, None, None,
+                              0, None) == 2                           # W < C with lambda > 128
     assert lib.still_backward(*args(Shape(1, 24, 3, 64, 128, 128), 64, 64, p, p)) == 2   # G = 8
     assert lib.still_backward(*args(Shape(1, 8, 2, 64, 128, 64), 64, 64, p, p)) == 2     # d != d_f
     assert lib.still_backward(*args(tr, 64, 64, None, p)) == 1        # null q

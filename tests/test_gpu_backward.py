@@ -111,6 +111,11 @@ CASES = [
     ("g2_d64_w48_c32", Workload("g2_d64_w48_c32", 1, 4, 2, 64, 200, 48, 32, 48 + 3 * 7, 7, 64)),
     ("g1_d128_lam0", Workload("g1_d128_lam0", 1, 2, 2, 128, 150, 32, 32, 32, 4, 128)),
     ("g4_d64_w_ge_n", Workload("g4_d64_w_ge_n", 1, 4, 1, 64, 90, 128, 64, 128 + 4, 2, 64)),
+    # W < C: kept keys stay linear keys of their own chunk's later queries
+    ("g4_d64_w16_c32", Workload("g4_d64_w16_c32", 1, 8, 2, 64, 300, 16, 32, 16 + 4 * 9, 9, 64)),
+    ("g2_d128_w24_c64_ragged", Workload("g2_d128_w24_c64_ragged", 2, 4, 2, 128, 333, 24, 64, 24 + 6 * 5, 5, 128)),
+    ("g1_d64_w8_c48", Workload("g1_d64_w8_c48", 1, 2, 2, 64, 200, 8, 48, 8 + 20 * 4, 4, 64)),
+    ("llama32_1b_shape_n1024", Workload("llama32_1b_shape_n1024", 1, 32, 8, 64, 1024, 64, 256, 288, 16, 64)),
 ]
 
 
@@ -132,8 +137,8 @@ def test_backward_training_workload(still):
 
 
 def test_backward_refuses_what_it_does_not_cover(still):
-    w = inputs.WORKLOADS["llama32_1b_layer_prefill_4k"]   # W < C
-    q, k, v, Wf = (t.to(DEV) for t in inputs.make_inputs(w, seed=0, N=128))
+    w = Workload("g8", 1, 16, 2, 64, 128, 64, 64, 128, 8, 64)   # G = 8
+    q, k, v, Wf = (t.to(DEV) for t in inputs.make_inputs(w, seed=0))
     sel = torch.full((1, w.Hkv, w.T_max, w.lam), -1, dtype=torch.int32, device=DEV)
     dy = torch.zeros_like(q)
     with pytest.raises(still.StillError) as ei:
