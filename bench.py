@@ -521,6 +521,8 @@ def run_ours(args):
     # -------- the other prefill workloads --------
     if not args.no_backward and rank == 0:
         line["backward"] = bench_backward(still, dev, stream, pk, pk_kind, args.seed + 13, cpu=not args.no_cpu)
+        line["backward_llama32_1b_layer_prefill_4k"] = bench_backward(
+            still, dev, stream, pk, pk_kind, args.seed + 14, cpu=not args.no_cpu, name="llama32_1b_layer_prefill_4k")
     if not args.no_workloads and rank == 0:
         line["workloads"] = {nm: bench_workload(still, nm, dev, stream, pk, pk_kind, args.seed + 11,
                                                 cpu=not args.no_cpu)
@@ -694,9 +696,9 @@ def backward_algorithmic(w, sel_idx):
     return {"flops": F_soft + F_lin + F_np, "F_softmax": F_soft, "F_linear": F_lin, "F_npmap": F_np, "bytes": by}
 
 
-def bench_backward(still, dev, stream, pk, pk_kind, seed, steps=20, cpu=True):
-    """The backward pass (still_backward, routing held fixed) of the
-    training-shaped batch: `steps` timed calls after 3 warm-up ones, L2 flushed
+def bench_backward(still, dev, stream, pk, pk_kind, seed, steps=20, cpu=True, name=BACKWARD_WORKLOAD):
+    """The backward pass (still_backward, routing held fixed) of a workload (the
+    training-shaped batch by default): `steps` timed calls after 3 warm-up ones, L2 flushed
     before each (CUDA events around every call), the step against its roofline,
     its kernels' times from the library's event timers, and -- unless cpu is
     False -- the gradient oracle on one sequence of the batch on the host
@@ -705,7 +707,7 @@ def bench_backward(still, dev, stream, pk, pk_kind, seed, steps=20, cpu=True):
     import torch
     from linear_attention_linearization_gb300 import inputs
     from linear_attention_linearization_gb300.inputs import to_f64
-    w = inputs.WORKLOADS[BACKWARD_WORKLOAD]
+    w = inputs.WORKLOADS[name]
     q, k, v, Wf = inputs.make_inputs(w, seed=seed, device=dev)
     dy = inputs.make_dout(w, seed=seed, device=dev)
     _, sel = still.prefill(q, k, v, Wf, w.W, w.C, w.m, w.T_max, stream=stream)
@@ -751,7 +753,7 @@ def bench_backward(still, dev, stream, pk, pk_kind, seed, steps=20, cpu=True):
                         "frac": max(t_flop, t_hbm) * 1e3 / ms, "peak_source": pk_kind,
                         "split": {k2: alg[k2] for k2 in ("F_softmax", "F_linear", "F_npmap")}},
            "kernels": {k2: {"launches": n, "ms_per_launch": m / n} for k2, (n, m) in kt.items()},
-           "gpu_launches_per_step": 10}
+           "gpu_launches_per_step": 10 + (1 if w.W < w.C else 0)}
     if cpu:
         from oracle import grad
         torch_threads = torch.get_num_threads()

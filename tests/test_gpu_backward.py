@@ -136,6 +136,15 @@ def test_backward_training_workload(still):
     assert np.isfinite(grads[3].cpu().numpy()).all()
 
 
+def test_backward_1b_layer_4k(still):
+    # the Llama-3.2-1B-shaped layer at 4K (W = 64 < C = 256, lambda = 14): every element of
+    # dq, dk, dv and dWf against the oracle
+    w = inputs.WORKLOADS["llama32_1b_layer_prefill_4k"]
+    host, sel, cidx, grads, names = gpu_backward(still, w, seed=4, timers=True)
+    assert "bwd_kept_lin" in names, names
+    check_against_oracle("llama32_1b_layer_prefill_4k", w, host, sel, cidx, grads)
+
+
 def test_backward_refuses_what_it_does_not_cover(still):
     w = Workload("g8", 1, 16, 2, 64, 128, 64, 64, 128, 8, 64)   # G = 8
     q, k, v, Wf = (t.to(DEV) for t in inputs.make_inputs(w, seed=0))
