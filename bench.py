@@ -757,23 +757,33 @@ def bench_backward(still, dev, stream, pk, pk_kind, seed, steps=20, cpu=True, na
     if cpu:
         from oracle import grad
         torch_threads = torch.get_num_threads()
-        hq, hk, hv, hW, hdy = (to_f64(t[:1]) if t.dim() == 4 else to_f64(t) for t in (q, k, v, Wf, dy))
+        # the sample: sequence 0 and its first two kv heads (with their query heads); the kv
+        # heads are independent units, so the tokens/s of the sample scales to the batch
+        nkv = min(2, w.Hkv)
+        nq = nkv * (w.Hq // w.Hkv)
+        hq, hdy = (to_f64(t[:1, :nq]) for t in (q, dy))
+        hk, hv = (to_f64(t[:1, :nkv]) for t in (k, v))
+        hW = to_f64(Wf)
         cidx = torch.empty((w.B, w.Hq, w.N), dtype=torch.int32, device=dev)
         still.backward(q, k, v, Wf, w.W, w.C, w.m, w.T_max, sel, dy, grads=grads, cmax_idx=cidx, workspace=ws,
                        stream=stream)
         torch.cuda.synchronize(dev)
+        sel_s = sel_h[:1, :nkv]
         t0 = time.perf_counter()
-        _, dq_r, dk_r, dv_r, _, c_r = grad.layer_grad(hq, hk, hv, hW, w.W, w.C, sel_h[:1], hdy)
+        _, dq_r, dk_r, dv_r, _, c_r = grad.layer_grad(hq, hk, hv, hW, w.W, w.C, sel_s, hdy)
         sec = time.perf_counter() - t0
-        c_g = cidx[:1].cpu().numpy().astype(np.int64)
+        c_g = cidx[:1, :nq].cpu().numpy().astype(np.int64)
         moved = int((c_g != c_r).sum())
         if moved:   # near-equal row maxima: the oracle takes the GPU's choice of the key that holds c
-            _, dq_r, dk_r, dv_r, _, _ = grad.layer_grad(hq, hk, hv, hW, w.W, w.C, sel_h[:1], hdy, cidx=c_g)
-        res["cpu_baseline"] = {"value": w.N / sec, "unit": "tokens/s", "cores": torch_threads, "kind": "oracle",
-                               "sample": f"the gradient oracle (fp64) on sequence 0 of the {w.B} ({w.N} tokens, "
-                                         f"{w.Hq} heads), {sec:.2f} s"}
+            _, dq_r, dk_r, dv_r, _, _ = grad.layer_grad(hq, hk, hv, hW, w.W, w.C, sel_s, hdy, cidx=c_g)
+        res["cpu_baseline"] = {"value": w.N * nkv / w.Hkv / sec, "unit": "tokens/s", "cores": torch_threads,
+                               "kind": "oracle",
+                               "sample": f"the gradient oracle (fp64) on sequence 0, kv heads 0..{nkv - 1} of "
+                                         f"{w.Hkv} ({nq} query heads, {w.N} tokens): {sec:.2f} s, scaled to all "
+                                         f"kv heads"}
         par = {}
-        for nm, g_gpu, g_ref in (("dq", grads[0][:1], dq_r), ("dk", grads[1][:1], dk_r), ("dv", grads[2][:1], dv_r)):
+        for nm, g_gpu, g_ref in (("dq", grads[0][:1, :nq], dq_r), ("dk", grads[1][:1, :nkv], dk_r),
+                                 ("dv", grads[2][:1, :nkv], dv_r)):
             par[f"{nm}_err_rel"] = float(np.abs(g_gpu.cpu().double().numpy() - g_ref).max() / np.abs(g_ref).max())
         par["rows_row_max_differs"] = moved
         par["tolerance"] = "max|g_gpu - g_ref| <= 1e-2 max|g_ref| per tensor"
