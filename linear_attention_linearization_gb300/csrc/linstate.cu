@@ -26,12 +26,12 @@ __global__ void scan_kernel(float *__restrict__ dS, float *__restrict__ dz, int 
         return;
     }
     float run = 0.f;
-    for (int s0 = 0; s0 < nseg; s0 += 16) {
-        float x[16];
+    for (int s0 = 0; s0 < nseg; s0 += 32) {
+        float x[32];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) x[i] = s0 + i < nseg ? p[(size_t)(s0 + i) * stride] : 0.f;
+        for (int i = 0; i < 32; ++i) x[i] = s0 + i < nseg ? p[(size_t)(s0 + i) * stride] : 0.f;
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
+        for (int i = 0; i < 32; ++i) {
             if (s0 + i < nseg) p[(size_t)(s0 + i) * stride] = run;
             run += x[i];
         }
