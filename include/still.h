@@ -219,14 +219,30 @@ still_status still_prefill_routed(const still_shape *shape, const still_bf16 *q,
  * of query head h at token t (the linear part of y includes the own-chunk and
  * lagged linear keys, gated alike).  A gate of +inf everywhere gives
  * still_prefill's layer.  Everything else -- routing, selection, workspace
- * (still_prefill_workspace_size bytes, or NULL) -- is as for still_prefill.
- * No decode state is exported: the decode step of the gated layer is not
- * provided.
+ * (still_prefill_workspace_size bytes, or NULL) and the optional export of the
+ * decode state -- is as for still_prefill.  The gate scales the output only:
+ * the exported state is the ungated layer's, and still_decode_step_gated
+ * continues the gated layer from it.
  */
 still_status still_prefill_gated(const still_shape *shape, const still_bf16 *q, const still_bf16 *k,
                                  const still_bf16 *v, const still_bf16 *gate, const float *Wf, int W, int C, int m,
                                  int T_max, still_bf16 *out, int32_t *sel_idx, void *workspace,
-                                 size_t workspace_bytes, still_stream_t stream);
+                                 size_t workspace_bytes, const still_decode_state *export_state,
+                                 still_stream_t stream);
+
+/*
+ * The decode step of the gated layer: still_decode_step with the gate
+ * pre-activations of this step, gate_t bf16 [B,Hq,d] (the layout of q_t),
+ *   y_t = (sum_SA e^{s-c} v + sigmoid(gate_t) * (phi(q)^T S + the linear keys' terms))
+ *         / (sum_SA e^{s-c} + phi(q)^T z + the linear keys' weights).
+ * Everything else is as for still_decode_step.  Only the staged decode kernel
+ * carries the gate: states whose cache does not fit it (still_decode_step's
+ * general path) return STILL_ERR_UNSUPPORTED.
+ */
+still_status still_decode_step_gated(const still_shape *shape, const still_decode_state *state, const still_bf16 *q_t,
+                                     const still_bf16 *k_t, const still_bf16 *v_t, const still_bf16 *gate_t,
+                                     const float *Wf, int W, int C, int m, int T_max, still_bf16 *out_t,
+                                     still_stream_t stream);
 
 /*
  * Backward pass of the layer (still_prefill's forward, ungated) with the

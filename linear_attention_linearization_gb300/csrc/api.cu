@@ -382,11 +382,12 @@ still_status still_prefill_routed(const still_shape *shape, const still_bf16 *q,
 still_status still_prefill_gated(const still_shape *shape, const still_bf16 *q, const still_bf16 *k,
                                  const still_bf16 *v, const still_bf16 *gate, const float *Wf, int W, int C, int m,
                                  int T_max, still_bf16 *out, int32_t *sel_idx, void *workspace,
-                                 size_t workspace_bytes, still_stream_t stream)
+                                 size_t workspace_bytes, const still_decode_state *export_state,
+                                 still_stream_t stream)
 {
     if (shape && shape->N > 0 && (!gate || !aligned16(gate))) return STILL_ERR_INVALID_ARG;
     return prefill_impl(shape, q, k, v, Wf, W, C, m, T_max, STILL_METRIC_SELF_SALIENCY, 0, out, sel_idx, workspace,
-                        workspace_bytes, nullptr, stream, gate);
+                        workspace_bytes, export_state, stream, gate);
 }
 
 size_t still_backward_workspace_size(const still_shape *shape, int W, int C, int m, int T_max)
@@ -488,6 +489,25 @@ still_status still_decode_step(const still_shape *shape, const still_decode_stat
     if (dm.G > 8) return STILL_ERR_UNSUPPORTED;
     if (decode_smem_bytes(dm) > 200 * 1024) return STILL_ERR_UNSUPPORTED;
     return cuda_status(launch_decode(dm, *state, q_t, k_t, v_t, Wf, out_t, (cudaStream_t)stream));
+}
+
+still_status still_decode_step_gated(const still_shape *shape, const still_decode_state *state, const still_bf16 *q_t,
+                                     const still_bf16 *k_t, const still_bf16 *v_t, const still_bf16 *gate_t,
+                                     const float *Wf, int W, int C, int m, int T_max, still_bf16 *out_t,
+                                     still_stream_t stream)
+{
+    if (!shape) return STILL_ERR_INVALID_ARG;
+    still_shape sh = *shape;
+    sh.N = 0;
+    Dims dm;
+    still_status st = make_dims(&sh, W, C, m, T_max, &dm);
+    if (st != STILL_OK) return st;
+    if (!gate_t || !aligned16(gate_t)) return STILL_ERR_INVALID_ARG;
+    if (!state_ok(state, dm.m) || !q_t || !k_t || !v_t || !Wf || !out_t) return STILL_ERR_INVALID_ARG;
+    if (!aligned16(q_t) || !aligned16(k_t) || !aligned16(v_t) || !aligned16(Wf) || !aligned16(out_t))
+        return STILL_ERR_INVALID_ARG;
+    if (dm.G > 8 || !decode_staged(dm, *state)) return STILL_ERR_UNSUPPORTED;
+    return cuda_status(launch_decode(dm, *state, q_t, k_t, v_t, Wf, out_t, (cudaStream_t)stream, gate_t));
 }
 
 still_status still_read_status(const int32_t *status_word, still_stream_t stream, int32_t *host_value)

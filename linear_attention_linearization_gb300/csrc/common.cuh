@@ -233,9 +233,12 @@ cudaError_t launch_hybrid_tc(const Dims &dm, const SegPlan &sp, const TCBuffers 
 cudaError_t launch_export(const Dims &dm, const SegPlan &sp, const uint16_t *k, const uint16_t *v,
                           const float *scores, const int32_t *fsel, const float *dS, const float *dz,
                           const still_decode_state &st, cudaStream_t s);
+// gate_t (nullable): the gated layer's pre-activations [B, Hq, d] of this step
 cudaError_t launch_decode(const Dims &dm, const still_decode_state &st, const uint16_t *q_t,
                           const uint16_t *k_t, const uint16_t *v_t, const float *Wf, uint16_t *out_t,
-                          cudaStream_t s);
+                          cudaStream_t s, const uint16_t *gate_t = nullptr);
+// the decode step runs its staged kernel (the one the gated layer needs) for this state
+bool decode_staged(const Dims &dm, const still_decode_state &st);
 
 
 // ---- backward pass (backward.cu) ----------------------------------------------

@@ -631,7 +631,7 @@ __global__ void __launch_bounds__(DS_THREADS, 2)
     decode_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CUtensorMap mapV,
                   still_decode_state st, const uint16_t *__restrict__ q_t, const uint16_t *__restrict__ k_t,
                   const uint16_t *__restrict__ v_t, const float *__restrict__ Wf, Dims dm, DecodeSmem L,
-                  uint16_t *__restrict__ out_t)
+                  uint16_t *__restrict__ out_t, const uint16_t *__restrict__ gate_t)
 {
     grid_dep_sync();
     using namespace sm100;
@@ -1041,12 +1041,18 @@ __global__ void __launch_bounds__(DS_THREADS, 2)
             }
     }
     __syncthreads();
+    // the parts below RG hold the linear numerator (state readout and linear keys), the
+    // others the softmax one; the gated layer scales the linear numerator by sigmoid(gate)
     for (int i = tid; i < G * D; i += DS_THREADS) {
         const int hh = i / D, c = i % D;
-        float num = 0.f;
-        for (int p2 = 0; p2 < RG + KSPLIT; ++p2) num += red[((size_t)p2 * G + hh) * D + c];
+        const size_t oi = ((size_t)b * dm.Hq + (size_t)g * G + hh) * D + c;
+        float lin = 0.f, sm = 0.f;
+        for (int p2 = 0; p2 < RG; ++p2) lin += red[((size_t)p2 * G + hh) * D + c];
+        for (int p2 = RG; p2 < RG + KSPLIT; ++p2) sm += red[((size_t)p2 * G + hh) * D + c];
+        const float gch = gate_t ? 1.f / (1.f + expf(-bf2f(gate_t[oi]))) : 1.f;
+        const float num = fmaf(gch, lin, sm);
         const float den = s_den[hh];
-        out_t[((size_t)b * dm.Hq + (size_t)g * G + hh) * D + c] = f2bf(den != 0.f ? num / den : 0.f);
+        out_t[oi] = f2bf(den != 0.f ? num / den : 0.f);
     }
 
     // ---- state: the new candidate's slot, then t into the window ring --------------
@@ -1178,11 +1184,12 @@ bool staged_ok(const Dims &dm, const still_decode_state &st)
 }  // namespace
 
 cudaError_t launch_decode(const Dims &dm, const still_decode_state &st, const uint16_t *q_t, const uint16_t *k_t,
-                          const uint16_t *v_t, const float *Wf, uint16_t *out_t, cudaStream_t s)
+                          const uint16_t *v_t, const float *Wf, uint16_t *out_t, cudaStream_t s, const uint16_t *gate_t)
 {
-    KTimer tm("decode_step", s);
+    KTimer tm(gate_t ? "decode_step_gated" : "decode_step", s);
     dim3 grid(dm.Hkv, dm.B);
     cudaError_t e;
+    if (gate_t && !staged_ok(dm, st)) return cudaErrorNotSupported;   // the gate is in the staged kernel only
     if (staged_ok(dm, st)) {
         const DecodeSmem L = decode_smem(dm);
         CUtensorMap mk, mv;
@@ -1203,7 +1210,7 @@ cudaError_t launch_decode(const Dims &dm, const still_decode_state &st, const ui
         }                                                                                                      \
     }                                                                                                          \
     e = launch_kernel(decode_kernel<DD, FF, GG>, grid, dim3(DS_THREADS), L.total, s, mk, mv, st, q_t, k_t, v_t, Wf, dm, \
-                      L, out_t);
+                      L, out_t, gate_t);
 #define STILL_DECODE_G(DD, FF)                                                                                 \
     switch (dm.G) {                                                                                              \
     case 1: STILL_DECODE(DD, FF, 1) break;                                                                       \
@@ -1232,6 +1239,8 @@ cudaError_t launch_decode(const Dims &dm, const still_decode_state &st, const ui
 #undef STILL_DECODE
     return cudaGetLastError();
 }
+
+bool decode_staged(const Dims &dm, const still_decode_state &st) { return staged_ok(dm, st); }
 
 // Shared memory of the variant that runs for these sizes (the general one when
 // the staged plan does not fit); the caller rejects sizes above its limit.

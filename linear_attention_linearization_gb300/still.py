@@ -66,7 +66,10 @@ SIGNATURES = {
                                         ct.c_void_p, ct.c_void_p, ct.c_void_p, ct.c_size_t, ct.c_void_p]),
     "still_prefill_gated": (ct.c_int, [ct.POINTER(Shape), ct.c_void_p, ct.c_void_p, ct.c_void_p, ct.c_void_p,
                                        ct.c_void_p, ct.c_int, ct.c_int, ct.c_int, ct.c_int, ct.c_void_p,
-                                       ct.c_void_p, ct.c_void_p, ct.c_size_t, ct.c_void_p]),
+                                       ct.c_void_p, ct.c_void_p, ct.c_size_t, ct.POINTER(DecodeStateC), ct.c_void_p]),
+    "still_decode_step_gated": (ct.c_int, [ct.POINTER(Shape), ct.POINTER(DecodeStateC), ct.c_void_p, ct.c_void_p,
+                                           ct.c_void_p, ct.c_void_p, ct.c_void_p, ct.c_int, ct.c_int, ct.c_int,
+                                           ct.c_int, ct.c_void_p, ct.c_void_p]),
     "still_backward_workspace_size": (ct.c_size_t, [ct.POINTER(Shape), ct.c_int, ct.c_int, ct.c_int, ct.c_int]),
     "still_backward": (ct.c_int, [ct.POINTER(Shape), ct.c_void_p, ct.c_void_p, ct.c_void_p, ct.c_void_p,
                                   ct.c_int, ct.c_int, ct.c_int, ct.c_int, ct.c_void_p, ct.c_void_p,
@@ -273,9 +276,12 @@ def prefill_routed(q, k, v, Wf, W, C, m, T_max, metric, seed=0, out=None, sel_id
     return out, sel_idx
 
 
-def prefill_gated(q, k, v, gate, Wf, W, C, m, T_max, out=None, sel_idx=None, workspace=None, stream=None):
+def prefill_gated(q, k, v, gate, Wf, W, C, m, T_max, out=None, sel_idx=None, workspace=None, export_state=None,
+                  stream=None):
     """The layer with a per-channel sigmoid gate on the linear branch's numerator:
-    gate [B,Hq,N,d] bf16 holds the pre-activations (see still_prefill_gated)."""
+    gate [B,Hq,N,d] bf16 holds the pre-activations (see still_prefill_gated).
+    export_state (optional DecodeState) receives the state still_decode_step_gated
+    continues from."""
     B, Hq, N, d = q.shape
     if tuple(gate.shape) != tuple(q.shape):
         raise ValueError("gate must have the shape of q")
@@ -292,7 +298,9 @@ def prefill_gated(q, k, v, gate, Wf, W, C, m, T_max, out=None, sel_idx=None, wor
                                      _ptr(v, torch.bfloat16, "v"), _ptr(gate, torch.bfloat16, "gate"),
                                      _ptr(Wf, torch.float32, "Wf"), W, C, m, T_max, _ptr(out, torch.bfloat16, "out"),
                                      _ptr(sel_idx, torch.int32, "sel_idx") if sel_idx.numel() else None,
-                                     ws_ptr, ws_bytes, _stream(stream)), "still_prefill_gated")
+                                     ws_ptr, ws_bytes,
+                                     ct.byref(export_state.c_struct()) if export_state is not None else None,
+                                     _stream(stream)), "still_prefill_gated")
     return out, sel_idx
 
 
@@ -379,6 +387,23 @@ def decode_step(state: DecodeState, q_t, k_t, v_t, Wf, W, C, m, T_max, out_t=Non
                                    _ptr(k_t, torch.bfloat16, "k_t"), _ptr(v_t, torch.bfloat16, "v_t"),
                                    _ptr(Wf, torch.float32, "Wf"), W, C, m, T_max,
                                    _ptr(out_t, torch.bfloat16, "out_t"), _stream(stream)), "still_decode_step")
+    return out_t
+
+
+def decode_step_gated(state: DecodeState, q_t, k_t, v_t, gate_t, Wf, W, C, m, T_max, out_t=None, stream=None):
+    """One token per sequence of the gated layer: gate_t [B,Hq,d] bf16 holds this
+    step's gate pre-activations (see still_decode_step_gated)."""
+    B, Hq, d = q_t.shape
+    if tuple(gate_t.shape) != tuple(q_t.shape):
+        raise ValueError("gate_t must have the shape of q_t")
+    sh = Shape(B, Hq, k_t.shape[1], 0, d, Wf.shape[1])
+    if out_t is None:
+        out_t = torch.empty_like(q_t)
+    _check(lib().still_decode_step_gated(ct.byref(sh), ct.byref(state.c_struct()), _ptr(q_t, torch.bfloat16, "q_t"),
+                                         _ptr(k_t, torch.bfloat16, "k_t"), _ptr(v_t, torch.bfloat16, "v_t"),
+                                         _ptr(gate_t, torch.bfloat16, "gate_t"), _ptr(Wf, torch.float32, "Wf"),
+                                         W, C, m, T_max, _ptr(out_t, torch.bfloat16, "out_t"), _stream(stream)),
+           "still_decode_step_gated")
     return out_t
 
 

@@ -71,6 +71,8 @@ def test_workspace_size_and_argument_errors(lib):
     assert lib.still_prefill(ct.byref(sh0), p, p, p, p, 64, 256, 288, 64, p, None, p, 100, None, None) == 6  # small ws
     st = DecodeStateC()
     assert lib.still_decode_step(ct.byref(sh), ct.byref(st), p, p, p, p, 64, 256, 288, 64, p, None) == 1
+    assert lib.still_decode_step_gated(ct.byref(sh), ct.byref(st), p, p, p, None, p, 64, 256, 288, 64, p,
+                                       None) == 1                    # no gate
     assert lib.still_score(ct.byref(sh), p, p, 0, p, None) == 1
     # routing metrics: unknown metric, missing inputs, windowed metric without a window
     assert lib.still_score_metric(ct.byref(sh), p, p, 64, 256, 288, 64, 6, 0, p, None) == 1

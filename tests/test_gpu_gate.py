@@ -95,3 +95,48 @@ def test_open_gate_equals_the_ungated_layer(still):
     assert torch.equal(sg, s_)
     yg64, y64 = to_f64(yg), to_f64(y)
     assert np.abs(yg64 - y64).max() <= 2 ** -7 * np.abs(y64).max()
+
+
+@pytest.mark.parametrize("w", [Workload("gdec_w_lt_c", 1, 8, 2, 64, 150, 16, 32, 16 + 4 * 6, 6, 64),
+                               Workload("gdec_w_eq_c", 2, 4, 1, 128, 140, 32, 32, 32 + 3 * 5, 5, 128)],
+                         ids=lambda w: w.name)
+def test_gated_prefill_then_gated_decode_steps(still, w):
+    # the gated layer's state is the ungated one's: a gated prefill of N0 tokens, exported,
+    # continued by gated decode steps, equals the oracle's gated layer over all N tokens
+    N0 = 96
+    q, k, v, Wf = inputs.make_inputs(w, seed=5)
+    a = inputs.make_gate(w, seed=5)
+    qd, kd, vd, ad, Wd = (t.to(DEV) for t in (q, k, v, a, Wf))
+    st = still.DecodeState(w.B, w.Hkv, w.d, w.df, w.C, w.m, device=DEV)
+    y0, _ = still.prefill_gated(qd[:, :, :N0].contiguous(), kd[:, :, :N0].contiguous(), vd[:, :, :N0].contiguous(),
+                                ad[:, :, :N0].contiguous(), Wd, w.W, w.C, w.m, w.T_max, export_state=st)
+    ys = []
+    for t in range(N0, w.N):
+        ys.append(still.decode_step_gated(st, qd[:, :, t].contiguous(), kd[:, :, t].contiguous(),
+                                          vd[:, :, t].contiguous(), ad[:, :, t].contiguous(), Wd, w.W, w.C, w.m,
+                                          w.T_max))
+    torch.cuda.synchronize()
+    assert st.read_status() == 0
+    y = torch.cat([y0, torch.stack(ys, dim=2)], dim=2)
+    y_ref, _, _ = ref.prefill(*(to_f64(t) for t in (q, k, v, Wf)), w.W, w.C, w.m, w.T_max, gate=to_f64(a))
+    err = np.abs(to_f64(y) - y_ref).max()
+    record_parity(f"gated prefill {N0} + {w.N - N0} gated decode steps {w.name}",
+                  max_err_rel=float(err / np.abs(y_ref).max()))
+    assert err <= OUT_TOL * np.abs(y_ref).max()
+
+
+def test_open_gate_decode_equals_ungated_decode(still):
+    w = Workload("gdec_open", 1, 4, 2, 64, 120, 16, 32, 16 + 4 * 4, 4, 64)
+    q, k, v, Wf = (t.to(DEV) for t in inputs.make_inputs(w, seed=6))
+    sa = still.DecodeState(w.B, w.Hkv, w.d, w.df, w.C, w.m, device=DEV)
+    sb = still.DecodeState(w.B, w.Hkv, w.d, w.df, w.C, w.m, device=DEV)
+    still.prefill(q[:, :, :80].contiguous(), k[:, :, :80].contiguous(), v[:, :, :80].contiguous(), Wf,
+                  w.W, w.C, w.m, w.T_max, export_state=sa)
+    still.prefill(q[:, :, :80].contiguous(), k[:, :, :80].contiguous(), v[:, :, :80].contiguous(), Wf,
+                  w.W, w.C, w.m, w.T_max, export_state=sb)
+    open_gate = torch.full((w.B, w.Hq, w.d), 40.0, dtype=torch.bfloat16, device=DEV)
+    for t in range(80, w.N):
+        qt, kt, vt = (x[:, :, t].contiguous() for x in (q, k, v))
+        ya = still.decode_step(sa, qt, kt, vt, Wf, w.W, w.C, w.m, w.T_max)
+        yb = still.decode_step_gated(sb, qt, kt, vt, open_gate, Wf, w.W, w.C, w.m, w.T_max)
+        assert torch.equal(ya, yb), t
