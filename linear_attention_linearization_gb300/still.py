@@ -416,3 +416,32 @@ def timing_read():
     buf = (KernelTime * 64)()
     n = lib().still_timing_read(buf, 64)
     return {buf[i].name.decode(): (buf[i].launches, buf[i].ms) for i in range(min(n, 64))}
+
+
+class HybridAttention(torch.autograd.Function):
+    """The layer as a differentiable PyTorch op: forward = still_prefill, backward =
+    still_backward with the forward's selection held fixed (the selection is a
+    discrete choice and carries no gradient).  Inputs: q [B,Hq,N,d], k, v
+    [B,Hkv,N,d] bf16, Wf [d,d_f] fp32; returns (y bf16, sel_idx int32).
+    Gradients come back in the inputs' dtypes (bf16 for q, k, v; fp32 for Wf)."""
+
+    @staticmethod
+    def forward(ctx, q, k, v, Wf, W, C, m, T_max):
+        y, sel = prefill(q, k, v, Wf, W, C, m, T_max)
+        ctx.save_for_backward(q, k, v, Wf, sel)
+        ctx.routing = (W, C, m, T_max)
+        ctx.mark_non_differentiable(sel)
+        return y, sel
+
+    @staticmethod
+    def backward(ctx, dy, _dsel):
+        q, k, v, Wf, sel = ctx.saved_tensors
+        W, C, m, T_max = ctx.routing
+        dq, dk, dv, dWf = backward(q, k, v, Wf, W, C, m, T_max, sel, dy.to(torch.bfloat16).contiguous())
+        return dq.to(q.dtype), dk.to(k.dtype), dv.to(v.dtype), dWf, None, None, None, None
+
+
+def hybrid_attention(q, k, v, Wf, W, C, m, T_max):
+    """y of the layer with autograd support (see HybridAttention)."""
+    y, _ = HybridAttention.apply(q, k, v, Wf, W, C, m, T_max)
+    return y

@@ -203,3 +203,21 @@ def test_backward_ignores_selection_entries_out_of_range(still):
     assert torch.equal(ga[0], gb[0])
     for x, y in zip(ga[1:], gb[1:]):
         assert (x - y).abs().max().item() <= 1e-5 * x.abs().max().item()
+
+
+def test_autograd_op_matches_the_gradient_oracle(still):
+    # still.hybrid_attention inside a torch autograd graph: the loss sum(y * dy) gives the
+    # oracle's gradients (bf16 for q, k, v as the inputs, fp32 for Wf)
+    w = Workload("ag", 1, 4, 2, 64, 200, 32, 32, 32 + 8 * 4, 8, 64)
+    q, k, v, Wf = inputs.make_inputs(w, seed=12)
+    dy = inputs.make_dout(w, seed=12)
+    qd, kd, vd, Wd = (t.to(DEV).requires_grad_(True) for t in (q, k, v, Wf))
+    y = still.hybrid_attention(qd, kd, vd, Wd, w.W, w.C, w.m, w.T_max)
+    (y.float() * dy.to(DEV).float()).sum().backward()
+    _, sel = still.prefill(qd.detach(), kd.detach(), vd.detach(), Wd.detach(), w.W, w.C, w.m, w.T_max)
+    _, dq_r, dk_r, dv_r, dW_r, _ = grad.layer_grad(*(to_f64(t) for t in (q, k, v, Wf)), w.W, w.C,
+                                                   sel.cpu().numpy(), to_f64(dy))
+    assert qd.grad.dtype == torch.bfloat16 and Wd.grad.dtype == torch.float32
+    for g_gpu, g_ref in ((qd.grad, dq_r), (kd.grad, dk_r), (vd.grad, dv_r), (Wd.grad, dW_r)):
+        err = np.abs(g_gpu.detach().cpu().double().numpy() - g_ref).max()
+        assert err <= GRAD_TOL * np.abs(g_ref).max()
