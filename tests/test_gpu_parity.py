@@ -336,8 +336,11 @@ def test_decode_from_empty_state_equals_prefill(w):
     compare_state(st, st_ref, w, ka, va, Wa)
 
 
-@pytest.mark.parametrize("w", DEC[:3] + [custom(1, 4, 2, 64, 301, 16, 32, 16 + 3 * 8, 8)],
-                         ids=lambda w: f"N{w.N}_W{w.W}_C{w.C}")
+# the last case: 48 sequences x 8 kv heads = 384 units of the decode kernel,
+# more than one wave of its CTAs, at the 16K layer's head shape
+@pytest.mark.parametrize("w", DEC[:3] + [custom(1, 4, 2, 64, 301, 16, 32, 16 + 3 * 8, 8),
+                                         custom(48, 32, 8, 128, 300, 16, 32, 16 + 3 * 10, 10)],
+                         ids=lambda w: f"B{w.B}_N{w.N}_W{w.W}_C{w.C}")
 def test_prefill_export_then_decode(w):
     r = run_prefill_case(w, seed=4, state=True)
     _, k, v, Wf = r["inputs"]
