@@ -14,7 +14,8 @@ Feature Map"),
     s_tj = q_t.k_j / sqrt(d),  c_t = max_{j in SA(t)} s_tj,
     phi(x) = ||x|| u / ||u||,  u = softmax(x Wf),
 
-with respect to q, k, v and Wf, for an upstream gradient dy, with the kept
+with respect to q, k, v and Wf (and, for the gated layer, the gate's
+pre-activations), for an upstream gradient dy, with the kept
 set (the selection) held fixed: the selection is a discrete choice made from
 the scores, and the training path of the pages' "Experiments" section trains
 through the layer with the routing given.  The stabiliser c_t is part of the
@@ -24,6 +25,15 @@ several logits attain it the lowest key position takes it (the one the row
 keeps after a first-maximum scan), or the position a caller passes in
 ``cidx`` -- the GPU reports its own choice, and near-equal maxima are
 compared with that choice.
+
+The gated layer (section "NP-Map: Norm-Preserving Feature Map": a gate raises
+the linear branch's rank; its equation is lost, and the reading taken is a
+per-channel sigmoid gate on the linear numerator) is
+
+    y_t = (sum_SA e^{s_tj - c_t} v_j + sigmoid(a_t) * sum_LA (phi(q_t).phi(k_j)) v_j)
+          / (sum_SA e^{s_tj - c_t} + sum_LA phi(q_t).phi(k_j)),
+
+a_t of the layout of q_t, the denominator ungated.
 
 The derivative is taken by reverse-mode automatic differentiation of the
 forward written out below (a library primitive); the tests pin it against
@@ -45,9 +55,10 @@ def _npmap_t(x: torch.Tensor, Wf: torch.Tensor) -> torch.Tensor:
     return torch.linalg.vector_norm(x, dim=-1, keepdim=True) * u / torch.linalg.vector_norm(u, dim=-1, keepdim=True)
 
 
-def _group_forward(qg, kg, vg, Wf, sa, la, cidx_g):
+def _group_forward(qg, kg, vg, Wf, sa, la, cidx_g, gate_g=None):
     """Outputs [G, N, d] of the G query heads of one kv head, and the row-max
-    positions used for c ([G, N], -1 where SA(t) is empty)."""
+    positions used for c ([G, N], -1 where SA(t) is empty).  gate_g: the
+    gate's pre-activations [G, N, d] of the gated layer, or None."""
     G, N, d = qg.shape
     s = qg @ kg.T / np.sqrt(d)                                     # [G, N, N]
     sa_t = torch.as_tensor(sa)[None].expand(G, N, N)
@@ -66,20 +77,25 @@ def _group_forward(qg, kg, vg, Wf, sa, la, cidx_g):
     phq = _npmap_t(qg, Wf)                                          # [G, N, df]
     phk = _npmap_t(kg, Wf)                                          # [N, df]
     a = torch.where(la_t, phq @ phk.T, torch.zeros_like(s))
-    num = (e + a) @ vg
+    if gate_g is None:
+        num = (e + a) @ vg
+    else:
+        num = e @ vg + torch.sigmoid(gate_g) * (a @ vg)
     den = (e + a).sum(dim=-1, keepdim=True)
     nz = den != 0
     y = torch.where(nz, num / torch.where(nz, den, torch.ones_like(den)), torch.zeros_like(num))
     return y, idx
 
 
-def layer_grad(q, k, v, Wf, W, C, sel, dy, cidx=None):
+def layer_grad(q, k, v, Wf, W, C, sel, dy, cidx=None, gate=None):
     """Gradients of sum(dy * y) for one layer call.
 
     q [B, Hq, N, d], k, v [B, Hkv, N, d], Wf [d, df], sel [B, Hkv, T_max, lam]
     (the kept positions, -1 padded), dy [B, Hq, N, d]; cidx (optional)
-    [B, Hq, N] row-max positions to use for c.
-    Returns (y, dq, dk, dv, dWf, cidx) as float64 / int64 numpy arrays."""
+    [B, Hq, N] row-max positions to use for c; gate (optional) [B, Hq, N, d]
+    the pre-activations of the gated layer.
+    Returns (y, dq, dk, dv, dWf, cidx) as float64 / int64 numpy arrays, and
+    dgate [B, Hq, N, d] after them when gate is given."""
     q, k, v, Wf, dy = (np.asarray(a, dtype=np.float64) for a in (q, k, v, Wf, dy))
     B, Hq, N, d = q.shape
     Hkv = k.shape[1]
@@ -90,6 +106,10 @@ def layer_grad(q, k, v, Wf, W, C, sel, dy, cidx=None):
     dv = np.zeros_like(v)
     dWf = np.zeros_like(Wf)
     cid = np.full((B, Hq, N), -1, dtype=np.int64)
+    gated = gate is not None
+    if gated:
+        gate = np.asarray(gate, dtype=np.float64)
+        dgate = np.zeros_like(gate)
     Wf_t = torch.tensor(Wf, requires_grad=True)
     for b in range(B):
         kept = brute.kept_mask(np.asarray(sel[b]), N)
@@ -99,7 +119,8 @@ def layer_grad(q, k, v, Wf, W, C, sel, dy, cidx=None):
             qg = torch.tensor(q[b, hs], requires_grad=True)
             kg = torch.tensor(k[b, g], requires_grad=True)
             vg = torch.tensor(v[b, g], requires_grad=True)
-            yg, idx = _group_forward(qg, kg, vg, Wf_t, sa, la, None if cidx is None else cidx[b, hs])
+            ag = torch.tensor(gate[b, hs], requires_grad=True) if gated else None
+            yg, idx = _group_forward(qg, kg, vg, Wf_t, sa, la, None if cidx is None else cidx[b, hs], ag)
             loss = (yg * torch.tensor(dy[b, hs])).sum()
             loss.backward()
             y[b, hs] = yg.detach().numpy()
@@ -107,7 +128,11 @@ def layer_grad(q, k, v, Wf, W, C, sel, dy, cidx=None):
             dk[b, g] = kg.grad.numpy()
             dv[b, g] = vg.grad.numpy()
             cid[b, hs] = idx.numpy()
+            if gated:
+                dgate[b, hs] = ag.grad.numpy()
     dWf[...] = Wf_t.grad.numpy() if Wf_t.grad is not None else 0.0
+    if gated:
+        return y, dq, dk, dv, dWf, cid, dgate
     return y, dq, dk, dv, dWf, cid
 
 

@@ -10,7 +10,10 @@
   torch's scaled_dot_product_attention, a library routine, and no gradient
   for Wf;
 * the linear-attention reduction (W = 0, lambda = 0) against central
-  differences, where only the NP-Map carries the gradient to q, k and Wf.
+  differences, where only the NP-Map carries the gradient to q, k and Wf;
+* for the gated layer: a hand-derived gated example, central differences of
+  the C oracle's gated recurrence (including the gate's pre-activations), and
+  the open-gate limit, which is the ungated gradient.
 """
 import math
 import os
@@ -35,9 +38,9 @@ def _cases():
             name, *nums = rest[0].split()
             cur = dict(name=name, dims=[int(x) for x in nums], vals={}, expect=[])
             cases.append(cur)
-        elif tag in ("q", "k", "v"):
+        elif tag in ("q", "k", "v", "gate"):
             cur["vals"][tag] = [float(x) for x in rest[0].split()]
-        elif tag in ("dq", "dk", "dv"):
+        elif tag in ("dq", "dk", "dv", "dgate"):
             t, expr = rest[0].split(None, 1)
             cur["expect"].append((tag, int(t), eval(expr, {"math": math})))
         elif tag == "dWf":
@@ -52,8 +55,15 @@ def test_hand_derived_gradients(case):
     Wf = np.zeros((d, 1))
     lam = brute.lam_of(m, W, T_max)
     sel = np.full((1, 1, T_max, lam), -1)
-    _, dq, dk, dv, dWf, _ = grad.layer_grad(q, k, v, Wf, W, C, sel, np.ones_like(q))
+    if "gate" in case["vals"]:
+        gate = np.array(case["vals"]["gate"]).reshape(1, 1, N, d)
+        _, dq, dk, dv, dWf, _, dgate = grad.layer_grad(q, k, v, Wf, W, C, sel, np.ones_like(q), gate=gate)
+    else:
+        _, dq, dk, dv, dWf, _ = grad.layer_grad(q, k, v, Wf, W, C, sel, np.ones_like(q))
+        dgate = None
     got = {"dq": dq[0, 0, :, 0], "dk": dk[0, 0, :, 0], "dv": dv[0, 0, :, 0]}
+    if dgate is not None:
+        got["dgate"] = dgate[0, 0, :, 0]
     for tag, t, want in case["expect"]:
         val = dWf[0, 0] if tag == "dWf" else got[tag][t]
         assert val == pytest.approx(want, rel=1e-12, abs=1e-12), (tag, t)
@@ -108,6 +118,54 @@ def test_gradient_matches_central_differences_of_the_streaming_oracle(cfg):
                   - _loss_c(minus["q"], minus["k"], minus["v"], minus["Wf"], dy, W, C, m, T_max, sel, lam)) / (2 * h)
             an = float((grads[name] * dirn).sum())
             assert an == pytest.approx(fd, rel=1e-6, abs=1e-7), name
+
+
+def _loss_c_gated(q, k, v, Wf, gate, dy, W, C, m, T_max, sel, lam):
+    y, _, _ = ref.prefill(q, k, v, Wf, W, C, m, T_max, sel_override=sel.astype(np.int32) if lam > 0 else None,
+                          gate=gate)
+    return float((y * dy).sum())
+
+
+@pytest.mark.parametrize("cfg", FD_CASES[:3], ids=[f"gated_fd{i}" for i in range(3)])
+def test_gated_gradient_matches_central_differences_of_the_streaming_oracle(cfg):
+    # the gated layer: the C oracle's own gated recurrence, differenced along
+    # random directions of q, k, v, Wf and the gate's pre-activations
+    B, Hq, Hkv, N, d, df, W, C, m, T_max = cfg
+    q, k, v, Wf, dy, sel, lam = _random_case(29 + N, *cfg)
+    gate = np.random.default_rng(7).normal(0.0, 2.0, q.shape)
+    y, dq, dk, dv, dWf, _, dgate = grad.layer_grad(q, k, v, Wf, W, C, sel, dy, gate=gate)
+    y_c, _, _ = ref.prefill(q, k, v, Wf, W, C, m, T_max, sel_override=sel.astype(np.int32) if lam > 0 else None,
+                            gate=gate)
+    assert np.abs(y - y_c).max() <= 1e-12 * max(1.0, np.abs(y_c).max())
+    rng = np.random.default_rng(6)
+    h = 1e-5
+    args = {"q": q, "k": k, "v": v, "Wf": Wf, "gate": gate}
+    grads = {"q": dq, "k": dk, "v": dv, "Wf": dWf, "gate": dgate}
+    for name in args:
+        for _ in range(2):
+            dirn = rng.standard_normal(args[name].shape)
+            plus = dict(args)
+            minus = dict(args)
+            plus[name] = args[name] + h * dirn
+            minus[name] = args[name] - h * dirn
+            fd = (_loss_c_gated(plus["q"], plus["k"], plus["v"], plus["Wf"], plus["gate"], dy, W, C, m, T_max, sel, lam)
+                  - _loss_c_gated(minus["q"], minus["k"], minus["v"], minus["Wf"], minus["gate"], dy, W, C, m, T_max,
+                                  sel, lam)) / (2 * h)
+            an = float((grads[name] * dirn).sum())
+            assert an == pytest.approx(fd, rel=1e-6, abs=1e-7), name
+
+
+def test_open_gate_gradient_is_the_ungated_gradient():
+    # sigmoid(60) rounds to 1 in fp64: the gated layer is the ungated one, and the
+    # gate's own gradient (sigmoid' ~ e^-60) vanishes
+    cfg = FD_CASES[1]
+    q, k, v, Wf, dy, sel, lam = _random_case(41, *cfg)
+    W, C = cfg[6], cfg[7]
+    ref_g = grad.layer_grad(q, k, v, Wf, W, C, sel, dy)
+    got = grad.layer_grad(q, k, v, Wf, W, C, sel, dy, gate=np.full(q.shape, 60.0))
+    for a, b in zip(ref_g[:5], got[:5]):
+        assert np.abs(a - b).max() <= 1e-12 * max(1.0, np.abs(a).max())
+    assert np.abs(got[6]).max() <= 1e-20 * np.abs(got[1]).max()
 
 
 def test_softmax_reduction_matches_scaled_dot_product_attention():
